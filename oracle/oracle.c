@@ -1,0 +1,378 @@
+/*
+ * Reference oracle for paged GQA attention — TEST INFRASTRUCTURE ONLY.
+ *
+ * This file is the plain, slow, obviously correct CPU statement of what the
+ * attention hot path computes.  Only the test suite, the smoke check and the
+ * CPU-baseline leg of the benchmark may load it.  It shares no code, header,
+ * table or helper with the CUDA library, and the CUDA library never calls it.
+ *
+ * Precision: every bf16 input is widened exactly to double, and everything
+ * after that (scores, softmax, weighted sum) is double with no intermediate
+ * rounding.  Outputs are double.
+ *
+ * What is computed (the definition, not a fast algorithm):
+ *
+ *   attention of one query row q over keys K[0..n) and values V[0..n):
+ *       s_j = scale * sum_d q[d] * K[j][d]
+ *       p_j = exp(s_j - max_i s_i) / sum_i exp(s_i - max_i s_i)
+ *       out = sum_j p_j * V[j]
+ *   (qwenasr.cpp ARCHITECTURE.md, "Attention and RoPE" and "Qwen3 Thinker
+ *   decoder": the manual F32 chain mul_mat -> soft_max_ext -> mul_mat; the
+ *   OneSpeech Qwen3 page, "Front end and graph numerics": score and softmax
+ *   intermediates stay in higher precision than the attended output.)
+ *   A row with no visible key (n == 0) returns zeros.
+ *
+ *   GQA head mapping: query head h reads KV head h / (Hq / Hkv), contiguous
+ *   grouping (qwenasr.cpp ARCHITECTURE.md, "GGUF layout": head_count 16,
+ *   head_count_kv 8, GQA 2:1; Glossary "GQA").
+ *
+ *   Decode: request b attends over positions [0, seq_lens[b]); position j
+ *   lives in physical page page_table[b][j / page_size], slot j % page_size
+ *   (qwenasr.cpp ARCHITECTURE.md, "Qwen3 Thinker decoder": decode attends
+ *   over [0, cur_len + 1); M* "Speech recognition: Whisper and Qwen3-ASR",
+ *   "Graph" and "Serving notes": decode runs on paged KV, requests hold pages).
+ *   Pool layout [num_pages][page_size][Hkv][D].
+ *
+ *   Prefill: packed requests, request r owns rows [cu[r], cu[r+1]); row i of
+ *   a request attends over rows j <= i of the same request, using K/V from
+ *   the packed input (qwenasr.cpp ARCHITECTURE.md, "Qwen3 Thinker decoder":
+ *   prefill rewinds the cache, writes the prompt span and attends over
+ *   [0, n_past + T) with n_past = 0; causal).
+ *
+ *   Page write: row i of request r is copied bit for bit to page
+ *   page_table[r][i / page_size], slot i % page_size ("write fresh K/V into
+ *   the cache at [n_past, n_past + T)", same section).
+ *
+ *   Window: packed windows, window w owns rows [cu_w[w], cu_w[w+1]); every
+ *   row attends over every row of its own window, no mask inside, no GQA
+ *   (qwenasr.cpp ARCHITECTURE.md, "Windowed audio tower": block-diagonal
+ *   mask over windows, plain bidirectional MHA scaled by 1/sqrt(head_dim);
+ *   M* page, "Qwen3-ASR / Graph": one packed forward, one segment per window).
+ *
+ * Threads: rows are independent; n_threads worker threads take contiguous
+ * slices of the row list.  This is the only concession to speed.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORACLE_EXPORT __attribute__((visibility("default")))
+
+/* bf16 is the upper half of an IEEE binary32: widening is exact. */
+static double bf16_to_double(uint16_t h)
+{
+    uint32_t u = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* The definition of attention for one query row (see the file header).
+ * p_out, when not NULL, receives the n softmax probabilities. */
+ORACLE_EXPORT void oracle_attend_row(const double *q, const double *K, const double *V,
+                                     int n, int D, double scale, double *out, double *p_out)
+{
+    for (int d = 0; d < D; ++d)
+        out[d] = 0.0;
+    if (n <= 0)
+        return;
+
+    double *s = (double *)malloc(sizeof(double) * (size_t)n);
+    double m = -INFINITY;
+    for (int j = 0; j < n; ++j) {
+        double acc = 0.0;
+        for (int d = 0; d < D; ++d)
+            acc += q[d] * K[(size_t)j * D + d];
+        s[j] = scale * acc;
+        if (s[j] > m)
+            m = s[j];
+    }
+    double z = 0.0;
+    for (int j = 0; j < n; ++j) {
+        s[j] = exp(s[j] - m);
+        z += s[j];
+    }
+    for (int j = 0; j < n; ++j) {
+        double p = s[j] / z;
+        if (p_out)
+            p_out[j] = p;
+        for (int d = 0; d < D; ++d)
+            out[d] += p * V[(size_t)j * D + d];
+    }
+    free(s);
+}
+
+/* ------------------------------------------------------------------------- */
+/* Row-parallel driver.                                                       */
+
+typedef void (*row_fn)(const void *ctx, int row, double *out);
+
+typedef struct {
+    const void *ctx;
+    row_fn fn;
+    const int32_t *rows; /* NULL: row i is i */
+    int first, last;     /* slice of the row list */
+    int D;
+    double *out;
+} slice_t;
+
+static void *run_slice(void *arg)
+{
+    slice_t *sl = (slice_t *)arg;
+    for (int i = sl->first; i < sl->last; ++i) {
+        int row = sl->rows ? sl->rows[i] : i;
+        sl->fn(sl->ctx, row, sl->out + (size_t)i * sl->D);
+    }
+    return NULL;
+}
+
+static void run_rows(const void *ctx, row_fn fn, const int32_t *rows, int n_rows, int D,
+                     double *out, int n_threads)
+{
+    if (n_threads < 1)
+        n_threads = 1;
+    if (n_threads > n_rows)
+        n_threads = n_rows > 0 ? n_rows : 1;
+    pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)n_threads);
+    slice_t *sl = (slice_t *)malloc(sizeof(slice_t) * (size_t)n_threads);
+    for (int t = 0; t < n_threads; ++t) {
+        sl[t].ctx = ctx;
+        sl[t].fn = fn;
+        sl[t].rows = rows;
+        sl[t].first = (int)((long long)n_rows * t / n_threads);
+        sl[t].last = (int)((long long)n_rows * (t + 1) / n_threads);
+        sl[t].D = D;
+        sl[t].out = out;
+    }
+    for (int t = 1; t < n_threads; ++t)
+        pthread_create(&th[t], NULL, run_slice, &sl[t]);
+    run_slice(&sl[0]);
+    for (int t = 1; t < n_threads; ++t)
+        pthread_join(th[t], NULL);
+    free(sl);
+    free(th);
+}
+
+/* ------------------------------------------------------------------------- */
+/* Decode over a paged pool.                                                  */
+
+typedef struct {
+    const uint16_t *q, *k_pages, *v_pages;
+    const int32_t *page_table, *seq_lens;
+    int batch, Hq, Hkv, D, page_size, max_pages, num_pages;
+    double scale;
+} decode_ctx;
+
+static void decode_row(const void *vctx, int row, double *out)
+{
+    const decode_ctx *c = (const decode_ctx *)vctx;
+    int b = row / c->Hq, h = row % c->Hq;
+    int g = h / (c->Hq / c->Hkv);
+    int n = c->seq_lens[b];
+    double *q = (double *)malloc(sizeof(double) * (size_t)c->D);
+    double *K = (double *)malloc(sizeof(double) * (size_t)c->D * (size_t)(n > 0 ? n : 1));
+    double *V = (double *)malloc(sizeof(double) * (size_t)c->D * (size_t)(n > 0 ? n : 1));
+    for (int d = 0; d < c->D; ++d)
+        q[d] = bf16_to_double(c->q[((size_t)b * c->Hq + h) * c->D + d]);
+    for (int j = 0; j < n; ++j) {
+        int page = c->page_table[(size_t)b * c->max_pages + j / c->page_size];
+        int slot = j % c->page_size;
+        size_t base = (((size_t)page * c->page_size + slot) * c->Hkv + g) * c->D;
+        for (int d = 0; d < c->D; ++d) {
+            K[(size_t)j * c->D + d] = bf16_to_double(c->k_pages[base + d]);
+            V[(size_t)j * c->D + d] = bf16_to_double(c->v_pages[base + d]);
+        }
+    }
+    oracle_attend_row(q, K, V, n, c->D, c->scale, out, NULL);
+    free(V);
+    free(K);
+    free(q);
+}
+
+/* out[i] = attention of row rows[i] = b * Hq + h (all B*Hq rows when rows is
+ * NULL).  Returns 0, or -1 on inconsistent arguments (nothing computed). */
+ORACLE_EXPORT int oracle_decode(const uint16_t *q, const uint16_t *k_pages, const uint16_t *v_pages,
+                                const int32_t *page_table, const int32_t *seq_lens, int batch,
+                                int Hq, int Hkv, int D, int page_size, int max_pages, int num_pages,
+                                double scale, const int32_t *rows, int n_rows, double *out,
+                                int n_threads)
+{
+    if (batch < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || D <= 0 || page_size <= 0)
+        return -1;
+    for (int b = 0; b < batch; ++b) {
+        int n = seq_lens[b];
+        if (n < 0 || n > max_pages * page_size)
+            return -1;
+        for (int p = 0; p < (n + page_size - 1) / page_size; ++p) {
+            int page = page_table[(size_t)b * max_pages + p];
+            if (page < 0 || page >= num_pages)
+                return -1;
+        }
+    }
+    if (!rows)
+        n_rows = batch * Hq;
+    for (int i = 0; rows && i < n_rows; ++i)
+        if (rows[i] < 0 || rows[i] >= batch * Hq)
+            return -1;
+    decode_ctx c = {q, k_pages, v_pages, page_table, seq_lens, batch, Hq, Hkv, D,
+                    page_size, max_pages, num_pages, scale};
+    run_rows(&c, decode_row, rows, n_rows, D, out, n_threads);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Causal prefill over packed requests.                                       */
+
+typedef struct {
+    const uint16_t *q, *k, *v;
+    const int32_t *cu;
+    int batch, Hq, Hkv, D;
+    double scale;
+} prefill_ctx;
+
+static void prefill_row(const void *vctx, int row, double *out)
+{
+    const prefill_ctx *c = (const prefill_ctx *)vctx;
+    int t = row / c->Hq, h = row % c->Hq;
+    int g = h / (c->Hq / c->Hkv);
+    int r = 0;
+    while (!(c->cu[r] <= t && t < c->cu[r + 1]))
+        ++r;
+    int first = c->cu[r];
+    int n = t - first + 1; /* keys j <= i within the request */
+    double *q = (double *)malloc(sizeof(double) * (size_t)c->D);
+    double *K = (double *)malloc(sizeof(double) * (size_t)c->D * (size_t)n);
+    double *V = (double *)malloc(sizeof(double) * (size_t)c->D * (size_t)n);
+    for (int d = 0; d < c->D; ++d)
+        q[d] = bf16_to_double(c->q[((size_t)t * c->Hq + h) * c->D + d]);
+    for (int j = 0; j < n; ++j) {
+        size_t base = ((size_t)(first + j) * c->Hkv + g) * c->D;
+        for (int d = 0; d < c->D; ++d) {
+            K[(size_t)j * c->D + d] = bf16_to_double(c->k[base + d]);
+            V[(size_t)j * c->D + d] = bf16_to_double(c->v[base + d]);
+        }
+    }
+    oracle_attend_row(q, K, V, n, c->D, c->scale, out, NULL);
+    free(V);
+    free(K);
+    free(q);
+}
+
+/* out[i] = attention of row rows[i] = t * Hq + h over its request's keys
+ * j <= t (all total_tokens*Hq rows when rows is NULL). */
+ORACLE_EXPORT int oracle_prefill(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                                 const int32_t *cu_seqlens, int batch, int total_tokens,
+                                 int Hq, int Hkv, int D, double scale, const int32_t *rows,
+                                 int n_rows, double *out, int n_threads)
+{
+    if (batch <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || D <= 0)
+        return -1;
+    if (cu_seqlens[0] != 0 || cu_seqlens[batch] != total_tokens)
+        return -1;
+    for (int r = 0; r < batch; ++r)
+        if (cu_seqlens[r + 1] < cu_seqlens[r])
+            return -1;
+    if (!rows)
+        n_rows = total_tokens * Hq;
+    for (int i = 0; rows && i < n_rows; ++i)
+        if (rows[i] < 0 || rows[i] >= total_tokens * Hq)
+            return -1;
+    prefill_ctx c = {q, k, v, cu_seqlens, batch, Hq, Hkv, D, scale};
+    run_rows(&c, prefill_row, rows, n_rows, D, out, n_threads);
+    return 0;
+}
+
+/* Bit copy of the packed K/V rows of every request into its pages.  Slots
+ * that no row maps to are left as they were.  Returns -1 (and writes
+ * nothing) if a needed page id is outside [0, num_pages). */
+ORACLE_EXPORT int oracle_page_write(const uint16_t *k, const uint16_t *v, const int32_t *cu_seqlens,
+                                    int batch, const int32_t *page_table, int max_pages,
+                                    int page_size, int num_pages, int Hkv, int D,
+                                    uint16_t *k_pages, uint16_t *v_pages)
+{
+    for (int r = 0; r < batch; ++r) {
+        int n = cu_seqlens[r + 1] - cu_seqlens[r];
+        if (n < 0 || n > max_pages * page_size)
+            return -1;
+        for (int i = 0; i < n; ++i) {
+            int page = page_table[(size_t)r * max_pages + i / page_size];
+            if (page < 0 || page >= num_pages)
+                return -1;
+        }
+    }
+    size_t row_elems = (size_t)Hkv * D;
+    for (int r = 0; r < batch; ++r) {
+        int n = cu_seqlens[r + 1] - cu_seqlens[r];
+        for (int i = 0; i < n; ++i) {
+            int page = page_table[(size_t)r * max_pages + i / page_size];
+            size_t dst = ((size_t)page * page_size + i % page_size) * row_elems;
+            size_t src = (size_t)(cu_seqlens[r] + i) * row_elems;
+            memcpy(k_pages + dst, k + src, row_elems * sizeof(uint16_t));
+            memcpy(v_pages + dst, v + src, row_elems * sizeof(uint16_t));
+        }
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Windowed bidirectional attention over packed windows.                      */
+
+typedef struct {
+    const uint16_t *q, *k, *v;
+    const int32_t *cu;
+    int n_windows, H, D;
+    double scale;
+} window_ctx;
+
+static void window_row(const void *vctx, int row, double *out)
+{
+    const window_ctx *c = (const window_ctx *)vctx;
+    int t = row / c->H, h = row % c->H;
+    int w = 0;
+    while (!(c->cu[w] <= t && t < c->cu[w + 1]))
+        ++w;
+    int first = c->cu[w];
+    int n = c->cu[w + 1] - first; /* every row of the window */
+    double *q = (double *)malloc(sizeof(double) * (size_t)c->D);
+    double *K = (double *)malloc(sizeof(double) * (size_t)c->D * (size_t)n);
+    double *V = (double *)malloc(sizeof(double) * (size_t)c->D * (size_t)n);
+    for (int d = 0; d < c->D; ++d)
+        q[d] = bf16_to_double(c->q[((size_t)t * c->H + h) * c->D + d]);
+    for (int j = 0; j < n; ++j) {
+        size_t base = ((size_t)(first + j) * c->H + h) * c->D;
+        for (int d = 0; d < c->D; ++d) {
+            K[(size_t)j * c->D + d] = bf16_to_double(c->k[base + d]);
+            V[(size_t)j * c->D + d] = bf16_to_double(c->v[base + d]);
+        }
+    }
+    oracle_attend_row(q, K, V, n, c->D, c->scale, out, NULL);
+    free(V);
+    free(K);
+    free(q);
+}
+
+/* out[i] = attention of row rows[i] = t * H + h over its own window (all
+ * total_tokens*H rows when rows is NULL). */
+ORACLE_EXPORT int oracle_window(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                                const int32_t *cu_windows, int n_windows, int total_tokens, int H,
+                                int D, double scale, const int32_t *rows, int n_rows, double *out,
+                                int n_threads)
+{
+    if (n_windows <= 0 || H <= 0 || D <= 0)
+        return -1;
+    if (cu_windows[0] != 0 || cu_windows[n_windows] != total_tokens)
+        return -1;
+    for (int w = 0; w < n_windows; ++w)
+        if (cu_windows[w + 1] < cu_windows[w])
+            return -1;
+    if (!rows)
+        n_rows = total_tokens * H;
+    for (int i = 0; rows && i < n_rows; ++i)
+        if (rows[i] < 0 || rows[i] >= total_tokens * H)
+            return -1;
+    window_ctx c = {q, k, v, cu_windows, n_windows, H, D, scale};
+    run_rows(&c, window_row, rows, n_rows, D, out, n_threads);
+    return 0;
+}

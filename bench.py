@@ -1,0 +1,493 @@
+"""Benchmark of the paged GQA attention hot path on one GB300 (or N replicas).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--rows all|none]
+
+Prints ONE JSON line (rank 0).  The headline workload is the batched decode
+of the 0.6B Thinker shape: 32 requests, GQA 16/8, head_dim 128, contexts
+~ U[200, 2000], 16-token pages scattered over a 4096-page pool.  One step is
+one qa_decode_attn call over that batch (split-K kernel + combine kernel).
+The metric is the decode's algorithmic HBM bandwidth: K+V bytes of every
+cached position read plus q and out, 4096 B per position + 8192 B per
+request, divided by the device time of the call.
+
+Timing: inputs resident in HBM; four rotating copies of the decode inputs
+(about 4 x 144 MB, far above the 129 MB L2) so no step finds its K/V in L2;
+steps run back to back inside CUDA graphs (launch overhead amortised) and are
+timed with CUDA events on the launching stream; barrier + synchronize on both
+sides, max over ranks.  nvidia-smi samples clocks during the timed region.
+
+Other keys: `e2e` (the same metric with q, page table and lengths copied from
+pinned host memory and the output copied back and read every step),
+`roofline` (the decode call against the measured HBM copy bandwidth),
+`cpu_baseline` (the fp64 oracle on this host's cores, whole workload),
+`rows` (the other hot-path operations measured the same way: ragged causal
+prefill with page write, AuT windowed attention, long-context decode, the
+tiny case).  With --impl reference the oracle itself is timed as the
+reference arm.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as wl  # noqa: E402
+
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+# ------------------------------------------------------------------ helpers
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return dict(hbm=float(pk["hbm_gbs"]), bf16=float(pk["bf16_tflops"]),
+                    bf16_sustained=float(pk.get("bf16_tflops_sustained", pk["bf16_tflops"])), source="measured")
+    except Exception:
+        return dict(hbm=FALLBACK_HBM_GBS, bf16=FALLBACK_BF16_TFLOPS, bf16_sustained=1700.0, source="fallback")
+
+
+def decode_bytes(lengths, hq=16, hkv=8, d=128):
+    """Algorithmic bytes of one decode call: K and V rows of every cached
+    position, plus q and out."""
+    return int(np.sum(lengths)) * hkv * d * 2 * 2 + len(lengths) * hq * d * 2 * 2
+
+
+def prefill_flops(lengths, hq=16, d=128):
+    return int(sum(4 * hq * d * (L * (L + 1) // 2) for L in lengths))
+
+
+def prefill_bytes(total, hq=16, hkv=8, d=128):
+    # q + out (2 * hq rows), k + v read (2 * hkv rows), k + v page write (2 * hkv)
+    return total * d * 2 * (2 * hq + 4 * hkv)
+
+
+def window_flops(cu, h=14, d=64):
+    n = np.diff(np.asarray(cu, np.int64))
+    return int(4 * h * d * np.sum(n * n))
+
+
+def window_bytes(total, h=14, d=64):
+    return total * h * d * 2 * 4  # q, k, v, out
+
+
+def source_digest(*names):
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "paged_kv_gqa_attention_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(profile_name, digest):
+    """DRAM bytes per launch from a committed ncu summary, when that summary
+    was taken on the current kernel source (same digest); else None."""
+    path = os.path.join(ROOT, "profiles", profile_name)
+    try:
+        kv = {}
+        with open(path) as f:
+            for line in f:
+                if ":" in line and not line.startswith("#"):
+                    k, v = line.split(":", 1)
+                    kv[k.strip()] = v.strip()
+        if kv.get("source_digest") == digest:
+            return int(float(kv["dram_bytes_per_launch_full_workload"]))
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu_index}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = [r.split(",") for r in out.strip().splitlines() if r.strip()]
+        sm, reasons, mx = [], set(), None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [x.strip() for x in r]
+            try:
+                sm.append(float(r[1]))
+                mx = float(r[2])
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------ device setup
+def dev_tensor(a, device):
+    import torch
+
+    if a.dtype == np.uint16:
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(device)
+    return torch.from_numpy(np.ascontiguousarray(a)).to(device)
+
+
+def graph_time(fns, steps, warmup, stream, sampler=None, max_per_graph=64):
+    """Runs `steps` calls (fns cycled) inside CUDA graphs; returns seconds of
+    device time for exactly `steps` calls (events on the launching stream)."""
+    import torch
+
+    for i in range(warmup):
+        fns[i % len(fns)]()
+    torch.cuda.synchronize()
+    per = min(max_per_graph, steps)
+    if per >= len(fns):
+        per -= per % len(fns)  # every graph starts on input copy 0
+    graphs = []
+    full, rem = divmod(steps, per)
+    for n in ([per] if full else []) + ([rem] if rem else []):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(n):
+                fns[i % len(fns)]()
+        graphs.append((g, n))
+    torch.cuda.synchronize()
+    for g, _ in graphs:  # warm the graphs
+        g.replay()
+    torch.cuda.synchronize()
+    plan = [graphs[0][0]] * full + ([graphs[-1][0]] if rem else [])
+    if sampler:
+        sampler.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for g in plan:
+            g.replay()
+        e1.record(stream)
+    e1.synchronize()
+    clocks = sampler.stop() if sampler else None
+    return e0.elapsed_time(e1) / 1e3, clocks
+
+
+# ------------------------------------------------------------------ arms
+def cpu_oracle_decode(w, rank_threads=None):
+    import oracle
+
+    n = rank_threads or (os.cpu_count() or 1)
+    t0 = time.perf_counter()
+    oracle.decode(w["q"], w["k_pages"], w["v_pages"], w["page_table"], w["seq_lens"], n_threads=n)
+    return time.perf_counter() - t0, n
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    w = wl.decode_0p6b()
+    nbytes = decode_bytes(w["seq_lens"])
+    for _ in range(args.warmup):
+        cpu_oracle_decode(w)
+    times = []
+    cores = os.cpu_count() or 1
+    for _ in range(args.steps):
+        t, cores = cpu_oracle_decode(w)
+        times.append(t)
+    total = sum(times)
+    value = nbytes * args.steps / total / 1e9
+    sample = "whole workload per step: all 32 requests x 16 query heads, fp64 oracle, threads over rows"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": CONFIG_DECODE(w),
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+METRIC = "paged GQA decode attn HBM GB/s (% of peak); prefill/window attn TFLOP/s"
+
+
+def CONFIG_DECODE(w):
+    return {"workload": "batched decode 0.6B Thinker shape: 32 requests, GQA 16/8, head_dim 128, "
+                        "context ~U[200,2000], 16-token pages over a 4096-page pool (seeded shuffle)",
+            "batch": int(len(w["seq_lens"])), "sum_seq_len": int(np.sum(w["seq_lens"])),
+            "l2": "4 rotating input copies (~576 MB) > 129 MB L2", "parallelism": "replicas"}
+
+
+def run_ours(args, world, rank, local_rank):
+    import torch
+
+    import paged_kv_gqa_attention_gb300 as qa
+
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    stream = torch.cuda.Stream(device)
+    peaks = load_peaks()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist  # timing barrier / max only; no data-path collective
+
+    # ---------------- headline: batched decode 0.6B
+    w = wl.decode_0p6b()
+    nbytes = decode_bytes(w["seq_lens"])
+    copies = []
+    for _ in range(4):
+        copies.append({k: dev_tensor(w[k], device) for k in ("q", "k_pages", "v_pages", "page_table", "seq_lens")})
+    B = len(w["seq_lens"])
+    ws_bytes = qa.qa_decode_workspace_size(B, int(w["seq_lens"].max()), num_pages=4096, max_pages_per_seq=125)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=device)
+    out = torch.empty(B, 16, 128, dtype=torch.bfloat16, device=device)
+
+    def mk(c):
+        return lambda: qa.qa_decode_attn(c["q"], c["k_pages"], c["v_pages"], c["page_table"], c["seq_lens"], out,
+                                         workspace=ws, stream=stream)
+
+    fns = [mk(c) for c in copies]
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    elapsed, clocks = graph_time(fns, args.steps, args.warmup, stream, sampler)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+        t = torch.tensor([elapsed], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed = float(t.item())
+    status = qa.qa_device_status(stream)
+    if status:
+        raise RuntimeError(f"device status {status:#x} after the timed region")
+    per_call = elapsed / args.steps
+    gbs = nbytes / per_call / 1e9
+    value = gbs * world
+
+    # ---------------- end to end: host buffers, copies inside the timed region
+    hq = torch.from_numpy(w["q"].view(np.int16)).view(torch.bfloat16).pin_memory()
+    hpt = torch.from_numpy(w["page_table"]).pin_memory()
+    hsl = torch.from_numpy(w["seq_lens"]).pin_memory()
+    hout = torch.empty(B, 16, 128, dtype=torch.bfloat16).pin_memory()
+    dq, dpt, dsl = torch.empty_like(copies[0]["q"]), torch.empty_like(copies[0]["page_table"]), torch.empty_like(
+        copies[0]["seq_lens"])
+    e2e_steps = max(3, min(args.steps, 2000))
+    checksum = 0.0
+
+    def e2e_step(c):
+        with torch.cuda.stream(stream):
+            dq.copy_(hq, non_blocking=True)
+            dpt.copy_(hpt, non_blocking=True)
+            dsl.copy_(hsl, non_blocking=True)
+            qa.qa_decode_attn(dq, c["k_pages"], c["v_pages"], dpt, dsl, out, workspace=ws, stream=stream)
+            hout.copy_(out, non_blocking=True)
+        stream.synchronize()
+        return float(hout[0, 0, 0])  # the host reads the result
+
+    for i in range(max(3, args.warmup)):
+        e2e_step(copies[i % 4])
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(e2e_steps):
+        checksum += e2e_step(copies[i % 4])
+    e2e_elapsed = time.perf_counter() - t0
+    if dist:
+        t = torch.tensor([e2e_elapsed], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_elapsed = float(t.item())
+    e2e_value = nbytes / (e2e_elapsed / e2e_steps) / 1e9 * world
+    h2d = hq.numel() * 2 + hpt.numel() * 4 + hsl.numel() * 4
+    d2h = hout.numel() * 2
+
+    digest = source_digest("decode.cu", "common.cuh")
+    roofline = {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm"], "unit": "GB/s",
+                "frac": round(gbs / peaks["hbm"], 4),
+                "traffic": profiled_traffic("decode_splitk_decode0p6b.txt", digest),
+                "kernel": "decode_splitk_kernel + decode_combine_kernel (one qa_decode_attn call)",
+                "algorithmic_bytes_per_launch": nbytes, "peak_source": peaks["source"] + " (burst copy)",
+                "source_digest": digest}
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(per_call * 1e3, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": CONFIG_DECODE(w),
+        "clocks": clocks, "e2e": {"value": round(e2e_value, 3), "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
+                                  "d2h_bytes_per_step": int(d2h), "steps": e2e_steps},
+        "gpu_launches": 2 * args.steps, "roofline": roofline,
+        "tokens_per_s": round(B / per_call * world, 1),
+    }
+    del copies
+    torch.cuda.empty_cache()
+
+    if args.rows == "all":
+        line["rows"] = measure_rows(qa, device, stream, peaks, args)
+
+    if rank == 0 and not args.no_cpu:
+        t, cores = cpu_oracle_decode(w)
+        line["cpu_baseline"] = {"value": round(nbytes / t / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                                "sample": "whole batched-decode workload once (32 requests x 16 heads), fp64"}
+    if rank == 0:
+        print(json.dumps(line))
+
+
+def measure_rows(qa, device, stream, peaks, args):
+    """The other hot-path operations, each timed the same way (graphs of
+    back-to-back calls, inputs in HBM, above L2 or rotated)."""
+    import torch
+
+    rows = {}
+    steps = max(20, min(args.steps, 400))
+
+    # ragged causal prefill with page write (16 requests, ~3.9K tokens)
+    w = wl.prefill_bucket()
+    T = int(w["cu_seqlens"][-1])
+    cps = []
+    for _ in range(4):
+        cps.append({k: dev_tensor(w[k], device) for k in ("q", "k", "v", "cu_seqlens", "page_table", "k_pages", "v_pages")})
+    outp = torch.empty(T, 16, 128, dtype=torch.bfloat16, device=device)
+
+    def mkp(c):
+        return lambda: qa.qa_prefill_attn(c["q"], c["k"], c["v"], c["cu_seqlens"], c["page_table"], c["k_pages"],
+                                          c["v_pages"], outp, stream=stream)
+
+    el, _ = graph_time([mkp(c) for c in cps], steps, 5, stream)
+    t = el / steps
+    fl, by = prefill_flops(w["lengths"]), prefill_bytes(T)
+    rows["prefill"] = {"workload": "ragged causal prefill + KV page write: 16 requests, ceil(13 d)+40 tokens "
+                                   "(d~U[1,30] s), GQA 16/8 x 128", "total_tokens": T, "us_per_call": round(t * 1e6, 2),
+                       "tflops": round(fl / t / 1e12, 3), "gbs": round(by / t / 1e9, 1),
+                       "frac_bf16_peak": round(fl / t / 1e12 / peaks["bf16"], 4),
+                       "frac_hbm": round(by / t / 1e9 / peaks["hbm"], 4), "flops": fl, "bytes": by,
+                       "gpu_launches_per_call": 2}
+    del cps
+    # AuT windowed attention (8 requests, ~63K tokens, 14 x 64)
+    w = wl.window_aut()
+    cu = qa.qa_window_plan(w["token_counts"])
+    T = int(cu[-1])
+    cps = []
+    for _ in range(2):
+        cps.append({k: dev_tensor(w[k], device) for k in ("q", "k", "v")})
+    dcu = dev_tensor(cu, device)
+    outw = torch.empty(T, 14, 64, dtype=torch.bfloat16, device=device)
+
+    def mkw(c):
+        return lambda: qa.qa_window_attn(c["q"], c["k"], c["v"], dcu, outw, stream=stream)
+
+    el, _ = graph_time([mkw(c) for c in cps], max(10, steps // 4), 3, stream)
+    t = el / max(10, steps // 4)
+    fl, by = window_flops(cu), window_bytes(T)
+    rows["window"] = {"workload": "AuT windowed attention: 8 requests d~U[10,1200] s, 104-token windows, 14 x 64",
+                      "total_tokens": T, "windows": int(len(cu) - 1), "us_per_call": round(t * 1e6, 2),
+                      "tflops": round(fl / t / 1e12, 3), "gbs": round(by / t / 1e9, 1),
+                      "frac_bf16_peak": round(fl / t / 1e12 / peaks["bf16"], 4),
+                      "frac_hbm": round(by / t / 1e9 / peaks["hbm"], 4), "flops": fl, "bytes": by,
+                      "gpu_launches_per_call": 1}
+    del cps
+    # long-context decode 1.7B (64 requests, ~9K tokens each)
+    w = wl.decode_1p7b()
+    c = {k: dev_tensor(w[k], device) for k in ("q", "k_pages", "v_pages", "page_table", "seq_lens")}
+    B = len(w["seq_lens"])
+    ws = torch.empty(qa.qa_decode_workspace_size(B, int(w["seq_lens"].max()), num_pages=65536, max_pages_per_seq=1000),
+                     dtype=torch.uint8, device=device)
+    outd = torch.empty(B, 16, 128, dtype=torch.bfloat16, device=device)
+    f = lambda: qa.qa_decode_attn(c["q"], c["k_pages"], c["v_pages"], c["page_table"], c["seq_lens"], outd,  # noqa
+                                  workspace=ws, stream=stream)
+    n = max(10, steps // 4)
+    el, _ = graph_time([f], n, 3, stream)
+    t = el / n
+    by = decode_bytes(w["seq_lens"])
+    rows["decode_long"] = {"workload": "long-context decode 1.7B Thinker shape: 64 requests, L~U[2000,16000], "
+                                       "65536-page pool", "sum_seq_len": int(np.sum(w["seq_lens"])),
+                           "us_per_call": round(t * 1e6, 2), "gbs": round(by / t / 1e9, 1),
+                           "frac_hbm": round(by / t / 1e9 / peaks["hbm"], 4), "bytes": by,
+                           "tokens_per_s": round(B / t, 1), "gpu_launches_per_call": 2}
+    del c
+    torch.cuda.empty_cache()
+    # tiny: prefill 64 then decode (latency)
+    w = wl.tiny()
+    c = {k: dev_tensor(w[k], device) for k in ("q", "k", "v", "cu_seqlens", "page_table", "k_pages", "v_pages",
+                                                "decode_q", "seq_lens")}
+    outt = torch.empty(64, 16, 128, dtype=torch.bfloat16, device=device)
+    outd = torch.empty(1, 16, 128, dtype=torch.bfloat16, device=device)
+    ws = torch.empty(qa.qa_decode_workspace_size(1, 64, num_pages=4, max_pages_per_seq=4), dtype=torch.uint8,
+                     device=device)
+
+    def tiny_step():
+        qa.qa_prefill_attn(c["q"], c["k"], c["v"], c["cu_seqlens"], c["page_table"], c["k_pages"], c["v_pages"], outt,
+                           stream=stream)
+        qa.qa_decode_attn(c["decode_q"], c["k_pages"], c["v_pages"], c["page_table"], c["seq_lens"], outd,
+                          workspace=ws, stream=stream)
+
+    el, _ = graph_time([tiny_step], steps, 5, stream)
+    rows["tiny"] = {"workload": "tiny: prefill of 64 tokens into 4 permuted pages, then 1 decode token",
+                    "us_per_step": round(el / steps * 1e6, 2), "note": "latency-bound; no roofline fraction"}
+    status = qa.qa_device_status(stream)
+    if status:
+        raise RuntimeError(f"device status {status:#x} after the row measurements")
+    return rows
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--rows", choices=["all", "none"], default="all")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the cpu_baseline leg")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1 and args.impl == "ours":
+        import torch
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local_rank)
+    if world > 1 and args.impl == "ours":
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,212 @@
+/*
+ * qa.h -- paged GQA attention for Qwen3-ASR-shaped serving, C ABI.
+ *
+ * Plain C99, extern "C".  The shared library libqa.so exports only the qa_*
+ * symbols declared here; every kernel and helper stays hidden.  The
+ * conventions follow the qwenasr.cpp public ABI (qwenasr.cpp ARCHITECTURE.md,
+ * "Public API" and "ABI guarantee"): integer status codes with the same
+ * numbering, a thread-local last-error message, a version string, and an
+ * abi_version field that callers set through the default-params helper and
+ * that the entry points check against the closed range
+ * [QA_ABI_MIN_VERSION, QA_ABI_VERSION].
+ *
+ * Three operations make up the attention core:
+ *
+ *   qa_decode_attn   batched single-token decode over a paged KV cache with
+ *                    grouped-query attention (16 query heads over 8 KV heads,
+ *                    head_dim 128).  qwenasr.cpp ARCHITECTURE.md, "Qwen3
+ *                    Thinker decoder" (decode appends one position at cur_len
+ *                    and attends over [0, cur_len + 1)) and "GGUF layout"
+ *                    (head_count 16, head_count_kv 8, key_length 128); M*
+ *                    "Speech recognition: Whisper and Qwen3-ASR", "Graph"
+ *                    (decode runs on paged KV) and "Serving notes" (pages).
+ *   qa_prefill_attn  ragged causal prefill of packed prompts, writing the
+ *                    fresh K/V into their pages.  qwenasr.cpp ARCHITECTURE.md,
+ *                    "Qwen3 Thinker decoder" (prefill rewinds the cache, writes
+ *                    K/V at [n_past, n_past + T) and attends over
+ *                    [0, n_past + T)); M* page, "Graph" (prefill on packed
+ *                    token buckets).
+ *   qa_window_attn   bidirectional attention confined to windows of the
+ *                    packed encoder sequence.  qwenasr.cpp ARCHITECTURE.md,
+ *                    "Windowed audio tower" (block-diagonal mask over windows
+ *                    of 104 tokens, plain bidirectional MHA, 1/sqrt(head_dim));
+ *                    M* page, "Graph" (one packed forward with one segment per
+ *                    window of every request).
+ *
+ * Common rules
+ *
+ *   - Every tensor argument is a DEVICE pointer to caller-owned memory,
+ *     row-major and contiguous, except where a function says "host".  The
+ *     library allocates nothing during a call.
+ *   - bf16 means IEEE bfloat16.  Inputs are bf16; scores and softmax run in
+ *     fp32; outputs are rounded to bf16 (round to nearest even).  (OneSpeech
+ *     Qwen3 page, "Front end and graph numerics": score and softmax
+ *     intermediates in float32, attended output rounded to bfloat16.)
+ *   - Calls are asynchronous on params->stream (NULL = the legacy default
+ *     stream) unless params->debug_checks is set, in which case the call
+ *     synchronises the stream and reports device-side errors.
+ *   - Host-checkable errors (NULL pointers, unsupported shapes, a workspace
+ *     that is too small, a bad abi_version) return QA_STATUS_INVALID_PARAMS
+ *     before anything is launched and set qa_last_error().  A failed launch
+ *     returns QA_STATUS_LAUNCH_FAILED.
+ *   - Device-side checks never fault or trap: a page id outside
+ *     [0, num_pages), a sequence longer than its page-table row, a malformed
+ *     cu_* array or an expired bounded wait skips the affected work and sets
+ *     a bit in a per-library device status word, which qa_device_status()
+ *     (or a debug_checks call) reads and clears.
+ *   - Decode layout of the paged pool: [num_pages][page_size][n_kv_heads]
+ *     [head_dim], token-major inside a page like the packed [T][Hkv][D] rows.
+ *     Query head h reads KV head h / (n_q_heads / n_kv_heads) (contiguous
+ *     GQA grouping).
+ */
+#ifndef QA_H
+#define QA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define QA_ABI_VERSION 1
+#define QA_ABI_MIN_VERSION 1
+
+/* Status codes: numbering of the qwenasr.cpp public ABI ("Public API");
+ * -2 (load failed) and -5 (cancelled) have no use here.  -6 is new: a kernel
+ * reported an error through the device status word. */
+typedef enum qa_status {
+    QA_STATUS_OK = 0,
+    QA_STATUS_INVALID_PARAMS = -1,
+    QA_STATUS_LAUNCH_FAILED = -3,
+    QA_STATUS_OOM = -4,
+    QA_STATUS_DEVICE_ERROR = -6
+} qa_status;
+
+/* Bits of the device status word (qa_device_status). */
+#define QA_DEVICE_BAD_PAGE 0x1u     /* page id outside [0, num_pages)            */
+#define QA_DEVICE_BAD_LENGTH 0x2u   /* seq_len < 0 or > max_pages * page_size    */
+#define QA_DEVICE_BAD_SEGMENTS 0x4u /* cu_seqlens / cu_windows not monotonic, or
+                                       not ending at total_tokens               */
+#define QA_DEVICE_TIMEOUT 0x8u      /* a bounded wait inside a kernel expired    */
+
+typedef struct qa_attn_params {
+    int abi_version;       /* set by qa_attn_default_params()                    */
+    int n_q_heads;         /* decode/prefill: 16; window: 14                     */
+    int n_kv_heads;        /* decode/prefill: 8;  window: must equal n_q_heads   */
+    int head_dim;          /* decode/prefill: 128; window: 64 or 128             */
+    int page_size;         /* tokens per page; 16                                */
+    int num_pages;         /* pool size P (pages in k_pages and v_pages)         */
+    int max_pages_per_seq; /* page_table row stride                              */
+    float scale;           /* softmax scale; 0 => 1/sqrt(head_dim)               */
+    void *stream;          /* cudaStream_t; NULL => legacy default stream        */
+    void *workspace;       /* decode scratch (device), caller-owned              */
+    size_t workspace_bytes;
+    int debug_checks;      /* 1 => synchronise and report device-side errors     */
+} qa_attn_params;
+
+/* Defaults: abi_version = QA_ABI_VERSION, 16/8/128 heads, page_size 16,
+ * scale 0 (1/sqrt(head_dim)), stream NULL, no workspace, debug_checks 0.
+ * num_pages and max_pages_per_seq are 0 and must be set by the caller. */
+qa_attn_params qa_attn_default_params(void);
+
+/* Bytes of device workspace qa_decode_attn needs for `batch` requests on the
+ * CURRENT device with these params (the split-K partial results: one fp32
+ * (max, sum, accumulator[head_dim]) record per query head per work segment).
+ * max_seq_len is the longest sequence the caller will pass (used only for
+ * validation).  Returns 0 on invalid arguments and sets qa_last_error(). */
+size_t qa_decode_workspace_size(int batch, int max_seq_len, const qa_attn_params *params);
+
+/* Paged GQA decode: one query token per request.
+ *
+ *   q          bf16 [batch][n_q_heads][head_dim]
+ *   k_pages    bf16 [num_pages][page_size][n_kv_heads][head_dim]
+ *   v_pages    bf16, same layout as k_pages
+ *   page_table int32 [batch][max_pages_per_seq]; entry j of row b is the
+ *              physical page holding positions [j*page_size, (j+1)*page_size)
+ *              of request b; entries past ceil(seq_lens[b]/page_size) are
+ *              never read
+ *   seq_lens   int32 [batch]: number of cached positions request b attends
+ *              over, including the current token, whose K/V must already be
+ *              in its page; 0 gives a zero output row
+ *   out        bf16 [batch][n_q_heads][head_dim]
+ *
+ * out[b][h] = softmax_j(q[b][h] . K_b[j] * scale) . V_b[j] over
+ * j in [0, seq_lens[b]).  Slots past seq_lens[b] in the last page are never
+ * read into the result (they may hold anything, NaN included).
+ * Supported: head_dim 128, page_size 16, n_kv_heads in [1, 8],
+ * n_q_heads / n_kv_heads in {1, 2}.  Needs params->workspace of at least
+ * qa_decode_workspace_size(batch, ...) bytes, 256-byte aligned. */
+qa_status qa_decode_attn(const void *q, const void *k_pages, const void *v_pages,
+                         const int32_t *page_table, const int32_t *seq_lens, int batch,
+                         void *out, const qa_attn_params *params);
+
+/* Ragged causal prefill with the KV page write.
+ *
+ *   q          bf16 [total_tokens][n_q_heads][head_dim], requests packed
+ *   k, v       bf16 [total_tokens][n_kv_heads][head_dim]
+ *   cu_seqlens int32 [batch + 1]: request r owns rows [cu[r], cu[r+1]);
+ *              cu[0] = 0, cu[batch] = total_tokens, non-decreasing
+ *   page_table int32 [batch][max_pages_per_seq]: destination pages
+ *   k_pages, v_pages  destination pools (layout as in qa_decode_attn)
+ *   out        bf16 [total_tokens][n_q_heads][head_dim]
+ *
+ * Writes row i of request r, bit for bit, to page page_table[r][i/page_size]
+ * slot i % page_size of both pools (positions [0, len) of each request:
+ * n_past = 0, the cache was rewound), and computes
+ * out[t][h] = softmax over j <= t within the request of q[t][h] . k[j][g]
+ * (g = h / group) times v[j][g], from the packed k and v.  Pool slots that no
+ * row maps to are left untouched.
+ * Supported: head_dim 128, page_size 16, n_q_heads / n_kv_heads in {1, 2}. */
+qa_status qa_prefill_attn(const void *q, const void *k, const void *v,
+                          const int32_t *cu_seqlens, int batch, int total_tokens,
+                          const int32_t *page_table, void *k_pages, void *v_pages, void *out,
+                          const qa_attn_params *params);
+
+/* Windowed bidirectional attention over a packed sequence.
+ *
+ *   q, k, v    bf16 [total_tokens][n_q_heads][head_dim] (n_kv_heads must equal
+ *              n_q_heads: plain MHA)
+ *   cu_windows int32 [n_windows + 1]: window w owns rows
+ *              [cu_windows[w], cu_windows[w+1]); cu_windows[0] = 0,
+ *              cu_windows[n_windows] = total_tokens, non-decreasing
+ *   out        bf16 [total_tokens][n_q_heads][head_dim]
+ *
+ * Every row attends over all rows of its own window and nothing else.
+ * Supported: head_dim 64 or 128, windows of any length. */
+qa_status qa_window_attn(const void *q, const void *k, const void *v,
+                         const int32_t *cu_windows, int n_windows, int total_tokens, void *out,
+                         const qa_attn_params *params);
+
+/* Window plan (HOST helper, host pointers).  Cuts each request's encoder
+ * tokens into consecutive windows of window_tokens tokens counted from the
+ * request's own start, the last window partial (qwenasr.cpp ARCHITECTURE.md,
+ * "Windowed audio tower": windows of window_aftercnn = conv_out(chunk_mel) *
+ * window_chunks = 13 * 8 = 104 tokens).  A request with no token gives no
+ * window.  window_tokens <= 0 selects 104.
+ *
+ *   token_counts  host int32 [n_requests]
+ *   cu_windows    host int32 [capacity]; receives n_windows + 1 offsets
+ *
+ * Returns the number of windows, or -1 (and sets qa_last_error()) on a
+ * negative count, a capacity that is too small, or int32 overflow. */
+int qa_window_plan(const int32_t *token_counts, int n_requests, int window_tokens,
+                   int32_t *cu_windows, int capacity);
+
+/* Synchronises `stream` (cudaStream_t, NULL = legacy default), then reads and
+ * clears the device status word of the current device.  Returns its bits
+ * (QA_DEVICE_*), 0 when nothing went wrong, or -1 on a CUDA error. */
+int qa_device_status(void *stream);
+
+/* Thread-local message describing the last failure on this thread; valid
+ * until the next qa_* call on the same thread.  Never NULL. */
+const char *qa_last_error(void);
+
+/* Library version string ("qa-attn <version> abi <n>"). */
+const char *qa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QA_H */

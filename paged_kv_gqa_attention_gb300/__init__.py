@@ -1,0 +1,247 @@
+"""Python binding of libqa, the GB300 paged GQA attention library.
+
+Thin argument marshalling over the C ABI declared in ``include/qa.h``: each
+function takes torch CUDA tensors, checks dtype / device / contiguity, and
+passes raw pointers, sizes and the current CUDA stream to the ``qa_*`` entry
+point of the same name.  Every step of the computation runs in the library's
+CUDA kernels; there is no other implementation behind these names, and
+importing this package fails loudly when ``libqa.so`` has not been built.
+
+    qa_decode_attn    paged GQA decode (split-K flash decode + combine)
+    qa_prefill_attn   ragged causal prefill with the KV page write
+    qa_window_attn    windowed bidirectional encoder attention
+    qa_window_plan    cu_windows from per-request encoder token counts (host)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+__all__ = [
+    "QA_ABI_VERSION", "QAError", "lib_path", "qa_version", "qa_last_error", "qa_attn_default_params",
+    "qa_decode_workspace_size", "qa_decode_attn", "qa_prefill_attn", "qa_window_attn", "qa_window_plan",
+    "qa_device_status", "DEVICE_STATUS_BITS",
+]
+
+QA_ABI_VERSION = 1
+_PKG = os.path.dirname(os.path.abspath(__file__))
+lib_path = os.path.join(_PKG, "libqa.so")
+
+DEVICE_STATUS_BITS = {0x1: "bad page id", 0x2: "bad length", 0x4: "bad segments", 0x8: "timeout"}
+
+
+class QAError(RuntimeError):
+    """A qa_* call returned a non-zero status."""
+
+    def __init__(self, fn: str, status: int, message: str):
+        super().__init__(f"{fn} failed with status {status}: {message}")
+        self.status = status
+
+
+class qa_attn_params(ctypes.Structure):
+    _fields_ = [
+        ("abi_version", ctypes.c_int),
+        ("n_q_heads", ctypes.c_int),
+        ("n_kv_heads", ctypes.c_int),
+        ("head_dim", ctypes.c_int),
+        ("page_size", ctypes.c_int),
+        ("num_pages", ctypes.c_int),
+        ("max_pages_per_seq", ctypes.c_int),
+        ("scale", ctypes.c_float),
+        ("stream", ctypes.c_void_p),
+        ("workspace", ctypes.c_void_p),
+        ("workspace_bytes", ctypes.c_size_t),
+        ("debug_checks", ctypes.c_int),
+    ]
+
+
+def _load():
+    if not os.path.exists(lib_path):
+        raise ImportError(
+            f"libqa.so is not built ({lib_path}); run `python -c 'import __graft_entry__ as g; g.build()'`")
+    lib = ctypes.CDLL(lib_path)
+    P, I, PP = ctypes.c_void_p, ctypes.c_int, ctypes.POINTER(qa_attn_params)
+    lib.qa_attn_default_params.restype = qa_attn_params
+    lib.qa_attn_default_params.argtypes = []
+    lib.qa_decode_workspace_size.restype = ctypes.c_size_t
+    lib.qa_decode_workspace_size.argtypes = [I, I, PP]
+    lib.qa_decode_attn.restype = I
+    lib.qa_decode_attn.argtypes = [P, P, P, P, P, I, P, PP]
+    lib.qa_prefill_attn.restype = I
+    lib.qa_prefill_attn.argtypes = [P, P, P, P, I, I, P, P, P, P, PP]
+    lib.qa_window_attn.restype = I
+    lib.qa_window_attn.argtypes = [P, P, P, P, I, I, P, PP]
+    lib.qa_window_plan.restype = I
+    lib.qa_window_plan.argtypes = [P, I, I, P, I]
+    lib.qa_device_status.restype = I
+    lib.qa_device_status.argtypes = [P]
+    lib.qa_last_error.restype = ctypes.c_char_p
+    lib.qa_last_error.argtypes = []
+    lib.qa_version.restype = ctypes.c_char_p
+    lib.qa_version.argtypes = []
+    return lib
+
+
+_lib = _load()
+
+
+def qa_version() -> str:
+    return _lib.qa_version().decode()
+
+
+def qa_last_error() -> str:
+    return _lib.qa_last_error().decode()
+
+
+def _check(fn: str, status: int):
+    if status != 0:
+        raise QAError(fn, status, qa_last_error())
+
+
+def _torch():
+    import torch
+
+    return torch
+
+
+def _stream_ptr(stream):
+    torch = _torch()
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dev(t, name, dtype=None, ndim=None):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {tuple(t.shape)}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def qa_attn_default_params() -> qa_attn_params:
+    return _lib.qa_attn_default_params()
+
+
+def _params(*, n_q_heads, n_kv_heads, head_dim, page_size=16, num_pages=0, max_pages_per_seq=0, scale=0.0,
+            stream=None, workspace=None, debug_checks=False):
+    p = _lib.qa_attn_default_params()
+    p.n_q_heads, p.n_kv_heads, p.head_dim = n_q_heads, n_kv_heads, head_dim
+    p.page_size, p.num_pages, p.max_pages_per_seq = page_size, num_pages, max_pages_per_seq
+    p.scale = float(scale)
+    p.stream = _stream_ptr(stream)
+    if workspace is not None:
+        p.workspace = _dev(workspace, "workspace")
+        p.workspace_bytes = workspace.numel() * workspace.element_size()
+    p.debug_checks = 1 if debug_checks else 0
+    return p
+
+
+def qa_decode_workspace_size(batch: int, max_seq_len: int, *, n_q_heads=16, n_kv_heads=8, head_dim=128,
+                             page_size=16, num_pages=1, max_pages_per_seq=1) -> int:
+    """Bytes of decode workspace for `batch` requests on the current device."""
+    p = _lib.qa_attn_default_params()
+    p.n_q_heads, p.n_kv_heads, p.head_dim = n_q_heads, n_kv_heads, head_dim
+    p.page_size, p.num_pages, p.max_pages_per_seq = page_size, num_pages, max_pages_per_seq
+    n = _lib.qa_decode_workspace_size(int(batch), int(max_seq_len), ctypes.byref(p))
+    if n == 0:
+        raise QAError("qa_decode_workspace_size", -1, qa_last_error())
+    return int(n)
+
+
+def qa_decode_attn(q, k_pages, v_pages, page_table, seq_lens, out=None, *, workspace=None, scale=0.0,
+                   stream=None, debug_checks=False):
+    """Paged GQA decode.  q bf16 [B,Hq,D]; pools bf16 [P,16,Hkv,D];
+    page_table int32 [B,max_pages]; seq_lens int32 [B].  Returns out bf16
+    [B,Hq,D].  `workspace` is a device byte tensor of at least
+    qa_decode_workspace_size(B, ...) bytes (allocated here if omitted)."""
+    torch = _torch()
+    B, Hq, D = q.shape
+    P, PS, Hkv, D2 = k_pages.shape
+    if D2 != D or tuple(v_pages.shape) != tuple(k_pages.shape) or page_table.dim() != 2 or page_table.shape[0] != B:
+        raise ValueError("inconsistent decode shapes")
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None:
+        nbytes = qa_decode_workspace_size(B, 0, n_q_heads=Hq, n_kv_heads=Hkv, head_dim=D, page_size=PS,
+                                          num_pages=P, max_pages_per_seq=page_table.shape[1])
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    p = _params(n_q_heads=Hq, n_kv_heads=Hkv, head_dim=D, page_size=PS, num_pages=P,
+                max_pages_per_seq=page_table.shape[1], scale=scale, stream=stream, workspace=workspace,
+                debug_checks=debug_checks)
+    st = _lib.qa_decode_attn(_dev(q, "q", torch.bfloat16, 3), _dev(k_pages, "k_pages", torch.bfloat16, 4),
+                             _dev(v_pages, "v_pages", torch.bfloat16, 4),
+                             _dev(page_table, "page_table", torch.int32, 2), _dev(seq_lens, "seq_lens", torch.int32, 1),
+                             B, _dev(out, "out", torch.bfloat16, 3), ctypes.byref(p))
+    _check("qa_decode_attn", st)
+    return out
+
+
+def qa_prefill_attn(q, k, v, cu_seqlens, page_table, k_pages, v_pages, out=None, *, scale=0.0, stream=None,
+                    debug_checks=False):
+    """Ragged causal prefill with the KV page write.  q bf16 [T,Hq,D]; k/v
+    bf16 [T,Hkv,D]; cu_seqlens int32 [B+1]; page_table int32 [B,max_pages];
+    pools bf16 [P,16,Hkv,D] (written in place).  Returns out bf16 [T,Hq,D]."""
+    torch = _torch()
+    T, Hq, D = q.shape
+    Hkv = k.shape[1]
+    B = cu_seqlens.shape[0] - 1
+    P, PS = k_pages.shape[0], k_pages.shape[1]
+    if out is None:
+        out = torch.empty_like(q)
+    p = _params(n_q_heads=Hq, n_kv_heads=Hkv, head_dim=D, page_size=PS, num_pages=P,
+                max_pages_per_seq=page_table.shape[1], scale=scale, stream=stream, debug_checks=debug_checks)
+    st = _lib.qa_prefill_attn(_dev(q, "q", torch.bfloat16, 3), _dev(k, "k", torch.bfloat16, 3),
+                              _dev(v, "v", torch.bfloat16, 3), _dev(cu_seqlens, "cu_seqlens", torch.int32, 1), B, T,
+                              _dev(page_table, "page_table", torch.int32, 2), _dev(k_pages, "k_pages", torch.bfloat16, 4),
+                              _dev(v_pages, "v_pages", torch.bfloat16, 4), _dev(out, "out", torch.bfloat16, 3),
+                              ctypes.byref(p))
+    _check("qa_prefill_attn", st)
+    return out
+
+
+def qa_window_attn(q, k, v, cu_windows, out=None, *, scale=0.0, stream=None, debug_checks=False):
+    """Windowed bidirectional attention.  q/k/v bf16 [T,H,D]; cu_windows
+    int32 [W+1].  Returns out bf16 [T,H,D]."""
+    torch = _torch()
+    T, H, D = q.shape
+    W = cu_windows.shape[0] - 1
+    if out is None:
+        out = torch.empty_like(q)
+    p = _params(n_q_heads=H, n_kv_heads=k.shape[1], head_dim=D, scale=scale, stream=stream,
+                debug_checks=debug_checks)
+    st = _lib.qa_window_attn(_dev(q, "q", torch.bfloat16, 3), _dev(k, "k", torch.bfloat16, 3),
+                             _dev(v, "v", torch.bfloat16, 3), _dev(cu_windows, "cu_windows", torch.int32, 1), W, T,
+                             _dev(out, "out", torch.bfloat16, 3), ctypes.byref(p))
+    _check("qa_window_attn", st)
+    return out
+
+
+def qa_window_plan(token_counts, window_tokens: int = 0) -> np.ndarray:
+    """cu_windows (int32 numpy) for per-request encoder token counts; windows
+    of window_tokens (0 = 104) from each request's start, last one partial."""
+    counts = np.ascontiguousarray(np.asarray(token_counts, dtype=np.int32))
+    w = int(window_tokens) if window_tokens > 0 else 104
+    cap = int(sum(-(-int(c) // w) for c in counts if c > 0)) + 1
+    cu = np.zeros(max(cap, 1), dtype=np.int32)
+    n = _lib.qa_window_plan(counts.ctypes.data_as(ctypes.c_void_p), len(counts), int(window_tokens),
+                            cu.ctypes.data_as(ctypes.c_void_p), len(cu))
+    if n < 0:
+        raise QAError("qa_window_plan", -1, qa_last_error())
+    return cu[: n + 1]
+
+
+def qa_device_status(stream=None) -> int:
+    """Synchronise the stream, then read and clear the device status bits."""
+    n = _lib.qa_device_status(_stream_ptr(stream))
+    if n < 0:
+        raise QAError("qa_device_status", -1, qa_last_error())
+    return n

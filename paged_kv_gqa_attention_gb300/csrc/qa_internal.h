@@ -1,0 +1,41 @@
+// Internal interface between the C-ABI layer (qa_api.cu) and the kernel
+// translation units.  Not installed, not exported.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "qa.h"
+
+namespace qa {
+
+// ---- decode (decode.cu)
+// CTAs of the persistent split-K decode grid on `device` (one per SM).
+int decode_grid_ctas(int device);
+// Workspace bytes for the split-K partials.
+size_t decode_workspace_bytes(int batch, int n_q_heads, int head_dim, int ctas);
+// Largest batch the decode kernel accepts (its page prefix sums live in
+// shared memory).
+constexpr int kDecodeMaxBatch = 4096;
+cudaError_t launch_decode(const void *q, const void *k_pages, const void *v_pages,
+                          const int32_t *page_table, const int32_t *seq_lens, int batch, void *out,
+                          const qa_attn_params &p, float scale, int ctas, cudaStream_t stream);
+unsigned int status_read_clear_decode(cudaStream_t stream, cudaError_t *err);
+
+// ---- prefill (prefill.cu): page write + causal attention
+cudaError_t launch_page_write(const void *k, const void *v, const int32_t *cu_seqlens, int batch,
+                              int total_tokens, const int32_t *page_table, void *k_pages,
+                              void *v_pages, const qa_attn_params &p, cudaStream_t stream);
+cudaError_t launch_prefill(const void *q, const void *k, const void *v, const int32_t *cu_seqlens,
+                           int batch, int total_tokens, void *out, const qa_attn_params &p,
+                           float scale, cudaStream_t stream);
+unsigned int status_read_clear_prefill(cudaStream_t stream, cudaError_t *err);
+
+// ---- window (window.cu)
+cudaError_t launch_window(const void *q, const void *k, const void *v, const int32_t *cu_windows,
+                          int n_windows, int total_tokens, void *out, const qa_attn_params &p,
+                          float scale, cudaStream_t stream);
+unsigned int status_read_clear_window(cudaStream_t stream, cudaError_t *err);
+
+}  // namespace qa

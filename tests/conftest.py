@@ -1,9 +1,20 @@
-"""Shared pytest configuration: the ``gpu`` marker and the oracle build."""
+"""Shared pytest configuration: the ``gpu`` marker, and building the CUDA
+library and the CPU oracle before any test module imports them (so a missing
+build fails loudly instead of skipping)."""
 import pytest
 
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a) and the built CUDA library")
+
+
+def pytest_sessionstart(session):
+    from paged_kv_gqa_attention_gb300 import _build
+
+    _build.build()
+    import oracle
+
+    oracle.build()
 
 
 @pytest.fixture(scope="session")

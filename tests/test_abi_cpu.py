@@ -1,0 +1,141 @@
+"""C-ABI checks that need no GPU: the library builds, loads and exports
+exactly the qa_* entry points declared in include/qa.h; the header compiles
+as strict C99; host-side validation returns status codes without touching a
+device; the host window planner matches the oracle's bit for bit."""
+import ctypes
+import os
+import re
+import subprocess
+
+import numpy as np
+import pytest
+
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "qa.h")
+
+
+@pytest.fixture(scope="session")
+def libqa():
+    from paged_kv_gqa_attention_gb300 import _build
+
+    path = _build.build()
+    return ctypes.CDLL(path)
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(qa_[a-z_]+)\s*\(", src)))
+
+
+def test_exports_exactly_the_declared_symbols(libqa):
+    from paged_kv_gqa_attention_gb300 import _build
+
+    out = subprocess.run(["nm", "-D", "--defined-only", _build.LIB], capture_output=True, text=True, check=True).stdout
+    exported = sorted(line.split()[-1] for line in out.splitlines() if line.strip())
+    declared = declared_functions()
+    assert declared, "no declarations parsed from qa.h"
+    assert exported == declared
+    for name in declared:
+        assert hasattr(libqa, name)
+
+
+def test_header_is_strict_c99(libqa, tmp_path):
+    from paged_kv_gqa_attention_gb300 import _build
+
+    c = tmp_path / "abi_c.c"
+    c.write_text(r'''
+#include "qa.h"
+#include <stdio.h>
+#include <string.h>
+int main(void) {
+    qa_attn_params p = qa_attn_default_params();
+    int32_t counts[2] = {117, 5};
+    int32_t cu[8];
+    if (p.abi_version != QA_ABI_VERSION || p.n_q_heads != 16 || p.n_kv_heads != 8) return 1;
+    if (qa_decode_attn(NULL, NULL, NULL, NULL, NULL, 1, NULL, &p) != QA_STATUS_INVALID_PARAMS) return 2;
+    if (strlen(qa_last_error()) == 0) return 3;
+    if (qa_window_attn(NULL, NULL, NULL, NULL, 1, 0, NULL, NULL) != QA_STATUS_INVALID_PARAMS) return 4;
+    p.abi_version = QA_ABI_VERSION + 1;
+    if (qa_prefill_attn(NULL, NULL, NULL, NULL, 1, 0, NULL, NULL, NULL, NULL, &p) != QA_STATUS_INVALID_PARAMS) return 5;
+    if (qa_window_plan(counts, 2, 0, cu, 8) != 3 || cu[1] != 104 || cu[2] != 117 || cu[3] != 122) return 6;
+    printf("%s\n", qa_version());
+    return 0;
+}
+''')
+    exe = tmp_path / "abi_c"
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic", "-I", os.path.join(ROOT, "include"),
+                    str(c), "-o", str(exe), _build.LIB, f"-Wl,-rpath,{os.path.dirname(_build.LIB)}"], check=True)
+    res = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert res.returncode == 0, res.stdout + res.stderr
+    assert "abi 1" in res.stdout
+
+
+def _params(libqa):
+    import paged_kv_gqa_attention_gb300 as qa
+
+    return qa.qa_attn_default_params()
+
+
+def test_invalid_arguments_return_status_without_device(libqa):
+    import paged_kv_gqa_attention_gb300 as qa
+
+    lib = qa._lib
+    p = qa.qa_attn_default_params()
+    fake = ctypes.c_void_p(0x1000)
+    # NULL params
+    assert lib.qa_decode_attn(fake, fake, fake, fake, fake, 1, fake, None) == -1
+    assert "params is NULL" in qa.qa_last_error()
+    # wrong abi version
+    p.abi_version = 99
+    assert lib.qa_window_attn(fake, fake, fake, fake, 1, 1, fake, ctypes.byref(p)) == -1
+    assert "abi_version" in qa.qa_last_error()
+    p = qa.qa_attn_default_params()
+    p.num_pages, p.max_pages_per_seq = 4, 4
+    # unsupported head_dim / heads / page size / batch
+    for field, bad in (("head_dim", 96), ("n_kv_heads", 9), ("n_q_heads", 24), ("page_size", 32)):
+        q = qa.qa_attn_default_params()
+        q.num_pages, q.max_pages_per_seq = 4, 4
+        setattr(q, field, bad)
+        assert lib.qa_decode_attn(fake, fake, fake, fake, fake, 1, fake, ctypes.byref(q)) == -1, field
+    assert lib.qa_decode_attn(fake, fake, fake, fake, fake, 0, fake, ctypes.byref(p)) == -1
+    assert "batch" in qa.qa_last_error()
+    assert lib.qa_decode_attn(None, fake, fake, fake, fake, 1, fake, ctypes.byref(p)) == -1
+    assert "NULL" in qa.qa_last_error()
+    # misaligned pointer
+    odd = ctypes.c_void_p(0x1002)
+    assert lib.qa_decode_attn(odd, fake, fake, fake, fake, 1, fake, ctypes.byref(p)) == -1
+    assert "aligned" in qa.qa_last_error()
+    # prefill: negative total, window: n_kv != n_q, bad scale
+    assert lib.qa_prefill_attn(fake, fake, fake, fake, 1, -1, fake, fake, fake, fake, ctypes.byref(p)) == -1
+    w = qa.qa_attn_default_params()
+    w.n_q_heads, w.n_kv_heads, w.head_dim = 14, 7, 64
+    assert lib.qa_window_attn(fake, fake, fake, fake, 1, 1, fake, ctypes.byref(w)) == -1
+    w.n_kv_heads, w.scale = 14, float("nan")
+    assert lib.qa_window_attn(fake, fake, fake, fake, 1, 1, fake, ctypes.byref(w)) == -1
+    assert "scale" in qa.qa_last_error()
+
+
+def test_window_plan_matches_oracle(libqa):
+    import paged_kv_gqa_attention_gb300 as qa
+
+    rng = np.random.default_rng(7)
+    for _ in range(50):
+        counts = rng.integers(0, 1000, size=rng.integers(1, 12))
+        np.testing.assert_array_equal(qa.qa_window_plan(counts), oracle.window_plan(counts))
+        w = int(rng.integers(1, 200))
+        np.testing.assert_array_equal(qa.qa_window_plan(counts, w), oracle.window_plan(counts, w))
+    assert qa.qa_window_plan([117]).tolist() == [0, 104, 117]
+    with pytest.raises(qa.QAError):
+        qa.qa_window_plan([5, -1])
+
+
+def test_window_plan_capacity_error(libqa):
+    import paged_kv_gqa_attention_gb300 as qa
+
+    counts = np.array([300], np.int32)
+    cu = np.zeros(2, np.int32)
+    n = qa._lib.qa_window_plan(counts.ctypes.data_as(ctypes.c_void_p), 1, 0, cu.ctypes.data_as(ctypes.c_void_p), 2)
+    assert n == -1 and "capacity" in qa.qa_last_error()

@@ -1,0 +1,123 @@
+"""GPU parity of qa_decode_attn against the fp64 oracle, through the C ABI."""
+import numpy as np
+import pytest
+
+import oracle
+import workloads as wl
+from _util import assert_close, bits, f64, to_dev
+
+pytestmark = pytest.mark.gpu
+import torch  # noqa: E402
+
+import paged_kv_gqa_attention_gb300 as qa  # noqa: E402
+
+
+def run_decode(w, **kw):
+    q = to_dev(w["q"])
+    kp, vp = to_dev(w["k_pages"]), to_dev(w["v_pages"])
+    pt, sl = to_dev(w["page_table"]), to_dev(w["seq_lens"])
+    out = qa.qa_decode_attn(q, kp, vp, pt, sl, **kw)
+    torch.cuda.synchronize()
+    return out
+
+
+@pytest.mark.parametrize("lengths", [
+    (1, 15, 16, 17, 127, 128, 129),
+    (0, 5, 0, 33),
+    (2000,),
+    (16,) * 40,
+])
+def test_small_lengths(lengths):
+    maxp = max(1, -(-max(lengths) // 16))
+    w = wl.decode_workload(100 + len(lengths), lengths, num_pages=sum(-(-l // 16) for l in lengths) + 9, max_pages=maxp)
+    out = run_decode(w, debug_checks=True)
+    ref = oracle.decode(w["q"], w["k_pages"], w["v_pages"], w["page_table"], w["seq_lens"])
+    assert_close(f64(out), ref, f"lengths {lengths}")
+    for b, L in enumerate(lengths):
+        if L == 0:
+            assert (bits(out[b]) == 0).all()
+
+
+def test_many_requests_share_ctas():
+    rng = np.random.default_rng(9)
+    lengths = rng.integers(1, 70, size=600)
+    w = wl.decode_workload(77, lengths, num_pages=int(sum(-(-l // 16) for l in lengths)) + 3, max_pages=5)
+    out = run_decode(w, debug_checks=True)
+    ref = oracle.decode(w["q"], w["k_pages"], w["v_pages"], w["page_table"], w["seq_lens"])
+    assert_close(f64(out), ref, "600 short requests")
+
+
+def test_mha_group_one():
+    w = wl.decode_workload(31, (300, 45, 1), num_pages=40, max_pages=20, hq=8, hkv=8)
+    out = run_decode(w, debug_checks=True)
+    ref = oracle.decode(w["q"], w["k_pages"], w["v_pages"], w["page_table"], w["seq_lens"])
+    assert_close(f64(out), ref, "MHA 8/8")
+
+
+def test_single_key_returns_value_bit_exact():
+    w = wl.decode_workload(5, (1, 1, 1, 1), num_pages=8, max_pages=2)
+    out = run_decode(w)
+    for b in range(4):
+        v0 = w["v_pages"][w["page_table"][b, 0], 0]  # [Hkv, D]
+        np.testing.assert_array_equal(bits(out[b]), np.repeat(v0, 2, axis=0))
+
+
+def test_permuted_page_table_gives_identical_output():
+    w = wl.decode_workload(6, (300, 17, 999), num_pages=128, max_pages=63)
+    out_a = run_decode(w)
+    ck, cv = np.full_like(w["k_pages"], wl.BF16_NAN), np.full_like(w["v_pages"], wl.BF16_NAN)
+    table = np.full_like(w["page_table"], -1)
+    nxt = 0
+    for b, L in enumerate(w["seq_lens"]):
+        for p in range(-(-int(L) // 16)):
+            ck[nxt], cv[nxt] = w["k_pages"][w["page_table"][b, p]], w["v_pages"][w["page_table"][b, p]]
+            table[b, p] = nxt
+            nxt += 1
+    w2 = dict(w, k_pages=ck, v_pages=cv, page_table=table)
+    out_b = run_decode(w2)
+    np.testing.assert_array_equal(bits(out_a), bits(out_b))
+
+
+def test_workload_batched_decode_0p6b_full():
+    w = wl.decode_0p6b()
+    out = run_decode(w, debug_checks=True)
+    ref = oracle.decode(w["q"], w["k_pages"], w["v_pages"], w["page_table"], w["seq_lens"])
+    assert_close(f64(out), ref, "decode 0.6B workload")
+
+
+def test_workload_long_context_1p7b_sampled():
+    w = wl.decode_1p7b()
+    out = run_decode(w, debug_checks=True)
+    got = f64(out).reshape(-1, 128)
+    assert np.isfinite(got).all()
+    rng = np.random.default_rng(0)
+    rows = np.sort(rng.choice(got.shape[0], size=96, replace=False)).astype(np.int32)
+    ref = oracle.decode(w["q"], w["k_pages"], w["v_pages"], w["page_table"], w["seq_lens"], rows=rows)
+    assert_close(got[rows], ref, "decode 1.7B workload (96 sampled rows)")
+
+
+def test_tiny_workload_decode():
+    t = wl.tiny()
+    ekp, evp = oracle.page_write(t["k"], t["v"], t["cu_seqlens"], t["page_table"], t["k_pages"], t["v_pages"])
+    w = dict(q=t["decode_q"], k_pages=ekp, v_pages=evp, page_table=t["page_table"], seq_lens=t["seq_lens"])
+    out = run_decode(w, debug_checks=True)
+    ref = oracle.decode(t["decode_q"], ekp, evp, t["page_table"], t["seq_lens"])
+    assert_close(f64(out), ref, "tiny decode")
+
+
+def test_bad_page_id_is_reported_not_faulted():
+    w = wl.decode_workload(8, (40, 20), num_pages=8, max_pages=3)
+    w["page_table"] = w["page_table"].copy()
+    w["page_table"][0, 1] = 1 << 20  # outside the pool: must be skipped and reported
+    with pytest.raises(qa.QAError) as e:
+        run_decode(w, debug_checks=True)
+    assert e.value.status == -6 and "bad page" in str(e.value)
+    assert qa.qa_device_status() == 0  # cleared
+
+
+def test_workspace_too_small_is_rejected():
+    w = wl.decode_workload(8, (40,), num_pages=8, max_pages=3)
+    ws = torch.empty(64, dtype=torch.uint8, device="cuda")
+    with pytest.raises(qa.QAError) as e:
+        run_decode(w, workspace=ws)
+    assert e.value.status == -1 and "workspace" in str(e.value)

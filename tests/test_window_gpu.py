@@ -1,0 +1,68 @@
+"""GPU parity of qa_window_attn against the fp64 oracle, through the C ABI."""
+import numpy as np
+import pytest
+
+import oracle
+import workloads as wl
+from _util import assert_close, bits, f64, to_dev
+
+pytestmark = pytest.mark.gpu
+import torch  # noqa: E402
+
+import paged_kv_gqa_attention_gb300 as qa  # noqa: E402
+
+
+def run_window(w, cu, **kw):
+    q, k, v = to_dev(w["q"]), to_dev(w["k"]), to_dev(w["v"])
+    out = qa.qa_window_attn(q, k, v, to_dev(cu), **kw)
+    torch.cuda.synchronize()
+    return out
+
+
+@pytest.mark.parametrize("counts", [(1,), (103,), (104,), (105,), (13, 117, 250), (600, 7)])
+def test_small_windows(counts):
+    w = wl.window_workload(300 + sum(counts), counts)
+    cu = oracle.window_plan(counts)
+    np.testing.assert_array_equal(qa.qa_window_plan(counts), cu)
+    out = run_window(w, cu, debug_checks=True)
+    ref = oracle.window(w["q"], w["k"], w["v"], cu)
+    assert_close(f64(out), ref, f"counts {counts}")
+
+
+def test_head_dim_128_and_long_windows():
+    counts = (300, 129)
+    w = wl.window_workload(41, counts, h=4, d=128)
+    cu = oracle.window_plan(counts, 200)
+    out = run_window(w, cu, debug_checks=True)
+    ref = oracle.window(w["q"], w["k"], w["v"], cu)
+    assert_close(f64(out), ref, "D=128, windows of 200")
+
+
+def test_window_split_equals_separate_calls():
+    counts = (250,)
+    w = wl.window_workload(42, counts)
+    cu = oracle.window_plan(counts)
+    whole = bits(run_window(w, cu))
+    for i in range(len(cu) - 1):
+        a, b = cu[i], cu[i + 1]
+        part = dict(q=w["q"][a:b], k=w["k"][a:b], v=w["v"][a:b])
+        one = bits(run_window(part, np.array([0, b - a], np.int32)))
+        np.testing.assert_array_equal(whole[a:b], one)
+
+
+def test_workload_aut_window_sampled_and_mid_size_full():
+    w = wl.window_aut()
+    cu = qa.qa_window_plan(w["token_counts"])
+    np.testing.assert_array_equal(cu, oracle.window_plan(w["token_counts"]))
+    out = run_window(w, cu, debug_checks=True)
+    got = f64(out).reshape(-1, 64)
+    assert np.isfinite(got).all()
+    rng = np.random.default_rng(1)
+    rows = np.sort(rng.choice(got.shape[0], size=4096, replace=False)).astype(np.int32)
+    ref = oracle.window(w["q"], w["k"], w["v"], cu, rows=rows)
+    assert_close(got[rows], ref, "AuT window workload (4096 sampled rows)")
+    # a contiguous slice of whole windows, checked on every row
+    a, b = int(cu[100]), int(cu[140])
+    sub = dict(q=w["q"][a:b], k=w["k"][a:b], v=w["v"][a:b])
+    ref = oracle.window(sub["q"], sub["k"], sub["v"], cu[100:141] - a)
+    assert_close(f64(out)[a:b], ref, "AuT window workload (40 windows, all rows)")

@@ -9,9 +9,9 @@ def pytest_configure(config):
 
 
 def pytest_sessionstart(session):
-    from paged_kv_gqa_attention_gb300 import _build
+    import __graft_entry__
 
-    _build.build()
+    __graft_entry__._builder().build()
     import oracle
 
     oracle.build()

@@ -18,9 +18,9 @@ HEADER = os.path.join(ROOT, "include", "qa.h")
 
 @pytest.fixture(scope="session")
 def libqa():
-    from paged_kv_gqa_attention_gb300 import _build
+    import __graft_entry__
 
-    path = _build.build()
+    path = __graft_entry__._builder().build()
     return ctypes.CDLL(path)
 
 
@@ -31,8 +31,9 @@ def declared_functions():
 
 
 def test_exports_exactly_the_declared_symbols(libqa):
-    from paged_kv_gqa_attention_gb300 import _build
+    import __graft_entry__
 
+    _build = __graft_entry__._builder()
     out = subprocess.run(["nm", "-D", "--defined-only", _build.LIB], capture_output=True, text=True, check=True).stdout
     exported = sorted(line.split()[-1] for line in out.splitlines() if line.strip())
     declared = declared_functions()
@@ -43,7 +44,9 @@ def test_exports_exactly_the_declared_symbols(libqa):
 
 
 def test_header_is_strict_c99(libqa, tmp_path):
-    from paged_kv_gqa_attention_gb300 import _build
+    import __graft_entry__
+
+    _build = __graft_entry__._builder()
 
     c = tmp_path / "abi_c.c"
     c.write_text(r'''

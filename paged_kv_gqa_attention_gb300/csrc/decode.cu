@@ -41,6 +41,9 @@ constexpr int kD = 128;
 constexpr int kPS = 16;
 constexpr int kStages = 3;
 constexpr int kMaxHkv = 8;
+// Merge record of one query head in shared memory: m, l, two pad words (so
+// the accumulator starts on a 16-byte boundary), then acc[kD].
+constexpr int kRec = 4 + kD;
 
 struct DecodeArgs {
     const uint16_t *q;
@@ -86,7 +89,7 @@ __host__ __device__ inline SmemLayout smem_layout(int hkv, int batch, int group)
     o += (batch + 1) * 4;
     o = (o + 15) & ~15u;
     s.off_merge = o;
-    o += hkv * group * (2 + kD) * 4;
+    o += hkv * group * kRec * 4;
     s.total = o;
     return s;
 }
@@ -183,7 +186,7 @@ __global__ void __launch_bounds__((2 * kMaxHkv + 1) * 32, 1) decode_splitk_kerne
 
     // ---------------- consumer warps
     const int g = warp >> 1, half = warp & 1;
-    float *merge = reinterpret_cast<float *>(smem + L.off_merge) + g * GROUP * (2 + kD);
+    float *merge = reinterpret_cast<float *>(smem + L.off_merge) + g * GROUP * kRec;
     int it = 0;
     for (int b = b0; b < a.batch && prefix[b] < hi; ++b) {
         const int p0 = prefix[b], p1 = prefix[b + 1];
@@ -267,12 +270,12 @@ __global__ void __launch_bounds__((2 * kMaxHkv + 1) * 32, 1) decode_splitk_kerne
         if (half == 1) {
 #pragma unroll
             for (int i = 0; i < GROUP; ++i) {
-                float *mr = merge + i * (2 + kD);
+                float *mr = merge + i * kRec;
                 if (lane == 0) {
                     mr[0] = m[i];
                     mr[1] = l[i];
                 }
-                *reinterpret_cast<float4 *>(mr + 2 + 4 * lane) = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+                *reinterpret_cast<float4 *>(mr + 4 + 4 * lane) = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
             }
         }
         named_barrier(1 + g, 64);
@@ -281,9 +284,9 @@ __global__ void __launch_bounds__((2 * kMaxHkv + 1) * 32, 1) decode_splitk_kerne
             const int slot = blockIdx.x + b;
 #pragma unroll
             for (int i = 0; i < GROUP; ++i) {
-                const float *mr = merge + i * (2 + kD);
+                const float *mr = merge + i * kRec;
                 const float m1 = mr[0], l1 = mr[1];
-                const float4 a1 = *reinterpret_cast<const float4 *>(mr + 2 + 4 * lane);
+                const float4 a1 = *reinterpret_cast<const float4 *>(mr + 4 + 4 * lane);
                 const float mm = fmaxf(m[i], m1);
                 float ls = 0.f, o[4] = {0.f, 0.f, 0.f, 0.f};
                 if (mm != -INFINITY) {

@@ -67,7 +67,7 @@ def decode_bytes(lengths, hq=16, hkv=8, d=128):
 
 
 def prefill_flops(lengths, hq=16, d=128):
-    return int(sum(4 * hq * d * (L * (L + 1) // 2) for L in lengths))
+    return int(sum(4 * hq * d * (int(L) * (int(L) + 1) // 2) for L in lengths))
 
 
 def prefill_bytes(total, hq=16, hkv=8, d=128):

@@ -1,0 +1,269 @@
+// Tensor-core flash attention over packed segments (tcgen05 + TMEM + TMA).
+//
+// One CTA of four warps computes 128-row query tiles of one query head h of
+// one segment (a prefill request or an encoder window).  Per key tile of 128
+// rows:
+//   1. TMA brings the K and V tiles ([128 rows][D] bf16, 128B-swizzled,
+//      64-dim sub-tiles) into shared memory; the Q tile arrived once per
+//      query tile.
+//   2. One thread issues S = Q K^T (M = 128, N = 128, K = D in steps of 16)
+//      into TMEM columns [0, 128) and commits to an mbarrier.
+//   3. Each thread owns one query row (= TMEM lane): it reads its 128 scores
+//      with tcgen05.ld, masks keys outside the segment (and, causal, keys
+//      after the row), runs the online softmax in fp32 with base-2
+//      exponentials, and writes P as bf16 into a 128B-swizzled K-major tile.
+//   4. When the running max of a row moved, the thread rescales its row of
+//      the fp32 output accumulator O (TMEM columns [128, 128 + D)) by
+//      alpha = 2^(m_old - m_new) with tcgen05.ld / tcgen05.st.
+//   5. One thread issues O += P V (M = 128, N = 64 per MMA, K = 128 keys in
+//      steps of 16, V read MN-major), accumulating in TMEM.
+// After the last key tile each row of O is read back, divided by its softmax
+// sum, rounded to bf16 and stored.
+//
+// Masks.  Window (bidirectional): key j is visible to row i iff both lie in
+// the same segment.  Causal prefill: additionally j <= i.  Rows past the
+// segment end are computed on whatever the tile holds and never stored; keys
+// past it get probability 0, and their V rows (the next segment's, or TMA's
+// zero fill past the tensor) are finite, so they contribute exactly 0.
+#pragma once
+
+#include <cuda.h>
+#include <stdint.h>
+
+#include "common.cuh"
+#include "tc.cuh"
+
+namespace qa {
+
+struct AttnTcArgs {
+    const int32_t *cu;  // [n_seg + 1]
+    uint16_t *out;      // [T][hq][D]
+    int n_seg, total, hq;
+    float scale_log2;
+};
+
+template <int D>
+struct AttnTcLayout {
+    static constexpr int kSub = D / 64;  // 64-dim sub-tiles per row block
+    static constexpr uint32_t kQ = 0;
+    static constexpr uint32_t kK = kQ + kSub * tc::kSubTileBytes;
+    static constexpr uint32_t kV = kK + kSub * tc::kSubTileBytes;
+    static constexpr uint32_t kP = kV + kSub * tc::kSubTileBytes;  // 128 keys = 2 sub-tiles
+    static constexpr uint32_t kBar = kP + 2 * tc::kSubTileBytes;  // 4 mbarriers
+    static constexpr uint32_t kTmemSlot = kBar + 32;
+    static constexpr uint32_t kBytes = kTmemSlot + 16;
+    static constexpr uint32_t kSmem = kBytes + 1024;  // slack for 1024-byte alignment
+    static constexpr uint32_t kTmemCols = 256;
+    static constexpr uint32_t kColS = 0;
+    static constexpr uint32_t kColO = 128;
+};
+
+// CAUSAL: grid (q-tiles, hq, segments), one query tile per CTA.
+// !CAUSAL: grid (segments, hq), every query tile of the segment in turn.
+template <int D, int GROUP, bool CAUSAL>
+__global__ void __launch_bounds__(128, 1)
+    attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, const AttnTcArgs a, unsigned int *status) {
+    using L = AttnTcLayout<D>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t sb = (raw + 1023u) & ~1023u;
+    uint8_t *smem = smem_raw + (sb - raw);
+    const int tid = threadIdx.x, warp = tid >> 5;
+
+    const int h = blockIdx.y;
+    const int g = h / GROUP;
+    const int seg = CAUSAL ? blockIdx.z : blockIdx.x;
+    const int s0 = a.cu[seg], s1 = a.cu[seg + 1];
+    if (!(0 <= s0 && s0 <= s1 && s1 <= a.total) || a.cu[a.n_seg] != a.total) {
+        if (tid == 0) atomicOr(status, QA_DEVICE_BAD_SEGMENTS);
+        return;
+    }
+    const int n = s1 - s0;
+    const int n_tiles = (n + 127) / 128;
+    int qt0, qt1;
+    if (CAUSAL) {
+        qt0 = blockIdx.x;
+        qt1 = qt0 + 1;
+        if (qt0 >= n_tiles) return;
+    } else {
+        qt0 = 0;
+        qt1 = n_tiles;
+        if (n_tiles == 0) return;
+    }
+
+    const uint32_t bar_q = sb + L::kBar, bar_kv = bar_q + 8, bar_s = bar_q + 16, bar_o = bar_q + 24;
+    if (tid == 0) {
+        mbar_init(bar_q, 1);
+        mbar_init(bar_kv, 1);
+        mbar_init(bar_s, 1);
+        mbar_init(bar_o, 1);
+        fence_mbar_init();
+        tc::prefetch_tmap(&tm_q);
+        tc::prefetch_tmap(&tm_k);
+        tc::prefetch_tmap(&tm_v);
+    }
+    if (warp == 0) tc::tmem_alloc(sb + L::kTmemSlot, L::kTmemCols);
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + L::kTmemSlot);
+    const uint32_t t_row = tmem + ((uint32_t)(warp * 32) << 16);  // this warp's TMEM lanes
+
+    constexpr uint32_t idesc_s = tc::idesc_bf16(128, 128, false);
+    constexpr uint32_t idesc_o = tc::idesc_bf16(128, 64, true);
+    uint32_t ph_q = 0, ph_kv = 0, ph_s = 0, ph_o = 0;
+    const int r = tid;  // query row in the tile = TMEM lane
+    const uint32_t p_row = sb + L::kP + r * 128;
+    const uint32_t sw = (uint32_t)(r & 7);
+
+    for (int qt = qt0; qt < qt1; ++qt) {
+        const int q0 = s0 + qt * 128;
+        const int qi = q0 + r;
+        if (tid == 0) {
+            mbar_arrive_expect_tx(bar_q, L::kSub * tc::kSubTileBytes);
+#pragma unroll
+            for (int sd = 0; sd < L::kSub; ++sd)
+                tc::tma_load_3d(sb + L::kQ + sd * tc::kSubTileBytes, &tm_q, sd * 64, h, q0, bar_q);
+        }
+        const int kt_end = CAUSAL ? qt + 1 : n_tiles;
+        float m = -INFINITY, l = 0.f;
+
+        for (int kt = 0; kt < kt_end; ++kt) {
+            const int k0 = s0 + kt * 128;
+            if (tid == 0) {
+                mbar_arrive_expect_tx(bar_kv, 2 * L::kSub * tc::kSubTileBytes);
+#pragma unroll
+                for (int sd = 0; sd < L::kSub; ++sd) {
+                    tc::tma_load_3d(sb + L::kK + sd * tc::kSubTileBytes, &tm_k, sd * 64, g, k0, bar_kv);
+                    tc::tma_load_3d(sb + L::kV + sd * tc::kSubTileBytes, &tm_v, sd * 64, g, k0, bar_kv);
+                }
+                if (kt == 0) mbar_wait(bar_q, ph_q, status);
+                mbar_wait(bar_kv, ph_kv, status);
+                tc::fence_after();
+                // S = Q K^T over D in steps of 16 (32 bytes inside a 128-byte row)
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * tc::kSubTileBytes + (kk & 3) * 32;
+                    tc::mma_bf16(tmem + L::kColS, tc::sw128_desc(sb + L::kQ + off), tc::sw128_desc(sb + L::kK + off),
+                                 idesc_s, kk > 0);
+                }
+                tc::mma_commit(bar_s);
+            }
+            if (kt == 0) ph_q ^= 1;
+            ph_kv ^= 1;
+            mbar_wait(bar_s, ph_s, status);
+            ph_s ^= 1;
+            tc::fence_after();
+
+            // ---- softmax over this key tile (row r)
+            const bool full_tile = (k0 + 128 <= s1) && (!CAUSAL || k0 + 127 <= q0);
+            float mx = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                float sv[32];
+                tc::tmem_ld32(t_row + L::kColS + c * 32, sv);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const int key = k0 + c * 32 + j;
+                    const bool ok = full_tile || (key < s1 && (!CAUSAL || key <= qi));
+                    if (ok) mx = fmaxf(mx, sv[j]);
+                }
+            }
+            const float m_new = fmaxf(m, mx * a.scale_log2);
+            const float alpha = m == -INFINITY ? 0.f : exp2_approx(m - m_new);
+            float psum = 0.f;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                float sv[32];
+                tc::tmem_ld32(t_row + L::kColS + c * 32, sv);
+                uint32_t pk[16];
+#pragma unroll
+                for (int j = 0; j < 32; j += 2) {
+                    const int key = k0 + c * 32 + j;
+                    const bool ok0 = full_tile || (key < s1 && (!CAUSAL || key <= qi));
+                    const bool ok1 = full_tile || (key + 1 < s1 && (!CAUSAL || key + 1 <= qi));
+                    const float p0 = ok0 ? exp2_approx(sv[j] * a.scale_log2 - m_new) : 0.f;
+                    const float p1 = ok1 ? exp2_approx(sv[j + 1] * a.scale_log2 - m_new) : 0.f;
+                    psum += p0 + p1;
+                    pk[j >> 1] = pack_bf16x2(p0, p1);
+                }
+                // 32 keys = 4 chunks of 16 bytes, sub-tile c / 2, chunks (c % 2) * 4 + u
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const uint32_t chunk = (uint32_t)((c & 1) * 4 + u);
+                    const uint32_t addr = p_row + (uint32_t)(c >> 1) * tc::kSubTileBytes + ((chunk ^ sw) << 4);
+                    tc::st_shared_v4(addr, pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+                }
+            }
+            l = l * alpha + psum;
+            m = m_new;
+            // rescale this row of the output accumulator (warp-collective)
+            if (kt > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    float ov[32];
+                    tc::tmem_ld32(t_row + L::kColO + c * 32, ov);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) ov[j] *= alpha;
+                    tc::tmem_st32(t_row + L::kColO + c * 32, ov);
+                }
+            }
+            tc::fence_proxy_async_smem();
+            tc::fence_before();
+            __syncthreads();
+
+            if (tid == 0) {
+                tc::fence_after();
+                // O_tile = P V: K = 128 keys in steps of 16 (two 8-row groups of
+                // V = 2048 bytes), N = 64 dims per MMA (one V sub-tile each)
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t a_off = (kk >> 2) * tc::kSubTileBytes + (kk & 3) * 32;
+#pragma unroll
+                    for (int sd = 0; sd < L::kSub; ++sd) {
+                        tc::mma_bf16(tmem + L::kColO + sd * 64, tc::sw128_desc(sb + L::kP + a_off),
+                                     tc::sw128_desc(sb + L::kV + sd * tc::kSubTileBytes + kk * 2048), idesc_o,
+                                     (kt > 0 || kk > 0) ? 1u : 0u);
+                    }
+                }
+                tc::mma_commit(bar_o);
+            }
+            mbar_wait(bar_o, ph_o, status);
+            ph_o ^= 1;
+            tc::fence_after();
+            __syncthreads();  // K, V, P and the S columns are free again
+        }
+
+        // epilogue: O / l -> bf16 (warp-collective TMEM reads, masked stores)
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        uint4 *dst = reinterpret_cast<uint4 *>(a.out + ((size_t)qi * a.hq + h) * D);
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+            float ov[32];
+            tc::tmem_ld32(t_row + L::kColO + c * 32, ov);
+            if (qi < s1) {
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    uint4 w;
+                    w.x = pack_bf16x2(ov[8 * u + 0] * inv, ov[8 * u + 1] * inv);
+                    w.y = pack_bf16x2(ov[8 * u + 2] * inv, ov[8 * u + 3] * inv);
+                    w.z = pack_bf16x2(ov[8 * u + 4] * inv, ov[8 * u + 5] * inv);
+                    w.w = pack_bf16x2(ov[8 * u + 6] * inv, ov[8 * u + 7] * inv);
+                    dst[c * 4 + u] = w;
+                }
+            }
+        }
+        tc::fence_before();
+        __syncthreads();  // O columns are read before the next query tile's MMAs
+    }
+
+    tc::fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc::fence_after();
+        tc::tmem_dealloc(tmem, L::kTmemCols);
+    }
+}
+
+}  // namespace qa

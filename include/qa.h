@@ -141,6 +141,31 @@ qa_status qa_decode_attn(const void *q, const void *k_pages, const void *v_pages
                          const int32_t *page_table, const int32_t *seq_lens, int batch,
                          void *out, const qa_attn_params *params);
 
+/* Paged GQA decode for callers that cannot allocate device memory.
+ *
+ * Not part of the method described by the Qwen3-ASR pages (they have no
+ * counterpart): a convenience for callers that cannot call cudaMalloc -- for
+ * example a plugin whose host application owns every device allocation, a
+ * real-time path that may not wait on or fail in an allocator, or plain C
+ * code without an allocator of its own.  Same arguments, layouts and result
+ * as qa_decode_attn, but params->workspace is ignored: the split-K scratch
+ * lives in a fixed 4 MiB array inside the library, reserved on every GPU that
+ * loads it until the process exits.  Nothing is allocated.
+ *
+ *   - A batch whose scratch would exceed 4 MiB is rejected with
+ *     QA_STATUS_INVALID_PARAMS and a message giving the sizes (with 16 query
+ *     heads and head_dim 128 about 350 requests fit on a 152-SM GPU).
+ *   - All calls on a device share the array: calls whose kernels overlap on
+ *     the GPU (unordered streams or host threads) race and give wrong
+ *     results.  Calls ordered on one stream are safe.  The array keeps the
+ *     last call's contents; nothing in it needs clearing between calls.
+ *   - The first call made with a given device current looks up the array's
+ *     device address and caches it; make that first call before any CUDA
+ *     stream capture begins. */
+qa_status qa_decode_attn_noalloc(const void *q, const void *k_pages, const void *v_pages,
+                                 const int32_t *page_table, const int32_t *seq_lens, int batch,
+                                 void *out, const qa_attn_params *params);
+
 /* Ragged causal prefill with the KV page write.
  *
  *   q          bf16 [total_tokens][n_q_heads][head_dim], requests packed

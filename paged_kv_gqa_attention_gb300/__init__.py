@@ -22,7 +22,7 @@ import numpy as np
 __all__ = [
     "QA_ABI_VERSION", "QAError", "lib_path", "qa_version", "qa_last_error", "qa_attn_default_params",
     "qa_decode_workspace_size", "qa_decode_attn", "qa_prefill_attn", "qa_window_attn", "qa_window_plan",
-    "qa_device_status", "DEVICE_STATUS_BITS",
+    "qa_device_status", "DEVICE_STATUS_BITS", "qa_decode_attn_noalloc",
 ]
 
 QA_ABI_VERSION = 1
@@ -69,6 +69,8 @@ def _load():
     lib.qa_decode_workspace_size.argtypes = [I, I, PP]
     lib.qa_decode_attn.restype = I
     lib.qa_decode_attn.argtypes = [P, P, P, P, P, I, P, PP]
+    lib.qa_decode_attn_noalloc.restype = I
+    lib.qa_decode_attn_noalloc.argtypes = [P, P, P, P, P, I, P, PP]
     lib.qa_prefill_attn.restype = I
     lib.qa_prefill_attn.argtypes = [P, P, P, P, I, I, P, P, P, P, PP]
     lib.qa_window_attn.restype = I
@@ -182,6 +184,34 @@ def qa_decode_attn(q, k_pages, v_pages, page_table, seq_lens, out=None, *, works
                              _dev(page_table, "page_table", torch.int32, 2), _dev(seq_lens, "seq_lens", torch.int32, 1),
                              B, _dev(out, "out", torch.bfloat16, 3), ctypes.byref(p))
     _check("qa_decode_attn", st)
+    return out
+
+
+def qa_decode_attn_noalloc(q, k_pages, v_pages, page_table, seq_lens, out=None, *, scale=0.0, stream=None,
+                           debug_checks=False):
+    """qa_decode_attn without a workspace, for callers that cannot allocate
+    device memory: the split-K scratch is a fixed 4 MiB array inside the
+    library, shared by every call on the device (calls that overlap on the
+    GPU race on it; calls ordered on one stream are fine).  Batches whose
+    scratch would not fit are rejected.  The first call on each device looks
+    up the array's address, so make it before any stream capture.  With
+    out=None the output tensor is allocated here by torch; pass `out` to keep
+    the call allocation-free."""
+    torch = _torch()
+    B, Hq, D = q.shape
+    P, PS, Hkv, D2 = k_pages.shape
+    if D2 != D or tuple(v_pages.shape) != tuple(k_pages.shape) or page_table.dim() != 2 or page_table.shape[0] != B:
+        raise ValueError("inconsistent decode shapes")
+    if out is None:
+        out = torch.empty_like(q)
+    p = _params(n_q_heads=Hq, n_kv_heads=Hkv, head_dim=D, page_size=PS, num_pages=P,
+                max_pages_per_seq=page_table.shape[1], scale=scale, stream=stream, debug_checks=debug_checks)
+    st = _lib.qa_decode_attn_noalloc(_dev(q, "q", torch.bfloat16, 3), _dev(k_pages, "k_pages", torch.bfloat16, 4),
+                                     _dev(v_pages, "v_pages", torch.bfloat16, 4),
+                                     _dev(page_table, "page_table", torch.int32, 2),
+                                     _dev(seq_lens, "seq_lens", torch.int32, 1), B,
+                                     _dev(out, "out", torch.bfloat16, 3), ctypes.byref(p))
+    _check("qa_decode_attn_noalloc", st)
     return out
 
 

@@ -267,3 +267,9 @@ QA_API const char *qa_version(void) {
     snprintf(v, sizeof v, "qa-attn 0.1.0 abi %d", QA_ABI_VERSION);
     return v;
 }
+
+namespace qa {
+// Lets entry points defined in other translation units report through the
+// same thread-local qa_last_error() slot.
+void set_last_error(const char *msg) { snprintf(t_last_error, sizeof t_last_error, "%s", msg); }
+}  // namespace qa

@@ -38,4 +38,8 @@ cudaError_t launch_window(const void *q, const void *k, const void *v, const int
                           float scale, cudaStream_t stream);
 unsigned int status_read_clear_window(cudaStream_t stream, cudaError_t *err);
 
+// ---- qa_api.cu
+// Writes the thread-local qa_last_error() message.
+void set_last_error(const char *msg);
+
 }  // namespace qa

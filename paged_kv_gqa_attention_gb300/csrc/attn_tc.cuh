@@ -11,12 +11,17 @@
 //   3. Each thread owns one query row (= TMEM lane): it reads its 128 scores
 //      with tcgen05.ld, masks keys outside the segment (and, causal, keys
 //      after the row), runs the online softmax in fp32 with base-2
-//      exponentials, and writes P as bf16 into a 128B-swizzled K-major tile.
+//      exponentials, and writes P as two bf16 terms, P_hi = bf16(p) and
+//      P_lo = bf16(p - P_hi), into 128B-swizzled K-major tiles.  The pair
+//      carries p to about 16 significant bits, so the P V product keeps the
+//      softmax probabilities at (nearly) fp32 precision, as the precision
+//      policy asks (score and softmax intermediates in float32); P_lo reuses
+//      the K tile's shared memory, which is dead once S is computed.
 //   4. When the running max of a row moved, the thread rescales its row of
 //      the fp32 output accumulator O (TMEM columns [128, 128 + D)) by
 //      alpha = 2^(m_old - m_new) with tcgen05.ld / tcgen05.st.
-//   5. One thread issues O += P V (M = 128, N = 64 per MMA, K = 128 keys in
-//      steps of 16, V read MN-major), accumulating in TMEM.
+//   5. One thread issues O += P_hi V + P_lo V (M = 128, N = 64 per MMA,
+//      K = 128 keys in steps of 16, V read MN-major), accumulating in TMEM.
 // After the last key tile each row of O is read back, divided by its softmax
 // sum, rounded to bf16 and stored.
 //
@@ -46,9 +51,11 @@ template <int D>
 struct AttnTcLayout {
     static constexpr int kSub = D / 64;  // 64-dim sub-tiles per row block
     static constexpr uint32_t kQ = 0;
-    static constexpr uint32_t kK = kQ + kSub * tc::kSubTileBytes;
-    static constexpr uint32_t kV = kK + kSub * tc::kSubTileBytes;
-    static constexpr uint32_t kP = kV + kSub * tc::kSubTileBytes;  // 128 keys = 2 sub-tiles
+    static constexpr uint32_t kK = kQ + kSub * tc::kSubTileBytes;  // K tile, then P_lo (2 sub-tiles)
+    static constexpr uint32_t kKBytes = (kSub > 2 ? kSub : 2) * tc::kSubTileBytes;
+    static constexpr uint32_t kPlo = kK;
+    static constexpr uint32_t kV = kK + kKBytes;
+    static constexpr uint32_t kP = kV + kSub * tc::kSubTileBytes;  // P_hi: 128 keys = 2 sub-tiles
     static constexpr uint32_t kBar = kP + 2 * tc::kSubTileBytes;  // 4 mbarriers
     static constexpr uint32_t kTmemSlot = kBar + 32;
     static constexpr uint32_t kBytes = kTmemSlot + 16;
@@ -115,6 +122,7 @@ __global__ void __launch_bounds__(128, 1)
     uint32_t ph_q = 0, ph_kv = 0, ph_s = 0, ph_o = 0;
     const int r = tid;  // query row in the tile = TMEM lane
     const uint32_t p_row = sb + L::kP + r * 128;
+    const uint32_t plo_row = sb + L::kPlo + r * 128;
     const uint32_t sw = (uint32_t)(r & 7);
 
     for (int qt = qt0; qt < qt1; ++qt) {
@@ -177,7 +185,7 @@ __global__ void __launch_bounds__(128, 1)
             for (int c = 0; c < 4; ++c) {
                 float sv[32];
                 tc::tmem_ld32(t_row + L::kColS + c * 32, sv);
-                uint32_t pk[16];
+                uint32_t pk[16], pl[16];
 #pragma unroll
                 for (int j = 0; j < 32; j += 2) {
                     const int key = k0 + c * 32 + j;
@@ -186,14 +194,17 @@ __global__ void __launch_bounds__(128, 1)
                     const float p0 = ok0 ? exp2_approx(sv[j] * a.scale_log2 - m_new) : 0.f;
                     const float p1 = ok1 ? exp2_approx(sv[j + 1] * a.scale_log2 - m_new) : 0.f;
                     psum += p0 + p1;
-                    pk[j >> 1] = pack_bf16x2(p0, p1);
+                    const uint32_t hi = pack_bf16x2(p0, p1);
+                    pk[j >> 1] = hi;
+                    pl[j >> 1] = pack_bf16x2(p0 - bf16lo(hi), p1 - bf16hi(hi));
                 }
                 // 32 keys = 4 chunks of 16 bytes, sub-tile c / 2, chunks (c % 2) * 4 + u
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
                     const uint32_t chunk = (uint32_t)((c & 1) * 4 + u);
-                    const uint32_t addr = p_row + (uint32_t)(c >> 1) * tc::kSubTileBytes + ((chunk ^ sw) << 4);
-                    tc::st_shared_v4(addr, pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+                    const uint32_t off = (uint32_t)(c >> 1) * tc::kSubTileBytes + ((chunk ^ sw) << 4);
+                    tc::st_shared_v4(p_row + off, pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+                    tc::st_shared_v4(plo_row + off, pl[4 * u], pl[4 * u + 1], pl[4 * u + 2], pl[4 * u + 3]);
                 }
             }
             l = l * alpha + psum;
@@ -222,9 +233,11 @@ __global__ void __launch_bounds__(128, 1)
                     const uint32_t a_off = (kk >> 2) * tc::kSubTileBytes + (kk & 3) * 32;
 #pragma unroll
                     for (int sd = 0; sd < L::kSub; ++sd) {
-                        tc::mma_bf16(tmem + L::kColO + sd * 64, tc::sw128_desc(sb + L::kP + a_off),
-                                     tc::sw128_desc(sb + L::kV + sd * tc::kSubTileBytes + kk * 2048), idesc_o,
+                        const uint64_t vdesc = tc::sw128_desc(sb + L::kV + sd * tc::kSubTileBytes + kk * 2048);
+                        tc::mma_bf16(tmem + L::kColO + sd * 64, tc::sw128_desc(sb + L::kP + a_off), vdesc, idesc_o,
                                      (kt > 0 || kk > 0) ? 1u : 0u);
+                        tc::mma_bf16(tmem + L::kColO + sd * 64, tc::sw128_desc(sb + L::kPlo + a_off), vdesc, idesc_o,
+                                     1u);
                     }
                 }
                 tc::mma_commit(bar_o);

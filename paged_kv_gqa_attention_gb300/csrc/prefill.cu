@@ -7,13 +7,15 @@
 //
 // Attention: row i of request r attends over rows j <= i of the same request
 // (same section: attend over [0, n_past + T)), GQA group h / 2, from the
-// packed k and v.
+// packed k and v, on the tensor cores (attn_tc.cuh): one CTA per (128-row
+// query tile, query head, request), causal key tiles 0..tile.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
 #include "common.cuh"
 #include "qa_internal.h"
-#include "row_attn.cuh"
+#include "attn_tc.cuh"
+#include "tmap.h"
 
 namespace qa {
 namespace {
@@ -88,26 +90,36 @@ cudaError_t launch_prefill(const void *q, const void *k, const void *v, const in
                            int batch, int total_tokens, void *out, const qa_attn_params &p,
                            float scale, cudaStream_t stream) {
     if (total_tokens == 0) return cudaSuccess;
-    RowAttnArgs a;
-    a.q = static_cast<const uint16_t *>(q);
-    a.k = static_cast<const uint16_t *>(k);
-    a.v = static_cast<const uint16_t *>(v);
+    if (batch > 65535) return cudaErrorInvalidValue;
+    CUtensorMap tq, tk, tv;
+    if (!make_rows_tmap(&tq, q, p.head_dim, p.n_q_heads, total_tokens) ||
+        !make_rows_tmap(&tk, k, p.head_dim, p.n_kv_heads, total_tokens) ||
+        !make_rows_tmap(&tv, v, p.head_dim, p.n_kv_heads, total_tokens))
+        return cudaErrorInvalidValue;
+    AttnTcArgs a;
     a.cu = cu_seqlens;
     a.out = static_cast<uint16_t *>(out);
     a.n_seg = batch;
     a.total = total_tokens;
-    a.hkv = p.n_kv_heads;
+    a.hq = p.n_q_heads;
     a.scale_log2 = scale * kLog2e;
     unsigned int *status = nullptr;
     cudaError_t e = cudaGetSymbolAddress(reinterpret_cast<void **>(&status), g_status);
     if (e != cudaSuccess) return e;
-    const long long warps = (long long)total_tokens * a.hkv;
-    const int blocks = (int)((warps + 7) / 8);
-    const int group = p.n_q_heads / p.n_kv_heads;
-    if (group == 2)
-        row_attn_kernel<128, 2, true><<<blocks, 256, 0, stream>>>(a, status);
-    else
-        row_attn_kernel<128, 1, true><<<blocks, 256, 0, stream>>>(a, status);
+    // a request holds at most max_pages_per_seq * page_size rows
+    const long long max_len = (long long)p.max_pages_per_seq * p.page_size;
+    const int qtiles = (int)((max_len + 127) / 128);
+    const dim3 grid(qtiles, p.n_q_heads, batch);
+    constexpr uint32_t smem = AttnTcLayout<128>::kSmem;
+    if (p.n_q_heads == 2 * p.n_kv_heads) {
+        e = cudaFuncSetAttribute(attn_tc_kernel<128, 2, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        attn_tc_kernel<128, 2, true><<<grid, 128, smem, stream>>>(tq, tk, tv, a, status);
+    } else {
+        e = cudaFuncSetAttribute(attn_tc_kernel<128, 1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        attn_tc_kernel<128, 1, true><<<grid, 128, smem, stream>>>(tq, tk, tv, a, status);
+    }
     return cudaGetLastError();
 }
 

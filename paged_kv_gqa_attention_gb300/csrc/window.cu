@@ -5,13 +5,16 @@
 // bidirectional MHA scaled by 1/sqrt(head_dim).  M* "Speech recognition:
 // Whisper and Qwen3-ASR", "Graph": one packed forward per batch with one
 // segment per window of every request.  Row t of window w attends over every
-// row of w and nothing else.
+// row of w and nothing else.  Runs on the tensor cores (attn_tc.cuh): one CTA
+// per (window, head); a 104-token window is one 128-row tile, longer windows
+// loop over query and key tiles.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
 #include "common.cuh"
 #include "qa_internal.h"
-#include "row_attn.cuh"
+#include "attn_tc.cuh"
+#include "tmap.h"
 
 namespace qa {
 namespace {
@@ -22,25 +25,34 @@ cudaError_t launch_window(const void *q, const void *k, const void *v, const int
                           int n_windows, int total_tokens, void *out, const qa_attn_params &p,
                           float scale, cudaStream_t stream) {
     if (total_tokens == 0) return cudaSuccess;
-    RowAttnArgs a;
-    a.q = static_cast<const uint16_t *>(q);
-    a.k = static_cast<const uint16_t *>(k);
-    a.v = static_cast<const uint16_t *>(v);
+    if (p.n_q_heads > 65535) return cudaErrorInvalidValue;
+    CUtensorMap tq, tk, tv;
+    if (!make_rows_tmap(&tq, q, p.head_dim, p.n_q_heads, total_tokens) ||
+        !make_rows_tmap(&tk, k, p.head_dim, p.n_kv_heads, total_tokens) ||
+        !make_rows_tmap(&tv, v, p.head_dim, p.n_kv_heads, total_tokens))
+        return cudaErrorInvalidValue;
+    AttnTcArgs a;
     a.cu = cu_windows;
     a.out = static_cast<uint16_t *>(out);
     a.n_seg = n_windows;
     a.total = total_tokens;
-    a.hkv = p.n_kv_heads;
+    a.hq = p.n_q_heads;
     a.scale_log2 = scale * kLog2e;
     unsigned int *status = nullptr;
     cudaError_t e = cudaGetSymbolAddress(reinterpret_cast<void **>(&status), g_status);
     if (e != cudaSuccess) return e;
-    const long long warps = (long long)total_tokens * a.hkv;
-    const int blocks = (int)((warps + 7) / 8);
-    if (p.head_dim == 64)
-        row_attn_kernel<64, 1, false><<<blocks, 256, 0, stream>>>(a, status);
-    else
-        row_attn_kernel<128, 1, false><<<blocks, 256, 0, stream>>>(a, status);
+    const dim3 grid(n_windows, p.n_q_heads);
+    if (p.head_dim == 64) {
+        constexpr uint32_t smem = AttnTcLayout<64>::kSmem;
+        e = cudaFuncSetAttribute(attn_tc_kernel<64, 1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        attn_tc_kernel<64, 1, false><<<grid, 128, smem, stream>>>(tq, tk, tv, a, status);
+    } else {
+        constexpr uint32_t smem = AttnTcLayout<128>::kSmem;
+        e = cudaFuncSetAttribute(attn_tc_kernel<128, 1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        attn_tc_kernel<128, 1, false><<<grid, 128, smem, stream>>>(tq, tk, tv, a, status);
+    }
     return cudaGetLastError();
 }
 

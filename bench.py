@@ -5,7 +5,8 @@
 Prints ONE JSON line (rank 0).  The headline workload is the batched decode
 of the 0.6B Thinker shape: 32 requests, GQA 16/8, head_dim 128, contexts
 ~ U[200, 2000], 16-token pages scattered over a 4096-page pool.  One step is
-one qa_decode_attn call over that batch (split-K kernel + combine kernel).
+one qa_decode_attn call over that batch (one split-K kernel launch that also
+merges the splits).
 The metric is the decode's algorithmic HBM bandwidth: K+V bytes of every
 cached position read plus q and out, 4096 B per position + 8192 B per
 request, divided by the device time of the call.
@@ -270,7 +271,7 @@ def run_ours(args, world, rank, local_rank):
         copies.append({k: dev_tensor(w[k], device) for k in ("q", "k_pages", "v_pages", "page_table", "seq_lens")})
     B = len(w["seq_lens"])
     ws_bytes = qa.qa_decode_workspace_size(B, int(w["seq_lens"].max()), num_pages=4096, max_pages_per_seq=125)
-    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=device)
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=device)
     out = torch.empty(B, 16, 128, dtype=torch.bfloat16, device=device)
 
     def mk(c):
@@ -335,7 +336,7 @@ def run_ours(args, world, rank, local_rank):
     roofline = {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm"], "unit": "GB/s",
                 "frac": round(gbs / peaks["hbm"], 4),
                 "traffic": profiled_traffic("decode_splitk_decode0p6b.txt", digest),
-                "kernel": "decode_splitk_kernel + decode_combine_kernel (one qa_decode_attn call)",
+                "kernel": "decode_splitk_kernel (one qa_decode_attn call = one launch)",
                 "algorithmic_bytes_per_launch": nbytes, "peak_source": peaks["source"] + " (burst copy)",
                 "source_digest": digest}
 
@@ -345,14 +346,18 @@ def run_ours(args, world, rank, local_rank):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": CONFIG_DECODE(w),
         "clocks": clocks, "e2e": {"value": round(e2e_value, 3), "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
                                   "d2h_bytes_per_step": int(d2h), "steps": e2e_steps},
-        "gpu_launches": 2 * args.steps, "roofline": roofline,
+        "gpu_launches": args.steps, "roofline": roofline,
         "tokens_per_s": round(B / per_call * world, 1),
     }
     del copies
     torch.cuda.empty_cache()
 
-    if args.rows == "all":
-        line["rows"] = measure_rows(qa, device, stream, peaks, args)
+    rows = {"all": ROW_NAMES, "none": ()}.get(args.rows, tuple(r for r in args.rows.split(",") if r))
+    unknown = set(rows) - set(ROW_NAMES)
+    if unknown:
+        raise SystemExit(f"unknown rows: {sorted(unknown)}")
+    if rows:
+        line["rows"] = measure_rows(qa, device, stream, peaks, args, rows)
 
     if rank == 0 and not args.no_cpu:
         t, cores = cpu_oracle_decode(w)
@@ -362,15 +367,35 @@ def run_ours(args, world, rank, local_rank):
         print(json.dumps(line))
 
 
-def measure_rows(qa, device, stream, peaks, args):
+ROW_NAMES = ("prefill", "window", "decode_long", "tiny")
+
+
+def measure_rows(qa, device, stream, peaks, args, which=ROW_NAMES):
     """The other hot-path operations, each timed the same way (graphs of
     back-to-back calls, inputs in HBM, above L2 or rotated)."""
     import torch
 
     rows = {}
     steps = max(20, min(args.steps, 400))
+    if "prefill" in which:
+        _row_prefill(qa, device, stream, peaks, steps, rows)
+    if "window" in which:
+        _row_window(qa, device, stream, peaks, steps, rows)
+    if "decode_long" in which:
+        _row_decode_long(qa, device, stream, peaks, steps, rows)
+    if "tiny" in which:
+        _row_tiny(qa, device, stream, steps, rows)
+    status = qa.qa_device_status(stream)
+    if status:
+        raise RuntimeError(f"device status {status:#x} after the row measurements")
+    torch.cuda.empty_cache()
+    return rows
 
-    # ragged causal prefill with page write (16 requests, ~3.9K tokens)
+
+def _row_prefill(qa, device, stream, peaks, steps, rows):
+    """Ragged causal prefill with page write (16 requests, ~3.6K tokens)."""
+    import torch
+
     w = wl.prefill_bucket()
     T = int(w["cu_seqlens"][-1])
     cps = []
@@ -391,8 +416,12 @@ def measure_rows(qa, device, stream, peaks, args):
                        "frac_bf16_peak": round(fl / t / 1e12 / peaks["bf16"], 4),
                        "frac_hbm": round(by / t / 1e9 / peaks["hbm"], 4), "flops": fl, "bytes": by,
                        "gpu_launches_per_call": 2}
-    del cps
-    # AuT windowed attention (8 requests, ~63K tokens, 14 x 64)
+
+
+def _row_window(qa, device, stream, peaks, steps, rows):
+    """AuT windowed attention (8 requests, ~70K tokens, 14 x 64)."""
+    import torch
+
     w = wl.window_aut()
     cu = qa.qa_window_plan(w["token_counts"])
     T = int(cu[-1])
@@ -414,12 +443,16 @@ def measure_rows(qa, device, stream, peaks, args):
                       "frac_bf16_peak": round(fl / t / 1e12 / peaks["bf16"], 4),
                       "frac_hbm": round(by / t / 1e9 / peaks["hbm"], 4), "flops": fl, "bytes": by,
                       "gpu_launches_per_call": 1}
-    del cps
-    # long-context decode 1.7B (64 requests, ~9K tokens each)
+
+
+def _row_decode_long(qa, device, stream, peaks, steps, rows):
+    """Long-context decode 1.7B (64 requests, ~9K tokens each)."""
+    import torch
+
     w = wl.decode_1p7b()
     c = {k: dev_tensor(w[k], device) for k in ("q", "k_pages", "v_pages", "page_table", "seq_lens")}
     B = len(w["seq_lens"])
-    ws = torch.empty(qa.qa_decode_workspace_size(B, int(w["seq_lens"].max()), num_pages=65536, max_pages_per_seq=1000),
+    ws = torch.zeros(qa.qa_decode_workspace_size(B, int(w["seq_lens"].max()), num_pages=65536, max_pages_per_seq=1000),
                      dtype=torch.uint8, device=device)
     outd = torch.empty(B, 16, 128, dtype=torch.bfloat16, device=device)
     f = lambda: qa.qa_decode_attn(c["q"], c["k_pages"], c["v_pages"], c["page_table"], c["seq_lens"], outd,  # noqa
@@ -432,16 +465,21 @@ def measure_rows(qa, device, stream, peaks, args):
                                        "65536-page pool", "sum_seq_len": int(np.sum(w["seq_lens"])),
                            "us_per_call": round(t * 1e6, 2), "gbs": round(by / t / 1e9, 1),
                            "frac_hbm": round(by / t / 1e9 / peaks["hbm"], 4), "bytes": by,
-                           "tokens_per_s": round(B / t, 1), "gpu_launches_per_call": 2}
+                           "tokens_per_s": round(B / t, 1), "gpu_launches_per_call": 1}
     del c
     torch.cuda.empty_cache()
-    # tiny: prefill 64 then decode (latency)
+
+
+def _row_tiny(qa, device, stream, steps, rows):
+    """Tiny: prefill of 64 tokens then one decode token (latency)."""
+    import torch
+
     w = wl.tiny()
     c = {k: dev_tensor(w[k], device) for k in ("q", "k", "v", "cu_seqlens", "page_table", "k_pages", "v_pages",
                                                 "decode_q", "seq_lens")}
     outt = torch.empty(64, 16, 128, dtype=torch.bfloat16, device=device)
     outd = torch.empty(1, 16, 128, dtype=torch.bfloat16, device=device)
-    ws = torch.empty(qa.qa_decode_workspace_size(1, 64, num_pages=4, max_pages_per_seq=4), dtype=torch.uint8,
+    ws = torch.zeros(qa.qa_decode_workspace_size(1, 64, num_pages=4, max_pages_per_seq=4), dtype=torch.uint8,
                      device=device)
 
     def tiny_step():
@@ -452,11 +490,8 @@ def measure_rows(qa, device, stream, peaks, args):
 
     el, _ = graph_time([tiny_step], steps, 5, stream)
     rows["tiny"] = {"workload": "tiny: prefill of 64 tokens into 4 permuted pages, then 1 decode token",
-                    "us_per_step": round(el / steps * 1e6, 2), "note": "latency-bound; no roofline fraction"}
-    status = qa.qa_device_status(stream)
-    if status:
-        raise RuntimeError(f"device status {status:#x} after the row measurements")
-    return rows
+                    "us_per_step": round(el / steps * 1e6, 2), "note": "latency-bound; no roofline fraction",
+                    "gpu_launches_per_step": 3}
 
 
 def main():
@@ -465,7 +500,8 @@ def main():
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--rows", choices=["all", "none"], default="all")
+    ap.add_argument("--rows", default="all",
+                    help="other hot-path rows to measure: all, none, or a comma list of prefill,window,decode_long,tiny")
     ap.add_argument("--no-cpu", action="store_true", help="skip the cpu_baseline leg")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -111,8 +111,11 @@ typedef struct qa_attn_params {
 qa_attn_params qa_attn_default_params(void);
 
 /* Bytes of device workspace qa_decode_attn needs for `batch` requests on the
- * CURRENT device with these params (the split-K partial results: one fp32
- * (max, sum, accumulator[head_dim]) record per query head per work segment).
+ * CURRENT device with these params: the split-K partial results (one fp32
+ * (max, sum, accumulator[head_dim]) record per query head per work segment)
+ * and one int32 arrival counter per request.  The workspace must be
+ * zero-filled once before its first use (e.g. cudaMemset); every call leaves
+ * the counters at zero again, so it can be reused without clearing.
  * max_seq_len is the longest sequence the caller will pass (used only for
  * validation).  Returns 0 on invalid arguments and sets qa_last_error(). */
 size_t qa_decode_workspace_size(int batch, int max_seq_len, const qa_attn_params *params);
@@ -136,7 +139,9 @@ size_t qa_decode_workspace_size(int batch, int max_seq_len, const qa_attn_params
  * read into the result (they may hold anything, NaN included).
  * Supported: head_dim 128, page_size 16, n_kv_heads in [1, 8],
  * n_q_heads / n_kv_heads in {1, 2}.  Needs params->workspace of at least
- * qa_decode_workspace_size(batch, ...) bytes, 256-byte aligned. */
+ * qa_decode_workspace_size(batch, ...) bytes, 256-byte aligned, zero-filled
+ * before its first use (see qa_decode_workspace_size).  Calls sharing one
+ * workspace must be ordered (one stream), since they share its counters. */
 qa_status qa_decode_attn(const void *q, const void *k_pages, const void *v_pages,
                          const int32_t *page_table, const int32_t *seq_lens, int batch,
                          void *out, const qa_attn_params *params);

@@ -163,8 +163,9 @@ def qa_decode_attn(q, k_pages, v_pages, page_table, seq_lens, out=None, *, works
                    stream=None, debug_checks=False):
     """Paged GQA decode.  q bf16 [B,Hq,D]; pools bf16 [P,16,Hkv,D];
     page_table int32 [B,max_pages]; seq_lens int32 [B].  Returns out bf16
-    [B,Hq,D].  `workspace` is a device byte tensor of at least
-    qa_decode_workspace_size(B, ...) bytes (allocated here if omitted)."""
+    [B,Hq,D].  `workspace` is a zero-filled device byte tensor of at least
+    qa_decode_workspace_size(B, ...) bytes (allocated here if omitted); the
+    call leaves it zero-filled, so it can be reused across calls."""
     torch = _torch()
     B, Hq, D = q.shape
     P, PS, Hkv, D2 = k_pages.shape
@@ -175,7 +176,7 @@ def qa_decode_attn(q, k_pages, v_pages, page_table, seq_lens, out=None, *, works
     if workspace is None:
         nbytes = qa_decode_workspace_size(B, 0, n_q_heads=Hq, n_kv_heads=Hkv, head_dim=D, page_size=PS,
                                           num_pages=P, max_pages_per_seq=page_table.shape[1])
-        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+        workspace = torch.zeros(nbytes, dtype=torch.uint8, device=q.device)
     p = _params(n_q_heads=Hq, n_kv_heads=Hkv, head_dim=D, page_size=PS, num_pages=P,
                 max_pages_per_seq=page_table.shape[1], scale=scale, stream=stream, workspace=workspace,
                 debug_checks=debug_checks)

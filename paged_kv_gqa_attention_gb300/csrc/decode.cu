@@ -1,5 +1,5 @@
-// Paged GQA decode: split-K flash decode over a paged KV pool, then a
-// split-combine pass.
+// Paged GQA decode: split-K flash decode over a paged KV pool, with the
+// split-combine folded into the same kernel.
 //
 // What it computes (qwenasr.cpp ARCHITECTURE.md, "Qwen3 Thinker decoder":
 // decode attends over [0, cur_len + 1) of the cache; "GGUF layout": 16 query
@@ -14,18 +14,21 @@
 // ranges, so every CTA streams the same number of pages whatever the mix of
 // lengths.  A CTA's range intersects one or more requests; each intersection
 // is a "segment".  A segment that holds a whole request writes the final
-// bf16 output; otherwise it writes an fp32 partial (running max, running sum,
-// un-normalised accumulator) that the combine kernel merges.  Segment (c, b)
-// of CTA c and request b is stored at slot c + b, which is unique because
-// both ranges are ordered.
+// bf16 output.  Otherwise it writes an fp32 partial (running max, running
+// sum, un-normalised accumulator) to slot c + b (CTA c, request b: unique
+// because both ranges are ordered), then counts itself in the request's
+// arrival counter; the CTA that arrives last merges every partial of the
+// request, writes the output and resets the counter to zero, so nothing ever
+// waits on another CTA and the workspace is left as it was found.
 //
 // Inside a CTA.  One producer warp streams whole pages (K page and V page,
 // 16 tokens x Hkv heads x 128 dims of bf16 each, contiguous in the pool) into
 // a ring of shared-memory stages with the bulk-copy engine, completing on an
-// mbarrier per stage.  2*Hkv consumer warps share each stage: warp (g, half)
-// handles KV head g for tokens [8*half, 8*half + 8) of the page and both
-// query heads of that KV head (GQA sharing), with the fp32 online softmax in
-// registers and warp-shuffle reductions.  Lane l owns dims [4l, 4l + 4).
+// mbarrier per stage; its lanes fetch the page ids 32 at a time.  2*Hkv
+// consumer warps share each stage: warp (g, half) handles KV head g for tokens
+// [8*half, 8*half + 8) of the page and both query heads of that KV head (GQA
+// sharing), with the fp32 online softmax in registers and warp-shuffle
+// reductions.  Lane l owns dims [4l, 4l + 4).
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -44,6 +47,8 @@ constexpr int kMaxHkv = 8;
 // Merge record of one query head in shared memory: m, l, two pad words (so
 // the accumulator starts on a 16-byte boundary), then acc[kD].
 constexpr int kRec = 4 + kD;
+// Named barrier over every consumer warp (ids 1..8 are the KV-head pairs).
+constexpr int kBarConsumers = 9;
 
 struct DecodeArgs {
     const uint16_t *q;
@@ -54,6 +59,7 @@ struct DecodeArgs {
     uint16_t *out;
     float *part_acc;  // [slots][Hq][D]
     float *part_ml;   // [slots][Hq][2]
+    int *arrivals;    // [batch], zero between calls
     int batch, hkv, max_pages, num_pages;
     float scale_log2;  // scale * log2(e)
 };
@@ -82,8 +88,8 @@ __host__ __device__ inline SmemLayout smem_layout(int hkv, int batch, int group)
     uint32_t o = kStages * s.stage_bytes;
     s.off_bar = o;
     o += 2 * kStages * 8;
-    s.off_flag = o;
-    o += kStages * 4;
+    s.off_flag = o;  // page_ok[kStages], then the "merge here" flag
+    o += (kStages + 1) * 4;
     o = (o + 15) & ~15u;
     s.off_prefix = o;
     o += (batch + 1) * 4;
@@ -92,6 +98,20 @@ __host__ __device__ inline SmemLayout smem_layout(int hkv, int batch, int group)
     o += hkv * group * kRec * 4;
     s.total = o;
     return s;
+}
+
+struct WorkspaceLayout {
+    size_t acc, ml, arrivals, total;
+};
+
+__host__ __device__ inline WorkspaceLayout workspace_layout(int batch, int hq, int ctas) {
+    const size_t slots = (size_t)ctas + (size_t)batch;
+    WorkspaceLayout w;
+    w.acc = 0;
+    w.ml = (slots * hq * kD * sizeof(float) + 255) & ~(size_t)255;
+    w.arrivals = w.ml + ((slots * hq * 2 * sizeof(float) + 255) & ~(size_t)255);
+    w.total = w.arrivals + (((size_t)batch * sizeof(int) + 255) & ~(size_t)255);
+    return w;
 }
 
 template <int GROUP>
@@ -104,6 +124,7 @@ __global__ void __launch_bounds__((2 * kMaxHkv + 1) * 32, 1) decode_splitk_kerne
 
     int *prefix = reinterpret_cast<int *>(smem + L.off_prefix);
     int *page_ok = reinterpret_cast<int *>(smem + L.off_flag);
+    volatile int *merge_here = reinterpret_cast<volatile int *>(smem + L.off_flag) + kStages;
     const uint32_t bar_full = smem_u32(smem + L.off_bar);
     const uint32_t bar_empty = bar_full + kStages * 8;
 
@@ -132,6 +153,16 @@ __global__ void __launch_bounds__((2 * kMaxHkv + 1) * 32, 1) decode_splitk_kerne
     }
     __syncthreads();
 
+    // CTA 0 writes the zero rows of requests with nothing to attend over.
+    if (blockIdx.x == 0) {
+        const int chunks = hq * kD * 2 / 16;  // 16-byte chunks per request
+        for (int b = 0; b < a.batch; ++b) {
+            if (prefix[b + 1] != prefix[b]) continue;
+            uint4 *dst = reinterpret_cast<uint4 *>(a.out + (size_t)b * hq * kD);
+            for (int c = threadIdx.x; c < chunks; c += blockDim.x) dst[c] = make_uint4(0u, 0u, 0u, 0u);
+        }
+    }
+
     const int total = prefix[a.batch];
     if (total == 0) return;
     const int per = (total + gridDim.x - 1) / gridDim.x;
@@ -151,38 +182,42 @@ __global__ void __launch_bounds__((2 * kMaxHkv + 1) * 32, 1) decode_splitk_kerne
     }
 
     if (warp == n_consumers) {
-        // ---------------- producer warp: one lane issues the bulk copies
-        if (lane == 0) {
-            const uint64_t policy = policy_evict_first();
-            int it = 0;
-            for (int b = b0; b < a.batch && prefix[b] < hi; ++b) {
-                const int p0 = prefix[b], p1 = prefix[b + 1];
-                if (p1 == p0) continue;
-                const int j0 = max(lo, p0) - p0, j1 = min(hi, p1) - p0;
-                const int32_t *row = a.page_table + (size_t)b * a.max_pages;
-                for (int j = j0; j < j1; ++j, ++it) {
-                    const int s = it % kStages;
-                    if (it >= kStages) mbar_wait(bar_empty + 8 * s, ((it / kStages) & 1) ^ 1, &g_status);
-                    const int page = row[j];
-                    uint8_t *dst = smem + s * L.stage_bytes;
-                    if (page < 0 || page >= a.num_pages) {
-                        atomicOr(&g_status, QA_DEVICE_BAD_PAGE);
-                        page_ok[s] = 0;
-                        mbar_arrive(bar_full + 8 * s);
-                    } else {
-                        page_ok[s] = 1;
-                        mbar_arrive_expect_tx(bar_full + 8 * s, L.stage_bytes);
-                        const size_t off = (size_t)page * L.page_bytes;
-                        bulk_g2s_hint(smem_u32(dst), a.k_pages + off, L.page_bytes, bar_full + 8 * s, policy);
-                        bulk_g2s_hint(smem_u32(dst + L.page_bytes), a.v_pages + off, L.page_bytes,
-                                      bar_full + 8 * s, policy);
+        // ---------------- producer warp: lanes fetch page ids, lane 0 issues copies
+        const uint64_t policy = policy_evict_first();
+        int it = 0;
+        for (int b = b0; b < a.batch && prefix[b] < hi; ++b) {
+            const int p0 = prefix[b], p1 = prefix[b + 1];
+            if (p1 == p0) continue;
+            const int j0 = max(lo, p0) - p0, j1 = min(hi, p1) - p0;
+            const int32_t *row = a.page_table + (size_t)b * a.max_pages;
+            for (int jb = j0; jb < j1; jb += 32) {
+                const int mine = jb + lane < j1 ? row[jb + lane] : -1;
+                const int cnt = min(32, j1 - jb);
+                for (int u = 0; u < cnt; ++u, ++it) {
+                    const int page = __shfl_sync(0xffffffffu, mine, u);
+                    if (lane == 0) {
+                        const int s = it % kStages;
+                        if (it >= kStages) mbar_wait(bar_empty + 8 * s, ((it / kStages) & 1) ^ 1, &g_status);
+                        uint8_t *dst = smem + s * L.stage_bytes;
+                        if (page < 0 || page >= a.num_pages) {
+                            atomicOr(&g_status, QA_DEVICE_BAD_PAGE);
+                            page_ok[s] = 0;
+                            mbar_arrive(bar_full + 8 * s);
+                        } else {
+                            page_ok[s] = 1;
+                            mbar_arrive_expect_tx(bar_full + 8 * s, L.stage_bytes);
+                            const size_t off = (size_t)page * L.page_bytes;
+                            bulk_g2s_hint(smem_u32(dst), a.k_pages + off, L.page_bytes, bar_full + 8 * s, policy);
+                            bulk_g2s_hint(smem_u32(dst + L.page_bytes), a.v_pages + off, L.page_bytes,
+                                          bar_full + 8 * s, policy);
+                        }
                     }
+                    __syncwarp();
                 }
             }
         }
         return;
     }
-    if (warp > n_consumers) return;
 
     // ---------------- consumer warps
     const int g = warp >> 1, half = warp & 1;
@@ -279,8 +314,8 @@ __global__ void __launch_bounds__((2 * kMaxHkv + 1) * 32, 1) decode_splitk_kerne
             }
         }
         named_barrier(1 + g, 64);
+        const bool whole = (j0 == 0 && j1 == p1 - p0);
         if (half == 0) {
-            const bool whole = (j0 == 0 && j1 == p1 - p0);
             const int slot = blockIdx.x + b;
 #pragma unroll
             for (int i = 0; i < GROUP; ++i) {
@@ -311,74 +346,49 @@ __global__ void __launch_bounds__((2 * kMaxHkv + 1) * 32, 1) decode_splitk_kerne
                         a.part_ml[((size_t)slot * hq + h) * 2 + 0] = mm;
                         a.part_ml[((size_t)slot * hq + h) * 2 + 1] = ls;
                     }
+                    __threadfence();  // the partial is visible device-wide before the arrival below
                 }
             }
         }
         named_barrier(1 + g, 64);
-    }
-}
 
-// One CTA per request, one warp per query head: merges the partials of a
-// request that spans several segments, writes zeros for an empty request,
-// and leaves single-segment requests (already written) alone.
-__global__ void decode_combine_kernel(const DecodeArgs a, int ctas, int group) {
-    __shared__ int red[2][32];
-    const int b = blockIdx.x;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int hq = a.hkv * group;
-    int before = 0, total = 0;
-    for (int i = threadIdx.x; i < a.batch; i += blockDim.x) {
-        const int n = pages_of(a, i, false);
-        total += n;
-        if (i < b) before += n;
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        before += __shfl_xor_sync(0xffffffffu, before, o);
-        total += __shfl_xor_sync(0xffffffffu, total, o);
-    }
-    if (lane == 0) {
-        red[0][warp] = before;
-        red[1][warp] = total;
-    }
-    __syncthreads();
-    before = 0;
-    total = 0;
-    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) {
-        before += red[0][w];
-        total += red[1][w];
-    }
-    const int np = pages_of(a, b, false);
-    if (warp >= hq) return;
-    const int h = warp;
-    uint16_t *dst = a.out + ((size_t)b * hq + h) * kD + 4 * lane;
-    if (np == 0) {
-        *reinterpret_cast<uint2 *>(dst) = make_uint2(0u, 0u);
-        return;
-    }
-    const int per = (total + ctas - 1) / ctas;
-    const int c_lo = before / per, c_hi = (before + np - 1) / per;
-    if (c_lo == c_hi) return;
-    float mm = -INFINITY;
-    for (int c = c_lo; c <= c_hi; ++c) mm = fmaxf(mm, a.part_ml[((size_t)(c + b) * hq + h) * 2]);
-    float ls = 0.f, o[4] = {0.f, 0.f, 0.f, 0.f};
-    if (mm != -INFINITY) {
-        for (int c = c_lo; c <= c_hi; ++c) {
-            const size_t r = (size_t)(c + b) * hq + h;
-            const float w = exp2_approx(a.part_ml[r * 2] - mm);
-            ls += w * a.part_ml[r * 2 + 1];
-            const float4 v = *reinterpret_cast<const float4 *>(a.part_acc + r * kD + 4 * lane);
-            o[0] += w * v.x;
-            o[1] += w * v.y;
-            o[2] += w * v.z;
-            o[3] += w * v.w;
+        if (!whole) {
+            // Count this segment in; the last of the request's segments merges.
+            const int c_lo = p0 / per, c_hi = (p1 - 1) / per;
+            named_barrier(kBarConsumers, n_consumers * 32);
+            if (threadIdx.x == 0) {
+                const int prev = atomicAdd(a.arrivals + b, 1);
+                *merge_here = (prev == c_hi - c_lo);
+            }
+            named_barrier(kBarConsumers, n_consumers * 32);
+            if (*merge_here) {
+                __threadfence();
+                for (int h = warp; h < hq; h += n_consumers) {
+                    float mm = -INFINITY, ls = 0.f, o[4] = {0.f, 0.f, 0.f, 0.f};
+                    for (int c = c_lo; c <= c_hi; ++c) {
+                        const size_t r = (size_t)(c + b) * hq + h;
+                        const float mc = __ldcg(a.part_ml + r * 2), lc = __ldcg(a.part_ml + r * 2 + 1);
+                        const float4 v = __ldcg(reinterpret_cast<const float4 *>(a.part_acc + r * kD + 4 * lane));
+                        const float mn = fmaxf(mm, mc);
+                        if (mn == -INFINITY) continue;
+                        const float so = exp2_approx(mm - mn), sn = exp2_approx(mc - mn);
+                        ls = ls * so + lc * sn;
+                        o[0] = o[0] * so + v.x * sn;
+                        o[1] = o[1] * so + v.y * sn;
+                        o[2] = o[2] * so + v.z * sn;
+                        o[3] = o[3] * so + v.w * sn;
+                        mm = mn;
+                    }
+                    const float inv = ls > 0.f ? 1.f / ls : 0.f;
+                    uint2 w;
+                    w.x = pack_bf16x2(o[0] * inv, o[1] * inv);
+                    w.y = pack_bf16x2(o[2] * inv, o[3] * inv);
+                    *reinterpret_cast<uint2 *>(a.out + ((size_t)b * hq + h) * kD + 4 * lane) = w;
+                }
+                if (threadIdx.x == 0) a.arrivals[b] = 0;  // ready for the next call
+            }
         }
     }
-    const float inv = ls > 0.f ? 1.f / ls : 0.f;
-    uint2 w;
-    w.x = pack_bf16x2(o[0] * inv, o[1] * inv);
-    w.y = pack_bf16x2(o[2] * inv, o[3] * inv);
-    *reinterpret_cast<uint2 *>(dst) = w;
 }
 
 }  // namespace
@@ -391,16 +401,16 @@ int decode_grid_ctas(int device) {
 }
 
 size_t decode_workspace_bytes(int batch, int n_q_heads, int head_dim, int ctas) {
-    const size_t slots = (size_t)ctas + (size_t)batch;
-    const size_t acc = slots * n_q_heads * head_dim * sizeof(float);
-    const size_t ml = slots * n_q_heads * 2 * sizeof(float);
-    return ((acc + 255) & ~(size_t)255) + ml;
+    (void)head_dim;
+    return workspace_layout(batch, n_q_heads, ctas).total;
 }
 
 cudaError_t launch_decode(const void *q, const void *k_pages, const void *v_pages,
                           const int32_t *page_table, const int32_t *seq_lens, int batch, void *out,
                           const qa_attn_params &p, float scale, int ctas, cudaStream_t stream) {
     const int group = p.n_q_heads / p.n_kv_heads;
+    const WorkspaceLayout W = workspace_layout(batch, p.n_q_heads, ctas);
+    uint8_t *ws = static_cast<uint8_t *>(p.workspace);
     DecodeArgs a;
     a.q = static_cast<const uint16_t *>(q);
     a.k_pages = static_cast<const uint8_t *>(k_pages);
@@ -408,10 +418,9 @@ cudaError_t launch_decode(const void *q, const void *k_pages, const void *v_page
     a.page_table = page_table;
     a.seq_lens = seq_lens;
     a.out = static_cast<uint16_t *>(out);
-    const size_t slots = (size_t)ctas + (size_t)batch;
-    const size_t acc_bytes = (slots * p.n_q_heads * kD * sizeof(float) + 255) & ~(size_t)255;
-    a.part_acc = static_cast<float *>(p.workspace);
-    a.part_ml = reinterpret_cast<float *>(static_cast<uint8_t *>(p.workspace) + acc_bytes);
+    a.part_acc = reinterpret_cast<float *>(ws + W.acc);
+    a.part_ml = reinterpret_cast<float *>(ws + W.ml);
+    a.arrivals = reinterpret_cast<int *>(ws + W.arrivals);
     a.batch = batch;
     a.hkv = p.n_kv_heads;
     a.max_pages = p.max_pages_per_seq;
@@ -430,9 +439,6 @@ cudaError_t launch_decode(const void *q, const void *k_pages, const void *v_page
         if (e != cudaSuccess) return e;
         decode_splitk_kernel<1><<<ctas, threads, L.total, stream>>>(a);
     }
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    decode_combine_kernel<<<batch, p.n_q_heads * 32, 0, stream>>>(a, ctas, group);
     return cudaGetLastError();
 }
 

@@ -163,7 +163,9 @@ qa_status qa_decode_attn(const void *q, const void *k_pages, const void *v_pages
  *   - All calls on a device share the array: calls whose kernels overlap on
  *     the GPU (unordered streams or host threads) race and give wrong
  *     results.  Calls ordered on one stream are safe.  The array keeps the
- *     last call's contents; nothing in it needs clearing between calls.
+ *     last call's contents; the only part that must start at zero (the
+ *     per-request arrival counters) starts zeroed and every call leaves it
+ *     zeroed, so nothing needs clearing between calls.
  *   - The first call made with a given device current looks up the array's
  *     device address and caches it; make that first call before any CUDA
  *     stream capture begins. */

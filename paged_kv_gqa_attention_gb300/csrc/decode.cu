@@ -100,17 +100,22 @@ __host__ __device__ inline SmemLayout smem_layout(int hkv, int batch, int group)
     return s;
 }
 
+// Workspace: the arrival counters first, in a region of fixed size (one int
+// per request up to the largest batch), so they sit at the same place whatever
+// the batch of a call; then the partials, whose placement depends on the
+// batch.  A zero-filled workspace therefore stays valid across calls of
+// different batch sizes: each call only touches counters it leaves at zero.
 struct WorkspaceLayout {
-    size_t acc, ml, arrivals, total;
+    size_t arrivals, acc, ml, total;
 };
 
 __host__ __device__ inline WorkspaceLayout workspace_layout(int batch, int hq, int ctas) {
     const size_t slots = (size_t)ctas + (size_t)batch;
     WorkspaceLayout w;
-    w.acc = 0;
-    w.ml = (slots * hq * kD * sizeof(float) + 255) & ~(size_t)255;
-    w.arrivals = w.ml + ((slots * hq * 2 * sizeof(float) + 255) & ~(size_t)255);
-    w.total = w.arrivals + (((size_t)batch * sizeof(int) + 255) & ~(size_t)255);
+    w.arrivals = 0;
+    w.acc = ((size_t)kDecodeMaxBatch * sizeof(int) + 255) & ~(size_t)255;
+    w.ml = w.acc + ((slots * hq * kD * sizeof(float) + 255) & ~(size_t)255);
+    w.total = w.ml + ((slots * hq * 2 * sizeof(float) + 255) & ~(size_t)255);
     return w;
 }
 

@@ -15,8 +15,11 @@
 // device share the one array: two calls whose kernels overlap on the GPU
 // (different streams, or different host threads, without ordering between
 // them) race on it and give wrong results; calls ordered on one stream are
-// fine.  The array keeps whatever the last call left in it; the decode writes
-// every partial it later reads, so nothing needs clearing between calls.
+// fine.  The array keeps whatever the last call left in it.  The only part
+// that must start at zero is the block of per-request arrival counters at
+// its head (a fixed-size region whatever the batch): the loader zero-fills
+// the array and every call leaves the counters it used at zero again; the
+// partial results behind them are always written before they are read.
 //
 // Set-up: the device address of the array is looked up (cudaGetSymbolAddress)
 // on the first call made with each device current and cached per device, so

@@ -159,7 +159,7 @@ qa_status qa_decode_attn(const void *q, const void *k_pages, const void *v_pages
  *
  *   - A batch whose scratch would exceed 4 MiB is rejected with
  *     QA_STATUS_INVALID_PARAMS and a message giving the sizes (with 16 query
- *     heads and head_dim 128 about 350 requests fit on a 152-SM GPU).
+ *     heads and head_dim 128 about 330 requests fit on a 152-SM GPU).
  *   - All calls on a device share the array: calls whose kernels overlap on
  *     the GPU (unordered streams or host threads) race and give wrong
  *     results.  Calls ordered on one stream are safe.  The array keeps the

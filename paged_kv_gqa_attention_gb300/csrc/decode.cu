@@ -16,10 +16,13 @@
 // is a "segment".  A segment that holds a whole request writes the final
 // bf16 output.  Otherwise it writes an fp32 partial (running max, running
 // sum, un-normalised accumulator) to slot c + b (CTA c, request b: unique
-// because both ranges are ordered), then counts itself in the request's
-// arrival counter; the CTA that arrives last merges every partial of the
-// request, writes the output and resets the counter to zero, so nothing ever
-// waits on another CTA and the workspace is left as it was found.
+// because both ranges are ordered), then counts itself in the arrival counter
+// of (request, KV head); the warp that arrives last merges every partial of
+// its two query heads, writes the output and resets the counter to zero, so
+// nothing ever waits on another CTA and the workspace is left as it was
+// found.  A CTA takes its last segment first and its first segment second:
+// those are the only ones it can share with a neighbour, so partial results
+// (and the merges) happen early, not at the end of the run.
 //
 // Inside a CTA.  One producer warp streams whole pages (K page and V page,
 // 16 tokens x Hkv heads x 128 dims of bf16 each, contiguous in the pool) into
@@ -27,8 +30,12 @@
 // mbarrier per stage; its lanes fetch the page ids 32 at a time.  2*Hkv
 // consumer warps share each stage: warp (g, half) handles KV head g for tokens
 // [8*half, 8*half + 8) of the page and both query heads of that KV head (GQA
-// sharing), with the fp32 online softmax in registers and warp-shuffle
-// reductions.  Lane l owns dims [4l, 4l + 4).
+// sharing).  Lane l owns dims [4l, 4l + 4): it forms partial dot products
+// for the 16 (token, head) pairs with packed fp32 FMAs, a butterfly
+// reduce-scatter over the warp leaves each pair's full score on two lanes,
+// so each lane runs one exponential of the fp32 online softmax, and the
+// probabilities reach every lane through 128 bytes of shared memory for the
+// P V update.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -47,8 +54,6 @@ constexpr int kMaxHkv = 8;
 // Merge record of one query head in shared memory: m, l, two pad words (so
 // the accumulator starts on a 16-byte boundary), then acc[kD].
 constexpr int kRec = 4 + kD;
-// Named barrier over every consumer warp (ids 1..8 are the KV-head pairs).
-constexpr int kBarConsumers = 9;
 
 struct DecodeArgs {
     const uint16_t *q;
@@ -59,7 +64,7 @@ struct DecodeArgs {
     uint16_t *out;
     float *part_acc;  // [slots][Hq][D]
     float *part_ml;   // [slots][Hq][2]
-    int *arrivals;    // [batch], zero between calls
+    int *arrivals;    // [kDecodeMaxBatch][kMaxHkv], zero between calls
     int batch, hkv, max_pages, num_pages;
     float scale_log2;  // scale * log2(e)
 };
@@ -78,7 +83,7 @@ __device__ __forceinline__ int pages_of(const DecodeArgs &a, int b, bool report)
 struct SmemLayout {
     uint32_t stage_bytes;  // one stage: K page + V page
     uint32_t page_bytes;
-    uint32_t off_bar, off_flag, off_prefix, off_merge, total;
+    uint32_t off_bar, off_flag, off_prefix, off_merge, off_pbuf, total;
 };
 
 __host__ __device__ inline SmemLayout smem_layout(int hkv, int batch, int group) {
@@ -88,20 +93,22 @@ __host__ __device__ inline SmemLayout smem_layout(int hkv, int batch, int group)
     uint32_t o = kStages * s.stage_bytes;
     s.off_bar = o;
     o += 2 * kStages * 8;
-    s.off_flag = o;  // page_ok[kStages], then the "merge here" flag
-    o += (kStages + 1) * 4;
+    s.off_flag = o;  // page_ok[kStages]
+    o += kStages * 4;
     o = (o + 15) & ~15u;
     s.off_prefix = o;
     o += (batch + 1) * 4;
     o = (o + 15) & ~15u;
     s.off_merge = o;
     o += hkv * group * kRec * 4;
+    s.off_pbuf = o;  // 16 float2 per consumer warp
+    o += 2 * hkv * 16 * 8;
     s.total = o;
     return s;
 }
 
 // Workspace: the arrival counters first, in a region of fixed size (one int
-// per request up to the largest batch), so they sit at the same place whatever
+// per request and KV head up to the largest batch), so they sit at the same place whatever
 // the batch of a call; then the partials, whose placement depends on the
 // batch.  A zero-filled workspace therefore stays valid across calls of
 // different batch sizes: each call only touches counters it leaves at zero.
@@ -113,10 +120,34 @@ __host__ __device__ inline WorkspaceLayout workspace_layout(int batch, int hq, i
     const size_t slots = (size_t)ctas + (size_t)batch;
     WorkspaceLayout w;
     w.arrivals = 0;
-    w.acc = ((size_t)kDecodeMaxBatch * sizeof(int) + 255) & ~(size_t)255;
+    w.acc = ((size_t)kDecodeMaxBatch * kMaxHkv * sizeof(int) + 255) & ~(size_t)255;
     w.ml = w.acc + ((slots * hq * kD * sizeof(float) + 255) & ~(size_t)255);
     w.total = w.ml + ((slots * hq * 2 * sizeof(float) + 255) & ~(size_t)255);
     return w;
+}
+
+// First request b whose pages reach past page index x (prefix[b + 1] > x).
+__device__ __forceinline__ int first_request_past(const int *prefix, int batch, int x) {
+    int l = 0, r = batch - 1;
+    while (l < r) {
+        const int mid = (l + r) >> 1;
+        if (prefix[mid + 1] > x) r = mid; else l = mid + 1;
+    }
+    return l;
+}
+
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;"
+        : "=l"(d)
+        : "l"(*reinterpret_cast<uint64_t *>(&a)), "l"(*reinterpret_cast<uint64_t *>(&b)),
+          "l"(*reinterpret_cast<uint64_t *>(&c)));
+    return *reinterpret_cast<float2 *>(&d);
+}
+
+__device__ __forceinline__ void bf16x4(uint2 w, float2 &lo, float2 &hi) {
+    lo = make_float2(bf16lo(w.x), bf16hi(w.x));
+    hi = make_float2(bf16lo(w.y), bf16hi(w.y));
 }
 
 template <int GROUP>
@@ -129,7 +160,6 @@ __global__ void __launch_bounds__((2 * kMaxHkv + 1) * 32, 1) decode_splitk_kerne
 
     int *prefix = reinterpret_cast<int *>(smem + L.off_prefix);
     int *page_ok = reinterpret_cast<int *>(smem + L.off_flag);
-    volatile int *merge_here = reinterpret_cast<volatile int *>(smem + L.off_flag) + kStages;
     const uint32_t bar_full = smem_u32(smem + L.off_bar);
     const uint32_t bar_empty = bar_full + kStages * 8;
 
@@ -175,22 +205,18 @@ __global__ void __launch_bounds__((2 * kMaxHkv + 1) * 32, 1) decode_splitk_kerne
     const int hi = min(lo + per, total);
     if (lo >= hi) return;
 
-    // First request whose pages reach past lo.
-    int b0 = 0;
-    {
-        int l = 0, r = a.batch - 1;
-        while (l < r) {
-            int mid = (l + r) >> 1;
-            if (prefix[mid + 1] > lo) r = mid; else l = mid + 1;
-        }
-        b0 = l;
-    }
+    // Requests b0 (holding page lo) .. b_last (holding page hi - 1).  Visit
+    // order: b_last, then b0 .. b_last - 1 (see the header comment).
+    const int b0 = first_request_past(prefix, a.batch, lo);
+    const int b_last = first_request_past(prefix, a.batch, hi - 1);
+    const int n_visit = b_last - b0 + 1;
 
     if (warp == n_consumers) {
         // ---------------- producer warp: lanes fetch page ids, lane 0 issues copies
         const uint64_t policy = policy_evict_first();
         int it = 0;
-        for (int b = b0; b < a.batch && prefix[b] < hi; ++b) {
+        for (int k = 0; k < n_visit; ++k) {
+            const int b = k == 0 ? b_last : b0 + k - 1;
             const int p0 = prefix[b], p1 = prefix[b + 1];
             if (p1 == p0) continue;
             const int j0 = max(lo, p0) - p0, j1 = min(hi, p1) - p0;
@@ -227,27 +253,36 @@ __global__ void __launch_bounds__((2 * kMaxHkv + 1) * 32, 1) decode_splitk_kerne
     // ---------------- consumer warps
     const int g = warp >> 1, half = warp & 1;
     float *merge = reinterpret_cast<float *>(smem + L.off_merge) + g * GROUP * kRec;
+    float2 *pbuf = reinterpret_cast<float2 *>(smem + L.off_pbuf) + warp * 16;
+    // After the reduce-scatter lane l holds the score of token my_t of this
+    // warp's 8 and query head my_h of the group (lanes l, l ^ 1 agree).
+    constexpr int NV = 8 * GROUP;          // (token, head) pairs per warp and page
+    constexpr int LOG = GROUP == 2 ? 4 : 3;
+    const int my_t = lane >> 2;
+    const int my_h = GROUP == 2 ? (lane >> 1) & 1 : 0;
+    const bool p_writer = GROUP == 2 ? (lane & 1) == 0 : (lane & 3) == 0;
     int it = 0;
-    for (int b = b0; b < a.batch && prefix[b] < hi; ++b) {
+    for (int k = 0; k < n_visit; ++k) {
+        const int b = k == 0 ? b_last : b0 + k - 1;
         const int p0 = prefix[b], p1 = prefix[b + 1];
         if (p1 == p0) continue;
         const int j0 = max(lo, p0) - p0, j1 = min(hi, p1) - p0;
         const int seq_len = a.seq_lens[b];
 
-        float q[GROUP][4], acc[GROUP][4], m[GROUP], l[GROUP];
+        float2 q01[GROUP], q23[GROUP], acc01[GROUP], acc23[GROUP];
 #pragma unroll
         for (int i = 0; i < GROUP; ++i) {
             const uint2 w = *reinterpret_cast<const uint2 *>(
                 a.q + ((size_t)b * hq + g * GROUP + i) * kD + 4 * lane);
-            q[i][0] = bf16lo(w.x) * a.scale_log2;
-            q[i][1] = bf16hi(w.x) * a.scale_log2;
-            q[i][2] = bf16lo(w.y) * a.scale_log2;
-            q[i][3] = bf16hi(w.y) * a.scale_log2;
-            m[i] = -INFINITY;
-            l[i] = 0.f;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) acc[i][e] = 0.f;
+            bf16x4(w, q01[i], q23[i]);
+            q01[i].x *= a.scale_log2;
+            q01[i].y *= a.scale_log2;
+            q23[i].x *= a.scale_log2;
+            q23[i].y *= a.scale_log2;
+            acc01[i] = make_float2(0.f, 0.f);
+            acc23[i] = make_float2(0.f, 0.f);
         }
+        float m_own = -INFINITY, l_own = 0.f;
 
         for (int j = j0; j < j1; ++j, ++it) {
             const int s = it % kStages;
@@ -256,54 +291,121 @@ __global__ void __launch_bounds__((2 * kMaxHkv + 1) * 32, 1) decode_splitk_kerne
             const int t0 = half * 8;
             const int nt = min(8, n_valid - t0);
             if (page_ok[s] && nt > 0) {
-                const uint8_t *Ks = smem + s * L.stage_bytes;
+                const uint8_t *Ks = smem + s * L.stage_bytes + ((t0 * a.hkv + g) * kD + 4 * lane) * 2;
                 const uint8_t *Vs = Ks + L.page_bytes;
-                float sc[GROUP][8];
+                const int row_stride = a.hkv * kD * 2;
+                // partial dots of every (token, head); rows past the sequence
+                // (sentinels, possibly NaN) only ever touch their own entry
+                float v[NV];
 #pragma unroll
                 for (int t = 0; t < 8; ++t) {
-                    if (t < nt) {
-                        const uint2 w = *reinterpret_cast<const uint2 *>(
-                            Ks + (((t0 + t) * a.hkv + g) * kD + 4 * lane) * 2);
-                        const float k0 = bf16lo(w.x), k1 = bf16hi(w.x), k2 = bf16lo(w.y), k3 = bf16hi(w.y);
+                    float2 k01, k23;
+                    bf16x4(*reinterpret_cast<const uint2 *>(Ks + t * row_stride), k01, k23);
 #pragma unroll
-                        for (int i = 0; i < GROUP; ++i)
-                            sc[i][t] = warp_sum(q[i][0] * k0 + q[i][1] * k1 + q[i][2] * k2 + q[i][3] * k3);
-                    } else {
+                    for (int i = 0; i < GROUP; ++i) {
+                        const float2 sp = ffma2(q23[i], k23, ffma2(q01[i], k01, make_float2(0.f, 0.f)));
+                        v[t * GROUP + i] = sp.x + sp.y;
+                    }
+                }
+                // butterfly reduce-scatter: stage `st` halves the live entries
 #pragma unroll
-                        for (int i = 0; i < GROUP; ++i) sc[i][t] = -INFINITY;
+                for (int st = 0; st < LOG; ++st) {
+                    const int off = 16 >> st;
+                    const int hn = NV >> (st + 1);
+                    const bool upper = (lane & off) != 0;
+#pragma unroll
+                    for (int i = 0; i < hn; ++i) {
+                        const float send = upper ? v[i] : v[i + hn];
+                        const float keep = upper ? v[i + hn] : v[i];
+                        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
                     }
                 }
 #pragma unroll
-                for (int i = 0; i < GROUP; ++i) {
-                    float mx = m[i];
-#pragma unroll
-                    for (int t = 0; t < 8; ++t) mx = fmaxf(mx, sc[i][t]);
-                    const float alpha = exp2_approx(m[i] - mx);
-                    m[i] = mx;
-                    l[i] *= alpha;
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) acc[i][e] *= alpha;
+                for (int off = 16 >> LOG; off > 0; off >>= 1) v[0] += __shfl_xor_sync(0xffffffffu, v[0], off);
+                const float sc = my_t < nt ? v[0] : -INFINITY;
+                // online softmax of this lane's query head
+                float tmax = sc;
+                tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 4));
+                tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 8));
+                tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 16));
+                const float m_new = fmaxf(m_own, tmax);
+                const float alpha_own = exp2_approx(m_own - m_new);
+                const float p = exp2_approx(sc - m_new);
+                l_own = l_own * alpha_own + p;
+                m_own = m_new;
+                float alpha[GROUP];
+                if (GROUP == 2) {
+                    const float other = __shfl_xor_sync(0xffffffffu, alpha_own, 2);
+                    alpha[0] = my_h == 0 ? alpha_own : other;
+                    alpha[GROUP - 1] = my_h == 1 ? alpha_own : other;
+                } else {
+                    alpha[0] = alpha_own;
                 }
 #pragma unroll
-                for (int t = 0; t < 8; ++t) {
-                    if (t < nt) {
-                        const uint2 w = *reinterpret_cast<const uint2 *>(
-                            Vs + (((t0 + t) * a.hkv + g) * kD + 4 * lane) * 2);
-                        const float v0 = bf16lo(w.x), v1 = bf16hi(w.x), v2 = bf16lo(w.y), v3 = bf16hi(w.y);
+                for (int i = 0; i < GROUP; ++i) {
+                    if (alpha[i] != 1.f) {  // uniform across the warp
+                        acc01[i].x *= alpha[i];
+                        acc01[i].y *= alpha[i];
+                        acc23[i].x *= alpha[i];
+                        acc23[i].y *= alpha[i];
+                    }
+                }
+                __syncwarp();
+                if (p_writer) pbuf[GROUP == 2 ? (lane >> 1) : (lane >> 2)] = make_float2(p, p);
+                __syncwarp();
+                if (nt == 8) {
+#pragma unroll
+                    for (int t = 0; t < 8; ++t) {
+                        float2 v01, v23;
+                        bf16x4(*reinterpret_cast<const uint2 *>(Vs + t * row_stride), v01, v23);
 #pragma unroll
                         for (int i = 0; i < GROUP; ++i) {
-                            const float p = exp2_approx(sc[i][t] - m[i]);
-                            l[i] += p;
-                            acc[i][0] += p * v0;
-                            acc[i][1] += p * v1;
-                            acc[i][2] += p * v2;
-                            acc[i][3] += p * v3;
+                            const float2 pp = pbuf[t * GROUP + i];
+                            acc01[i] = ffma2(v01, pp, acc01[i]);
+                            acc23[i] = ffma2(v23, pp, acc23[i]);
+                        }
+                    }
+                } else {
+                    for (int t = 0; t < nt; ++t) {  // tail page: skip rows past the sequence
+                        float2 v01, v23;
+                        bf16x4(*reinterpret_cast<const uint2 *>(Vs + t * row_stride), v01, v23);
+#pragma unroll
+                        for (int i = 0; i < GROUP; ++i) {
+                            const float2 pp = pbuf[t * GROUP + i];
+                            acc01[i] = ffma2(v01, pp, acc01[i]);
+                            acc23[i] = ffma2(v23, pp, acc23[i]);
                         }
                     }
                 }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_empty + 8 * s);
+        }
+
+        // Sum of probabilities per query head (over the 8 token lanes), and
+        // both heads' (m, l) on every lane.
+        float l_head = l_own;
+        l_head += __shfl_xor_sync(0xffffffffu, l_head, 4);
+        l_head += __shfl_xor_sync(0xffffffffu, l_head, 8);
+        l_head += __shfl_xor_sync(0xffffffffu, l_head, 16);
+        float m[GROUP], l[GROUP], acc[GROUP][4];
+        if (GROUP == 2) {
+            const float m_other = __shfl_xor_sync(0xffffffffu, m_own, 2);
+            const float l_other = __shfl_xor_sync(0xffffffffu, l_head, 2);
+            m[0] = my_h == 0 ? m_own : m_other;
+            l[0] = my_h == 0 ? l_head : l_other;
+            m[GROUP - 1] = my_h == 1 ? m_own : m_other;
+            l[GROUP - 1] = my_h == 1 ? l_head : l_other;
+        } else {
+            m[0] = m_own;
+            l[0] = l_head;
+        }
+#pragma unroll
+        for (int i = 0; i < GROUP; ++i) {
+            acc[i][0] = acc01[i].x;
+            acc[i][1] = acc01[i].y;
+            acc[i][2] = acc23[i].x;
+            acc[i][3] = acc23[i].y;
         }
 
         // Merge the two halves of KV head g through shared memory.
@@ -319,8 +421,8 @@ __global__ void __launch_bounds__((2 * kMaxHkv + 1) * 32, 1) decode_splitk_kerne
             }
         }
         named_barrier(1 + g, 64);
-        const bool whole = (j0 == 0 && j1 == p1 - p0);
         if (half == 0) {
+            const bool whole = (j0 == 0 && j1 == p1 - p0);
             const int slot = blockIdx.x + b;
 #pragma unroll
             for (int i = 0; i < GROUP; ++i) {
@@ -351,48 +453,47 @@ __global__ void __launch_bounds__((2 * kMaxHkv + 1) * 32, 1) decode_splitk_kerne
                         a.part_ml[((size_t)slot * hq + h) * 2 + 0] = mm;
                         a.part_ml[((size_t)slot * hq + h) * 2 + 1] = ls;
                     }
-                    __threadfence();  // the partial is visible device-wide before the arrival below
+                }
+            }
+            if (!whole) {
+                // Count this partial in; the last arriving warp of (b, g) merges.
+                const int c_lo = p0 / per, c_hi = (p1 - 1) / per;
+                __threadfence();
+                __syncwarp();
+                int prev = 0;
+                if (lane == 0) prev = atomicAdd(a.arrivals + (size_t)b * kMaxHkv + g, 1);
+                prev = __shfl_sync(0xffffffffu, prev, 0);
+                if (prev == c_hi - c_lo) {
+                    __threadfence();
+#pragma unroll
+                    for (int i = 0; i < GROUP; ++i) {
+                        const int h = g * GROUP + i;
+                        float mm = -INFINITY, ls = 0.f, o[4] = {0.f, 0.f, 0.f, 0.f};
+                        for (int c = c_lo; c <= c_hi; ++c) {
+                            const size_t r = (size_t)(c + b) * hq + h;
+                            const float mc = __ldcg(a.part_ml + r * 2), lc = __ldcg(a.part_ml + r * 2 + 1);
+                            const float4 pv = __ldcg(reinterpret_cast<const float4 *>(a.part_acc + r * kD + 4 * lane));
+                            const float mn = fmaxf(mm, mc);
+                            if (mn == -INFINITY) continue;
+                            const float so = exp2_approx(mm - mn), sn = exp2_approx(mc - mn);
+                            ls = ls * so + lc * sn;
+                            o[0] = o[0] * so + pv.x * sn;
+                            o[1] = o[1] * so + pv.y * sn;
+                            o[2] = o[2] * so + pv.z * sn;
+                            o[3] = o[3] * so + pv.w * sn;
+                            mm = mn;
+                        }
+                        const float inv = ls > 0.f ? 1.f / ls : 0.f;
+                        uint2 w;
+                        w.x = pack_bf16x2(o[0] * inv, o[1] * inv);
+                        w.y = pack_bf16x2(o[2] * inv, o[3] * inv);
+                        *reinterpret_cast<uint2 *>(a.out + ((size_t)b * hq + h) * kD + 4 * lane) = w;
+                    }
+                    if (lane == 0) a.arrivals[(size_t)b * kMaxHkv + g] = 0;  // ready for the next call
                 }
             }
         }
         named_barrier(1 + g, 64);
-
-        if (!whole) {
-            // Count this segment in; the last of the request's segments merges.
-            const int c_lo = p0 / per, c_hi = (p1 - 1) / per;
-            named_barrier(kBarConsumers, n_consumers * 32);
-            if (threadIdx.x == 0) {
-                const int prev = atomicAdd(a.arrivals + b, 1);
-                *merge_here = (prev == c_hi - c_lo);
-            }
-            named_barrier(kBarConsumers, n_consumers * 32);
-            if (*merge_here) {
-                __threadfence();
-                for (int h = warp; h < hq; h += n_consumers) {
-                    float mm = -INFINITY, ls = 0.f, o[4] = {0.f, 0.f, 0.f, 0.f};
-                    for (int c = c_lo; c <= c_hi; ++c) {
-                        const size_t r = (size_t)(c + b) * hq + h;
-                        const float mc = __ldcg(a.part_ml + r * 2), lc = __ldcg(a.part_ml + r * 2 + 1);
-                        const float4 v = __ldcg(reinterpret_cast<const float4 *>(a.part_acc + r * kD + 4 * lane));
-                        const float mn = fmaxf(mm, mc);
-                        if (mn == -INFINITY) continue;
-                        const float so = exp2_approx(mm - mn), sn = exp2_approx(mc - mn);
-                        ls = ls * so + lc * sn;
-                        o[0] = o[0] * so + v.x * sn;
-                        o[1] = o[1] * so + v.y * sn;
-                        o[2] = o[2] * so + v.z * sn;
-                        o[3] = o[3] * so + v.w * sn;
-                        mm = mn;
-                    }
-                    const float inv = ls > 0.f ? 1.f / ls : 0.f;
-                    uint2 w;
-                    w.x = pack_bf16x2(o[0] * inv, o[1] * inv);
-                    w.y = pack_bf16x2(o[2] * inv, o[3] * inv);
-                    *reinterpret_cast<uint2 *>(a.out + ((size_t)b * hq + h) * kD + 4 * lane) = w;
-                }
-                if (threadIdx.x == 0) a.arrivals[b] = 0;  // ready for the next call
-            }
-        }
     }
 }
 

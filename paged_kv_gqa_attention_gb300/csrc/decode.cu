@@ -26,8 +26,9 @@
 //
 // Inside a CTA.  One producer warp streams whole pages (K page and V page,
 // 16 tokens x Hkv heads x 128 dims of bf16 each, contiguous in the pool) into
-// a ring of shared-memory stages with the bulk-copy engine, completing on an
-// mbarrier per stage; its lanes fetch the page ids 32 at a time.  2*Hkv
+// a ring of shared-memory stages with the bulk-copy engine; the K page and the
+// V page of a stage complete on separate mbarriers, so scores start while V
+// is still in flight.  The producer's lanes fetch the page ids 32 at a time.  2*Hkv
 // consumer warps share each stage: warp (g, half) handles KV head g for tokens
 // [8*half, 8*half + 8) of the page and both query heads of that KV head (GQA
 // sharing).  Lane l owns dims [4l, 4l + 4): it forms partial dot products
@@ -91,8 +92,8 @@ __host__ __device__ inline SmemLayout smem_layout(int hkv, int batch, int group)
     s.page_bytes = kPS * hkv * kD * 2;
     s.stage_bytes = 2 * s.page_bytes;
     uint32_t o = kStages * s.stage_bytes;
-    s.off_bar = o;
-    o += 2 * kStages * 8;
+    s.off_bar = o;  // full_k[kStages], full_v[kStages], empty[kStages]
+    o += 3 * kStages * 8;
     s.off_flag = o;  // page_ok[kStages]
     o += kStages * 4;
     o = (o + 15) & ~15u;
@@ -136,6 +137,12 @@ __device__ __forceinline__ int first_request_past(const int *prefix, int batch, 
     return l;
 }
 
+__device__ __forceinline__ int atom_add_acq_rel_gpu(int *p, int v) {
+    int old;
+    asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
 __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
     uint64_t d;
     asm("fma.rn.f32x2 %0, %1, %2, %3;"
@@ -160,8 +167,9 @@ __global__ void __launch_bounds__((2 * kMaxHkv + 1) * 32, 1) decode_splitk_kerne
 
     int *prefix = reinterpret_cast<int *>(smem + L.off_prefix);
     int *page_ok = reinterpret_cast<int *>(smem + L.off_flag);
-    const uint32_t bar_full = smem_u32(smem + L.off_bar);
-    const uint32_t bar_empty = bar_full + kStages * 8;
+    const uint32_t bar_full_k = smem_u32(smem + L.off_bar);
+    const uint32_t bar_full_v = bar_full_k + kStages * 8;
+    const uint32_t bar_empty = bar_full_v + kStages * 8;
 
     // Prefix sums of page counts over requests (warp 0), barrier init.
     if (warp == 0) {
@@ -180,7 +188,8 @@ __global__ void __launch_bounds__((2 * kMaxHkv + 1) * 32, 1) decode_splitk_kerne
         }
         if (lane == 0) {
             for (int s = 0; s < kStages; ++s) {
-                mbar_init(bar_full + 8 * s, 1);
+                mbar_init(bar_full_k + 8 * s, 1);
+                mbar_init(bar_full_v + 8 * s, 1);
                 mbar_init(bar_empty + 8 * s, n_consumers);
             }
             fence_mbar_init();
@@ -233,14 +242,16 @@ __global__ void __launch_bounds__((2 * kMaxHkv + 1) * 32, 1) decode_splitk_kerne
                         if (page < 0 || page >= a.num_pages) {
                             atomicOr(&g_status, QA_DEVICE_BAD_PAGE);
                             page_ok[s] = 0;
-                            mbar_arrive(bar_full + 8 * s);
+                            mbar_arrive(bar_full_k + 8 * s);
+                            mbar_arrive(bar_full_v + 8 * s);
                         } else {
                             page_ok[s] = 1;
-                            mbar_arrive_expect_tx(bar_full + 8 * s, L.stage_bytes);
                             const size_t off = (size_t)page * L.page_bytes;
-                            bulk_g2s_hint(smem_u32(dst), a.k_pages + off, L.page_bytes, bar_full + 8 * s, policy);
+                            mbar_arrive_expect_tx(bar_full_k + 8 * s, L.page_bytes);
+                            bulk_g2s_hint(smem_u32(dst), a.k_pages + off, L.page_bytes, bar_full_k + 8 * s, policy);
+                            mbar_arrive_expect_tx(bar_full_v + 8 * s, L.page_bytes);
                             bulk_g2s_hint(smem_u32(dst + L.page_bytes), a.v_pages + off, L.page_bytes,
-                                          bar_full + 8 * s, policy);
+                                          bar_full_v + 8 * s, policy);
                         }
                     }
                     __syncwarp();
@@ -286,7 +297,8 @@ __global__ void __launch_bounds__((2 * kMaxHkv + 1) * 32, 1) decode_splitk_kerne
 
         for (int j = j0; j < j1; ++j, ++it) {
             const int s = it % kStages;
-            mbar_wait(bar_full + 8 * s, (it / kStages) & 1, &g_status);
+            const uint32_t phase = (it / kStages) & 1;
+            mbar_wait(bar_full_k + 8 * s, phase, &g_status);
             const int n_valid = min(kPS, seq_len - j * kPS);
             const int t0 = half * 8;
             const int nt = min(8, n_valid - t0);
@@ -353,6 +365,7 @@ __global__ void __launch_bounds__((2 * kMaxHkv + 1) * 32, 1) decode_splitk_kerne
                 __syncwarp();
                 if (p_writer) pbuf[GROUP == 2 ? (lane >> 1) : (lane >> 2)] = make_float2(p, p);
                 __syncwarp();
+                mbar_wait(bar_full_v + 8 * s, phase, &g_status);
                 if (nt == 8) {
 #pragma unroll
                     for (int t = 0; t < 8; ++t) {
@@ -377,6 +390,8 @@ __global__ void __launch_bounds__((2 * kMaxHkv + 1) * 32, 1) decode_splitk_kerne
                         }
                     }
                 }
+            } else {
+                mbar_wait(bar_full_v + 8 * s, phase, &g_status);  // the stage is reused only once V landed
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_empty + 8 * s);
@@ -458,13 +473,13 @@ __global__ void __launch_bounds__((2 * kMaxHkv + 1) * 32, 1) decode_splitk_kerne
             if (!whole) {
                 // Count this partial in; the last arriving warp of (b, g) merges.
                 const int c_lo = p0 / per, c_hi = (p1 - 1) / per;
-                __threadfence();
+                // the warp barrier orders every lane's partial before lane 0's
+                // release; lane 0's acquire orders the reads below after it
                 __syncwarp();
                 int prev = 0;
-                if (lane == 0) prev = atomicAdd(a.arrivals + (size_t)b * kMaxHkv + g, 1);
+                if (lane == 0) prev = atom_add_acq_rel_gpu(a.arrivals + (size_t)b * kMaxHkv + g, 1);
                 prev = __shfl_sync(0xffffffffu, prev, 0);
                 if (prev == c_hi - c_lo) {
-                    __threadfence();
 #pragma unroll
                     for (int i = 0; i < GROUP; ++i) {
                         const int h = g * GROUP + i;

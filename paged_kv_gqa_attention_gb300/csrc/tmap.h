@@ -1,6 +1,7 @@
-// Host helper: tiled TMA descriptors for packed [T][H][D] bf16 tensors, with
-// boxes of 128 rows x 64 dims of one head and 128-byte swizzling (the operand
-// layout of the tensor-core attention kernels).
+// Host helpers of the tensor-core attention launches: tiled TMA descriptors
+// for packed [T][H][D] bf16 tensors (boxes of 128 rows x 64 dims of one head,
+// 128-byte swizzling: the operand layout of attn_tc.cuh) and the persistent
+// grid size.
 #pragma once
 
 #include <cuda.h>
@@ -36,6 +37,15 @@ inline bool make_rows_tmap(CUtensorMap *map, const void *base, int D, int H, int
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
+}
+
+// Persistent grid size: one CTA per SM of the current device, no more CTAs
+// than jobs.  0 when no device answers.
+inline int persistent_grid(int n_items) {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) return 0;
+    return n_items < sms ? (n_items > 0 ? n_items : 1) : sms;
 }
 
 }  // namespace qa

@@ -7,10 +7,10 @@
 //
 // Attention: row i of request r attends over rows j <= i of the same request
 // (same section: attend over [0, n_past + T)), GQA group h / 2, from the
-// packed k and v, on the tensor cores (attn_tc.cuh): jobs are (request,
-// 128-row query tile, query head) with causal key tiles 0..tile, walked by a
-// persistent grid of one CTA per SM; the two query heads of a KV head are
-// adjacent in the job order, so their K/V tiles are fetched from L2 once.
+// packed k and v, on the tensor cores (attn_tc.cuh): one CTA per (128-row
+// query tile, query head, request) with causal key tiles 0..tile; the two
+// query heads of a KV head are adjacent in launch order, so their K/V tiles
+// come from L2 the second time.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -111,21 +111,17 @@ cudaError_t launch_prefill(const void *q, const void *k, const void *v, const in
     // a request holds at most max_pages_per_seq * page_size rows
     const long long max_len = (long long)p.max_pages_per_seq * p.page_size;
     const long long qtiles = (max_len + 127) / 128;
-    const long long items = (long long)batch * qtiles * p.n_q_heads;
-    if (items > 0x7fffffffLL) return cudaErrorInvalidValue;
-    a.qtiles = (int)qtiles;
-    a.n_items = (int)items;
-    const int grid = persistent_grid(a.n_items);
-    if (grid <= 0) return cudaErrorInvalidDevice;
+    if (qtiles > 0x7fffffffLL) return cudaErrorInvalidValue;
+    const dim3 grid((unsigned)qtiles, p.n_q_heads, batch);
     constexpr uint32_t smem = AttnTcLayout<128>::kSmem;
     if (p.n_q_heads == 2 * p.n_kv_heads) {
         e = cudaFuncSetAttribute(attn_tc_kernel<128, 2, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
-        attn_tc_kernel<128, 2, true><<<grid, 192, smem, stream>>>(tq, tk, tv, a, status);
+        attn_tc_kernel<128, 2, true><<<grid, 128, smem, stream>>>(tq, tk, tv, a, status);
     } else {
         e = cudaFuncSetAttribute(attn_tc_kernel<128, 1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
-        attn_tc_kernel<128, 1, true><<<grid, 192, smem, stream>>>(tq, tk, tv, a, status);
+        attn_tc_kernel<128, 1, true><<<grid, 128, smem, stream>>>(tq, tk, tv, a, status);
     }
     return cudaGetLastError();
 }

@@ -5,10 +5,9 @@
 // bidirectional MHA scaled by 1/sqrt(head_dim).  M* "Speech recognition:
 // Whisper and Qwen3-ASR", "Graph": one packed forward per batch with one
 // segment per window of every request.  Row t of window w attends over every
-// row of w and nothing else.  Runs on the tensor cores (attn_tc.cuh): jobs
-// are (window, head), walked by a persistent grid of one CTA per SM; a
-// 104-token window is one 128-row tile, longer windows loop over query and key
-// tiles inside their job.
+// row of w and nothing else.  Runs on the tensor cores (attn_tc.cuh): one CTA
+// per (window, head), four CTAs per SM; a 104-token window is one 128-row
+// tile, longer windows loop over query and key tiles.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -42,22 +41,17 @@ cudaError_t launch_window(const void *q, const void *k, const void *v, const int
     unsigned int *status = nullptr;
     cudaError_t e = cudaGetSymbolAddress(reinterpret_cast<void **>(&status), g_status);
     if (e != cudaSuccess) return e;
-    const long long items = (long long)n_windows * p.n_q_heads;
-    if (items > 0x7fffffffLL) return cudaErrorInvalidValue;
-    a.qtiles = 1;
-    a.n_items = (int)items;
-    const int grid = persistent_grid(a.n_items);
-    if (grid <= 0) return cudaErrorInvalidDevice;
+    const dim3 grid(n_windows, p.n_q_heads);
     if (p.head_dim == 64) {
         constexpr uint32_t smem = AttnTcLayout<64>::kSmem;
         e = cudaFuncSetAttribute(attn_tc_kernel<64, 1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
-        attn_tc_kernel<64, 1, false><<<grid, 192, smem, stream>>>(tq, tk, tv, a, status);
+        attn_tc_kernel<64, 1, false><<<grid, 128, smem, stream>>>(tq, tk, tv, a, status);
     } else {
         constexpr uint32_t smem = AttnTcLayout<128>::kSmem;
         e = cudaFuncSetAttribute(attn_tc_kernel<128, 1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
-        attn_tc_kernel<128, 1, false><<<grid, 192, smem, stream>>>(tq, tk, tv, a, status);
+        attn_tc_kernel<128, 1, false><<<grid, 128, smem, stream>>>(tq, tk, tv, a, status);
     }
     return cudaGetLastError();
 }

@@ -29,14 +29,15 @@
 // a ring of shared-memory stages with the bulk-copy engine; the K page and the
 // V page of a stage complete on separate mbarriers, so scores start while V
 // is still in flight.  The producer's lanes fetch the page ids 32 at a time.  2*Hkv
-// consumer warps share each stage: warp (g, half) handles KV head g for tokens
-// [8*half, 8*half + 8) of the page and both query heads of that KV head (GQA
-// sharing).  Lane l owns dims [4l, 4l + 4): it forms partial dot products
-// for the 16 (token, head) pairs with packed fp32 FMAs, a butterfly
-// reduce-scatter over the warp leaves each pair's full score on two lanes,
-// so each lane runs one exponential of the fp32 online softmax, and the
-// probabilities reach every lane through 128 bytes of shared memory for the
-// P V update.
+// consumer warps take the pages in turn: warp (g, half) handles KV head g of
+// every other page (all 16 tokens) and both query heads of that KV head (GQA
+// sharing).  Lane l owns dims [4l, 4l + 4): it forms partial dot products for
+// the 32 (token, head) pairs with packed fp32 FMAs, a butterfly
+// reduce-scatter over the warp leaves pair l's full score on lane l, so each
+// lane runs one exponential of the fp32 online softmax, and the probabilities
+// reach every lane through 256 bytes of shared memory for the P V update.
+// The two warps of a KV head keep separate running states and merge them at
+// the end of the segment.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -102,8 +103,8 @@ __host__ __device__ inline SmemLayout smem_layout(int hkv, int batch, int group)
     o = (o + 15) & ~15u;
     s.off_merge = o;
     o += hkv * group * kRec * 4;
-    s.off_pbuf = o;  // 16 float2 per consumer warp
-    o += 2 * hkv * 16 * 8;
+    s.off_pbuf = o;  // 32 float2 per consumer warp
+    o += 2 * hkv * 32 * 8;
     s.total = o;
     return s;
 }
@@ -190,7 +191,7 @@ __global__ void __launch_bounds__((2 * kMaxHkv + 1) * 32, 1) decode_splitk_kerne
             for (int s = 0; s < kStages; ++s) {
                 mbar_init(bar_full_k + 8 * s, 1);
                 mbar_init(bar_full_v + 8 * s, 1);
-                mbar_init(bar_empty + 8 * s, n_consumers);
+                mbar_init(bar_empty + 8 * s, a.hkv);  // the warps of one parity release a stage
             }
             fence_mbar_init();
         }
@@ -262,16 +263,18 @@ __global__ void __launch_bounds__((2 * kMaxHkv + 1) * 32, 1) decode_splitk_kerne
     }
 
     // ---------------- consumer warps
+    // Warp (g, half) takes KV head g of every other page of the CTA's list
+    // (pages with it % 2 == half), all 16 tokens of it.
     const int g = warp >> 1, half = warp & 1;
     float *merge = reinterpret_cast<float *>(smem + L.off_merge) + g * GROUP * kRec;
-    float2 *pbuf = reinterpret_cast<float2 *>(smem + L.off_pbuf) + warp * 16;
-    // After the reduce-scatter lane l holds the score of token my_t of this
-    // warp's 8 and query head my_h of the group (lanes l, l ^ 1 agree).
-    constexpr int NV = 8 * GROUP;          // (token, head) pairs per warp and page
-    constexpr int LOG = GROUP == 2 ? 4 : 3;
-    const int my_t = lane >> 2;
-    const int my_h = GROUP == 2 ? (lane >> 1) & 1 : 0;
-    const bool p_writer = GROUP == 2 ? (lane & 1) == 0 : (lane & 3) == 0;
+    float2 *pbuf = reinterpret_cast<float2 *>(smem + L.off_pbuf) + warp * 32;
+    // After the reduce-scatter lane l holds the score of (token my_t, query
+    // head my_h of the group); with GROUP == 1 lanes l and l ^ 1 agree.
+    constexpr int NV = 16 * GROUP;  // (token, head) pairs per page
+    constexpr int LOG = GROUP == 2 ? 5 : 4;
+    const int my_t = lane >> 1;
+    const int my_h = GROUP == 2 ? lane & 1 : 0;
+    const bool p_writer = GROUP == 2 ? true : (lane & 1) == 0;
     int it = 0;
     for (int k = 0; k < n_visit; ++k) {
         const int b = k == 0 ? b_last : b0 + k - 1;
@@ -296,21 +299,20 @@ __global__ void __launch_bounds__((2 * kMaxHkv + 1) * 32, 1) decode_splitk_kerne
         float m_own = -INFINITY, l_own = 0.f;
 
         for (int j = j0; j < j1; ++j, ++it) {
+            if ((it & 1) != half) continue;  // the other warp of the pair takes this page
             const int s = it % kStages;
             const uint32_t phase = (it / kStages) & 1;
             mbar_wait(bar_full_k + 8 * s, phase, &g_status);
-            const int n_valid = min(kPS, seq_len - j * kPS);
-            const int t0 = half * 8;
-            const int nt = min(8, n_valid - t0);
+            const int nt = min(kPS, seq_len - j * kPS);
             if (page_ok[s] && nt > 0) {
-                const uint8_t *Ks = smem + s * L.stage_bytes + ((t0 * a.hkv + g) * kD + 4 * lane) * 2;
+                const uint8_t *Ks = smem + s * L.stage_bytes + (g * kD + 4 * lane) * 2;
                 const uint8_t *Vs = Ks + L.page_bytes;
                 const int row_stride = a.hkv * kD * 2;
                 // partial dots of every (token, head); rows past the sequence
                 // (sentinels, possibly NaN) only ever touch their own entry
                 float v[NV];
 #pragma unroll
-                for (int t = 0; t < 8; ++t) {
+                for (int t = 0; t < kPS; ++t) {
                     float2 k01, k23;
                     bf16x4(*reinterpret_cast<const uint2 *>(Ks + t * row_stride), k01, k23);
 #pragma unroll
@@ -332,14 +334,12 @@ __global__ void __launch_bounds__((2 * kMaxHkv + 1) * 32, 1) decode_splitk_kerne
                         v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
                     }
                 }
-#pragma unroll
-                for (int off = 16 >> LOG; off > 0; off >>= 1) v[0] += __shfl_xor_sync(0xffffffffu, v[0], off);
+                if (GROUP == 1) v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
                 const float sc = my_t < nt ? v[0] : -INFINITY;
-                // online softmax of this lane's query head
+                // online softmax of this lane's query head (max over the 16 token lanes)
                 float tmax = sc;
-                tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 4));
-                tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 8));
-                tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 16));
+#pragma unroll
+                for (int off = 2; off < 32; off <<= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, off));
                 const float m_new = fmaxf(m_own, tmax);
                 const float alpha_own = exp2_approx(m_own - m_new);
                 const float p = exp2_approx(sc - m_new);
@@ -347,7 +347,7 @@ __global__ void __launch_bounds__((2 * kMaxHkv + 1) * 32, 1) decode_splitk_kerne
                 m_own = m_new;
                 float alpha[GROUP];
                 if (GROUP == 2) {
-                    const float other = __shfl_xor_sync(0xffffffffu, alpha_own, 2);
+                    const float other = __shfl_xor_sync(0xffffffffu, alpha_own, 1);
                     alpha[0] = my_h == 0 ? alpha_own : other;
                     alpha[GROUP - 1] = my_h == 1 ? alpha_own : other;
                 } else {
@@ -363,12 +363,12 @@ __global__ void __launch_bounds__((2 * kMaxHkv + 1) * 32, 1) decode_splitk_kerne
                     }
                 }
                 __syncwarp();
-                if (p_writer) pbuf[GROUP == 2 ? (lane >> 1) : (lane >> 2)] = make_float2(p, p);
+                if (p_writer) pbuf[GROUP == 2 ? lane : (lane >> 1)] = make_float2(p, p);
                 __syncwarp();
                 mbar_wait(bar_full_v + 8 * s, phase, &g_status);
-                if (nt == 8) {
+                if (nt == kPS) {
 #pragma unroll
-                    for (int t = 0; t < 8; ++t) {
+                    for (int t = 0; t < kPS; ++t) {
                         float2 v01, v23;
                         bf16x4(*reinterpret_cast<const uint2 *>(Vs + t * row_stride), v01, v23);
 #pragma unroll
@@ -397,16 +397,16 @@ __global__ void __launch_bounds__((2 * kMaxHkv + 1) * 32, 1) decode_splitk_kerne
             if (lane == 0) mbar_arrive(bar_empty + 8 * s);
         }
 
-        // Sum of probabilities per query head (over the 8 token lanes), and
-        // both heads' (m, l) on every lane.
+        // Sum of probabilities per query head over its 16 token lanes (bit 0
+        // of the lane is the head, or a duplicate when GROUP == 1), and both
+        // heads' (m, l) on every lane.
         float l_head = l_own;
-        l_head += __shfl_xor_sync(0xffffffffu, l_head, 4);
-        l_head += __shfl_xor_sync(0xffffffffu, l_head, 8);
-        l_head += __shfl_xor_sync(0xffffffffu, l_head, 16);
+#pragma unroll
+        for (int off = 2; off < 32; off <<= 1) l_head += __shfl_xor_sync(0xffffffffu, l_head, off);
         float m[GROUP], l[GROUP], acc[GROUP][4];
         if (GROUP == 2) {
-            const float m_other = __shfl_xor_sync(0xffffffffu, m_own, 2);
-            const float l_other = __shfl_xor_sync(0xffffffffu, l_head, 2);
+            const float m_other = __shfl_xor_sync(0xffffffffu, m_own, 1);
+            const float l_other = __shfl_xor_sync(0xffffffffu, l_head, 1);
             m[0] = my_h == 0 ? m_own : m_other;
             l[0] = my_h == 0 ? l_head : l_other;
             m[GROUP - 1] = my_h == 1 ? m_own : m_other;

@@ -28,16 +28,15 @@
 // 16 tokens x Hkv heads x 128 dims of bf16 each, contiguous in the pool) into
 // a ring of shared-memory stages with the bulk-copy engine; the K page and the
 // V page of a stage complete on separate mbarriers, so scores start while V
-// is still in flight.  The producer's lanes fetch the page ids 32 at a time.  2*Hkv
-// consumer warps take the pages in turn: warp (g, half) handles KV head g of
-// every other page (all 16 tokens) and both query heads of that KV head (GQA
-// sharing).  Lane l owns dims [4l, 4l + 4): it forms partial dot products for
+// is still in flight.  The producer's lanes fetch the page ids 32 at a time.
+// Hkv consumer warps share every stage: warp g handles KV head g of the page
+// (all 16 tokens) and both query heads of that KV head (GQA sharing).  Lane l owns dims [4l, 4l + 4): it forms partial dot products for
 // the 32 (token, head) pairs with packed fp32 FMAs, a butterfly
 // reduce-scatter over the warp leaves pair l's full score on lane l, so each
 // lane runs one exponential of the fp32 online softmax, and the probabilities
 // reach every lane through 256 bytes of shared memory for the P V update.
-// The two warps of a KV head keep separate running states and merge them at
-// the end of the segment.
+// Every consumer waits on every stage it reads, in order, so no mbarrier
+// phase is ever skipped.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -53,9 +52,6 @@ constexpr int kD = 128;
 constexpr int kPS = 16;
 constexpr int kStages = 3;
 constexpr int kMaxHkv = 8;
-// Merge record of one query head in shared memory: m, l, two pad words (so
-// the accumulator starts on a 16-byte boundary), then acc[kD].
-constexpr int kRec = 4 + kD;
 
 struct DecodeArgs {
     const uint16_t *q;
@@ -85,7 +81,7 @@ __device__ __forceinline__ int pages_of(const DecodeArgs &a, int b, bool report)
 struct SmemLayout {
     uint32_t stage_bytes;  // one stage: K page + V page
     uint32_t page_bytes;
-    uint32_t off_bar, off_flag, off_prefix, off_merge, off_pbuf, total;
+    uint32_t off_bar, off_flag, off_prefix, off_pbuf, total;
 };
 
 __host__ __device__ inline SmemLayout smem_layout(int hkv, int batch, int group) {
@@ -101,10 +97,8 @@ __host__ __device__ inline SmemLayout smem_layout(int hkv, int batch, int group)
     s.off_prefix = o;
     o += (batch + 1) * 4;
     o = (o + 15) & ~15u;
-    s.off_merge = o;
-    o += hkv * group * kRec * 4;
     s.off_pbuf = o;  // 32 float2 per consumer warp
-    o += 2 * hkv * 32 * 8;
+    o += hkv * 32 * 8;
     s.total = o;
     return s;
 }
@@ -159,11 +153,11 @@ __device__ __forceinline__ void bf16x4(uint2 w, float2 &lo, float2 &hi) {
 }
 
 template <int GROUP>
-__global__ void __launch_bounds__((2 * kMaxHkv + 1) * 32, 1) decode_splitk_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__((kMaxHkv + 1) * 32, 1) decode_splitk_kernel(const DecodeArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
     const SmemLayout L = smem_layout(a.hkv, a.batch, GROUP);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n_consumers = 2 * a.hkv;
+    const int n_consumers = a.hkv;
     const int hq = a.hkv * GROUP;
 
     int *prefix = reinterpret_cast<int *>(smem + L.off_prefix);
@@ -191,7 +185,7 @@ __global__ void __launch_bounds__((2 * kMaxHkv + 1) * 32, 1) decode_splitk_kerne
             for (int s = 0; s < kStages; ++s) {
                 mbar_init(bar_full_k + 8 * s, 1);
                 mbar_init(bar_full_v + 8 * s, 1);
-                mbar_init(bar_empty + 8 * s, a.hkv);  // the warps of one parity release a stage
+                mbar_init(bar_empty + 8 * s, n_consumers);
             }
             fence_mbar_init();
         }
@@ -262,11 +256,8 @@ __global__ void __launch_bounds__((2 * kMaxHkv + 1) * 32, 1) decode_splitk_kerne
         return;
     }
 
-    // ---------------- consumer warps
-    // Warp (g, half) takes KV head g of every other page of the CTA's list
-    // (pages with it % 2 == half), all 16 tokens of it.
-    const int g = warp >> 1, half = warp & 1;
-    float *merge = reinterpret_cast<float *>(smem + L.off_merge) + g * GROUP * kRec;
+    // ---------------- consumer warps: warp g takes KV head g of every page
+    const int g = warp;
     float2 *pbuf = reinterpret_cast<float2 *>(smem + L.off_pbuf) + warp * 32;
     // After the reduce-scatter lane l holds the score of (token my_t, query
     // head my_h of the group); with GROUP == 1 lanes l and l ^ 1 agree.
@@ -299,7 +290,6 @@ __global__ void __launch_bounds__((2 * kMaxHkv + 1) * 32, 1) decode_splitk_kerne
         float m_own = -INFINITY, l_own = 0.f;
 
         for (int j = j0; j < j1; ++j, ++it) {
-            if ((it & 1) != half) continue;  // the other warp of the pair takes this page
             const int s = it % kStages;
             const uint32_t phase = (it / kStages) & 1;
             mbar_wait(bar_full_k + 8 * s, phase, &g_status);
@@ -423,92 +413,63 @@ __global__ void __launch_bounds__((2 * kMaxHkv + 1) * 32, 1) decode_splitk_kerne
             acc[i][3] = acc23[i].y;
         }
 
-        // Merge the two halves of KV head g through shared memory.
-        if (half == 1) {
+        const bool whole = (j0 == 0 && j1 == p1 - p0);
+        const int slot = blockIdx.x + b;
 #pragma unroll
-            for (int i = 0; i < GROUP; ++i) {
-                float *mr = merge + i * kRec;
+        for (int i = 0; i < GROUP; ++i) {
+            const int h = g * GROUP + i;
+            if (whole) {
+                const float inv = l[i] > 0.f ? 1.f / l[i] : 0.f;
+                uint2 w;
+                w.x = pack_bf16x2(acc[i][0] * inv, acc[i][1] * inv);
+                w.y = pack_bf16x2(acc[i][2] * inv, acc[i][3] * inv);
+                *reinterpret_cast<uint2 *>(a.out + ((size_t)b * hq + h) * kD + 4 * lane) = w;
+            } else {
+                *reinterpret_cast<float4 *>(a.part_acc + ((size_t)slot * hq + h) * kD + 4 * lane) =
+                    make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
                 if (lane == 0) {
-                    mr[0] = m[i];
-                    mr[1] = l[i];
+                    a.part_ml[((size_t)slot * hq + h) * 2 + 0] = m[i];
+                    a.part_ml[((size_t)slot * hq + h) * 2 + 1] = l[i];
                 }
-                *reinterpret_cast<float4 *>(mr + 4 + 4 * lane) = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
             }
         }
-        named_barrier(1 + g, 64);
-        if (half == 0) {
-            const bool whole = (j0 == 0 && j1 == p1 - p0);
-            const int slot = blockIdx.x + b;
+        if (!whole) {
+            // Count this partial in; the last arriving warp of (b, g) merges.
+            const int c_lo = p0 / per, c_hi = (p1 - 1) / per;
+            // the warp barrier orders every lane's partial before lane 0's
+            // release; lane 0's acquire orders the reads below after it
+            __syncwarp();
+            int prev = 0;
+            if (lane == 0) prev = atom_add_acq_rel_gpu(a.arrivals + (size_t)b * kMaxHkv + g, 1);
+            prev = __shfl_sync(0xffffffffu, prev, 0);
+            if (prev == c_hi - c_lo) {
 #pragma unroll
-            for (int i = 0; i < GROUP; ++i) {
-                const float *mr = merge + i * kRec;
-                const float m1 = mr[0], l1 = mr[1];
-                const float4 a1 = *reinterpret_cast<const float4 *>(mr + 4 + 4 * lane);
-                const float mm = fmaxf(m[i], m1);
-                float ls = 0.f, o[4] = {0.f, 0.f, 0.f, 0.f};
-                if (mm != -INFINITY) {
-                    const float c0 = exp2_approx(m[i] - mm), c1 = exp2_approx(m1 - mm);
-                    ls = l[i] * c0 + l1 * c1;
-                    o[0] = acc[i][0] * c0 + a1.x * c1;
-                    o[1] = acc[i][1] * c0 + a1.y * c1;
-                    o[2] = acc[i][2] * c0 + a1.z * c1;
-                    o[3] = acc[i][3] * c0 + a1.w * c1;
-                }
-                const int h = g * GROUP + i;
-                if (whole) {
+                for (int i = 0; i < GROUP; ++i) {
+                    const int h = g * GROUP + i;
+                    float mm = -INFINITY, ls = 0.f, o[4] = {0.f, 0.f, 0.f, 0.f};
+                    for (int c = c_lo; c <= c_hi; ++c) {
+                        const size_t r = (size_t)(c + b) * hq + h;
+                        const float mc = __ldcg(a.part_ml + r * 2), lc = __ldcg(a.part_ml + r * 2 + 1);
+                        const float4 pv = __ldcg(reinterpret_cast<const float4 *>(a.part_acc + r * kD + 4 * lane));
+                        const float mn = fmaxf(mm, mc);
+                        if (mn == -INFINITY) continue;
+                        const float so = exp2_approx(mm - mn), sn = exp2_approx(mc - mn);
+                        ls = ls * so + lc * sn;
+                        o[0] = o[0] * so + pv.x * sn;
+                        o[1] = o[1] * so + pv.y * sn;
+                        o[2] = o[2] * so + pv.z * sn;
+                        o[3] = o[3] * so + pv.w * sn;
+                        mm = mn;
+                    }
                     const float inv = ls > 0.f ? 1.f / ls : 0.f;
                     uint2 w;
                     w.x = pack_bf16x2(o[0] * inv, o[1] * inv);
                     w.y = pack_bf16x2(o[2] * inv, o[3] * inv);
                     *reinterpret_cast<uint2 *>(a.out + ((size_t)b * hq + h) * kD + 4 * lane) = w;
-                } else {
-                    *reinterpret_cast<float4 *>(a.part_acc + ((size_t)slot * hq + h) * kD + 4 * lane) =
-                        make_float4(o[0], o[1], o[2], o[3]);
-                    if (lane == 0) {
-                        a.part_ml[((size_t)slot * hq + h) * 2 + 0] = mm;
-                        a.part_ml[((size_t)slot * hq + h) * 2 + 1] = ls;
-                    }
                 }
-            }
-            if (!whole) {
-                // Count this partial in; the last arriving warp of (b, g) merges.
-                const int c_lo = p0 / per, c_hi = (p1 - 1) / per;
-                // the warp barrier orders every lane's partial before lane 0's
-                // release; lane 0's acquire orders the reads below after it
-                __syncwarp();
-                int prev = 0;
-                if (lane == 0) prev = atom_add_acq_rel_gpu(a.arrivals + (size_t)b * kMaxHkv + g, 1);
-                prev = __shfl_sync(0xffffffffu, prev, 0);
-                if (prev == c_hi - c_lo) {
-#pragma unroll
-                    for (int i = 0; i < GROUP; ++i) {
-                        const int h = g * GROUP + i;
-                        float mm = -INFINITY, ls = 0.f, o[4] = {0.f, 0.f, 0.f, 0.f};
-                        for (int c = c_lo; c <= c_hi; ++c) {
-                            const size_t r = (size_t)(c + b) * hq + h;
-                            const float mc = __ldcg(a.part_ml + r * 2), lc = __ldcg(a.part_ml + r * 2 + 1);
-                            const float4 pv = __ldcg(reinterpret_cast<const float4 *>(a.part_acc + r * kD + 4 * lane));
-                            const float mn = fmaxf(mm, mc);
-                            if (mn == -INFINITY) continue;
-                            const float so = exp2_approx(mm - mn), sn = exp2_approx(mc - mn);
-                            ls = ls * so + lc * sn;
-                            o[0] = o[0] * so + pv.x * sn;
-                            o[1] = o[1] * so + pv.y * sn;
-                            o[2] = o[2] * so + pv.z * sn;
-                            o[3] = o[3] * so + pv.w * sn;
-                            mm = mn;
-                        }
-                        const float inv = ls > 0.f ? 1.f / ls : 0.f;
-                        uint2 w;
-                        w.x = pack_bf16x2(o[0] * inv, o[1] * inv);
-                        w.y = pack_bf16x2(o[2] * inv, o[3] * inv);
-                        *reinterpret_cast<uint2 *>(a.out + ((size_t)b * hq + h) * kD + 4 * lane) = w;
-                    }
-                    if (lane == 0) a.arrivals[(size_t)b * kMaxHkv + g] = 0;  // ready for the next call
-                }
+                if (lane == 0) a.arrivals[(size_t)b * kMaxHkv + g] = 0;  // ready for the next call
             }
         }
-        named_barrier(1 + g, 64);
     }
 }
 
@@ -549,7 +510,7 @@ cudaError_t launch_decode(const void *q, const void *k_pages, const void *v_page
     a.scale_log2 = scale * kLog2e;
 
     const SmemLayout L = smem_layout(a.hkv, batch, group);
-    const int threads = (2 * a.hkv + 1) * 32;
+    const int threads = (a.hkv + 1) * 32;
     cudaError_t e;
     if (group == 2) {
         e = cudaFuncSetAttribute(decode_splitk_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);

@@ -166,6 +166,12 @@ __global__ void __launch_bounds__((kMaxHkv + 1) * 32, 1) decode_splitk_kernel(co
     const uint32_t bar_full_v = bar_full_k + kStages * 8;
     const uint32_t bar_empty = bar_full_v + kStages * 8;
 
+    // Launched as a programmatic dependent: wait for the previous kernel on the
+    // stream to finish (and its writes to land) before touching global
+    // memory, and let the next one start its own prologue early.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
     // Prefix sums of page counts over requests (warp 0), barrier init.
     if (warp == 0) {
         int carry = 0;
@@ -446,20 +452,25 @@ __global__ void __launch_bounds__((kMaxHkv + 1) * 32, 1) decode_splitk_kernel(co
 #pragma unroll
                 for (int i = 0; i < GROUP; ++i) {
                     const int h = g * GROUP + i;
-                    float mm = -INFINITY, ls = 0.f, o[4] = {0.f, 0.f, 0.f, 0.f};
-                    for (int c = c_lo; c <= c_hi; ++c) {
-                        const size_t r = (size_t)(c + b) * hq + h;
-                        const float mc = __ldcg(a.part_ml + r * 2), lc = __ldcg(a.part_ml + r * 2 + 1);
-                        const float4 pv = __ldcg(reinterpret_cast<const float4 *>(a.part_acc + r * kD + 4 * lane));
-                        const float mn = fmaxf(mm, mc);
-                        if (mn == -INFINITY) continue;
-                        const float so = exp2_approx(mm - mn), sn = exp2_approx(mc - mn);
-                        ls = ls * so + lc * sn;
-                        o[0] = o[0] * so + pv.x * sn;
-                        o[1] = o[1] * so + pv.y * sn;
-                        o[2] = o[2] * so + pv.z * sn;
-                        o[3] = o[3] * so + pv.w * sn;
-                        mm = mn;
+                    // two passes of independent loads: the global max, then
+                    // the weighted sums (no load waits on an earlier result)
+                    float mm = -INFINITY;
+#pragma unroll 4
+                    for (int c = c_lo; c <= c_hi; ++c) mm = fmaxf(mm, __ldcg(a.part_ml + ((size_t)(c + b) * hq + h) * 2));
+                    float ls = 0.f, o[4] = {0.f, 0.f, 0.f, 0.f};
+                    if (mm != -INFINITY) {
+#pragma unroll 4
+                        for (int c = c_lo; c <= c_hi; ++c) {
+                            const size_t r = (size_t)(c + b) * hq + h;
+                            const float mc = __ldcg(a.part_ml + r * 2), lc = __ldcg(a.part_ml + r * 2 + 1);
+                            const float4 pv = __ldcg(reinterpret_cast<const float4 *>(a.part_acc + r * kD + 4 * lane));
+                            const float w = exp2_approx(mc - mm);  // 0 for an empty partial (mc = -inf)
+                            ls += w * lc;
+                            o[0] += w * pv.x;
+                            o[1] += w * pv.y;
+                            o[2] += w * pv.z;
+                            o[3] += w * pv.w;
+                        }
                     }
                     const float inv = ls > 0.f ? 1.f / ls : 0.f;
                     uint2 w;
@@ -510,17 +521,23 @@ cudaError_t launch_decode(const void *q, const void *k_pages, const void *v_page
     a.scale_log2 = scale * kLog2e;
 
     const SmemLayout L = smem_layout(a.hkv, batch, group);
-    const int threads = (a.hkv + 1) * 32;
-    cudaError_t e;
-    if (group == 2) {
-        e = cudaFuncSetAttribute(decode_splitk_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
-        if (e != cudaSuccess) return e;
-        decode_splitk_kernel<2><<<ctas, threads, L.total, stream>>>(a);
-    } else {
-        e = cudaFuncSetAttribute(decode_splitk_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
-        if (e != cudaSuccess) return e;
-        decode_splitk_kernel<1><<<ctas, threads, L.total, stream>>>(a);
-    }
+    // programmatic dependent launch: the kernel's prologue overlaps the tail of
+    // the previous kernel on the stream (it waits before touching memory)
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(ctas);
+    cfg.blockDim = dim3((a.hkv + 1) * 32);
+    cfg.dynamicSmemBytes = L.total;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    auto kernel = group == 2 ? decode_splitk_kernel<2> : decode_splitk_kernel<1>;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
+    if (e != cudaSuccess) return e;
+    e = cudaLaunchKernelEx(&cfg, kernel, a);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

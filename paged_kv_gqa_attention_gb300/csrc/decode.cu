@@ -253,6 +253,10 @@ __global__ void __launch_bounds__((kMaxHkv + 1) * 32, 1) decode_splitk_kernel(co
                             mbar_arrive_expect_tx(bar_full_v + 8 * s, L.page_bytes);
                             bulk_g2s_hint(smem_u32(dst + L.page_bytes), a.v_pages + off, L.page_bytes,
                                           bar_full_v + 8 * s, policy);
+                            // Staggered start: every SM asks for its first page
+                            // alone, so the first pages are not interleaved with
+                            // the whole ring's worth of requests of all SMs.
+                            if (it == 0) mbar_wait(bar_full_k, 0, &g_status);
                         }
                     }
                     __syncwarp();

@@ -10,9 +10,9 @@
 // h / group.
 //
 // Work split.  The pages of all requests form one flat list (request-major).
-// A persistent grid of one CTA per SM cuts that list into equal contiguous
-// ranges, so every CTA streams the same number of pages whatever the mix of
-// lengths.  A CTA's range intersects one or more requests; each intersection
+// A persistent grid of one CTA per SM cuts that list into contiguous ranges
+// of floor(T / N) or floor(T / N) + 1 pages, so every CTA streams the same
+// amount whatever the mix of lengths.  A CTA's range intersects one or more requests; each intersection
 // is a "segment".  A segment that holds a whole request writes the final
 // bf16 output.  Otherwise it writes an fp32 partial (running max, running
 // sum, un-normalised accumulator) to slot c + b (CTA c, request b: unique
@@ -132,6 +132,11 @@ __device__ __forceinline__ int first_request_past(const int *prefix, int batch, 
     return l;
 }
 
+// The CTA whose range [c T / N, (c + 1) T / N) holds page x.
+__device__ __forceinline__ int owner_cta(int x, int total, int ncta) {
+    return (int)(((long long)(x + 1) * ncta - 1) / total);
+}
+
 __device__ __forceinline__ int atom_add_acq_rel_gpu(int *p, int v) {
     int old;
     asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
@@ -210,9 +215,11 @@ __global__ void __launch_bounds__((kMaxHkv + 1) * 32, 1) decode_splitk_kernel(co
 
     const int total = prefix[a.batch];
     if (total == 0) return;
-    const int per = (total + gridDim.x - 1) / gridDim.x;
-    const int lo = blockIdx.x * per;
-    const int hi = min(lo + per, total);
+    // CTA c streams pages [c T / N, (c + 1) T / N) of the T pages (N CTAs):
+    // every CTA gets floor(T / N) or one more.
+    const int ncta = gridDim.x;
+    const int lo = (int)((long long)blockIdx.x * total / ncta);
+    const int hi = (int)((long long)(blockIdx.x + 1) * total / ncta);
     if (lo >= hi) return;
 
     // Requests b0 (holding page lo) .. b_last (holding page hi - 1).  Visit
@@ -253,10 +260,6 @@ __global__ void __launch_bounds__((kMaxHkv + 1) * 32, 1) decode_splitk_kernel(co
                             mbar_arrive_expect_tx(bar_full_v + 8 * s, L.page_bytes);
                             bulk_g2s_hint(smem_u32(dst + L.page_bytes), a.v_pages + off, L.page_bytes,
                                           bar_full_v + 8 * s, policy);
-                            // Staggered start: every SM asks for its first page
-                            // alone, so the first pages are not interleaved with
-                            // the whole ring's worth of requests of all SMs.
-                            if (it == 0) mbar_wait(bar_full_k, 0, &g_status);
                         }
                     }
                     __syncwarp();
@@ -445,7 +448,7 @@ __global__ void __launch_bounds__((kMaxHkv + 1) * 32, 1) decode_splitk_kernel(co
         }
         if (!whole) {
             // Count this partial in; the last arriving warp of (b, g) merges.
-            const int c_lo = p0 / per, c_hi = (p1 - 1) / per;
+            const int c_lo = owner_cta(p0, total, ncta), c_hi = owner_cta(p1 - 1, total, ncta);
             // the warp barrier orders every lane's partial before lane 0's
             // release; lane 0's acquire orders the reads below after it
             __syncwarp();

@@ -16,9 +16,9 @@
 // is a "segment".  A segment that holds a whole request writes the final
 // bf16 output.  Otherwise it writes an fp32 partial (running max, running
 // sum, un-normalised accumulator) to slot c + b (CTA c, request b: unique
-// because both ranges are ordered), then counts itself in the arrival counter
-// of (request, KV head); the warp that arrives last merges every partial of
-// its two query heads, writes the output and resets the counter to zero, so
+// because both ranges are ordered), then adds its page count to the arrival
+// counter of (request, KV head); the warp that completes the count merges
+// every partial of its two query heads, writes the output and resets the counter to zero, so
 // nothing ever waits on another CTA and the workspace is left as it was
 // found.  A CTA takes its last segment first and its first segment second:
 // those are the only ones it can share with a neighbour, so partial results
@@ -132,6 +132,11 @@ __device__ __forceinline__ int first_request_past(const int *prefix, int batch, 
     return l;
 }
 
+// First page of CTA c's range: c T / N (rounded down).
+__device__ __forceinline__ int cta_lo(int c, int total, int ncta) {
+    return (int)((long long)c * total / ncta);
+}
+
 // The CTA whose range [c T / N, (c + 1) T / N) holds page x.
 __device__ __forceinline__ int owner_cta(int x, int total, int ncta) {
     return (int)(((long long)(x + 1) * ncta - 1) / total);
@@ -218,8 +223,8 @@ __global__ void __launch_bounds__((kMaxHkv + 1) * 32, 1) decode_splitk_kernel(co
     // CTA c streams pages [c T / N, (c + 1) T / N) of the T pages (N CTAs):
     // every CTA gets floor(T / N) or one more.
     const int ncta = gridDim.x;
-    const int lo = (int)((long long)blockIdx.x * total / ncta);
-    const int hi = (int)((long long)(blockIdx.x + 1) * total / ncta);
+    const int lo = cta_lo(blockIdx.x, total, ncta);
+    const int hi = cta_lo(blockIdx.x + 1, total, ncta);
     if (lo >= hi) return;
 
     // Requests b0 (holding page lo) .. b_last (holding page hi - 1).  Visit
@@ -453,9 +458,11 @@ __global__ void __launch_bounds__((kMaxHkv + 1) * 32, 1) decode_splitk_kernel(co
             // release; lane 0's acquire orders the reads below after it
             __syncwarp();
             int prev = 0;
-            if (lane == 0) prev = atom_add_acq_rel_gpu(a.arrivals + (size_t)b * kMaxHkv + g, 1);
+            // arrivals are counted in pages: the request is complete when all
+            // of its pages are in (CTAs between c_lo and c_hi may hold none)
+            if (lane == 0) prev = atom_add_acq_rel_gpu(a.arrivals + (size_t)b * kMaxHkv + g, j1 - j0);
             prev = __shfl_sync(0xffffffffu, prev, 0);
-            if (prev == c_hi - c_lo) {
+            if (prev + (j1 - j0) == p1 - p0) {
 #pragma unroll
                 for (int i = 0; i < GROUP; ++i) {
                     const int h = g * GROUP + i;
@@ -463,11 +470,15 @@ __global__ void __launch_bounds__((kMaxHkv + 1) * 32, 1) decode_splitk_kernel(co
                     // the weighted sums (no load waits on an earlier result)
                     float mm = -INFINITY;
 #pragma unroll 4
-                    for (int c = c_lo; c <= c_hi; ++c) mm = fmaxf(mm, __ldcg(a.part_ml + ((size_t)(c + b) * hq + h) * 2));
+                    for (int c = c_lo; c <= c_hi; ++c) {
+                        if (cta_lo(c, total, ncta) == cta_lo(c + 1, total, ncta)) continue;  // no pages
+                        mm = fmaxf(mm, __ldcg(a.part_ml + ((size_t)(c + b) * hq + h) * 2));
+                    }
                     float ls = 0.f, o[4] = {0.f, 0.f, 0.f, 0.f};
                     if (mm != -INFINITY) {
 #pragma unroll 4
                         for (int c = c_lo; c <= c_hi; ++c) {
+                            if (cta_lo(c, total, ncta) == cta_lo(c + 1, total, ncta)) continue;
                             const size_t r = (size_t)(c + b) * hq + h;
                             const float mc = __ldcg(a.part_ml + r * 2), lc = __ldcg(a.part_ml + r * 2 + 1);
                             const float4 pv = __ldcg(reinterpret_cast<const float4 *>(a.part_acc + r * kD + 4 * lane));

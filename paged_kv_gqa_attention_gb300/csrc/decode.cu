@@ -52,6 +52,7 @@ constexpr int kD = 128;
 constexpr int kPS = 16;
 constexpr int kStages = 3;
 constexpr int kMaxHkv = 8;
+constexpr int kMaxCtas = 1023;  // grid limit (one CTA per SM)
 
 struct DecodeArgs {
     const uint16_t *q;
@@ -81,7 +82,7 @@ __device__ __forceinline__ int pages_of(const DecodeArgs &a, int b, bool report)
 struct SmemLayout {
     uint32_t stage_bytes;  // one stage: K page + V page
     uint32_t page_bytes;
-    uint32_t off_bar, off_flag, off_prefix, off_pbuf, total;
+    uint32_t off_bar, off_flag, off_prefix, off_pbuf, off_bound, total;
 };
 
 __host__ __device__ inline SmemLayout smem_layout(int hkv, int batch, int group) {
@@ -99,6 +100,8 @@ __host__ __device__ inline SmemLayout smem_layout(int hkv, int batch, int group)
     o = (o + 15) & ~15u;
     s.off_pbuf = o;  // 32 float2 per consumer warp
     o += hkv * 32 * 8;
+    s.off_bound = o;  // first page of every CTA's range, kMaxCtas + 1 entries
+    o += (kMaxCtas + 1) * 4;
     s.total = o;
     return s;
 }
@@ -132,14 +135,15 @@ __device__ __forceinline__ int first_request_past(const int *prefix, int batch, 
     return l;
 }
 
-// First page of CTA c's range: c T / N (rounded down).
-__device__ __forceinline__ int cta_lo(int c, int total, int ncta) {
-    return (int)((long long)c * total / ncta);
-}
-
-// The CTA whose range [c T / N, (c + 1) T / N) holds page x.
-__device__ __forceinline__ int owner_cta(int x, int total, int ncta) {
-    return (int)(((long long)(x + 1) * ncta - 1) / total);
+// The CTA whose range [bound[c], bound[c + 1]) holds page x (the last c with
+// bound[c] <= x; empty ranges share their bound with the next CTA).
+__device__ __forceinline__ int owner_cta(const int *bound, int ncta, int x) {
+    int l = 0, r = ncta - 1;
+    while (l < r) {
+        const int mid = (l + r + 1) >> 1;
+        if (bound[mid] <= x) l = mid; else r = mid - 1;
+    }
+    return l;
 }
 
 __device__ __forceinline__ int atom_add_acq_rel_gpu(int *p, int v) {
@@ -223,8 +227,11 @@ __global__ void __launch_bounds__((kMaxHkv + 1) * 32, 1) decode_splitk_kernel(co
     // CTA c streams pages [c T / N, (c + 1) T / N) of the T pages (N CTAs):
     // every CTA gets floor(T / N) or one more.
     const int ncta = gridDim.x;
-    const int lo = cta_lo(blockIdx.x, total, ncta);
-    const int hi = cta_lo(blockIdx.x + 1, total, ncta);
+    int *bound = reinterpret_cast<int *>(smem + L.off_bound);
+    for (int c = threadIdx.x; c <= ncta; c += blockDim.x) bound[c] = (int)((long long)c * total / ncta);
+    __syncthreads();
+    const int lo = bound[blockIdx.x];
+    const int hi = bound[blockIdx.x + 1];
     if (lo >= hi) return;
 
     // Requests b0 (holding page lo) .. b_last (holding page hi - 1).  Visit
@@ -453,7 +460,7 @@ __global__ void __launch_bounds__((kMaxHkv + 1) * 32, 1) decode_splitk_kernel(co
         }
         if (!whole) {
             // Count this partial in; the last arriving warp of (b, g) merges.
-            const int c_lo = owner_cta(p0, total, ncta), c_hi = owner_cta(p1 - 1, total, ncta);
+            const int c_lo = owner_cta(bound, ncta, p0), c_hi = owner_cta(bound, ncta, p1 - 1);
             // the warp barrier orders every lane's partial before lane 0's
             // release; lane 0's acquire orders the reads below after it
             __syncwarp();
@@ -471,14 +478,14 @@ __global__ void __launch_bounds__((kMaxHkv + 1) * 32, 1) decode_splitk_kernel(co
                     float mm = -INFINITY;
 #pragma unroll 4
                     for (int c = c_lo; c <= c_hi; ++c) {
-                        if (cta_lo(c, total, ncta) == cta_lo(c + 1, total, ncta)) continue;  // no pages
+                        if (bound[c] == bound[c + 1]) continue;  // no pages
                         mm = fmaxf(mm, __ldcg(a.part_ml + ((size_t)(c + b) * hq + h) * 2));
                     }
                     float ls = 0.f, o[4] = {0.f, 0.f, 0.f, 0.f};
                     if (mm != -INFINITY) {
 #pragma unroll 4
                         for (int c = c_lo; c <= c_hi; ++c) {
-                            if (cta_lo(c, total, ncta) == cta_lo(c + 1, total, ncta)) continue;
+                            if (bound[c] == bound[c + 1]) continue;
                             const size_t r = (size_t)(c + b) * hq + h;
                             const float mc = __ldcg(a.part_ml + r * 2), lc = __ldcg(a.part_ml + r * 2 + 1);
                             const float4 pv = __ldcg(reinterpret_cast<const float4 *>(a.part_acc + r * kD + 4 * lane));
@@ -508,7 +515,7 @@ int decode_grid_ctas(int device) {
     int sms = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess || sms <= 0)
         return 0;
-    return sms;
+    return sms < kMaxCtas ? sms : kMaxCtas;
 }
 
 size_t decode_workspace_bytes(int batch, int n_q_heads, int head_dim, int ctas) {

@@ -10,15 +10,15 @@
 // h / group.
 //
 // Work split.  The pages of all requests form one flat list (request-major).
-// A persistent grid of one CTA per SM cuts that list into contiguous ranges
-// of floor(T / N) or floor(T / N) + 1 pages, so every CTA streams the same
-// amount whatever the mix of lengths.  A CTA's range intersects one or more requests; each intersection
+// A persistent grid of one CTA per SM cuts that list into equal contiguous
+// ranges, so every CTA streams the same number of pages whatever the mix of
+// lengths.  A CTA's range intersects one or more requests; each intersection
 // is a "segment".  A segment that holds a whole request writes the final
 // bf16 output.  Otherwise it writes an fp32 partial (running max, running
 // sum, un-normalised accumulator) to slot c + b (CTA c, request b: unique
-// because both ranges are ordered), then adds its page count to the arrival
-// counter of (request, KV head); the warp that completes the count merges
-// every partial of its two query heads, writes the output and resets the counter to zero, so
+// because both ranges are ordered), then counts itself in the arrival counter
+// of (request, KV head); the warp that arrives last merges every partial of
+// its two query heads, writes the output and resets the counter to zero, so
 // nothing ever waits on another CTA and the workspace is left as it was
 // found.  A CTA takes its last segment first and its first segment second:
 // those are the only ones it can share with a neighbour, so partial results
@@ -52,7 +52,6 @@ constexpr int kD = 128;
 constexpr int kPS = 16;
 constexpr int kStages = 3;
 constexpr int kMaxHkv = 8;
-constexpr int kMaxCtas = 1023;  // grid limit (one CTA per SM)
 
 struct DecodeArgs {
     const uint16_t *q;
@@ -82,7 +81,7 @@ __device__ __forceinline__ int pages_of(const DecodeArgs &a, int b, bool report)
 struct SmemLayout {
     uint32_t stage_bytes;  // one stage: K page + V page
     uint32_t page_bytes;
-    uint32_t off_bar, off_flag, off_prefix, off_pbuf, off_bound, total;
+    uint32_t off_bar, off_flag, off_prefix, off_pbuf, total;
 };
 
 __host__ __device__ inline SmemLayout smem_layout(int hkv, int batch, int group) {
@@ -100,8 +99,6 @@ __host__ __device__ inline SmemLayout smem_layout(int hkv, int batch, int group)
     o = (o + 15) & ~15u;
     s.off_pbuf = o;  // 32 float2 per consumer warp
     o += hkv * 32 * 8;
-    s.off_bound = o;  // first page of every CTA's range, kMaxCtas + 1 entries
-    o += (kMaxCtas + 1) * 4;
     s.total = o;
     return s;
 }
@@ -131,17 +128,6 @@ __device__ __forceinline__ int first_request_past(const int *prefix, int batch, 
     while (l < r) {
         const int mid = (l + r) >> 1;
         if (prefix[mid + 1] > x) r = mid; else l = mid + 1;
-    }
-    return l;
-}
-
-// The CTA whose range [bound[c], bound[c + 1]) holds page x (the last c with
-// bound[c] <= x; empty ranges share their bound with the next CTA).
-__device__ __forceinline__ int owner_cta(const int *bound, int ncta, int x) {
-    int l = 0, r = ncta - 1;
-    while (l < r) {
-        const int mid = (l + r + 1) >> 1;
-        if (bound[mid] <= x) l = mid; else r = mid - 1;
     }
     return l;
 }
@@ -224,14 +210,9 @@ __global__ void __launch_bounds__((kMaxHkv + 1) * 32, 1) decode_splitk_kernel(co
 
     const int total = prefix[a.batch];
     if (total == 0) return;
-    // CTA c streams pages [c T / N, (c + 1) T / N) of the T pages (N CTAs):
-    // every CTA gets floor(T / N) or one more.
-    const int ncta = gridDim.x;
-    int *bound = reinterpret_cast<int *>(smem + L.off_bound);
-    for (int c = threadIdx.x; c <= ncta; c += blockDim.x) bound[c] = (int)((long long)c * total / ncta);
-    __syncthreads();
-    const int lo = bound[blockIdx.x];
-    const int hi = bound[blockIdx.x + 1];
+    const int per = (total + gridDim.x - 1) / gridDim.x;
+    const int lo = blockIdx.x * per;
+    const int hi = min(lo + per, total);
     if (lo >= hi) return;
 
     // Requests b0 (holding page lo) .. b_last (holding page hi - 1).  Visit
@@ -460,16 +441,14 @@ __global__ void __launch_bounds__((kMaxHkv + 1) * 32, 1) decode_splitk_kernel(co
         }
         if (!whole) {
             // Count this partial in; the last arriving warp of (b, g) merges.
-            const int c_lo = owner_cta(bound, ncta, p0), c_hi = owner_cta(bound, ncta, p1 - 1);
+            const int c_lo = p0 / per, c_hi = (p1 - 1) / per;
             // the warp barrier orders every lane's partial before lane 0's
             // release; lane 0's acquire orders the reads below after it
             __syncwarp();
             int prev = 0;
-            // arrivals are counted in pages: the request is complete when all
-            // of its pages are in (CTAs between c_lo and c_hi may hold none)
-            if (lane == 0) prev = atom_add_acq_rel_gpu(a.arrivals + (size_t)b * kMaxHkv + g, j1 - j0);
+            if (lane == 0) prev = atom_add_acq_rel_gpu(a.arrivals + (size_t)b * kMaxHkv + g, 1);
             prev = __shfl_sync(0xffffffffu, prev, 0);
-            if (prev + (j1 - j0) == p1 - p0) {
+            if (prev == c_hi - c_lo) {
 #pragma unroll
                 for (int i = 0; i < GROUP; ++i) {
                     const int h = g * GROUP + i;
@@ -477,15 +456,11 @@ __global__ void __launch_bounds__((kMaxHkv + 1) * 32, 1) decode_splitk_kernel(co
                     // the weighted sums (no load waits on an earlier result)
                     float mm = -INFINITY;
 #pragma unroll 4
-                    for (int c = c_lo; c <= c_hi; ++c) {
-                        if (bound[c] == bound[c + 1]) continue;  // no pages
-                        mm = fmaxf(mm, __ldcg(a.part_ml + ((size_t)(c + b) * hq + h) * 2));
-                    }
+                    for (int c = c_lo; c <= c_hi; ++c) mm = fmaxf(mm, __ldcg(a.part_ml + ((size_t)(c + b) * hq + h) * 2));
                     float ls = 0.f, o[4] = {0.f, 0.f, 0.f, 0.f};
                     if (mm != -INFINITY) {
 #pragma unroll 4
                         for (int c = c_lo; c <= c_hi; ++c) {
-                            if (bound[c] == bound[c + 1]) continue;
                             const size_t r = (size_t)(c + b) * hq + h;
                             const float mc = __ldcg(a.part_ml + r * 2), lc = __ldcg(a.part_ml + r * 2 + 1);
                             const float4 pv = __ldcg(reinterpret_cast<const float4 *>(a.part_acc + r * kD + 4 * lane));
@@ -515,7 +490,7 @@ int decode_grid_ctas(int device) {
     int sms = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess || sms <= 0)
         return 0;
-    return sms < kMaxCtas ? sms : kMaxCtas;
+    return sms;
 }
 
 size_t decode_workspace_bytes(int batch, int n_q_heads, int head_dim, int ctas) {

@@ -95,7 +95,8 @@ __global__ void __launch_bounds__(128, 4)
     const int n_tiles = (s1 - s0 + 127) / 128;
     int qt0, qt1;
     if (CAUSAL) {
-        qt0 = blockIdx.x;
+        // the longest jobs (last query tiles: most key tiles) launch first
+        qt0 = (int)(gridDim.x - 1 - blockIdx.x);
         qt1 = qt0 + 1;
         if (qt0 >= n_tiles) return;
     } else {
@@ -174,16 +175,16 @@ __global__ void __launch_bounds__(128, 4)
             const int warp_min = __reduce_min_sync(0xffffffffu, n_ok);
             float mx = -INFINITY;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < 4; c += 2) {  // two chunks of 32 scores per TMEM round trip
                 if (c * 32 >= warp_max) break;  // warp-uniform: nothing left in this warp's rows
-                float sv[32];
-                tc::tmem_ld32(t_row + c * 32, sv);
-                if (c * 32 + 32 <= warp_min) {
+                float sv[64];
+                tc::tmem_ld64(t_row + c * 32, sv);
+                if (c * 32 + 64 <= warp_min) {
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) mx = fmaxf(mx, sv[j]);
+                    for (int j = 0; j < 64; ++j) mx = fmaxf(mx, sv[j]);
                 } else {
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) mx = fmaxf(mx, c * 32 + j < n_ok ? sv[j] : -INFINITY);
+                    for (int j = 0; j < 64; ++j) mx = fmaxf(mx, c * 32 + j < n_ok ? sv[j] : -INFINITY);
                 }
             }
             const float m_new = fmaxf(m, mx * a.scale_log2);

@@ -117,6 +117,37 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 64 consecutive fp32 columns of this thread's TMEM lane: two 32-column loads
+// in flight before a single wait.
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
+    uint32_t r[64];
+#define QA_LD32(OFF, B)                                                                                              \
+    asm volatile(                                                                                                    \
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "                                                                    \
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "                                    \
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"                    \
+        : "=r"(r[B + 0]), "=r"(r[B + 1]), "=r"(r[B + 2]), "=r"(r[B + 3]), "=r"(r[B + 4]), "=r"(r[B + 5]),            \
+          "=r"(r[B + 6]), "=r"(r[B + 7]), "=r"(r[B + 8]), "=r"(r[B + 9]), "=r"(r[B + 10]), "=r"(r[B + 11]),          \
+          "=r"(r[B + 12]), "=r"(r[B + 13]), "=r"(r[B + 14]), "=r"(r[B + 15]), "=r"(r[B + 16]), "=r"(r[B + 17]),      \
+          "=r"(r[B + 18]), "=r"(r[B + 19]), "=r"(r[B + 20]), "=r"(r[B + 21]), "=r"(r[B + 22]), "=r"(r[B + 23]),      \
+          "=r"(r[B + 24]), "=r"(r[B + 25]), "=r"(r[B + 26]), "=r"(r[B + 27]), "=r"(r[B + 28]), "=r"(r[B + 29]),      \
+          "=r"(r[B + 30]), "=r"(r[B + 31])                                                                           \
+        : "r"(taddr + OFF)                                                                                           \
+        : "memory")
+    QA_LD32(0, 0);
+    QA_LD32(32, 32);
+#undef QA_LD32
+#define QA_R8(B) "+r"(r[B]), "+r"(r[B + 1]), "+r"(r[B + 2]), "+r"(r[B + 3]), "+r"(r[B + 4]), "+r"(r[B + 5]), \
+                 "+r"(r[B + 6]), "+r"(r[B + 7])
+    asm volatile("tcgen05.wait::ld.sync.aligned;" : QA_R8(0), QA_R8(8), QA_R8(16), QA_R8(24), QA_R8(32), QA_R8(40),
+                 QA_R8(48), QA_R8(56)
+                 :
+                 : "memory");
+#undef QA_R8
+#pragma unroll
+    for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
+}
+
 // Stores 32 consecutive fp32 columns of this thread's TMEM lane and waits
 // for the store to complete.
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {

@@ -71,7 +71,7 @@ struct AttnTcLayout {
     static constexpr uint32_t kSmem = kBytes + 1024;  // slack for 1024-byte alignment
 };
 
-// CAUSAL: grid (q-tiles, hq, segments), one query tile per CTA.
+// CAUSAL: grid (hq, segments, q-tiles), one query tile per CTA.
 // !CAUSAL: grid (segments, hq), every query tile of the segment in turn.
 template <int D, int GROUP, bool CAUSAL>
 __global__ void __launch_bounds__(128, 4)
@@ -84,9 +84,9 @@ __global__ void __launch_bounds__(128, 4)
     uint8_t *smem = smem_raw + (sb - raw);
     const int tid = threadIdx.x, warp = tid >> 5;
 
-    const int h = blockIdx.y;
+    const int h = CAUSAL ? blockIdx.x : blockIdx.y;
     const int g = h / GROUP;
-    const int seg = CAUSAL ? blockIdx.z : blockIdx.x;
+    const int seg = CAUSAL ? blockIdx.y : blockIdx.x;
     const int s0 = a.cu[seg], s1 = a.cu[seg + 1];
     if (!(0 <= s0 && s0 <= s1 && s1 <= a.total) || a.cu[a.n_seg] != a.total) {
         if (tid == 0) atomicOr(status, QA_DEVICE_BAD_SEGMENTS);
@@ -95,8 +95,9 @@ __global__ void __launch_bounds__(128, 4)
     const int n_tiles = (s1 - s0 + 127) / 128;
     int qt0, qt1;
     if (CAUSAL) {
-        // the longest jobs (last query tiles: most key tiles) launch first
-        qt0 = (int)(gridDim.x - 1 - blockIdx.x);
+        // the longest jobs (last query tiles: most key tiles) launch first:
+        // the query tile is the slowest-varying grid coordinate, reversed
+        qt0 = (int)(gridDim.z - 1 - blockIdx.z);
         qt1 = qt0 + 1;
         if (qt0 >= n_tiles) return;
     } else {
@@ -179,17 +180,18 @@ __global__ void __launch_bounds__(128, 4)
                 if (c * 32 >= warp_max) break;  // warp-uniform: nothing left in this warp's rows
                 float sv[64];
                 tc::tmem_ld64(t_row + c * 32, sv);
-                if (c * 32 + 64 <= warp_min) {
+                if (c * 32 + 64 > warp_min) {
 #pragma unroll
-                    for (int j = 0; j < 64; ++j) mx = fmaxf(mx, sv[j]);
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 64; ++j) mx = fmaxf(mx, c * 32 + j < n_ok ? sv[j] : -INFINITY);
+                    for (int j = 0; j < 64; ++j) sv[j] = c * 32 + j < n_ok ? sv[j] : -INFINITY;
                 }
+#pragma unroll
+                for (int j = 0; j < 64; j += 2) mx = fmax3(mx, sv[j], sv[j + 1]);
             }
             const float m_new = fmaxf(m, mx * a.scale_log2);
             const float alpha = m == -INFINITY ? 0.f : exp2_approx(m - m_new);
-            float psum = 0.f;
+            float2 psum2 = make_float2(0.f, 0.f);
+            const float2 scale2 = make_float2(a.scale_log2, a.scale_log2);
+            const float2 neg_m2 = make_float2(-m_new, -m_new);
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 uint32_t pk[16], pl[16];
@@ -202,13 +204,20 @@ __global__ void __launch_bounds__(128, 4)
                     const bool full = c * 32 + 32 <= warp_min;
 #pragma unroll
                     for (int j = 0; j < 32; j += 2) {
-                        const float x0 = full || c * 32 + j < n_ok ? sv[j] * a.scale_log2 - m_new : -INFINITY;
-                        const float x1 = full || c * 32 + j + 1 < n_ok ? sv[j + 1] * a.scale_log2 - m_new : -INFINITY;
-                        const float p0 = exp2_approx(x0), p1 = exp2_approx(x1);
-                        psum += p0 + p1;
-                        const uint32_t hi = pack_bf16x2(p0, p1);
-                        pk[j >> 1] = hi;
-                        pl[j >> 1] = pack_bf16x2(p0 - bf16lo(hi), p1 - bf16hi(hi));
+                        // x = s * scale * log2(e) - m for the pair, on packed fp32
+                        float2 x = ffma2(make_float2(sv[j], sv[j + 1]), scale2, neg_m2);
+                        if (!full) {
+                            x.x = c * 32 + j < n_ok ? x.x : -INFINITY;
+                            x.y = c * 32 + j + 1 < n_ok ? x.y : -INFINITY;
+                        }
+                        const float2 pp = make_float2(exp2_approx(x.x), exp2_approx(x.y));
+                        psum2 = fadd2(psum2, pp);
+                        // P_hi = p truncated to bf16 (exact), P_lo = bf16(p - P_hi)
+                        const uint32_t b0 = __float_as_uint(pp.x), b1 = __float_as_uint(pp.y);
+                        pk[j >> 1] = __byte_perm(b0, b1, 0x7632);
+                        const float2 lo = fsub2(pp, make_float2(__uint_as_float(b0 & 0xffff0000u),
+                                                                __uint_as_float(b1 & 0xffff0000u)));
+                        pl[j >> 1] = pack_bf16x2(lo.x, lo.y);
                     }
                 }
                 // P_hi: 32 keys = 16 TMEM columns [16c, 16c + 16) (scores there are consumed)
@@ -222,6 +231,7 @@ __global__ void __launch_bounds__(128, 4)
                 }
             }
             tc::tmem_wait_st();
+            const float psum = psum2.x + psum2.y;
             l = l * alpha + psum;
             m = m_new;
             // rescale this row of the output accumulator (warp-collective)
@@ -270,14 +280,15 @@ __global__ void __launch_bounds__(128, 4)
             float ov[32];
             tc::tmem_ld32(t_row + col_o + c * 32, ov);
             if (qi < s1) {
+                const float2 inv2 = make_float2(inv, inv);
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
-                    uint4 w;
-                    w.x = pack_bf16x2(ov[8 * u + 0] * inv, ov[8 * u + 1] * inv);
-                    w.y = pack_bf16x2(ov[8 * u + 2] * inv, ov[8 * u + 3] * inv);
-                    w.z = pack_bf16x2(ov[8 * u + 4] * inv, ov[8 * u + 5] * inv);
-                    w.w = pack_bf16x2(ov[8 * u + 6] * inv, ov[8 * u + 7] * inv);
-                    dst[c * 4 + u] = w;
+                    const float2 o0 = fmul2(make_float2(ov[8 * u + 0], ov[8 * u + 1]), inv2);
+                    const float2 o1 = fmul2(make_float2(ov[8 * u + 2], ov[8 * u + 3]), inv2);
+                    const float2 o2 = fmul2(make_float2(ov[8 * u + 4], ov[8 * u + 5]), inv2);
+                    const float2 o3 = fmul2(make_float2(ov[8 * u + 6], ov[8 * u + 7]), inv2);
+                    dst[c * 4 + u] = make_uint4(pack_bf16x2(o0.x, o0.y), pack_bf16x2(o1.x, o1.y),
+                                                pack_bf16x2(o2.x, o2.y), pack_bf16x2(o3.x, o3.y));
                 }
             }
         }

@@ -138,15 +138,6 @@ __device__ __forceinline__ int atom_add_acq_rel_gpu(int *p, int v) {
     return old;
 }
 
-__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
-    uint64_t d;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;"
-        : "=l"(d)
-        : "l"(*reinterpret_cast<uint64_t *>(&a)), "l"(*reinterpret_cast<uint64_t *>(&b)),
-          "l"(*reinterpret_cast<uint64_t *>(&c)));
-    return *reinterpret_cast<float2 *>(&d);
-}
-
 __device__ __forceinline__ void bf16x4(uint2 w, float2 &lo, float2 &hi) {
     lo = make_float2(bf16lo(w.x), bf16hi(w.x));
     hi = make_float2(bf16lo(w.y), bf16hi(w.y));

@@ -112,7 +112,8 @@ cudaError_t launch_prefill(const void *q, const void *k, const void *v, const in
     const long long max_len = (long long)p.max_pages_per_seq * p.page_size;
     const long long qtiles = (max_len + 127) / 128;
     if (qtiles > 0x7fffffffLL) return cudaErrorInvalidValue;
-    const dim3 grid((unsigned)qtiles, p.n_q_heads, batch);
+    if (qtiles > 65535 || batch > 65535) return cudaErrorInvalidValue;
+    const dim3 grid(p.n_q_heads, batch, (unsigned)qtiles);
     constexpr uint32_t smem = AttnTcLayout<128>::kSmem;
     if (p.n_q_heads == 2 * p.n_kv_heads) {
         e = cudaFuncSetAttribute(attn_tc_kernel<128, 2, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);

@@ -174,38 +174,52 @@ __global__ void __launch_bounds__(128, 4)
             n_ok = max(n_ok, 0);
             const int warp_max = __reduce_max_sync(0xffffffffu, n_ok);
             const int warp_min = __reduce_min_sync(0xffffffffu, n_ok);
+            // TMEM reads are software-pipelined: chunk c + 1 (32 columns) is in
+            // flight while chunk c is processed; dead chunks (warp-uniform) are
+            // neither read nor computed.
+            const int n_chunks = (warp_max + 31) >> 5;
+            uint32_t ra[32], rb[32];
             float mx = -INFINITY;
+            tc::tmem_ld32_issue(t_row, ra);
+            tc::tmem_ld32_wait(ra);
 #pragma unroll
-            for (int c = 0; c < 4; c += 2) {  // two chunks of 32 scores per TMEM round trip
-                if (c * 32 >= warp_max) break;  // warp-uniform: nothing left in this warp's rows
-                float sv[64];
-                tc::tmem_ld64(t_row + c * 32, sv);
-                if (c * 32 + 64 > warp_min) {
+            for (int c = 0; c < 4; ++c) {
+                if (c >= n_chunks) break;
+                uint32_t(&cur)[32] = (c & 1) ? rb : ra;
+                uint32_t(&nxt)[32] = (c & 1) ? ra : rb;
+                if (c + 1 < n_chunks) tc::tmem_ld32_issue(t_row + (c + 1) * 32, nxt);
+                if (c * 32 + 32 > warp_min) {
 #pragma unroll
-                    for (int j = 0; j < 64; ++j) sv[j] = c * 32 + j < n_ok ? sv[j] : -INFINITY;
+                    for (int j = 0; j < 32; ++j)
+                        cur[j] = c * 32 + j < n_ok ? cur[j] : __float_as_uint(-INFINITY);
                 }
 #pragma unroll
-                for (int j = 0; j < 64; j += 2) mx = fmax3(mx, sv[j], sv[j + 1]);
+                for (int j = 0; j < 32; j += 2) mx = fmax3(mx, __uint_as_float(cur[j]), __uint_as_float(cur[j + 1]));
+                if (c + 1 < n_chunks) tc::tmem_ld32_wait(nxt);
             }
             const float m_new = fmaxf(m, mx * a.scale_log2);
             const float alpha = m == -INFINITY ? 0.f : exp2_approx(m - m_new);
             float2 psum2 = make_float2(0.f, 0.f);
             const float2 scale2 = make_float2(a.scale_log2, a.scale_log2);
             const float2 neg_m2 = make_float2(-m_new, -m_new);
+            tc::tmem_ld32_issue(t_row, ra);
+            tc::tmem_ld32_wait(ra);
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 uint32_t pk[16], pl[16];
-                if (c * 32 >= warp_max) {  // warp-uniform: a dead chunk gets zero probabilities
+                uint32_t(&cur)[32] = (c & 1) ? rb : ra;
+                uint32_t(&nxt)[32] = (c & 1) ? ra : rb;
+                if (c >= n_chunks) {  // warp-uniform: a dead chunk gets zero probabilities
 #pragma unroll
                     for (int i = 0; i < 16; ++i) pk[i] = pl[i] = 0u;
                 } else {
-                    float sv[32];
-                    tc::tmem_ld32(t_row + c * 32, sv);
+                    if (c + 1 < n_chunks) tc::tmem_ld32_issue(t_row + (c + 1) * 32, nxt);
                     const bool full = c * 32 + 32 <= warp_min;
 #pragma unroll
                     for (int j = 0; j < 32; j += 2) {
                         // x = s * scale * log2(e) - m for the pair, on packed fp32
-                        float2 x = ffma2(make_float2(sv[j], sv[j + 1]), scale2, neg_m2);
+                        float2 x = ffma2(make_float2(__uint_as_float(cur[j]), __uint_as_float(cur[j + 1])), scale2,
+                                         neg_m2);
                         if (!full) {
                             x.x = c * 32 + j < n_ok ? x.x : -INFINITY;
                             x.y = c * 32 + j + 1 < n_ok ? x.y : -INFINITY;
@@ -219,6 +233,7 @@ __global__ void __launch_bounds__(128, 4)
                                                                 __uint_as_float(b1 & 0xffff0000u)));
                         pl[j >> 1] = pack_bf16x2(lo.x, lo.y);
                     }
+                    if (c + 1 < n_chunks) tc::tmem_ld32_wait(nxt);
                 }
                 // P_hi: 32 keys = 16 TMEM columns [16c, 16c + 16) (scores there are consumed)
                 tc::tmem_st16(t_row + c * 16, pk);

@@ -71,6 +71,159 @@ struct AttnTcLayout {
     static constexpr uint32_t kSmem = kBytes + 1024;  // slack for 1024-byte alignment
 };
 
+// Online softmax of one 128-key tile for this thread's query row, whose
+// scores sit in TMEM columns [0, 128) of s_row.  Keys [0, n_ok) of the tile
+// are visible.  Writes P_hi (bf16, two keys per column) over the scores in
+// columns [0, 64), P_lo as a 128B-swizzled K-major row at plo_row, updates
+// the running (m, l) and, when `rescale`, multiplies the row of O at o_row by
+// 2^(m_old - m_new).  Warp-collective (every lane of the warp calls it).
+template <int D>
+__device__ __forceinline__ void softmax_tile(uint32_t s_row, int n_ok, float scale_log2, uint32_t plo_row,
+                                             uint32_t sw, uint32_t o_row, bool rescale, float &m, float &l) {
+    const int warp_max = __reduce_max_sync(0xffffffffu, n_ok);
+    const int warp_min = __reduce_min_sync(0xffffffffu, n_ok);
+    // TMEM reads are software-pipelined: chunk c + 1 (32 columns) is in
+    // flight while chunk c is processed; dead chunks (warp-uniform) are
+    // neither read nor computed.
+    const int n_chunks = (warp_max + 31) >> 5;
+    uint32_t ra[32], rb[32];
+    float mx = -INFINITY;
+    tc::tmem_ld32_issue(s_row, ra);
+    tc::tmem_ld32_wait(ra);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        if (c >= n_chunks) break;
+        uint32_t(&cur)[32] = (c & 1) ? rb : ra;
+        uint32_t(&nxt)[32] = (c & 1) ? ra : rb;
+        if (c + 1 < n_chunks) tc::tmem_ld32_issue(s_row + (c + 1) * 32, nxt);
+        if (c * 32 + 32 > warp_min) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) cur[j] = c * 32 + j < n_ok ? cur[j] : __float_as_uint(-INFINITY);
+        }
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) mx = fmax3(mx, __uint_as_float(cur[j]), __uint_as_float(cur[j + 1]));
+        if (c + 1 < n_chunks) tc::tmem_ld32_wait(nxt);
+    }
+    const float m_new = fmaxf(m, mx * scale_log2);
+    const float alpha = m == -INFINITY ? 0.f : exp2_approx(m - m_new);
+    float2 psum2 = make_float2(0.f, 0.f);
+    const float2 scale2 = make_float2(scale_log2, scale_log2);
+    const float2 neg_m2 = make_float2(-m_new, -m_new);
+    tc::tmem_ld32_issue(s_row, ra);
+    tc::tmem_ld32_wait(ra);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        uint32_t pk[16], pl[16];
+        uint32_t(&cur)[32] = (c & 1) ? rb : ra;
+        uint32_t(&nxt)[32] = (c & 1) ? ra : rb;
+        if (c >= n_chunks) {  // warp-uniform: a dead chunk gets zero probabilities
+#pragma unroll
+            for (int i = 0; i < 16; ++i) pk[i] = pl[i] = 0u;
+        } else {
+            if (c + 1 < n_chunks) tc::tmem_ld32_issue(s_row + (c + 1) * 32, nxt);
+            const bool full = c * 32 + 32 <= warp_min;
+#pragma unroll
+            for (int j = 0; j < 32; j += 2) {
+                // x = s * scale * log2(e) - m for the pair, on packed fp32
+                float2 x = ffma2(make_float2(__uint_as_float(cur[j]), __uint_as_float(cur[j + 1])), scale2, neg_m2);
+                if (!full) {
+                    x.x = c * 32 + j < n_ok ? x.x : -INFINITY;
+                    x.y = c * 32 + j + 1 < n_ok ? x.y : -INFINITY;
+                }
+                const float2 pp = make_float2(exp2_approx(x.x), exp2_approx(x.y));
+                psum2 = fadd2(psum2, pp);
+                // P_hi = p truncated to bf16 (exact), P_lo = bf16(p - P_hi)
+                const uint32_t b0 = __float_as_uint(pp.x), b1 = __float_as_uint(pp.y);
+                pk[j >> 1] = __byte_perm(b0, b1, 0x7632);
+                const float2 lo =
+                    fsub2(pp, make_float2(__uint_as_float(b0 & 0xffff0000u), __uint_as_float(b1 & 0xffff0000u)));
+                pl[j >> 1] = pack_bf16x2(lo.x, lo.y);
+            }
+            if (c + 1 < n_chunks) tc::tmem_ld32_wait(nxt);
+        }
+        // P_hi: 32 keys = 16 TMEM columns [16c, 16c + 16) (scores there are consumed)
+        tc::tmem_st16(s_row + c * 16, pk);
+        // P_lo: 4 chunks of 16 bytes, sub-tile c / 2, chunks (c % 2) * 4 + u
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const uint32_t chunk = (uint32_t)((c & 1) * 4 + u);
+            const uint32_t off = (uint32_t)(c >> 1) * tc::kSubTileBytes + ((chunk ^ sw) << 4);
+            tc::st_shared_v4(plo_row + off, pl[4 * u], pl[4 * u + 1], pl[4 * u + 2], pl[4 * u + 3]);
+        }
+    }
+    tc::tmem_wait_st();
+    l = l * alpha + (psum2.x + psum2.y);
+    m = m_new;
+    // rescale this row of the output accumulator (warp-collective)
+    if (rescale && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+            float ov[32];
+            tc::tmem_ld32(o_row + c * 32, ov);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) ov[j] *= alpha;
+            tc::tmem_st32(o_row + c * 32, ov);
+        }
+    }
+}
+
+// O row (TMEM columns [0, D) of o_row) divided by l, rounded to bf16 and
+// stored at dst when `valid`.  Warp-collective.
+template <int D>
+__device__ __forceinline__ void store_rows(uint32_t o_row, float l, uint16_t *dst_row, bool valid) {
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    uint4 *dst = reinterpret_cast<uint4 *>(dst_row);
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) {
+        float ov[32];
+        tc::tmem_ld32(o_row + c * 32, ov);
+        if (valid) {
+            const float2 inv2 = make_float2(inv, inv);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float2 o0 = fmul2(make_float2(ov[8 * u + 0], ov[8 * u + 1]), inv2);
+                const float2 o1 = fmul2(make_float2(ov[8 * u + 2], ov[8 * u + 3]), inv2);
+                const float2 o2 = fmul2(make_float2(ov[8 * u + 4], ov[8 * u + 5]), inv2);
+                const float2 o3 = fmul2(make_float2(ov[8 * u + 6], ov[8 * u + 7]), inv2);
+                dst[c * 4 + u] = make_uint4(pack_bf16x2(o0.x, o0.y), pack_bf16x2(o1.x, o1.y),
+                                            pack_bf16x2(o2.x, o2.y), pack_bf16x2(o3.x, o3.y));
+            }
+        }
+    }
+}
+
+// S = Q K^T (M = 128, N = 128 keys, K = D in steps of 16: 32 bytes inside a
+// 128-byte row) into TMEM columns [0, 128) of tmem.  One thread.
+template <int D>
+__device__ __forceinline__ void issue_s(uint32_t tmem, uint32_t q_base, uint32_t k_base) {
+    constexpr uint32_t idesc_s = tc::idesc_bf16(128, 128, false);
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = (kk >> 2) * tc::kSubTileBytes + (kk & 3) * 32;
+        tc::mma_bf16(tmem, tc::sw128_desc(q_base + off), tc::sw128_desc(k_base + off), idesc_s, kk > 0);
+    }
+}
+
+// O += P_hi V + P_lo V: K = 128 keys in steps of 16 (8 TMEM columns of P_hi;
+// two 8-row groups of V = 2048 bytes), N = 64 dims per MMA (one V sub-tile
+// each).  P_hi in TMEM columns [0, 64) of tmem, O at o_col.  One thread.
+template <int D>
+__device__ __forceinline__ void issue_pv(uint32_t tmem, uint32_t o_col, uint32_t plo_base, uint32_t v_base,
+                                         bool accumulate) {
+    constexpr uint32_t idesc_o = tc::idesc_bf16(128, 64, true);
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t a_off = (kk >> 2) * tc::kSubTileBytes + (kk & 3) * 32;
+#pragma unroll
+        for (int sd = 0; sd < D / 64; ++sd) {
+            const uint64_t vdesc = tc::sw128_desc(v_base + sd * tc::kSubTileBytes + kk * 2048);
+            const uint32_t o = o_col + sd * 64;
+            tc::mma_bf16_ts(o, tmem + kk * 8, vdesc, idesc_o, (accumulate || kk > 0) ? 1u : 0u);
+            tc::mma_bf16(o, tc::sw128_desc(plo_base + a_off), vdesc, idesc_o, 1u);
+        }
+    }
+}
+
 // CAUSAL: grid (hq, segments, q-tiles), one query tile per CTA.
 // !CAUSAL: grid (segments, hq), every query tile of the segment in turn.
 template <int D, int GROUP, bool CAUSAL>
@@ -128,8 +281,6 @@ __global__ void __launch_bounds__(128, 4)
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + L::kTmemSlot);
     const uint32_t t_row = tmem + ((uint32_t)(warp * 32) << 16);  // this warp's TMEM lanes
 
-    constexpr uint32_t idesc_s = tc::idesc_bf16(128, 128, false);
-    constexpr uint32_t idesc_o = tc::idesc_bf16(128, 64, true);
     uint32_t ph_ld = 0, ph_s = 0, ph_o = 0;
     const int r = tid;  // query row in the tile = TMEM lane
     const uint32_t plo_row = sb + L::kPlo + r * 128;
@@ -154,13 +305,7 @@ __global__ void __launch_bounds__(128, 4)
                 }
                 mbar_wait(bar_ld, ph_ld, status);
                 tc::fence_after();
-                // S = Q K^T over D in steps of 16 (32 bytes inside a 128-byte row)
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * tc::kSubTileBytes + (kk & 3) * 32;
-                    tc::mma_bf16(tmem, tc::sw128_desc(sb + L::kQ + off), tc::sw128_desc(sb + L::kK + off), idesc_s,
-                                 kk > 0);
-                }
+                issue_s<D>(tmem, sb + L::kQ, sb + L::kK);
                 tc::mma_commit(bar_s);
             }
             ph_ld ^= 1;
@@ -172,114 +317,14 @@ __global__ void __launch_bounds__(128, 4)
             int n_ok = min(128, s1 - k0);
             if (CAUSAL) n_ok = min(n_ok, qi - k0 + 1);
             n_ok = max(n_ok, 0);
-            const int warp_max = __reduce_max_sync(0xffffffffu, n_ok);
-            const int warp_min = __reduce_min_sync(0xffffffffu, n_ok);
-            // TMEM reads are software-pipelined: chunk c + 1 (32 columns) is in
-            // flight while chunk c is processed; dead chunks (warp-uniform) are
-            // neither read nor computed.
-            const int n_chunks = (warp_max + 31) >> 5;
-            uint32_t ra[32], rb[32];
-            float mx = -INFINITY;
-            tc::tmem_ld32_issue(t_row, ra);
-            tc::tmem_ld32_wait(ra);
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                if (c >= n_chunks) break;
-                uint32_t(&cur)[32] = (c & 1) ? rb : ra;
-                uint32_t(&nxt)[32] = (c & 1) ? ra : rb;
-                if (c + 1 < n_chunks) tc::tmem_ld32_issue(t_row + (c + 1) * 32, nxt);
-                if (c * 32 + 32 > warp_min) {
-#pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        cur[j] = c * 32 + j < n_ok ? cur[j] : __float_as_uint(-INFINITY);
-                }
-#pragma unroll
-                for (int j = 0; j < 32; j += 2) mx = fmax3(mx, __uint_as_float(cur[j]), __uint_as_float(cur[j + 1]));
-                if (c + 1 < n_chunks) tc::tmem_ld32_wait(nxt);
-            }
-            const float m_new = fmaxf(m, mx * a.scale_log2);
-            const float alpha = m == -INFINITY ? 0.f : exp2_approx(m - m_new);
-            float2 psum2 = make_float2(0.f, 0.f);
-            const float2 scale2 = make_float2(a.scale_log2, a.scale_log2);
-            const float2 neg_m2 = make_float2(-m_new, -m_new);
-            tc::tmem_ld32_issue(t_row, ra);
-            tc::tmem_ld32_wait(ra);
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t pk[16], pl[16];
-                uint32_t(&cur)[32] = (c & 1) ? rb : ra;
-                uint32_t(&nxt)[32] = (c & 1) ? ra : rb;
-                if (c >= n_chunks) {  // warp-uniform: a dead chunk gets zero probabilities
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) pk[i] = pl[i] = 0u;
-                } else {
-                    if (c + 1 < n_chunks) tc::tmem_ld32_issue(t_row + (c + 1) * 32, nxt);
-                    const bool full = c * 32 + 32 <= warp_min;
-#pragma unroll
-                    for (int j = 0; j < 32; j += 2) {
-                        // x = s * scale * log2(e) - m for the pair, on packed fp32
-                        float2 x = ffma2(make_float2(__uint_as_float(cur[j]), __uint_as_float(cur[j + 1])), scale2,
-                                         neg_m2);
-                        if (!full) {
-                            x.x = c * 32 + j < n_ok ? x.x : -INFINITY;
-                            x.y = c * 32 + j + 1 < n_ok ? x.y : -INFINITY;
-                        }
-                        const float2 pp = make_float2(exp2_approx(x.x), exp2_approx(x.y));
-                        psum2 = fadd2(psum2, pp);
-                        // P_hi = p truncated to bf16 (exact), P_lo = bf16(p - P_hi)
-                        const uint32_t b0 = __float_as_uint(pp.x), b1 = __float_as_uint(pp.y);
-                        pk[j >> 1] = __byte_perm(b0, b1, 0x7632);
-                        const float2 lo = fsub2(pp, make_float2(__uint_as_float(b0 & 0xffff0000u),
-                                                                __uint_as_float(b1 & 0xffff0000u)));
-                        pl[j >> 1] = pack_bf16x2(lo.x, lo.y);
-                    }
-                    if (c + 1 < n_chunks) tc::tmem_ld32_wait(nxt);
-                }
-                // P_hi: 32 keys = 16 TMEM columns [16c, 16c + 16) (scores there are consumed)
-                tc::tmem_st16(t_row + c * 16, pk);
-                // P_lo: 4 chunks of 16 bytes, sub-tile c / 2, chunks (c % 2) * 4 + u
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const uint32_t chunk = (uint32_t)((c & 1) * 4 + u);
-                    const uint32_t off = (uint32_t)(c >> 1) * tc::kSubTileBytes + ((chunk ^ sw) << 4);
-                    tc::st_shared_v4(plo_row + off, pl[4 * u], pl[4 * u + 1], pl[4 * u + 2], pl[4 * u + 3]);
-                }
-            }
-            tc::tmem_wait_st();
-            const float psum = psum2.x + psum2.y;
-            l = l * alpha + psum;
-            m = m_new;
-            // rescale this row of the output accumulator (warp-collective)
-            if (kt > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    float ov[32];
-                    tc::tmem_ld32(t_row + col_o + c * 32, ov);
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) ov[j] *= alpha;
-                    tc::tmem_st32(t_row + col_o + c * 32, ov);
-                }
-            }
+            softmax_tile<D>(t_row, n_ok, a.scale_log2, plo_row, sw, t_row + col_o, kt > 0, m, l);
             tc::fence_proxy_async_smem();
             tc::fence_before();
             __syncthreads();
 
             if (tid == 0) {
                 tc::fence_after();
-                // O += P_hi V + P_lo V: K = 128 keys in steps of 16 (8 TMEM
-                // columns of P_hi; two 8-row groups of V = 2048 bytes), N = 64
-                // dims per MMA (one V sub-tile each)
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t a_off = (kk >> 2) * tc::kSubTileBytes + (kk & 3) * 32;
-#pragma unroll
-                    for (int sd = 0; sd < L::kSub; ++sd) {
-                        const uint64_t vdesc = tc::sw128_desc(sb + L::kV + sd * tc::kSubTileBytes + kk * 2048);
-                        const uint32_t o = tmem + col_o + sd * 64;
-                        tc::mma_bf16_ts(o, tmem + kk * 8, vdesc, idesc_o, (kt > 0 || kk > 0) ? 1u : 0u);
-                        tc::mma_bf16(o, tc::sw128_desc(sb + L::kPlo + a_off), vdesc, idesc_o, 1u);
-                    }
-                }
+                issue_pv<D>(tmem, tmem + col_o, sb + L::kPlo, sb + L::kV, kt > 0);
                 tc::mma_commit(bar_o);
             }
             mbar_wait(bar_o, ph_o, status);
@@ -288,25 +333,7 @@ __global__ void __launch_bounds__(128, 4)
         }
 
         // epilogue: O / l -> bf16 (warp-collective TMEM reads, masked stores)
-        const float inv = l > 0.f ? 1.f / l : 0.f;
-        uint4 *dst = reinterpret_cast<uint4 *>(a.out + ((size_t)qi * a.hq + h) * D);
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-            float ov[32];
-            tc::tmem_ld32(t_row + col_o + c * 32, ov);
-            if (qi < s1) {
-                const float2 inv2 = make_float2(inv, inv);
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const float2 o0 = fmul2(make_float2(ov[8 * u + 0], ov[8 * u + 1]), inv2);
-                    const float2 o1 = fmul2(make_float2(ov[8 * u + 2], ov[8 * u + 3]), inv2);
-                    const float2 o2 = fmul2(make_float2(ov[8 * u + 4], ov[8 * u + 5]), inv2);
-                    const float2 o3 = fmul2(make_float2(ov[8 * u + 6], ov[8 * u + 7]), inv2);
-                    dst[c * 4 + u] = make_uint4(pack_bf16x2(o0.x, o0.y), pack_bf16x2(o1.x, o1.y),
-                                                pack_bf16x2(o2.x, o2.y), pack_bf16x2(o3.x, o3.y));
-                }
-            }
-        }
+        store_rows<D>(t_row + col_o, l, a.out + ((size_t)qi * a.hq + h) * D, qi < s1);
         tc::fence_before();
         __syncthreads();  // every TMEM read is done before the next query tile's MMAs
     }
@@ -314,6 +341,143 @@ __global__ void __launch_bounds__(128, 4)
     if (warp == 0) {
         tc::fence_after();
         tc::tmem_dealloc(tmem, tmem_cols);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Windowed attention, persistent form: each CTA walks (window, head) jobs
+// j = blockIdx.x + k * gridDim.x and prefetches the next job's Q/K/V tiles
+// into a second shared-memory stage while the current job computes, so the
+// tile loads overlap the softmax and MMAs.  Two CTAs run on each SM.  A job
+// whose window spans more than one 128-row tile processes its further tiles
+// synchronously in its own stage.
+template <int D>
+struct WindowLayout {
+    static constexpr int kSub = D / 64;
+    // stage: Q | K (P_lo over both once S is computed) | V
+    static constexpr uint32_t kQ = 0;
+    static constexpr uint32_t kK = kQ + kSub * tc::kSubTileBytes;
+    static constexpr uint32_t kV = kK + (kSub > 1 ? kSub : 1) * tc::kSubTileBytes;
+    static constexpr uint32_t kStage = kV + kSub * tc::kSubTileBytes;
+    static constexpr uint32_t kBar = 2 * kStage;  // ld[2], s, o
+    static constexpr uint32_t kTmemSlot = kBar + 32;
+    static constexpr uint32_t kBytes = kTmemSlot + 8;
+    static constexpr uint32_t kSmem = kBytes + 1024;
+    static constexpr uint32_t kTmemCols = 256;  // S / P_hi in [0, 128), O in [128, 128 + D)
+    static constexpr uint32_t kColO = 128;
+    static_assert(D == 64, "the persistent window kernel keeps P_lo over Q and K (head_dim 64)");
+};
+
+template <int D>
+__global__ void __launch_bounds__(128, 2)
+    window_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_v, const AttnTcArgs a, int n_items,
+                     unsigned int *status) {
+    using L = WindowLayout<D>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t sb = (raw + 1023u) & ~1023u;
+    uint8_t *smem = smem_raw + (sb - raw);
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const uint32_t bar_ld = sb + L::kBar, bar_s = bar_ld + 16, bar_o = bar_ld + 24;
+    const bool cu_ok = a.cu[a.n_seg] == a.total;
+
+    if (tid == 0) {
+        mbar_init(bar_ld, 1);
+        mbar_init(bar_ld + 8, 1);
+        mbar_init(bar_s, 1);
+        mbar_init(bar_o, 1);
+        fence_mbar_init();
+        tc::prefetch_tmap(&tm_q);
+        tc::prefetch_tmap(&tm_k);
+        tc::prefetch_tmap(&tm_v);
+    }
+    if (warp == 0) tc::tmem_alloc(sb + L::kTmemSlot, L::kTmemCols);
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + L::kTmemSlot);
+    const uint32_t t_row = tmem + ((uint32_t)(warp * 32) << 16);
+    const int r = tid;
+    const uint32_t sw = (uint32_t)(r & 7);
+
+    // Loads Q (query tile qt), K and V (key tile kt) of job j into stage st;
+    // a job with a malformed window gets a plain arrival (no data) so that
+    // every stage use completes exactly one phase.
+    auto load = [&](int j, int st, int qt, int kt) {
+        const int w = j / a.hq, h = j % a.hq;
+        const int s0 = a.cu[w], s1 = a.cu[w + 1];
+        const uint32_t base = sb + st * L::kStage, bar = bar_ld + 8 * st;
+        if (!cu_ok || !(0 <= s0 && s0 <= s1 && s1 <= a.total) || s1 == s0) {
+            mbar_arrive(bar);
+            return;
+        }
+        mbar_arrive_expect_tx(bar, 3 * L::kSub * tc::kSubTileBytes);
+#pragma unroll
+        for (int sd = 0; sd < L::kSub; ++sd) {
+            tc::tma_load_3d(base + L::kQ + sd * tc::kSubTileBytes, &tm_q, sd * 64, h, s0 + qt * 128, bar);
+            tc::tma_load_3d(base + L::kK + sd * tc::kSubTileBytes, &tm_k, sd * 64, h, s0 + kt * 128, bar);
+            tc::tma_load_3d(base + L::kV + sd * tc::kSubTileBytes, &tm_v, sd * 64, h, s0 + kt * 128, bar);
+        }
+    };
+
+    uint32_t ph_ld[2] = {0u, 0u}, ph_s = 0, ph_o = 0;
+    if (tid == 0 && (int)blockIdx.x < n_items) load(blockIdx.x, 0, 0, 0);
+    int k = 0;
+    for (int j = blockIdx.x; j < n_items; j += gridDim.x, ++k) {
+        const int st = k & 1;
+        const uint32_t base = sb + st * L::kStage;
+        // prefetch the next job into the other stage (its last user, job k - 1, is done)
+        if (tid == 0 && j + (int)gridDim.x < n_items) load(j + gridDim.x, st ^ 1, 0, 0);
+        const int w = j / a.hq, h = j % a.hq;
+        const int s0 = a.cu[w], s1 = a.cu[w + 1];
+        const bool ok = cu_ok && 0 <= s0 && s0 <= s1 && s1 <= a.total;
+        if (!ok && tid == 0) atomicOr(status, QA_DEVICE_BAD_SEGMENTS);
+        const int n_tiles = ok ? (s1 - s0 + 127) / 128 : 0;
+        if (n_tiles == 0) {  // nothing to compute; still consume the stage's phase
+            if (tid == 0) mbar_wait(bar_ld + 8 * st, ph_ld[st], status);
+            ph_ld[st] ^= 1;
+            continue;
+        }
+        for (int qt = 0; qt < n_tiles; ++qt) {
+            const int qi = s0 + qt * 128 + r;
+            float m = -INFINITY, l = 0.f;
+            for (int kt = 0; kt < n_tiles; ++kt) {
+                const int k0 = s0 + kt * 128;
+                if (tid == 0) {
+                    if (qt > 0 || kt > 0) load(j, st, qt, kt);  // further tiles: synchronous, same stage
+                    mbar_wait(bar_ld + 8 * st, ph_ld[st], status);
+                    tc::fence_after();
+                    issue_s<D>(tmem, base + L::kQ, base + L::kK);
+                    tc::mma_commit(bar_s);
+                }
+                ph_ld[st] ^= 1;
+                mbar_wait(bar_s, ph_s, status);
+                ph_s ^= 1;
+                tc::fence_after();
+                const int n_ok = max(min(128, s1 - k0), 0);
+                softmax_tile<D>(t_row, n_ok, a.scale_log2, base + L::kQ + r * 128, sw, t_row + L::kColO, kt > 0, m, l);
+                tc::fence_proxy_async_smem();
+                tc::fence_before();
+                __syncthreads();
+                if (tid == 0) {
+                    tc::fence_after();
+                    issue_pv<D>(tmem, tmem + L::kColO, base + L::kQ, base + L::kV, kt > 0);
+                    tc::mma_commit(bar_o);
+                }
+                mbar_wait(bar_o, ph_o, status);
+                ph_o ^= 1;
+                tc::fence_after();
+            }
+            store_rows<D>(t_row + L::kColO, l, a.out + ((size_t)qi * a.hq + h) * D, qi < s1);
+            tc::fence_before();
+            __syncthreads();  // O and the stage are free before the next tile's MMAs and loads
+        }
+    }
+
+    if (warp == 0) {
+        tc::fence_after();
+        tc::tmem_dealloc(tmem, L::kTmemCols);
     }
 }
 

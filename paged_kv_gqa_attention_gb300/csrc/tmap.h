@@ -39,13 +39,14 @@ inline bool make_rows_tmap(CUtensorMap *map, const void *base, int D, int H, int
     return r == CUDA_SUCCESS;
 }
 
-// Persistent grid size: one CTA per SM of the current device, no more CTAs
-// than jobs.  0 when no device answers.
-inline int persistent_grid(int n_items) {
+// Persistent grid size: per_sm CTAs on every SM of the current device, no
+// more CTAs than jobs.  0 when no device answers.
+inline int persistent_grid(int n_items, int per_sm) {
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) return 0;
-    return n_items < sms ? (n_items > 0 ? n_items : 1) : sms;
+    const int slots = sms * per_sm;
+    return n_items < slots ? (n_items > 0 ? n_items : 1) : slots;
 }
 
 }  // namespace qa

@@ -344,141 +344,4 @@ __global__ void __launch_bounds__(128, 4)
     }
 }
 
-// ---------------------------------------------------------------------------
-// Windowed attention, persistent form: each CTA walks (window, head) jobs
-// j = blockIdx.x + k * gridDim.x and prefetches the next job's Q/K/V tiles
-// into a second shared-memory stage while the current job computes, so the
-// tile loads overlap the softmax and MMAs.  Two CTAs run on each SM.  A job
-// whose window spans more than one 128-row tile processes its further tiles
-// synchronously in its own stage.
-template <int D>
-struct WindowLayout {
-    static constexpr int kSub = D / 64;
-    // stage: Q | K (P_lo over both once S is computed) | V
-    static constexpr uint32_t kQ = 0;
-    static constexpr uint32_t kK = kQ + kSub * tc::kSubTileBytes;
-    static constexpr uint32_t kV = kK + (kSub > 1 ? kSub : 1) * tc::kSubTileBytes;
-    static constexpr uint32_t kStage = kV + kSub * tc::kSubTileBytes;
-    static constexpr uint32_t kBar = 2 * kStage;  // ld[2], s, o
-    static constexpr uint32_t kTmemSlot = kBar + 32;
-    static constexpr uint32_t kBytes = kTmemSlot + 8;
-    static constexpr uint32_t kSmem = kBytes + 1024;
-    static constexpr uint32_t kTmemCols = 256;  // S / P_hi in [0, 128), O in [128, 128 + D)
-    static constexpr uint32_t kColO = 128;
-    static_assert(D == 64, "the persistent window kernel keeps P_lo over Q and K (head_dim 64)");
-};
-
-template <int D>
-__global__ void __launch_bounds__(128, 2)
-    window_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                     const __grid_constant__ CUtensorMap tm_v, const AttnTcArgs a, int n_items,
-                     unsigned int *status) {
-    using L = WindowLayout<D>;
-    extern __shared__ uint8_t smem_raw[];
-    const uint32_t raw = smem_u32(smem_raw);
-    const uint32_t sb = (raw + 1023u) & ~1023u;
-    uint8_t *smem = smem_raw + (sb - raw);
-    const int tid = threadIdx.x, warp = tid >> 5;
-    const uint32_t bar_ld = sb + L::kBar, bar_s = bar_ld + 16, bar_o = bar_ld + 24;
-    const bool cu_ok = a.cu[a.n_seg] == a.total;
-
-    if (tid == 0) {
-        mbar_init(bar_ld, 1);
-        mbar_init(bar_ld + 8, 1);
-        mbar_init(bar_s, 1);
-        mbar_init(bar_o, 1);
-        fence_mbar_init();
-        tc::prefetch_tmap(&tm_q);
-        tc::prefetch_tmap(&tm_k);
-        tc::prefetch_tmap(&tm_v);
-    }
-    if (warp == 0) tc::tmem_alloc(sb + L::kTmemSlot, L::kTmemCols);
-    tc::fence_before();
-    __syncthreads();
-    tc::fence_after();
-    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + L::kTmemSlot);
-    const uint32_t t_row = tmem + ((uint32_t)(warp * 32) << 16);
-    const int r = tid;
-    const uint32_t sw = (uint32_t)(r & 7);
-
-    // Loads Q (query tile qt), K and V (key tile kt) of job j into stage st;
-    // a job with a malformed window gets a plain arrival (no data) so that
-    // every stage use completes exactly one phase.
-    auto load = [&](int j, int st, int qt, int kt) {
-        const int w = j / a.hq, h = j % a.hq;
-        const int s0 = a.cu[w], s1 = a.cu[w + 1];
-        const uint32_t base = sb + st * L::kStage, bar = bar_ld + 8 * st;
-        if (!cu_ok || !(0 <= s0 && s0 <= s1 && s1 <= a.total) || s1 == s0) {
-            mbar_arrive(bar);
-            return;
-        }
-        mbar_arrive_expect_tx(bar, 3 * L::kSub * tc::kSubTileBytes);
-#pragma unroll
-        for (int sd = 0; sd < L::kSub; ++sd) {
-            tc::tma_load_3d(base + L::kQ + sd * tc::kSubTileBytes, &tm_q, sd * 64, h, s0 + qt * 128, bar);
-            tc::tma_load_3d(base + L::kK + sd * tc::kSubTileBytes, &tm_k, sd * 64, h, s0 + kt * 128, bar);
-            tc::tma_load_3d(base + L::kV + sd * tc::kSubTileBytes, &tm_v, sd * 64, h, s0 + kt * 128, bar);
-        }
-    };
-
-    uint32_t ph_ld[2] = {0u, 0u}, ph_s = 0, ph_o = 0;
-    if (tid == 0 && (int)blockIdx.x < n_items) load(blockIdx.x, 0, 0, 0);
-    int k = 0;
-    for (int j = blockIdx.x; j < n_items; j += gridDim.x, ++k) {
-        const int st = k & 1;
-        const uint32_t base = sb + st * L::kStage;
-        // prefetch the next job into the other stage (its last user, job k - 1, is done)
-        if (tid == 0 && j + (int)gridDim.x < n_items) load(j + gridDim.x, st ^ 1, 0, 0);
-        const int w = j / a.hq, h = j % a.hq;
-        const int s0 = a.cu[w], s1 = a.cu[w + 1];
-        const bool ok = cu_ok && 0 <= s0 && s0 <= s1 && s1 <= a.total;
-        if (!ok && tid == 0) atomicOr(status, QA_DEVICE_BAD_SEGMENTS);
-        const int n_tiles = ok ? (s1 - s0 + 127) / 128 : 0;
-        if (n_tiles == 0) {  // nothing to compute; still consume the stage's phase
-            if (tid == 0) mbar_wait(bar_ld + 8 * st, ph_ld[st], status);
-            ph_ld[st] ^= 1;
-            continue;
-        }
-        for (int qt = 0; qt < n_tiles; ++qt) {
-            const int qi = s0 + qt * 128 + r;
-            float m = -INFINITY, l = 0.f;
-            for (int kt = 0; kt < n_tiles; ++kt) {
-                const int k0 = s0 + kt * 128;
-                if (tid == 0) {
-                    if (qt > 0 || kt > 0) load(j, st, qt, kt);  // further tiles: synchronous, same stage
-                    mbar_wait(bar_ld + 8 * st, ph_ld[st], status);
-                    tc::fence_after();
-                    issue_s<D>(tmem, base + L::kQ, base + L::kK);
-                    tc::mma_commit(bar_s);
-                }
-                ph_ld[st] ^= 1;
-                mbar_wait(bar_s, ph_s, status);
-                ph_s ^= 1;
-                tc::fence_after();
-                const int n_ok = max(min(128, s1 - k0), 0);
-                softmax_tile<D>(t_row, n_ok, a.scale_log2, base + L::kQ + r * 128, sw, t_row + L::kColO, kt > 0, m, l);
-                tc::fence_proxy_async_smem();
-                tc::fence_before();
-                __syncthreads();
-                if (tid == 0) {
-                    tc::fence_after();
-                    issue_pv<D>(tmem, tmem + L::kColO, base + L::kQ, base + L::kV, kt > 0);
-                    tc::mma_commit(bar_o);
-                }
-                mbar_wait(bar_o, ph_o, status);
-                ph_o ^= 1;
-                tc::fence_after();
-            }
-            store_rows<D>(t_row + L::kColO, l, a.out + ((size_t)qi * a.hq + h) * D, qi < s1);
-            tc::fence_before();
-            __syncthreads();  // O and the stage are free before the next tile's MMAs and loads
-        }
-    }
-
-    if (warp == 0) {
-        tc::fence_after();
-        tc::tmem_dealloc(tmem, L::kTmemCols);
-    }
-}
-
 }  // namespace qa

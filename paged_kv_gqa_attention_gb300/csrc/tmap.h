@@ -1,7 +1,6 @@
-// Host helpers of the tensor-core attention launches: tiled TMA descriptors
+// Host helper of the tensor-core attention launches: tiled TMA descriptors
 // for packed [T][H][D] bf16 tensors (boxes of 128 rows x 64 dims of one head,
-// 128-byte swizzling: the operand layout of attn_tc.cuh) and the persistent
-// grid size.
+// 128-byte swizzling: the operand layout of attn_tc.cuh).
 #pragma once
 
 #include <cuda.h>
@@ -37,16 +36,6 @@ inline bool make_rows_tmap(CUtensorMap *map, const void *base, int D, int H, int
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
-}
-
-// Persistent grid size: per_sm CTAs on every SM of the current device, no
-// more CTAs than jobs.  0 when no device answers.
-inline int persistent_grid(int n_items, int per_sm) {
-    int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) return 0;
-    const int slots = sms * per_sm;
-    return n_items < slots ? (n_items > 0 ? n_items : 1) : slots;
 }
 
 }  // namespace qa

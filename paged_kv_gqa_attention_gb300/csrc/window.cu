@@ -5,11 +5,9 @@
 // bidirectional MHA scaled by 1/sqrt(head_dim).  M* "Speech recognition:
 // Whisper and Qwen3-ASR", "Graph": one packed forward per batch with one
 // segment per window of every request.  Row t of window w attends over every
-// row of w and nothing else.  Runs on the tensor cores (attn_tc.cuh): for
-// head_dim 64 a persistent grid of two CTAs per SM walks (window, head) jobs
-// and prefetches the next job's tiles during the current one; head_dim 128
-// takes one CTA per (window, head).  A 104-token window is one 128-row tile;
-// longer windows loop over query and key tiles.
+// row of w and nothing else.  Runs on the tensor cores (attn_tc.cuh): one CTA
+// per (window, head), four CTAs per SM; a 104-token window is one 128-row
+// tile, longer windows loop over query and key tiles.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -43,18 +41,13 @@ cudaError_t launch_window(const void *q, const void *k, const void *v, const int
     unsigned int *status = nullptr;
     cudaError_t e = cudaGetSymbolAddress(reinterpret_cast<void **>(&status), g_status);
     if (e != cudaSuccess) return e;
+    const dim3 grid(n_windows, p.n_q_heads);
     if (p.head_dim == 64) {
-        // persistent: two CTAs per SM walking (window, head) jobs
-        const long long items = (long long)n_windows * p.n_q_heads;
-        if (items > 0x7fffffffLL) return cudaErrorInvalidValue;
-        const int grid = persistent_grid((int)items, 2);
-        if (grid <= 0) return cudaErrorInvalidDevice;
-        constexpr uint32_t smem = WindowLayout<64>::kSmem;
-        e = cudaFuncSetAttribute(window_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        constexpr uint32_t smem = AttnTcLayout<64>::kSmem;
+        e = cudaFuncSetAttribute(attn_tc_kernel<64, 1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
-        window_tc_kernel<64><<<grid, 128, smem, stream>>>(tq, tk, tv, a, (int)items, status);
+        attn_tc_kernel<64, 1, false><<<grid, 128, smem, stream>>>(tq, tk, tv, a, status);
     } else {
-        const dim3 grid(n_windows, p.n_q_heads);
         constexpr uint32_t smem = AttnTcLayout<128>::kSmem;
         e = cudaFuncSetAttribute(attn_tc_kernel<128, 1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;

@@ -422,7 +422,7 @@ def _row_prefill(qa, device, stream, peaks, steps, rows):
                        "tflops": round(fl / t / 1e12, 3), "gbs": round(by / t / 1e9, 1),
                        "frac_bf16_peak": round(fl / t / 1e12 / peaks["bf16"], 4),
                        "frac_hbm": round(by / t / 1e9 / peaks["hbm"], 4), "flops": fl, "bytes": by,
-                       "gpu_launches_per_call": 2}
+                       "gpu_launches_per_call": 1}
 
 
 def _row_window(qa, device, stream, peaks, steps, rows):
@@ -498,7 +498,7 @@ def _row_tiny(qa, device, stream, steps, rows):
     el, _ = graph_time([tiny_step], steps, 5, stream)
     rows["tiny"] = {"workload": "tiny: prefill of 64 tokens into 4 permuted pages, then 1 decode token",
                     "us_per_step": round(el / steps * 1e6, 2), "note": "latency-bound; no roofline fraction",
-                    "gpu_launches_per_step": 3}
+                    "gpu_launches_per_step": 2}
 
 
 def main():

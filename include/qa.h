@@ -188,7 +188,12 @@ qa_status qa_decode_attn_noalloc(const void *q, const void *k_pages, const void 
  * n_past = 0, the cache was rewound), and computes
  * out[t][h] = softmax over j <= t within the request of q[t][h] . k[j][g]
  * (g = h / group) times v[j][g], from the packed k and v.  Pool slots that no
- * row maps to are left untouched.
+ * row maps to are left untouched.  Rows are checked on the device: a page id
+ * outside [0, num_pages) sets QA_DEVICE_BAD_PAGE and that row is not written;
+ * a request longer than max_pages_per_seq * page_size sets
+ * QA_DEVICE_BAD_LENGTH, and its rows past that bound are not written to the
+ * pools (nor, past the next multiple of 128, attended: those out rows are left
+ * as they were).
  * Supported: head_dim 128, page_size 16, n_q_heads / n_kv_heads in {1, 2}. */
 qa_status qa_prefill_attn(const void *q, const void *k, const void *v,
                           const int32_t *cu_seqlens, int batch, int total_tokens,

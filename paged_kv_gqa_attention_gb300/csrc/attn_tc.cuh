@@ -9,6 +9,9 @@
 //      sub-tiles) and the Q tile into shared memory.
 //   2. One thread issues S = Q K^T (M = 128, N = 128 keys, K = D in steps of
 //      16) into TMEM columns [0, 128) and commits to an mbarrier.
+//      Causal prefill, diagonal key tile (the query tile's own rows), first
+//      query head of each KV head: while S is computed, the CTA copies the
+//      K and V rows of the tile from shared memory to their KV-cache pages.
 //   3. Thread r owns query row r (= TMEM lane r): it reads its scores with
 //      tcgen05.ld, keeps the first n_ok keys of the tile (the rest lie outside
 //      the segment or, causal, after the row), runs the online softmax in fp32
@@ -54,6 +57,10 @@ struct AttnTcArgs {
     uint16_t *out;      // [T][hq][D]
     int n_seg, total, hq;
     float scale_log2;
+    // causal prefill: the KV page write (k_pages == nullptr: none)
+    const int32_t *page_table;     // [n_seg][max_pages]
+    uint16_t *k_pages, *v_pages;   // [num_pages][page_size][hkv][D]
+    int hkv, max_pages, num_pages, page_size;
 };
 
 template <int D>
@@ -224,6 +231,38 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem, uint32_t o_col, uint32_t
     }
 }
 
+// KV page write from the K and V tiles in shared memory (128B-swizzled 64-dim
+// sub-tiles): tile row rr is row i0 + rr of segment seg and goes, bit for bit,
+// to slot i % page_size of page page_table[seg][i / page_size], KV head g.
+// Rows at or past len, or past max_pages * page_size, are not written; a page
+// id outside [0, num_pages) sets QA_DEVICE_BAD_PAGE and skips the row.  Each
+// row is written by D / 8 adjacent threads (16 bytes each), so one warp store
+// covers whole 256-byte rows.
+template <int D>
+__device__ __forceinline__ void write_kv_pages(const uint8_t *k_tile, const uint8_t *v_tile, const AttnTcArgs &a,
+                                               int seg, int i0, int len, int g, unsigned int *status) {
+    constexpr int kChunks = D / 8;              // 16-byte chunks per row
+    constexpr int kRowsPerPass = 128 / kChunks;
+    const int c = threadIdx.x % kChunks;
+    const uint32_t sub = (uint32_t)(c >> 3) * tc::kSubTileBytes;
+    const int end = min(len, a.max_pages * a.page_size) - i0;
+    const int32_t *pt = a.page_table + (size_t)seg * a.max_pages;
+    for (int rr = threadIdx.x / kChunks; rr < min(end, 128); rr += kRowsPerPass) {
+        const int i = i0 + rr;
+        const int page = pt[i / a.page_size];
+        if (page < 0 || page >= a.num_pages) {
+            if (c == 0) atomicOr(status, QA_DEVICE_BAD_PAGE);
+            continue;
+        }
+        const uint32_t off = (uint32_t)rr * 128u + sub + ((uint32_t)((c & 7) ^ (rr & 7)) << 4);
+        const uint4 kx = *reinterpret_cast<const uint4 *>(k_tile + off);
+        const uint4 vx = *reinterpret_cast<const uint4 *>(v_tile + off);
+        const size_t dst = (((size_t)page * a.page_size + i % a.page_size) * a.hkv + g) * D + (size_t)c * 8;
+        *reinterpret_cast<uint4 *>(a.k_pages + dst) = kx;
+        *reinterpret_cast<uint4 *>(a.v_pages + dst) = vx;
+    }
+}
+
 // CAUSAL: grid (hq, segments, q-tiles), one query tile per CTA.
 // !CAUSAL: grid (segments, hq), every query tile of the segment in turn.
 template <int D, int GROUP, bool CAUSAL>
@@ -252,6 +291,10 @@ __global__ void __launch_bounds__(128, 4)
         // the query tile is the slowest-varying grid coordinate, reversed
         qt0 = (int)(gridDim.z - 1 - blockIdx.z);
         qt1 = qt0 + 1;
+        // a request longer than its page-table row: flagged once, its rows past
+        // the row's capacity are neither written nor (beyond the grid) attended
+        if (a.k_pages && qt0 == 0 && h == 0 && tid == 0 && s1 - s0 > a.max_pages * a.page_size)
+            atomicOr(status, QA_DEVICE_BAD_LENGTH);
         if (qt0 >= n_tiles) return;
     } else {
         qt0 = 0;
@@ -307,6 +350,14 @@ __global__ void __launch_bounds__(128, 4)
                 tc::fence_after();
                 issue_s<D>(tmem, sb + L::kQ, sb + L::kK);
                 tc::mma_commit(bar_s);
+            }
+            if (CAUSAL && kt == qt && a.k_pages && h % GROUP == 0) {
+                // the diagonal key tile holds this query tile's own K/V rows:
+                // one query head per KV head writes them to their pages while
+                // S is computed, before P_lo overwrites the K tile
+                mbar_wait(bar_ld, ph_ld, status);
+                write_kv_pages<D>(smem + L::kK, smem + L::kV, a, seg, qt * 128, s1 - s0, g, status);
+                __syncthreads();
             }
             ph_ld ^= 1;
             mbar_wait(bar_s, ph_s, status);

@@ -1,9 +1,12 @@
-// Ragged causal prefill: the KV page write and the causal attention.
+// Ragged causal prefill: the causal attention with the KV page write fused in.
 //
 // Page write (qwenasr.cpp ARCHITECTURE.md, "Qwen3 Thinker decoder": prefill
 // rewinds the cache and writes the fresh K/V of the whole prompt span at
 // [n_past, n_past + T) with n_past = 0): row i of request r is copied bit for
-// bit to slot i % 16 of page page_table[r][i / 16], for K and V.
+// bit to slot i % 16 of page page_table[r][i / 16], for K and V.  The CTA of
+// query tile t and the first query head of each KV head writes the rows of
+// tile t from its diagonal K/V tile, already in shared memory for the
+// attention, so the prompt's K and V are read from HBM once for both.
 //
 // Attention: row i of request r attends over rows j <= i of the same request
 // (same section: attend over [0, n_past + T)), GQA group h / 2, from the
@@ -24,73 +27,12 @@ namespace {
 
 __device__ unsigned int g_status;
 
-struct PageWriteArgs {
-    const uint4 *k, *v;  // [T][row_chunks] 16-byte chunks
-    const int32_t *cu;
-    const int32_t *page_table;
-    uint4 *k_pages, *v_pages;
-    int batch, total, max_pages, num_pages, page_size, row_chunks;
-};
-
-// One CTA per packed row; thread c copies 16-byte chunk c of the row's K and
-// V (row_chunks = Hkv * D * 2 / 16 chunks).
-__global__ void page_write_kernel(const PageWriteArgs a) {
-    const int t = blockIdx.x;
-    int lo = 0, hi = a.batch - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (a.cu[mid] <= t) lo = mid; else hi = mid - 1;
-    }
-    const int r0 = a.cu[lo], r1 = a.cu[lo + 1];
-    if (!(0 <= r0 && r0 <= t && t < r1 && r1 <= a.total) || a.cu[a.batch] != a.total) {
-        if (threadIdx.x == 0) atomicOr(&g_status, QA_DEVICE_BAD_SEGMENTS);
-        return;
-    }
-    const int i = t - r0;
-    if (i >= a.max_pages * a.page_size) {
-        if (threadIdx.x == 0) atomicOr(&g_status, QA_DEVICE_BAD_LENGTH);
-        return;
-    }
-    const int page = a.page_table[(size_t)lo * a.max_pages + i / a.page_size];
-    if (page < 0 || page >= a.num_pages) {
-        if (threadIdx.x == 0) atomicOr(&g_status, QA_DEVICE_BAD_PAGE);
-        return;
-    }
-    const size_t dst = ((size_t)page * a.page_size + i % a.page_size) * a.row_chunks;
-    const size_t src = (size_t)t * a.row_chunks;
-    for (int c = threadIdx.x; c < a.row_chunks; c += blockDim.x) {
-        a.k_pages[dst + c] = a.k[src + c];
-        a.v_pages[dst + c] = a.v[src + c];
-    }
-}
-
 }  // namespace
 
-cudaError_t launch_page_write(const void *k, const void *v, const int32_t *cu_seqlens, int batch,
-                              int total_tokens, const int32_t *page_table, void *k_pages,
-                              void *v_pages, const qa_attn_params &p, cudaStream_t stream) {
-    if (total_tokens == 0) return cudaSuccess;
-    PageWriteArgs a;
-    a.k = static_cast<const uint4 *>(k);
-    a.v = static_cast<const uint4 *>(v);
-    a.cu = cu_seqlens;
-    a.page_table = page_table;
-    a.k_pages = static_cast<uint4 *>(k_pages);
-    a.v_pages = static_cast<uint4 *>(v_pages);
-    a.batch = batch;
-    a.total = total_tokens;
-    a.max_pages = p.max_pages_per_seq;
-    a.num_pages = p.num_pages;
-    a.page_size = p.page_size;
-    a.row_chunks = p.n_kv_heads * p.head_dim * 2 / 16;
-    const int threads = a.row_chunks < 128 ? ((a.row_chunks + 31) / 32) * 32 : 128;
-    page_write_kernel<<<total_tokens, threads, 0, stream>>>(a);
-    return cudaGetLastError();
-}
-
 cudaError_t launch_prefill(const void *q, const void *k, const void *v, const int32_t *cu_seqlens,
-                           int batch, int total_tokens, void *out, const qa_attn_params &p,
-                           float scale, cudaStream_t stream) {
+                           int batch, int total_tokens, const int32_t *page_table, void *k_pages,
+                           void *v_pages, void *out, const qa_attn_params &p, float scale,
+                           cudaStream_t stream) {
     if (total_tokens == 0) return cudaSuccess;
     if (batch > 65535) return cudaErrorInvalidValue;
     CUtensorMap tq, tk, tv;
@@ -98,13 +40,20 @@ cudaError_t launch_prefill(const void *q, const void *k, const void *v, const in
         !make_rows_tmap(&tk, k, p.head_dim, p.n_kv_heads, total_tokens) ||
         !make_rows_tmap(&tv, v, p.head_dim, p.n_kv_heads, total_tokens))
         return cudaErrorInvalidValue;
-    AttnTcArgs a;
+    AttnTcArgs a{};
     a.cu = cu_seqlens;
     a.out = static_cast<uint16_t *>(out);
     a.n_seg = batch;
     a.total = total_tokens;
     a.hq = p.n_q_heads;
     a.scale_log2 = scale * kLog2e;
+    a.page_table = page_table;
+    a.k_pages = static_cast<uint16_t *>(k_pages);
+    a.v_pages = static_cast<uint16_t *>(v_pages);
+    a.hkv = p.n_kv_heads;
+    a.max_pages = p.max_pages_per_seq;
+    a.num_pages = p.num_pages;
+    a.page_size = p.page_size;
     unsigned int *status = nullptr;
     cudaError_t e = cudaGetSymbolAddress(reinterpret_cast<void **>(&status), g_status);
     if (e != cudaSuccess) return e;

@@ -173,11 +173,9 @@ QA_API qa_status qa_prefill_attn(const void *q, const void *k, const void *v, co
         !aligned(v_pages, 16) || !aligned(cu_seqlens, 4) || !aligned(page_table, 4))
         return fail(QA_STATUS_INVALID_PARAMS, "%s: tensors must be 16-byte aligned (int32 arrays 4-byte)", fn);
     cudaStream_t stream = static_cast<cudaStream_t>(p->stream);
-    st = launch_result(
-        qa::launch_page_write(k, v, cu_seqlens, batch, total_tokens, page_table, k_pages, v_pages, *p, stream), fn);
-    if (st != QA_STATUS_OK) return st;
-    st = launch_result(
-        qa::launch_prefill(q, k, v, cu_seqlens, batch, total_tokens, out, *p, effective_scale(p), stream), fn);
+    st = launch_result(qa::launch_prefill(q, k, v, cu_seqlens, batch, total_tokens, page_table, k_pages, v_pages, out,
+                                          *p, effective_scale(p), stream),
+                       fn);
     if (st != QA_STATUS_OK || !p->debug_checks) return st;
     cudaError_t e;
     const unsigned int bits = qa::status_read_clear_prefill(stream, &e);

@@ -23,13 +23,11 @@ cudaError_t launch_decode(const void *q, const void *k_pages, const void *v_page
                           const qa_attn_params &p, float scale, int ctas, cudaStream_t stream);
 unsigned int status_read_clear_decode(cudaStream_t stream, cudaError_t *err);
 
-// ---- prefill (prefill.cu): page write + causal attention
-cudaError_t launch_page_write(const void *k, const void *v, const int32_t *cu_seqlens, int batch,
-                              int total_tokens, const int32_t *page_table, void *k_pages,
-                              void *v_pages, const qa_attn_params &p, cudaStream_t stream);
+// ---- prefill (prefill.cu): causal attention with the KV page write fused in
 cudaError_t launch_prefill(const void *q, const void *k, const void *v, const int32_t *cu_seqlens,
-                           int batch, int total_tokens, void *out, const qa_attn_params &p,
-                           float scale, cudaStream_t stream);
+                           int batch, int total_tokens, const int32_t *page_table, void *k_pages,
+                           void *v_pages, void *out, const qa_attn_params &p, float scale,
+                           cudaStream_t stream);
 unsigned int status_read_clear_prefill(cudaStream_t stream, cudaError_t *err);
 
 // ---- window (window.cu)

@@ -31,7 +31,7 @@ cudaError_t launch_window(const void *q, const void *k, const void *v, const int
         !make_rows_tmap(&tk, k, p.head_dim, p.n_kv_heads, total_tokens) ||
         !make_rows_tmap(&tv, v, p.head_dim, p.n_kv_heads, total_tokens))
         return cudaErrorInvalidValue;
-    AttnTcArgs a;
+    AttnTcArgs a{};
     a.cu = cu_windows;
     a.out = static_cast<uint16_t *>(out);
     a.n_seg = n_windows;

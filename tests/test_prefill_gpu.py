@@ -76,3 +76,20 @@ def test_bad_page_id_is_reported_not_faulted():
     with pytest.raises(qa.QAError) as e:
         run_prefill(w, debug_checks=True)
     assert e.value.status == -6
+
+
+def test_overlong_request_is_reported_and_clipped():
+    # request 0 has 40 rows but its page-table row holds 2 pages (32 rows)
+    w = wl.prefill_workload(11, (40, 5), num_pages=8, max_pages=3)
+    w["page_table"] = np.ascontiguousarray(w["page_table"][:, :2])
+    d = {k: to_dev(w[k]) for k in ("q", "k", "v", "cu_seqlens", "page_table", "k_pages", "v_pages")}
+    with pytest.raises(qa.QAError) as e:
+        qa.qa_prefill_attn(d["q"], d["k"], d["v"], d["cu_seqlens"], d["page_table"], d["k_pages"], d["v_pages"],
+                           debug_checks=True)
+    assert e.value.status == -6 and "bad length" in str(e.value)
+    # rows [0, 32) of request 0 and all of request 1 reach the pools, nothing else
+    keep = np.r_[0:32, 40:45]
+    ekp, evp = oracle.page_write(w["k"][keep], w["v"][keep], np.array([0, 32, 37], np.int32), w["page_table"],
+                                 w["k_pages"], w["v_pages"])
+    np.testing.assert_array_equal(bits(d["k_pages"]), ekp)
+    np.testing.assert_array_equal(bits(d["v_pages"]), evp)

@@ -18,9 +18,12 @@ arithmetic:
   (13 * 8 = 104 by default), the last one partial (same page, "Windowed audio
   tower"; GGUF keys n_window 50 and n_window_infer 800 in "GGUF layout").
 
-Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
-(brute force, torch float64 SDPA, mpmath, closed forms, invariants, printed
-values under ``tests/golden/``).
+Parity status: every function here is pinned: the attention functions by
+``tests/test_oracle_pins.py`` (brute force, torch float64 SDPA, mpmath,
+closed forms, invariants, printed values under ``tests/golden/``), QK-norm,
+RoPE and the decode append by ``tests/test_oracle_rope_pins.py`` (torch
+float64 ``rms_norm``, closed-form rotations, rotation invariants, a numpy
+scatter of the append).
 """
 from __future__ import annotations
 
@@ -69,6 +72,10 @@ def bind_library(path: str):
     lib.oracle_page_write.restype = I
     lib.oracle_window.argtypes = [P, P, P, P, I, I, I, I, Dbl, P, I, P, I]
     lib.oracle_window.restype = I
+    lib.oracle_qk_norm_rope.argtypes = [P, I, I, I, P, P, Dbl, Dbl, P]
+    lib.oracle_qk_norm_rope.restype = I
+    lib.oracle_decode_append.argtypes = [P, P, P, P, P, Dbl, Dbl, P, P, I, I, I, I, I, I, I, P, P, P, P, P]
+    lib.oracle_decode_append.restype = I
     return lib
 
 
@@ -178,6 +185,48 @@ def window(q, k, v, cu_windows, *, scale=None, rows=None, n_threads=0):
     if rc != 0:
         raise ValueError("oracle_window rejected its arguments")
     return out.reshape(T, H, D) if rows_a is None else out
+
+
+def _f32(a):
+    return np.ascontiguousarray(a, dtype=np.float32)
+
+
+def qk_norm_rope(x, pos, gain, *, eps, theta):
+    """Per-head RMSNorm (gain [D] float32) then NEOX RoPE at pos[t] for every
+    head of row t.  x [T,H,D] bf16 bits.  Returns float64 [T,H,D]."""
+    x, pos, gain = _u16(x), _i32(pos), _f32(gain)
+    T, H, D = x.shape
+    assert pos.shape == (T,) and gain.shape == (D,)
+    out = np.zeros((T, H, D), np.float64)
+    rc = _load().oracle_qk_norm_rope(_ptr(x), T, H, D, _ptr(pos), _ptr(gain), float(eps), float(theta), _ptr(out))
+    if rc != 0:
+        raise ValueError("oracle_qk_norm_rope rejected its arguments")
+    return out
+
+
+def decode_append(q, k, v, q_gain, k_gain, page_table, seq_lens, k_pages, v_pages, *, eps, theta):
+    """Decode KV append: QK-norm + NEOX RoPE of the new token (position
+    seq_lens[b] - 1), its K/V written into the pools.  Returns a dict with
+    q_rot/k_rot (float64, before rounding), q (bf16 bits, rounded) and the new
+    k_pages/v_pages arrays."""
+    q, k, v = _u16(q), _u16(k), _u16(v)
+    q_gain, k_gain = _f32(q_gain), _f32(k_gain)
+    page_table, seq_lens = _i32(page_table), _i32(seq_lens)
+    kp, vp = _u16(k_pages).copy(), _u16(v_pages).copy()
+    B, Hq, D = q.shape
+    Hkv = k.shape[1]
+    P, PS, Hkv2, D2 = kp.shape
+    assert Hkv2 == Hkv and D2 == D and v.shape == k.shape and page_table.shape[0] == B
+    q_rot = np.zeros((B, Hq, D), np.float64)
+    k_rot = np.zeros((B, Hkv, D), np.float64)
+    q_bf16 = np.zeros((B, Hq, D), np.uint16)
+    rc = _load().oracle_decode_append(_ptr(q), _ptr(k), _ptr(v), _ptr(q_gain), _ptr(k_gain), float(eps),
+                                      float(theta), _ptr(page_table), _ptr(seq_lens), B, Hq, Hkv, D, PS,
+                                      page_table.shape[1], P, _ptr(q_rot), _ptr(k_rot), _ptr(q_bf16), _ptr(kp),
+                                      _ptr(vp))
+    if rc != 0:
+        raise ValueError("oracle_decode_append rejected its arguments")
+    return dict(q_rot=q_rot, k_rot=k_rot, q=q_bf16, k_pages=kp, v_pages=vp)
 
 
 def after_cnn_len(mel_len: int) -> int:

@@ -49,6 +49,21 @@
  *   mask over windows, plain bidirectional MHA scaled by 1/sqrt(head_dim);
  *   M* page, "Qwen3-ASR / Graph": one packed forward, one segment per window).
  *
+ *   QK-norm and RoPE (qwenasr.cpp ARCHITECTURE.md, "Qwen3 Thinker decoder":
+ *   per-head RMSNorm on q and k, RMS over head_dim then a [head_dim] gain,
+ *   before a 1D NEOX RoPE with freq_base 1e6; "Attention and RoPE": rotate
+ *   half).  For one head vector x at position pos:
+ *       y[d] = x[d] / sqrt(mean_d x[d]^2 + eps) * gain[d]
+ *       a_i  = pos * theta^(-2 i / D),  i in [0, D/2)
+ *       z[i]       = y[i] cos a_i - y[i + D/2] sin a_i
+ *       z[i + D/2] = y[i] sin a_i + y[i + D/2] cos a_i
+ *
+ *   Decode append: the new token of request b sits at cur_len =
+ *   seq_lens[b] - 1 ("appends one position at cur_len and attends over
+ *   [0, cur_len + 1)"); q and k are normalised and rotated at that position,
+ *   rounded to bf16 at the operator boundary, and k with the untouched v go
+ *   to slot cur_len % page_size of page page_table[b][cur_len / page_size].
+ *
  * Threads: rows are independent; n_threads worker threads take contiguous
  * slices of the row list.  This is the only concession to speed.
  */
@@ -374,5 +389,103 @@ ORACLE_EXPORT int oracle_window(const uint16_t *q, const uint16_t *k, const uint
             return -1;
     window_ctx c = {q, k, v, cu_windows, n_windows, H, D, scale};
     run_rows(&c, window_row, rows, n_rows, D, out, n_threads);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Per-head QK-norm, NEOX RoPE and the decode KV append.                      */
+
+/* z[0..D) = RoPE_pos(RMSNorm(x) * gain) for one head vector (file header). */
+static void norm_rope_vec(const uint16_t *x, int D, long pos, const float *gain, double eps,
+                          double theta, double *z)
+{
+    double ms = 0.0;
+    for (int d = 0; d < D; ++d) {
+        double xd = bf16_to_double(x[d]);
+        ms += xd * xd;
+    }
+    ms /= D;
+    double r = 1.0 / sqrt(ms + eps);
+    int half = D / 2;
+    for (int i = 0; i < half; ++i) {
+        double y0 = bf16_to_double(x[i]) * r * (double)gain[i];
+        double y1 = bf16_to_double(x[i + half]) * r * (double)gain[i + half];
+        double a = (double)pos * pow(theta, -2.0 * i / D);
+        double ca = cos(a), sa = sin(a);
+        z[i] = y0 * ca - y1 * sa;
+        z[i + half] = y0 * sa + y1 * ca;
+    }
+}
+
+/* x [n_rows][H][D] bf16, row t at position pos[t]; out [n_rows][H][D]. */
+ORACLE_EXPORT int oracle_qk_norm_rope(const uint16_t *x, int n_rows, int H, int D,
+                                      const int32_t *pos, const float *gain, double eps,
+                                      double theta, double *out)
+{
+    if (n_rows < 0 || H <= 0 || D <= 0 || D % 2)
+        return -1;
+    for (int t = 0; t < n_rows; ++t)
+        for (int h = 0; h < H; ++h) {
+            size_t o = ((size_t)t * H + h) * D;
+            norm_rope_vec(x + o, D, pos[t], gain, eps, theta, out + o);
+        }
+    return 0;
+}
+
+/* bf16 at an operator boundary: the value as a binary32 (round to nearest),
+ * then to bf16, round to nearest even (finite values). */
+static uint16_t bf16_round(double v)
+{
+    float f = (float)v;
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    u += 0x7FFFu + ((u >> 16) & 1u);
+    return (uint16_t)(u >> 16);
+}
+
+/* One new token per request (file header, "Decode append").  q [B][Hq][D],
+ * k and v [B][Hkv][D] bf16; gains [D] float.  Writes q_rot [B][Hq][D] and
+ * k_rot [B][Hkv][D] (double, before rounding), q_bf16 [B][Hq][D] (rounded),
+ * and the token's K (rounded) and V rows into the pools.  Returns -1 and
+ * writes nothing on a length outside [1, max_pages * page_size] or a page id
+ * outside [0, num_pages). */
+ORACLE_EXPORT int oracle_decode_append(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                                       const float *q_gain, const float *k_gain, double eps,
+                                       double theta, const int32_t *page_table,
+                                       const int32_t *seq_lens, int batch, int Hq, int Hkv, int D,
+                                       int page_size, int max_pages, int num_pages, double *q_rot,
+                                       double *k_rot, uint16_t *q_bf16, uint16_t *k_pages,
+                                       uint16_t *v_pages)
+{
+    if (batch < 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || D % 2 || page_size <= 0)
+        return -1;
+    for (int b = 0; b < batch; ++b) {
+        int n = seq_lens[b];
+        if (n < 1 || n > max_pages * page_size)
+            return -1;
+        int page = page_table[(size_t)b * max_pages + (n - 1) / page_size];
+        if (page < 0 || page >= num_pages)
+            return -1;
+    }
+    for (int b = 0; b < batch; ++b) {
+        int cur = seq_lens[b] - 1; /* the new token's position */
+        for (int h = 0; h < Hq; ++h) {
+            size_t o = ((size_t)b * Hq + h) * D;
+            norm_rope_vec(q + o, D, cur, q_gain, eps, theta, q_rot + o);
+            for (int d = 0; d < D; ++d)
+                q_bf16[o + d] = bf16_round(q_rot[o + d]);
+        }
+        int page = page_table[(size_t)b * max_pages + cur / page_size];
+        int slot = cur % page_size;
+        for (int g = 0; g < Hkv; ++g) {
+            size_t o = ((size_t)b * Hkv + g) * D;
+            size_t dst = (((size_t)page * page_size + slot) * Hkv + g) * D;
+            norm_rope_vec(k + o, D, cur, k_gain, eps, theta, k_rot + o);
+            for (int d = 0; d < D; ++d) {
+                k_pages[dst + d] = bf16_round(k_rot[o + d]);
+                v_pages[dst + d] = v[o + d];
+            }
+        }
+    }
     return 0;
 }

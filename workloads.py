@@ -13,6 +13,9 @@ Recipe (identical for every consumer):
 * values are N(0, 1) float32 rounded to bf16 with round-to-nearest-even and
   kept as their uint16 bit patterns, so the oracle and the GPU see identical
   bits;
+* decode-append inputs (the new token's pre-norm q/k/v and the two RMSNorm
+  gains) come after those draws, or from the stream PCG64([seed, 1]) when
+  they extend a named workload, so that workload's own draws stay unchanged;
 * a KV pool starts as all-NaN sentinels (bf16 0x7FC0); pages are handed to the
   requests in the order of a seeded permutation of the whole pool; each
   request's page-table row is padded with -1; slots past a request's length
@@ -144,6 +147,47 @@ def encoder_tokens_for_frames(n_frames: int) -> int:
     100-frame chunk, and ceil(r / 8) for a final chunk of r frames (three
     stride-2 convolutions)."""
     return 13 * (n_frames // 100) + -(-(n_frames % 100) // 8)
+
+
+# Decode-append parameters of the Qwen3 Thinker (qwenasr.cpp ARCHITECTURE.md,
+# "GGUF layout": rope.freq_base 1e6; the RMS epsilon key carries no value
+# there, and the Qwen3 decoders of the TTS page state 1e-6).
+ROPE_THETA = 1.0e6
+RMS_EPS = 1.0e-6
+
+
+def append_inputs(rng: np.random.Generator, batch: int, hq: int = HQ, hkv: int = HKV, d: int = D_DEC,
+                  x_scale: float = 1.0) -> dict:
+    """Pre-norm q/k/v projections of one new token per request (N(0, 1) times
+    x_scale, rounded to bf16) and the two [d] RMSNorm gains (U[0.5, 1.5],
+    bf16-representable, stored as float32).  Draw order q, k, v, q gain, k gain."""
+    def proj(shape):
+        return bf16_bits(rng.standard_normal(size=shape, dtype=np.float32) * np.float32(x_scale))
+
+    def gain():
+        g = bf16_bits(rng.uniform(0.5, 1.5, size=d).astype(np.float32))
+        return bf16_to_f64(g).astype(np.float32)
+
+    q, k, v = proj((batch, hq, d)), proj((batch, hkv, d)), proj((batch, hkv, d))
+    return dict(q_new=q, k_new=k, v_new=v, q_gain=gain(), k_gain=gain(), rope_theta=ROPE_THETA, rms_eps=RMS_EPS)
+
+
+def decode_append_workload(seed: int, lengths, num_pages: int, max_pages: int, x_scale: float = 1.0) -> dict:
+    """decode_workload plus the new token of every request: seq_lens count it,
+    its slot (position seq_lens - 1) already holds random K/V that the append
+    overwrites."""
+    rng = rng_for(seed)
+    w = _decode_from_rng(rng, np.asarray(lengths, np.int32), num_pages, max_pages, HQ, HKV, D_DEC)
+    w.update(append_inputs(rng, len(lengths), x_scale=x_scale))
+    return w
+
+
+def with_append(w: dict, seed: int) -> dict:
+    """A named decode workload plus new-token inputs drawn from a second
+    stream of the same seed (the workload's own draws are unchanged)."""
+    w = dict(w)
+    w.update(append_inputs(np.random.Generator(np.random.PCG64([seed, 1])), len(w["seq_lens"])))
+    return w
 
 
 def tiny(seed: int = 1) -> dict:

@@ -23,7 +23,7 @@ pinned host memory and the output copied back and read every step),
 `cpu_baseline` (the fp64 oracle on this host's cores, whole workload),
 `rows` (the other hot-path operations measured the same way: ragged causal
 prefill with page write, AuT windowed attention, long-context decode, the
-tiny case).  With --impl reference the oracle itself is timed as the
+decode step with the QK-norm + RoPE KV append, the tiny case).  With --impl reference the oracle itself is timed as the
 reference arm.
 """
 from __future__ import annotations
@@ -374,7 +374,7 @@ def run_ours(args, world, rank, local_rank):
         print(json.dumps(line))
 
 
-ROW_NAMES = ("prefill", "window", "decode_long", "tiny")
+ROW_NAMES = ("prefill", "window", "decode_long", "decode_step", "tiny")
 
 
 def measure_rows(qa, device, stream, peaks, args, which=ROW_NAMES):
@@ -390,6 +390,8 @@ def measure_rows(qa, device, stream, peaks, args, which=ROW_NAMES):
         _row_window(qa, device, stream, peaks, steps, rows)
     if "decode_long" in which:
         _row_decode_long(qa, device, stream, peaks, steps, rows)
+    if "decode_step" in which:
+        _row_decode_step(qa, device, stream, peaks, steps, rows)
     if "tiny" in which:
         _row_tiny(qa, device, stream, steps, rows)
     status = qa.qa_device_status(stream)
@@ -477,6 +479,59 @@ def _row_decode_long(qa, device, stream, peaks, steps, rows):
     torch.cuda.empty_cache()
 
 
+def append_bytes(batch, hq=16, hkv=8, d=128):
+    """Algorithmic bytes of one decode append: the new token's q, k, v read,
+    the two gains, the rotated q written and the K/V slot rows written."""
+    return batch * d * 2 * (hq + 2 * hkv) * 2 + 2 * d * 4
+
+
+def _row_decode_step(qa, device, stream, peaks, steps, rows):
+    """Decode step of the 0.6B workload: QK-norm + RoPE + KV append, then the
+    paged decode (two launches, the second launched early)."""
+    import torch
+
+    w = wl.with_append(wl.decode_0p6b(), 2)
+    B = len(w["seq_lens"])
+    pt, sl = dev_tensor(w["page_table"], device), dev_tensor(w["seq_lens"], device)
+    gq, gk = dev_tensor(w["q_gain"], device), dev_tensor(w["k_gain"], device)
+    cps = []
+    for _ in range(4):  # layer copies: new-token projections and the pools (> L2 in all)
+        cps.append({k: dev_tensor(w[k], device) for k in ("q_new", "k_new", "v_new", "k_pages", "v_pages")})
+    ws = torch.zeros(qa.qa_decode_workspace_size(B, int(w["seq_lens"].max()), num_pages=4096, max_pages_per_seq=125),
+                     dtype=torch.uint8, device=device)
+    q_rot = torch.empty(B, 16, 128, dtype=torch.bfloat16, device=device)
+    outd = torch.empty(B, 16, 128, dtype=torch.bfloat16, device=device)
+
+    def fused(c):
+        return lambda: qa.qa_decode_step(c["q_new"], c["k_new"], c["v_new"], gq, gk, pt, sl, c["k_pages"],
+                                         c["v_pages"], outd, workspace=ws, rms_eps=w["rms_eps"],
+                                         rope_theta=w["rope_theta"], stream=stream)
+
+    def two_calls(c):
+        def step():
+            qa.qa_decode_append(c["q_new"], c["k_new"], c["v_new"], gq, gk, pt, sl, c["k_pages"], c["v_pages"],
+                                q_out=q_rot, rms_eps=w["rms_eps"], rope_theta=w["rope_theta"], stream=stream)
+            qa.qa_decode_attn(q_rot, c["k_pages"], c["v_pages"], pt, sl, outd, workspace=ws, stream=stream)
+        return step
+
+    n = max(20, steps // 2)
+    el, _ = graph_time([fused(c) for c in cps], n, 5, stream)
+    t = el / n
+    el2, _ = graph_time([two_calls(c) for c in cps], n, 5, stream)
+    t2 = el2 / n
+    by = decode_bytes(w["seq_lens"]) + append_bytes(B)
+    rows["decode_step"] = {"workload": "decode step 0.6B: per-head QK-norm + NEOX RoPE (theta 1e6) + KV append of "
+                                       "the new token and paged GQA decode (qa_decode_step, one launch); "
+                                       "32 requests, L~U[200,2000]",
+                           "us_per_step": round(t * 1e6, 2), "gbs": round(by / t / 1e9, 1),
+                           "frac_hbm": round(by / t / 1e9 / peaks["hbm"], 4), "bytes": by,
+                           "tokens_per_s": round(B / t, 1), "gpu_launches_per_step": 1,
+                           "us_per_step_two_calls": round(t2 * 1e6, 2),
+                           "two_calls": "qa_decode_append then qa_decode_attn (2 launches)"}
+    del cps
+    torch.cuda.empty_cache()
+
+
 def _row_tiny(qa, device, stream, steps, rows):
     """Tiny: prefill of 64 tokens then one decode token (latency)."""
     import torch
@@ -508,7 +563,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--rows", default="all",
-                    help="other hot-path rows to measure: all, none, or a comma list of prefill,window,decode_long,tiny")
+                    help="other hot-path rows to measure: all, none, or a comma list of prefill,window,decode_long,decode_step,tiny")
     ap.add_argument("--no-cpu", action="store_true", help="skip the cpu_baseline leg")
     args = ap.parse_args()
     if args.warmup < 3:

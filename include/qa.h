@@ -200,6 +200,68 @@ qa_status qa_prefill_attn(const void *q, const void *k, const void *v,
                           const int32_t *page_table, void *k_pages, void *v_pages, void *out,
                           const qa_attn_params *params);
 
+/* Decode KV append with per-head QK-norm and NEOX RoPE (one new token per
+ * request), the step that precedes qa_decode_attn in a decode layer.
+ *
+ * qwenasr.cpp ARCHITECTURE.md, "Qwen3 Thinker decoder": per layer, q and k
+ * get a per-head RMSNorm (RMS over head_dim, then a [head_dim] gain), then a
+ * 1D NEOX RoPE (freq_base 1e6; "Attention and RoPE": rotate half); decode
+ * appends the new token at position cur_len and attends over
+ * [0, cur_len + 1).  With cur = seq_lens[b] - 1 and D = head_dim:
+ *
+ *   y[d] = x[d] / sqrt(mean_d x[d]^2 + rms_eps) * gain[d]
+ *   a_i  = cur * rope_theta^(-2 i / D),                 i in [0, D/2)
+ *   z[i] = y[i] cos a_i - y[i + D/2] sin a_i,  z[i + D/2] = y[i] sin a_i + y[i + D/2] cos a_i
+ *
+ *   q          bf16 [batch][n_q_heads][head_dim]   pre-norm query projection
+ *   k, v       bf16 [batch][n_kv_heads][head_dim]  pre-norm key, value projections
+ *   q_gain, k_gain  float [head_dim]               the two RMSNorm gains
+ *   rms_eps    > 0 (1e-6 for the Qwen3 decoders); rope_theta > 0 (1e6)
+ *   page_table, seq_lens  as in qa_decode_attn; seq_lens[b] >= 1 counts the
+ *              new token
+ *   k_pages, v_pages  pools [num_pages][page_size][n_kv_heads][head_dim]:
+ *              slot cur % page_size of page page_table[b][cur / page_size]
+ *              receives z of k (bf16) and v unchanged
+ *   q_out      bf16 [batch][n_q_heads][head_dim]: z of q (bf16), the query
+ *              for qa_decode_attn; may be q itself (in place), must not
+ *              otherwise overlap an input
+ *
+ * Arithmetic in fp32.  Each angle is carried as an exact sum of fp32 terms
+ * (frequencies computed on the host in fp64, passed as fp32 hi + lo parts)
+ * and reduced modulo 2 pi by the Cody-Waite three-constant scheme before an
+ * fp32 sin/cos; results rounded to bf16, nearest even.  One launch (one CTA per
+ * request), asynchronous on params->stream, launched so that a following
+ * qa_decode_attn on the same stream can start its launch early.  Device
+ * checks: seq_lens[b] outside [1, max_pages_per_seq * page_size] sets
+ * QA_DEVICE_BAD_LENGTH and a page id outside [0, num_pages) sets
+ * QA_DEVICE_BAD_PAGE; such a request is skipped entirely (q_out row
+ * unwritten).  params->scale is not used.
+ * Supported: head_dim 128, page_size 16, n_q_heads / n_kv_heads in {1, 2},
+ * max_pages_per_seq * page_size <= 262144 (positions below 2^18). */
+qa_status qa_decode_append(const void *q, const void *k, const void *v, const float *q_gain,
+                           const float *k_gain, float rms_eps, float rope_theta,
+                           const int32_t *page_table, const int32_t *seq_lens, int batch,
+                           void *k_pages, void *v_pages, void *q_out, const qa_attn_params *params);
+
+/* The fused decode step: qa_decode_append and qa_decode_attn in one launch.
+ *
+ * Same arguments and results as calling qa_decode_append (q, k, v, gains,
+ * rms_eps, rope_theta, pools, page_table, seq_lens) and then qa_decode_attn
+ * on its rotated query (workspace, scale and out as in qa_decode_attn), but
+ * the rotated query never leaves the chip: every CTA normalises and rotates
+ * the query heads it reads, and the CTA that holds a request's last page
+ * normalises and rotates the new key, writes the new K/V row to its slot and
+ * uses it from shared memory in place of the slot's old contents.  No grid
+ * waits on another.  The rotated query is rounded to bf16 before use, as in
+ * the two-call sequence; results agree with it up to fp32 evaluation order.
+ * Device checks as in both calls (a request with seq_lens[b] = 0 sets
+ * QA_DEVICE_BAD_LENGTH here, since it has no new token).
+ * Supported: as qa_decode_append; k, v and the gains 16-byte aligned. */
+qa_status qa_decode_step(const void *q, const void *k, const void *v, const float *q_gain,
+                         const float *k_gain, float rms_eps, float rope_theta, void *k_pages,
+                         void *v_pages, const int32_t *page_table, const int32_t *seq_lens,
+                         int batch, void *out, const qa_attn_params *params);
+
 /* Windowed bidirectional attention over a packed sequence.
  *
  *   q, k, v    bf16 [total_tokens][n_q_heads][head_dim] (n_kv_heads must equal

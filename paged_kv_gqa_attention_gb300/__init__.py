@@ -73,6 +73,10 @@ def _load():
     lib.qa_decode_attn_noalloc.argtypes = [P, P, P, P, P, I, P, PP]
     lib.qa_prefill_attn.restype = I
     lib.qa_prefill_attn.argtypes = [P, P, P, P, I, I, P, P, P, P, PP]
+    lib.qa_decode_append.restype = I
+    lib.qa_decode_append.argtypes = [P, P, P, P, P, ctypes.c_float, ctypes.c_float, P, P, I, P, P, P, PP]
+    lib.qa_decode_step.restype = I
+    lib.qa_decode_step.argtypes = [P, P, P, P, P, ctypes.c_float, ctypes.c_float, P, P, P, P, I, P, PP]
     lib.qa_window_attn.restype = I
     lib.qa_window_attn.argtypes = [P, P, P, P, I, I, P, PP]
     lib.qa_window_plan.restype = I
@@ -236,6 +240,70 @@ def qa_prefill_attn(q, k, v, cu_seqlens, page_table, k_pages, v_pages, out=None,
                               _dev(v_pages, "v_pages", torch.bfloat16, 4), _dev(out, "out", torch.bfloat16, 3),
                               ctypes.byref(p))
     _check("qa_prefill_attn", st)
+    return out
+
+
+def qa_decode_append(q, k, v, q_gain, k_gain, page_table, seq_lens, k_pages, v_pages, q_out=None, *,
+                     rms_eps=1e-6, rope_theta=1e6, stream=None, debug_checks=False):
+    """Decode KV append: per-head RMSNorm (gains float32 [D]) and NEOX RoPE
+    of the new token at position seq_lens[b] - 1, its K/V written into the
+    pools.  q bf16 [B,Hq,D]; k/v bf16 [B,Hkv,D]; page_table int32
+    [B,max_pages]; seq_lens int32 [B]; pools bf16 [P,16,Hkv,D] (written in
+    place).  Returns q_out bf16 [B,Hq,D], the rotated query (q_out=q is
+    allowed: in place)."""
+    torch = _torch()
+    B, Hq, D = q.shape
+    Hkv = k.shape[1]
+    P, PS = k_pages.shape[0], k_pages.shape[1]
+    if tuple(k.shape) != (B, Hkv, D) or tuple(v.shape) != (B, Hkv, D) or page_table.shape[0] != B:
+        raise ValueError("inconsistent append shapes")
+    if tuple(q_gain.shape) != (D,) or tuple(k_gain.shape) != (D,):
+        raise ValueError("gains must be [head_dim]")
+    if q_out is None:
+        q_out = torch.empty_like(q)
+    p = _params(n_q_heads=Hq, n_kv_heads=Hkv, head_dim=D, page_size=PS, num_pages=P,
+                max_pages_per_seq=page_table.shape[1], stream=stream, debug_checks=debug_checks)
+    st = _lib.qa_decode_append(_dev(q, "q", torch.bfloat16, 3), _dev(k, "k", torch.bfloat16, 3),
+                               _dev(v, "v", torch.bfloat16, 3), _dev(q_gain, "q_gain", torch.float32, 1),
+                               _dev(k_gain, "k_gain", torch.float32, 1), float(rms_eps), float(rope_theta),
+                               _dev(page_table, "page_table", torch.int32, 2), _dev(seq_lens, "seq_lens", torch.int32, 1),
+                               B, _dev(k_pages, "k_pages", torch.bfloat16, 4), _dev(v_pages, "v_pages", torch.bfloat16, 4),
+                               _dev(q_out, "q_out", torch.bfloat16, 3), ctypes.byref(p))
+    _check("qa_decode_append", st)
+    return q_out
+
+
+def qa_decode_step(q, k, v, q_gain, k_gain, page_table, seq_lens, k_pages, v_pages, out=None, *, workspace=None,
+                   rms_eps=1e-6, rope_theta=1e6, scale=0.0, stream=None, debug_checks=False):
+    """The fused decode step: qa_decode_append (QK-norm + NEOX RoPE of the
+    new token at seq_lens[b] - 1, its K/V written into the pools) and
+    qa_decode_attn on the rotated query, in one launch.  q pre-norm bf16
+    [B,Hq,D]; k/v bf16 [B,Hkv,D]; gains float32 [D]; workspace as for
+    qa_decode_attn.  Returns out bf16 [B,Hq,D]."""
+    torch = _torch()
+    B, Hq, D = q.shape
+    P, PS, Hkv, D2 = k_pages.shape
+    if (D2 != D or tuple(v_pages.shape) != tuple(k_pages.shape) or page_table.dim() != 2 or page_table.shape[0] != B
+            or tuple(k.shape) != (B, Hkv, D) or tuple(v.shape) != (B, Hkv, D)):
+        raise ValueError("inconsistent decode-step shapes")
+    if tuple(q_gain.shape) != (D,) or tuple(k_gain.shape) != (D,):
+        raise ValueError("gains must be [head_dim]")
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None:
+        nbytes = qa_decode_workspace_size(B, 0, n_q_heads=Hq, n_kv_heads=Hkv, head_dim=D, page_size=PS,
+                                          num_pages=P, max_pages_per_seq=page_table.shape[1])
+        workspace = torch.zeros(nbytes, dtype=torch.uint8, device=q.device)
+    p = _params(n_q_heads=Hq, n_kv_heads=Hkv, head_dim=D, page_size=PS, num_pages=P,
+                max_pages_per_seq=page_table.shape[1], scale=scale, stream=stream, workspace=workspace,
+                debug_checks=debug_checks)
+    st = _lib.qa_decode_step(_dev(q, "q", torch.bfloat16, 3), _dev(k, "k", torch.bfloat16, 3),
+                             _dev(v, "v", torch.bfloat16, 3), _dev(q_gain, "q_gain", torch.float32, 1),
+                             _dev(k_gain, "k_gain", torch.float32, 1), float(rms_eps), float(rope_theta),
+                             _dev(k_pages, "k_pages", torch.bfloat16, 4), _dev(v_pages, "v_pages", torch.bfloat16, 4),
+                             _dev(page_table, "page_table", torch.int32, 2), _dev(seq_lens, "seq_lens", torch.int32, 1),
+                             B, _dev(out, "out", torch.bfloat16, 3), ctypes.byref(p))
+    _check("qa_decode_step", st)
     return out
 
 

@@ -74,6 +74,35 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
     return d;
 }
 
+// cos/sin of pos * f for an integer position 0 <= pos < 2^18 and a frequency
+// f = f_hi + f_lo (f_hi = f rounded to fp32, f_lo the fp32 rounding of the
+// rest), in fp32 without fp64 arithmetic: the product is carried as
+// a_hi + a_lo + pos * f_lo (a_lo the exact FMA residual of pos * f_hi), and
+// reduced modulo 2 pi by the three-constant Cody-Waite scheme (W. J. Cody and
+// W. Waite, "Software Manual for the Elementary Functions", 1980): 2 pi =
+// C1 + C2 + C3 with C1 = 6.28125 (8 significant bits), so n * C1 is exact for
+// n < 2^16 and the first subtraction is exact.  The reduced angle is within a
+// few fp32 ulps of the true one, then an fp32 sincos.
+__device__ __forceinline__ void sincos_pos_freq(int pos, float f_hi, float f_lo, float *s, float *c) {
+    constexpr double kTwoPiD = 6.283185307179586476925286766559;
+    constexpr float kC1 = 6.28125f;
+    constexpr float kC2 = (float)(kTwoPiD - 6.28125);
+    constexpr float kC3 = (float)(kTwoPiD - 6.28125 - (double)(float)(kTwoPiD - 6.28125));
+    constexpr float kInvTwoPi = (float)(1.0 / kTwoPiD);
+    const float p = (float)pos;
+    const float a_hi = p * f_hi;
+    const float a_lo = fmaf(p, f_hi, -a_hi) + p * f_lo;
+    const float n = rintf(a_hi * kInvTwoPi);
+    float r = fmaf(-n, kC1, a_hi);
+    r = fmaf(-n, kC2, r);
+    r = fmaf(-n, kC3, r);
+    sincosf(r + a_lo, s, c);
+}
+
+__device__ __forceinline__ void prefetch_l2(const void *p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);

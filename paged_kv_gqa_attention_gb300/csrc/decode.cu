@@ -38,6 +38,7 @@
 // Every consumer waits on every stage it reads, in order, so no mbarrier
 // phase is ever skipped.
 #include <cuda_runtime.h>
+#include <math.h>
 #include <stdint.h>
 
 #include "common.cuh"
@@ -65,13 +66,54 @@ struct DecodeArgs {
     int *arrivals;    // [kDecodeMaxBatch][kMaxHkv], zero between calls
     int batch, hkv, max_pages, num_pages;
     float scale_log2;  // scale * log2(e)
+    // fused decode step only: q is the pre-norm projection; the new token's
+    // pre-norm k and its v are appended at position seq_lens[b] - 1
+    const uint16_t *k_new, *v_new;  // [B][Hkv][D]
+    const float *q_gain, *k_gain;   // [D]
+    uint8_t *k_pages_w, *v_pages_w; // the pools, written at the new token's slot
+    float eps;
+    // theta^(-2i/D), computed on the host in fp64, as fp32 hi + lo parts
+    float freq_hi[kD / 2], freq_lo[kD / 2];
 };
+
+// Per-head QK-norm and NEOX RoPE of one head vector spread over a warp
+// (qwenasr.cpp ARCHITECTURE.md, "Qwen3 Thinker decoder": RMSNorm over
+// head_dim with a [head_dim] gain, then rotate-half RoPE).  Lane l holds dims
+// [4l, 4l + 4) in x01/x23; dim d pairs with d +- 64, which lives on lane
+// l ^ 16.  cs/sn: cos/sin of the angles of the lane's four pairs.  Returns
+// the rotated dims rounded to bf16 (the operator boundary), as two packed
+// words.  Warp-collective.
+__device__ __forceinline__ uint2 norm_rope4(float2 x01, float2 x23, const float *gain, float eps, const float *cs,
+                                            const float *sn, int lane) {
+    const float ss = warp_sum(x01.x * x01.x + x01.y * x01.y + x23.x * x23.x + x23.y * x23.y);
+    const float r = 1.0f / sqrtf(ss * (1.0f / kD) + eps);
+    const float4 gn = *reinterpret_cast<const float4 *>(gain + 4 * lane);
+    const float y[4] = {x01.x * r * gn.x, x01.y * r * gn.y, x23.x * r * gn.z, x23.y * r * gn.w};
+    float z[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        const float p = __shfl_xor_sync(0xffffffffu, y[c], 16);  // the pair's other element
+        z[c] = lane < 16 ? y[c] * cs[c] - p * sn[c] : p * sn[c] + y[c] * cs[c];
+    }
+    return make_uint2(pack_bf16x2(z[0], z[1]), pack_bf16x2(z[2], z[3]));
+}
+
+// cos/sin of the angles pos * theta^(-2i/D) of pairs i = 4 (l mod 16) + c
+// (positions below 2^18; the host rejects longer page tables).
+__device__ __forceinline__ void rope_angles(const DecodeArgs &a, int pos, int lane, float *cs, float *sn) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        const int i = 4 * (lane & 15) + c;
+        sincos_pos_freq(pos, a.freq_hi[i], a.freq_lo[i], &sn[c], &cs[c]);
+    }
+}
 
 // Pages request b contributes; invalid lengths contribute none (and are
 // reported once by CTA 0).
+template <bool APPEND>
 __device__ __forceinline__ int pages_of(const DecodeArgs &a, int b, bool report) {
     int L = a.seq_lens[b];
-    if (L < 0 || L > a.max_pages * kPS) {
+    if (L < (APPEND ? 1 : 0) || L > a.max_pages * kPS) {
         if (report) atomicOr(&g_status, QA_DEVICE_BAD_LENGTH);
         return 0;
     }
@@ -143,8 +185,8 @@ __device__ __forceinline__ void bf16x4(uint2 w, float2 &lo, float2 &hi) {
     hi = make_float2(bf16lo(w.y), bf16hi(w.y));
 }
 
-template <int GROUP>
-__global__ void __launch_bounds__((kMaxHkv + 1) * 32, 1) decode_splitk_kernel(const DecodeArgs a) {
+template <int GROUP, bool APPEND>
+__global__ void __launch_bounds__((kMaxHkv + 1) * 32, 1) decode_splitk_kernel(const __grid_constant__ DecodeArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
     const SmemLayout L = smem_layout(a.hkv, a.batch, GROUP);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -152,7 +194,7 @@ __global__ void __launch_bounds__((kMaxHkv + 1) * 32, 1) decode_splitk_kernel(co
     const int hq = a.hkv * GROUP;
 
     int *prefix = reinterpret_cast<int *>(smem + L.off_prefix);
-    int *page_ok = reinterpret_cast<int *>(smem + L.off_flag);
+    int *page_ok = reinterpret_cast<int *>(smem + L.off_flag);  // page id of each stage, -1 if invalid
     const uint32_t bar_full_k = smem_u32(smem + L.off_bar);
     const uint32_t bar_full_v = bar_full_k + kStages * 8;
     const uint32_t bar_empty = bar_full_v + kStages * 8;
@@ -169,7 +211,7 @@ __global__ void __launch_bounds__((kMaxHkv + 1) * 32, 1) decode_splitk_kernel(co
         if (lane == 0) prefix[0] = 0;
         for (int base = 0; base < a.batch; base += 32) {
             int b = base + lane;
-            int v = b < a.batch ? pages_of(a, b, blockIdx.x == 0) : 0;
+            int v = b < a.batch ? pages_of<APPEND>(a, b, blockIdx.x == 0) : 0;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
                 int u = __shfl_up_sync(0xffffffffu, v, o);
@@ -212,6 +254,25 @@ __global__ void __launch_bounds__((kMaxHkv + 1) * 32, 1) decode_splitk_kernel(co
     const int b_last = first_request_past(prefix, a.batch, hi - 1);
     const int n_visit = b_last - b0 + 1;
 
+    // Warm L2 with the per-request rows read at the start of every later
+    // segment (q; for the fused step the new token's k and v too), so those
+    // segments do not start with a round trip to HBM.
+    if (warp < n_consumers) {
+        for (int k = 1 + lane; k < n_visit; k += 32) {
+            const int b = b0 + k - 1;
+            const uint8_t *qrow = reinterpret_cast<const uint8_t *>(a.q + ((size_t)b * hq + warp * GROUP) * kD);
+#pragma unroll
+            for (int o = 0; o < GROUP * kD * 2; o += 128) prefetch_l2(qrow + o);
+            if (APPEND) {
+                const size_t o = ((size_t)b * a.hkv + warp) * kD;
+                prefetch_l2(a.k_new + o);
+                prefetch_l2(a.k_new + o + 64);
+                prefetch_l2(a.v_new + o);
+                prefetch_l2(a.v_new + o + 64);
+            }
+        }
+    }
+
     if (warp == n_consumers) {
         // ---------------- producer warp: lanes fetch page ids, lane 0 issues copies
         const uint64_t policy = policy_evict_first();
@@ -233,11 +294,11 @@ __global__ void __launch_bounds__((kMaxHkv + 1) * 32, 1) decode_splitk_kernel(co
                         uint8_t *dst = smem + s * L.stage_bytes;
                         if (page < 0 || page >= a.num_pages) {
                             atomicOr(&g_status, QA_DEVICE_BAD_PAGE);
-                            page_ok[s] = 0;
+                            page_ok[s] = -1;
                             mbar_arrive(bar_full_k + 8 * s);
                             mbar_arrive(bar_full_v + 8 * s);
                         } else {
-                            page_ok[s] = 1;
+                            page_ok[s] = page;
                             const size_t off = (size_t)page * L.page_bytes;
                             mbar_arrive_expect_tx(bar_full_k + 8 * s, L.page_bytes);
                             bulk_g2s_hint(smem_u32(dst), a.k_pages + off, L.page_bytes, bar_full_k + 8 * s, policy);
@@ -272,10 +333,30 @@ __global__ void __launch_bounds__((kMaxHkv + 1) * 32, 1) decode_splitk_kernel(co
         const int seq_len = a.seq_lens[b];
 
         float2 q01[GROUP], q23[GROUP], acc01[GROUP], acc23[GROUP];
+        // fused step: the new token's K/V rows for KV head g (rotated k,
+        // bf16) when this segment holds the request's last page
+        const bool has_new = APPEND && j1 == p1 - p0;
+        uint2 k_new_w = make_uint2(0u, 0u), v_new_w = make_uint2(0u, 0u);
+        float cs[4], sn[4];
+        if (APPEND) {
+            rope_angles(a, seq_len - 1, lane, cs, sn);
+            if (has_new) {
+                const size_t o = ((size_t)b * a.hkv + g) * kD + 4 * lane;
+                float2 k01, k23;
+                bf16x4(*reinterpret_cast<const uint2 *>(a.k_new + o), k01, k23);
+                k_new_w = norm_rope4(k01, k23, a.k_gain, a.eps, cs, sn, lane);
+                v_new_w = *reinterpret_cast<const uint2 *>(a.v_new + o);
+            }
+        }
 #pragma unroll
         for (int i = 0; i < GROUP; ++i) {
-            const uint2 w = *reinterpret_cast<const uint2 *>(
+            uint2 w = *reinterpret_cast<const uint2 *>(
                 a.q + ((size_t)b * hq + g * GROUP + i) * kD + 4 * lane);
+            if (APPEND) {
+                float2 x01, x23;
+                bf16x4(w, x01, x23);
+                w = norm_rope4(x01, x23, a.q_gain, a.eps, cs, sn, lane);
+            }
             bf16x4(w, q01[i], q23[i]);
             q01[i].x *= a.scale_log2;
             q01[i].y *= a.scale_log2;
@@ -291,10 +372,20 @@ __global__ void __launch_bounds__((kMaxHkv + 1) * 32, 1) decode_splitk_kernel(co
             const uint32_t phase = (it / kStages) & 1;
             mbar_wait(bar_full_k + 8 * s, phase, &g_status);
             const int nt = min(kPS, seq_len - j * kPS);
-            if (page_ok[s] && nt > 0) {
-                const uint8_t *Ks = smem + s * L.stage_bytes + (g * kD + 4 * lane) * 2;
-                const uint8_t *Vs = Ks + L.page_bytes;
+            const int page = page_ok[s];
+            // fused step: this page holds the new token (last slot in use)
+            const bool patch = APPEND && has_new && j == j1 - 1 && page >= 0;
+            if (page >= 0 && nt > 0) {
+                uint8_t *Ks = smem + s * L.stage_bytes + (g * kD + 4 * lane) * 2;
+                uint8_t *Vs = Ks + L.page_bytes;
                 const int row_stride = a.hkv * kD * 2;
+                if (patch) {
+                    // the row this lane reads is its own 8 bytes: no warp sync needed
+                    const size_t off = ((size_t)page * kPS + (nt - 1)) * row_stride + (g * kD + 4 * lane) * 2;
+                    *reinterpret_cast<uint2 *>(Ks + (nt - 1) * row_stride) = k_new_w;
+                    *reinterpret_cast<uint2 *>(a.k_pages_w + off) = k_new_w;
+                    *reinterpret_cast<uint2 *>(a.v_pages_w + off) = v_new_w;
+                }
                 // partial dots of every (token, head); rows past the sequence
                 // (sentinels, possibly NaN) only ever touch their own entry
                 float v[NV];
@@ -353,6 +444,7 @@ __global__ void __launch_bounds__((kMaxHkv + 1) * 32, 1) decode_splitk_kernel(co
                 if (p_writer) pbuf[GROUP == 2 ? lane : (lane >> 1)] = make_float2(p, p);
                 __syncwarp();
                 mbar_wait(bar_full_v + 8 * s, phase, &g_status);
+                if (patch) *reinterpret_cast<uint2 *>(Vs + (nt - 1) * row_stride) = v_new_w;
                 if (nt == kPS) {
 #pragma unroll
                     for (int t = 0; t < kPS; ++t) {
@@ -380,6 +472,8 @@ __global__ void __launch_bounds__((kMaxHkv + 1) * 32, 1) decode_splitk_kernel(co
             } else {
                 mbar_wait(bar_full_v + 8 * s, phase, &g_status);  // the stage is reused only once V landed
             }
+            // generic stores into the stage come before the next bulk copy into it
+            if (patch) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_empty + 8 * s);
         }
@@ -491,7 +585,8 @@ size_t decode_workspace_bytes(int batch, int n_q_heads, int head_dim, int ctas) 
 
 cudaError_t launch_decode(const void *q, const void *k_pages, const void *v_pages,
                           const int32_t *page_table, const int32_t *seq_lens, int batch, void *out,
-                          const qa_attn_params &p, float scale, int ctas, cudaStream_t stream) {
+                          const qa_attn_params &p, float scale, int ctas, cudaStream_t stream,
+                          const DecodeAppend *app) {
     const int group = p.n_q_heads / p.n_kv_heads;
     const WorkspaceLayout W = workspace_layout(batch, p.n_q_heads, ctas);
     uint8_t *ws = static_cast<uint8_t *>(p.workspace);
@@ -510,6 +605,25 @@ cudaError_t launch_decode(const void *q, const void *k_pages, const void *v_page
     a.max_pages = p.max_pages_per_seq;
     a.num_pages = p.num_pages;
     a.scale_log2 = scale * kLog2e;
+    a.k_new = a.v_new = nullptr;
+    a.q_gain = a.k_gain = nullptr;
+    a.k_pages_w = a.v_pages_w = nullptr;
+    a.eps = 0.f;
+    for (int i = 0; i < kD / 2; ++i) a.freq_hi[i] = a.freq_lo[i] = 0.f;
+    if (app) {
+        a.k_new = static_cast<const uint16_t *>(app->k_new);
+        a.v_new = static_cast<const uint16_t *>(app->v_new);
+        a.q_gain = app->q_gain;
+        a.k_gain = app->k_gain;
+        a.k_pages_w = static_cast<uint8_t *>(app->k_pages);
+        a.v_pages_w = static_cast<uint8_t *>(app->v_pages);
+        a.eps = app->rms_eps;
+        for (int i = 0; i < kD / 2; ++i) {
+            const double f = pow((double)app->rope_theta, -2.0 * i / kD);
+            a.freq_hi[i] = (float)f;
+            a.freq_lo[i] = (float)(f - (double)a.freq_hi[i]);
+        }
+    }
 
     const SmemLayout L = smem_layout(a.hkv, batch, group);
     // programmatic dependent launch: the kernel's prologue overlaps the tail of
@@ -524,7 +638,8 @@ cudaError_t launch_decode(const void *q, const void *k_pages, const void *v_page
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    auto kernel = group == 2 ? decode_splitk_kernel<2> : decode_splitk_kernel<1>;
+    auto kernel = app ? (group == 2 ? decode_splitk_kernel<2, true> : decode_splitk_kernel<1, true>)
+                      : (group == 2 ? decode_splitk_kernel<2, false> : decode_splitk_kernel<1, false>);
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
     if (e != cudaSuccess) return e;
     e = cudaLaunchKernelEx(&cfg, kernel, a);

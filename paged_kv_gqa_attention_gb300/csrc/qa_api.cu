@@ -30,6 +30,10 @@ void clear_error() { t_last_error[0] = '\0'; }
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
+// RoPE angles are reduced in fp32 with an exact first step for positions
+// below 2^18 (sincos_pos_freq).
+constexpr int kMaxRopePositions = 1 << 18;
+
 qa_status check_common(const qa_attn_params *p, const char *fn) {
     if (!p) return fail(QA_STATUS_INVALID_PARAMS, "%s: params is NULL", fn);
     if (p->abi_version < QA_ABI_MIN_VERSION || p->abi_version > QA_ABI_VERSION)
@@ -125,10 +129,12 @@ QA_API size_t qa_decode_workspace_size(int batch, int max_seq_len, const qa_attn
     return qa::decode_workspace_bytes(batch, p->n_q_heads, p->head_dim, ctas);
 }
 
-QA_API qa_status qa_decode_attn(const void *q, const void *k_pages, const void *v_pages, const int32_t *page_table,
-                                const int32_t *seq_lens, int batch, void *out, const qa_attn_params *p) {
-    const char *fn = "qa_decode_attn";
-    clear_error();
+namespace {
+
+// Shared by qa_decode_attn and qa_decode_step (app != nullptr).
+qa_status decode_entry(const char *fn, const void *q, const void *k_pages, const void *v_pages,
+                       const int32_t *page_table, const int32_t *seq_lens, int batch, void *out,
+                       const qa_attn_params *p, const qa::DecodeAppend *app) {
     qa_status st = check_common(p, fn);
     if (st != QA_STATUS_OK) return st;
     if ((st = check_gqa(p, fn)) != QA_STATUS_OK) return st;
@@ -147,12 +153,40 @@ QA_API qa_status qa_decode_attn(const void *q, const void *k_pages, const void *
                     need, p->workspace_bytes);
     cudaStream_t stream = static_cast<cudaStream_t>(p->stream);
     st = launch_result(qa::launch_decode(q, k_pages, v_pages, page_table, seq_lens, batch, out, *p,
-                                         effective_scale(p), ctas, stream),
+                                         effective_scale(p), ctas, stream, app),
                        fn);
     if (st != QA_STATUS_OK || !p->debug_checks) return st;
     cudaError_t e;
     const unsigned int bits = qa::status_read_clear_decode(stream, &e);
     return debug_status(bits, e, fn);
+}
+
+}  // namespace
+
+QA_API qa_status qa_decode_attn(const void *q, const void *k_pages, const void *v_pages, const int32_t *page_table,
+                                const int32_t *seq_lens, int batch, void *out, const qa_attn_params *p) {
+    clear_error();
+    return decode_entry("qa_decode_attn", q, k_pages, v_pages, page_table, seq_lens, batch, out, p, nullptr);
+}
+
+QA_API qa_status qa_decode_step(const void *q, const void *k, const void *v, const float *q_gain, const float *k_gain,
+                                float rms_eps, float rope_theta, void *k_pages, void *v_pages,
+                                const int32_t *page_table, const int32_t *seq_lens, int batch, void *out,
+                                const qa_attn_params *p) {
+    const char *fn = "qa_decode_step";
+    clear_error();
+    if (!(rms_eps > 0.f) || !isfinite(rms_eps))
+        return fail(QA_STATUS_INVALID_PARAMS, "%s: rms_eps must be finite and > 0", fn);
+    if (!(rope_theta > 0.f) || !isfinite(rope_theta))
+        return fail(QA_STATUS_INVALID_PARAMS, "%s: rope_theta must be finite and > 0", fn);
+    if (p && (long long)p->max_pages_per_seq * p->page_size > kMaxRopePositions)
+        return fail(QA_STATUS_INVALID_PARAMS, "%s: positions up to %d supported (max_pages_per_seq * page_size = %lld)",
+                    fn, kMaxRopePositions, (long long)p->max_pages_per_seq * p->page_size);
+    if (!k || !v || !q_gain || !k_gain) return fail(QA_STATUS_INVALID_PARAMS, "%s: NULL pointer", fn);
+    if (!aligned(k, 16) || !aligned(v, 16) || !aligned(q_gain, 16) || !aligned(k_gain, 16))
+        return fail(QA_STATUS_INVALID_PARAMS, "%s: k, v and the gains must be 16-byte aligned", fn);
+    qa::DecodeAppend app{k, v, q_gain, k_gain, k_pages, v_pages, rms_eps, rope_theta};
+    return decode_entry(fn, q, k_pages, v_pages, page_table, seq_lens, batch, out, p, &app);
 }
 
 QA_API qa_status qa_prefill_attn(const void *q, const void *k, const void *v, const int32_t *cu_seqlens, int batch,
@@ -179,6 +213,40 @@ QA_API qa_status qa_prefill_attn(const void *q, const void *k, const void *v, co
     if (st != QA_STATUS_OK || !p->debug_checks) return st;
     cudaError_t e;
     const unsigned int bits = qa::status_read_clear_prefill(stream, &e);
+    return debug_status(bits, e, fn);
+}
+
+QA_API qa_status qa_decode_append(const void *q, const void *k, const void *v, const float *q_gain,
+                                  const float *k_gain, float rms_eps, float rope_theta, const int32_t *page_table,
+                                  const int32_t *seq_lens, int batch, void *k_pages, void *v_pages, void *q_out,
+                                  const qa_attn_params *p) {
+    const char *fn = "qa_decode_append";
+    clear_error();
+    qa_status st = check_common(p, fn);
+    if (st != QA_STATUS_OK) return st;
+    if ((st = check_gqa(p, fn)) != QA_STATUS_OK) return st;
+    if (!(rms_eps > 0.f) || !isfinite(rms_eps))
+        return fail(QA_STATUS_INVALID_PARAMS, "%s: rms_eps must be finite and > 0", fn);
+    if (!(rope_theta > 0.f) || !isfinite(rope_theta))
+        return fail(QA_STATUS_INVALID_PARAMS, "%s: rope_theta must be finite and > 0", fn);
+    if ((long long)p->max_pages_per_seq * p->page_size > kMaxRopePositions)
+        return fail(QA_STATUS_INVALID_PARAMS, "%s: positions up to %d supported (max_pages_per_seq * page_size = %lld)",
+                    fn, kMaxRopePositions, (long long)p->max_pages_per_seq * p->page_size);
+    if (batch < 1) return fail(QA_STATUS_INVALID_PARAMS, "%s: batch %d < 1", fn, batch);
+    if (!q || !k || !v || !q_gain || !k_gain || !page_table || !seq_lens || !k_pages || !v_pages || !q_out)
+        return fail(QA_STATUS_INVALID_PARAMS, "%s: NULL pointer", fn);
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(q_out, 16) || !aligned(k_pages, 16) ||
+        !aligned(v_pages, 16) || !aligned(q_gain, 8) || !aligned(k_gain, 8) || !aligned(page_table, 4) ||
+        !aligned(seq_lens, 4))
+        return fail(QA_STATUS_INVALID_PARAMS,
+                    "%s: tensors must be 16-byte aligned (gains 8-byte, int32 arrays 4-byte)", fn);
+    cudaStream_t stream = static_cast<cudaStream_t>(p->stream);
+    st = launch_result(qa::launch_append(q, k, v, q_gain, k_gain, rms_eps, rope_theta, page_table, seq_lens, batch,
+                                         k_pages, v_pages, q_out, *p, stream),
+                       fn);
+    if (st != QA_STATUS_OK || !p->debug_checks) return st;
+    cudaError_t e;
+    const unsigned int bits = qa::status_read_clear_append(stream, &e);
     return debug_status(bits, e, fn);
 }
 
@@ -247,14 +315,14 @@ QA_API int qa_window_plan(const int32_t *token_counts, int n_requests, int windo
 QA_API int qa_device_status(void *stream) {
     clear_error();
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e1, e2, e3;
-    const unsigned int bits = qa::status_read_clear_decode(s, &e1) | qa::status_read_clear_prefill(s, &e2) |
-                              qa::status_read_clear_window(s, &e3);
-    if (e1 != cudaSuccess || e2 != cudaSuccess || e3 != cudaSuccess) {
-        fail(QA_STATUS_LAUNCH_FAILED, "qa_device_status: CUDA error %s",
-             cudaGetErrorString(e1 != cudaSuccess ? e1 : (e2 != cudaSuccess ? e2 : e3)));
-        return -1;
-    }
+    cudaError_t e[4];
+    const unsigned int bits = qa::status_read_clear_decode(s, &e[0]) | qa::status_read_clear_prefill(s, &e[1]) |
+                              qa::status_read_clear_window(s, &e[2]) | qa::status_read_clear_append(s, &e[3]);
+    for (cudaError_t ei : e)
+        if (ei != cudaSuccess) {
+            fail(QA_STATUS_LAUNCH_FAILED, "qa_device_status: CUDA error %s", cudaGetErrorString(ei));
+            return -1;
+        }
     return (int)bits;
 }
 

@@ -18,9 +18,18 @@ size_t decode_workspace_bytes(int batch, int n_q_heads, int head_dim, int ctas);
 // Largest batch the decode kernel accepts (its page prefix sums live in
 // shared memory).
 constexpr int kDecodeMaxBatch = 4096;
+// The fused decode step: q is the pre-norm projection; the new token (pre-norm
+// k, v) is normalised, rotated and appended at position seq_lens[b] - 1.
+struct DecodeAppend {
+    const void *k_new, *v_new;
+    const float *q_gain, *k_gain;
+    void *k_pages, *v_pages;  // the same pools, writable
+    float rms_eps, rope_theta;
+};
 cudaError_t launch_decode(const void *q, const void *k_pages, const void *v_pages,
                           const int32_t *page_table, const int32_t *seq_lens, int batch, void *out,
-                          const qa_attn_params &p, float scale, int ctas, cudaStream_t stream);
+                          const qa_attn_params &p, float scale, int ctas, cudaStream_t stream,
+                          const DecodeAppend *app = nullptr);
 unsigned int status_read_clear_decode(cudaStream_t stream, cudaError_t *err);
 
 // ---- prefill (prefill.cu): causal attention with the KV page write fused in
@@ -29,6 +38,13 @@ cudaError_t launch_prefill(const void *q, const void *k, const void *v, const in
                            void *v_pages, void *out, const qa_attn_params &p, float scale,
                            cudaStream_t stream);
 unsigned int status_read_clear_prefill(cudaStream_t stream, cudaError_t *err);
+
+// ---- decode append (append.cu): QK-norm + NEOX RoPE + page write of the new token
+cudaError_t launch_append(const void *q, const void *k, const void *v, const float *q_gain, const float *k_gain,
+                          float rms_eps, float rope_theta, const int32_t *page_table, const int32_t *seq_lens,
+                          int batch, void *k_pages, void *v_pages, void *q_out, const qa_attn_params &p,
+                          cudaStream_t stream);
+unsigned int status_read_clear_append(cudaStream_t stream, cudaError_t *err);
 
 // ---- window (window.cu)
 cudaError_t launch_window(const void *q, const void *k, const void *v, const int32_t *cu_windows,

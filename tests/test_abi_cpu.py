@@ -63,6 +63,8 @@ int main(void) {
     if (qa_window_attn(NULL, NULL, NULL, NULL, 1, 0, NULL, NULL) != QA_STATUS_INVALID_PARAMS) return 4;
     p.abi_version = QA_ABI_VERSION + 1;
     if (qa_prefill_attn(NULL, NULL, NULL, NULL, 1, 0, NULL, NULL, NULL, NULL, &p) != QA_STATUS_INVALID_PARAMS) return 5;
+    if (qa_decode_append(NULL, NULL, NULL, NULL, NULL, 1e-6f, 1e6f, NULL, NULL, 1, NULL, NULL, NULL, &p) !=
+        QA_STATUS_INVALID_PARAMS) return 9;
     if (qa_window_plan(counts, 2, 0, cu, 8) != 3 || cu[1] != 104 || cu[2] != 117 || cu[3] != 122) return 6;
     printf("%s\n", qa_version());
     return 0;
@@ -119,6 +121,33 @@ def test_invalid_arguments_return_status_without_device(libqa):
     w.n_kv_heads, w.scale = 14, float("nan")
     assert lib.qa_window_attn(fake, fake, fake, fake, 1, 1, fake, ctypes.byref(w)) == -1
     assert "scale" in qa.qa_last_error()
+    # decode append: eps and theta must be positive, pointers non-NULL, gains 8-byte aligned
+    app = lib.qa_decode_append
+    assert app(fake, fake, fake, fake, fake, 0.0, 1e6, fake, fake, 1, fake, fake, fake, ctypes.byref(p)) == -1
+    assert "rms_eps" in qa.qa_last_error()
+    assert app(fake, fake, fake, fake, fake, 1e-6, float("inf"), fake, fake, 1, fake, fake, fake, ctypes.byref(p)) == -1
+    assert "rope_theta" in qa.qa_last_error()
+    assert app(fake, fake, fake, None, fake, 1e-6, 1e6, fake, fake, 1, fake, fake, fake, ctypes.byref(p)) == -1
+    assert "NULL" in qa.qa_last_error()
+    assert app(fake, fake, fake, ctypes.c_void_p(0x1004), fake, 1e-6, 1e6, fake, fake, 1, fake, fake, fake,
+               ctypes.byref(p)) == -1
+    assert "aligned" in qa.qa_last_error()
+    assert app(fake, fake, fake, fake, fake, 1e-6, 1e6, fake, fake, 0, fake, fake, fake, ctypes.byref(p)) == -1
+    assert "batch" in qa.qa_last_error()
+    big = qa.qa_attn_default_params()
+    big.num_pages, big.max_pages_per_seq = 4, 20000  # positions up to 320000 > 2^18
+    assert app(fake, fake, fake, fake, fake, 1e-6, 1e6, fake, fake, 1, fake, fake, fake, ctypes.byref(big)) == -1
+    assert "positions" in qa.qa_last_error()
+    # fused decode step: the append's checks, then the decode's
+    stp = lib.qa_decode_step
+    assert stp(fake, fake, fake, fake, fake, -1.0, 1e6, fake, fake, fake, fake, 1, fake, ctypes.byref(p)) == -1
+    assert "rms_eps" in qa.qa_last_error()
+    assert stp(fake, fake, fake, ctypes.c_void_p(0x1008), fake, 1e-6, 1e6, fake, fake, fake, fake, 1, fake,
+               ctypes.byref(p)) == -1
+    assert "aligned" in qa.qa_last_error()
+    # then the decode's own checks: no workspace (or, on a machine without a GPU, no device)
+    assert stp(fake, fake, fake, fake, fake, 1e-6, 1e6, fake, fake, fake, fake, 1, fake, ctypes.byref(p)) in (-1, -3)
+    assert "workspace" in qa.qa_last_error() or "device" in qa.qa_last_error()
 
 
 def test_window_plan_matches_oracle(libqa):

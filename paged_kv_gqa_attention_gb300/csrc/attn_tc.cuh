@@ -395,4 +395,153 @@ __global__ void __launch_bounds__(128, 4)
     }
 }
 
+// TMA loads of one key tile of a job (and of its query tile when load_q)
+// into the Q/K/V buffers, completing on bar_ld.  One thread.
+template <int D>
+__device__ __forceinline__ void issue_tile_loads(uint32_t sb, const CUtensorMap *tm_q, const CUtensorMap *tm_k,
+                                                 const CUtensorMap *tm_v, int h, int g, int q0, int k0, bool load_q,
+                                                 uint32_t bar_ld) {
+    using L = AttnTcLayout<D>;
+    mbar_arrive_expect_tx(bar_ld, (load_q ? 3 : 2) * L::kSub * tc::kSubTileBytes);
+#pragma unroll
+    for (int sd = 0; sd < L::kSub; ++sd) {
+        if (load_q) tc::tma_load_3d(sb + L::kQ + sd * tc::kSubTileBytes, tm_q, sd * 64, h, q0, bar_ld);
+        tc::tma_load_3d(sb + L::kK + sd * tc::kSubTileBytes, tm_k, sd * 64, g, k0, bar_ld);
+        tc::tma_load_3d(sb + L::kV + sd * tc::kSubTileBytes, tm_v, sd * 64, g, k0, bar_ld);
+    }
+}
+
+// Window attention, persistent: a grid of a few CTAs per SM walks the jobs
+// (window, head) in the order job = blockIdx.x + i * gridDim.x, job = head *
+// n_windows + window, so the CTAs running at any time hold neighbouring
+// windows of one head.  Barriers and TMEM are set up once per CTA, and the
+// first tiles of the next job are requested as soon as the current job's
+// last P V has finished reading shared memory, so those loads overlap the
+// epilogue.  Each job is computed exactly as in attn_tc_kernel.  TMEM: 128
+// columns when every job of the CTA is a single 128-row tile and D = 64
+// (four CTAs share the 512 columns of an SM), else 256.
+template <int D>
+__global__ void __launch_bounds__(128, D == 64 ? 4 : 2)
+    window_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_v, const AttnTcArgs a, unsigned int *status) {
+    using L = AttnTcLayout<D>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t sb = (raw + 1023u) & ~1023u;
+    uint8_t *smem = smem_raw + (sb - raw);
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int G = gridDim.x;
+    const int n_jobs = a.n_seg * a.hq;
+
+    if (a.cu[a.n_seg] != a.total) {
+        if (blockIdx.x == 0 && tid == 0) atomicOr(status, QA_DEVICE_BAD_SEGMENTS);
+        return;
+    }
+    // does any job of this CTA span more than one 128-row tile?
+    int multi = 0;
+    for (int j = blockIdx.x + tid * G; j < n_jobs; j += 128 * G) {
+        const int seg = j % a.n_seg;
+        multi |= a.cu[seg + 1] - a.cu[seg] > 128;
+    }
+    multi = __syncthreads_or(multi);
+    const uint32_t tmem_cols = (D == 64 && !multi) ? 128u : 256u;
+
+    const uint32_t bar_ld = sb + L::kBar, bar_s = bar_ld + 8, bar_o = bar_ld + 16;
+    if (tid == 0) {
+        mbar_init(bar_ld, 1);
+        mbar_init(bar_s, 1);
+        mbar_init(bar_o, 1);
+        fence_mbar_init();
+        tc::prefetch_tmap(&tm_q);
+        tc::prefetch_tmap(&tm_k);
+        tc::prefetch_tmap(&tm_v);
+    }
+    if (warp == 0) tc::tmem_alloc(sb + L::kTmemSlot, tmem_cols);
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + L::kTmemSlot);
+    const uint32_t t_row = tmem + ((uint32_t)(warp * 32) << 16);
+
+    uint32_t ph_ld = 0, ph_s = 0, ph_o = 0;
+    const int r = tid;
+    const uint32_t plo_row = sb + L::kPlo + r * 128;
+    const uint32_t sw = (uint32_t)(r & 7);
+    bool prefetched = false;  // thread 0: the job's first tiles are already requested
+
+    for (int job = blockIdx.x; job < n_jobs; job += G) {
+        const int seg = job % a.n_seg, h = job / a.n_seg;
+        const int s0 = a.cu[seg], s1 = a.cu[seg + 1];
+        // thread 0 reads the next job's bounds now, for its early loads
+        int nx_h = 0, nx_s0 = 0, nx_s1 = 0;
+        const bool has_next = job + G < n_jobs;
+        if (tid == 0 && has_next) {
+            const int nseg = (job + G) % a.n_seg;
+            nx_h = (job + G) / a.n_seg;
+            nx_s0 = a.cu[nseg];
+            nx_s1 = a.cu[nseg + 1];
+        }
+        if (!(0 <= s0 && s0 <= s1 && s1 <= a.total)) {
+            if (tid == 0) atomicOr(status, QA_DEVICE_BAD_SEGMENTS);
+            continue;  // nothing was requested for an invalid job
+        }
+        const int n_tiles = (s1 - s0 + 127) / 128;
+        if (n_tiles == 0) continue;
+        const bool o_in_s = D == 64 && n_tiles == 1;
+        const uint32_t col_o = o_in_s ? 64u : 128u;
+
+        for (int qt = 0; qt < n_tiles; ++qt) {
+            const int q0 = s0 + qt * 128;
+            const int qi = q0 + r;
+            float m = -INFINITY, l = 0.f;
+            for (int kt = 0; kt < n_tiles; ++kt) {
+                const int k0 = s0 + kt * 128;
+                const bool last = qt == n_tiles - 1 && kt == n_tiles - 1;
+                if (tid == 0) {
+                    if (!(prefetched && qt == 0 && kt == 0))
+                        issue_tile_loads<D>(sb, &tm_q, &tm_k, &tm_v, h, h, q0, k0, D == 64 || kt == 0, bar_ld);
+                    prefetched = false;
+                    mbar_wait(bar_ld, ph_ld, status);
+                    tc::fence_after();
+                    issue_s<D>(tmem, sb + L::kQ, sb + L::kK);
+                    tc::mma_commit(bar_s);
+                }
+                ph_ld ^= 1;
+                mbar_wait(bar_s, ph_s, status);
+                ph_s ^= 1;
+                tc::fence_after();
+
+                int n_ok = min(128, s1 - k0);
+                n_ok = max(n_ok, 0);
+                softmax_tile<D>(t_row, n_ok, a.scale_log2, plo_row, sw, t_row + col_o, kt > 0, m, l);
+                tc::fence_proxy_async_smem();
+                tc::fence_before();
+                __syncthreads();
+
+                if (tid == 0) {
+                    tc::fence_after();
+                    issue_pv<D>(tmem, tmem + col_o, sb + L::kPlo, sb + L::kV, kt > 0);
+                    tc::mma_commit(bar_o);
+                }
+                mbar_wait(bar_o, ph_o, status);
+                ph_o ^= 1;
+                tc::fence_after();
+                // the job's shared memory is free: request the next job's first tiles
+                if (tid == 0 && last && has_next && 0 <= nx_s0 && nx_s0 < nx_s1 && nx_s1 <= a.total) {
+                    issue_tile_loads<D>(sb, &tm_q, &tm_k, &tm_v, nx_h, nx_h, nx_s0, nx_s0, true, bar_ld);
+                    prefetched = true;
+                }
+            }
+            store_rows<D>(t_row + col_o, l, a.out + ((size_t)qi * a.hq + h) * D, qi < s1);
+            tc::fence_before();
+            __syncthreads();  // every TMEM read is done before the next tile's MMAs
+        }
+    }
+
+    if (warp == 0) {
+        tc::fence_after();
+        tc::tmem_dealloc(tmem, tmem_cols);
+    }
+}
+
 }  // namespace qa

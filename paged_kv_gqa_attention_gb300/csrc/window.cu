@@ -5,11 +5,14 @@
 // bidirectional MHA scaled by 1/sqrt(head_dim).  M* "Speech recognition:
 // Whisper and Qwen3-ASR", "Graph": one packed forward per batch with one
 // segment per window of every request.  Row t of window w attends over every
-// row of w and nothing else.  Runs on the tensor cores (attn_tc.cuh): one CTA
-// per (window, head), four CTAs per SM; a 104-token window is one 128-row
-// tile, longer windows loop over query and key tiles.
+// row of w and nothing else.  Runs on the tensor cores (attn_tc.cuh,
+// window_tc_kernel): a persistent grid of four CTAs per SM (two for head_dim
+// 128) walks the (window, head) jobs; a 104-token window is one 128-row tile,
+// longer windows loop over query and key tiles.
 #include <cuda_runtime.h>
 #include <stdint.h>
+
+#include <algorithm>
 
 #include "common.cuh"
 #include "qa_internal.h"
@@ -41,18 +44,32 @@ cudaError_t launch_window(const void *q, const void *k, const void *v, const int
     unsigned int *status = nullptr;
     cudaError_t e = cudaGetSymbolAddress(reinterpret_cast<void **>(&status), g_status);
     if (e != cudaSuccess) return e;
-    const dim3 grid(n_windows, p.n_q_heads);
-    if (p.head_dim == 64) {
-        constexpr uint32_t smem = AttnTcLayout<64>::kSmem;
-        e = cudaFuncSetAttribute(attn_tc_kernel<64, 1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        attn_tc_kernel<64, 1, false><<<grid, 128, smem, stream>>>(tq, tk, tv, a, status);
-    } else {
-        constexpr uint32_t smem = AttnTcLayout<128>::kSmem;
-        e = cudaFuncSetAttribute(attn_tc_kernel<128, 1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        attn_tc_kernel<128, 1, false><<<grid, 128, smem, stream>>>(tq, tk, tv, a, status);
-    }
+    // persistent grid: as many CTAs as fit on the GPU at once, at most one per job
+    int dev = 0, sms = 0;
+    e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    const long long n_jobs = (long long)n_windows * p.n_q_heads;
+    if (n_jobs > 0x7fffffffLL) return cudaErrorInvalidValue;
+    // CTAs per SM as the launch bounds size them (registers and shared memory
+    // both fit: 4 x 49 KiB for head_dim 64, 2 x 97 KiB for 128); the
+    // occupancy query under-reports for these kernels, so it is not used.
+    // Extra CTAs would only queue: no CTA waits on another.
+    auto launch = [&](auto kernel, uint32_t smem, int per_sm) -> cudaError_t {
+        cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (err != cudaSuccess) return err;
+        err = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                   (int)cudaSharedmemCarveoutMaxShared);
+        if (err != cudaSuccess) return err;
+        const long long ctas = std::min<long long>(n_jobs, (long long)sms * per_sm);
+        kernel<<<(unsigned)ctas, 128, smem, stream>>>(tq, tk, tv, a, status);
+        return cudaSuccess;
+    };
+    if (p.head_dim == 64)
+        e = launch(window_tc_kernel<64>, AttnTcLayout<64>::kSmem, 4);
+    else
+        e = launch(window_tc_kernel<128>, AttnTcLayout<128>::kSmem, 2);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

@@ -72,9 +72,10 @@ struct AttnTcLayout {
     // P_lo (128 keys = 2 sub-tiles): over Q and K when D = 64 (Q is reloaded
     // with every key tile), over K when D = 128
     static constexpr uint32_t kPlo = D == 64 ? kQ : kK;
-    static constexpr uint32_t kBar = kV + kSub * tc::kSubTileBytes;  // 3 mbarriers
-    static constexpr uint32_t kTmemSlot = kBar + 24;
-    static constexpr uint32_t kBytes = kTmemSlot + 8;
+    static constexpr uint32_t kBar = kV + kSub * tc::kSubTileBytes;  // 4 mbarriers
+    static constexpr uint32_t kTmemSlot = kBar + 32;
+    static constexpr uint32_t kNext = kTmemSlot + 8;  // window kernel: next job's (head, s0, s1)
+    static constexpr uint32_t kBytes = kNext + 16;
     static constexpr uint32_t kSmem = kBytes + 1024;  // slack for 1024-byte alignment
 };
 
@@ -196,6 +197,53 @@ __device__ __forceinline__ void store_rows(uint32_t o_row, float l, uint16_t *ds
                                             pack_bf16x2(o2.x, o2.y), pack_bf16x2(o3.x, o3.y));
             }
         }
+    }
+}
+
+// Epilogue through shared memory: thread r rounds its O row (divided by l)
+// to bf16 and writes it to row r of a staging tile (D * 2 bytes per row,
+// 16-byte chunk c of row r at chunk position c ^ (r & 7), so the writes of 8
+// consecutive rows hit all banks); then each warp writes back its own 32 rows
+// with D / 8 lanes per row, whole rows per store instruction.  Rows at or
+// past row_end (= s1 - q0) are not stored.  Warp-collective; the staging rows
+// of a warp are touched by that warp only.
+template <int D>
+__device__ __forceinline__ void store_rows_staged(uint32_t o_row, float l, uint32_t stage, uint16_t *out, int hq,
+                                                  int h, int q0, int row_end) {
+    constexpr int kChunks = D / 8;  // 16-byte chunks per row
+    const int r = threadIdx.x, lane = r & 31, warp = r >> 5;
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    const uint32_t my_row = stage + (uint32_t)r * (D * 2);
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) {
+        float ov[32];
+        tc::tmem_ld32(o_row + c * 32, ov);
+        const float2 inv2 = make_float2(inv, inv);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const float2 o0 = fmul2(make_float2(ov[8 * u + 0], ov[8 * u + 1]), inv2);
+            const float2 o1 = fmul2(make_float2(ov[8 * u + 2], ov[8 * u + 3]), inv2);
+            const float2 o2 = fmul2(make_float2(ov[8 * u + 4], ov[8 * u + 5]), inv2);
+            const float2 o3 = fmul2(make_float2(ov[8 * u + 6], ov[8 * u + 7]), inv2);
+            const uint32_t chunk = (uint32_t)(c * 4 + u);
+            const uint32_t pos = (chunk & ~7u) | ((chunk ^ (uint32_t)r) & 7u);
+            tc::st_shared_v4(my_row + pos * 16, pack_bf16x2(o0.x, o0.y), pack_bf16x2(o1.x, o1.y),
+                             pack_bf16x2(o2.x, o2.y), pack_bf16x2(o3.x, o3.y));
+        }
+    }
+    __syncwarp();
+    constexpr int kRowsPerStep = 32 / kChunks;  // rows one warp instruction covers
+    const int c = lane % kChunks;
+#pragma unroll
+    for (int i = 0; i < 32 / kRowsPerStep; ++i) {
+        const int rr = warp * 32 + i * kRowsPerStep + lane / kChunks;
+        const uint32_t pos = ((uint32_t)c & ~7u) | (((uint32_t)c ^ (uint32_t)rr) & 7u);
+        uint32_t x0, x1, x2, x3;
+        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(x0), "=r"(x1), "=r"(x2), "=r"(x3)
+                     : "r"(stage + (uint32_t)rr * (D * 2) + pos * 16));
+        if (rr < row_end)
+            *reinterpret_cast<uint4 *>(out + ((size_t)(q0 + rr) * hq + h) * D + c * 8) = make_uint4(x0, x1, x2, x3);
     }
 }
 
@@ -395,31 +443,41 @@ __global__ void __launch_bounds__(128, 4)
     }
 }
 
-// TMA loads of one key tile of a job (and of its query tile when load_q)
-// into the Q/K/V buffers, completing on bar_ld.  One thread.
+// TMA loads of one key tile of a job (and of its query tile when load_q):
+// Q and K complete on bar_qk, V on bar_v.  One thread.
 template <int D>
-__device__ __forceinline__ void issue_tile_loads(uint32_t sb, const CUtensorMap *tm_q, const CUtensorMap *tm_k,
-                                                 const CUtensorMap *tm_v, int h, int g, int q0, int k0, bool load_q,
-                                                 uint32_t bar_ld) {
+__device__ __forceinline__ void issue_qk_loads(uint32_t sb, const CUtensorMap *tm_q, const CUtensorMap *tm_k, int h,
+                                               int g, int q0, int k0, bool load_q, uint32_t bar_qk) {
     using L = AttnTcLayout<D>;
-    mbar_arrive_expect_tx(bar_ld, (load_q ? 3 : 2) * L::kSub * tc::kSubTileBytes);
+    mbar_arrive_expect_tx(bar_qk, (load_q ? 2 : 1) * L::kSub * tc::kSubTileBytes);
 #pragma unroll
     for (int sd = 0; sd < L::kSub; ++sd) {
-        if (load_q) tc::tma_load_3d(sb + L::kQ + sd * tc::kSubTileBytes, tm_q, sd * 64, h, q0, bar_ld);
-        tc::tma_load_3d(sb + L::kK + sd * tc::kSubTileBytes, tm_k, sd * 64, g, k0, bar_ld);
-        tc::tma_load_3d(sb + L::kV + sd * tc::kSubTileBytes, tm_v, sd * 64, g, k0, bar_ld);
+        if (load_q) tc::tma_load_3d(sb + L::kQ + sd * tc::kSubTileBytes, tm_q, sd * 64, h, q0, bar_qk);
+        tc::tma_load_3d(sb + L::kK + sd * tc::kSubTileBytes, tm_k, sd * 64, g, k0, bar_qk);
     }
+}
+
+template <int D>
+__device__ __forceinline__ void issue_v_loads(uint32_t sb, const CUtensorMap *tm_v, int g, int k0, uint32_t bar_v) {
+    using L = AttnTcLayout<D>;
+    mbar_arrive_expect_tx(bar_v, L::kSub * tc::kSubTileBytes);
+#pragma unroll
+    for (int sd = 0; sd < L::kSub; ++sd)
+        tc::tma_load_3d(sb + L::kV + sd * tc::kSubTileBytes, tm_v, sd * 64, g, k0, bar_v);
 }
 
 // Window attention, persistent: a grid of a few CTAs per SM walks the jobs
 // (window, head) in the order job = blockIdx.x + i * gridDim.x, job = head *
 // n_windows + window, so the CTAs running at any time hold neighbouring
-// windows of one head.  Barriers and TMEM are set up once per CTA, and the
-// first tiles of the next job are requested as soon as the current job's
-// last P V has finished reading shared memory, so those loads overlap the
-// epilogue.  Each job is computed exactly as in attn_tc_kernel.  TMEM: 128
-// columns when every job of the CTA is a single 128-row tile and D = 64
-// (four CTAs share the 512 columns of an SM), else 256.
+// windows of one head.  Barriers and TMEM are set up once per CTA.  Q + K and
+// V land on separate barriers, so S starts before V is in.  The next job's
+// Q and K are requested as soon as the current job's last P V has finished
+// reading shared memory, so they load during the epilogue; the epilogue
+// stages the output rows in the V buffer and writes whole rows per store
+// (store_rows_staged), after which the next job's V is requested.  Each job
+// is computed exactly as in attn_tc_kernel.  TMEM: 128 columns when
+// every job of the CTA is a single 128-row tile and D = 64 (four CTAs share
+// the 512 columns of an SM), else 256.
 template <int D>
 __global__ void __launch_bounds__(128, D == 64 ? 4 : 2)
     window_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -446,11 +504,12 @@ __global__ void __launch_bounds__(128, D == 64 ? 4 : 2)
     multi = __syncthreads_or(multi);
     const uint32_t tmem_cols = (D == 64 && !multi) ? 128u : 256u;
 
-    const uint32_t bar_ld = sb + L::kBar, bar_s = bar_ld + 8, bar_o = bar_ld + 16;
+    const uint32_t bar_qk = sb + L::kBar, bar_s = bar_qk + 8, bar_o = bar_qk + 16, bar_v = bar_qk + 24;
     if (tid == 0) {
-        mbar_init(bar_ld, 1);
+        mbar_init(bar_qk, 1);
         mbar_init(bar_s, 1);
         mbar_init(bar_o, 1);
+        mbar_init(bar_v, 1);
         fence_mbar_init();
         tc::prefetch_tmap(&tm_q);
         tc::prefetch_tmap(&tm_k);
@@ -463,23 +522,30 @@ __global__ void __launch_bounds__(128, D == 64 ? 4 : 2)
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + L::kTmemSlot);
     const uint32_t t_row = tmem + ((uint32_t)(warp * 32) << 16);
 
-    uint32_t ph_ld = 0, ph_s = 0, ph_o = 0;
+    uint32_t ph_qk = 0, ph_v = 0, ph_s = 0, ph_o = 0;
     const int r = tid;
     const uint32_t plo_row = sb + L::kPlo + r * 128;
     const uint32_t sw = (uint32_t)(r & 7);
-    bool prefetched = false;  // thread 0: the job's first tiles are already requested
+    bool prefetched = false;  // thread 0: the job's first Q/K tiles are already requested
 
     for (int job = blockIdx.x; job < n_jobs; job += G) {
         const int seg = job % a.n_seg, h = job / a.n_seg;
         const int s0 = a.cu[seg], s1 = a.cu[seg + 1];
-        // thread 0 reads the next job's bounds now, for its early loads
-        int nx_h = 0, nx_s0 = 0, nx_s1 = 0;
-        const bool has_next = job + G < n_jobs;
-        if (tid == 0 && has_next) {
-            const int nseg = (job + G) % a.n_seg;
-            nx_h = (job + G) / a.n_seg;
-            nx_s0 = a.cu[nseg];
-            nx_s1 = a.cu[nseg + 1];
+        // one thread off the MMA-issue path reads the next job's bounds into
+        // shared memory for thread 0's early loads (seen after the softmax barrier)
+        int *nx = reinterpret_cast<int *>(smem + L::kNext);
+        if (tid == 32) {
+            const int nj = job + G;
+            int v0 = 0, v1 = 0, v2 = 0;  // (head, s0, s1); s0 == s1: nothing to request
+            if (nj < n_jobs) {
+                const int nseg = nj % a.n_seg;
+                v0 = nj / a.n_seg;
+                v1 = a.cu[nseg];
+                v2 = a.cu[nseg + 1];
+            }
+            nx[0] = v0;
+            nx[1] = v1;
+            nx[2] = v2;
         }
         if (!(0 <= s0 && s0 <= s1 && s1 <= a.total)) {
             if (tid == 0) atomicOr(status, QA_DEVICE_BAD_SEGMENTS);
@@ -498,15 +564,17 @@ __global__ void __launch_bounds__(128, D == 64 ? 4 : 2)
                 const int k0 = s0 + kt * 128;
                 const bool last = qt == n_tiles - 1 && kt == n_tiles - 1;
                 if (tid == 0) {
-                    if (!(prefetched && qt == 0 && kt == 0))
-                        issue_tile_loads<D>(sb, &tm_q, &tm_k, &tm_v, h, h, q0, k0, D == 64 || kt == 0, bar_ld);
+                    if (!(prefetched && qt == 0 && kt == 0)) {
+                        issue_qk_loads<D>(sb, &tm_q, &tm_k, h, h, q0, k0, D == 64 || kt == 0, bar_qk);
+                        issue_v_loads<D>(sb, &tm_v, h, k0, bar_v);
+                    }
                     prefetched = false;
-                    mbar_wait(bar_ld, ph_ld, status);
+                    mbar_wait(bar_qk, ph_qk, status);
                     tc::fence_after();
                     issue_s<D>(tmem, sb + L::kQ, sb + L::kK);
                     tc::mma_commit(bar_s);
                 }
-                ph_ld ^= 1;
+                ph_qk ^= 1;
                 mbar_wait(bar_s, ph_s, status);
                 ph_s ^= 1;
                 tc::fence_after();
@@ -519,22 +587,30 @@ __global__ void __launch_bounds__(128, D == 64 ? 4 : 2)
                 __syncthreads();
 
                 if (tid == 0) {
+                    mbar_wait(bar_v, ph_v, status);
                     tc::fence_after();
                     issue_pv<D>(tmem, tmem + col_o, sb + L::kPlo, sb + L::kV, kt > 0);
                     tc::mma_commit(bar_o);
                 }
+                ph_v ^= 1;
                 mbar_wait(bar_o, ph_o, status);
                 ph_o ^= 1;
                 tc::fence_after();
-                // the job's shared memory is free: request the next job's first tiles
-                if (tid == 0 && last && has_next && 0 <= nx_s0 && nx_s0 < nx_s1 && nx_s1 <= a.total) {
-                    issue_tile_loads<D>(sb, &tm_q, &tm_k, &tm_v, nx_h, nx_h, nx_s0, nx_s0, true, bar_ld);
-                    prefetched = true;
+                // Q/K/P buffers are free: request the next job's Q and K
+                if (tid == 0 && last) {
+                    const int nx_h = nx[0], nx_s0 = nx[1], nx_s1 = nx[2];
+                    if (0 <= nx_s0 && nx_s0 < nx_s1 && nx_s1 <= a.total) {
+                        issue_qk_loads<D>(sb, &tm_q, &tm_k, nx_h, nx_h, nx_s0, nx_s0, true, bar_qk);
+                        prefetched = true;
+                    }
                 }
             }
-            store_rows<D>(t_row + col_o, l, a.out + ((size_t)qi * a.hq + h) * D, qi < s1);
+            // epilogue staged in the V buffer (free since the last P V)
+            store_rows_staged<D>(t_row + col_o, l, sb + L::kV, a.out, a.hq, h, q0, s1 - q0);
             tc::fence_before();
-            __syncthreads();  // every TMEM read is done before the next tile's MMAs
+            __syncthreads();  // every TMEM read and staging read is done
+            // the V buffer is free again: request the next job's V
+            if (tid == 0 && prefetched) issue_v_loads<D>(sb, &tm_v, nx[0], nx[1], bar_v);
         }
     }
 

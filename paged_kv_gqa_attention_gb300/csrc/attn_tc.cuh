@@ -1,38 +1,34 @@
-// Tensor-core flash attention over packed segments (tcgen05 + TMEM + TMA).
-//
-// One CTA of four warps computes the 128-row query tiles of one query head h
-// of one segment (a prefill request or an encoder window); CTAs are small
-// (48 KiB of shared memory and 128 TMEM columns for a 104-token window), so
-// four run on each SM and hide each other's load and softmax latency.  Per
-// key tile of 128 rows:
+// Tensor-core flash attention over packed segments (tcgen05 + TMEM + TMA):
+// the AuT window attention (window_tc_kernel) and the causal prefill with
+// its KV page write (prefill_tc_kernel).  A job is the 128-row query tiles
+// of one query head of one segment (an encoder window, or one query tile of
+// a prefill request); CTAs have four warps.  The window kernel is persistent
+// (small, uniform jobs: barriers and TMEM set up once per CTA, the next
+// job's tiles requested while the current one finishes); the prefill runs
+// one CTA per job (uneven jobs, balanced by the hardware scheduler).  Per key
+// tile of 128 rows:
 //   1. TMA brings the K and V tiles ([128 rows][D] bf16, 128B-swizzled, 64-dim
-//      sub-tiles) and the Q tile into shared memory.
+//      sub-tiles) and the Q tile into shared memory; Q + K and V complete on
+//      separate mbarriers, so S starts before V is in.
 //   2. One thread issues S = Q K^T (M = 128, N = 128 keys, K = D in steps of
 //      16) into TMEM columns [0, 128) and commits to an mbarrier.
-//      Causal prefill, diagonal key tile (the query tile's own rows), first
-//      query head of each KV head: while S is computed, the CTA copies the
-//      K and V rows of the tile from shared memory to their KV-cache pages.
 //   3. Thread r owns query row r (= TMEM lane r): it reads its scores with
 //      tcgen05.ld, keeps the first n_ok keys of the tile (the rest lie outside
 //      the segment or, causal, after the row), runs the online softmax in fp32
-//      with base-2 exponentials, and writes P as two bf16 terms: P_hi = bf16(p)
-//      into TMEM over the consumed scores (columns [0, 64), two keys per
-//      column), P_lo = bf16(p - P_hi) into the dead Q/K shared memory as a
-//      128B-swizzled K-major tile.  The pair carries p to about 16 significant
-//      bits, so the P V product keeps the softmax probabilities at (nearly)
-//      fp32 precision, as the precision policy asks (score and softmax
-//      intermediates in float32).
+//      with base-2 exponentials, and writes P as two bf16 terms, P_hi = p
+//      truncated to bf16 and P_lo = bf16(p - P_hi) (softmax_tile: P_hi in
+//      TMEM over the consumed scores; P_lo in the dead Q/K shared memory for
+//      the window kernel, in TMEM too for the prefill).  The pair carries p to
+//      about 16 significant bits, so the P V product keeps the softmax
+//      probabilities at (nearly) fp32 precision, as the precision policy asks
+//      (score and softmax intermediates in float32).
 //   4. When the running max of a row moved, the thread rescales its row of
 //      the fp32 output accumulator O in TMEM by alpha = 2^(m_old - m_new).
-//   5. One thread issues O += P_hi V (A operand read from TMEM) and
-//      O += P_lo V (A from shared memory), M = 128, N = 64 per MMA, K = 128
-//      keys in steps of 16, V read MN-major.
+//   5. One thread issues O += P_hi V and O += P_lo V (M = 128, N = 64 per
+//      MMA, K = 128 keys in steps of 16, V read MN-major).
 // After the last key tile each row of O is read back, divided by its softmax
-// sum, rounded to bf16 and stored.
-//
-// O lives in TMEM columns [64, 64 + D) when the job has a single key tile and
-// D = 64 (the scores there are consumed before the first P V), else in
-// [128, 128 + D).
+// sum, rounded to bf16, staged in shared memory and stored whole rows at a
+// time (store_rows_staged).
 //
 // Masks.  Window: key j is visible to row i iff both lie in the segment.
 // Causal prefill: additionally j <= i.  Rows past the segment end are computed
@@ -74,18 +70,22 @@ struct AttnTcLayout {
     static constexpr uint32_t kPlo = D == 64 ? kQ : kK;
     static constexpr uint32_t kBar = kV + kSub * tc::kSubTileBytes;  // 4 mbarriers
     static constexpr uint32_t kTmemSlot = kBar + 32;
-    static constexpr uint32_t kNext = kTmemSlot + 8;  // window kernel: next job's (head, s0, s1)
-    static constexpr uint32_t kBytes = kNext + 16;
+    static constexpr uint32_t kNext = kTmemSlot + 8;  // next-job records of the persistent kernels
+    static constexpr uint32_t kBytes = kNext + 32;
     static constexpr uint32_t kSmem = kBytes + 1024;  // slack for 1024-byte alignment
 };
 
 // Online softmax of one 128-key tile for this thread's query row, whose
 // scores sit in TMEM columns [0, 128) of s_row.  Keys [0, n_ok) of the tile
-// are visible.  Writes P_hi (bf16, two keys per column) over the scores in
-// columns [0, 64), P_lo as a 128B-swizzled K-major row at plo_row, updates
-// the running (m, l) and, when `rescale`, multiplies the row of O at o_row by
-// 2^(m_old - m_new).  Warp-collective (every lane of the warp calls it).
-template <int D>
+// are visible.  Writes P as P_hi (bf16, two keys per column) and P_lo:
+//   P_TMEM = false: P_hi over the scores in columns [0, 64), P_lo as a
+//                   128B-swizzled K-major row at plo_row (shared memory);
+//   P_TMEM = true:  both in TMEM over the chunk of scores they replace: keys
+//                   [32c, 32c + 32) give P_hi in columns [32c, 32c + 16) and
+//                   P_lo in [32c + 16, 32c + 32) (plo_row and sw unused).
+// Updates the running (m, l) and, when `rescale`, multiplies the row of O at
+// o_row by 2^(m_old - m_new).  Warp-collective (every lane of the warp calls it).
+template <int D, bool P_TMEM = false>
 __device__ __forceinline__ void softmax_tile(uint32_t s_row, int n_ok, float scale_log2, uint32_t plo_row,
                                              uint32_t sw, uint32_t o_row, bool rescale, float &m, float &l) {
     const int warp_max = __reduce_max_sync(0xffffffffu, n_ok);
@@ -94,6 +94,9 @@ __device__ __forceinline__ void softmax_tile(uint32_t s_row, int n_ok, float sca
     // flight while chunk c is processed; dead chunks (warp-uniform) are
     // neither read nor computed.
     const int n_chunks = (warp_max + 31) >> 5;
+    // the last live chunk holds at most 16 live keys: its upper half is
+    // neither reduced nor exponentiated (its probabilities are written as 0)
+    const bool half_tail = warp_max - (n_chunks - 1) * 32 <= 16;
     uint32_t ra[32], rb[32];
     float mx = -INFINITY;
     tc::tmem_ld32_issue(s_row, ra);
@@ -109,7 +112,11 @@ __device__ __forceinline__ void softmax_tile(uint32_t s_row, int n_ok, float sca
             for (int j = 0; j < 32; ++j) cur[j] = c * 32 + j < n_ok ? cur[j] : __float_as_uint(-INFINITY);
         }
 #pragma unroll
-        for (int j = 0; j < 32; j += 2) mx = fmax3(mx, __uint_as_float(cur[j]), __uint_as_float(cur[j + 1]));
+        for (int j = 0; j < 16; j += 2) mx = fmax3(mx, __uint_as_float(cur[j]), __uint_as_float(cur[j + 1]));
+        if (!(half_tail && c == n_chunks - 1)) {
+#pragma unroll
+            for (int j = 16; j < 32; j += 2) mx = fmax3(mx, __uint_as_float(cur[j]), __uint_as_float(cur[j + 1]));
+        }
         if (c + 1 < n_chunks) tc::tmem_ld32_wait(nxt);
     }
     const float m_new = fmaxf(m, mx * scale_log2);
@@ -130,9 +137,9 @@ __device__ __forceinline__ void softmax_tile(uint32_t s_row, int n_ok, float sca
         } else {
             if (c + 1 < n_chunks) tc::tmem_ld32_issue(s_row + (c + 1) * 32, nxt);
             const bool full = c * 32 + 32 <= warp_min;
-#pragma unroll
-            for (int j = 0; j < 32; j += 2) {
-                // x = s * scale * log2(e) - m for the pair, on packed fp32
+            // x = s * scale * log2(e) - m for a pair, on packed fp32; then
+            // P_hi = p truncated to bf16 (exact), P_lo = bf16(p - P_hi)
+            auto pair = [&](int j) {
                 float2 x = ffma2(make_float2(__uint_as_float(cur[j]), __uint_as_float(cur[j + 1])), scale2, neg_m2);
                 if (!full) {
                     x.x = c * 32 + j < n_ok ? x.x : -INFINITY;
@@ -140,23 +147,37 @@ __device__ __forceinline__ void softmax_tile(uint32_t s_row, int n_ok, float sca
                 }
                 const float2 pp = make_float2(exp2_approx(x.x), exp2_approx(x.y));
                 psum2 = fadd2(psum2, pp);
-                // P_hi = p truncated to bf16 (exact), P_lo = bf16(p - P_hi)
                 const uint32_t b0 = __float_as_uint(pp.x), b1 = __float_as_uint(pp.y);
                 pk[j >> 1] = __byte_perm(b0, b1, 0x7632);
                 const float2 lo =
                     fsub2(pp, make_float2(__uint_as_float(b0 & 0xffff0000u), __uint_as_float(b1 & 0xffff0000u)));
                 pl[j >> 1] = pack_bf16x2(lo.x, lo.y);
+            };
+#pragma unroll
+            for (int j = 0; j < 16; j += 2) pair(j);
+            if (half_tail && c == n_chunks - 1) {
+#pragma unroll
+                for (int i = 8; i < 16; ++i) pk[i] = pl[i] = 0u;
+            } else {
+#pragma unroll
+                for (int j = 16; j < 32; j += 2) pair(j);
             }
             if (c + 1 < n_chunks) tc::tmem_ld32_wait(nxt);
         }
-        // P_hi: 32 keys = 16 TMEM columns [16c, 16c + 16) (scores there are consumed)
-        tc::tmem_st16(s_row + c * 16, pk);
-        // P_lo: 4 chunks of 16 bytes, sub-tile c / 2, chunks (c % 2) * 4 + u
+        if (P_TMEM) {
+            // chunk c's own 32 columns (its scores are in registers already)
+            tc::tmem_st16(s_row + c * 32, pk);
+            tc::tmem_st16(s_row + c * 32 + 16, pl);
+        } else {
+            // P_hi: 32 keys = 16 TMEM columns [16c, 16c + 16) (scores there are consumed)
+            tc::tmem_st16(s_row + c * 16, pk);
+            // P_lo: 4 chunks of 16 bytes, sub-tile c / 2, chunks (c % 2) * 4 + u
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const uint32_t chunk = (uint32_t)((c & 1) * 4 + u);
-            const uint32_t off = (uint32_t)(c >> 1) * tc::kSubTileBytes + ((chunk ^ sw) << 4);
-            tc::st_shared_v4(plo_row + off, pl[4 * u], pl[4 * u + 1], pl[4 * u + 2], pl[4 * u + 3]);
+            for (int u = 0; u < 4; ++u) {
+                const uint32_t chunk = (uint32_t)((c & 1) * 4 + u);
+                const uint32_t off = (uint32_t)(c >> 1) * tc::kSubTileBytes + ((chunk ^ sw) << 4);
+                tc::st_shared_v4(plo_row + off, pl[4 * u], pl[4 * u + 1], pl[4 * u + 2], pl[4 * u + 3]);
+            }
         }
     }
     tc::tmem_wait_st();
@@ -171,31 +192,6 @@ __device__ __forceinline__ void softmax_tile(uint32_t s_row, int n_ok, float sca
 #pragma unroll
             for (int j = 0; j < 32; ++j) ov[j] *= alpha;
             tc::tmem_st32(o_row + c * 32, ov);
-        }
-    }
-}
-
-// O row (TMEM columns [0, D) of o_row) divided by l, rounded to bf16 and
-// stored at dst when `valid`.  Warp-collective.
-template <int D>
-__device__ __forceinline__ void store_rows(uint32_t o_row, float l, uint16_t *dst_row, bool valid) {
-    const float inv = l > 0.f ? 1.f / l : 0.f;
-    uint4 *dst = reinterpret_cast<uint4 *>(dst_row);
-#pragma unroll
-    for (int c = 0; c < D / 32; ++c) {
-        float ov[32];
-        tc::tmem_ld32(o_row + c * 32, ov);
-        if (valid) {
-            const float2 inv2 = make_float2(inv, inv);
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const float2 o0 = fmul2(make_float2(ov[8 * u + 0], ov[8 * u + 1]), inv2);
-                const float2 o1 = fmul2(make_float2(ov[8 * u + 2], ov[8 * u + 3]), inv2);
-                const float2 o2 = fmul2(make_float2(ov[8 * u + 4], ov[8 * u + 5]), inv2);
-                const float2 o3 = fmul2(make_float2(ov[8 * u + 6], ov[8 * u + 7]), inv2);
-                dst[c * 4 + u] = make_uint4(pack_bf16x2(o0.x, o0.y), pack_bf16x2(o1.x, o1.y),
-                                            pack_bf16x2(o2.x, o2.y), pack_bf16x2(o3.x, o3.y));
-            }
         }
     }
 }
@@ -311,135 +307,23 @@ __device__ __forceinline__ void write_kv_pages(const uint8_t *k_tile, const uint
     }
 }
 
-// CAUSAL: grid (hq, segments, q-tiles), one query tile per CTA.
-// !CAUSAL: grid (segments, hq), every query tile of the segment in turn.
-template <int D, int GROUP, bool CAUSAL>
-__global__ void __launch_bounds__(128, 4)
-    attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                   const __grid_constant__ CUtensorMap tm_v, const AttnTcArgs a, unsigned int *status) {
-    using L = AttnTcLayout<D>;
-    extern __shared__ uint8_t smem_raw[];
-    const uint32_t raw = smem_u32(smem_raw);
-    const uint32_t sb = (raw + 1023u) & ~1023u;
-    uint8_t *smem = smem_raw + (sb - raw);
-    const int tid = threadIdx.x, warp = tid >> 5;
-
-    const int h = CAUSAL ? blockIdx.x : blockIdx.y;
-    const int g = h / GROUP;
-    const int seg = CAUSAL ? blockIdx.y : blockIdx.x;
-    const int s0 = a.cu[seg], s1 = a.cu[seg + 1];
-    if (!(0 <= s0 && s0 <= s1 && s1 <= a.total) || a.cu[a.n_seg] != a.total) {
-        if (tid == 0) atomicOr(status, QA_DEVICE_BAD_SEGMENTS);
-        return;
-    }
-    const int n_tiles = (s1 - s0 + 127) / 128;
-    int qt0, qt1;
-    if (CAUSAL) {
-        // the longest jobs (last query tiles: most key tiles) launch first:
-        // the query tile is the slowest-varying grid coordinate, reversed
-        qt0 = (int)(gridDim.z - 1 - blockIdx.z);
-        qt1 = qt0 + 1;
-        // a request longer than its page-table row: flagged once, its rows past
-        // the row's capacity are neither written nor (beyond the grid) attended
-        if (a.k_pages && qt0 == 0 && h == 0 && tid == 0 && s1 - s0 > a.max_pages * a.page_size)
-            atomicOr(status, QA_DEVICE_BAD_LENGTH);
-        if (qt0 >= n_tiles) return;
-    } else {
-        qt0 = 0;
-        qt1 = n_tiles;
-        if (n_tiles == 0) return;
-    }
-    // one key tile in all (window of <= 128 rows, or the first causal tile)
-    const bool single = CAUSAL ? qt0 == 0 : n_tiles == 1;
-    const bool o_in_s = D == 64 && single;
-    const uint32_t tmem_cols = o_in_s ? 128u : 256u;
-    const uint32_t col_o = o_in_s ? 64u : 128u;
-
-    const uint32_t bar_ld = sb + L::kBar, bar_s = bar_ld + 8, bar_o = bar_ld + 16;
-    if (tid == 0) {
-        mbar_init(bar_ld, 1);
-        mbar_init(bar_s, 1);
-        mbar_init(bar_o, 1);
-        fence_mbar_init();
-        tc::prefetch_tmap(&tm_q);
-        tc::prefetch_tmap(&tm_k);
-        tc::prefetch_tmap(&tm_v);
-    }
-    if (warp == 0) tc::tmem_alloc(sb + L::kTmemSlot, tmem_cols);
-    tc::fence_before();
-    __syncthreads();
-    tc::fence_after();
-    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + L::kTmemSlot);
-    const uint32_t t_row = tmem + ((uint32_t)(warp * 32) << 16);  // this warp's TMEM lanes
-
-    uint32_t ph_ld = 0, ph_s = 0, ph_o = 0;
-    const int r = tid;  // query row in the tile = TMEM lane
-    const uint32_t plo_row = sb + L::kPlo + r * 128;
-    const uint32_t sw = (uint32_t)(r & 7);
-
-    for (int qt = qt0; qt < qt1; ++qt) {
-        const int q0 = s0 + qt * 128;
-        const int qi = q0 + r;
-        const int kt_end = CAUSAL ? qt + 1 : n_tiles;
-        float m = -INFINITY, l = 0.f;
-
-        for (int kt = 0; kt < kt_end; ++kt) {
-            const int k0 = s0 + kt * 128;
-            if (tid == 0) {
-                const bool load_q = D == 64 || kt == 0;
-                mbar_arrive_expect_tx(bar_ld, (load_q ? 3 : 2) * L::kSub * tc::kSubTileBytes);
+// O += P_hi V + P_lo V with both P terms in TMEM in the chunk layout of
+// softmax_tile<D, true>: keys [16kk, 16kk + 16) are P_hi columns
+// 32 (kk / 2) + 8 (kk % 2) + [0, 8) and P_lo columns 16 further.  N = 64
+// dims per MMA, V read MN-major.  One thread.
+template <int D>
+__device__ __forceinline__ void issue_pv_tp(uint32_t tmem, uint32_t o_col, uint32_t v_base, bool accumulate) {
+    constexpr uint32_t idesc_o = tc::idesc_bf16(128, 64, true);
 #pragma unroll
-                for (int sd = 0; sd < L::kSub; ++sd) {
-                    if (load_q) tc::tma_load_3d(sb + L::kQ + sd * tc::kSubTileBytes, &tm_q, sd * 64, h, q0, bar_ld);
-                    tc::tma_load_3d(sb + L::kK + sd * tc::kSubTileBytes, &tm_k, sd * 64, g, k0, bar_ld);
-                    tc::tma_load_3d(sb + L::kV + sd * tc::kSubTileBytes, &tm_v, sd * 64, g, k0, bar_ld);
-                }
-                mbar_wait(bar_ld, ph_ld, status);
-                tc::fence_after();
-                issue_s<D>(tmem, sb + L::kQ, sb + L::kK);
-                tc::mma_commit(bar_s);
-            }
-            if (CAUSAL && kt == qt && a.k_pages && h % GROUP == 0) {
-                // the diagonal key tile holds this query tile's own K/V rows:
-                // one query head per KV head writes them to their pages while
-                // S is computed, before P_lo overwrites the K tile
-                mbar_wait(bar_ld, ph_ld, status);
-                write_kv_pages<D>(smem + L::kK, smem + L::kV, a, seg, qt * 128, s1 - s0, g, status);
-                __syncthreads();
-            }
-            ph_ld ^= 1;
-            mbar_wait(bar_s, ph_s, status);
-            ph_s ^= 1;
-            tc::fence_after();
-
-            // ---- softmax over this key tile (row r): keys [k0, k0 + n_ok)
-            int n_ok = min(128, s1 - k0);
-            if (CAUSAL) n_ok = min(n_ok, qi - k0 + 1);
-            n_ok = max(n_ok, 0);
-            softmax_tile<D>(t_row, n_ok, a.scale_log2, plo_row, sw, t_row + col_o, kt > 0, m, l);
-            tc::fence_proxy_async_smem();
-            tc::fence_before();
-            __syncthreads();
-
-            if (tid == 0) {
-                tc::fence_after();
-                issue_pv<D>(tmem, tmem + col_o, sb + L::kPlo, sb + L::kV, kt > 0);
-                tc::mma_commit(bar_o);
-            }
-            mbar_wait(bar_o, ph_o, status);
-            ph_o ^= 1;
-            tc::fence_after();
+    for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t a_hi = tmem + (uint32_t)(kk >> 1) * 32 + (uint32_t)(kk & 1) * 8;
+#pragma unroll
+        for (int sd = 0; sd < D / 64; ++sd) {
+            const uint64_t vdesc = tc::sw128_desc(v_base + sd * tc::kSubTileBytes + kk * 2048);
+            const uint32_t o = o_col + sd * 64;
+            tc::mma_bf16_ts(o, a_hi, vdesc, idesc_o, (accumulate || kk > 0) ? 1u : 0u);
+            tc::mma_bf16_ts(o, a_hi + 16, vdesc, idesc_o, 1u);
         }
-
-        // epilogue: O / l -> bf16 (warp-collective TMEM reads, masked stores)
-        store_rows<D>(t_row + col_o, l, a.out + ((size_t)qi * a.hq + h) * D, qi < s1);
-        tc::fence_before();
-        __syncthreads();  // every TMEM read is done before the next query tile's MMAs
-    }
-
-    if (warp == 0) {
-        tc::fence_after();
-        tc::tmem_dealloc(tmem, tmem_cols);
     }
 }
 
@@ -475,7 +359,7 @@ __device__ __forceinline__ void issue_v_loads(uint32_t sb, const CUtensorMap *tm
 // reading shared memory, so they load during the epilogue; the epilogue
 // stages the output rows in the V buffer and writes whole rows per store
 // (store_rows_staged), after which the next job's V is requested.  Each job
-// is computed exactly as in attn_tc_kernel.  TMEM: 128 columns when
+// is computed as described at the top of this file.  TMEM: 128 columns when
 // every job of the CTA is a single 128-row tile and D = 64 (four CTAs share
 // the 512 columns of an SM), else 256.
 template <int D>
@@ -617,6 +501,117 @@ __global__ void __launch_bounds__(128, D == 64 ? 4 : 2)
     if (warp == 0) {
         tc::fence_after();
         tc::tmem_dealloc(tmem, tmem_cols);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Causal prefill, head_dim 128: one CTA per job (query tile t, request b,
+// query head h) on the grid (hq, batch, qtiles) with the query tile reversed,
+// so the last query tiles (the most key tiles) launch first and the query
+// heads of a KV head are adjacent (their K/V tiles come from L2 the second
+// time); the hardware scheduler balances the uneven jobs, two CTAs per SM.
+// The first tiles are requested right after the barriers are set up, before
+// the TMEM allocation.
+//
+// Per key tile kt of the job (key tiles 0..t):
+//   - S = Q K^T (Q loaded with key tile 0 and kept);
+//   - as soon as S has read K, the next key tile's K is requested;
+//   - diagonal tile (kt == t), first query head of each KV head: the K and V
+//     rows of the tile go to their KV-cache pages (write_kv_pages);
+//   - softmax with P_hi and P_lo both in TMEM over the scores
+//     (softmax_tile<128, true>), so no shared memory is written and K stays
+//     free for its prefetch;
+//   - O += P V with both P terms read from TMEM (issue_pv_tp); when it is
+//     done the next key tile's V is requested.
+// The epilogue stages O in the V buffer (store_rows_staged).  TMEM: S/P in
+// columns [0, 128), O in [128, 256).
+template <int GROUP>
+__global__ void __launch_bounds__(128, 2)
+    prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                      const __grid_constant__ CUtensorMap tm_v, const AttnTcArgs a, unsigned int *status) {
+    constexpr int D = 128;
+    using L = AttnTcLayout<D>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t sb = (raw + 1023u) & ~1023u;
+    uint8_t *smem = smem_raw + (sb - raw);
+    const int tid = threadIdx.x, warp = tid >> 5;
+
+    const int h = blockIdx.x, g = h / GROUP;
+    const int b = blockIdx.y;
+    const int qt = (int)(gridDim.z - 1 - blockIdx.z);
+    const int s0 = a.cu[b], s1 = a.cu[b + 1];
+    if (!(0 <= s0 && s0 <= s1 && s1 <= a.total) || a.cu[a.n_seg] != a.total) {
+        if (tid == 0) atomicOr(status, QA_DEVICE_BAD_SEGMENTS);
+        return;
+    }
+    // a request longer than its page-table row: flagged once; its rows past
+    // the row's capacity are neither written nor (beyond the grid) attended
+    if (a.k_pages && qt == 0 && h == 0 && tid == 0 && s1 - s0 > a.max_pages * a.page_size)
+        atomicOr(status, QA_DEVICE_BAD_LENGTH);
+    if (qt * 128 >= s1 - s0) return;
+    const int q0 = s0 + qt * 128;
+
+    const uint32_t bar_k = sb + L::kBar, bar_s = bar_k + 8, bar_o = bar_k + 16, bar_v = bar_k + 24;
+    if (tid == 0) {
+        mbar_init(bar_k, 1);
+        mbar_init(bar_s, 1);
+        mbar_init(bar_o, 1);
+        mbar_init(bar_v, 1);
+        fence_mbar_init();
+        issue_qk_loads<D>(sb, &tm_q, &tm_k, h, g, q0, s0, true, bar_k);
+        issue_v_loads<D>(sb, &tm_v, g, s0, bar_v);
+    }
+    if (warp == 0) tc::tmem_alloc(sb + L::kTmemSlot, 256);
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + L::kTmemSlot);
+    const uint32_t t_row = tmem + ((uint32_t)(warp * 32) << 16);
+    const uint32_t col_o = 128;
+    uint32_t ph = 0;  // every barrier completes once per key tile
+    const int qi = q0 + tid;
+    float m = -INFINITY, l = 0.f;
+
+    for (int kt = 0; kt <= qt; ++kt, ph ^= 1) {
+        const int k0 = s0 + kt * 128;
+        if (tid == 0) {
+            mbar_wait(bar_k, ph, status);
+            tc::fence_after();
+            issue_s<D>(tmem, sb + L::kQ, sb + L::kK);
+            tc::mma_commit(bar_s);
+        }
+        mbar_wait(bar_s, ph, status);
+        tc::fence_after();
+        // S has read K: the next key tile's K
+        if (tid == 0 && kt < qt) issue_qk_loads<D>(sb, &tm_q, &tm_k, h, g, q0, k0 + 128, false, bar_k);
+        if (kt == qt && a.k_pages && h % GROUP == 0) {
+            // diagonal tile: its K/V rows are this query tile's own
+            mbar_wait(bar_v, ph, status);
+            write_kv_pages<D>(smem + L::kK, smem + L::kV, a, b, qt * 128, s1 - s0, g, status);
+        }
+        int n_ok = min(128, s1 - k0);
+        n_ok = min(n_ok, qi - k0 + 1);
+        n_ok = max(n_ok, 0);
+        softmax_tile<D, true>(t_row, n_ok, a.scale_log2, 0u, 0u, t_row + col_o, kt > 0, m, l);
+        tc::fence_before();
+        __syncthreads();
+        if (tid == 0) {
+            mbar_wait(bar_v, ph, status);
+            tc::fence_after();
+            issue_pv_tp<D>(tmem, tmem + col_o, sb + L::kV, kt > 0);
+            tc::mma_commit(bar_o);
+        }
+        mbar_wait(bar_o, ph, status);
+        tc::fence_after();
+        if (tid == 0 && kt < qt) issue_v_loads<D>(sb, &tm_v, g, k0 + 128, bar_v);
+    }
+    store_rows_staged<D>(t_row + col_o, l, sb + L::kV, a.out, a.hq, h, q0, min(128, s1 - q0));
+    tc::fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc::fence_after();
+        tc::tmem_dealloc(tmem, 256);
     }
 }
 

@@ -3,19 +3,22 @@
 // Page write (qwenasr.cpp ARCHITECTURE.md, "Qwen3 Thinker decoder": prefill
 // rewinds the cache and writes the fresh K/V of the whole prompt span at
 // [n_past, n_past + T) with n_past = 0): row i of request r is copied bit for
-// bit to slot i % 16 of page page_table[r][i / 16], for K and V.  The CTA of
+// bit to slot i % 16 of page page_table[r][i / 16], for K and V.  The job of
 // query tile t and the first query head of each KV head writes the rows of
 // tile t from its diagonal K/V tile, already in shared memory for the
 // attention, so the prompt's K and V are read from HBM once for both.
 //
 // Attention: row i of request r attends over rows j <= i of the same request
 // (same section: attend over [0, n_past + T)), GQA group h / 2, from the
-// packed k and v, on the tensor cores (attn_tc.cuh): one CTA per (128-row
-// query tile, query head, request) with causal key tiles 0..tile; the two
-// query heads of a KV head are adjacent in launch order, so their K/V tiles
-// come from L2 the second time.
+// packed k and v, on the tensor cores (attn_tc.cuh, prefill_tc_kernel): one
+// CTA per (128-row query tile, request, query head), longest jobs launched
+// first, each over its causal key tiles 0..tile; the two query heads of a KV
+// head are adjacent in launch order, so their K/V tiles come from L2 the
+// second time.
 #include <cuda_runtime.h>
 #include <stdint.h>
+
+#include <algorithm>
 
 #include "common.cuh"
 #include "qa_internal.h"
@@ -60,19 +63,20 @@ cudaError_t launch_prefill(const void *q, const void *k, const void *v, const in
     // a request holds at most max_pages_per_seq * page_size rows
     const long long max_len = (long long)p.max_pages_per_seq * p.page_size;
     const long long qtiles = (max_len + 127) / 128;
-    if (qtiles > 0x7fffffffLL) return cudaErrorInvalidValue;
     if (qtiles > 65535 || batch > 65535) return cudaErrorInvalidValue;
     const dim3 grid(p.n_q_heads, batch, (unsigned)qtiles);
     constexpr uint32_t smem = AttnTcLayout<128>::kSmem;
-    if (p.n_q_heads == 2 * p.n_kv_heads) {
-        e = cudaFuncSetAttribute(attn_tc_kernel<128, 2, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        attn_tc_kernel<128, 2, true><<<grid, 128, smem, stream>>>(tq, tk, tv, a, status);
-    } else {
-        e = cudaFuncSetAttribute(attn_tc_kernel<128, 1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        attn_tc_kernel<128, 1, true><<<grid, 128, smem, stream>>>(tq, tk, tv, a, status);
-    }
+    auto launch = [&](auto kernel) -> cudaError_t {
+        cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (err != cudaSuccess) return err;
+        err = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                   (int)cudaSharedmemCarveoutMaxShared);
+        if (err != cudaSuccess) return err;
+        kernel<<<grid, 128, smem, stream>>>(tq, tk, tv, a, status);
+        return cudaSuccess;
+    };
+    e = p.n_q_heads == 2 * p.n_kv_heads ? launch(prefill_tc_kernel<2>) : launch(prefill_tc_kernel<1>);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

@@ -23,7 +23,8 @@ pinned host memory and the output copied back and read every step),
 `cpu_baseline` (the fp64 oracle on this host's cores, whole workload),
 `rows` (the other hot-path operations measured the same way: ragged causal
 prefill with page write, AuT windowed attention, long-context decode, the
-decode step with the QK-norm + RoPE KV append, the tiny case).  With --impl reference the oracle itself is timed as the
+decode step with the QK-norm + RoPE KV append, paged cross-attention decode,
+the tiny case).  With --impl reference the oracle itself is timed as the
 reference arm.
 """
 from __future__ import annotations
@@ -374,7 +375,7 @@ def run_ours(args, world, rank, local_rank):
         print(json.dumps(line))
 
 
-ROW_NAMES = ("prefill", "window", "decode_long", "decode_step", "tiny")
+ROW_NAMES = ("prefill", "window", "decode_long", "decode_step", "cross_decode", "tiny")
 
 
 def measure_rows(qa, device, stream, peaks, args, which=ROW_NAMES):
@@ -392,6 +393,8 @@ def measure_rows(qa, device, stream, peaks, args, which=ROW_NAMES):
         _row_decode_long(qa, device, stream, peaks, steps, rows)
     if "decode_step" in which:
         _row_decode_step(qa, device, stream, peaks, steps, rows)
+    if "cross_decode" in which:
+        _row_cross_decode(qa, device, stream, peaks, steps, rows)
     if "tiny" in which:
         _row_tiny(qa, device, stream, steps, rows)
     status = qa.qa_device_status(stream)
@@ -532,6 +535,37 @@ def _row_decode_step(qa, device, stream, peaks, steps, rows):
     torch.cuda.empty_cache()
 
 
+def _row_cross_decode(qa, device, stream, peaks, steps, rows):
+    """Paged cross-attention decode: 32 requests x 1500 encoder frames, 8 query
+    heads over 8 KV heads (a cache written once, read every step)."""
+    import torch
+
+    B, L, H = 32, 1500, 8
+    n_pages = B * -(-L // 16)
+    w = wl.decode_workload(6, [L] * B, num_pages=n_pages, max_pages=-(-L // 16), hq=H, hkv=H)
+    pt, sl = dev_tensor(w["page_table"], device), dev_tensor(w["seq_lens"], device)
+    cps = [{k: dev_tensor(w[k], device) for k in ("q", "k_pages", "v_pages")} for _ in range(2)]  # 2 x 197 MB > L2
+    ws = torch.zeros(qa.qa_decode_workspace_size(B, L, n_q_heads=H, n_kv_heads=H, num_pages=n_pages,
+                                                 max_pages_per_seq=-(-L // 16)), dtype=torch.uint8, device=device)
+    outd = torch.empty(B, H, 128, dtype=torch.bfloat16, device=device)
+
+    def mk(c):
+        return lambda: qa.qa_decode_attn(c["q"], c["k_pages"], c["v_pages"], pt, sl, outd, workspace=ws,
+                                         stream=stream)
+
+    n = max(20, steps // 2)
+    el, _ = graph_time([mk(c) for c in cps], n, 5, stream)
+    t = el / n
+    by = decode_bytes(w["seq_lens"], hq=H, hkv=H)
+    rows["cross_decode"] = {"workload": "paged cross-attention decode: 32 requests x 1500 encoder frames, "
+                                        "8 query heads over 8 KV heads x 128, 16-token pages",
+                            "us_per_call": round(t * 1e6, 2), "gbs": round(by / t / 1e9, 1),
+                            "frac_hbm": round(by / t / 1e9 / peaks["hbm"], 4), "bytes": by,
+                            "gpu_launches_per_call": 1}
+    del cps
+    torch.cuda.empty_cache()
+
+
 def _row_tiny(qa, device, stream, steps, rows):
     """Tiny: prefill of 64 tokens then one decode token (latency)."""
     import torch
@@ -563,7 +597,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--rows", default="all",
-                    help="other hot-path rows to measure: all, none, or a comma list of prefill,window,decode_long,decode_step,tiny")
+                    help="other hot-path rows to measure: all, none, or a comma list of prefill,window,decode_long,decode_step,cross_decode,tiny")
     ap.add_argument("--no-cpu", action="store_true", help="skip the cpu_baseline leg")
     args = ap.parse_args()
     if args.warmup < 3:

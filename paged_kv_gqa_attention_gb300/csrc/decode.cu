@@ -537,25 +537,47 @@ __global__ void __launch_bounds__((kMaxHkv + 1) * 32, 1) decode_splitk_kernel(co
 #pragma unroll
                 for (int i = 0; i < GROUP; ++i) {
                     const int h = g * GROUP + i;
-                    // two passes of independent loads: the global max, then
-                    // the weighted sums (no load waits on an earlier result)
-                    float mm = -INFINITY;
-#pragma unroll 4
-                    for (int c = c_lo; c <= c_hi; ++c) mm = fmaxf(mm, __ldcg(a.part_ml + ((size_t)(c + b) * hq + h) * 2));
-                    float ls = 0.f, o[4] = {0.f, 0.f, 0.f, 0.f};
-                    if (mm != -INFINITY) {
-#pragma unroll 4
-                        for (int c = c_lo; c <= c_hi; ++c) {
-                            const size_t r = (size_t)(c + b) * hq + h;
-                            const float mc = __ldcg(a.part_ml + r * 2), lc = __ldcg(a.part_ml + r * 2 + 1);
-                            const float4 pv = __ldcg(reinterpret_cast<const float4 *>(a.part_acc + r * kD + 4 * lane));
-                            const float w = exp2_approx(mc - mm);  // 0 for an empty partial (mc = -inf)
-                            ls += w * lc;
-                            o[0] += w * pv.x;
-                            o[1] += w * pv.y;
-                            o[2] += w * pv.z;
-                            o[3] += w * pv.w;
+                    // online merge over batches of up to 8 partials whose
+                    // loads are all in flight together (one L2 round trip per
+                    // batch; requests of this workload span a few CTAs)
+                    constexpr int kBatch = 8;
+                    float mm = -INFINITY, ls = 0.f, o[4] = {0.f, 0.f, 0.f, 0.f};
+                    for (int c0 = c_lo; c0 <= c_hi; c0 += kBatch) {
+                        float mc[kBatch], lc[kBatch];
+                        float4 pv[kBatch];
+#pragma unroll
+                        for (int u = 0; u < kBatch; ++u) {
+                            if (c0 + u <= c_hi) {
+                                const size_t r = (size_t)(c0 + u + b) * hq + h;
+                                mc[u] = __ldcg(a.part_ml + r * 2);
+                                lc[u] = __ldcg(a.part_ml + r * 2 + 1);
+                                pv[u] = __ldcg(reinterpret_cast<const float4 *>(a.part_acc + r * kD + 4 * lane));
+                            } else {
+                                mc[u] = -INFINITY;
+                                lc[u] = 0.f;
+                                pv[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                            }
                         }
+                        float mb = mm;
+#pragma unroll
+                        for (int u = 0; u < kBatch; ++u) mb = fmaxf(mb, mc[u]);
+                        if (mb == -INFINITY) continue;  // nothing attended so far
+                        const float alpha = exp2_approx(mm - mb);  // 0 while mm = -inf
+                        ls *= alpha;
+                        o[0] *= alpha;
+                        o[1] *= alpha;
+                        o[2] *= alpha;
+                        o[3] *= alpha;
+#pragma unroll
+                        for (int u = 0; u < kBatch; ++u) {
+                            const float w = exp2_approx(mc[u] - mb);  // 0 for an empty partial (mc = -inf)
+                            ls += w * lc[u];
+                            o[0] += w * pv[u].x;
+                            o[1] += w * pv[u].y;
+                            o[2] += w * pv[u].z;
+                            o[3] += w * pv[u].w;
+                        }
+                        mm = mb;
                     }
                     const float inv = ls > 0.f ? 1.f / ls : 0.f;
                     uint2 w;

@@ -24,7 +24,7 @@ pinned host memory and the output copied back and read every step),
 `rows` (the other hot-path operations measured the same way: ragged causal
 prefill with page write, AuT windowed attention, long-context decode, the
 decode step with the QK-norm + RoPE KV append, paged cross-attention decode,
-the tiny case).  With --impl reference the oracle itself is timed as the
+a captured 28-layer decode step, the tiny case).  With --impl reference the oracle itself is timed as the
 reference arm.
 """
 from __future__ import annotations
@@ -375,7 +375,7 @@ def run_ours(args, world, rank, local_rank):
         print(json.dumps(line))
 
 
-ROW_NAMES = ("prefill", "window", "decode_long", "decode_step", "cross_decode", "tiny")
+ROW_NAMES = ("prefill", "window", "decode_long", "decode_step", "cross_decode", "decode_graph", "tiny")
 
 
 def measure_rows(qa, device, stream, peaks, args, which=ROW_NAMES):
@@ -395,6 +395,8 @@ def measure_rows(qa, device, stream, peaks, args, which=ROW_NAMES):
         _row_decode_step(qa, device, stream, peaks, steps, rows)
     if "cross_decode" in which:
         _row_cross_decode(qa, device, stream, peaks, steps, rows)
+    if "decode_graph" in which:
+        _row_decode_graph(qa, device, stream, peaks, steps, rows)
     if "tiny" in which:
         _row_tiny(qa, device, stream, steps, rows)
     status = qa.qa_device_status(stream)
@@ -566,6 +568,55 @@ def _row_cross_decode(qa, device, stream, peaks, steps, rows):
     torch.cuda.empty_cache()
 
 
+def _row_decode_graph(qa, device, stream, peaks, steps, rows):
+    """A whole 28-layer decode step of the 0.6B workload captured once
+    (qa_decode_graph_create) and replayed with one launch, against the same
+    28 calls launched one by one from the host."""
+    import torch
+
+    n_layers = 28
+    w = wl.decode_0p6b()
+    B = len(w["seq_lens"])
+    pt, sl = dev_tensor(w["page_table"], device), dev_tensor(w["seq_lens"], device)
+    cps = [{k: dev_tensor(w[k], device) for k in ("q", "k_pages", "v_pages")} for _ in range(4)]  # > L2, cycled
+    layers = [cps[i % 4] for i in range(n_layers)]
+    outs = [torch.empty(B, 16, 128, dtype=torch.bfloat16, device=device) for _ in range(n_layers)]
+    ws = torch.zeros(qa.qa_decode_workspace_size(B, int(w["seq_lens"].max()), num_pages=4096, max_pages_per_seq=125),
+                     dtype=torch.uint8, device=device)
+    g = qa.qa_decode_graph_create([c["q"] for c in layers], [c["k_pages"] for c in layers],
+                                  [c["v_pages"] for c in layers], pt, sl, outs, workspace=ws)
+    n = max(5, min(50, steps // 40))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def run(fn):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(n):
+                fn()
+            e1.record(stream)
+        e1.synchronize()
+        return e0.elapsed_time(e1) / 1e3 / n
+
+    def eager():
+        for i, c in enumerate(layers):
+            qa.qa_decode_attn(c["q"], c["k_pages"], c["v_pages"], pt, sl, outs[i], workspace=ws, stream=stream)
+
+    t_graph = run(lambda: g.launch(stream=stream))
+    t_eager = run(eager)
+    g.close()
+    by = decode_bytes(w["seq_lens"]) * n_layers
+    rows["decode_graph"] = {"workload": "28-layer decode step of the 0.6B workload (32 requests, L~U[200,2000]) "
+                                        "captured as one CUDA graph (qa_decode_graph_create)",
+                            "us_per_step": round(t_graph * 1e6, 2), "us_per_layer": round(t_graph * 1e6 / n_layers, 2),
+                            "gbs": round(by / t_graph / 1e9, 1), "frac_hbm": round(by / t_graph / 1e9 / peaks["hbm"], 4),
+                            "us_per_step_eager_calls": round(t_eager * 1e6, 2), "gpu_launches_per_step": n_layers}
+    del cps, layers
+    torch.cuda.empty_cache()
+
+
 def _row_tiny(qa, device, stream, steps, rows):
     """Tiny: prefill of 64 tokens then one decode token (latency)."""
     import torch
@@ -597,7 +648,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--rows", default="all",
-                    help="other hot-path rows to measure: all, none, or a comma list of prefill,window,decode_long,decode_step,cross_decode,tiny")
+                    help="other hot-path rows to measure: all, none, or a comma list of prefill,window,decode_long,decode_step,cross_decode,decode_graph,tiny")
     ap.add_argument("--no-cpu", action="store_true", help="skip the cpu_baseline leg")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -262,6 +262,39 @@ qa_status qa_decode_step(const void *q, const void *k, const void *v, const floa
                          void *v_pages, const int32_t *page_table, const int32_t *seq_lens,
                          int batch, void *out, const qa_attn_params *params);
 
+/* Captured steps (CUDA graphs): a decode step of n_layers qa_decode_attn
+ * calls, or a prefill step of a packed bucket of n_layers qa_prefill_attn
+ * calls, captured once and replayed with one launch.  M* "Speech recognition:
+ * Whisper and Qwen3-ASR", "Serving notes": steps are captured per decode batch
+ * size and per packed prefill bucket and replayed.
+ *
+ *   q, k, v, k_pages, v_pages, out: arrays of n_layers device pointers, layer
+ *   i's tensors as for the single call; page_table, seq_lens / cu_seqlens,
+ *   batch, total_tokens and params (including the decode workspace, shared by
+ *   the layers, which run one after another) are common to all layers.
+ *
+ * Every pointer and size is fixed at capture.  A replay (qa_graph_launch on
+ * any stream of the capturing device) reads the buffers' contents at replay
+ * time: refill q, lengths, page table and so on in place between replays;
+ * for another batch size or bucket, capture another graph.  The capture
+ * validates each call exactly as the single call does (returning its status
+ * and message); params->debug_checks must be 0 (it synchronises).  The pointer
+ * arrays themselves are read during the call only.  Make one ordinary call of
+ * each operation on the device before the first capture (it loads the
+ * kernels).  qa_graph_destroy releases the graph (NULL is ignored). */
+typedef struct qa_graph qa_graph;
+qa_status qa_decode_graph_create(int n_layers, const void *const *q, const void *const *k_pages,
+                                 const void *const *v_pages, const int32_t *page_table,
+                                 const int32_t *seq_lens, int batch, void *const *out,
+                                 const qa_attn_params *params, qa_graph **graph);
+qa_status qa_prefill_graph_create(int n_layers, const void *const *q, const void *const *k,
+                                  const void *const *v, const int32_t *cu_seqlens, int batch,
+                                  int total_tokens, const int32_t *page_table, void *const *k_pages,
+                                  void *const *v_pages, void *const *out, const qa_attn_params *params,
+                                  qa_graph **graph);
+qa_status qa_graph_launch(qa_graph *graph, void *stream);
+void qa_graph_destroy(qa_graph *graph);
+
 /* Windowed bidirectional attention over a packed sequence.
  *
  *   q, k, v    bf16 [total_tokens][n_q_heads][head_dim] (n_kv_heads must equal

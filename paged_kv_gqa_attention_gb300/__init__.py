@@ -77,6 +77,15 @@ def _load():
     lib.qa_decode_append.argtypes = [P, P, P, P, P, ctypes.c_float, ctypes.c_float, P, P, I, P, P, P, PP]
     lib.qa_decode_step.restype = I
     lib.qa_decode_step.argtypes = [P, P, P, P, P, ctypes.c_float, ctypes.c_float, P, P, P, P, I, P, PP]
+    PA = ctypes.POINTER(ctypes.c_void_p)
+    lib.qa_decode_graph_create.restype = I
+    lib.qa_decode_graph_create.argtypes = [I, PA, PA, PA, P, P, I, PA, PP, ctypes.POINTER(ctypes.c_void_p)]
+    lib.qa_prefill_graph_create.restype = I
+    lib.qa_prefill_graph_create.argtypes = [I, PA, PA, PA, P, I, I, P, PA, PA, PA, PP, ctypes.POINTER(ctypes.c_void_p)]
+    lib.qa_graph_launch.restype = I
+    lib.qa_graph_launch.argtypes = [P, P]
+    lib.qa_graph_destroy.restype = None
+    lib.qa_graph_destroy.argtypes = [P]
     lib.qa_window_attn.restype = I
     lib.qa_window_attn.argtypes = [P, P, P, P, I, I, P, PP]
     lib.qa_window_plan.restype = I
@@ -305,6 +314,86 @@ def qa_decode_step(q, k, v, q_gain, k_gain, page_table, seq_lens, k_pages, v_pag
                              B, _dev(out, "out", torch.bfloat16, 3), ctypes.byref(p))
     _check("qa_decode_step", st)
     return out
+
+
+class QAGraph:
+    """A captured step (qa_decode_graph_create / qa_prefill_graph_create).
+    Holds the tensors it was captured with, so their storage stays alive;
+    launch() replays it, reading the tensors' current contents."""
+
+    def __init__(self, handle, keep):
+        self._h = handle
+        self._keep = keep
+
+    def launch(self, stream=None):
+        _check("qa_graph_launch", _lib.qa_graph_launch(self._h, _stream_ptr(stream)))
+
+    def close(self):
+        if self._h:
+            _lib.qa_graph_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def _ptr_array(ts, name, dtype, ndim):
+    arr = (ctypes.c_void_p * len(ts))()
+    for i, t in enumerate(ts):
+        arr[i] = _dev(t, f"{name}[{i}]", dtype, ndim).value
+    return arr
+
+
+def qa_decode_graph_create(qs, k_pages, v_pages, page_table, seq_lens, outs, *, workspace, scale=0.0):
+    """Captures one decode step: layer i runs qa_decode_attn(qs[i],
+    k_pages[i], v_pages[i], page_table, seq_lens, outs[i]) with the shared
+    workspace.  Returns a QAGraph."""
+    torch = _torch()
+    n = len(qs)
+    if not (len(k_pages) == len(v_pages) == len(outs) == n):
+        raise ValueError("per-layer lists must have the same length")
+    B, Hq, D = qs[0].shape
+    P, PS, Hkv, _ = k_pages[0].shape
+    p = _params(n_q_heads=Hq, n_kv_heads=Hkv, head_dim=D, page_size=PS, num_pages=P,
+                max_pages_per_seq=page_table.shape[1], scale=scale, workspace=workspace)
+    h = ctypes.c_void_p()
+    st = _lib.qa_decode_graph_create(n, _ptr_array(qs, "q", torch.bfloat16, 3),
+                                     _ptr_array(k_pages, "k_pages", torch.bfloat16, 4),
+                                     _ptr_array(v_pages, "v_pages", torch.bfloat16, 4),
+                                     _dev(page_table, "page_table", torch.int32, 2),
+                                     _dev(seq_lens, "seq_lens", torch.int32, 1), B,
+                                     _ptr_array(outs, "out", torch.bfloat16, 3), ctypes.byref(p), ctypes.byref(h))
+    _check("qa_decode_graph_create", st)
+    return QAGraph(h, (qs, k_pages, v_pages, page_table, seq_lens, outs, workspace))
+
+
+def qa_prefill_graph_create(qs, ks, vs, cu_seqlens, page_table, k_pages, v_pages, outs, *, scale=0.0):
+    """Captures one prefill step of a packed bucket: layer i runs
+    qa_prefill_attn(qs[i], ks[i], vs[i], cu_seqlens, page_table, k_pages[i],
+    v_pages[i], outs[i]).  Returns a QAGraph."""
+    torch = _torch()
+    n = len(qs)
+    if not (len(ks) == len(vs) == len(k_pages) == len(v_pages) == len(outs) == n):
+        raise ValueError("per-layer lists must have the same length")
+    T, Hq, D = qs[0].shape
+    Hkv = ks[0].shape[1]
+    B = cu_seqlens.shape[0] - 1
+    P, PS = k_pages[0].shape[0], k_pages[0].shape[1]
+    p = _params(n_q_heads=Hq, n_kv_heads=Hkv, head_dim=D, page_size=PS, num_pages=P,
+                max_pages_per_seq=page_table.shape[1], scale=scale)
+    h = ctypes.c_void_p()
+    st = _lib.qa_prefill_graph_create(n, _ptr_array(qs, "q", torch.bfloat16, 3), _ptr_array(ks, "k", torch.bfloat16, 3),
+                                      _ptr_array(vs, "v", torch.bfloat16, 3),
+                                      _dev(cu_seqlens, "cu_seqlens", torch.int32, 1), B, T,
+                                      _dev(page_table, "page_table", torch.int32, 2),
+                                      _ptr_array(k_pages, "k_pages", torch.bfloat16, 4),
+                                      _ptr_array(v_pages, "v_pages", torch.bfloat16, 4),
+                                      _ptr_array(outs, "out", torch.bfloat16, 3), ctypes.byref(p), ctypes.byref(h))
+    _check("qa_prefill_graph_create", st)
+    return QAGraph(h, (qs, ks, vs, cu_seqlens, page_table, k_pages, v_pages, outs))
 
 
 def qa_window_attn(q, k, v, cu_windows, out=None, *, scale=0.0, stream=None, debug_checks=False):

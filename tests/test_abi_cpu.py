@@ -66,6 +66,12 @@ int main(void) {
     if (qa_decode_append(NULL, NULL, NULL, NULL, NULL, 1e-6f, 1e6f, NULL, NULL, 1, NULL, NULL, NULL, &p) !=
         QA_STATUS_INVALID_PARAMS) return 9;
     if (qa_window_plan(counts, 2, 0, cu, 8) != 3 || cu[1] != 104 || cu[2] != 117 || cu[3] != 122) return 6;
+    {
+        qa_graph *g = NULL;
+        if (qa_decode_graph_create(0, NULL, NULL, NULL, NULL, NULL, 1, NULL, &p, &g) != QA_STATUS_INVALID_PARAMS) return 7;
+        if (qa_graph_launch(NULL, NULL) != QA_STATUS_INVALID_PARAMS) return 8;
+        qa_graph_destroy(g);
+    }
     printf("%s\n", qa_version());
     return 0;
 }
@@ -148,6 +154,24 @@ def test_invalid_arguments_return_status_without_device(libqa):
     # then the decode's own checks: no workspace (or, on a machine without a GPU, no device)
     assert stp(fake, fake, fake, fake, fake, 1e-6, 1e6, fake, fake, fake, fake, 1, fake, ctypes.byref(p)) in (-1, -3)
     assert "workspace" in qa.qa_last_error() or "device" in qa.qa_last_error()
+
+
+def test_graph_api_rejects_bad_arguments_without_device(libqa):
+    import paged_kv_gqa_attention_gb300 as qa
+
+    lib = qa._lib
+    p = qa.qa_attn_default_params()
+    arr = (ctypes.c_void_p * 1)(0x1000)
+    h = ctypes.c_void_p(0x1234)
+    fake = ctypes.c_void_p(0x1000)
+    assert lib.qa_decode_graph_create(0, arr, arr, arr, fake, fake, 1, arr, ctypes.byref(p), ctypes.byref(h)) == -1
+    assert "n_layers" in qa.qa_last_error() and h.value is None
+    p.debug_checks = 1
+    assert lib.qa_prefill_graph_create(1, arr, arr, arr, fake, 1, 1, fake, arr, arr, arr, ctypes.byref(p),
+                                       ctypes.byref(h)) == -1
+    assert "debug_checks" in qa.qa_last_error()
+    assert lib.qa_graph_launch(None, None) == -1
+    lib.qa_graph_destroy(None)  # ignored
 
 
 def test_window_plan_matches_oracle(libqa):

@@ -72,6 +72,10 @@ def bind_library(path: str):
     lib.oracle_page_write.restype = I
     lib.oracle_window.argtypes = [P, P, P, P, I, I, I, I, Dbl, P, I, P, I]
     lib.oracle_window.restype = I
+    lib.oracle_prefill_chunk.argtypes = [P, P, P, P, P, I, I, I, I, I, P, P, P, I, I, I, Dbl, P, I, P, I]
+    lib.oracle_prefill_chunk.restype = I
+    lib.oracle_page_write_at.argtypes = [P, P, P, P, I, P, I, I, I, I, I, P, P]
+    lib.oracle_page_write_at.restype = I
     lib.oracle_qk_norm_rope.argtypes = [P, I, I, I, P, P, Dbl, Dbl, P]
     lib.oracle_qk_norm_rope.restype = I
     lib.oracle_decode_append.argtypes = [P, P, P, P, P, Dbl, Dbl, P, P, I, I, I, I, I, I, I, P, P, P, P, P]
@@ -167,6 +171,45 @@ def page_write(k, v, cu_seqlens, page_table, k_pages, v_pages):
                                    pt.shape[1], PS, P, Hkv, D, _ptr(kp), _ptr(vp))
     if rc != 0:
         raise ValueError("oracle_page_write rejected its arguments")
+    return kp, vp
+
+
+def prefill_chunk(q, k, v, cu_seqlens, n_past, page_table, k_pages, v_pages, *, scale=None, rows=None,
+                  n_threads=0):
+    """Chunked causal GQA prefill: request r has n_past[r] cached positions in
+    the pools [P,page_size,Hkv,D]; its packed new rows attend over those and
+    over new rows j <= i.  Returns float64 [T,Hq,D], or [len(rows),D] for
+    rows = flat t*Hq+h."""
+    q, k, v = _u16(q), _u16(k), _u16(v)
+    kp, vp = _u16(k_pages), _u16(v_pages)
+    cu, npast, pt = _i32(cu_seqlens), _i32(n_past), _i32(page_table)
+    T, Hq, D = q.shape
+    Hkv = k.shape[1]
+    P, PS, Hkv2, D2 = kp.shape
+    assert Hkv2 == Hkv and D2 == D and npast.shape == (len(cu) - 1,)
+    scale = 1.0 / np.sqrt(D) if scale is None else scale
+    rows_a = None if rows is None else _i32(rows)
+    n = T * Hq if rows_a is None else len(rows_a)
+    out = np.zeros((n, D), np.float64)
+    rc = _load().oracle_prefill_chunk(_ptr(q), _ptr(k), _ptr(v), _ptr(cu), _ptr(npast), len(cu) - 1, T, Hq, Hkv, D,
+                                      _ptr(kp), _ptr(vp), _ptr(pt), pt.shape[1], PS, P, float(scale), _ptr(rows_a), n,
+                                      _ptr(out), _threads(n_threads))
+    if rc != 0:
+        raise ValueError("oracle_prefill_chunk rejected its arguments")
+    return out.reshape(T, Hq, D) if rows_a is None else out
+
+
+def page_write_at(k, v, cu_seqlens, n_past, page_table, k_pages, v_pages):
+    """Bit copy of the new rows to positions n_past[r] + i of their pages;
+    returns new pool arrays."""
+    k, v = _u16(k), _u16(v)
+    kp, vp = _u16(k_pages).copy(), _u16(v_pages).copy()
+    cu, npast, pt = _i32(cu_seqlens), _i32(n_past), _i32(page_table)
+    P, PS, Hkv, D = kp.shape
+    rc = _load().oracle_page_write_at(_ptr(k), _ptr(v), _ptr(cu), _ptr(npast), len(cu) - 1, _ptr(pt), pt.shape[1],
+                                      PS, P, Hkv, D, _ptr(kp), _ptr(vp))
+    if rc != 0:
+        raise ValueError("oracle_page_write_at rejected its arguments")
     return kp, vp
 
 

@@ -43,6 +43,14 @@
  *   page_table[r][i / page_size], slot i % page_size ("write fresh K/V into
  *   the cache at [n_past, n_past + T)", same section).
  *
+ *   Chunked prefill (same section: the fresh span sits at [n_past,
+ *   n_past + T) and attends over [0, n_past + T)): request r already holds
+ *   n_past[r] positions in its pages; its new row i (absolute position
+ *   n_past + i) attends over the cached positions [0, n_past) read through
+ *   the page table and the new rows j <= i from the packed input, and the
+ *   new rows are written at positions n_past + i.  With n_past = 0 this is
+ *   the prefill above.
+ *
  *   Window: packed windows, window w owns rows [cu_w[w], cu_w[w+1]); every
  *   row attends over every row of its own window, no mask inside, no GQA
  *   (qwenasr.cpp ARCHITECTURE.md, "Windowed audio tower": block-diagonal
@@ -323,6 +331,128 @@ ORACLE_EXPORT int oracle_page_write(const uint16_t *k, const uint16_t *v, const 
         for (int i = 0; i < n; ++i) {
             int page = page_table[(size_t)r * max_pages + i / page_size];
             size_t dst = ((size_t)page * page_size + i % page_size) * row_elems;
+            size_t src = (size_t)(cu_seqlens[r] + i) * row_elems;
+            memcpy(k_pages + dst, k + src, row_elems * sizeof(uint16_t));
+            memcpy(v_pages + dst, v + src, row_elems * sizeof(uint16_t));
+        }
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Chunked prefill: new rows after n_past cached positions.                   */
+
+typedef struct {
+    const uint16_t *q, *k, *v;
+    const int32_t *cu, *n_past;
+    const uint16_t *k_pages, *v_pages;
+    const int32_t *page_table;
+    int batch, Hq, Hkv, D, max_pages, page_size;
+    double scale;
+} chunk_ctx;
+
+static void chunk_row(const void *vctx, int row, double *out)
+{
+    const chunk_ctx *c = (const chunk_ctx *)vctx;
+    int t = row / c->Hq, h = row % c->Hq;
+    int g = h / (c->Hq / c->Hkv);
+    int r = 0;
+    while (!(c->cu[r] <= t && t < c->cu[r + 1]))
+        ++r;
+    int first = c->cu[r];
+    int i = t - first;          /* local index of the new row */
+    int past = c->n_past[r];    /* cached positions before it */
+    int n = past + i + 1;       /* keys: every cached position and new rows j <= i */
+    double *q = (double *)malloc(sizeof(double) * (size_t)c->D);
+    double *K = (double *)malloc(sizeof(double) * (size_t)c->D * (size_t)n);
+    double *V = (double *)malloc(sizeof(double) * (size_t)c->D * (size_t)n);
+    for (int d = 0; d < c->D; ++d)
+        q[d] = bf16_to_double(c->q[((size_t)t * c->Hq + h) * c->D + d]);
+    for (int j = 0; j < n; ++j) {
+        const uint16_t *ks, *vs;
+        if (j < past) { /* cached: through the page table */
+            int page = c->page_table[(size_t)r * c->max_pages + j / c->page_size];
+            size_t base = (((size_t)page * c->page_size + j % c->page_size) * c->Hkv + g) * c->D;
+            ks = c->k_pages + base;
+            vs = c->v_pages + base;
+        } else { /* new: the packed rows */
+            size_t base = ((size_t)(first + (j - past)) * c->Hkv + g) * c->D;
+            ks = c->k + base;
+            vs = c->v + base;
+        }
+        for (int d = 0; d < c->D; ++d) {
+            K[(size_t)j * c->D + d] = bf16_to_double(ks[d]);
+            V[(size_t)j * c->D + d] = bf16_to_double(vs[d]);
+        }
+    }
+    oracle_attend_row(q, K, V, n, c->D, c->scale, out, NULL);
+    free(V);
+    free(K);
+    free(q);
+}
+
+/* Checks of a chunked request list: n_past >= 0, cached and new positions
+ * within the page-table row, every page id they use in [0, num_pages). */
+static int chunk_args_ok(const int32_t *cu, const int32_t *n_past, int batch, const int32_t *page_table,
+                         int max_pages, int page_size, int num_pages)
+{
+    for (int r = 0; r < batch; ++r) {
+        int n = cu[r + 1] - cu[r];
+        if (n < 0 || n_past[r] < 0 || (long long)n_past[r] + n > (long long)max_pages * page_size)
+            return 0;
+        for (int p = 0; p < (n_past[r] + n + page_size - 1) / page_size; ++p) {
+            int page = page_table[(size_t)r * max_pages + p];
+            if (page < 0 || page >= num_pages)
+                return 0;
+        }
+    }
+    return 1;
+}
+
+/* out[i] = attention of row rows[i] = t * Hq + h of the chunked prefill
+ * (all total_tokens*Hq rows when rows is NULL); the pools hold the cached
+ * positions [0, n_past) of every request. */
+ORACLE_EXPORT int oracle_prefill_chunk(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                                       const int32_t *cu_seqlens, const int32_t *n_past, int batch,
+                                       int total_tokens, int Hq, int Hkv, int D, const uint16_t *k_pages,
+                                       const uint16_t *v_pages, const int32_t *page_table, int max_pages,
+                                       int page_size, int num_pages, double scale, const int32_t *rows,
+                                       int n_rows, double *out, int n_threads)
+{
+    if (batch <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || D <= 0 || page_size <= 0)
+        return -1;
+    if (cu_seqlens[0] != 0 || cu_seqlens[batch] != total_tokens)
+        return -1;
+    if (!chunk_args_ok(cu_seqlens, n_past, batch, page_table, max_pages, page_size, num_pages))
+        return -1;
+    if (!rows)
+        n_rows = total_tokens * Hq;
+    for (int i = 0; rows && i < n_rows; ++i)
+        if (rows[i] < 0 || rows[i] >= total_tokens * Hq)
+            return -1;
+    chunk_ctx c = {q, k, v, cu_seqlens, n_past, k_pages, v_pages, page_table, batch, Hq, Hkv, D,
+                   max_pages, page_size, scale};
+    run_rows(&c, chunk_row, rows, n_rows, D, out, n_threads);
+    return 0;
+}
+
+/* Bit copy of the new rows of every request to positions n_past[r] + i of
+ * its pages.  Slots that no row maps to are left as they were.  Returns -1
+ * (and writes nothing) on inconsistent arguments. */
+ORACLE_EXPORT int oracle_page_write_at(const uint16_t *k, const uint16_t *v, const int32_t *cu_seqlens,
+                                       const int32_t *n_past, int batch, const int32_t *page_table,
+                                       int max_pages, int page_size, int num_pages, int Hkv, int D,
+                                       uint16_t *k_pages, uint16_t *v_pages)
+{
+    if (!chunk_args_ok(cu_seqlens, n_past, batch, page_table, max_pages, page_size, num_pages))
+        return -1;
+    size_t row_elems = (size_t)Hkv * D;
+    for (int r = 0; r < batch; ++r) {
+        int n = cu_seqlens[r + 1] - cu_seqlens[r];
+        for (int i = 0; i < n; ++i) {
+            int pos = n_past[r] + i; /* the new row's position */
+            int page = page_table[(size_t)r * max_pages + pos / page_size];
+            size_t dst = ((size_t)page * page_size + pos % page_size) * row_elems;
             size_t src = (size_t)(cu_seqlens[r] + i) * row_elems;
             memcpy(k_pages + dst, k + src, row_elems * sizeof(uint16_t));
             memcpy(v_pages + dst, v + src, row_elems * sizeof(uint16_t));

@@ -139,6 +139,27 @@ def window_workload(seed: int, token_counts, h: int = HE, d: int = D_ENC, rng=No
     return dict(kind="window", q=q, k=k, v=v, token_counts=token_counts)
 
 
+def chunk_workload(seed: int, past_lengths, new_lengths, num_pages: int, max_pages: int,
+                   hq: int = HQ, hkv: int = HKV, d: int = D_DEC, rng=None) -> dict:
+    """Chunked prefill: request r already holds past_lengths[r] positions in
+    its pages (random K/V there, NaN sentinels in every other slot) and brings
+    new_lengths[r] packed rows.  Draw order: pages -> cached K -> cached V ->
+    q -> k -> v."""
+    rng = rng_for(seed) if rng is None else rng
+    past = np.asarray(past_lengths, np.int32)
+    new = np.asarray(new_lengths, np.int32)
+    table = _assign_pages(rng, past + new, num_pages, max_pages)
+    k_pages = _fill_pool(rng, past, table, num_pages, hkv, d)
+    v_pages = _fill_pool(rng, past, table, num_pages, hkv, d)
+    T = int(new.sum())
+    q = normal_bf16(rng, (T, hq, d))
+    k = normal_bf16(rng, (T, hkv, d))
+    v = normal_bf16(rng, (T, hkv, d))
+    return dict(kind="chunk", q=q, k=k, v=v, cu_seqlens=cu_from_lengths(new), n_past=past.copy(),
+                page_table=table, k_pages=k_pages, v_pages=v_pages, num_pages=num_pages, max_pages=max_pages,
+                lengths=new)
+
+
 # --------------------------------------------------------------------------
 # The five named workloads.
 

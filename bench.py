@@ -22,7 +22,7 @@ pinned host memory and the output copied back and read every step),
 `roofline` (the decode call against the measured HBM copy bandwidth),
 `cpu_baseline` (the fp64 oracle on this host's cores, whole workload),
 `rows` (the other hot-path operations measured the same way: ragged causal
-prefill with page write, AuT windowed attention, long-context decode, the
+prefill with page write, chunked prefill after cached positions, AuT windowed attention, long-context decode, the
 decode step with the QK-norm + RoPE KV append, paged cross-attention decode,
 a captured 28-layer decode step, the tiny case).  With --impl reference the oracle itself is timed as the
 reference arm.
@@ -375,7 +375,8 @@ def run_ours(args, world, rank, local_rank):
         print(json.dumps(line))
 
 
-ROW_NAMES = ("prefill", "window", "decode_long", "decode_step", "cross_decode", "decode_graph", "tiny")
+ROW_NAMES = ("prefill", "chunk_prefill", "window", "decode_long", "decode_step", "cross_decode", "decode_graph",
+             "tiny")
 
 
 def measure_rows(qa, device, stream, peaks, args, which=ROW_NAMES):
@@ -387,6 +388,8 @@ def measure_rows(qa, device, stream, peaks, args, which=ROW_NAMES):
     steps = max(20, min(args.steps, 400))
     if "prefill" in which:
         _row_prefill(qa, device, stream, peaks, steps, rows)
+    if "chunk_prefill" in which:
+        _row_chunk_prefill(qa, device, stream, peaks, steps, rows)
     if "window" in which:
         _row_window(qa, device, stream, peaks, steps, rows)
     if "decode_long" in which:
@@ -430,6 +433,34 @@ def _row_prefill(qa, device, stream, peaks, steps, rows):
                        "frac_bf16_peak": round(fl / t / 1e12 / peaks["bf16"], 4),
                        "frac_hbm": round(by / t / 1e9 / peaks["hbm"], 4), "flops": fl, "bytes": by,
                        "gpu_launches_per_call": 1}
+
+
+def _row_chunk_prefill(qa, device, stream, peaks, steps, rows):
+    """Chunked prefill: 16 requests with their audio prompt cached, 16..128
+    new tokens each."""
+    import torch
+
+    w = wl.chunk_reprefill()
+    T = int(w["cu_seqlens"][-1])
+    keys = ("q", "k", "v", "cu_seqlens", "n_past", "page_table", "k_pages", "v_pages")
+    cps = [{k: dev_tensor(w[k], device) for k in keys} for _ in range(4)]
+    outp = torch.empty(T, 16, 128, dtype=torch.bfloat16, device=device)
+
+    def mk(c):
+        return lambda: qa.qa_prefill_chunk_attn(c["q"], c["k"], c["v"], c["cu_seqlens"], c["n_past"],
+                                                c["page_table"], c["k_pages"], c["v_pages"], outp, stream=stream)
+
+    el, _ = graph_time([mk(c) for c in cps], steps, 5, stream)
+    t = el / steps
+    past, new = w["n_past"].astype(np.int64), w["lengths"].astype(np.int64)
+    fl = int(np.sum(4 * 16 * 128 * (new * past + new * (new + 1) // 2)))
+    by = int(prefill_bytes(T) + np.sum(past) * 8 * 128 * 2 * 2)  # + the cached K/V, once
+    rows["chunk_prefill"] = {"workload": "chunked prefill: 16 requests, cached ceil(13 d)+40 tokens (d~U[1,30] s), "
+                                         "16..128 new tokens, GQA 16/8 x 128, new K/V written at n_past",
+                             "new_tokens": T, "cached_tokens": int(np.sum(past)), "us_per_call": round(t * 1e6, 2),
+                             "tflops": round(fl / t / 1e12, 3), "gbs": round(by / t / 1e9, 1),
+                             "frac_hbm": round(by / t / 1e9 / peaks["hbm"], 4), "flops": fl, "bytes": by,
+                             "gpu_launches_per_call": 1}
 
 
 def _row_window(qa, device, stream, peaks, steps, rows):
@@ -648,7 +679,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--rows", default="all",
-                    help="other hot-path rows to measure: all, none, or a comma list of prefill,window,decode_long,decode_step,cross_decode,decode_graph,tiny")
+                    help="other hot-path rows to measure: all, none, or a comma list of prefill,chunk_prefill,window,decode_long,decode_step,cross_decode,decode_graph,tiny")
     ap.add_argument("--no-cpu", action="store_true", help="skip the cpu_baseline leg")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -200,6 +200,31 @@ qa_status qa_prefill_attn(const void *q, const void *k, const void *v,
                           const int32_t *page_table, void *k_pages, void *v_pages, void *out,
                           const qa_attn_params *params);
 
+/* Chunked prefill: new prompt rows after n_past cached positions.
+ *
+ * qwenasr.cpp ARCHITECTURE.md, "Qwen3 Thinker decoder": a forward writes its
+ * fresh K/V into the cache at [n_past, n_past + T) and attends over
+ * [0, n_past + T) (causal, aligned at the end).  Request r already holds
+ * n_past[r] positions in its pages (page_table row r); its new rows are
+ * packed as in qa_prefill_attn.  New row i (position n_past[r] + i) attends
+ * over every cached position [0, n_past[r]) (read through the page table)
+ * and over the new rows j <= i (from the packed k, v); the new rows are
+ * written bit for bit to positions n_past[r] + i.  With every n_past = 0
+ * this is qa_prefill_attn.
+ *
+ *   n_past     int32 [batch] (device): cached positions per request
+ *   other arguments as in qa_prefill_attn
+ *
+ * Device checks: n_past outside [0, max_pages_per_seq * page_size] or
+ * n_past + new rows beyond it sets QA_DEVICE_BAD_LENGTH (the request is
+ * skipped, or its rows past the page-table row are not written); a page id
+ * outside [0, num_pages) among the cached or new positions sets
+ * QA_DEVICE_BAD_PAGE.  Supported as qa_prefill_attn. */
+qa_status qa_prefill_chunk_attn(const void *q, const void *k, const void *v,
+                                const int32_t *cu_seqlens, const int32_t *n_past, int batch,
+                                int total_tokens, const int32_t *page_table, void *k_pages,
+                                void *v_pages, void *out, const qa_attn_params *params);
+
 /* Decode KV append with per-head QK-norm and NEOX RoPE (one new token per
  * request), the step that precedes qa_decode_attn in a decode layer.
  *

@@ -86,6 +86,8 @@ def _load():
     lib.qa_graph_launch.argtypes = [P, P]
     lib.qa_graph_destroy.restype = None
     lib.qa_graph_destroy.argtypes = [P]
+    lib.qa_prefill_chunk_attn.restype = I
+    lib.qa_prefill_chunk_attn.argtypes = [P, P, P, P, P, I, I, P, P, P, P, PP]
     lib.qa_window_attn.restype = I
     lib.qa_window_attn.argtypes = [P, P, P, P, I, I, P, PP]
     lib.qa_window_plan.restype = I
@@ -249,6 +251,33 @@ def qa_prefill_attn(q, k, v, cu_seqlens, page_table, k_pages, v_pages, out=None,
                               _dev(v_pages, "v_pages", torch.bfloat16, 4), _dev(out, "out", torch.bfloat16, 3),
                               ctypes.byref(p))
     _check("qa_prefill_attn", st)
+    return out
+
+
+def qa_prefill_chunk_attn(q, k, v, cu_seqlens, n_past, page_table, k_pages, v_pages, out=None, *, scale=0.0,
+                          stream=None, debug_checks=False):
+    """Chunked prefill: request r holds n_past[r] (int32 [B], device) cached
+    positions in its pages; its packed new rows attend over those and over
+    new rows j <= i, and are written to positions n_past[r] + i.  Shapes as
+    for qa_prefill_attn.  Returns out bf16 [T,Hq,D]."""
+    torch = _torch()
+    T, Hq, D = q.shape
+    Hkv = k.shape[1]
+    B = cu_seqlens.shape[0] - 1
+    P, PS = k_pages.shape[0], k_pages.shape[1]
+    if tuple(n_past.shape) != (B,):
+        raise ValueError("n_past must be [batch]")
+    if out is None:
+        out = torch.empty_like(q)
+    p = _params(n_q_heads=Hq, n_kv_heads=Hkv, head_dim=D, page_size=PS, num_pages=P,
+                max_pages_per_seq=page_table.shape[1], scale=scale, stream=stream, debug_checks=debug_checks)
+    st = _lib.qa_prefill_chunk_attn(_dev(q, "q", torch.bfloat16, 3), _dev(k, "k", torch.bfloat16, 3),
+                                    _dev(v, "v", torch.bfloat16, 3), _dev(cu_seqlens, "cu_seqlens", torch.int32, 1),
+                                    _dev(n_past, "n_past", torch.int32, 1), B, T,
+                                    _dev(page_table, "page_table", torch.int32, 2),
+                                    _dev(k_pages, "k_pages", torch.bfloat16, 4), _dev(v_pages, "v_pages", torch.bfloat16, 4),
+                                    _dev(out, "out", torch.bfloat16, 3), ctypes.byref(p))
+    _check("qa_prefill_chunk_attn", st)
     return out
 
 

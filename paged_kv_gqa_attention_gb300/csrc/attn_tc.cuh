@@ -57,6 +57,8 @@ struct AttnTcArgs {
     const int32_t *page_table;     // [n_seg][max_pages]
     uint16_t *k_pages, *v_pages;   // [num_pages][page_size][hkv][D]
     int hkv, max_pages, num_pages, page_size;
+    // chunked prefill: cached positions per request (nullptr: none)
+    const int32_t *n_past;
 };
 
 template <int D>
@@ -276,23 +278,24 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem, uint32_t o_col, uint32_t
 }
 
 // KV page write from the K and V tiles in shared memory (128B-swizzled 64-dim
-// sub-tiles): tile row rr is row i0 + rr of segment seg and goes, bit for bit,
-// to slot i % page_size of page page_table[seg][i / page_size], KV head g.
-// Rows at or past len, or past max_pages * page_size, are not written; a page
-// id outside [0, num_pages) sets QA_DEVICE_BAD_PAGE and skips the row.  Each
-// row is written by D / 8 adjacent threads (16 bytes each), so one warp store
-// covers whole 256-byte rows.
+// sub-tiles): tile row rr is new row i0 + rr of segment seg, at position
+// i = past + i0 + rr of its request, and goes, bit for bit, to slot
+// i % page_size of page page_table[seg][i / page_size], KV head g.  Rows at
+// or past len, or positions past max_pages * page_size, are not written; a
+// page id outside [0, num_pages) sets QA_DEVICE_BAD_PAGE and skips the row.
+// Each row is written by D / 8 adjacent threads (16 bytes each), so one warp
+// store covers whole 256-byte rows.
 template <int D>
 __device__ __forceinline__ void write_kv_pages(const uint8_t *k_tile, const uint8_t *v_tile, const AttnTcArgs &a,
-                                               int seg, int i0, int len, int g, unsigned int *status) {
+                                               int seg, int i0, int len, int past, int g, unsigned int *status) {
     constexpr int kChunks = D / 8;              // 16-byte chunks per row
     constexpr int kRowsPerPass = 128 / kChunks;
     const int c = threadIdx.x % kChunks;
     const uint32_t sub = (uint32_t)(c >> 3) * tc::kSubTileBytes;
-    const int end = min(len, a.max_pages * a.page_size) - i0;
+    const int end = min(len, a.max_pages * a.page_size - past) - i0;
     const int32_t *pt = a.page_table + (size_t)seg * a.max_pages;
     for (int rr = threadIdx.x / kChunks; rr < min(end, 128); rr += kRowsPerPass) {
-        const int i = i0 + rr;
+        const int i = past + i0 + rr;
         const int page = pt[i / a.page_size];
         if (page < 0 || page >= a.num_pages) {
             if (c == 0) atomicOr(status, QA_DEVICE_BAD_PAGE);
@@ -513,11 +516,21 @@ __global__ void __launch_bounds__(128, D == 64 ? 4 : 2)
 // The first tiles are requested right after the barriers are set up, before
 // the TMEM allocation.
 //
-// Per key tile kt of the job (key tiles 0..t):
-//   - S = Q K^T (Q loaded with key tile 0 and kept);
+// PAST (chunked prefill): request b already holds n_past[b] positions in its
+// pages; the job first walks the cached key tiles (positions [128u, 128u +
+// 128) < n_past, gathered page by page through the page table with 16-row
+// TMA boxes over the pool; every new row sees every cached position), then
+// the new key tiles 0..t as below.  Rows of a cached tile past n_past (slots
+// of the boundary page that this very launch is writing, or pages not
+// loaded) are masked, and their V rows are zeroed in shared memory before
+// P V, so stale bits (NaN sentinels included) never meet a zero probability.
+//
+// Per key tile:
+//   - S = Q K^T (Q loaded with the first key tile and kept);
 //   - as soon as S has read K, the next key tile's K is requested;
-//   - diagonal tile (kt == t), first query head of each KV head: the K and V
-//     rows of the tile go to their KV-cache pages (write_kv_pages);
+//   - diagonal tile (new tile t), first query head of each KV head: the K and
+//     V rows of the tile go to their KV-cache pages (write_kv_pages) at
+//     positions n_past + row;
 //   - softmax with P_hi and P_lo both in TMEM over the scores
 //     (softmax_tile<128, true>), so no shared memory is written and K stays
 //     free for its prefetch;
@@ -525,10 +538,51 @@ __global__ void __launch_bounds__(128, D == 64 ? 4 : 2)
 //     done the next key tile's V is requested.
 // The epilogue stages O in the V buffer (store_rows_staged).  TMEM: S/P in
 // columns [0, 128), O in [128, 256).
-template <int GROUP>
+// Cached key tile u of a chunked request (positions [128u, 128u + 128)):
+// the K or V rows of pages 8u .. 8u + 7 that hold positions < past, one
+// 16-row TMA box per page per 64-dim sub-tile, into the buffer at dst, plus
+// the Q tile when with_q; one arrival with the total byte count on bar.  A
+// page id outside [0, num_pages) sets QA_DEVICE_BAD_PAGE and is not loaded.
+// One thread.
+template <int D>
+__device__ __forceinline__ void cached_tile_loads(uint32_t sb, uint32_t dst, const CUtensorMap *tm_pool,
+                                                  const CUtensorMap *tm_q, bool with_q, int h, int q0,
+                                                  const int32_t *pt_row, int u, int past, int g, int num_pages,
+                                                  uint32_t bar, unsigned int *status) {
+    using L = AttnTcLayout<D>;
+    int n = 0;
+    int pages[8];
+#pragma unroll
+    for (int p = 0; p < 8; ++p) {
+        pages[p] = -1;
+        if (128 * u + 16 * p < past) {
+            const int id = pt_row[8 * u + p];
+            if (id < 0 || id >= num_pages) {
+                atomicOr(status, QA_DEVICE_BAD_PAGE);
+            } else {
+                pages[p] = id;
+                ++n;
+            }
+        }
+    }
+    mbar_arrive_expect_tx(bar, (uint32_t)n * L::kSub * 16 * 128 + (with_q ? L::kSub * tc::kSubTileBytes : 0u));
+    if (with_q)
+#pragma unroll
+        for (int sd = 0; sd < L::kSub; ++sd)
+            tc::tma_load_3d(sb + L::kQ + sd * tc::kSubTileBytes, tm_q, sd * 64, h, q0, bar);
+#pragma unroll
+    for (int p = 0; p < 8; ++p)
+        if (pages[p] >= 0)
+#pragma unroll
+            for (int sd = 0; sd < L::kSub; ++sd)
+                tc::tma_load_3d(dst + sd * tc::kSubTileBytes + p * 16 * 128, tm_pool, sd * 64, g, pages[p] * 16, bar);
+}
+
+template <int GROUP, bool PAST>
 __global__ void __launch_bounds__(128, 2)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                      const __grid_constant__ CUtensorMap tm_v, const AttnTcArgs a, unsigned int *status) {
+                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_kp,
+                      const __grid_constant__ CUtensorMap tm_vp, const AttnTcArgs a, unsigned int *status) {
     constexpr int D = 128;
     using L = AttnTcLayout<D>;
     extern __shared__ uint8_t smem_raw[];
@@ -545,22 +599,46 @@ __global__ void __launch_bounds__(128, 2)
         if (tid == 0) atomicOr(status, QA_DEVICE_BAD_SEGMENTS);
         return;
     }
+    const int past = PAST ? a.n_past[b] : 0;
+    const int max_len = a.max_pages * a.page_size;
+    if (PAST && (past < 0 || past > max_len)) {
+        if (tid == 0 && qt == 0 && h == 0) atomicOr(status, QA_DEVICE_BAD_LENGTH);
+        return;
+    }
     // a request longer than its page-table row: flagged once; its rows past
     // the row's capacity are neither written nor (beyond the grid) attended
-    if (a.k_pages && qt == 0 && h == 0 && tid == 0 && s1 - s0 > a.max_pages * a.page_size)
+    if (a.k_pages && qt == 0 && h == 0 && tid == 0 && s1 - s0 > max_len - past)
         atomicOr(status, QA_DEVICE_BAD_LENGTH);
     if (qt * 128 >= s1 - s0) return;
     const int q0 = s0 + qt * 128;
+    const int n_ct = PAST ? (past + 127) / 128 : 0;  // cached key tiles
+    const int n_tiles = n_ct + qt + 1;
+    const int32_t *pt_row = a.page_table + (size_t)b * a.max_pages;
 
     const uint32_t bar_k = sb + L::kBar, bar_s = bar_k + 8, bar_o = bar_k + 16, bar_v = bar_k + 24;
+    // thread 0: requests the K (with Q for the first tile) or V tile of key tile u
+    auto load_k = [&](int u, bool with_q) {
+        if (PAST && u < n_ct)
+            cached_tile_loads<D>(sb, sb + L::kK, &tm_kp, &tm_q, with_q, h, q0, pt_row, u, past, g, a.num_pages, bar_k,
+                                 status);
+        else
+            issue_qk_loads<D>(sb, &tm_q, &tm_k, h, g, q0, s0 + (u - n_ct) * 128, with_q, bar_k);
+    };
+    auto load_v = [&](int u) {
+        if (PAST && u < n_ct)
+            cached_tile_loads<D>(sb, sb + L::kV, &tm_vp, &tm_q, false, h, q0, pt_row, u, past, g, a.num_pages, bar_v,
+                                 status);
+        else
+            issue_v_loads<D>(sb, &tm_v, g, s0 + (u - n_ct) * 128, bar_v);
+    };
     if (tid == 0) {
         mbar_init(bar_k, 1);
         mbar_init(bar_s, 1);
         mbar_init(bar_o, 1);
         mbar_init(bar_v, 1);
         fence_mbar_init();
-        issue_qk_loads<D>(sb, &tm_q, &tm_k, h, g, q0, s0, true, bar_k);
-        issue_v_loads<D>(sb, &tm_v, g, s0, bar_v);
+        load_k(0, true);
+        load_v(0);
     }
     if (warp == 0) tc::tmem_alloc(sb + L::kTmemSlot, 256);
     tc::fence_before();
@@ -570,11 +648,12 @@ __global__ void __launch_bounds__(128, 2)
     const uint32_t t_row = tmem + ((uint32_t)(warp * 32) << 16);
     const uint32_t col_o = 128;
     uint32_t ph = 0;  // every barrier completes once per key tile
-    const int qi = q0 + tid;
+    const int li = qt * 128 + tid;  // local index of this thread's new row
     float m = -INFINITY, l = 0.f;
 
-    for (int kt = 0; kt <= qt; ++kt, ph ^= 1) {
-        const int k0 = s0 + kt * 128;
+    for (int u = 0; u < n_tiles; ++u, ph ^= 1) {
+        const bool cached = PAST && u < n_ct;
+        const int kt = u - n_ct;  // new key tile (when not cached)
         if (tid == 0) {
             mbar_wait(bar_k, ph, status);
             tc::fence_after();
@@ -584,27 +663,45 @@ __global__ void __launch_bounds__(128, 2)
         mbar_wait(bar_s, ph, status);
         tc::fence_after();
         // S has read K: the next key tile's K
-        if (tid == 0 && kt < qt) issue_qk_loads<D>(sb, &tm_q, &tm_k, h, g, q0, k0 + 128, false, bar_k);
-        if (kt == qt && a.k_pages && h % GROUP == 0) {
-            // diagonal tile: its K/V rows are this query tile's own
-            mbar_wait(bar_v, ph, status);
-            write_kv_pages<D>(smem + L::kK, smem + L::kV, a, b, qt * 128, s1 - s0, g, status);
+        if (tid == 0 && u + 1 < n_tiles) load_k(u + 1, false);
+        int n_ok;
+        if (cached) {
+            // every cached position before `past` is visible to every new row
+            n_ok = min(128, past - 128 * u);
+            if (n_ok < 128) {
+                // rows past n_ok: stale or in-flight bits; zero their V rows
+                mbar_wait(bar_v, ph, status);
+                if (tid >= n_ok) {
+#pragma unroll
+                    for (int sd = 0; sd < L::kSub; ++sd)
+#pragma unroll
+                        for (int c = 0; c < 8; ++c)
+                            tc::st_shared_v4(sb + L::kV + sd * tc::kSubTileBytes + tid * 128 + c * 16, 0u, 0u, 0u, 0u);
+                }
+                tc::fence_proxy_async_smem();
+            }
+        } else {
+            if (kt == qt && a.k_pages && h % GROUP == 0) {
+                // diagonal tile: its K/V rows are this query tile's own
+                mbar_wait(bar_v, ph, status);
+                write_kv_pages<D>(smem + L::kK, smem + L::kV, a, b, qt * 128, s1 - s0, past, g, status);
+            }
+            n_ok = min(128, (s1 - s0) - 128 * kt);
+            n_ok = min(n_ok, li - 128 * kt + 1);
+            n_ok = max(n_ok, 0);
         }
-        int n_ok = min(128, s1 - k0);
-        n_ok = min(n_ok, qi - k0 + 1);
-        n_ok = max(n_ok, 0);
-        softmax_tile<D, true>(t_row, n_ok, a.scale_log2, 0u, 0u, t_row + col_o, kt > 0, m, l);
+        softmax_tile<D, true>(t_row, n_ok, a.scale_log2, 0u, 0u, t_row + col_o, u > 0, m, l);
         tc::fence_before();
         __syncthreads();
         if (tid == 0) {
             mbar_wait(bar_v, ph, status);
             tc::fence_after();
-            issue_pv_tp<D>(tmem, tmem + col_o, sb + L::kV, kt > 0);
+            issue_pv_tp<D>(tmem, tmem + col_o, sb + L::kV, u > 0);
             tc::mma_commit(bar_o);
         }
         mbar_wait(bar_o, ph, status);
         tc::fence_after();
-        if (tid == 0 && kt < qt) issue_v_loads<D>(sb, &tm_v, g, k0 + 128, bar_v);
+        if (tid == 0 && u + 1 < n_tiles) load_v(u + 1);
     }
     store_rows_staged<D>(t_row + col_o, l, sb + L::kV, a.out, a.hq, h, q0, min(128, s1 - q0));
     tc::fence_before();

@@ -33,15 +33,18 @@ __device__ unsigned int g_status;
 }  // namespace
 
 cudaError_t launch_prefill(const void *q, const void *k, const void *v, const int32_t *cu_seqlens,
-                           int batch, int total_tokens, const int32_t *page_table, void *k_pages,
-                           void *v_pages, void *out, const qa_attn_params &p, float scale,
+                           const int32_t *n_past, int batch, int total_tokens, const int32_t *page_table,
+                           void *k_pages, void *v_pages, void *out, const qa_attn_params &p, float scale,
                            cudaStream_t stream) {
     if (total_tokens == 0) return cudaSuccess;
     if (batch > 65535) return cudaErrorInvalidValue;
-    CUtensorMap tq, tk, tv;
+    CUtensorMap tq, tk, tv, tkp, tvp;
+    const long long pool_rows = (long long)p.num_pages * p.page_size;
     if (!make_rows_tmap(&tq, q, p.head_dim, p.n_q_heads, total_tokens) ||
         !make_rows_tmap(&tk, k, p.head_dim, p.n_kv_heads, total_tokens) ||
-        !make_rows_tmap(&tv, v, p.head_dim, p.n_kv_heads, total_tokens))
+        !make_rows_tmap(&tv, v, p.head_dim, p.n_kv_heads, total_tokens) ||
+        !make_rows_tmap(&tkp, k_pages, p.head_dim, p.n_kv_heads, pool_rows, 16) ||
+        !make_rows_tmap(&tvp, v_pages, p.head_dim, p.n_kv_heads, pool_rows, 16))
         return cudaErrorInvalidValue;
     AttnTcArgs a{};
     a.cu = cu_seqlens;
@@ -57,6 +60,7 @@ cudaError_t launch_prefill(const void *q, const void *k, const void *v, const in
     a.max_pages = p.max_pages_per_seq;
     a.num_pages = p.num_pages;
     a.page_size = p.page_size;
+    a.n_past = n_past;
     unsigned int *status = nullptr;
     cudaError_t e = cudaGetSymbolAddress(reinterpret_cast<void **>(&status), g_status);
     if (e != cudaSuccess) return e;
@@ -72,10 +76,14 @@ cudaError_t launch_prefill(const void *q, const void *k, const void *v, const in
         err = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                                    (int)cudaSharedmemCarveoutMaxShared);
         if (err != cudaSuccess) return err;
-        kernel<<<grid, 128, smem, stream>>>(tq, tk, tv, a, status);
+        kernel<<<grid, 128, smem, stream>>>(tq, tk, tv, tkp, tvp, a, status);
         return cudaSuccess;
     };
-    e = p.n_q_heads == 2 * p.n_kv_heads ? launch(prefill_tc_kernel<2>) : launch(prefill_tc_kernel<1>);
+    const bool group2 = p.n_q_heads == 2 * p.n_kv_heads;
+    if (n_past)
+        e = group2 ? launch(prefill_tc_kernel<2, true>) : launch(prefill_tc_kernel<1, true>);
+    else
+        e = group2 ? launch(prefill_tc_kernel<2, false>) : launch(prefill_tc_kernel<1, false>);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }

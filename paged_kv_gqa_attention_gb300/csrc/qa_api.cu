@@ -189,11 +189,12 @@ QA_API qa_status qa_decode_step(const void *q, const void *k, const void *v, con
     return decode_entry(fn, q, k_pages, v_pages, page_table, seq_lens, batch, out, p, &app);
 }
 
-QA_API qa_status qa_prefill_attn(const void *q, const void *k, const void *v, const int32_t *cu_seqlens, int batch,
-                                 int total_tokens, const int32_t *page_table, void *k_pages, void *v_pages, void *out,
-                                 const qa_attn_params *p) {
-    const char *fn = "qa_prefill_attn";
-    clear_error();
+namespace {
+
+// Shared by qa_prefill_attn (n_past == nullptr) and qa_prefill_chunk_attn.
+qa_status prefill_entry(const char *fn, const void *q, const void *k, const void *v, const int32_t *cu_seqlens,
+                        const int32_t *n_past, int batch, int total_tokens, const int32_t *page_table,
+                        void *k_pages, void *v_pages, void *out, const qa_attn_params *p) {
     qa_status st = check_common(p, fn);
     if (st != QA_STATUS_OK) return st;
     if ((st = check_gqa(p, fn)) != QA_STATUS_OK) return st;
@@ -201,19 +202,41 @@ QA_API qa_status qa_prefill_attn(const void *q, const void *k, const void *v, co
     if (total_tokens < 0) return fail(QA_STATUS_INVALID_PARAMS, "%s: total_tokens %d < 0", fn, total_tokens);
     if ((long long)total_tokens * p->n_q_heads * p->head_dim > (1LL << 40))
         return fail(QA_STATUS_INVALID_PARAMS, "%s: total_tokens %d too large", fn, total_tokens);
+    if ((long long)p->num_pages * p->page_size > 0x7fffffffLL)
+        return fail(QA_STATUS_INVALID_PARAMS, "%s: num_pages * page_size overflows int32", fn);
     if (!q || !k || !v || !cu_seqlens || !page_table || !k_pages || !v_pages || !out)
         return fail(QA_STATUS_INVALID_PARAMS, "%s: NULL tensor pointer", fn);
     if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) || !aligned(k_pages, 16) ||
-        !aligned(v_pages, 16) || !aligned(cu_seqlens, 4) || !aligned(page_table, 4))
+        !aligned(v_pages, 16) || !aligned(cu_seqlens, 4) || !aligned(page_table, 4) || !aligned(n_past, 4))
         return fail(QA_STATUS_INVALID_PARAMS, "%s: tensors must be 16-byte aligned (int32 arrays 4-byte)", fn);
     cudaStream_t stream = static_cast<cudaStream_t>(p->stream);
-    st = launch_result(qa::launch_prefill(q, k, v, cu_seqlens, batch, total_tokens, page_table, k_pages, v_pages, out,
-                                          *p, effective_scale(p), stream),
+    st = launch_result(qa::launch_prefill(q, k, v, cu_seqlens, n_past, batch, total_tokens, page_table, k_pages,
+                                          v_pages, out, *p, effective_scale(p), stream),
                        fn);
     if (st != QA_STATUS_OK || !p->debug_checks) return st;
     cudaError_t e;
     const unsigned int bits = qa::status_read_clear_prefill(stream, &e);
     return debug_status(bits, e, fn);
+}
+
+}  // namespace
+
+QA_API qa_status qa_prefill_attn(const void *q, const void *k, const void *v, const int32_t *cu_seqlens, int batch,
+                                 int total_tokens, const int32_t *page_table, void *k_pages, void *v_pages, void *out,
+                                 const qa_attn_params *p) {
+    clear_error();
+    return prefill_entry("qa_prefill_attn", q, k, v, cu_seqlens, nullptr, batch, total_tokens, page_table, k_pages,
+                         v_pages, out, p);
+}
+
+QA_API qa_status qa_prefill_chunk_attn(const void *q, const void *k, const void *v, const int32_t *cu_seqlens,
+                                       const int32_t *n_past, int batch, int total_tokens,
+                                       const int32_t *page_table, void *k_pages, void *v_pages, void *out,
+                                       const qa_attn_params *p) {
+    clear_error();
+    if (!n_past) return fail(QA_STATUS_INVALID_PARAMS, "qa_prefill_chunk_attn: n_past is NULL");
+    return prefill_entry("qa_prefill_chunk_attn", q, k, v, cu_seqlens, n_past, batch, total_tokens, page_table,
+                         k_pages, v_pages, out, p);
 }
 
 QA_API qa_status qa_decode_append(const void *q, const void *k, const void *v, const float *q_gain,

@@ -33,9 +33,10 @@ cudaError_t launch_decode(const void *q, const void *k_pages, const void *v_page
 unsigned int status_read_clear_decode(cudaStream_t stream, cudaError_t *err);
 
 // ---- prefill (prefill.cu): causal attention with the KV page write fused in
+// n_past: cached positions per request (chunked prefill), or nullptr (none)
 cudaError_t launch_prefill(const void *q, const void *k, const void *v, const int32_t *cu_seqlens,
-                           int batch, int total_tokens, const int32_t *page_table, void *k_pages,
-                           void *v_pages, void *out, const qa_attn_params &p, float scale,
+                           const int32_t *n_past, int batch, int total_tokens, const int32_t *page_table,
+                           void *k_pages, void *v_pages, void *out, const qa_attn_params &p, float scale,
                            cudaStream_t stream);
 unsigned int status_read_clear_prefill(cudaStream_t stream, cudaError_t *err);
 

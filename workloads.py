@@ -265,4 +265,18 @@ def decode_1p7b(seed: int = 5) -> dict:
     return w
 
 
+def chunk_reprefill(seed: int = 7) -> dict:
+    """Chunked prefill of a bucket of 16 requests whose audio prompt is
+    already cached (n_past = ceil(13 d) + 40 for d ~ U[1, 30] s, the prefill
+    bucket's recipe) and that bring 16..128 new tokens each (an assistant
+    prefix for re-transcription); 512-page pool."""
+    rng = rng_for(seed)
+    dur = rng.uniform(1.0, 30.0, size=16)
+    past = np.array([math.ceil(13.0 * x) + 40 for x in dur], np.int32)
+    new = rng.integers(16, 128, size=16, endpoint=True).astype(np.int32)
+    w = chunk_workload(seed, past, new, num_pages=512, max_pages=40, rng=rng)
+    w["name"] = "chunked prefill (16 requests, cached ceil(13 d)+40, 16..128 new tokens)"
+    return w
+
+
 WORKLOADS = {1: tiny, 2: decode_0p6b, 3: prefill_bucket, 4: window_aut, 5: decode_1p7b}

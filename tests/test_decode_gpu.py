@@ -121,3 +121,19 @@ def test_workspace_too_small_is_rejected():
     with pytest.raises(qa.QAError) as e:
         run_decode(w, workspace=ws)
     assert e.value.status == -1 and "workspace" in str(e.value)
+
+
+@pytest.mark.parametrize("lengths", [
+    (2000, 2000),                # 250 pages over 152 CTAs: two pages each, some idle
+    (31,) * 100 + (500,),        # many 2-page requests and one long one
+    (1,) * 40 + (3000,) * 3,     # idle CTAs, single-page requests and long ones
+])
+def test_uneven_page_distributions(lengths):
+    # few pages per CTA, idle CTAs, many split requests: every page must
+    # reach exactly one partial and every partial the merge
+    n_pages = sum(-(-L // 16) for L in lengths)
+    w = wl.decode_workload(700 + len(lengths), lengths, num_pages=n_pages + 11, max_pages=max(-(-L // 16) for L in lengths))
+    for call in range(3):  # the counters must be left at zero between calls
+        out = run_decode(w, debug_checks=True)
+        ref = oracle.decode(w["q"], w["k_pages"], w["v_pages"], w["page_table"], w["seq_lens"])
+        assert_close(f64(out), ref, f"lengths {lengths[:3]}... call {call}")

@@ -134,3 +134,10 @@ def test_graph_replay():
     ref = oracle.decode(r["q"], r["k_pages"], r["v_pages"], w["page_table"], w["seq_lens"])
     assert_close(f64(out), ref, "graph replay")
     assert qa.qa_device_status() == 0
+
+
+def test_new_token_with_two_pages_per_cta():
+    # two pages per CTA: the request's last page (which the fused step
+    # patches) sits in a short segment of a CTA that also merges
+    w = wl.decode_append_workload(215, (2000, 2000, 1999), num_pages=400, max_pages=125)
+    check_step(w, "two pages per CTA")

@@ -100,7 +100,9 @@ __device__ __forceinline__ void softmax_tile(uint32_t s_row, int n_ok, float sca
     // neither reduced nor exponentiated (its probabilities are written as 0)
     const bool half_tail = warp_max - (n_chunks - 1) * 32 <= 16;
     uint32_t ra[32], rb[32];
-    float mx = -INFINITY;
+    // four independent running maxima and sums: no reduction is one long
+    // dependency chain
+    float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
     tc::tmem_ld32_issue(s_row, ra);
     tc::tmem_ld32_wait(ra);
 #pragma unroll
@@ -114,16 +116,19 @@ __device__ __forceinline__ void softmax_tile(uint32_t s_row, int n_ok, float sca
             for (int j = 0; j < 32; ++j) cur[j] = c * 32 + j < n_ok ? cur[j] : __float_as_uint(-INFINITY);
         }
 #pragma unroll
-        for (int j = 0; j < 16; j += 2) mx = fmax3(mx, __uint_as_float(cur[j]), __uint_as_float(cur[j + 1]));
+        for (int j = 0; j < 16; j += 2)
+            mx4[(j >> 1) & 3] = fmax3(mx4[(j >> 1) & 3], __uint_as_float(cur[j]), __uint_as_float(cur[j + 1]));
         if (!(half_tail && c == n_chunks - 1)) {
 #pragma unroll
-            for (int j = 16; j < 32; j += 2) mx = fmax3(mx, __uint_as_float(cur[j]), __uint_as_float(cur[j + 1]));
+            for (int j = 16; j < 32; j += 2)
+                mx4[(j >> 1) & 3] = fmax3(mx4[(j >> 1) & 3], __uint_as_float(cur[j]), __uint_as_float(cur[j + 1]));
         }
         if (c + 1 < n_chunks) tc::tmem_ld32_wait(nxt);
     }
+    const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
     const float m_new = fmaxf(m, mx * scale_log2);
     const float alpha = m == -INFINITY ? 0.f : exp2_approx(m - m_new);
-    float2 psum2 = make_float2(0.f, 0.f);
+    float2 psum4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
     const float2 scale2 = make_float2(scale_log2, scale_log2);
     const float2 neg_m2 = make_float2(-m_new, -m_new);
     tc::tmem_ld32_issue(s_row, ra);
@@ -148,7 +153,7 @@ __device__ __forceinline__ void softmax_tile(uint32_t s_row, int n_ok, float sca
                     x.y = c * 32 + j + 1 < n_ok ? x.y : -INFINITY;
                 }
                 const float2 pp = make_float2(exp2_approx(x.x), exp2_approx(x.y));
-                psum2 = fadd2(psum2, pp);
+                psum4[(j >> 1) & 3] = fadd2(psum4[(j >> 1) & 3], pp);
                 const uint32_t b0 = __float_as_uint(pp.x), b1 = __float_as_uint(pp.y);
                 pk[j >> 1] = __byte_perm(b0, b1, 0x7632);
                 const float2 lo =
@@ -183,6 +188,7 @@ __device__ __forceinline__ void softmax_tile(uint32_t s_row, int n_ok, float sca
         }
     }
     tc::tmem_wait_st();
+    const float2 psum2 = fadd2(fadd2(psum4[0], psum4[1]), fadd2(psum4[2], psum4[3]));
     l = l * alpha + (psum2.x + psum2.y);
     m = m_new;
     // rescale this row of the output accumulator (warp-collective)

@@ -69,7 +69,7 @@
 extern "C" {
 #endif
 
-#define QA_ABI_VERSION 1
+#define QA_ABI_VERSION 2
 #define QA_ABI_MIN_VERSION 1
 
 /* Status codes: numbering of the qwenasr.cpp public ABI ("Public API");
@@ -103,10 +103,28 @@ typedef struct qa_attn_params {
     void *workspace;       /* decode scratch (device), caller-owned              */
     size_t workspace_bytes;
     int debug_checks;      /* 1 => synchronise and report device-side errors     */
+    int stable_metadata;   /* ABI 2: 1 => see below; ignored when abi_version < 2 */
 } qa_attn_params;
 
+/* stable_metadata (decode calls: qa_decode_attn, qa_decode_attn_noalloc,
+ * qa_decode_step).  The decode kernel is launched as a programmatic dependent
+ * of the kernel before it on the stream, so its CTAs may start while that
+ * kernel is still finishing.  With stable_metadata = 1 the caller promises
+ * that seq_lens and page_table are not written by any kernel that may still
+ * be running when this call's kernel starts: the kernel directly before it on
+ * the stream, and, if that one lets its successor start before it has waited
+ * for its own predecessor, the kernels it waits for.  (Every kernel of this
+ * library lets its successor start only after its own wait.)  A decode step
+ * whose lengths and page table are copied in, or written by a kernel followed
+ * by at least one other kernel, before its first layer meets this.  The
+ * kernel then reads them, computes its work split and fetches its first page
+ * ids before that kernel has finished, and waits only before it reads q, the
+ * pools or the workspace or writes any output.  With 0 (the default) it waits
+ * before reading anything. */
+
 /* Defaults: abi_version = QA_ABI_VERSION, 16/8/128 heads, page_size 16,
- * scale 0 (1/sqrt(head_dim)), stream NULL, no workspace, debug_checks 0.
+ * scale 0 (1/sqrt(head_dim)), stream NULL, no workspace, debug_checks 0,
+ * stable_metadata 0.
  * num_pages and max_pages_per_seq are 0 and must be set by the caller. */
 qa_attn_params qa_attn_default_params(void);
 

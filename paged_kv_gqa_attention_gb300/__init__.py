@@ -54,6 +54,7 @@ class qa_attn_params(ctypes.Structure):
         ("workspace", ctypes.c_void_p),
         ("workspace_bytes", ctypes.c_size_t),
         ("debug_checks", ctypes.c_int),
+        ("stable_metadata", ctypes.c_int),
     ]
 
 
@@ -149,7 +150,7 @@ def qa_attn_default_params() -> qa_attn_params:
 
 
 def _params(*, n_q_heads, n_kv_heads, head_dim, page_size=16, num_pages=0, max_pages_per_seq=0, scale=0.0,
-            stream=None, workspace=None, debug_checks=False):
+            stream=None, workspace=None, debug_checks=False, stable_metadata=False):
     p = _lib.qa_attn_default_params()
     p.n_q_heads, p.n_kv_heads, p.head_dim = n_q_heads, n_kv_heads, head_dim
     p.page_size, p.num_pages, p.max_pages_per_seq = page_size, num_pages, max_pages_per_seq
@@ -159,6 +160,7 @@ def _params(*, n_q_heads, n_kv_heads, head_dim, page_size=16, num_pages=0, max_p
         p.workspace = _dev(workspace, "workspace")
         p.workspace_bytes = workspace.numel() * workspace.element_size()
     p.debug_checks = 1 if debug_checks else 0
+    p.stable_metadata = 1 if stable_metadata else 0
     return p
 
 
@@ -175,12 +177,16 @@ def qa_decode_workspace_size(batch: int, max_seq_len: int, *, n_q_heads=16, n_kv
 
 
 def qa_decode_attn(q, k_pages, v_pages, page_table, seq_lens, out=None, *, workspace=None, scale=0.0,
-                   stream=None, debug_checks=False):
+                   stream=None, debug_checks=False, stable_metadata=False):
     """Paged GQA decode.  q bf16 [B,Hq,D]; pools bf16 [P,16,Hkv,D];
     page_table int32 [B,max_pages]; seq_lens int32 [B].  Returns out bf16
     [B,Hq,D].  `workspace` is a zero-filled device byte tensor of at least
     qa_decode_workspace_size(B, ...) bytes (allocated here if omitted); the
-    call leaves it zero-filled, so it can be reused across calls."""
+    call leaves its arrival counters at zero, so it can be reused across
+    calls without clearing.
+    stable_metadata=True: the caller promises that page_table and seq_lens
+    are not written by the kernel just before this call on the stream (see
+    qa_attn_params::stable_metadata in qa.h)."""
     torch = _torch()
     B, Hq, D = q.shape
     P, PS, Hkv, D2 = k_pages.shape
@@ -194,7 +200,7 @@ def qa_decode_attn(q, k_pages, v_pages, page_table, seq_lens, out=None, *, works
         workspace = torch.zeros(nbytes, dtype=torch.uint8, device=q.device)
     p = _params(n_q_heads=Hq, n_kv_heads=Hkv, head_dim=D, page_size=PS, num_pages=P,
                 max_pages_per_seq=page_table.shape[1], scale=scale, stream=stream, workspace=workspace,
-                debug_checks=debug_checks)
+                debug_checks=debug_checks, stable_metadata=stable_metadata)
     st = _lib.qa_decode_attn(_dev(q, "q", torch.bfloat16, 3), _dev(k_pages, "k_pages", torch.bfloat16, 4),
                              _dev(v_pages, "v_pages", torch.bfloat16, 4),
                              _dev(page_table, "page_table", torch.int32, 2), _dev(seq_lens, "seq_lens", torch.int32, 1),
@@ -204,7 +210,7 @@ def qa_decode_attn(q, k_pages, v_pages, page_table, seq_lens, out=None, *, works
 
 
 def qa_decode_attn_noalloc(q, k_pages, v_pages, page_table, seq_lens, out=None, *, scale=0.0, stream=None,
-                           debug_checks=False):
+                           debug_checks=False, stable_metadata=False):
     """qa_decode_attn without a workspace, for callers that cannot allocate
     device memory: the split-K scratch is a fixed 4 MiB array inside the
     library, shared by every call on the device (calls that overlap on the
@@ -221,7 +227,8 @@ def qa_decode_attn_noalloc(q, k_pages, v_pages, page_table, seq_lens, out=None, 
     if out is None:
         out = torch.empty_like(q)
     p = _params(n_q_heads=Hq, n_kv_heads=Hkv, head_dim=D, page_size=PS, num_pages=P,
-                max_pages_per_seq=page_table.shape[1], scale=scale, stream=stream, debug_checks=debug_checks)
+                max_pages_per_seq=page_table.shape[1], scale=scale, stream=stream, debug_checks=debug_checks,
+                stable_metadata=stable_metadata)
     st = _lib.qa_decode_attn_noalloc(_dev(q, "q", torch.bfloat16, 3), _dev(k_pages, "k_pages", torch.bfloat16, 4),
                                      _dev(v_pages, "v_pages", torch.bfloat16, 4),
                                      _dev(page_table, "page_table", torch.int32, 2),
@@ -312,7 +319,7 @@ def qa_decode_append(q, k, v, q_gain, k_gain, page_table, seq_lens, k_pages, v_p
 
 
 def qa_decode_step(q, k, v, q_gain, k_gain, page_table, seq_lens, k_pages, v_pages, out=None, *, workspace=None,
-                   rms_eps=1e-6, rope_theta=1e6, scale=0.0, stream=None, debug_checks=False):
+                   rms_eps=1e-6, rope_theta=1e6, scale=0.0, stream=None, debug_checks=False, stable_metadata=False):
     """The fused decode step: qa_decode_append (QK-norm + NEOX RoPE of the
     new token at seq_lens[b] - 1, its K/V written into the pools) and
     qa_decode_attn on the rotated query, in one launch.  q pre-norm bf16
@@ -334,7 +341,7 @@ def qa_decode_step(q, k, v, q_gain, k_gain, page_table, seq_lens, k_pages, v_pag
         workspace = torch.zeros(nbytes, dtype=torch.uint8, device=q.device)
     p = _params(n_q_heads=Hq, n_kv_heads=Hkv, head_dim=D, page_size=PS, num_pages=P,
                 max_pages_per_seq=page_table.shape[1], scale=scale, stream=stream, workspace=workspace,
-                debug_checks=debug_checks)
+                debug_checks=debug_checks, stable_metadata=stable_metadata)
     st = _lib.qa_decode_step(_dev(q, "q", torch.bfloat16, 3), _dev(k, "k", torch.bfloat16, 3),
                              _dev(v, "v", torch.bfloat16, 3), _dev(q_gain, "q_gain", torch.float32, 1),
                              _dev(k_gain, "k_gain", torch.float32, 1), float(rms_eps), float(rope_theta),
@@ -376,10 +383,12 @@ def _ptr_array(ts, name, dtype, ndim):
     return arr
 
 
-def qa_decode_graph_create(qs, k_pages, v_pages, page_table, seq_lens, outs, *, workspace, scale=0.0):
+def qa_decode_graph_create(qs, k_pages, v_pages, page_table, seq_lens, outs, *, workspace, scale=0.0,
+                           stable_metadata=False):
     """Captures one decode step: layer i runs qa_decode_attn(qs[i],
     k_pages[i], v_pages[i], page_table, seq_lens, outs[i]) with the shared
-    workspace.  Returns a QAGraph."""
+    workspace.  stable_metadata as for qa_decode_attn (no layer writes the
+    page table or the lengths).  Returns a QAGraph."""
     torch = _torch()
     n = len(qs)
     if not (len(k_pages) == len(v_pages) == len(outs) == n):
@@ -387,7 +396,8 @@ def qa_decode_graph_create(qs, k_pages, v_pages, page_table, seq_lens, outs, *, 
     B, Hq, D = qs[0].shape
     P, PS, Hkv, _ = k_pages[0].shape
     p = _params(n_q_heads=Hq, n_kv_heads=Hkv, head_dim=D, page_size=PS, num_pages=P,
-                max_pages_per_seq=page_table.shape[1], scale=scale, workspace=workspace)
+                max_pages_per_seq=page_table.shape[1], scale=scale, workspace=workspace,
+                stable_metadata=stable_metadata)
     h = ctypes.c_void_p()
     st = _lib.qa_decode_graph_create(n, _ptr_array(qs, "q", torch.bfloat16, 3),
                                      _ptr_array(k_pages, "k_pages", torch.bfloat16, 4),

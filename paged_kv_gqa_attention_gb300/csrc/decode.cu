@@ -66,6 +66,9 @@ struct DecodeArgs {
     int *arrivals;    // [kDecodeMaxBatch][kMaxHkv], zero between calls
     int batch, hkv, max_pages, num_pages;
     float scale_log2;  // scale * log2(e)
+    // lengths and page table may be read before the preceding kernel ends
+    // (qa_attn_params::stable_metadata)
+    int early;
     // fused decode step only: q is the pre-norm projection; the new token's
     // pre-norm k and its v are appended at position seq_lens[b] - 1
     const uint16_t *k_new, *v_new;  // [B][Hkv][D]
@@ -201,9 +204,15 @@ __global__ void __launch_bounds__((kMaxHkv + 1) * 32, 1) decode_splitk_kernel(co
 
     // Launched as a programmatic dependent: wait for the previous kernel on the
     // stream to finish (and its writes to land) before touching global
-    // memory, and let the next one start its own prologue early.
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // memory -- or, when the caller vouches that lengths and page table are
+    // not its output (a.early), only before touching anything else -- and
+    // then let the next one start its own prologue early.  The trigger comes
+    // after the wait in both modes, so a kernel that starts early on this
+    // one's trigger never overlaps a kernel older than this one.
+    if (!a.early) {
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    }
 
     // Prefix sums of page counts over requests (warp 0), barrier init.
     if (warp == 0) {
@@ -231,6 +240,27 @@ __global__ void __launch_bounds__((kMaxHkv + 1) * 32, 1) decode_splitk_kernel(co
     }
     __syncthreads();
 
+    const int total = prefix[a.batch];
+    const int per = (total + gridDim.x - 1) / gridDim.x;
+    const int lo = blockIdx.x * per;
+    const int hi = min(lo + per, total);
+    // Requests b0 (holding page lo) .. b_last (holding page hi - 1).  Visit
+    // order: b_last, then b0 .. b_last - 1 (see the header comment).
+    const int b0 = lo < hi ? first_request_past(prefix, a.batch, lo) : 0;
+    const int b_last = lo < hi ? first_request_past(prefix, a.batch, hi - 1) : -1;
+    const int n_visit = lo < hi ? b_last - b0 + 1 : 0;
+    // the producer's first 32 page ids (page table only)
+    int first_ids = -1;
+    if (warp == n_consumers && n_visit > 0) {
+        const int p0 = prefix[b_last];
+        const int j0 = max(lo, p0) - p0, j1 = min(hi, prefix[b_last + 1]) - p0;
+        first_ids = j0 + lane < j1 ? a.page_table[(size_t)b_last * a.max_pages + j0 + lane] : -1;
+    }
+    if (a.early) {
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    }
+
     // CTA 0 writes the zero rows of requests with nothing to attend over.
     if (blockIdx.x == 0) {
         const int chunks = hq * kD * 2 / 16;  // 16-byte chunks per request
@@ -241,18 +271,7 @@ __global__ void __launch_bounds__((kMaxHkv + 1) * 32, 1) decode_splitk_kernel(co
         }
     }
 
-    const int total = prefix[a.batch];
-    if (total == 0) return;
-    const int per = (total + gridDim.x - 1) / gridDim.x;
-    const int lo = blockIdx.x * per;
-    const int hi = min(lo + per, total);
-    if (lo >= hi) return;
-
-    // Requests b0 (holding page lo) .. b_last (holding page hi - 1).  Visit
-    // order: b_last, then b0 .. b_last - 1 (see the header comment).
-    const int b0 = first_request_past(prefix, a.batch, lo);
-    const int b_last = first_request_past(prefix, a.batch, hi - 1);
-    const int n_visit = b_last - b0 + 1;
+    if (total == 0 || lo >= hi) return;
 
     // Warm L2 with the per-request rows read at the start of every later
     // segment (q; for the fused step the new token's k and v too), so those
@@ -284,7 +303,7 @@ __global__ void __launch_bounds__((kMaxHkv + 1) * 32, 1) decode_splitk_kernel(co
             const int j0 = max(lo, p0) - p0, j1 = min(hi, p1) - p0;
             const int32_t *row = a.page_table + (size_t)b * a.max_pages;
             for (int jb = j0; jb < j1; jb += 32) {
-                const int mine = jb + lane < j1 ? row[jb + lane] : -1;
+                const int mine = (k == 0 && jb == j0) ? first_ids : (jb + lane < j1 ? row[jb + lane] : -1);
                 const int cnt = min(32, j1 - jb);
                 for (int u = 0; u < cnt; ++u, ++it) {
                     const int page = __shfl_sync(0xffffffffu, mine, u);
@@ -627,6 +646,7 @@ cudaError_t launch_decode(const void *q, const void *k_pages, const void *v_page
     a.max_pages = p.max_pages_per_seq;
     a.num_pages = p.num_pages;
     a.scale_log2 = scale * kLog2e;
+    a.early = (p.abi_version >= 2 && p.stable_metadata) ? 1 : 0;
     a.k_new = a.v_new = nullptr;
     a.q_gain = a.k_gain = nullptr;
     a.k_pages_w = a.v_pages_w = nullptr;

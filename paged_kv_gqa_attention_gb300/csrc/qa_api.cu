@@ -105,6 +105,7 @@ QA_API qa_attn_params qa_attn_default_params(void) {
     p.workspace = nullptr;
     p.workspace_bytes = 0;
     p.debug_checks = 0;
+    p.stable_metadata = 0;
     return p;
 }
 

@@ -51,6 +51,7 @@ def test_header_is_strict_c99(libqa, tmp_path):
     c = tmp_path / "abi_c.c"
     c.write_text(r'''
 #include "qa.h"
+#include <stddef.h>
 #include <stdio.h>
 #include <string.h>
 int main(void) {
@@ -73,6 +74,8 @@ int main(void) {
         qa_graph_destroy(g);
     }
     printf("%s\n", qa_version());
+    printf("sizeof %u stable_metadata %u\n", (unsigned)sizeof(qa_attn_params),
+           (unsigned)offsetof(qa_attn_params, stable_metadata));
     return 0;
 }
 ''')
@@ -81,7 +84,13 @@ int main(void) {
                     str(c), "-o", str(exe), _build.LIB, f"-Wl,-rpath,{os.path.dirname(_build.LIB)}"], check=True)
     res = subprocess.run([str(exe)], capture_output=True, text=True)
     assert res.returncode == 0, res.stdout + res.stderr
-    assert "abi 1" in res.stdout
+    import paged_kv_gqa_attention_gb300 as qa
+
+    assert "abi 2" in res.stdout
+    # the ctypes mirror of qa_attn_params has the C layout
+    size, off = (int(x) for x in res.stdout.split()[-3::2])
+    assert ctypes.sizeof(qa.qa_attn_params) == size
+    assert qa.qa_attn_params.stable_metadata.offset == off
 
 
 def _params(libqa):

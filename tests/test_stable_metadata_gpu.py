@@ -1,0 +1,130 @@
+"""GPU parity of the decode calls with qa_attn_params.stable_metadata = 1
+(the kernel reads lengths and page table before the preceding kernel on the
+stream has finished, everything else after) against the fp64 oracle, in the
+orders a decode step launches them: after the append that writes q, after a
+plain kernel that writes q, as the layers of one captured graph; and a
+caller of ABI 1, whose struct has no such field, is not affected by the
+byte it leaves there.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads as wl
+from _util import assert_close, f64, to_dev
+
+pytestmark = pytest.mark.gpu
+import torch  # noqa: E402
+
+import paged_kv_gqa_attention_gb300 as qa  # noqa: E402
+
+EPS, THETA = wl.RMS_EPS, wl.ROPE_THETA
+KEYS = ("q_new", "k_new", "v_new", "q_gain", "k_gain", "page_table", "seq_lens", "k_pages", "v_pages")
+
+
+def _oracle_step(w):
+    r = oracle.decode_append(w["q_new"], w["k_new"], w["v_new"], w["q_gain"], w["k_gain"], w["page_table"],
+                             w["seq_lens"], w["k_pages"], w["v_pages"], eps=EPS, theta=THETA)
+    return oracle.decode(r["q"], r["k_pages"], r["v_pages"], w["page_table"], w["seq_lens"])
+
+
+def test_after_the_append_that_writes_q():
+    w = wl.with_append(wl.decode_0p6b(), 3)
+    ref = _oracle_step(w)
+    d = {k: to_dev(w[k]) for k in KEYS}
+    s = torch.cuda.Stream()
+    q_rot = torch.empty_like(d["q_new"])
+    out = torch.empty_like(d["q_new"])
+    with torch.cuda.stream(s):
+        qa.qa_decode_append(d["q_new"], d["k_new"], d["v_new"], d["q_gain"], d["k_gain"], d["page_table"],
+                            d["seq_lens"], d["k_pages"], d["v_pages"], q_out=q_rot, rms_eps=EPS, rope_theta=THETA,
+                            stream=s)
+        qa.qa_decode_attn(q_rot, d["k_pages"], d["v_pages"], d["page_table"], d["seq_lens"], out, stream=s,
+                          stable_metadata=True)
+    torch.cuda.synchronize()
+    assert_close(f64(out), ref, "append then decode, stable metadata")
+    assert qa.qa_device_status() == 0
+
+
+def test_fused_step_after_a_kernel_that_writes_q():
+    w = wl.with_append(wl.decode_0p6b(), 4)
+    ref = _oracle_step(w)
+    d = {k: to_dev(w[k]) for k in KEYS}
+    src = d["q_new"].clone()
+    d["q_new"].zero_()
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        d["q_new"].copy_(src)  # the q projection's stand-in, just before the step
+        out = qa.qa_decode_step(d["q_new"], d["k_new"], d["v_new"], d["q_gain"], d["k_gain"], d["page_table"],
+                                d["seq_lens"], d["k_pages"], d["v_pages"], rms_eps=EPS, rope_theta=THETA, stream=s,
+                                stable_metadata=True)
+    torch.cuda.synchronize()
+    assert_close(f64(out), ref, "fused step, stable metadata")
+    assert qa.qa_device_status() == 0
+
+
+def _layer(base, i):
+    """Layer i over the same page table and lengths: a fresh query and the
+    base keys scaled by 2^-i (exact in bf16); the values stay at N(0, 1),
+    the scale the absolute tolerance is stated for."""
+    c = dict(base)
+    c["q"] = wl.normal_bf16(wl.rng_for(700 + i), base["q"].shape)
+    c["k_pages"] = wl.bf16_bits((wl.bf16_to_f64(base["k_pages"]) * 2.0 ** -i).astype(np.float32))
+    return c
+
+
+def test_graph_of_layers_follows_refills():
+    base = wl.decode_0p6b()
+    layers = [_layer(base, i) for i in range(3)]
+    refs = [oracle.decode(c["q"], c["k_pages"], c["v_pages"], c["page_table"], c["seq_lens"]) for c in layers]
+    pt, sl = to_dev(base["page_table"]), to_dev(base["seq_lens"])
+    qs = [to_dev(c["q"]) for c in layers]
+    kp = [to_dev(c["k_pages"]) for c in layers]
+    vp = [to_dev(c["v_pages"]) for c in layers]
+    outs = [torch.empty_like(q) for q in qs]
+    B = len(base["seq_lens"])
+    ws = torch.zeros(qa.qa_decode_workspace_size(B, 2000, num_pages=kp[0].shape[0],
+                                                 max_pages_per_seq=pt.shape[1]), dtype=torch.uint8, device="cuda")
+    srcs = [q.clone() for q in qs]
+    g = qa.qa_decode_graph_create(qs, kp, vp, pt, sl, outs, workspace=ws, stable_metadata=True)
+    try:
+        for rep in range(2):
+            for q in qs:
+                q.zero_()
+            for o in outs:
+                o.zero_()
+            for q, src in zip(qs, srcs):
+                q.copy_(src)  # refilled in place right before the replay
+            g.launch()
+            torch.cuda.synchronize()
+            for i, (o, r) in enumerate(zip(outs, refs)):
+                assert_close(f64(o), r, f"replay {rep} layer {i}")
+    finally:
+        g.close()
+    assert qa.qa_device_status() == 0
+
+
+def test_abi1_caller_ignores_the_field():
+    w = wl.decode_0p6b()
+    ref = oracle.decode(w["q"], w["k_pages"], w["v_pages"], w["page_table"], w["seq_lens"])
+    d = {k: to_dev(w[k]) for k in ("q", "k_pages", "v_pages", "page_table", "seq_lens")}
+    B = len(w["seq_lens"])
+    out = torch.empty_like(d["q"])
+    ws = torch.zeros(qa.qa_decode_workspace_size(B, 2000, num_pages=d["k_pages"].shape[0],
+                                                 max_pages_per_seq=d["page_table"].shape[1]), dtype=torch.uint8,
+                     device="cuda")
+    p = qa._params(n_q_heads=16, n_kv_heads=8, head_dim=128, num_pages=d["k_pages"].shape[0],
+                   max_pages_per_seq=d["page_table"].shape[1], workspace=ws, stable_metadata=True)
+    p.abi_version = 1
+    vp = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
+    for call in range(2):  # the second call reuses the workspace the first left
+        out.zero_()
+        st = qa._lib.qa_decode_attn(vp(d["q"]), vp(d["k_pages"]), vp(d["v_pages"]), vp(d["page_table"]),
+                                    vp(d["seq_lens"]), B, vp(out), ctypes.byref(p))
+        assert st == 0, qa.qa_last_error()
+        torch.cuda.synchronize()
+        assert_close(f64(out), ref, f"ABI 1 caller, call {call}")
+    assert qa.qa_device_status() == 0

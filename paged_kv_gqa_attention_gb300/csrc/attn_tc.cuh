@@ -22,8 +22,13 @@
 //      about 16 significant bits, so the P V product keeps the softmax
 //      probabilities at (nearly) fp32 precision, as the precision policy asks
 //      (score and softmax intermediates in float32).
-//   4. When the running max of a row moved, the thread rescales its row of
-//      the fp32 output accumulator O in TMEM by alpha = 2^(m_old - m_new).
+//   4. The reference max m of a row (exponentials are taken relative to it)
+//      moves only when a tile's max exceeds it by more than kRescaleSlack
+//      (8, in log2 units): below that the probabilities stay <= 2^8 and the
+//      row keeps m, so O and the sum need no rescaling (softmax is invariant
+//      under the choice of reference; the sum uses the same one).  When it
+//      moves, the thread rescales its row of the fp32 output accumulator O
+//      in TMEM by alpha = 2^(m_old - m_new).
 //   5. One thread issues O += P_hi V and O += P_lo V (M = 128, N = 64 per
 //      MMA, K = 128 keys in steps of 16, V read MN-major).
 // After the last key tile each row of O is read back, divided by its softmax
@@ -85,8 +90,11 @@ struct AttnTcLayout {
 //   P_TMEM = true:  both in TMEM over the chunk of scores they replace: keys
 //                   [32c, 32c + 32) give P_hi in columns [32c, 32c + 16) and
 //                   P_lo in [32c + 16, 32c + 32) (plo_row and sw unused).
-// Updates the running (m, l) and, when `rescale`, multiplies the row of O at
-// o_row by 2^(m_old - m_new).  Warp-collective (every lane of the warp calls it).
+// Updates the running (m, l) and, when `rescale` and m moved, multiplies the
+// row of O at o_row by 2^(m_old - m_new).  Warp-collective (every lane of the warp calls it).
+// Slack of the lazy reference max, in log2 units: probabilities stay <= 2^8.
+constexpr float kRescaleSlack = 8.f;
+
 template <int D, bool P_TMEM = false>
 __device__ __forceinline__ void softmax_tile(uint32_t s_row, int n_ok, float scale_log2, uint32_t plo_row,
                                              uint32_t sw, uint32_t o_row, bool rescale, float &m, float &l) {
@@ -125,8 +133,10 @@ __device__ __forceinline__ void softmax_tile(uint32_t s_row, int n_ok, float sca
         }
         if (c + 1 < n_chunks) tc::tmem_ld32_wait(nxt);
     }
-    const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-    const float m_new = fmaxf(m, mx * scale_log2);
+    const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * scale_log2;
+    // lazy reference max (step 4 of the header); the first tile (m = -inf)
+    // always sets it
+    const float m_new = mx > m + kRescaleSlack ? mx : m;
     const float alpha = m == -INFINITY ? 0.f : exp2_approx(m - m_new);
     float2 psum4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
     const float2 scale2 = make_float2(scale_log2, scale_log2);
@@ -192,6 +202,97 @@ __device__ __forceinline__ void softmax_tile(uint32_t s_row, int n_ok, float sca
     l = l * alpha + (psum2.x + psum2.y);
     m = m_new;
     // rescale this row of the output accumulator (warp-collective)
+    if (rescale && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+            float ov[32];
+            tc::tmem_ld32(o_row + c * 32, ov);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) ov[j] *= alpha;
+            tc::tmem_st32(o_row + c * 32, ov);
+        }
+    }
+}
+
+// Single-pass form of softmax_tile<D, true> for kernels whose register
+// budget holds a whole score row (two 128-thread CTAs per SM): the live
+// 32-column chunks of the row are read from TMEM with one wait, the max and
+// the exponentials work on the registers, and P_hi / P_lo go back over the
+// scores in the softmax_tile<D, true> layout.  The scores are read once
+// instead of twice.  Same (m, l) update, lazy reference max and rescale as
+// softmax_tile.  Warp-collective.
+template <int D>
+__device__ __forceinline__ void softmax_tile_regs(uint32_t s_row, int n_ok, float scale_log2, uint32_t o_row,
+                                                  bool rescale, float &m, float &l) {
+    const int warp_max = __reduce_max_sync(0xffffffffu, n_ok);
+    const int warp_min = __reduce_min_sync(0xffffffffu, n_ok);
+    const int n_chunks = (warp_max + 31) >> 5;  // warp-uniform
+    const bool half_tail = warp_max - (n_chunks - 1) * 32 <= 16;
+    uint32_t sc[4][32];
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+        if (c < n_chunks) tc::tmem_ld32_issue(s_row + c * 32, sc[c]);
+    // one wait for all loads; each call names its chunk, so no use of a
+    // chunk moves above the wait
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+        if (c < n_chunks) tc::tmem_ld32_wait(sc[c]);
+    float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        if (c >= n_chunks) break;
+        if (c * 32 + 32 > warp_min) {  // masked keys become -inf in place
+#pragma unroll
+            for (int j = 0; j < 32; ++j) sc[c][j] = c * 32 + j < n_ok ? sc[c][j] : __float_as_uint(-INFINITY);
+        }
+        const bool upper = !(half_tail && c == n_chunks - 1);
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) {
+            if (j >= 16 && !upper) break;
+            mx4[(j >> 1) & 3] = fmax3(mx4[(j >> 1) & 3], __uint_as_float(sc[c][j]), __uint_as_float(sc[c][j + 1]));
+        }
+    }
+    const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * scale_log2;
+    const float m_new = mx > m + kRescaleSlack ? mx : m;  // lazy reference max (see softmax_tile)
+    const float alpha = m == -INFINITY ? 0.f : exp2_approx(m - m_new);
+    float2 psum4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+    const float2 scale2 = make_float2(scale_log2, scale_log2);
+    const float2 neg_m2 = make_float2(-m_new, -m_new);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        uint32_t pk[16], pl[16];
+        if (c >= n_chunks) {  // warp-uniform: a dead chunk gets zero probabilities
+#pragma unroll
+            for (int i = 0; i < 16; ++i) pk[i] = pl[i] = 0u;
+        } else {
+            auto pair = [&](int j) {
+                const float2 x =
+                    ffma2(make_float2(__uint_as_float(sc[c][j]), __uint_as_float(sc[c][j + 1])), scale2, neg_m2);
+                const float2 pp = make_float2(exp2_approx(x.x), exp2_approx(x.y));
+                psum4[(j >> 1) & 3] = fadd2(psum4[(j >> 1) & 3], pp);
+                const uint32_t b0 = __float_as_uint(pp.x), b1 = __float_as_uint(pp.y);
+                pk[j >> 1] = __byte_perm(b0, b1, 0x7632);
+                const float2 lo =
+                    fsub2(pp, make_float2(__uint_as_float(b0 & 0xffff0000u), __uint_as_float(b1 & 0xffff0000u)));
+                pl[j >> 1] = pack_bf16x2(lo.x, lo.y);
+            };
+#pragma unroll
+            for (int j = 0; j < 16; j += 2) pair(j);
+            if (half_tail && c == n_chunks - 1) {
+#pragma unroll
+                for (int i = 8; i < 16; ++i) pk[i] = pl[i] = 0u;
+            } else {
+#pragma unroll
+                for (int j = 16; j < 32; j += 2) pair(j);
+            }
+        }
+        tc::tmem_st16(s_row + c * 32, pk);
+        tc::tmem_st16(s_row + c * 32 + 16, pl);
+    }
+    tc::tmem_wait_st();
+    const float2 psum2 = fadd2(fadd2(psum4[0], psum4[1]), fadd2(psum4[2], psum4[3]));
+    l = l * alpha + (psum2.x + psum2.y);
+    m = m_new;
     if (rescale && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
@@ -696,7 +797,7 @@ __global__ void __launch_bounds__(128, 2)
             n_ok = min(n_ok, li - 128 * kt + 1);
             n_ok = max(n_ok, 0);
         }
-        softmax_tile<D, true>(t_row, n_ok, a.scale_log2, 0u, 0u, t_row + col_o, u > 0, m, l);
+        softmax_tile_regs<D>(t_row, n_ok, a.scale_log2, t_row + col_o, u > 0, m, l);
         tc::fence_before();
         __syncthreads();
         if (tid == 0) {

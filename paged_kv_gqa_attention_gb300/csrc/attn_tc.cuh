@@ -305,7 +305,8 @@ __device__ __forceinline__ void softmax_tile_regs(uint32_t s_row, int n_ok, floa
     }
 }
 
-// Epilogue through shared memory: thread r rounds its O row (divided by l)
+// Epilogue through shared memory: thread r (of the 128 threads that own the
+// tile's rows) rounds its O row (divided by l)
 // to bf16 and writes it to row r of a staging tile (D * 2 bytes per row,
 // 16-byte chunk c of row r at chunk position c ^ (r & 7), so the writes of 8
 // consecutive rows hit all banks); then each warp writes back its own 32 rows
@@ -314,9 +315,9 @@ __device__ __forceinline__ void softmax_tile_regs(uint32_t s_row, int n_ok, floa
 // of a warp are touched by that warp only.
 template <int D>
 __device__ __forceinline__ void store_rows_staged(uint32_t o_row, float l, uint32_t stage, uint16_t *out, int hq,
-                                                  int h, int q0, int row_end) {
+                                                  int h, int q0, int row_end, int r) {
     constexpr int kChunks = D / 8;  // 16-byte chunks per row
-    const int r = threadIdx.x, lane = r & 31, warp = r >> 5;
+    const int lane = r & 31, warp = r >> 5;
     const float inv = l > 0.f ? 1.f / l : 0.f;
     const uint32_t my_row = stage + (uint32_t)r * (D * 2);
 #pragma unroll
@@ -386,34 +387,70 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem, uint32_t o_col, uint32_t
 
 // KV page write from the K and V tiles in shared memory (128B-swizzled 64-dim
 // sub-tiles): tile row rr is new row i0 + rr of segment seg, at position
-// i = past + i0 + rr of its request, and goes, bit for bit, to slot
-// i % page_size of page page_table[seg][i / page_size], KV head g.  Rows at
-// or past len, or positions past max_pages * page_size, are not written; a
-// page id outside [0, num_pages) sets QA_DEVICE_BAD_PAGE and skips the row.
-// Each row is written by D / 8 adjacent threads (16 bytes each), so one warp
-// store covers whole 256-byte rows.
+// i = past + i0 + rr of its request, and goes, bit for bit, to slot i % 16 of
+// page page_table[seg][i / 16] (the page size is 16, the only one the
+// library accepts), KV head g.  Rows at or past len, or positions past
+// max_pages * 16, are not written; a page id outside [0, num_pages) sets
+// QA_DEVICE_BAD_PAGE and skips the row.
+//
+// kv_tile_page_id, called well ahead by every thread of the 128 (tix = 0 ..
+// 127, whole warps), reads the page ids: the tile's rows span at most 9
+// pages, and lane j of every warp holds the j-th.  write_kv_pages (the same
+// 128 threads) takes each row's page id from that lane with a shuffle.  Each
+// row is written by D / 8 adjacent threads (16 bytes each), so one warp store
+// covers whole 256-byte rows; a thread's rows are 8 apart, so its swizzled
+// chunk offset is the same for all of them.  A null k_tile or v_tile skips
+// that pool.
+__device__ __forceinline__ int kv_tile_page_id(const AttnTcArgs &a, int seg, int i0, int len, int past, int tix) {
+    const int lane = tix & 31;
+    const int end = min(min(len, a.max_pages * 16 - past) - i0, 128);
+    const int pos0 = past + i0;
+    if (end > 0 && pos0 / 16 + lane <= (pos0 + end - 1) / 16) return a.page_table[(size_t)seg * a.max_pages + pos0 / 16 + lane];
+    return -1;
+}
+
 template <int D>
 __device__ __forceinline__ void write_kv_pages(const uint8_t *k_tile, const uint8_t *v_tile, const AttnTcArgs &a,
-                                               int seg, int i0, int len, int past, int g, unsigned int *status) {
+                                               int i0, int len, int past, int g, unsigned int *status, int tix,
+                                               int my_page) {
+    constexpr int kPage = 16;
     constexpr int kChunks = D / 8;              // 16-byte chunks per row
     constexpr int kRowsPerPass = 128 / kChunks;
-    const int c = threadIdx.x % kChunks;
-    const uint32_t sub = (uint32_t)(c >> 3) * tc::kSubTileBytes;
-    const int end = min(len, a.max_pages * a.page_size - past) - i0;
-    const int32_t *pt = a.page_table + (size_t)seg * a.max_pages;
-    for (int rr = threadIdx.x / kChunks; rr < min(end, 128); rr += kRowsPerPass) {
-        const int i = past + i0 + rr;
-        const int page = pt[i / a.page_size];
+    const int c = tix % kChunks, rr0 = tix / kChunks;
+    const int end = min(min(len, a.max_pages * kPage - past) - i0, 128);
+    const int pos0 = past + i0;  // position of tile row 0
+    const int p_first = pos0 / kPage;
+    // shared offset of this thread's chunk in row rr: rr * 128 + this
+    const uint32_t chunk_off = (uint32_t)(c >> 3) * tc::kSubTileBytes + ((uint32_t)((c & 7) ^ (rr0 & 7)) << 4);
+    const uint32_t k_s = k_tile ? smem_u32(k_tile) + chunk_off : 0u;
+    const uint32_t v_s = v_tile ? smem_u32(v_tile) + chunk_off : 0u;
+    const size_t row_elems = (size_t)a.hkv * D;  // one pool row (slot): all KV heads
+    uint16_t *const k_dst = a.k_pages + (size_t)g * D + (size_t)c * 8;
+    uint16_t *const v_dst = a.v_pages + (size_t)g * D + (size_t)c * 8;
+#pragma unroll 4
+    for (int k = 0; k < 128 / kRowsPerPass; ++k) {  // warp-uniform trip count
+        const int rr = rr0 + k * kRowsPerPass;
+        const int pos = pos0 + rr;
+        const int page = __shfl_sync(0xffffffffu, my_page, (pos / kPage - p_first) & 31);
+        if (rr >= end) continue;
         if (page < 0 || page >= a.num_pages) {
             if (c == 0) atomicOr(status, QA_DEVICE_BAD_PAGE);
             continue;
         }
-        const uint32_t off = (uint32_t)rr * 128u + sub + ((uint32_t)((c & 7) ^ (rr & 7)) << 4);
-        const uint4 kx = *reinterpret_cast<const uint4 *>(k_tile + off);
-        const uint4 vx = *reinterpret_cast<const uint4 *>(v_tile + off);
-        const size_t dst = (((size_t)page * a.page_size + i % a.page_size) * a.hkv + g) * D + (size_t)c * 8;
-        *reinterpret_cast<uint4 *>(a.k_pages + dst) = kx;
-        *reinterpret_cast<uint4 *>(a.v_pages + dst) = vx;
+        const size_t row = ((size_t)page * kPage + (size_t)(pos % kPage)) * row_elems;
+        uint32_t x0, x1, x2, x3;
+        if (k_tile) {
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(x0), "=r"(x1), "=r"(x2), "=r"(x3)
+                         : "r"(k_s + (uint32_t)rr * 128u));
+            *reinterpret_cast<uint4 *>(k_dst + row) = make_uint4(x0, x1, x2, x3);
+        }
+        if (v_tile) {
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(x0), "=r"(x1), "=r"(x2), "=r"(x3)
+                         : "r"(v_s + (uint32_t)rr * 128u));
+            *reinterpret_cast<uint4 *>(v_dst + row) = make_uint4(x0, x1, x2, x3);
+        }
     }
 }
 
@@ -600,7 +637,7 @@ __global__ void __launch_bounds__(128, D == 64 ? 4 : 2)
                 }
             }
             // epilogue staged in the V buffer (free since the last P V)
-            store_rows_staged<D>(t_row + col_o, l, sb + L::kV, a.out, a.hq, h, q0, s1 - q0);
+            store_rows_staged<D>(t_row + col_o, l, sb + L::kV, a.out, a.hq, h, q0, s1 - q0, tid);
             tc::fence_before();
             __syncthreads();  // every TMEM read and staging read is done
             // the V buffer is free again: request the next job's V
@@ -757,6 +794,13 @@ __global__ void __launch_bounds__(128, 2)
     uint32_t ph = 0;  // every barrier completes once per key tile
     const int li = qt * 128 + tid;  // local index of this thread's new row
     float m = -INFINITY, l = 0.f;
+    // page write of the diagonal tile (the last one): with two query heads
+    // per KV head, the even head's CTA writes the K rows and the odd one the
+    // V rows (both hold the same tiles); the page ids are read now, long
+    // before they are needed
+    const bool write_k = a.k_pages && h % GROUP == 0;
+    const bool write_v = a.k_pages && (GROUP == 1 || h % GROUP == 1);
+    const int my_page = (write_k || write_v) ? kv_tile_page_id(a, b, qt * 128, s1 - s0, past, tid) : -1;
 
     for (int u = 0; u < n_tiles; ++u, ph ^= 1) {
         const bool cached = PAST && u < n_ct;
@@ -788,11 +832,6 @@ __global__ void __launch_bounds__(128, 2)
                 tc::fence_proxy_async_smem();
             }
         } else {
-            if (kt == qt && a.k_pages && h % GROUP == 0) {
-                // diagonal tile: its K/V rows are this query tile's own
-                mbar_wait(bar_v, ph, status);
-                write_kv_pages<D>(smem + L::kK, smem + L::kV, a, b, qt * 128, s1 - s0, past, g, status);
-            }
             n_ok = min(128, (s1 - s0) - 128 * kt);
             n_ok = min(n_ok, li - 128 * kt + 1);
             n_ok = max(n_ok, 0);
@@ -806,11 +845,19 @@ __global__ void __launch_bounds__(128, 2)
             issue_pv_tp<D>(tmem, tmem + col_o, sb + L::kV, u > 0);
             tc::mma_commit(bar_o);
         }
+        if (u == n_tiles - 1 && (write_k || write_v)) {
+            // diagonal tile: its K/V rows are this query tile's own; written
+            // while the last P V runs (both only read the tiles)
+            mbar_wait(bar_v, ph, status);
+            write_kv_pages<D>(write_k ? smem + L::kK : nullptr, write_v ? smem + L::kV : nullptr, a, qt * 128,
+                              s1 - s0, past, g, status, tid, my_page);
+        }
         mbar_wait(bar_o, ph, status);
         tc::fence_after();
         if (tid == 0 && u + 1 < n_tiles) load_v(u + 1);
     }
-    store_rows_staged<D>(t_row + col_o, l, sb + L::kV, a.out, a.hq, h, q0, min(128, s1 - q0));
+    // staged in the dead Q buffer (the page write may still read K and V)
+    store_rows_staged<D>(t_row + col_o, l, sb + L::kQ, a.out, a.hq, h, q0, min(128, s1 - q0), tid);
     tc::fence_before();
     __syncthreads();
     if (warp == 0) {

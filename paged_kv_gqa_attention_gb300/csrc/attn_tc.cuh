@@ -77,7 +77,7 @@ struct AttnTcLayout {
     static constexpr uint32_t kPlo = D == 64 ? kQ : kK;
     static constexpr uint32_t kBar = kV + kSub * tc::kSubTileBytes;  // 4 mbarriers
     static constexpr uint32_t kTmemSlot = kBar + 32;
-    static constexpr uint32_t kNext = kTmemSlot + 8;  // next-job records of the persistent kernels
+    static constexpr uint32_t kNext = kTmemSlot + 8;  // next-job records (persistent kernels; the prefill's job)
     static constexpr uint32_t kBytes = kNext + 32;
     static constexpr uint32_t kSmem = kBytes + 1024;  // slack for 1024-byte alignment
 };
@@ -400,7 +400,7 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem, uint32_t o_col, uint32_t
 // row is written by D / 8 adjacent threads (16 bytes each), so one warp store
 // covers whole 256-byte rows; a thread's rows are 8 apart, so its swizzled
 // chunk offset is the same for all of them.  A null k_tile or v_tile skips
-// that pool.
+// that pool; tile rows before row_begin are left to the caller.
 __device__ __forceinline__ int kv_tile_page_id(const AttnTcArgs &a, int seg, int i0, int len, int past, int tix) {
     const int lane = tix & 31;
     const int end = min(min(len, a.max_pages * 16 - past) - i0, 128);
@@ -412,7 +412,7 @@ __device__ __forceinline__ int kv_tile_page_id(const AttnTcArgs &a, int seg, int
 template <int D>
 __device__ __forceinline__ void write_kv_pages(const uint8_t *k_tile, const uint8_t *v_tile, const AttnTcArgs &a,
                                                int i0, int len, int past, int g, unsigned int *status, int tix,
-                                               int my_page) {
+                                               int my_page, int row_begin) {
     constexpr int kPage = 16;
     constexpr int kChunks = D / 8;              // 16-byte chunks per row
     constexpr int kRowsPerPass = 128 / kChunks;
@@ -432,7 +432,7 @@ __device__ __forceinline__ void write_kv_pages(const uint8_t *k_tile, const uint
         const int rr = rr0 + k * kRowsPerPass;
         const int pos = pos0 + rr;
         const int page = __shfl_sync(0xffffffffu, my_page, (pos / kPage - p_first) & 31);
-        if (rr >= end) continue;
+        if (rr < row_begin || rr >= end) continue;
         if (page < 0 || page >= a.num_pages) {
             if (c == 0) atomicOr(status, QA_DEVICE_BAD_PAGE);
             continue;
@@ -652,11 +652,84 @@ __global__ void __launch_bounds__(128, D == 64 ? 4 : 2)
 }
 
 // ---------------------------------------------------------------------------
+// Job order of the causal prefill.  A job (request r, query tile t) costs
+// n_ct(r) + t + 1 key tiles (n_ct: cached key tiles of the chunked form, 0
+// otherwise); request r has jobs at the costs lo_r = n_ct(r) + 1 .. hi_r =
+// n_ct(r) + qtiles(r).  Job index jj counts the jobs in decreasing cost,
+// requests in index order within a cost, so the longest jobs launch first and
+// no CTA of the grid's front is spent on an empty (request, tile) slot.
+// Warp-collective: reads the segment array (and the cached lengths), finds
+// the cost level by a binary search over count(c) = #jobs of cost >= c, and
+// the request inside the level by ballots.  Returns the request (tile in *t)
+// or -1 when jj is past the last job.  Invalid segments or cached lengths
+// count as empty here; the kernel checks its own request again.
+__device__ __forceinline__ int prefill_job(const AttnTcArgs &a, bool past_mode, int jj, int qtiles_grid, int max_len,
+                                           int *t) {
+    const int lane = threadIdx.x & 31;
+    auto range = [&](int r, int &lo, int &hi) {
+        lo = 1;
+        hi = 0;
+        if (r >= a.n_seg) return;
+        const int s0 = a.cu[r], s1 = a.cu[r + 1];
+        const int len = (0 <= s0 && s0 <= s1 && s1 <= a.total) ? s1 - s0 : 0;
+        int pst = past_mode ? a.n_past[r] : 0;
+        if (pst < 0 || pst > max_len) pst = 0;
+        lo = (pst + 127) / 128 + 1;
+        hi = lo - 1 + min((len + 127) / 128, qtiles_grid);
+    };
+    int lo0, hi0;  // the first 32 requests stay in registers
+    range(lane, lo0, hi0);
+    auto count = [&](int c) {  // jobs of cost >= c
+        int n = max(0, hi0 - max(lo0, c) + 1);
+        for (int r0 = 32; r0 < a.n_seg; r0 += 32) {
+            int lo, hi;
+            range(r0 + lane, lo, hi);
+            n += max(0, hi - max(lo, c) + 1);
+        }
+        return __reduce_add_sync(0xffffffffu, n);
+    };
+    int c_max = hi0;
+    for (int r0 = 32; r0 < a.n_seg; r0 += 32) {
+        int lo, hi;
+        range(r0 + lane, lo, hi);
+        c_max = max(c_max, hi);
+    }
+    c_max = __reduce_max_sync(0xffffffffu, c_max);
+    if (c_max < 1 || jj >= count(1)) return -1;
+    int c_lo = 1, c_hi = c_max;  // largest c with count(c) > jj
+    while (c_lo < c_hi) {
+        const int mid = (c_lo + c_hi + 1) >> 1;
+        if (count(mid) > jj) c_lo = mid;
+        else c_hi = mid - 1;
+    }
+    const int c = c_lo;
+    int k = jj - (c < c_max ? count(c + 1) : 0);  // rank inside level c
+    for (int r0 = 0; r0 < a.n_seg; r0 += 32) {
+        int lo = lo0, hi = hi0;
+        if (r0 > 0) range(r0 + lane, lo, hi);
+        const unsigned has = __ballot_sync(0xffffffffu, lo <= c && c <= hi);
+        const int n = __popc(has);
+        if (k < n) {
+            const int bit = __fns(has, 0, k + 1);
+            const int r = r0 + bit;
+            const int lo_r = __shfl_sync(0xffffffffu, lo, bit);
+            *t = c - lo_r;
+            return r;
+        }
+        k -= n;
+    }
+    return -1;
+}
+
 // Causal prefill, head_dim 128: one CTA per job (query tile t, request b,
-// query head h) on the grid (hq, batch, qtiles) with the query tile reversed,
-// so the last query tiles (the most key tiles) launch first and the query
-// heads of a KV head are adjacent (their K/V tiles come from L2 the second
-// time); the hardware scheduler balances the uneven jobs, two CTAs per SM.
+// query head h) on the grid (hq, batch, qtiles), blockIdx.x the head.  The
+// longest jobs launch first: for the plain prefill the query tile is the
+// reversed z index (a job's key tiles grow with it); for the chunked form,
+// whose jobs differ by their cached tiles too, the rest of the block index is
+// the job in prefill_job's order (most key tiles first, empty slots of the
+// grid last).  The query heads of a KV head are adjacent (their K/V tiles
+// come from L2 the second time); the hardware scheduler balances the uneven
+// jobs, two CTAs per SM.
 // The first tiles are requested right after the barriers are set up, before
 // the TMEM allocation.
 //
@@ -736,22 +809,57 @@ __global__ void __launch_bounds__(128, 2)
     const int tid = threadIdx.x, warp = tid >> 5;
 
     const int h = blockIdx.x, g = h / GROUP;
-    const int b = blockIdx.y;
-    const int qt = (int)(gridDim.z - 1 - blockIdx.z);
+    const int max_len = a.max_pages * a.page_size;
+    int b, qt;
+    if (PAST) {
+        // chunked form: jobs differ by their cached tiles too, so the rest
+        // of the block index is the job in prefill_job's order
+        const int jj = (int)(blockIdx.y + gridDim.y * blockIdx.z);
+        volatile int *job = reinterpret_cast<volatile int *>(smem + L::kNext);
+        if (warp == 0) {
+            const int lane = tid & 31;
+            if (jj == 0 && h == 0) {
+                // the first CTA checks every request once: segments, cached
+                // lengths, and requests longer than their page-table row
+                // (clipped: rows past the row's capacity are neither written
+                // nor, beyond the grid, attended)
+                bool bad_seg = a.cu[a.n_seg] != a.total, bad_len = false;
+                for (int r = lane; r < a.n_seg; r += 32) {
+                    const int r0 = a.cu[r], r1 = a.cu[r + 1], pst = a.n_past[r];
+                    bad_seg |= !(0 <= r0 && r0 <= r1 && r1 <= a.total);
+                    bad_len |= pst < 0 || pst > max_len || (a.k_pages && r1 - r0 > max_len - pst);
+                }
+                const bool any_seg = __any_sync(0xffffffffu, bad_seg), any_len = __any_sync(0xffffffffu, bad_len);
+                if (lane == 0 && any_seg) atomicOr(status, QA_DEVICE_BAD_SEGMENTS);
+                if (lane == 0 && any_len) atomicOr(status, QA_DEVICE_BAD_LENGTH);
+            }
+            int t = 0;
+            const int bb = prefill_job(a, true, jj, (int)gridDim.z, max_len, &t);  // gridDim.z: tiles of a row
+            if (lane == 0) {
+                job[0] = bb;
+                job[1] = t;
+            }
+        }
+        __syncthreads();
+        b = job[0];
+        qt = job[1];
+        if (b < 0 || a.cu[a.n_seg] != a.total) return;
+    } else {
+        // the query tile reversed: the last query tiles (the most key tiles)
+        // launch first
+        b = blockIdx.y;
+        qt = (int)(gridDim.z - 1 - blockIdx.z);
+    }
     const int s0 = a.cu[b], s1 = a.cu[b + 1];
     if (!(0 <= s0 && s0 <= s1 && s1 <= a.total) || a.cu[a.n_seg] != a.total) {
-        if (tid == 0) atomicOr(status, QA_DEVICE_BAD_SEGMENTS);
+        if (!PAST && tid == 0) atomicOr(status, QA_DEVICE_BAD_SEGMENTS);
         return;
     }
     const int past = PAST ? a.n_past[b] : 0;
-    const int max_len = a.max_pages * a.page_size;
-    if (PAST && (past < 0 || past > max_len)) {
-        if (tid == 0 && qt == 0 && h == 0) atomicOr(status, QA_DEVICE_BAD_LENGTH);
-        return;
-    }
+    if (PAST && (past < 0 || past > max_len)) return;
     // a request longer than its page-table row: flagged once; its rows past
     // the row's capacity are neither written nor (beyond the grid) attended
-    if (a.k_pages && qt == 0 && h == 0 && tid == 0 && s1 - s0 > max_len - past)
+    if (!PAST && a.k_pages && qt == 0 && h == 0 && tid == 0 && s1 - s0 > max_len)
         atomicOr(status, QA_DEVICE_BAD_LENGTH);
     if (qt * 128 >= s1 - s0) return;
     const int q0 = s0 + qt * 128;
@@ -847,10 +955,35 @@ __global__ void __launch_bounds__(128, 2)
         }
         if (u == n_tiles - 1 && (write_k || write_v)) {
             // diagonal tile: its K/V rows are this query tile's own; written
-            // while the last P V runs (both only read the tiles)
+            // while the last P V runs (both only read the tiles).  Whole
+            // pages (the tile's rows start a page when past is a multiple of
+            // 16) go out as 16-row TMA stores through the pool maps, one per
+            // page and 64-dim sub-tile, issued by lane j of warp 0 for the
+            // j-th page; the rows of a partial last page, or every row when
+            // the tile does not start a page, with plain stores.
             mbar_wait(bar_v, ph, status);
-            write_kv_pages<D>(write_k ? smem + L::kK : nullptr, write_v ? smem + L::kV : nullptr, a, qt * 128,
-                              s1 - s0, past, g, status, tid, my_page);
+            const int end = min(min(s1 - s0, max_len - past) - qt * 128, 128);
+            const int tma_rows = (past % 16 == 0 && end > 0) ? end / 16 * 16 : 0;
+            if (warp == 0 && (tid & 31) < tma_rows / 16) {
+                if (my_page < 0 || my_page >= a.num_pages) {
+                    atomicOr(status, QA_DEVICE_BAD_PAGE);
+                } else {
+                    const uint32_t row_off = (uint32_t)(tid & 31) * 16u * 128u;
+#pragma unroll
+                    for (int sd = 0; sd < L::kSub; ++sd) {
+                        if (write_k)
+                            tc::tma_store_3d(&tm_kp, sb + L::kK + sd * tc::kSubTileBytes + row_off, sd * 64, g,
+                                             my_page * 16);
+                        if (write_v)
+                            tc::tma_store_3d(&tm_vp, sb + L::kV + sd * tc::kSubTileBytes + row_off, sd * 64, g,
+                                             my_page * 16);
+                    }
+                    tc::bulk_commit_group();
+                }
+            }
+            if (tma_rows < end)
+                write_kv_pages<D>(write_k ? smem + L::kK : nullptr, write_v ? smem + L::kV : nullptr, a, qt * 128,
+                                  s1 - s0, past, g, status, tid, my_page, tma_rows);
         }
         mbar_wait(bar_o, ph, status);
         tc::fence_after();
@@ -858,6 +991,7 @@ __global__ void __launch_bounds__(128, 2)
     }
     // staged in the dead Q buffer (the page write may still read K and V)
     store_rows_staged<D>(t_row + col_o, l, sb + L::kQ, a.out, a.hq, h, q0, min(128, s1 - q0), tid);
+    if (warp == 0) tc::bulk_wait_group_read_all();  // the TMA page stores have read K and V
     tc::fence_before();
     __syncthreads();
     if (warp == 0) {

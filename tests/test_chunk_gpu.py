@@ -52,6 +52,15 @@ def test_small_chunks(past, new):
     check(_workload(600 + sum(past) + sum(new), past, new), f"past {past} new {new}")
 
 
+def test_many_requests_mixed_costs():
+    # more than 32 requests (the job order reads the lengths 32 at a time),
+    # costs from 1 to 6 key tiles, empty requests and empty histories mixed
+    rng = np.random.default_rng(615)
+    past = tuple(int(x) for x in rng.choice([0, 3, 16, 130, 257, 400], size=45))
+    new = tuple(int(x) for x in rng.choice([0, 1, 17, 128, 129, 200], size=45))
+    check(_workload(615, past, new), "45 requests")
+
+
 def test_split_prompt_equals_one_shot_on_the_gpu():
     # the first 200 rows by qa_prefill_attn, the remaining 157 by the chunked call
     L, split = 357, 200

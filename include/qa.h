@@ -103,7 +103,7 @@ typedef struct qa_attn_params {
     void *workspace;       /* decode scratch (device), caller-owned              */
     size_t workspace_bytes;
     int debug_checks;      /* 1 => synchronise and report device-side errors     */
-    int stable_metadata;   /* ABI 2: 1 => see below; ignored when abi_version < 2 */
+    int stable_metadata;   /* ABI 2: 0, 1 or 2 (below); ignored if abi_version < 2 */
 } qa_attn_params;
 
 /* stable_metadata (decode calls: qa_decode_attn, qa_decode_attn_noalloc,
@@ -119,8 +119,13 @@ typedef struct qa_attn_params {
  * by at least one other kernel, before its first layer meets this.  The
  * kernel then reads them, computes its work split and fetches its first page
  * ids before that kernel has finished, and waits only before it reads q, the
- * pools or the workspace or writes any output.  With 0 (the default) it waits
- * before reading anything. */
+ * pools or the workspace or writes any output.  With 2 the caller promises the
+ * same of k_pages and v_pages, and the kernel also streams its first pages
+ * into shared memory before that wait.  Back-to-back layers of a decode step
+ * (each reads its own layer's pools) and qa_decode_step (it writes the new
+ * row itself) meet this; a decode after a qa_decode_append into the same
+ * pools does not.  With 0 (the default) it waits before reading anything.
+ * Other values are rejected. */
 
 /* Defaults: abi_version = QA_ABI_VERSION, 16/8/128 heads, page_size 16,
  * scale 0 (1/sqrt(head_dim)), stream NULL, no workspace, debug_checks 0,

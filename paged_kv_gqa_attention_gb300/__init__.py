@@ -160,7 +160,7 @@ def _params(*, n_q_heads, n_kv_heads, head_dim, page_size=16, num_pages=0, max_p
         p.workspace = _dev(workspace, "workspace")
         p.workspace_bytes = workspace.numel() * workspace.element_size()
     p.debug_checks = 1 if debug_checks else 0
-    p.stable_metadata = 1 if stable_metadata else 0
+    p.stable_metadata = int(stable_metadata)  # False/True/2 -> 0/1/2
     return p
 
 
@@ -184,8 +184,9 @@ def qa_decode_attn(q, k_pages, v_pages, page_table, seq_lens, out=None, *, works
     qa_decode_workspace_size(B, ...) bytes (allocated here if omitted); the
     call leaves its arrival counters at zero, so it can be reused across
     calls without clearing.
-    stable_metadata=True: the caller promises that page_table and seq_lens
-    are not written by the kernel just before this call on the stream (see
+    stable_metadata=True (1): the caller promises that page_table and
+    seq_lens are not written by the kernel just before this call on the
+    stream; 2: the same of the pools as well (see
     qa_attn_params::stable_metadata in qa.h)."""
     torch = _torch()
     B, Hq, D = q.shape

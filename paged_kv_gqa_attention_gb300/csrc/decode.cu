@@ -67,8 +67,8 @@ struct DecodeArgs {
     int batch, hkv, max_pages, num_pages;
     float scale_log2;  // scale * log2(e)
     // lengths and page table may be read before the preceding kernel ends
-    // (qa_attn_params::stable_metadata)
-    int early;
+    // (qa_attn_params::stable_metadata >= 1), and the pools too (>= 2)
+    int early, early_pools;
     // fused decode step only: q is the pre-norm projection; the new token's
     // pre-norm k and its v are appended at position seq_lens[b] - 1
     const uint16_t *k_new, *v_new;  // [B][Hkv][D]
@@ -256,22 +256,33 @@ __global__ void __launch_bounds__((kMaxHkv + 1) * 32, 1) decode_splitk_kernel(co
         const int j0 = max(lo, p0) - p0, j1 = min(hi, prefix[b_last + 1]) - p0;
         first_ids = j0 + lane < j1 ? a.page_table[(size_t)b_last * a.max_pages + j0 + lane] : -1;
     }
-    if (a.early) {
+    // With the pools vouched for too (a.early_pools) the producer warp starts
+    // streaming its first kStages pages before it waits (below).
+    const bool producer_first = a.early_pools && warp == n_consumers;
+    if (a.early && !producer_first) {
         asm volatile("griddepcontrol.wait;" ::: "memory");
         asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     }
 
-    // CTA 0 writes the zero rows of requests with nothing to attend over.
+    // CTA 0 writes the zero rows of requests with nothing to attend over
+    // (threads that have waited only).
     if (blockIdx.x == 0) {
         const int chunks = hq * kD * 2 / 16;  // 16-byte chunks per request
-        for (int b = 0; b < a.batch; ++b) {
+        const int n_thr = producer_first ? n_consumers * 32 : (int)blockDim.x;
+        for (int b = 0; b < a.batch && (int)threadIdx.x < n_thr; ++b) {
             if (prefix[b + 1] != prefix[b]) continue;
             uint4 *dst = reinterpret_cast<uint4 *>(a.out + (size_t)b * hq * kD);
-            for (int c = threadIdx.x; c < chunks; c += blockDim.x) dst[c] = make_uint4(0u, 0u, 0u, 0u);
+            for (int c = threadIdx.x; c < chunks; c += n_thr) dst[c] = make_uint4(0u, 0u, 0u, 0u);
         }
     }
 
-    if (total == 0 || lo >= hi) return;
+    if (total == 0 || lo >= hi) {
+        if (producer_first) {
+            asm volatile("griddepcontrol.wait;" ::: "memory");
+            asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+        }
+        return;
+    }
 
     // Warm L2 with the per-request rows read at the start of every later
     // segment (q; for the fused step the new token's k and v too), so those
@@ -296,6 +307,7 @@ __global__ void __launch_bounds__((kMaxHkv + 1) * 32, 1) decode_splitk_kernel(co
         // ---------------- producer warp: lanes fetch page ids, lane 0 issues copies
         const uint64_t policy = policy_evict_first();
         int it = 0;
+        bool waited = !producer_first;
         for (int k = 0; k < n_visit; ++k) {
             const int b = k == 0 ? b_last : b0 + k - 1;
             const int p0 = prefix[b], p1 = prefix[b + 1];
@@ -307,6 +319,11 @@ __global__ void __launch_bounds__((kMaxHkv + 1) * 32, 1) decode_splitk_kernel(co
                 const int cnt = min(32, j1 - jb);
                 for (int u = 0; u < cnt; ++u, ++it) {
                     const int page = __shfl_sync(0xffffffffu, mine, u);
+                    if (!waited && it == kStages) {  // the ring is full: wait now (warp-uniform)
+                        asm volatile("griddepcontrol.wait;" ::: "memory");
+                        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+                        waited = true;
+                    }
                     if (lane == 0) {
                         const int s = it % kStages;
                         if (it >= kStages) mbar_wait(bar_empty + 8 * s, ((it / kStages) & 1) ^ 1, &g_status);
@@ -329,6 +346,10 @@ __global__ void __launch_bounds__((kMaxHkv + 1) * 32, 1) decode_splitk_kernel(co
                     __syncwarp();
                 }
             }
+        }
+        if (!waited) {  // fewer than kStages pages
+            asm volatile("griddepcontrol.wait;" ::: "memory");
+            asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
         }
         return;
     }
@@ -646,7 +667,8 @@ cudaError_t launch_decode(const void *q, const void *k_pages, const void *v_page
     a.max_pages = p.max_pages_per_seq;
     a.num_pages = p.num_pages;
     a.scale_log2 = scale * kLog2e;
-    a.early = (p.abi_version >= 2 && p.stable_metadata) ? 1 : 0;
+    a.early = (p.abi_version >= 2 && p.stable_metadata >= 1) ? 1 : 0;
+    a.early_pools = (p.abi_version >= 2 && p.stable_metadata >= 2) ? 1 : 0;
     a.k_new = a.v_new = nullptr;
     a.q_gain = a.k_gain = nullptr;
     a.k_pages_w = a.v_pages_w = nullptr;

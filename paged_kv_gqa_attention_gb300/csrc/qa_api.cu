@@ -41,6 +41,8 @@ qa_status check_common(const qa_attn_params *p, const char *fn) {
                     QA_ABI_MIN_VERSION, QA_ABI_VERSION);
     if (!(p->scale >= 0.f) || !isfinite(p->scale))
         return fail(QA_STATUS_INVALID_PARAMS, "%s: scale must be finite and >= 0 (0 = 1/sqrt(head_dim))", fn);
+    if (p->abi_version >= 2 && (p->stable_metadata < 0 || p->stable_metadata > 2))
+        return fail(QA_STATUS_INVALID_PARAMS, "%s: stable_metadata %d outside [0, 2]", fn, p->stable_metadata);
     return QA_STATUS_OK;
 }
 

@@ -204,3 +204,16 @@ def test_window_plan_capacity_error(libqa):
     cu = np.zeros(2, np.int32)
     n = qa._lib.qa_window_plan(counts.ctypes.data_as(ctypes.c_void_p), 1, 0, cu.ctypes.data_as(ctypes.c_void_p), 2)
     assert n == -1 and "capacity" in qa.qa_last_error()
+
+
+def test_stable_metadata_levels_are_checked(libqa):
+    import paged_kv_gqa_attention_gb300 as qa
+
+    p = qa.qa_attn_default_params()
+    fake = ctypes.c_void_p(0x1000)
+    p.stable_metadata = 3
+    assert qa._lib.qa_decode_attn(fake, fake, fake, fake, fake, 1, fake, ctypes.byref(p)) == -1
+    assert "stable_metadata" in qa.qa_last_error()
+    p.abi_version = 1  # ABI 1 callers have no such field: the value is ignored
+    assert "stable_metadata" not in (qa._lib.qa_decode_attn(fake, fake, fake, fake, fake, 1, fake, ctypes.byref(p)),
+                                     qa.qa_last_error())[1]

@@ -1,10 +1,11 @@
 """GPU parity of the decode calls with qa_attn_params.stable_metadata = 1
 (the kernel reads lengths and page table before the preceding kernel on the
-stream has finished, everything else after) against the fp64 oracle, in the
-orders a decode step launches them: after the append that writes q, after a
-plain kernel that writes q, as the layers of one captured graph; and a
-caller of ABI 1, whose struct has no such field, is not affected by the
-byte it leaves there.
+stream has finished, everything else after) and 2 (it also streams its first
+pool pages before) against the fp64 oracle, in the orders a decode step
+launches them: after the append that writes q (level 1: the append writes
+the pools), after a plain kernel that writes q, layers queued back to back
+on one stream, the layers of one captured graph; and a caller of ABI 1,
+whose struct has no such field, is not affected by the byte it leaves there.
 """
 import ctypes
 
@@ -48,7 +49,34 @@ def test_after_the_append_that_writes_q():
     assert qa.qa_device_status() == 0
 
 
-def test_fused_step_after_a_kernel_that_writes_q():
+@pytest.mark.parametrize("level", [1, 2])
+def test_back_to_back_layers_on_one_stream(level):
+    # three layers' calls queued without a host sync: each may start while
+    # the one before it is finishing (level 2: streaming its pools early)
+    base = wl.decode_0p6b()
+    layers = [_layer(base, i) for i in range(3)]
+    refs = [oracle.decode(c["q"], c["k_pages"], c["v_pages"], c["page_table"], c["seq_lens"]) for c in layers]
+    pt, sl = to_dev(base["page_table"]), to_dev(base["seq_lens"])
+    dev = [{k: to_dev(c[k]) for k in ("q", "k_pages", "v_pages")} for c in layers]
+    B = len(base["seq_lens"])
+    ws = torch.zeros(qa.qa_decode_workspace_size(B, 2000, num_pages=dev[0]["k_pages"].shape[0],
+                                                 max_pages_per_seq=pt.shape[1]), dtype=torch.uint8, device="cuda")
+    outs = [torch.empty_like(d["q"]) for d in dev]
+    s = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        for rep in range(3):
+            for d, o in zip(dev, outs):
+                qa.qa_decode_attn(d["q"], d["k_pages"], d["v_pages"], pt, sl, o, workspace=ws, stream=s,
+                                  stable_metadata=level)
+    torch.cuda.synchronize()
+    for i, (o, r) in enumerate(zip(outs, refs)):
+        assert_close(f64(o), r, f"level {level} layer {i}")
+    assert qa.qa_device_status() == 0
+
+
+@pytest.mark.parametrize("level", [1, 2])
+def test_fused_step_after_a_kernel_that_writes_q(level):
     w = wl.with_append(wl.decode_0p6b(), 4)
     ref = _oracle_step(w)
     d = {k: to_dev(w[k]) for k in KEYS}
@@ -60,7 +88,7 @@ def test_fused_step_after_a_kernel_that_writes_q():
         d["q_new"].copy_(src)  # the q projection's stand-in, just before the step
         out = qa.qa_decode_step(d["q_new"], d["k_new"], d["v_new"], d["q_gain"], d["k_gain"], d["page_table"],
                                 d["seq_lens"], d["k_pages"], d["v_pages"], rms_eps=EPS, rope_theta=THETA, stream=s,
-                                stable_metadata=True)
+                                stable_metadata=level)
     torch.cuda.synchronize()
     assert_close(f64(out), ref, "fused step, stable metadata")
     assert qa.qa_device_status() == 0
@@ -89,7 +117,7 @@ def test_graph_of_layers_follows_refills():
     ws = torch.zeros(qa.qa_decode_workspace_size(B, 2000, num_pages=kp[0].shape[0],
                                                  max_pages_per_seq=pt.shape[1]), dtype=torch.uint8, device="cuda")
     srcs = [q.clone() for q in qs]
-    g = qa.qa_decode_graph_create(qs, kp, vp, pt, sl, outs, workspace=ws, stable_metadata=True)
+    g = qa.qa_decode_graph_create(qs, kp, vp, pt, sl, outs, workspace=ws, stable_metadata=2)
     try:
         for rep in range(2):
             for q in qs:

@@ -521,6 +521,11 @@ __global__ void __launch_bounds__(128, D == 64 ? 4 : 2)
     const int tid = threadIdx.x, warp = tid >> 5;
     const int G = gridDim.x;
     const int n_jobs = a.n_seg * a.hq;
+    // launched as a programmatic dependent: wait for the kernel before it
+    // (and its writes) before reading anything, then let the next one be
+    // scheduled as this grid's CTAs retire
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (a.cu[a.n_seg] != a.total) {
         if (blockIdx.x == 0 && tid == 0) atomicOr(status, QA_DEVICE_BAD_SEGMENTS);
@@ -807,6 +812,11 @@ __global__ void __launch_bounds__(128, 2)
     const uint32_t sb = (raw + 1023u) & ~1023u;
     uint8_t *smem = smem_raw + (sb - raw);
     const int tid = threadIdx.x, warp = tid >> 5;
+    // launched as a programmatic dependent: wait for the kernel before it
+    // (and its writes) before reading anything; the next kernel is scheduled
+    // once every CTA of this grid has started (the last wave is resident)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     const int h = blockIdx.x, g = h / GROUP;
     const int max_len = a.max_pages * a.page_size;

@@ -76,8 +76,20 @@ cudaError_t launch_prefill(const void *q, const void *k, const void *v, const in
         err = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                                    (int)cudaSharedmemCarveoutMaxShared);
         if (err != cudaSuccess) return err;
-        kernel<<<grid, 128, smem, stream>>>(tq, tk, tv, tkp, tvp, a, status);
-        return cudaSuccess;
+        // a programmatic dependent of the kernel before it on the stream:
+        // its CTAs are scheduled as that kernel's last CTAs retire, and wait
+        // for it (griddepcontrol.wait) before they read anything
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = grid;
+        cfg.blockDim = dim3(128);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, kernel, tq, tk, tv, tkp, tvp, a, status);
     };
     const bool group2 = p.n_q_heads == 2 * p.n_kv_heads;
     if (n_past)

@@ -62,8 +62,19 @@ cudaError_t launch_window(const void *q, const void *k, const void *v, const int
                                    (int)cudaSharedmemCarveoutMaxShared);
         if (err != cudaSuccess) return err;
         const long long ctas = std::min<long long>(n_jobs, (long long)sms * per_sm);
-        kernel<<<(unsigned)ctas, 128, smem, stream>>>(tq, tk, tv, a, status);
-        return cudaSuccess;
+        // a programmatic dependent of the kernel before it on the stream (it
+        // waits for that kernel before it reads anything)
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)ctas);
+        cfg.blockDim = dim3(128);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, kernel, tq, tk, tv, a, status);
     };
     if (p.head_dim == 64)
         e = launch(window_tc_kernel<64>, AttnTcLayout<64>::kSmem, 4);

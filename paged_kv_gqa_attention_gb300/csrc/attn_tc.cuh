@@ -83,19 +83,17 @@ struct AttnTcLayout {
 };
 
 // Online softmax of one 128-key tile for this thread's query row, whose
-// scores sit in TMEM columns [0, 128) of s_row.  Keys [0, n_ok) of the tile
-// are visible.  Writes P as P_hi (bf16, two keys per column) and P_lo:
-//   P_TMEM = false: P_hi over the scores in columns [0, 64), P_lo as a
-//                   128B-swizzled K-major row at plo_row (shared memory);
-//   P_TMEM = true:  both in TMEM over the chunk of scores they replace: keys
-//                   [32c, 32c + 32) give P_hi in columns [32c, 32c + 16) and
-//                   P_lo in [32c + 16, 32c + 32) (plo_row and sw unused).
-// Updates the running (m, l) and, when `rescale` and m moved, multiplies the
-// row of O at o_row by 2^(m_old - m_new).  Warp-collective (every lane of the warp calls it).
+// scores sit in TMEM columns [0, 128) of s_row (window kernel).  Keys
+// [0, n_ok) of the tile are visible.  Writes P as P_hi (bf16, two keys per
+// column) over the scores in columns [0, 64) and P_lo as a 128B-swizzled
+// K-major row at plo_row (shared memory).  Two passes over the scores (max,
+// then exponentials), each reading them from TMEM.  Updates the running
+// (m, l) and, when `rescale` and m moved, multiplies the row of O at o_row
+// by 2^(m_old - m_new).  Warp-collective (every lane of the warp calls it).
 // Slack of the lazy reference max, in log2 units: probabilities stay <= 2^8.
 constexpr float kRescaleSlack = 8.f;
 
-template <int D, bool P_TMEM = false>
+template <int D>
 __device__ __forceinline__ void softmax_tile(uint32_t s_row, int n_ok, float scale_log2, uint32_t plo_row,
                                              uint32_t sw, uint32_t o_row, bool rescale, float &m, float &l) {
     const int warp_max = __reduce_max_sync(0xffffffffu, n_ok);
@@ -181,20 +179,14 @@ __device__ __forceinline__ void softmax_tile(uint32_t s_row, int n_ok, float sca
             }
             if (c + 1 < n_chunks) tc::tmem_ld32_wait(nxt);
         }
-        if (P_TMEM) {
-            // chunk c's own 32 columns (its scores are in registers already)
-            tc::tmem_st16(s_row + c * 32, pk);
-            tc::tmem_st16(s_row + c * 32 + 16, pl);
-        } else {
-            // P_hi: 32 keys = 16 TMEM columns [16c, 16c + 16) (scores there are consumed)
-            tc::tmem_st16(s_row + c * 16, pk);
-            // P_lo: 4 chunks of 16 bytes, sub-tile c / 2, chunks (c % 2) * 4 + u
+        // P_hi: 32 keys = 16 TMEM columns [16c, 16c + 16) (scores there are consumed)
+        tc::tmem_st16(s_row + c * 16, pk);
+        // P_lo: 4 chunks of 16 bytes, sub-tile c / 2, chunks (c % 2) * 4 + u
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const uint32_t chunk = (uint32_t)((c & 1) * 4 + u);
-                const uint32_t off = (uint32_t)(c >> 1) * tc::kSubTileBytes + ((chunk ^ sw) << 4);
-                tc::st_shared_v4(plo_row + off, pl[4 * u], pl[4 * u + 1], pl[4 * u + 2], pl[4 * u + 3]);
-            }
+        for (int u = 0; u < 4; ++u) {
+            const uint32_t chunk = (uint32_t)((c & 1) * 4 + u);
+            const uint32_t off = (uint32_t)(c >> 1) * tc::kSubTileBytes + ((chunk ^ sw) << 4);
+            tc::st_shared_v4(plo_row + off, pl[4 * u], pl[4 * u + 1], pl[4 * u + 2], pl[4 * u + 3]);
         }
     }
     tc::tmem_wait_st();
@@ -214,11 +206,12 @@ __device__ __forceinline__ void softmax_tile(uint32_t s_row, int n_ok, float sca
     }
 }
 
-// Single-pass form of softmax_tile<D, true> for kernels whose register
-// budget holds a whole score row (two 128-thread CTAs per SM): the live
-// 32-column chunks of the row are read from TMEM with one wait, the max and
-// the exponentials work on the registers, and P_hi / P_lo go back over the
-// scores in the softmax_tile<D, true> layout.  The scores are read once
+// Single-pass softmax with both P terms in TMEM (prefill), for kernels whose
+// register budget holds a whole score row (two 128-thread CTAs per SM): the
+// live 32-column chunks of the row are read from TMEM with one wait, the max
+// and the exponentials work on the registers, and both P terms go back over
+// the scores they replace: keys [32c, 32c + 32) give P_hi in columns
+// [32c, 32c + 16) and P_lo in [32c + 16, 32c + 32).  The scores are read once
 // instead of twice.  Same (m, l) update, lazy reference max and rescale as
 // softmax_tile.  Warp-collective.
 template <int D>
@@ -455,7 +448,7 @@ __device__ __forceinline__ void write_kv_pages(const uint8_t *k_tile, const uint
 }
 
 // O += P_hi V + P_lo V with both P terms in TMEM in the chunk layout of
-// softmax_tile<D, true>: keys [16kk, 16kk + 16) are P_hi columns
+// softmax_tile_regs: keys [16kk, 16kk + 16) are P_hi columns
 // 32 (kk / 2) + 8 (kk % 2) + [0, 8) and P_lo columns 16 further.  N = 64
 // dims per MMA, V read MN-major.  One thread.
 template <int D>
@@ -750,15 +743,16 @@ __device__ __forceinline__ int prefill_job(const AttnTcArgs &a, bool past_mode, 
 // Per key tile:
 //   - S = Q K^T (Q loaded with the first key tile and kept);
 //   - as soon as S has read K, the next key tile's K is requested;
-//   - diagonal tile (new tile t), first query head of each KV head: the K and
-//     V rows of the tile go to their KV-cache pages (write_kv_pages) at
-//     positions n_past + row;
 //   - softmax with P_hi and P_lo both in TMEM over the scores
-//     (softmax_tile<128, true>), so no shared memory is written and K stays
-//     free for its prefetch;
+//     (softmax_tile_regs), so no shared memory is written and K stays free
+//     for its prefetch;
 //   - O += P V with both P terms read from TMEM (issue_pv_tp); when it is
 //     done the next key tile's V is requested.
-// The epilogue stages O in the V buffer (store_rows_staged).  TMEM: S/P in
+// While the last P V runs, the diagonal tile's (new tile t's) K and V rows go
+// to their KV-cache pages at positions n_past + row: the even query head's
+// job writes the K rows, the odd one's the V rows (one query head per KV
+// head: both), whole pages by TMA stores, the rest by write_kv_pages.  The
+// epilogue stages O in the dead Q buffer (store_rows_staged).  TMEM: S/P in
 // columns [0, 128), O in [128, 256).
 // Cached key tile u of a chunked request (positions [128u, 128u + 128)):
 // the K or V rows of pages 8u .. 8u + 7 that hold positions < past, one

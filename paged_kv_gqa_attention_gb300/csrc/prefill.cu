@@ -3,10 +3,11 @@
 // Page write (qwenasr.cpp ARCHITECTURE.md, "Qwen3 Thinker decoder": prefill
 // rewinds the cache and writes the fresh K/V of the whole prompt span at
 // [n_past, n_past + T) with n_past = 0): row i of request r is copied bit for
-// bit to slot i % 16 of page page_table[r][i / 16], for K and V.  The job of
-// query tile t and the first query head of each KV head writes the rows of
-// tile t from its diagonal K/V tile, already in shared memory for the
-// attention, so the prompt's K and V are read from HBM once for both.
+// bit to slot i % 16 of page page_table[r][i / 16], for K and V.  The jobs of
+// query tile t for the two query heads of a KV head write the rows of tile t
+// from their diagonal K/V tile, already in shared memory for the attention
+// (the even head the K rows, the odd one the V rows; whole pages by TMA
+// stores), so the prompt's K and V are read from HBM once for both.
 //
 // Attention: row i of request r attends over rows j <= i of the same request
 // (same section: attend over [0, n_past + T)), GQA group h / 2, from the

@@ -83,14 +83,14 @@ struct DecodeArgs {
 // (qwenasr.cpp ARCHITECTURE.md, "Qwen3 Thinker decoder": RMSNorm over
 // head_dim with a [head_dim] gain, then rotate-half RoPE).  Lane l holds dims
 // [4l, 4l + 4) in x01/x23; dim d pairs with d +- 64, which lives on lane
-// l ^ 16.  cs/sn: cos/sin of the angles of the lane's four pairs.  Returns
+// l ^ 16.  gn: the gain of the lane's four dims; cs/sn: cos/sin of the
+// angles of the lane's four pairs.  Returns
 // the rotated dims rounded to bf16 (the operator boundary), as two packed
 // words.  Warp-collective.
-__device__ __forceinline__ uint2 norm_rope4(float2 x01, float2 x23, const float *gain, float eps, const float *cs,
+__device__ __forceinline__ uint2 norm_rope4(float2 x01, float2 x23, float4 gn, float eps, const float *cs,
                                             const float *sn, int lane) {
     const float ss = warp_sum(x01.x * x01.x + x01.y * x01.y + x23.x * x23.x + x23.y * x23.y);
     const float r = 1.0f / sqrtf(ss * (1.0f / kD) + eps);
-    const float4 gn = *reinterpret_cast<const float4 *>(gain + 4 * lane);
     const float y[4] = {x01.x * r * gn.x, x01.y * r * gn.y, x23.x * r * gn.z, x23.y * r * gn.w};
     float z[4];
 #pragma unroll
@@ -256,6 +256,12 @@ __global__ void __launch_bounds__((kMaxHkv + 1) * 32, 1) decode_splitk_kernel(co
         const int j0 = max(lo, p0) - p0, j1 = min(hi, prefix[b_last + 1]) - p0;
         first_ids = j0 + lane < j1 ? a.page_table[(size_t)b_last * a.max_pages + j0 + lane] : -1;
     }
+    // Fused step: the rotation angles of the first request visited (they
+    // depend on its length only) are computed before the wait when lengths
+    // may be read early.
+    float cs_first[4], sn_first[4];
+    const bool angles_first = APPEND && a.early && warp < n_consumers && n_visit > 0;
+    if (angles_first) rope_angles(a, a.seq_lens[b_last] - 1, lane, cs_first, sn_first);
     // With the pools vouched for too (a.early_pools) the producer warp starts
     // streaming its first kStages pages before it waits (below).
     const bool producer_first = a.early_pools && warp == n_consumers;
@@ -376,26 +382,46 @@ __global__ void __launch_bounds__((kMaxHkv + 1) * 32, 1) decode_splitk_kernel(co
         // fused step: the new token's K/V rows for KV head g (rotated k,
         // bf16) when this segment holds the request's last page
         const bool has_new = APPEND && j1 == p1 - p0;
+        // every load of the segment's prologue is issued before any is used
+        uint2 qw[GROUP];
+#pragma unroll
+        for (int i = 0; i < GROUP; ++i)
+            qw[i] = *reinterpret_cast<const uint2 *>(a.q + ((size_t)b * hq + g * GROUP + i) * kD + 4 * lane);
         uint2 k_new_w = make_uint2(0u, 0u), v_new_w = make_uint2(0u, 0u);
-        float cs[4], sn[4];
+        float4 gain_q = make_float4(0.f, 0.f, 0.f, 0.f), gain_k = gain_q;
         if (APPEND) {
-            rope_angles(a, seq_len - 1, lane, cs, sn);
+            gain_q = *reinterpret_cast<const float4 *>(a.q_gain + 4 * lane);
             if (has_new) {
                 const size_t o = ((size_t)b * a.hkv + g) * kD + 4 * lane;
-                float2 k01, k23;
-                bf16x4(*reinterpret_cast<const uint2 *>(a.k_new + o), k01, k23);
-                k_new_w = norm_rope4(k01, k23, a.k_gain, a.eps, cs, sn, lane);
+                k_new_w = *reinterpret_cast<const uint2 *>(a.k_new + o);
                 v_new_w = *reinterpret_cast<const uint2 *>(a.v_new + o);
+                gain_k = *reinterpret_cast<const float4 *>(a.k_gain + 4 * lane);
+            }
+        }
+        float cs[4], sn[4];
+        if (APPEND) {
+            if (k == 0 && angles_first) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    cs[c] = cs_first[c];
+                    sn[c] = sn_first[c];
+                }
+            } else {
+                rope_angles(a, seq_len - 1, lane, cs, sn);
+            }
+            if (has_new) {
+                float2 k01, k23;
+                bf16x4(k_new_w, k01, k23);
+                k_new_w = norm_rope4(k01, k23, gain_k, a.eps, cs, sn, lane);
             }
         }
 #pragma unroll
         for (int i = 0; i < GROUP; ++i) {
-            uint2 w = *reinterpret_cast<const uint2 *>(
-                a.q + ((size_t)b * hq + g * GROUP + i) * kD + 4 * lane);
+            uint2 w = qw[i];
             if (APPEND) {
                 float2 x01, x23;
                 bf16x4(w, x01, x23);
-                w = norm_rope4(x01, x23, a.q_gain, a.eps, cs, sn, lane);
+                w = norm_rope4(x01, x23, gain_q, a.eps, cs, sn, lane);
             }
             bf16x4(w, q01[i], q23[i]);
             q01[i].x *= a.scale_log2;

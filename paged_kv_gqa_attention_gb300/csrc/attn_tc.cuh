@@ -587,7 +587,6 @@ __global__ void __launch_bounds__(128, D == 64 ? 4 : 2)
 
         for (int qt = 0; qt < n_tiles; ++qt) {
             const int q0 = s0 + qt * 128;
-            const int qi = q0 + r;
             float m = -INFINITY, l = 0.f;
             for (int kt = 0; kt < n_tiles; ++kt) {
                 const int k0 = s0 + kt * 128;

@@ -600,55 +600,68 @@ __global__ void __launch_bounds__((kMaxHkv + 1) * 32, 1) decode_splitk_kernel(co
             if (lane == 0) prev = atom_add_acq_rel_gpu(a.arrivals + (size_t)b * kMaxHkv + g, 1);
             prev = __shfl_sync(0xffffffffu, prev, 0);
             if (prev == c_hi - c_lo) {
+                // online merge over batches of up to 8 partials per query
+                // head, the loads of both heads of the group all in flight
+                // together (one L2 round trip per batch; requests of this
+                // workload span a few CTAs)
+                constexpr int kBatch = 8;
+                float mm[GROUP], ls[GROUP], o[GROUP][4];
 #pragma unroll
                 for (int i = 0; i < GROUP; ++i) {
-                    const int h = g * GROUP + i;
-                    // online merge over batches of up to 8 partials whose
-                    // loads are all in flight together (one L2 round trip per
-                    // batch; requests of this workload span a few CTAs)
-                    constexpr int kBatch = 8;
-                    float mm = -INFINITY, ls = 0.f, o[4] = {0.f, 0.f, 0.f, 0.f};
-                    for (int c0 = c_lo; c0 <= c_hi; c0 += kBatch) {
-                        float mc[kBatch], lc[kBatch];
-                        float4 pv[kBatch];
+                    mm[i] = -INFINITY;
+                    ls[i] = 0.f;
+                    o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+                }
+                for (int c0 = c_lo; c0 <= c_hi; c0 += kBatch) {
+                    float mc[GROUP][kBatch], lc[GROUP][kBatch];
+                    float4 pv[GROUP][kBatch];
+#pragma unroll
+                    for (int i = 0; i < GROUP; ++i) {
 #pragma unroll
                         for (int u = 0; u < kBatch; ++u) {
                             if (c0 + u <= c_hi) {
-                                const size_t r = (size_t)(c0 + u + b) * hq + h;
-                                mc[u] = __ldcg(a.part_ml + r * 2);
-                                lc[u] = __ldcg(a.part_ml + r * 2 + 1);
-                                pv[u] = __ldcg(reinterpret_cast<const float4 *>(a.part_acc + r * kD + 4 * lane));
+                                const size_t r = (size_t)(c0 + u + b) * hq + g * GROUP + i;
+                                mc[i][u] = __ldcg(a.part_ml + r * 2);
+                                lc[i][u] = __ldcg(a.part_ml + r * 2 + 1);
+                                pv[i][u] = __ldcg(reinterpret_cast<const float4 *>(a.part_acc + r * kD + 4 * lane));
                             } else {
-                                mc[u] = -INFINITY;
-                                lc[u] = 0.f;
-                                pv[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                                mc[i][u] = -INFINITY;
+                                lc[i][u] = 0.f;
+                                pv[i][u] = make_float4(0.f, 0.f, 0.f, 0.f);
                             }
                         }
-                        float mb = mm;
+                    }
 #pragma unroll
-                        for (int u = 0; u < kBatch; ++u) mb = fmaxf(mb, mc[u]);
+                    for (int i = 0; i < GROUP; ++i) {
+                        float mb = mm[i];
+#pragma unroll
+                        for (int u = 0; u < kBatch; ++u) mb = fmaxf(mb, mc[i][u]);
                         if (mb == -INFINITY) continue;  // nothing attended so far
-                        const float alpha = exp2_approx(mm - mb);  // 0 while mm = -inf
-                        ls *= alpha;
-                        o[0] *= alpha;
-                        o[1] *= alpha;
-                        o[2] *= alpha;
-                        o[3] *= alpha;
+                        const float alpha = exp2_approx(mm[i] - mb);  // 0 while mm = -inf
+                        ls[i] *= alpha;
+                        o[i][0] *= alpha;
+                        o[i][1] *= alpha;
+                        o[i][2] *= alpha;
+                        o[i][3] *= alpha;
 #pragma unroll
                         for (int u = 0; u < kBatch; ++u) {
-                            const float w = exp2_approx(mc[u] - mb);  // 0 for an empty partial (mc = -inf)
-                            ls += w * lc[u];
-                            o[0] += w * pv[u].x;
-                            o[1] += w * pv[u].y;
-                            o[2] += w * pv[u].z;
-                            o[3] += w * pv[u].w;
+                            const float w = exp2_approx(mc[i][u] - mb);  // 0 for an empty partial (mc = -inf)
+                            ls[i] += w * lc[i][u];
+                            o[i][0] += w * pv[i][u].x;
+                            o[i][1] += w * pv[i][u].y;
+                            o[i][2] += w * pv[i][u].z;
+                            o[i][3] += w * pv[i][u].w;
                         }
-                        mm = mb;
+                        mm[i] = mb;
                     }
-                    const float inv = ls > 0.f ? 1.f / ls : 0.f;
+                }
+#pragma unroll
+                for (int i = 0; i < GROUP; ++i) {
+                    const int h = g * GROUP + i;
+                    const float inv = ls[i] > 0.f ? 1.f / ls[i] : 0.f;
                     uint2 w;
-                    w.x = pack_bf16x2(o[0] * inv, o[1] * inv);
-                    w.y = pack_bf16x2(o[2] * inv, o[3] * inv);
+                    w.x = pack_bf16x2(o[i][0] * inv, o[i][1] * inv);
+                    w.y = pack_bf16x2(o[i][2] * inv, o[i][3] * inv);
                     *reinterpret_cast<uint2 *>(a.out + ((size_t)b * hq + h) * kD + 4 * lane) = w;
                 }
                 if (lane == 0) a.arrivals[(size_t)b * kMaxHkv + g] = 0;  // ready for the next call

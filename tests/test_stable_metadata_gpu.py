@@ -75,6 +75,27 @@ def test_back_to_back_layers_on_one_stream(level):
     assert qa.qa_device_status() == 0
 
 
+def test_noalloc_layers_back_to_back_at_level_2():
+    # the entry point without a workspace shares the library's scratch; calls
+    # ordered on one stream may overlap their prologues at level 2
+    base = wl.decode_0p6b()
+    layers = [_layer(base, i) for i in range(3)]
+    refs = [oracle.decode(c["q"], c["k_pages"], c["v_pages"], c["page_table"], c["seq_lens"]) for c in layers]
+    pt, sl = to_dev(base["page_table"]), to_dev(base["seq_lens"])
+    dev = [{k: to_dev(c[k]) for k in ("q", "k_pages", "v_pages")} for c in layers]
+    outs = [torch.empty_like(d["q"]) for d in dev]
+    s = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        for rep in range(2):
+            for d, o in zip(dev, outs):
+                qa.qa_decode_attn_noalloc(d["q"], d["k_pages"], d["v_pages"], pt, sl, o, stream=s, stable_metadata=2)
+    torch.cuda.synchronize()
+    for i, (o, r) in enumerate(zip(outs, refs)):
+        assert_close(f64(o), r, f"no-alloc layer {i}")
+    assert qa.qa_device_status() == 0
+
+
 @pytest.mark.parametrize("level", [1, 2])
 def test_fused_step_after_a_kernel_that_writes_q(level):
     w = wl.with_append(wl.decode_0p6b(), 4)

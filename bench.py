@@ -493,19 +493,23 @@ def _row_prefill(qa, device, stream, peaks, steps, rows):
         cps.append({k: dev_tensor(w[k], device) for k in ("q", "k", "v", "cu_seqlens", "page_table", "k_pages", "v_pages")})
     outp = torch.empty(T, 16, 128, dtype=torch.bfloat16, device=device)
 
-    def mkp(c):
+    # no kernel of the sequence writes the segments or page tables: each call
+    # may set its job up before the previous one ends (stable_metadata = 1)
+    def mkp(c, level):
         return lambda: qa.qa_prefill_attn(c["q"], c["k"], c["v"], c["cu_seqlens"], c["page_table"], c["k_pages"],
-                                          c["v_pages"], outp, stream=stream)
+                                          c["v_pages"], outp, stream=stream, stable_metadata=level)
 
-    el, _ = graph_time([mkp(c) for c in cps], steps, 5, stream)
+    el, _ = graph_time([mkp(c, 1) for c in cps], steps, 5, stream)
     t = el / steps
+    el0, _ = graph_time([mkp(c, 0) for c in cps], steps, 5, stream)
     fl, by = prefill_flops(w["lengths"]), prefill_bytes(T)
     rows["prefill"] = {"workload": "ragged causal prefill + KV page write: 16 requests, ceil(13 d)+40 tokens "
                                    "(d~U[1,30] s), GQA 16/8 x 128", "total_tokens": T, "us_per_call": round(t * 1e6, 2),
                        "tflops": round(fl / t / 1e12, 3), "gbs": round(by / t / 1e9, 1),
                        "frac_bf16_peak": round(fl / t / 1e12 / peaks["bf16"], 4),
                        "frac_hbm": round(by / t / 1e9 / peaks["hbm"], 4), "flops": fl, "bytes": by,
-                       "gpu_launches_per_call": 1}
+                       "gpu_launches_per_call": 1, "stable_metadata": 1,
+                       "us_per_call_stable_metadata_0": round(el0 / steps * 1e6, 2)}
 
 
 def _row_chunk_prefill(qa, device, stream, peaks, steps, rows):
@@ -519,12 +523,14 @@ def _row_chunk_prefill(qa, device, stream, peaks, steps, rows):
     cps = [{k: dev_tensor(w[k], device) for k in keys} for _ in range(4)]
     outp = torch.empty(T, 16, 128, dtype=torch.bfloat16, device=device)
 
-    def mk(c):
+    def mk(c, level):
         return lambda: qa.qa_prefill_chunk_attn(c["q"], c["k"], c["v"], c["cu_seqlens"], c["n_past"],
-                                                c["page_table"], c["k_pages"], c["v_pages"], outp, stream=stream)
+                                                c["page_table"], c["k_pages"], c["v_pages"], outp, stream=stream,
+                                                stable_metadata=level)
 
-    el, _ = graph_time([mk(c) for c in cps], steps, 5, stream)
+    el, _ = graph_time([mk(c, 1) for c in cps], steps, 5, stream)
     t = el / steps
+    el0, _ = graph_time([mk(c, 0) for c in cps], steps, 5, stream)
     past, new = w["n_past"].astype(np.int64), w["lengths"].astype(np.int64)
     fl = int(np.sum(4 * 16 * 128 * (new * past + new * (new + 1) // 2)))
     by = int(prefill_bytes(T) + np.sum(past) * 8 * 128 * 2 * 2)  # + the cached K/V, once
@@ -533,7 +539,8 @@ def _row_chunk_prefill(qa, device, stream, peaks, steps, rows):
                              "new_tokens": T, "cached_tokens": int(np.sum(past)), "us_per_call": round(t * 1e6, 2),
                              "tflops": round(fl / t / 1e12, 3), "gbs": round(by / t / 1e9, 1),
                              "frac_hbm": round(by / t / 1e9 / peaks["hbm"], 4), "flops": fl, "bytes": by,
-                             "gpu_launches_per_call": 1}
+                             "gpu_launches_per_call": 1, "stable_metadata": 1,
+                             "us_per_call_stable_metadata_0": round(el0 / steps * 1e6, 2)}
 
 
 def _row_window(qa, device, stream, peaks, steps, rows):

@@ -107,7 +107,8 @@ typedef struct qa_attn_params {
 } qa_attn_params;
 
 /* stable_metadata (decode calls: qa_decode_attn, qa_decode_attn_noalloc,
- * qa_decode_step).  The decode kernel is launched as a programmatic dependent
+ * qa_decode_step; prefill calls: see after this paragraph).  The decode
+ * kernel is launched as a programmatic dependent
  * of the kernel before it on the stream, so its CTAs may start while that
  * kernel is still finishing.  With stable_metadata = 1 the caller promises
  * that seq_lens and page_table are not written by any kernel that may still
@@ -125,7 +126,14 @@ typedef struct qa_attn_params {
  * (each reads its own layer's pools) and qa_decode_step (it writes the new
  * row itself) meet this; a decode after a qa_decode_append into the same
  * pools does not.  With 0 (the default) it waits before reading anything.
- * Other values are rejected. */
+ * Other values are rejected.
+ *
+ * Prefill calls (qa_prefill_attn, qa_prefill_chunk_attn) launch the same
+ * way.  With stable_metadata >= 1 the caller promises the same of cu_seqlens,
+ * page_table and n_past; the kernel then maps its job, checks it, reads its
+ * page ids and sets up its barriers and tensor memory before that wait, and
+ * waits before it reads q, k, v or the pools or writes any output or page.
+ * (1 and 2 act alike for prefill.) */
 
 /* Defaults: abi_version = QA_ABI_VERSION, 16/8/128 heads, page_size 16,
  * scale 0 (1/sqrt(head_dim)), stream NULL, no workspace, debug_checks 0,

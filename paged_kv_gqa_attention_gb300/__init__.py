@@ -240,7 +240,7 @@ def qa_decode_attn_noalloc(q, k_pages, v_pages, page_table, seq_lens, out=None, 
 
 
 def qa_prefill_attn(q, k, v, cu_seqlens, page_table, k_pages, v_pages, out=None, *, scale=0.0, stream=None,
-                    debug_checks=False):
+                    debug_checks=False, stable_metadata=False):
     """Ragged causal prefill with the KV page write.  q bf16 [T,Hq,D]; k/v
     bf16 [T,Hkv,D]; cu_seqlens int32 [B+1]; page_table int32 [B,max_pages];
     pools bf16 [P,16,Hkv,D] (written in place).  Returns out bf16 [T,Hq,D]."""
@@ -252,7 +252,8 @@ def qa_prefill_attn(q, k, v, cu_seqlens, page_table, k_pages, v_pages, out=None,
     if out is None:
         out = torch.empty_like(q)
     p = _params(n_q_heads=Hq, n_kv_heads=Hkv, head_dim=D, page_size=PS, num_pages=P,
-                max_pages_per_seq=page_table.shape[1], scale=scale, stream=stream, debug_checks=debug_checks)
+                max_pages_per_seq=page_table.shape[1], scale=scale, stream=stream, debug_checks=debug_checks,
+                stable_metadata=stable_metadata)
     st = _lib.qa_prefill_attn(_dev(q, "q", torch.bfloat16, 3), _dev(k, "k", torch.bfloat16, 3),
                               _dev(v, "v", torch.bfloat16, 3), _dev(cu_seqlens, "cu_seqlens", torch.int32, 1), B, T,
                               _dev(page_table, "page_table", torch.int32, 2), _dev(k_pages, "k_pages", torch.bfloat16, 4),
@@ -263,7 +264,7 @@ def qa_prefill_attn(q, k, v, cu_seqlens, page_table, k_pages, v_pages, out=None,
 
 
 def qa_prefill_chunk_attn(q, k, v, cu_seqlens, n_past, page_table, k_pages, v_pages, out=None, *, scale=0.0,
-                          stream=None, debug_checks=False):
+                          stream=None, debug_checks=False, stable_metadata=False):
     """Chunked prefill: request r holds n_past[r] (int32 [B], device) cached
     positions in its pages; its packed new rows attend over those and over
     new rows j <= i, and are written to positions n_past[r] + i.  Shapes as
@@ -278,7 +279,8 @@ def qa_prefill_chunk_attn(q, k, v, cu_seqlens, n_past, page_table, k_pages, v_pa
     if out is None:
         out = torch.empty_like(q)
     p = _params(n_q_heads=Hq, n_kv_heads=Hkv, head_dim=D, page_size=PS, num_pages=P,
-                max_pages_per_seq=page_table.shape[1], scale=scale, stream=stream, debug_checks=debug_checks)
+                max_pages_per_seq=page_table.shape[1], scale=scale, stream=stream, debug_checks=debug_checks,
+                stable_metadata=stable_metadata)
     st = _lib.qa_prefill_chunk_attn(_dev(q, "q", torch.bfloat16, 3), _dev(k, "k", torch.bfloat16, 3),
                                     _dev(v, "v", torch.bfloat16, 3), _dev(cu_seqlens, "cu_seqlens", torch.int32, 1),
                                     _dev(n_past, "n_past", torch.int32, 1), B, T,
@@ -410,7 +412,8 @@ def qa_decode_graph_create(qs, k_pages, v_pages, page_table, seq_lens, outs, *, 
     return QAGraph(h, (qs, k_pages, v_pages, page_table, seq_lens, outs, workspace))
 
 
-def qa_prefill_graph_create(qs, ks, vs, cu_seqlens, page_table, k_pages, v_pages, outs, *, scale=0.0):
+def qa_prefill_graph_create(qs, ks, vs, cu_seqlens, page_table, k_pages, v_pages, outs, *, scale=0.0,
+                            stable_metadata=False):
     """Captures one prefill step of a packed bucket: layer i runs
     qa_prefill_attn(qs[i], ks[i], vs[i], cu_seqlens, page_table, k_pages[i],
     v_pages[i], outs[i]).  Returns a QAGraph."""
@@ -423,7 +426,7 @@ def qa_prefill_graph_create(qs, ks, vs, cu_seqlens, page_table, k_pages, v_pages
     B = cu_seqlens.shape[0] - 1
     P, PS = k_pages[0].shape[0], k_pages[0].shape[1]
     p = _params(n_q_heads=Hq, n_kv_heads=Hkv, head_dim=D, page_size=PS, num_pages=P,
-                max_pages_per_seq=page_table.shape[1], scale=scale)
+                max_pages_per_seq=page_table.shape[1], scale=scale, stable_metadata=stable_metadata)
     h = ctypes.c_void_p()
     st = _lib.qa_prefill_graph_create(n, _ptr_array(qs, "q", torch.bfloat16, 3), _ptr_array(ks, "k", torch.bfloat16, 3),
                                       _ptr_array(vs, "v", torch.bfloat16, 3),

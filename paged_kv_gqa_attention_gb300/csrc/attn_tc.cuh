@@ -64,6 +64,9 @@ struct AttnTcArgs {
     int hkv, max_pages, num_pages, page_size;
     // chunked prefill: cached positions per request (nullptr: none)
     const int32_t *n_past;
+    // prefill: segments, cached lengths and page table may be read before the
+    // kernel before this one has finished (qa_attn_params::stable_metadata)
+    int early;
 };
 
 template <int D>
@@ -758,12 +761,13 @@ __device__ __forceinline__ int prefill_job(const AttnTcArgs &a, bool past_mode, 
 // 16-row TMA box per page per 64-dim sub-tile, into the buffer at dst, plus
 // the Q tile when with_q; one arrival with the total byte count on bar.  A
 // page id outside [0, num_pages) sets QA_DEVICE_BAD_PAGE and is not loaded.
-// One thread.
+// Page ids [0, n_pre) come from pid_s (shared memory, read once at the start
+// of the job), the rest from the page table.  One thread.
 template <int D>
 __device__ __forceinline__ void cached_tile_loads(uint32_t sb, uint32_t dst, const CUtensorMap *tm_pool,
                                                   const CUtensorMap *tm_q, bool with_q, int h, int q0,
-                                                  const int32_t *pt_row, int u, int past, int g, int num_pages,
-                                                  uint32_t bar, unsigned int *status) {
+                                                  const int32_t *pt_row, const int *pid_s, int n_pre, int u,
+                                                  int past, int g, int num_pages, uint32_t bar, unsigned int *status) {
     using L = AttnTcLayout<D>;
     int n = 0;
     int pages[8];
@@ -771,7 +775,8 @@ __device__ __forceinline__ void cached_tile_loads(uint32_t sb, uint32_t dst, con
     for (int p = 0; p < 8; ++p) {
         pages[p] = -1;
         if (128 * u + 16 * p < past) {
-            const int id = pt_row[8 * u + p];
+            const int j = 8 * u + p;
+            const int id = j < n_pre ? pid_s[j] : pt_row[j];
             if (id < 0 || id >= num_pages) {
                 atomicOr(status, QA_DEVICE_BAD_PAGE);
             } else {
@@ -806,10 +811,14 @@ __global__ void __launch_bounds__(128, 2)
     uint8_t *smem = smem_raw + (sb - raw);
     const int tid = threadIdx.x, warp = tid >> 5;
     // launched as a programmatic dependent: wait for the kernel before it
-    // (and its writes) before reading anything; the next kernel is scheduled
-    // once every CTA of this grid has started (the last wave is resident)
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // (and its writes) before reading anything -- or, when the caller vouches
+    // that segments, cached lengths and page table are not its output
+    // (a.early), only before the first tile loads -- then let the next kernel
+    // be scheduled once every CTA of this grid has started
+    if (!a.early) {
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    }
 
     const int h = blockIdx.x, g = h / GROUP;
     const int max_len = a.max_pages * a.page_size;
@@ -872,17 +881,27 @@ __global__ void __launch_bounds__(128, 2)
 
     const uint32_t bar_k = sb + L::kBar, bar_s = bar_k + 8, bar_o = bar_k + 16, bar_v = bar_k + 24;
     // thread 0: requests the K (with Q for the first tile) or V tile of key tile u
+    // chunked form: the page ids of the cached positions (up to kPre of
+    // them), read by warp 0 once so that the cached tiles' loads do not wait
+    // on the page table each time
+    constexpr int kPre = 256;
+    int *pid_s = reinterpret_cast<int *>(smem + L::kBytes);
+    const int n_pre = PAST ? min(kPre, (past + 15) / 16) : 0;
+    if (PAST && warp == 0) {
+        for (int j = tid; j < n_pre; j += 32) pid_s[j] = pt_row[j];
+        __syncwarp();
+    }
     auto load_k = [&](int u, bool with_q) {
         if (PAST && u < n_ct)
-            cached_tile_loads<D>(sb, sb + L::kK, &tm_kp, &tm_q, with_q, h, q0, pt_row, u, past, g, a.num_pages, bar_k,
-                                 status);
+            cached_tile_loads<D>(sb, sb + L::kK, &tm_kp, &tm_q, with_q, h, q0, pt_row, pid_s, n_pre, u, past, g,
+                                 a.num_pages, bar_k, status);
         else
             issue_qk_loads<D>(sb, &tm_q, &tm_k, h, g, q0, s0 + (u - n_ct) * 128, with_q, bar_k);
     };
     auto load_v = [&](int u) {
         if (PAST && u < n_ct)
-            cached_tile_loads<D>(sb, sb + L::kV, &tm_vp, &tm_q, false, h, q0, pt_row, u, past, g, a.num_pages, bar_v,
-                                 status);
+            cached_tile_loads<D>(sb, sb + L::kV, &tm_vp, &tm_q, false, h, q0, pt_row, pid_s, n_pre, u, past, g,
+                                 a.num_pages, bar_v, status);
         else
             issue_v_loads<D>(sb, &tm_v, g, s0 + (u - n_ct) * 128, bar_v);
     };
@@ -892,13 +911,23 @@ __global__ void __launch_bounds__(128, 2)
         mbar_init(bar_o, 1);
         mbar_init(bar_v, 1);
         fence_mbar_init();
-        load_k(0, true);
-        load_v(0);
+        if (!a.early) {
+            load_k(0, true);
+            load_v(0);
+        }
     }
     if (warp == 0) tc::tmem_alloc(sb + L::kTmemSlot, 256);
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
+    if (a.early) {  // the job is set up; q, k, v, the pools and out only now
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+        if (tid == 0) {
+            load_k(0, true);
+            load_v(0);
+        }
+    }
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + L::kTmemSlot);
     const uint32_t t_row = tmem + ((uint32_t)(warp * 32) << 16);
     const uint32_t col_o = 128;

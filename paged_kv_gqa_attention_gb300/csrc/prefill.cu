@@ -62,6 +62,7 @@ cudaError_t launch_prefill(const void *q, const void *k, const void *v, const in
     a.num_pages = p.num_pages;
     a.page_size = p.page_size;
     a.n_past = n_past;
+    a.early = (p.abi_version >= 2 && p.stable_metadata >= 1) ? 1 : 0;
     unsigned int *status = nullptr;
     cudaError_t e = cudaGetSymbolAddress(reinterpret_cast<void **>(&status), g_status);
     if (e != cudaSuccess) return e;
@@ -70,9 +71,10 @@ cudaError_t launch_prefill(const void *q, const void *k, const void *v, const in
     const long long qtiles = (max_len + 127) / 128;
     if (qtiles > 65535 || batch > 65535) return cudaErrorInvalidValue;
     const dim3 grid(p.n_q_heads, batch, (unsigned)qtiles);
-    constexpr uint32_t smem = AttnTcLayout<128>::kSmem;
+    // the chunked form keeps up to 256 cached page ids in 1 KiB more
+    const uint32_t smem = AttnTcLayout<128>::kSmem + (n_past ? 1024u : 0u);
     auto launch = [&](auto kernel) -> cudaError_t {
-        cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (err != cudaSuccess) return err;
         err = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                                    (int)cudaSharedmemCarveoutMaxShared);

@@ -14,7 +14,7 @@ import pytest
 
 import oracle
 import workloads as wl
-from _util import assert_close, f64, to_dev
+from _util import assert_close, bits, f64, to_dev
 
 pytestmark = pytest.mark.gpu
 import torch  # noqa: E402
@@ -123,6 +123,55 @@ def _layer(base, i):
     c["q"] = wl.normal_bf16(wl.rng_for(700 + i), base["q"].shape)
     c["k_pages"] = wl.bf16_bits((wl.bf16_to_f64(base["k_pages"]) * 2.0 ** -i).astype(np.float32))
     return c
+
+
+def test_prefill_layers_back_to_back_at_level_1():
+    # the prefill bucket's calls for three layers (own q, k, v and pools; one
+    # cu_seqlens and page table) queued on one stream without a host sync
+    base = wl.prefill_bucket()
+    layers = []
+    for i in range(3):
+        c = dict(base)
+        rng = wl.rng_for(800 + i)
+        for key in ("q", "k", "v"):
+            c[key] = wl.normal_bf16(rng, base[key].shape)
+        layers.append(c)
+    cu, pt = to_dev(base["cu_seqlens"]), to_dev(base["page_table"])
+    dev = [{key: to_dev(c[key]) for key in ("q", "k", "v", "k_pages", "v_pages")} for c in layers]
+    s = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        outs = [qa.qa_prefill_attn(d["q"], d["k"], d["v"], cu, pt, d["k_pages"], d["v_pages"], stream=s,
+                                   stable_metadata=1) for d in dev]
+    torch.cuda.synchronize()
+    for i, (c, d, o) in enumerate(zip(layers, dev, outs)):
+        assert_close(f64(o), oracle.prefill(c["q"], c["k"], c["v"], c["cu_seqlens"]), f"prefill layer {i}")
+        ekp, evp = oracle.page_write(c["k"], c["v"], c["cu_seqlens"], c["page_table"], c["k_pages"], c["v_pages"])
+        np.testing.assert_array_equal(bits(d["k_pages"]), ekp)
+        np.testing.assert_array_equal(bits(d["v_pages"]), evp)
+    assert qa.qa_device_status() == 0
+
+
+def test_chunked_prefill_twice_at_level_1():
+    w = wl.chunk_reprefill()
+    ref = oracle.prefill_chunk(w["q"], w["k"], w["v"], w["cu_seqlens"], w["n_past"], w["page_table"], w["k_pages"],
+                               w["v_pages"])
+    d = {key: to_dev(w[key]) for key in ("q", "k", "v", "cu_seqlens", "n_past", "page_table", "k_pages", "v_pages")}
+    s = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        # the second call rewrites the same rows with the same values and
+        # reads the same cached pages
+        outs = [qa.qa_prefill_chunk_attn(d["q"], d["k"], d["v"], d["cu_seqlens"], d["n_past"], d["page_table"],
+                                         d["k_pages"], d["v_pages"], stream=s, stable_metadata=1) for _ in range(2)]
+    torch.cuda.synchronize()
+    for i, o in enumerate(outs):
+        assert_close(f64(o), ref, f"chunked prefill call {i}")
+    ekp, evp = oracle.page_write_at(w["k"], w["v"], w["cu_seqlens"], w["n_past"], w["page_table"], w["k_pages"],
+                                    w["v_pages"])
+    np.testing.assert_array_equal(bits(d["k_pages"]), ekp)
+    np.testing.assert_array_equal(bits(d["v_pages"]), evp)
+    assert qa.qa_device_status() == 0
 
 
 def test_graph_of_layers_follows_refills():

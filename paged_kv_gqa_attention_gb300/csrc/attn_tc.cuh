@@ -349,6 +349,57 @@ __device__ __forceinline__ void store_rows_staged(uint32_t o_row, float l, uint3
     }
 }
 
+// Epilogue of the window kernel for head_dim 64: thread r stages its row of O
+// (divided by l, bf16) as store_rows_staged does -- 128-byte rows whose
+// 16-byte chunks are XOR-swizzled by r, which is exactly the layout of a
+// 128B-swizzled TMA box of 8 rows x 64 dims -- then thread 0 writes the rows
+// of whole 8-row boxes with TMA stores (tensor map tm_out, box {64, 1, 8};
+// tracked by its bulk group: wait for their shared-memory reads before the
+// stage is reused) and the threads of the remaining rows (< 8) store theirs.
+// Rows at or past row_end are not written.  CTA-collective (128 threads).
+__device__ __forceinline__ void store_rows_tma64(uint32_t o_row, float l, uint32_t stage, const CUtensorMap *tm_out,
+                                                 uint16_t *out, int hq, int h, int q0, int row_end) {
+    constexpr int D = 64;
+    const int r = threadIdx.x;
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    const uint32_t my_row = stage + (uint32_t)r * (D * 2);
+    const float2 inv2 = make_float2(inv, inv);
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) {
+        float ov[32];
+        tc::tmem_ld32(o_row + c * 32, ov);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const float2 o0 = fmul2(make_float2(ov[8 * u + 0], ov[8 * u + 1]), inv2);
+            const float2 o1 = fmul2(make_float2(ov[8 * u + 2], ov[8 * u + 3]), inv2);
+            const float2 o2 = fmul2(make_float2(ov[8 * u + 4], ov[8 * u + 5]), inv2);
+            const float2 o3 = fmul2(make_float2(ov[8 * u + 6], ov[8 * u + 7]), inv2);
+            const uint32_t pos = (uint32_t)(c * 4 + u) ^ (uint32_t)(r & 7);
+            tc::st_shared_v4(my_row + pos * 16, pack_bf16x2(o0.x, o0.y), pack_bf16x2(o1.x, o1.y),
+                             pack_bf16x2(o2.x, o2.y), pack_bf16x2(o3.x, o3.y));
+        }
+    }
+    tc::fence_proxy_async_smem();  // the staged rows are read by the TMA unit
+    __syncthreads();
+    const int n_rows = min(128, row_end);
+    const int full = n_rows / 8 * 8;
+    if (r == 0 && full > 0) {
+        for (int i = 0; i < full; i += 8) tc::tma_store_3d(tm_out, stage + (uint32_t)i * (D * 2), 0, h, q0 + i);
+        tc::bulk_commit_group();
+    }
+    if (r >= full && r < n_rows) {
+        uint16_t *dst = out + ((size_t)(q0 + r) * hq + h) * D;
+#pragma unroll
+        for (int c = 0; c < D / 8; ++c) {
+            uint32_t x0, x1, x2, x3;
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(x0), "=r"(x1), "=r"(x2), "=r"(x3)
+                         : "r"(my_row + (((uint32_t)c ^ (uint32_t)(r & 7)) << 4)));
+            *reinterpret_cast<uint4 *>(dst + c * 8) = make_uint4(x0, x1, x2, x3);
+        }
+    }
+}
+
 // S = Q K^T (M = 128, N = 128 keys, K = D in steps of 16: 32 bytes inside a
 // 128-byte row) into TMEM columns [0, 128) of tmem.  One thread.
 template <int D>
@@ -508,7 +559,8 @@ __device__ __forceinline__ void issue_v_loads(uint32_t sb, const CUtensorMap *tm
 template <int D>
 __global__ void __launch_bounds__(128, D == 64 ? 4 : 2)
     window_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                     const __grid_constant__ CUtensorMap tm_v, const AttnTcArgs a, unsigned int *status) {
+                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_out,
+                     const AttnTcArgs a, unsigned int *status) {
     using L = AttnTcLayout<D>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -559,6 +611,7 @@ __global__ void __launch_bounds__(128, D == 64 ? 4 : 2)
     const uint32_t plo_row = sb + L::kPlo + r * 128;
     const uint32_t sw = (uint32_t)(r & 7);
     bool prefetched = false;  // thread 0: the job's first Q/K tiles are already requested
+    int pf_h = 0, pf_s0 = 0;  // thread 0: head and first row of that job (its V comes later)
 
     for (int job = blockIdx.x; job < n_jobs; job += G) {
         const int seg = job % a.n_seg, h = job / a.n_seg;
@@ -633,15 +686,26 @@ __global__ void __launch_bounds__(128, D == 64 ? 4 : 2)
                     if (0 <= nx_s0 && nx_s0 < nx_s1 && nx_s1 <= a.total) {
                         issue_qk_loads<D>(sb, &tm_q, &tm_k, nx_h, nx_h, nx_s0, nx_s0, true, bar_qk);
                         prefetched = true;
+                        // kept in registers: thread 32 rewrites nx for the job
+                        // after next as soon as it passes the epilogue's barrier
+                        pf_h = nx_h;
+                        pf_s0 = nx_s0;
                     }
                 }
             }
             // epilogue staged in the V buffer (free since the last P V)
-            store_rows_staged<D>(t_row + col_o, l, sb + L::kV, a.out, a.hq, h, q0, s1 - q0, tid);
+            if (D == 64)
+                store_rows_tma64(t_row + col_o, l, sb + L::kV, &tm_out, a.out, a.hq, h, q0, s1 - q0);
+            else
+                store_rows_staged<D>(t_row + col_o, l, sb + L::kV, a.out, a.hq, h, q0, s1 - q0, tid);
             tc::fence_before();
             __syncthreads();  // every TMEM read and staging read is done
-            // the V buffer is free again: request the next job's V
-            if (tid == 0 && prefetched) issue_v_loads<D>(sb, &tm_v, nx[0], nx[1], bar_v);
+            // the V buffer is free again once the TMA stores have read it:
+            // request the next job's V
+            if (tid == 0) {
+                tc::bulk_wait_group_read_all();
+                if (prefetched) issue_v_loads<D>(sb, &tm_v, pf_h, pf_s0, bar_v);
+            }
         }
     }
 

@@ -29,11 +29,17 @@ cudaError_t launch_window(const void *q, const void *k, const void *v, const int
                           float scale, cudaStream_t stream) {
     if (total_tokens == 0) return cudaSuccess;
     if (p.n_q_heads > 65535) return cudaErrorInvalidValue;
-    CUtensorMap tq, tk, tv;
+    CUtensorMap tq, tk, tv, tout;
     if (!make_rows_tmap(&tq, q, p.head_dim, p.n_q_heads, total_tokens) ||
         !make_rows_tmap(&tk, k, p.head_dim, p.n_kv_heads, total_tokens) ||
         !make_rows_tmap(&tv, v, p.head_dim, p.n_kv_heads, total_tokens))
         return cudaErrorInvalidValue;
+    // head_dim 64: the output is written in 8-row TMA boxes (store_rows_tma64)
+    if (p.head_dim == 64) {
+        if (!make_rows_tmap(&tout, out, p.head_dim, p.n_q_heads, total_tokens, 8)) return cudaErrorInvalidValue;
+    } else {
+        tout = tq;  // not used
+    }
     AttnTcArgs a{};
     a.cu = cu_windows;
     a.out = static_cast<uint16_t *>(out);
@@ -74,7 +80,7 @@ cudaError_t launch_window(const void *q, const void *k, const void *v, const int
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        return cudaLaunchKernelEx(&cfg, kernel, tq, tk, tv, a, status);
+        return cudaLaunchKernelEx(&cfg, kernel, tq, tk, tv, tout, a, status);
     };
     if (p.head_dim == 64)
         e = launch(window_tc_kernel<64>, AttnTcLayout<64>::kSmem, 4);

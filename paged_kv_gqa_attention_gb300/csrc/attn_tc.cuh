@@ -32,8 +32,9 @@
 //   5. One thread issues O += P_hi V and O += P_lo V (M = 128, N = 64 per
 //      MMA, K = 128 keys in steps of 16, V read MN-major).
 // After the last key tile each row of O is read back, divided by its softmax
-// sum, rounded to bf16, staged in shared memory and stored whole rows at a
-// time (store_rows_staged).
+// sum, rounded to bf16 and staged in shared memory; the window kernel writes
+// the stage out with TMA stores of 8-row boxes (store_rows_tma), the prefill
+// with whole rows per warp store (store_rows_staged).
 //
 // Masks.  Window: key j is visible to row i iff both lie in the segment.
 // Causal prefill: additionally j <= i.  Rows past the segment end are computed
@@ -349,33 +350,35 @@ __device__ __forceinline__ void store_rows_staged(uint32_t o_row, float l, uint3
     }
 }
 
-// Epilogue of the window kernel for head_dim 64: thread r stages its row of O
-// (divided by l, bf16) as store_rows_staged does -- 128-byte rows whose
-// 16-byte chunks are XOR-swizzled by r, which is exactly the layout of a
-// 128B-swizzled TMA box of 8 rows x 64 dims -- then thread 0 writes the rows
-// of whole 8-row boxes with TMA stores (tensor map tm_out, box {64, 1, 8};
-// tracked by its bulk group: wait for their shared-memory reads before the
-// stage is reused) and the threads of the remaining rows (< 8) store theirs.
-// Rows at or past row_end are not written.  CTA-collective (128 threads).
-__device__ __forceinline__ void store_rows_tma64(uint32_t o_row, float l, uint32_t stage, const CUtensorMap *tm_out,
-                                                 uint16_t *out, int hq, int h, int q0, int row_end) {
-    constexpr int D = 64;
+// Epilogue through TMA stores: thread r stages its row of O (divided by l,
+// bf16) sub-tile by sub-tile -- dims [64 sd, 64 sd + 64) of row r at stage +
+// sd * 16 KiB + r * 128 with its 16-byte chunks XOR-swizzled by r, which is
+// the layout of a 128B-swizzled TMA box of 8 rows x 64 dims -- then thread 0
+// writes the rows of whole 8-row boxes with TMA stores (tensor map tm_out,
+// box {64, 1, 8}; tracked by its bulk group: wait for their reads of shared
+// memory before the stage is reused) and the threads of the remaining rows
+// (< 8) store theirs.  Rows at or past row_end are not written.
+// CTA-collective (128 threads).
+template <int D>
+__device__ __forceinline__ void store_rows_tma(uint32_t o_row, float l, uint32_t stage, const CUtensorMap *tm_out,
+                                               uint16_t *out, int hq, int h, int q0, int row_end) {
     const int r = threadIdx.x;
     const float inv = l > 0.f ? 1.f / l : 0.f;
-    const uint32_t my_row = stage + (uint32_t)r * (D * 2);
+    const uint32_t my_row = stage + (uint32_t)r * 128u;
     const float2 inv2 = make_float2(inv, inv);
 #pragma unroll
     for (int c = 0; c < D / 32; ++c) {
         float ov[32];
         tc::tmem_ld32(o_row + c * 32, ov);
+        const uint32_t sub = (uint32_t)(c >> 1) * tc::kSubTileBytes;  // 32 dims = half a sub-tile
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
             const float2 o0 = fmul2(make_float2(ov[8 * u + 0], ov[8 * u + 1]), inv2);
             const float2 o1 = fmul2(make_float2(ov[8 * u + 2], ov[8 * u + 3]), inv2);
             const float2 o2 = fmul2(make_float2(ov[8 * u + 4], ov[8 * u + 5]), inv2);
             const float2 o3 = fmul2(make_float2(ov[8 * u + 6], ov[8 * u + 7]), inv2);
-            const uint32_t pos = (uint32_t)(c * 4 + u) ^ (uint32_t)(r & 7);
-            tc::st_shared_v4(my_row + pos * 16, pack_bf16x2(o0.x, o0.y), pack_bf16x2(o1.x, o1.y),
+            const uint32_t pos = (uint32_t)((c & 1) * 4 + u) ^ (uint32_t)(r & 7);
+            tc::st_shared_v4(my_row + sub + pos * 16, pack_bf16x2(o0.x, o0.y), pack_bf16x2(o1.x, o1.y),
                              pack_bf16x2(o2.x, o2.y), pack_bf16x2(o3.x, o3.y));
         }
     }
@@ -384,7 +387,10 @@ __device__ __forceinline__ void store_rows_tma64(uint32_t o_row, float l, uint32
     const int n_rows = min(128, row_end);
     const int full = n_rows / 8 * 8;
     if (r == 0 && full > 0) {
-        for (int i = 0; i < full; i += 8) tc::tma_store_3d(tm_out, stage + (uint32_t)i * (D * 2), 0, h, q0 + i);
+        for (int i = 0; i < full; i += 8)
+#pragma unroll
+            for (int sd = 0; sd < D / 64; ++sd)
+                tc::tma_store_3d(tm_out, stage + sd * tc::kSubTileBytes + (uint32_t)i * 128u, sd * 64, h, q0 + i);
         tc::bulk_commit_group();
     }
     if (r >= full && r < n_rows) {
@@ -394,7 +400,8 @@ __device__ __forceinline__ void store_rows_tma64(uint32_t o_row, float l, uint32
             uint32_t x0, x1, x2, x3;
             asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
                          : "=r"(x0), "=r"(x1), "=r"(x2), "=r"(x3)
-                         : "r"(my_row + (((uint32_t)c ^ (uint32_t)(r & 7)) << 4)));
+                         : "r"(my_row + (uint32_t)(c >> 3) * tc::kSubTileBytes +
+                               ((((uint32_t)c & 7u) ^ (uint32_t)(r & 7)) << 4)));
             *reinterpret_cast<uint4 *>(dst + c * 8) = make_uint4(x0, x1, x2, x3);
         }
     }
@@ -552,7 +559,8 @@ __device__ __forceinline__ void issue_v_loads(uint32_t sb, const CUtensorMap *tm
 // Q and K are requested as soon as the current job's last P V has finished
 // reading shared memory, so they load during the epilogue; the epilogue
 // stages the output rows in the V buffer and writes whole rows per store
-// (store_rows_staged), after which the next job's V is requested.  Each job
+// (store_rows_tma: 8-row TMA stores), after which the next job's V is
+// requested.  Each job
 // is computed as described at the top of this file.  TMEM: 128 columns when
 // every job of the CTA is a single 128-row tile and D = 64 (four CTAs share
 // the 512 columns of an SM), else 256.
@@ -694,10 +702,7 @@ __global__ void __launch_bounds__(128, D == 64 ? 4 : 2)
                 }
             }
             // epilogue staged in the V buffer (free since the last P V)
-            if (D == 64)
-                store_rows_tma64(t_row + col_o, l, sb + L::kV, &tm_out, a.out, a.hq, h, q0, s1 - q0);
-            else
-                store_rows_staged<D>(t_row + col_o, l, sb + L::kV, a.out, a.hq, h, q0, s1 - q0, tid);
+            store_rows_tma<D>(t_row + col_o, l, sb + L::kV, &tm_out, a.out, a.hq, h, q0, s1 - q0);
             tc::fence_before();
             __syncthreads();  // every TMEM read and staging read is done
             // the V buffer is free again once the TMA stores have read it:

@@ -217,10 +217,13 @@ __device__ __forceinline__ void softmax_tile(uint32_t s_row, int n_ok, float sca
 // the scores they replace: keys [32c, 32c + 32) give P_hi in columns
 // [32c, 32c + 16) and P_lo in [32c + 16, 32c + 32).  The scores are read once
 // instead of twice.  Same (m, l) update, lazy reference max and rescale as
-// softmax_tile.  Warp-collective.
-template <int D>
+// softmax_tile, the rescale of O done before any P is written.  Once keys
+// [0, 64) of the row are in TMEM it calls mid() -- every thread of the CTA,
+// at the same point -- so the caller can start P V on that half while the
+// rest is exponentiated.  CTA-collective through mid().
+template <int D, typename Mid>
 __device__ __forceinline__ void softmax_tile_regs(uint32_t s_row, int n_ok, float scale_log2, uint32_t o_row,
-                                                  bool rescale, float &m, float &l) {
+                                                  bool rescale, float &m, float &l, Mid &&mid) {
     const int warp_max = __reduce_max_sync(0xffffffffu, n_ok);
     const int warp_min = __reduce_min_sync(0xffffffffu, n_ok);
     const int n_chunks = (warp_max + 31) >> 5;  // warp-uniform
@@ -257,6 +260,21 @@ __device__ __forceinline__ void softmax_tile_regs(uint32_t s_row, int n_ok, floa
     const float2 neg_m2 = make_float2(-m_new, -m_new);
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
+        if (c == 2) {
+            // O is rescaled before any P of this tile is handed over (the
+            // previous tile's P V has completed: this tile's S came after it)
+            if (rescale && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+                for (int cc = 0; cc < D / 32; ++cc) {
+                    float ov[32];
+                    tc::tmem_ld32(o_row + cc * 32, ov);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) ov[j] *= alpha;
+                    tc::tmem_st32(o_row + cc * 32, ov);
+                }
+            }
+            mid();  // keys [0, 64) of every row are in TMEM
+        }
         uint32_t pk[16], pl[16];
         if (c >= n_chunks) {  // warp-uniform: a dead chunk gets zero probabilities
 #pragma unroll
@@ -290,16 +308,6 @@ __device__ __forceinline__ void softmax_tile_regs(uint32_t s_row, int n_ok, floa
     const float2 psum2 = fadd2(fadd2(psum4[0], psum4[1]), fadd2(psum4[2], psum4[3]));
     l = l * alpha + (psum2.x + psum2.y);
     m = m_new;
-    if (rescale && __any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-            float ov[32];
-            tc::tmem_ld32(o_row + c * 32, ov);
-#pragma unroll
-            for (int j = 0; j < 32; ++j) ov[j] *= alpha;
-            tc::tmem_st32(o_row + c * 32, ov);
-        }
-    }
 }
 
 // Epilogue through shared memory: thread r (of the 128 threads that own the
@@ -511,12 +519,16 @@ __device__ __forceinline__ void write_kv_pages(const uint8_t *k_tile, const uint
 // O += P_hi V + P_lo V with both P terms in TMEM in the chunk layout of
 // softmax_tile_regs: keys [16kk, 16kk + 16) are P_hi columns
 // 32 (kk / 2) + 8 (kk % 2) + [0, 8) and P_lo columns 16 further.  N = 64
-// dims per MMA, V read MN-major.  One thread.
+// dims per MMA, V read MN-major.  half = 0 / 1: keys [0, 64) / [64, 128)
+// only (-1: all).  One thread.
 template <int D>
-__device__ __forceinline__ void issue_pv_tp(uint32_t tmem, uint32_t o_col, uint32_t v_base, bool accumulate) {
+__device__ __forceinline__ void issue_pv_tp(uint32_t tmem, uint32_t o_col, uint32_t v_base, bool accumulate,
+                                            int half = -1) {
     constexpr uint32_t idesc_o = tc::idesc_bf16(128, 64, true);
+    const int kk0 = half < 0 ? 0 : 4 * half, kk1 = half < 0 ? 8 : kk0 + 4;
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) {
+        if (kk < kk0 || kk >= kk1) continue;
         const uint32_t a_hi = tmem + (uint32_t)(kk >> 1) * 32 + (uint32_t)(kk & 1) * 8;
 #pragma unroll
         for (int sd = 0; sd < D / 64; ++sd) {
@@ -1045,13 +1057,23 @@ __global__ void __launch_bounds__(128, 2)
             n_ok = min(n_ok, li - 128 * kt + 1);
             n_ok = max(n_ok, 0);
         }
-        softmax_tile_regs<D>(t_row, n_ok, a.scale_log2, t_row + col_o, u > 0, m, l);
+        // P V in two halves of 64 keys: the first starts as soon as every
+        // row has written P for keys [0, 64), the second after the softmax
+        softmax_tile_regs<D>(t_row, n_ok, a.scale_log2, t_row + col_o, u > 0, m, l, [&] {
+            tc::tmem_wait_st();
+            tc::fence_before();
+            __syncthreads();
+            if (tid == 0) {
+                mbar_wait(bar_v, ph, status);
+                tc::fence_after();
+                issue_pv_tp<D>(tmem, tmem + col_o, sb + L::kV, u > 0, 0);
+            }
+        });
         tc::fence_before();
         __syncthreads();
         if (tid == 0) {
-            mbar_wait(bar_v, ph, status);
             tc::fence_after();
-            issue_pv_tp<D>(tmem, tmem + col_o, sb + L::kV, u > 0);
+            issue_pv_tp<D>(tmem, tmem + col_o, sb + L::kV, true, 1);
             tc::mma_commit(bar_o);
         }
         if (u == n_tiles - 1 && (write_k || write_v)) {

@@ -29,6 +29,24 @@ def test_small_windows(counts):
     assert_close(f64(out), ref, f"counts {counts}")
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_window_sizes_around_the_store_boxes(d):
+    # the output leaves in boxes of 8 rows plus the rows of a partial box:
+    # window sizes 1..17 and 127..129 around those boundaries, every row
+    # checked; the output starts NaN-filled, so a row left unwritten (or
+    # overwritten by a neighbouring window's box) fails
+    sizes = [1, 2, 7, 8, 9, 15, 16, 17, 127, 128, 129]
+    T = sum(sizes)
+    w = wl.window_workload(350 + d, (T,), h=3, d=d)
+    cu = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    q, k, v = to_dev(w["q"]), to_dev(w["k"]), to_dev(w["v"])
+    out = torch.full_like(q, float("nan"))
+    qa.qa_window_attn(q, k, v, to_dev(cu), out, debug_checks=True)
+    torch.cuda.synchronize()
+    ref = oracle.window(w["q"], w["k"], w["v"], cu)
+    assert_close(f64(out), ref, f"D={d}, window sizes {sizes}")
+
+
 def test_head_dim_128_and_long_windows():
     counts = (300, 129)
     w = wl.window_workload(41, counts, h=4, d=128)

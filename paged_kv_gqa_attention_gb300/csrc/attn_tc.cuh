@@ -564,9 +564,12 @@ __device__ __forceinline__ void issue_v_loads(uint32_t sb, const CUtensorMap *tm
 }
 
 // Window attention, persistent: a grid of a few CTAs per SM walks the jobs
-// (window, head) in the order job = blockIdx.x + i * gridDim.x, job = head *
-// n_windows + window, so the CTAs running at any time hold neighbouring
-// windows of one head.  Barriers and TMEM are set up once per CTA.  Q + K and
+// (window, head) in the order job = blockIdx.x + i * gridDim.x, job = window *
+// n_heads + head, so the CTAs running at any time hold every head of a run of
+// neighbouring windows: the heads' 128-byte slices of a token's row (all
+// heads side by side) are fetched at about the same time, which keeps DRAM
+// pages open for the whole row rather than reopening them once per head.
+// Barriers and TMEM are set up once per CTA.  Q + K and
 // V land on separate barriers, so S starts before V is in.  The next job's
 // Q and K are requested as soon as the current job's last P V has finished
 // reading shared memory, so they load during the epilogue; the epilogue
@@ -602,7 +605,7 @@ __global__ void __launch_bounds__(128, D == 64 ? 4 : 2)
     // does any job of this CTA span more than one 128-row tile?
     int multi = 0;
     for (int j = blockIdx.x + tid * G; j < n_jobs; j += 128 * G) {
-        const int seg = j % a.n_seg;
+        const int seg = j / a.hq;
         multi |= a.cu[seg + 1] - a.cu[seg] > 128;
     }
     multi = __syncthreads_or(multi);
@@ -634,7 +637,7 @@ __global__ void __launch_bounds__(128, D == 64 ? 4 : 2)
     int pf_h = 0, pf_s0 = 0;  // thread 0: head and first row of that job (its V comes later)
 
     for (int job = blockIdx.x; job < n_jobs; job += G) {
-        const int seg = job % a.n_seg, h = job / a.n_seg;
+        const int seg = job / a.hq, h = job % a.hq;
         const int s0 = a.cu[seg], s1 = a.cu[seg + 1];
         // one thread off the MMA-issue path reads the next job's bounds into
         // shared memory for thread 0's early loads (seen after the softmax barrier)
@@ -643,8 +646,8 @@ __global__ void __launch_bounds__(128, D == 64 ? 4 : 2)
             const int nj = job + G;
             int v0 = 0, v1 = 0, v2 = 0;  // (head, s0, s1); s0 == s1: nothing to request
             if (nj < n_jobs) {
-                const int nseg = nj % a.n_seg;
-                v0 = nj / a.n_seg;
+                const int nseg = nj / a.hq;
+                v0 = nj % a.hq;
                 v1 = a.cu[nseg];
                 v2 = a.cu[nseg + 1];
             }

@@ -846,40 +846,36 @@ __device__ __forceinline__ int prefill_job(const AttnTcArgs &a, bool past_mode, 
 // the Q tile when with_q; one arrival with the total byte count on bar.  A
 // page id outside [0, num_pages) sets QA_DEVICE_BAD_PAGE and is not loaded.
 // Page ids [0, n_pre) come from pid_s (shared memory, read once at the start
-// of the job), the rest from the page table.  One thread.
+// of the job), the rest from the page table.  Warp-collective: lane
+// kSub * p + sd issues page p's sub-tile sd (and lane sd the Q tile's), so
+// the sixteen box requests leave in parallel rather than one after another
+// from the thread that also runs a softmax row.
 template <int D>
 __device__ __forceinline__ void cached_tile_loads(uint32_t sb, uint32_t dst, const CUtensorMap *tm_pool,
                                                   const CUtensorMap *tm_q, bool with_q, int h, int q0,
                                                   const int32_t *pt_row, const int *pid_s, int n_pre, int u,
                                                   int past, int g, int num_pages, uint32_t bar, unsigned int *status) {
     using L = AttnTcLayout<D>;
-    int n = 0;
-    int pages[8];
-#pragma unroll
-    for (int p = 0; p < 8; ++p) {
-        pages[p] = -1;
-        if (128 * u + 16 * p < past) {
-            const int j = 8 * u + p;
-            const int id = j < n_pre ? pid_s[j] : pt_row[j];
-            if (id < 0 || id >= num_pages) {
-                atomicOr(status, QA_DEVICE_BAD_PAGE);
-            } else {
-                pages[p] = id;
-                ++n;
-            }
+    static_assert(8 * L::kSub <= 32, "one lane per box");
+    const int lane = threadIdx.x & 31;
+    const int p = lane / L::kSub, sd = lane % L::kSub;
+    int id = -1;
+    bool live = p < 8 && 128 * u + 16 * p < past;
+    if (live) {
+        const int j = 8 * u + p;
+        id = j < n_pre ? pid_s[j] : pt_row[j];
+        if (id < 0 || id >= num_pages) {
+            if (sd == 0) atomicOr(status, QA_DEVICE_BAD_PAGE);
+            live = false;
         }
     }
-    mbar_arrive_expect_tx(bar, (uint32_t)n * L::kSub * 16 * 128 + (with_q ? L::kSub * tc::kSubTileBytes : 0u));
-    if (with_q)
-#pragma unroll
-        for (int sd = 0; sd < L::kSub; ++sd)
-            tc::tma_load_3d(sb + L::kQ + sd * tc::kSubTileBytes, tm_q, sd * 64, h, q0, bar);
-#pragma unroll
-    for (int p = 0; p < 8; ++p)
-        if (pages[p] >= 0)
-#pragma unroll
-            for (int sd = 0; sd < L::kSub; ++sd)
-                tc::tma_load_3d(dst + sd * tc::kSubTileBytes + p * 16 * 128, tm_pool, sd * 64, g, pages[p] * 16, bar);
+    const unsigned boxes = __ballot_sync(0xffffffffu, live);
+    if (lane == 0)
+        mbar_arrive_expect_tx(bar, (uint32_t)__popc(boxes) * 16u * 128u + (with_q ? L::kSub * tc::kSubTileBytes : 0u));
+    __syncwarp();
+    if (live) tc::tma_load_3d(dst + sd * tc::kSubTileBytes + p * 16 * 128, tm_pool, sd * 64, g, id * 16, bar);
+    if (with_q && lane < L::kSub)
+        tc::tma_load_3d(sb + L::kQ + lane * tc::kSubTileBytes, tm_q, lane * 64, h, q0, bar);
 }
 
 template <int GROUP, bool PAST>
@@ -964,7 +960,6 @@ __global__ void __launch_bounds__(128, 2)
     const int32_t *pt_row = a.page_table + (size_t)b * a.max_pages;
 
     const uint32_t bar_k = sb + L::kBar, bar_s = bar_k + 8, bar_o = bar_k + 16, bar_v = bar_k + 24;
-    // thread 0: requests the K (with Q for the first tile) or V tile of key tile u
     // chunked form: the page ids of the cached positions (up to kPre of
     // them), read by warp 0 once so that the cached tiles' loads do not wait
     // on the page table each time
@@ -975,18 +970,21 @@ __global__ void __launch_bounds__(128, 2)
         for (int j = tid; j < n_pre; j += 32) pid_s[j] = pt_row[j];
         __syncwarp();
     }
+    // warp 0: requests the K (with Q for the first tile) or V tile of key
+    // tile u (a cached tile's boxes leave from its lanes, a new tile's from
+    // lane 0)
     auto load_k = [&](int u, bool with_q) {
         if (PAST && u < n_ct)
             cached_tile_loads<D>(sb, sb + L::kK, &tm_kp, &tm_q, with_q, h, q0, pt_row, pid_s, n_pre, u, past, g,
                                  a.num_pages, bar_k, status);
-        else
+        else if (tid == 0)
             issue_qk_loads<D>(sb, &tm_q, &tm_k, h, g, q0, s0 + (u - n_ct) * 128, with_q, bar_k);
     };
     auto load_v = [&](int u) {
         if (PAST && u < n_ct)
             cached_tile_loads<D>(sb, sb + L::kV, &tm_vp, &tm_q, false, h, q0, pt_row, pid_s, n_pre, u, past, g,
                                  a.num_pages, bar_v, status);
-        else
+        else if (tid == 0)
             issue_v_loads<D>(sb, &tm_v, g, s0 + (u - n_ct) * 128, bar_v);
     };
     if (tid == 0) {
@@ -995,10 +993,11 @@ __global__ void __launch_bounds__(128, 2)
         mbar_init(bar_o, 1);
         mbar_init(bar_v, 1);
         fence_mbar_init();
-        if (!a.early) {
-            load_k(0, true);
-            load_v(0);
-        }
+    }
+    if (warp == 0 && !a.early) {
+        __syncwarp();  // the barriers are set up
+        load_k(0, true);
+        load_v(0);
     }
     if (warp == 0) tc::tmem_alloc(sb + L::kTmemSlot, 256);
     tc::fence_before();
@@ -1007,7 +1006,7 @@ __global__ void __launch_bounds__(128, 2)
     if (a.early) {  // the job is set up; q, k, v, the pools and out only now
         asm volatile("griddepcontrol.wait;" ::: "memory");
         asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-        if (tid == 0) {
+        if (warp == 0) {
             load_k(0, true);
             load_v(0);
         }
@@ -1038,7 +1037,7 @@ __global__ void __launch_bounds__(128, 2)
         mbar_wait(bar_s, ph, status);
         tc::fence_after();
         // S has read K: the next key tile's K
-        if (tid == 0 && u + 1 < n_tiles) load_k(u + 1, false);
+        if (warp == 0 && u + 1 < n_tiles) load_k(u + 1, false);
         int n_ok;
         if (cached) {
             // every cached position before `past` is visible to every new row
@@ -1113,7 +1112,7 @@ __global__ void __launch_bounds__(128, 2)
         }
         mbar_wait(bar_o, ph, status);
         tc::fence_after();
-        if (tid == 0 && u + 1 < n_tiles) load_v(u + 1);
+        if (warp == 0 && u + 1 < n_tiles) load_v(u + 1);
     }
     // staged in the dead Q buffer (the page write may still read K and V)
     store_rows_staged<D>(t_row + col_o, l, sb + L::kQ, a.out, a.hq, h, q0, min(128, s1 - q0), tid);

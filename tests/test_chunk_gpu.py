@@ -93,3 +93,25 @@ def test_bad_history_length_is_reported():
     with pytest.raises(qa.QAError) as e:
         run_chunk(w, debug_checks=True)
     assert e.value.status == -6 and "bad length" in str(e.value)
+
+
+
+@pytest.mark.parametrize("cached_page", [0, 9])
+def test_bad_cached_page_id_is_reported_not_faulted(cached_page):
+    # a cached page id outside the pool: reported, that page not loaded, and
+    # the request that does not use it still right.  Page 0 sits in the first
+    # cached key tile, page 9 in the second (each tile's page boxes are
+    # requested from separate lanes).
+    w = _workload(630 + cached_page, (200, 40), (20, 7))
+    w["page_table"] = w["page_table"].copy()
+    w["page_table"][0, cached_page] = w["num_pages"] + 3
+    with pytest.raises(qa.QAError) as e:
+        run_chunk(w, debug_checks=True)
+    assert e.value.status == -6 and "bad page" in str(e.value)
+    assert qa.qa_device_status() == 0  # cleared
+    out, _ = run_chunk(w)
+    qa.qa_device_status()  # clear this call's report too
+    r0, r1 = int(w["cu_seqlens"][1]), int(w["cu_seqlens"][2])
+    ref = oracle.prefill_chunk(w["q"][r0:r1], w["k"][r0:r1], w["v"][r0:r1], np.array([0, r1 - r0], np.int32),
+                               w["n_past"][1:2], w["page_table"][1:2], w["k_pages"], w["v_pages"])
+    assert_close(f64(out)[r0:r1], ref, "the request without the bad page")

@@ -386,6 +386,16 @@ int qa_window_plan(const int32_t *token_counts, int n_requests, int window_token
  * (QA_DEVICE_*), 0 when nothing went wrong, or -1 on a CUDA error. */
 int qa_device_status(void *stream);
 
+/* Exercises the failure path of the kernels' waits without a fault: launches
+ * one CTA (asynchronous on `stream`) that waits, through the same bounded
+ * wait the attention kernels use, on a barrier that nothing ever completes.
+ * The wait gives up after limit_us microseconds (1 .. 1000000; the kernels
+ * themselves give up after 2 s), sets QA_DEVICE_TIMEOUT in the device status
+ * word and the kernel ends; the context stays usable.  Read the bit with
+ * qa_device_status().  INVALID_PARAMS for a limit outside that range,
+ * LAUNCH_FAILED on a launch error. */
+qa_status qa_check_bounded_wait(unsigned int limit_us, void *stream);
+
 /* Thread-local message describing the last failure on this thread; valid
  * until the next qa_* call on the same thread.  Never NULL. */
 const char *qa_last_error(void);

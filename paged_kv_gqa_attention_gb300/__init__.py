@@ -22,7 +22,7 @@ import numpy as np
 __all__ = [
     "QA_ABI_VERSION", "QAError", "lib_path", "qa_version", "qa_last_error", "qa_attn_default_params",
     "qa_decode_workspace_size", "qa_decode_attn", "qa_prefill_attn", "qa_window_attn", "qa_window_plan",
-    "qa_device_status", "DEVICE_STATUS_BITS", "qa_decode_attn_noalloc",
+    "qa_device_status", "DEVICE_STATUS_BITS", "qa_decode_attn_noalloc", "qa_check_bounded_wait",
 ]
 
 QA_ABI_VERSION = 1
@@ -95,6 +95,8 @@ def _load():
     lib.qa_window_plan.argtypes = [P, I, I, P, I]
     lib.qa_device_status.restype = I
     lib.qa_device_status.argtypes = [P]
+    lib.qa_check_bounded_wait.restype = I
+    lib.qa_check_bounded_wait.argtypes = [ctypes.c_uint, P]
     lib.qa_last_error.restype = ctypes.c_char_p
     lib.qa_last_error.argtypes = []
     lib.qa_version.restype = ctypes.c_char_p
@@ -468,6 +470,13 @@ def qa_window_plan(token_counts, window_tokens: int = 0) -> np.ndarray:
     if n < 0:
         raise QAError("qa_window_plan", -1, qa_last_error())
     return cu[: n + 1]
+
+
+def qa_check_bounded_wait(limit_us=20000, stream=None) -> None:
+    """Launches one CTA whose bounded wait (the one the kernels use) gives up
+    after limit_us microseconds on a barrier that nothing completes, setting
+    QA_DEVICE_TIMEOUT (read it with qa_device_status); the kernel then ends."""
+    _check("qa_check_bounded_wait", _lib.qa_check_bounded_wait(int(limit_us), _stream_ptr(stream)))
 
 
 def qa_device_status(stream=None) -> int:

@@ -670,7 +670,26 @@ __global__ void __launch_bounds__((kMaxHkv + 1) * 32, 1) decode_splitk_kernel(co
     }
 }
 
+// One CTA waits on a barrier that nothing ever completes: the bounded wait
+// the kernels use must give up after limit_ns, set QA_DEVICE_TIMEOUT in this
+// file's status word and let the kernel end (qa_check_bounded_wait).
+__global__ void bounded_wait_check_kernel(unsigned long long limit_ns) {
+    __shared__ __align__(8) unsigned long long bar;
+    const uint32_t b = smem_u32(&bar);
+    if (threadIdx.x == 0) {
+        mbar_init(b, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    mbar_wait(b, 0, &g_status, limit_ns);
+}
+
 }  // namespace
+
+cudaError_t launch_bounded_wait_check(unsigned int limit_us, cudaStream_t stream) {
+    bounded_wait_check_kernel<<<1, 32, 0, stream>>>((unsigned long long)limit_us * 1000ull);
+    return cudaGetLastError();
+}
 
 int decode_grid_ctas(int device) {
     int sms = 0;

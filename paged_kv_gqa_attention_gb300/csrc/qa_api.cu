@@ -352,6 +352,16 @@ QA_API int qa_device_status(void *stream) {
     return (int)bits;
 }
 
+QA_API qa_status qa_check_bounded_wait(unsigned int limit_us, void *stream) {
+    clear_error();
+    if (limit_us < 1 || limit_us > 1000000u)
+        return fail(QA_STATUS_INVALID_PARAMS, "qa_check_bounded_wait: limit_us %u outside [1, 1000000]", limit_us);
+    const cudaError_t e = qa::launch_bounded_wait_check(limit_us, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return fail(QA_STATUS_LAUNCH_FAILED, "qa_check_bounded_wait: CUDA error %s", cudaGetErrorString(e));
+    return QA_STATUS_OK;
+}
+
 QA_API const char *qa_last_error(void) { return t_last_error; }
 
 QA_API const char *qa_version(void) {

@@ -31,6 +31,8 @@ cudaError_t launch_decode(const void *q, const void *k_pages, const void *v_page
                           const qa_attn_params &p, float scale, int ctas, cudaStream_t stream,
                           const DecodeAppend *app = nullptr);
 unsigned int status_read_clear_decode(cudaStream_t stream, cudaError_t *err);
+// one CTA whose bounded wait expires after limit_us (decode.cu's status word)
+cudaError_t launch_bounded_wait_check(unsigned int limit_us, cudaStream_t stream);
 
 // ---- prefill (prefill.cu): causal attention with the KV page write fused in
 // n_past: cached positions per request (chunked prefill), or nullptr (none)

@@ -217,3 +217,11 @@ def test_stable_metadata_levels_are_checked(libqa):
     p.abi_version = 1  # ABI 1 callers have no such field: the value is ignored
     assert "stable_metadata" not in (qa._lib.qa_decode_attn(fake, fake, fake, fake, fake, 1, fake, ctypes.byref(p)),
                                      qa.qa_last_error())[1]
+
+
+def test_bounded_wait_check_rejects_bad_limits_without_device(libqa):
+    import paged_kv_gqa_attention_gb300 as qa
+
+    for limit in (0, 1000001):
+        assert qa._lib.qa_check_bounded_wait(limit, None) == -1
+        assert "limit_us" in qa.qa_last_error()

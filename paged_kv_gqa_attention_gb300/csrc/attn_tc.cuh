@@ -33,7 +33,7 @@
 //      MMA, K = 128 keys in steps of 16, V read MN-major).
 // After the last key tile each row of O is read back, divided by its softmax
 // sum, rounded to bf16 and staged in shared memory; the window kernel writes
-// the stage out with TMA stores of 8-row boxes (store_rows_tma), the prefill
+// the stage out with TMA stores of 32-row boxes (store_rows_tma), the prefill
 // with whole rows per warp store (store_rows_staged).
 //
 // Masks.  Window: key j is visible to row i iff both lie in the segment.
@@ -358,12 +358,16 @@ __device__ __forceinline__ void store_rows_staged(uint32_t o_row, float l, uint3
     }
 }
 
+// Rows per output TMA store box (the window output tensor map's box height):
+// a 104-row window leaves in three boxes plus eight rows of plain stores.
+constexpr int kOutBoxRows = 32;
+
 // Epilogue through TMA stores: thread r stages its row of O (divided by l,
 // bf16) sub-tile by sub-tile -- dims [64 sd, 64 sd + 64) of row r at stage +
 // sd * 16 KiB + r * 128 with its 16-byte chunks XOR-swizzled by r, which is
 // the layout of a 128B-swizzled TMA box of 8 rows x 64 dims -- then thread 0
-// writes the rows of whole 8-row boxes with TMA stores (tensor map tm_out,
-// box {64, 1, 8}; tracked by its bulk group: wait for their reads of shared
+// writes the rows of whole 32-row boxes with TMA stores (tensor map tm_out,
+// box {64, 1, kOutBoxRows}; tracked by its bulk group: wait for their reads of shared
 // memory before the stage is reused) and the threads of the remaining rows
 // (< 8) store theirs.  Rows at or past row_end are not written.
 // CTA-collective (128 threads).
@@ -393,9 +397,9 @@ __device__ __forceinline__ void store_rows_tma(uint32_t o_row, float l, uint32_t
     tc::fence_proxy_async_smem();  // the staged rows are read by the TMA unit
     __syncthreads();
     const int n_rows = min(128, row_end);
-    const int full = n_rows / 8 * 8;
+    const int full = n_rows / kOutBoxRows * kOutBoxRows;
     if (r == 0 && full > 0) {
-        for (int i = 0; i < full; i += 8)
+        for (int i = 0; i < full; i += kOutBoxRows)
 #pragma unroll
             for (int sd = 0; sd < D / 64; ++sd)
                 tc::tma_store_3d(tm_out, stage + sd * tc::kSubTileBytes + (uint32_t)i * 128u, sd * 64, h, q0 + i);
@@ -574,7 +578,7 @@ __device__ __forceinline__ void issue_v_loads(uint32_t sb, const CUtensorMap *tm
 // Q and K are requested as soon as the current job's last P V has finished
 // reading shared memory, so they load during the epilogue; the epilogue
 // stages the output rows in the V buffer and writes whole rows per store
-// (store_rows_tma: 8-row TMA stores), after which the next job's V is
+// (store_rows_tma: 32-row TMA stores), after which the next job's V is
 // requested.  Each job
 // is computed as described at the top of this file.  TMEM: 128 columns when
 // every job of the CTA is a single 128-row tile and D = 64 (four CTAs share

@@ -35,7 +35,7 @@ cudaError_t launch_window(const void *q, const void *k, const void *v, const int
         !make_rows_tmap(&tv, v, p.head_dim, p.n_kv_heads, total_tokens))
         return cudaErrorInvalidValue;
     // the output is written in 8-row TMA boxes (store_rows_tma)
-    if (!make_rows_tmap(&tout, out, p.head_dim, p.n_q_heads, total_tokens, 8)) return cudaErrorInvalidValue;
+    if (!make_rows_tmap(&tout, out, p.head_dim, p.n_q_heads, total_tokens, kOutBoxRows)) return cudaErrorInvalidValue;
     AttnTcArgs a{};
     a.cu = cu_windows;
     a.out = static_cast<uint16_t *>(out);

@@ -31,11 +31,11 @@ def test_small_windows(counts):
 
 @pytest.mark.parametrize("d", [64, 128])
 def test_window_sizes_around_the_store_boxes(d):
-    # the output leaves in boxes of 8 rows plus the rows of a partial box:
-    # window sizes 1..17 and 127..129 around those boundaries, every row
-    # checked; the output starts NaN-filled, so a row left unwritten (or
-    # overwritten by a neighbouring window's box) fails
-    sizes = [1, 2, 7, 8, 9, 15, 16, 17, 127, 128, 129]
+    # the output leaves in whole row boxes plus the rows of a partial box:
+    # window sizes around multiples of 8, 16 and 32 rows and around the
+    # 128-row tile, every row checked; the output starts NaN-filled, so a row
+    # left unwritten (or overwritten by a neighbouring window's box) fails
+    sizes = [1, 2, 7, 8, 9, 15, 16, 17, 31, 32, 33, 63, 64, 65, 95, 96, 97, 103, 104, 105, 127, 128, 129]
     T = sum(sizes)
     w = wl.window_workload(350 + d, (T,), h=3, d=d)
     cu = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)

@@ -365,12 +365,13 @@ constexpr int kOutBoxRows = 32;
 // Epilogue through TMA stores: thread r stages its row of O (divided by l,
 // bf16) sub-tile by sub-tile -- dims [64 sd, 64 sd + 64) of row r at stage +
 // sd * 16 KiB + r * 128 with its 16-byte chunks XOR-swizzled by r, which is
-// the layout of a 128B-swizzled TMA box of 8 rows x 64 dims -- then thread 0
-// writes the rows of whole 32-row boxes with TMA stores (tensor map tm_out,
-// box {64, 1, kOutBoxRows}; tracked by its bulk group: wait for their reads of shared
-// memory before the stage is reused) and the threads of the remaining rows
-// (< 8) store theirs.  Rows at or past row_end are not written.
-// CTA-collective (128 threads).
+// the layout of a 128B-swizzled TMA box of 64 dims (8-row swizzle atoms
+// stacked) -- then thread 0 writes the rows of whole kOutBoxRows-row boxes
+// with TMA stores (tensor map tm_out, box {64, 1, kOutBoxRows}; tracked by
+// its bulk group: wait for their reads of shared memory before the stage is
+// reused) and the threads of the remaining rows (< kOutBoxRows) store
+// theirs.  Rows at or past row_end are not written.  CTA-collective (128
+// threads).
 template <int D>
 __device__ __forceinline__ void store_rows_tma(uint32_t o_row, float l, uint32_t stage, const CUtensorMap *tm_out,
                                                uint16_t *out, int hq, int h, int q0, int row_end) {

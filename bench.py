@@ -206,6 +206,28 @@ def graph_time(fns, steps, warmup, stream, sampler=None, max_per_graph=64):
     return e0.elapsed_time(e1) / 1e3, clocks
 
 
+def lone_call_time(call, copies, stream, device, n=50):
+    """Median device time of one call with no neighbour to overlap: before
+    each call the stream writes 512 MiB (evicting L2 and giving the host
+    time to queue the call), then CUDA events bracket the call alone."""
+    import torch
+
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=device)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for i in range(3):  # warm-up
+            call(copies[i % len(copies)])
+        for i, (a, b) in enumerate(ev):
+            flush.fill_(i & 0xFF)
+            a.record(stream)
+            call(copies[i % len(copies)])
+            b.record(stream)
+    torch.cuda.synchronize()
+    del flush
+    return statistics.median(a.elapsed_time(b) for a, b in ev) / 1e3
+
+
 # ------------------------------------------------------------------ arms
 def cpu_oracle_decode(w, rank_threads=None, n_req=None):
     """The fp64 oracle over the decode workload (its first n_req requests,
@@ -222,6 +244,110 @@ def cpu_oracle_decode(w, rank_threads=None, n_req=None):
 
 
 REFERENCE_BUDGET_S = 120.0  # the timed steps of the reference arm, at most
+CPU_LEG_BUDGET_S = 1.0  # one timed run of a cpu_baseline leg, about
+
+
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        fields = {}
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if ":" in line:
+                    k, v = line.split(":", 1)
+                    fields.setdefault(k.strip().lower(), v.strip())
+        if "model name" in fields:
+            return fields["model name"]
+        return f"implementer {fields.get('cpu implementer', '?')} part {fields.get('cpu part', '?')}"
+    except Exception:
+        return "unknown"
+
+
+def cpu_leg(run, work, n_units, unit_name, unit, scale, what):
+    """The fp64 oracle on this host, once single-threaded and once on every
+    core.  run(n, threads) runs it over the first n units of the workload;
+    work(n) is their algorithmic bytes or flops.  For each thread count the
+    sample grows from one unit until a run takes 0.1 s (or covers the whole
+    workload), is then sized to about CPU_LEG_BUDGET_S, and the median of
+    three runs of it is reported as work / time / scale."""
+    legs = {}
+    for threads in (1, os.cpu_count() or 1):
+        def timed(n):
+            t0 = time.perf_counter()
+            run(n, threads)
+            return time.perf_counter() - t0
+
+        n = 1
+        while True:
+            t = timed(n)
+            if t >= 0.1 or n >= n_units:
+                break
+            n = min(n_units, n * 4)
+        n = int(min(n_units, max(n, n * CPU_LEG_BUDGET_S / max(t, 1e-6))))
+        med = statistics.median(timed(n) for _ in range(3))
+        legs[f"threads_{threads}"] = {
+            "value": round(work(n) / med / scale, 4), "unit": unit, "threads": threads, "seconds": round(med, 4),
+            "sample": f"first {n} of {n_units} {unit_name}" if n < n_units else f"all {n_units} {unit_name}"}
+    return {"workload": what, **legs}
+
+
+def cpu_leg_decode(w, what):
+    import oracle
+
+    hq = w["q"].shape[1]
+
+    def run(n, threads):
+        rows = None if n >= len(w["seq_lens"]) else np.arange(n * hq, dtype=np.int32)
+        oracle.decode(w["q"], w["k_pages"], w["v_pages"], w["page_table"], w["seq_lens"], rows=rows,
+                      n_threads=threads)
+
+    return cpu_leg(run, lambda n: decode_bytes(w["seq_lens"][:n], hq=hq, hkv=w["k_pages"].shape[2]),
+                   len(w["seq_lens"]), "requests (every query head)", "GB/s", 1e9, what)
+
+
+def cpu_leg_prefill(w, what):
+    import oracle
+
+    cu, hq = w["cu_seqlens"], w["q"].shape[1]
+
+    def run(n, threads):
+        rows = None if n >= len(cu) - 1 else np.arange(int(cu[n]) * hq, dtype=np.int32)
+        oracle.prefill(w["q"], w["k"], w["v"], cu, rows=rows, n_threads=threads)
+
+    return cpu_leg(run, lambda n: prefill_flops(np.diff(cu)[:n], hq=hq), len(cu) - 1,
+                   "requests (every token and query head)", "GFLOP/s", 1e9, what)
+
+
+def cpu_leg_window(w, cu, what):
+    import oracle
+
+    h = w["q"].shape[1]
+
+    def run(n, threads):
+        rows = None if n >= len(cu) - 1 else np.arange(int(cu[n]) * h, dtype=np.int32)
+        oracle.window(w["q"], w["k"], w["v"], cu, rows=rows, n_threads=threads)
+
+    return cpu_leg(run, lambda n: window_flops(cu[:n + 1], h=h), len(cu) - 1, "windows (every token and head)",
+                   "GFLOP/s", 1e9, what)
+
+
+def cpu_leg_tiny(w, what):
+    import oracle
+
+    def run(n, threads):
+        oracle.prefill(w["q"], w["k"], w["v"], w["cu_seqlens"], n_threads=threads)
+        kp, vp = oracle.page_write(w["k"], w["v"], w["cu_seqlens"], w["page_table"], w["k_pages"], w["v_pages"])
+        oracle.decode(w["decode_q"], kp, vp, w["page_table"], w["seq_lens"], n_threads=threads)
+
+    # reported as steps per second: one step is the prefill of 64 tokens, its page write and one decode token
+    return cpu_leg(run, lambda n: n, 1, "steps", "steps/s", 1.0, what)
 
 
 def run_reference(args, world, rank):
@@ -347,6 +473,11 @@ def run_ours(args, world, rank, local_rank):
                                 "ms_per_step": round(el / args.steps * 1e3, 5)}
     by_level["note"] = ("the same calls at stable_metadata 0 (everything read after the wait) and 1 (lengths and "
                         "page table read before it); the headline uses 2 (first pool pages streamed before it too)")
+    lone = lone_call_time(lambda c: mk(c, 0)(), copies, stream, device)
+    lone_call = {"value": round(nbytes / lone / 1e9, 2), "unit": "GB/s", "us_per_call": round(lone * 1e6, 3),
+                 "frac": round(nbytes / lone / 1e9 / peaks["hbm"], 4),
+                 "mode": "one call at a time (stable_metadata 0): 512 MiB written before each call to evict L2, "
+                         "then CUDA events around the call alone; median of 50 calls"}
 
     # ---------------- end to end: host buffers, copies inside the timed region
     # a step's inputs (q, page table, lengths) sit side by side in one pinned
@@ -458,7 +589,7 @@ def run_ours(args, world, rank, local_rank):
                                   "eager_calls": {"value": round(e2e_eager_value, 3), "unit": "GB/s",
                                                   "ms_per_step": round(e2e_eager_elapsed / e2e_steps * 1e3, 4)}},
         "gpu_launches": args.steps, "roofline": roofline,
-        "tokens_per_s": round(B / per_call * world, 1), "by_stable_metadata": by_level,
+        "tokens_per_s": round(B / per_call * world, 1), "by_stable_metadata": by_level, "lone_call": lone_call,
     }
     del copies
     torch.cuda.empty_cache()
@@ -467,13 +598,18 @@ def run_ours(args, world, rank, local_rank):
     unknown = set(rows) - set(ROW_NAMES)
     if unknown:
         raise SystemExit(f"unknown rows: {sorted(unknown)}")
+    # the oracle on this host's cores (rank 0 of a single-GPU run only)
+    cpu = {} if (rank == 0 and world == 1 and not args.no_cpu) else None
     if rows:
-        line["rows"] = measure_rows(qa, device, stream, peaks, args, rows)
+        line["rows"] = measure_rows(qa, device, stream, peaks, args, rows, cpu)
 
-    if rank == 0 and not args.no_cpu:
-        t, cores = cpu_oracle_decode(w)
-        line["cpu_baseline"] = {"value": round(nbytes / t / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
-                                "sample": "whole batched-decode workload once (32 requests x 16 heads), fp64"}
+    if cpu is not None:
+        cpu["decode_0p6b"] = cpu_leg_decode(w, "batched decode 0.6B: 32 requests, L~U[200,2000]")
+        head = cpu["decode_0p6b"][f"threads_{os.cpu_count() or 1}"]
+        line["cpu_baseline"] = {"value": head["value"], "unit": "GB/s", "cores": head["threads"], "kind": "oracle",
+                                "sample": f"batched decode 0.6B, {head['sample']}, fp64, median of 3 runs",
+                                "cpu_model": cpu_model(), "cpu_count": os.cpu_count(),
+                                "configs": cpu}
     if rank == 0:
         print(json.dumps(line))
 
@@ -482,21 +618,22 @@ ROW_NAMES = ("prefill", "chunk_prefill", "window", "decode_long", "decode_step",
              "tiny")
 
 
-def measure_rows(qa, device, stream, peaks, args, which=ROW_NAMES):
+def measure_rows(qa, device, stream, peaks, args, which=ROW_NAMES, cpu=None):
     """The other hot-path operations, each timed the same way (graphs of
-    back-to-back calls, inputs in HBM, above L2 or rotated)."""
+    back-to-back calls, inputs in HBM, above L2 or rotated).  With a `cpu`
+    dict, the oracle's legs for the named workloads go there too."""
     import torch
 
     rows = {}
     steps = max(20, min(args.steps, 400))
     if "prefill" in which:
-        _row_prefill(qa, device, stream, peaks, steps, rows)
+        _row_prefill(qa, device, stream, peaks, steps, rows, cpu)
     if "chunk_prefill" in which:
         _row_chunk_prefill(qa, device, stream, peaks, steps, rows)
     if "window" in which:
-        _row_window(qa, device, stream, peaks, steps, rows)
+        _row_window(qa, device, stream, peaks, steps, rows, cpu)
     if "decode_long" in which:
-        _row_decode_long(qa, device, stream, peaks, steps, rows)
+        _row_decode_long(qa, device, stream, peaks, steps, rows, cpu)
     if "decode_step" in which:
         _row_decode_step(qa, device, stream, peaks, steps, rows)
     if "cross_decode" in which:
@@ -504,7 +641,7 @@ def measure_rows(qa, device, stream, peaks, args, which=ROW_NAMES):
     if "decode_graph" in which:
         _row_decode_graph(qa, device, stream, peaks, steps, rows)
     if "tiny" in which:
-        _row_tiny(qa, device, stream, steps, rows)
+        _row_tiny(qa, device, stream, steps, rows, cpu)
     status = qa.qa_device_status(stream)
     if status:
         raise RuntimeError(f"device status {status:#x} after the row measurements")
@@ -512,7 +649,7 @@ def measure_rows(qa, device, stream, peaks, args, which=ROW_NAMES):
     return rows
 
 
-def _row_prefill(qa, device, stream, peaks, steps, rows):
+def _row_prefill(qa, device, stream, peaks, steps, rows, cpu=None):
     """Ragged causal prefill with page write (16 requests, ~3.6K tokens)."""
     import torch
 
@@ -540,6 +677,8 @@ def _row_prefill(qa, device, stream, peaks, steps, rows):
                        "frac_hbm": round(by / t / 1e9 / peaks["hbm"], 4), "flops": fl, "bytes": by,
                        "gpu_launches_per_call": 1, "stable_metadata": 1,
                        "us_per_call_stable_metadata_0": round(el0 / steps * 1e6, 2)}
+    if cpu is not None:
+        cpu["prefill_bucket"] = cpu_leg_prefill(w, "ragged causal prefill: 16 requests, ceil(13 d)+40 tokens")
 
 
 def _row_chunk_prefill(qa, device, stream, peaks, steps, rows):
@@ -573,7 +712,7 @@ def _row_chunk_prefill(qa, device, stream, peaks, steps, rows):
                              "us_per_call_stable_metadata_0": round(el0 / steps * 1e6, 2)}
 
 
-def _row_window(qa, device, stream, peaks, steps, rows):
+def _row_window(qa, device, stream, peaks, steps, rows, cpu=None):
     """AuT windowed attention (8 requests, ~70K tokens, 14 x 64)."""
     import torch
 
@@ -598,9 +737,11 @@ def _row_window(qa, device, stream, peaks, steps, rows):
                       "frac_bf16_peak": round(fl / t / 1e12 / peaks["bf16"], 4),
                       "frac_hbm": round(by / t / 1e9 / peaks["hbm"], 4), "flops": fl, "bytes": by,
                       "gpu_launches_per_call": 1}
+    if cpu is not None:
+        cpu["window_aut"] = cpu_leg_window(w, cu, "AuT windowed attention: 8 requests, 104-token windows, 14 x 64")
 
 
-def _row_decode_long(qa, device, stream, peaks, steps, rows):
+def _row_decode_long(qa, device, stream, peaks, steps, rows, cpu=None):
     """Long-context decode 1.7B (64 requests, ~9K tokens each)."""
     import torch
 
@@ -623,6 +764,8 @@ def _row_decode_long(qa, device, stream, peaks, steps, rows):
                            "tokens_per_s": round(B / t, 1), "gpu_launches_per_call": 1, "stable_metadata": 2}
     del c
     torch.cuda.empty_cache()
+    if cpu is not None:
+        cpu["decode_1p7b"] = cpu_leg_decode(w, "long-context decode 1.7B: 64 requests, L~U[2000,16000]")
 
 
 def append_bytes(batch, hq=16, hkv=8, d=128):
@@ -762,7 +905,7 @@ def _row_decode_graph(qa, device, stream, peaks, steps, rows):
     torch.cuda.empty_cache()
 
 
-def _row_tiny(qa, device, stream, steps, rows):
+def _row_tiny(qa, device, stream, steps, rows, cpu=None):
     """Tiny: prefill of 64 tokens then one decode token (latency)."""
     import torch
 
@@ -784,6 +927,8 @@ def _row_tiny(qa, device, stream, steps, rows):
     rows["tiny"] = {"workload": "tiny: prefill of 64 tokens into 4 permuted pages, then 1 decode token",
                     "us_per_step": round(el / steps * 1e6, 2), "note": "latency-bound; no roofline fraction",
                     "gpu_launches_per_step": 2}
+    if cpu is not None:
+        cpu["tiny"] = cpu_leg_tiny(w, "tiny: prefill of 64 tokens, its page write, then 1 decode token")
 
 
 def main():

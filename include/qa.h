@@ -197,9 +197,11 @@ qa_status qa_decode_attn(const void *q, const void *k_pages, const void *v_pages
  *     last call's contents; the only part that must start at zero (the
  *     per-request arrival counters) starts zeroed and every call leaves it
  *     zeroed, so nothing needs clearing between calls.
- *   - The first call made with a given device current looks up the array's
- *     device address and caches it; make that first call before any CUDA
- *     stream capture begins. */
+ *   - Every call looks up the array's device address on the current device
+ *     (cudaGetSymbolAddress) and hands it to the kernel; nothing is cached,
+ *     so a cudaDeviceReset between calls does not leave a stale address.
+ *   - Argument checks are those of qa_decode_attn (stable_metadata included),
+ *     except that there is no workspace to check. */
 qa_status qa_decode_attn_noalloc(const void *q, const void *k_pages, const void *v_pages,
                                  const int32_t *page_table, const int32_t *seq_lens, int batch,
                                  void *out, const qa_attn_params *params);

@@ -25,7 +25,6 @@ __all__ = [
     "qa_device_status", "DEVICE_STATUS_BITS", "qa_decode_attn_noalloc", "qa_check_bounded_wait",
 ]
 
-QA_ABI_VERSION = 1
 _PKG = os.path.dirname(os.path.abspath(__file__))
 lib_path = os.path.join(_PKG, "libqa.so")
 
@@ -105,6 +104,10 @@ def _load():
 
 
 _lib = _load()
+
+# The library's ABI version (include/qa.h QA_ABI_VERSION), read from the
+# library's own defaults so the two cannot disagree.
+QA_ABI_VERSION = int(_lib.qa_attn_default_params().abi_version)
 
 
 def qa_version() -> str:
@@ -218,9 +221,7 @@ def qa_decode_attn_noalloc(q, k_pages, v_pages, page_table, seq_lens, out=None, 
     device memory: the split-K scratch is a fixed 4 MiB array inside the
     library, shared by every call on the device (calls that overlap on the
     GPU race on it; calls ordered on one stream are fine).  Batches whose
-    scratch would not fit are rejected.  The first call on each device looks
-    up the array's address, so make it before any stream capture.  With
-    out=None the output tensor is allocated here by torch; pass `out` to keep
+    scratch would not fit are rejected.  With out=None the output tensor is allocated here by torch; pass `out` to keep
     the call allocation-free."""
     torch = _torch()
     B, Hq, D = q.shape

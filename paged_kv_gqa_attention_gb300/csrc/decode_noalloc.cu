@@ -21,12 +21,13 @@
 // the array and every call leaves the counters it used at zero again; the
 // partial results behind them are always written before they are read.
 //
-// Set-up: the device address of the array is looked up (cudaGetSymbolAddress)
-// on the first call made with each device current and cached per device, so
-// that first call should be made before any CUDA stream capture begins.
+// Set-up: every call looks up the device address of the array on the current
+// device (cudaGetSymbolAddress) and passes it to the kernel.  Host code cannot
+// name the array directly (its host-side name is only a stand-in), and the
+// address is not cached: it belongs to the module loaded in the current
+// context, which a cudaDeviceReset replaces.
 #include <cuda_runtime.h>
 #include <math.h>
-#include <mutex>
 #include <stdarg.h>
 #include <stdint.h>
 #include <stdio.h>
@@ -41,10 +42,6 @@ namespace {
 constexpr size_t kScratchBytes = (size_t)4 << 20;
 static __device__ __align__(256) unsigned char g_decode_scratch[kScratchBytes];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_setup_mutex;
-void *g_scratch_ptr[kMaxDevices] = {nullptr};
-
 qa_status reject(qa_status st, const char *fmt, ...) __attribute__((format(printf, 2, 3)));
 qa_status reject(qa_status st, const char *fmt, ...) {
     char msg[512];
@@ -56,28 +53,6 @@ qa_status reject(qa_status st, const char *fmt, ...) {
     return st;
 }
 
-bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
-
-// Device address of the scratch array on the current device (set up once per
-// device).  Returns nullptr and fills *err on failure.
-void *scratch_on_current_device(cudaError_t *err) {
-    int dev = 0;
-    *err = cudaGetDevice(&dev);
-    if (*err != cudaSuccess) return nullptr;
-    if (dev < 0 || dev >= kMaxDevices) {
-        *err = cudaErrorInvalidDevice;
-        return nullptr;
-    }
-    std::lock_guard<std::mutex> lock(g_setup_mutex);
-    if (!g_scratch_ptr[dev]) {
-        void *p = nullptr;
-        *err = cudaGetSymbolAddress(&p, g_decode_scratch);
-        if (*err != cudaSuccess) return nullptr;
-        g_scratch_ptr[dev] = p;
-    }
-    return g_scratch_ptr[dev];
-}
-
 }  // namespace
 
 QA_API qa_status qa_decode_attn_noalloc(const void *q, const void *k_pages, const void *v_pages,
@@ -85,31 +60,10 @@ QA_API qa_status qa_decode_attn_noalloc(const void *q, const void *k_pages, cons
                                         const qa_attn_params *p) {
     const char *fn = "qa_decode_attn_noalloc";
     qa::set_last_error("");
-    if (!p) return reject(QA_STATUS_INVALID_PARAMS, "%s: params is NULL", fn);
-    if (p->abi_version < QA_ABI_MIN_VERSION || p->abi_version > QA_ABI_VERSION)
-        return reject(QA_STATUS_INVALID_PARAMS, "%s: abi_version %d outside [%d, %d]", fn, p->abi_version,
-                      QA_ABI_MIN_VERSION, QA_ABI_VERSION);
-    if (!(p->scale >= 0.f) || !isfinite(p->scale))
-        return reject(QA_STATUS_INVALID_PARAMS, "%s: scale must be finite and >= 0 (0 = 1/sqrt(head_dim))", fn);
-    if (p->head_dim != 128 || p->page_size != 16 || p->n_kv_heads < 1 || p->n_kv_heads > 8 ||
-        (p->n_q_heads != p->n_kv_heads && p->n_q_heads != 2 * p->n_kv_heads))
-        return reject(QA_STATUS_INVALID_PARAMS,
-                      "%s: unsupported shape (head_dim 128, page_size 16, n_kv_heads 1..8, n_q_heads = 1 or 2 x "
-                      "n_kv_heads)",
-                      fn);
-    if (p->num_pages < 1 || p->max_pages_per_seq < 1 || (long long)p->max_pages_per_seq * p->page_size > 0x7fffffffLL)
-        return reject(QA_STATUS_INVALID_PARAMS, "%s: num_pages and max_pages_per_seq must be >= 1 (and fit int32)", fn);
-    if (!q || !k_pages || !v_pages || !page_table || !seq_lens || !out)
-        return reject(QA_STATUS_INVALID_PARAMS, "%s: NULL tensor pointer", fn);
-    if (batch < 1 || batch > qa::kDecodeMaxBatch)
-        return reject(QA_STATUS_INVALID_PARAMS, "%s: batch %d outside [1, %d]", fn, batch, qa::kDecodeMaxBatch);
-    if (!aligned(q, 16) || !aligned(k_pages, 16) || !aligned(v_pages, 16) || !aligned(out, 16) ||
-        !aligned(page_table, 4) || !aligned(seq_lens, 4))
-        return reject(QA_STATUS_INVALID_PARAMS, "%s: tensors must be 16-byte aligned (int32 arrays 4-byte)", fn);
-
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return reject(QA_STATUS_LAUNCH_FAILED, "%s: no CUDA device", fn);
-    const int ctas = qa::decode_grid_ctas(dev);
+    // the same checks as qa_decode_attn, minus its workspace
+    const qa_status st = qa::check_decode_call(fn, q, k_pages, v_pages, page_table, seq_lens, batch, out, p);
+    if (st != QA_STATUS_OK) return st;
+    const int ctas = qa::current_decode_ctas();
     if (ctas <= 0) return reject(QA_STATUS_LAUNCH_FAILED, "%s: no CUDA device", fn);
     const size_t need = qa::decode_workspace_bytes(batch, p->n_q_heads, p->head_dim, ctas);
     if (need > kScratchBytes)
@@ -118,9 +72,9 @@ QA_API qa_status qa_decode_attn_noalloc(const void *q, const void *k_pages, cons
                       "(use qa_decode_attn with a caller workspace for larger batches)",
                       fn, batch, p->n_q_heads, need, kScratchBytes);
 
-    cudaError_t e;
-    void *scratch = scratch_on_current_device(&e);
-    if (!scratch)
+    void *scratch = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&scratch, g_decode_scratch);
+    if (e != cudaSuccess || !scratch)
         return reject(QA_STATUS_LAUNCH_FAILED, "%s: cannot find the scratch array's device address: %s", fn,
                       cudaGetErrorString(e));
 

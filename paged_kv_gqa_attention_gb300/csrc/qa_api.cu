@@ -82,16 +82,36 @@ qa_status debug_status(unsigned int bits, cudaError_t e, const char *fn) {
     return QA_STATUS_OK;
 }
 
+}  // namespace
+
+namespace qa {
+
 int current_decode_ctas() {
     static int cache[64] = {0};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-    if (dev < 0 || dev >= 64) return qa::decode_grid_ctas(dev);
-    if (cache[dev] == 0) cache[dev] = qa::decode_grid_ctas(dev);
+    if (dev < 0 || dev >= 64) return decode_grid_ctas(dev);
+    if (cache[dev] == 0) cache[dev] = decode_grid_ctas(dev);
     return cache[dev];
 }
 
-}  // namespace
+qa_status check_decode_call(const char *fn, const void *q, const void *k_pages, const void *v_pages,
+                            const int32_t *page_table, const int32_t *seq_lens, int batch, const void *out,
+                            const qa_attn_params *p) {
+    qa_status st = check_common(p, fn);
+    if (st != QA_STATUS_OK) return st;
+    if ((st = check_gqa(p, fn)) != QA_STATUS_OK) return st;
+    if (!q || !k_pages || !v_pages || !page_table || !seq_lens || !out)
+        return fail(QA_STATUS_INVALID_PARAMS, "%s: NULL tensor pointer", fn);
+    if (batch < 1 || batch > kDecodeMaxBatch)
+        return fail(QA_STATUS_INVALID_PARAMS, "%s: batch %d outside [1, %d]", fn, batch, kDecodeMaxBatch);
+    if (!aligned(q, 16) || !aligned(k_pages, 16) || !aligned(v_pages, 16) || !aligned(out, 16) ||
+        !aligned(page_table, 4) || !aligned(seq_lens, 4))
+        return fail(QA_STATUS_INVALID_PARAMS, "%s: tensors must be 16-byte aligned (int32 arrays 4-byte)", fn);
+    return QA_STATUS_OK;
+}
+
+}  // namespace qa
 
 QA_API qa_attn_params qa_attn_default_params(void) {
     qa_attn_params p;
@@ -124,7 +144,7 @@ QA_API size_t qa_decode_workspace_size(int batch, int max_seq_len, const qa_attn
              max_seq_len);
         return 0;
     }
-    const int ctas = current_decode_ctas();
+    const int ctas = qa::current_decode_ctas();
     if (ctas <= 0) {
         fail(QA_STATUS_LAUNCH_FAILED, "qa_decode_workspace_size: no CUDA device");
         return 0;
@@ -138,17 +158,9 @@ namespace {
 qa_status decode_entry(const char *fn, const void *q, const void *k_pages, const void *v_pages,
                        const int32_t *page_table, const int32_t *seq_lens, int batch, void *out,
                        const qa_attn_params *p, const qa::DecodeAppend *app) {
-    qa_status st = check_common(p, fn);
+    qa_status st = qa::check_decode_call(fn, q, k_pages, v_pages, page_table, seq_lens, batch, out, p);
     if (st != QA_STATUS_OK) return st;
-    if ((st = check_gqa(p, fn)) != QA_STATUS_OK) return st;
-    if (!q || !k_pages || !v_pages || !page_table || !seq_lens || !out)
-        return fail(QA_STATUS_INVALID_PARAMS, "%s: NULL tensor pointer", fn);
-    if (batch < 1 || batch > qa::kDecodeMaxBatch)
-        return fail(QA_STATUS_INVALID_PARAMS, "%s: batch %d outside [1, %d]", fn, batch, qa::kDecodeMaxBatch);
-    if (!aligned(q, 16) || !aligned(k_pages, 16) || !aligned(v_pages, 16) || !aligned(out, 16) ||
-        !aligned(page_table, 4) || !aligned(seq_lens, 4))
-        return fail(QA_STATUS_INVALID_PARAMS, "%s: tensors must be 16-byte aligned (int32 arrays 4-byte)", fn);
-    const int ctas = current_decode_ctas();
+    const int ctas = qa::current_decode_ctas();
     if (ctas <= 0) return fail(QA_STATUS_LAUNCH_FAILED, "%s: no CUDA device", fn);
     const size_t need = qa::decode_workspace_bytes(batch, p->n_q_heads, p->head_dim, ctas);
     if (!p->workspace || p->workspace_bytes < need || !aligned(p->workspace, 256))

@@ -58,5 +58,14 @@ unsigned int status_read_clear_window(cudaStream_t stream, cudaError_t *err);
 // ---- qa_api.cu
 // Writes the thread-local qa_last_error() message.
 void set_last_error(const char *msg);
+// CTAs of the decode grid on the current device (0 when there is none).
+int current_decode_ctas();
+// Host checks of a decode call, everything but the workspace: the params
+// (ABI range, scale, stable_metadata, shape), the tensor pointers, the batch
+// and the alignments.  Sets qa_last_error() and returns INVALID_PARAMS on the
+// first failure.
+qa_status check_decode_call(const char *fn, const void *q, const void *k_pages, const void *v_pages,
+                            const int32_t *page_table, const int32_t *seq_lens, int batch, const void *out,
+                            const qa_attn_params *p);
 
 }  // namespace qa

@@ -34,7 +34,7 @@ cudaError_t launch_window(const void *q, const void *k, const void *v, const int
         !make_rows_tmap(&tk, k, p.head_dim, p.n_kv_heads, total_tokens) ||
         !make_rows_tmap(&tv, v, p.head_dim, p.n_kv_heads, total_tokens))
         return cudaErrorInvalidValue;
-    // the output is written in 8-row TMA boxes (store_rows_tma)
+    // the output is written in kOutBoxRows-row (32-row) TMA boxes (store_rows_tma)
     if (!make_rows_tmap(&tout, out, p.head_dim, p.n_q_heads, total_tokens, kOutBoxRows)) return cudaErrorInvalidValue;
     AttnTcArgs a{};
     a.cu = cu_windows;

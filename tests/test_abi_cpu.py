@@ -219,6 +219,40 @@ def test_stable_metadata_levels_are_checked(libqa):
                                      qa.qa_last_error())[1]
 
 
+def test_noalloc_decode_applies_the_decode_checks(libqa):
+    # the no-alloc entry point takes the same argument checks as qa_decode_attn
+    # (all of them run on the host, before any device is touched)
+    import paged_kv_gqa_attention_gb300 as qa
+
+    fn = qa._lib.qa_decode_attn_noalloc
+    fake = ctypes.c_void_p(0x1000)
+    p = qa.qa_attn_default_params()
+    p.num_pages, p.max_pages_per_seq = 8, 2
+    p.stable_metadata = 3
+    assert fn(fake, fake, fake, fake, fake, 1, fake, ctypes.byref(p)) == -1
+    assert "stable_metadata 3 outside [0, 2]" in qa.qa_last_error()
+    p.stable_metadata = 0
+    p.abi_version = qa.QA_ABI_VERSION + 1
+    assert fn(fake, fake, fake, fake, fake, 1, fake, ctypes.byref(p)) == -1
+    assert "abi_version" in qa.qa_last_error()
+    p.abi_version = qa.QA_ABI_VERSION
+    assert fn(fake, fake, fake, fake, fake, 0, fake, ctypes.byref(p)) == -1
+    assert "batch 0" in qa.qa_last_error()
+    assert fn(ctypes.c_void_p(0x1008), fake, fake, fake, fake, 1, fake, ctypes.byref(p)) == -1
+    assert "aligned" in qa.qa_last_error()
+    p.head_dim = 64
+    assert fn(fake, fake, fake, fake, fake, 1, fake, ctypes.byref(p)) == -1
+    assert "head_dim" in qa.qa_last_error()
+
+
+def test_python_abi_version_matches_the_header(libqa):
+    import paged_kv_gqa_attention_gb300 as qa
+
+    src = open(HEADER).read()
+    m = re.search(r"#define\s+QA_ABI_VERSION\s+(\d+)", src)
+    assert m and qa.QA_ABI_VERSION == int(m.group(1)) == qa.qa_attn_default_params().abi_version
+
+
 def test_bounded_wait_check_rejects_bad_limits_without_device(libqa):
     import paged_kv_gqa_attention_gb300 as qa
 

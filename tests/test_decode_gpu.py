@@ -85,15 +85,13 @@ def test_workload_batched_decode_0p6b_full():
     assert_close(f64(out), ref, "decode 0.6B workload")
 
 
-def test_workload_long_context_1p7b_sampled():
+def test_workload_long_context_1p7b_full():
+    # the long-context decode workload, every (request, head) row checked
+    # against the oracle over the whole output tensor
     w = wl.decode_1p7b()
     out = run_decode(w, debug_checks=True)
-    got = f64(out).reshape(-1, 128)
-    assert np.isfinite(got).all()
-    rng = np.random.default_rng(0)
-    rows = np.sort(rng.choice(got.shape[0], size=96, replace=False)).astype(np.int32)
-    ref = oracle.decode(w["q"], w["k_pages"], w["v_pages"], w["page_table"], w["seq_lens"], rows=rows)
-    assert_close(got[rows], ref, "decode 1.7B workload (96 sampled rows)")
+    ref = oracle.decode(w["q"], w["k_pages"], w["v_pages"], w["page_table"], w["seq_lens"])
+    assert_close(f64(out), ref, "decode 1.7B workload (all rows)")
 
 
 def test_tiny_workload_decode():

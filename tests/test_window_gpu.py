@@ -68,19 +68,20 @@ def test_window_split_equals_separate_calls():
         np.testing.assert_array_equal(whole[a:b], one)
 
 
-def test_workload_aut_window_sampled_and_mid_size_full():
+def test_workload_aut_window_full():
+    # the AuT windowed-attention workload, every row of every window checked
+    # against the oracle over the whole output tensor
     w = wl.window_aut()
     cu = qa.qa_window_plan(w["token_counts"])
     np.testing.assert_array_equal(cu, oracle.window_plan(w["token_counts"]))
-    out = run_window(w, cu, debug_checks=True)
-    got = f64(out).reshape(-1, 64)
-    assert np.isfinite(got).all()
-    rng = np.random.default_rng(1)
-    rows = np.sort(rng.choice(got.shape[0], size=4096, replace=False)).astype(np.int32)
-    ref = oracle.window(w["q"], w["k"], w["v"], cu, rows=rows)
-    assert_close(got[rows], ref, "AuT window workload (4096 sampled rows)")
-    # a contiguous slice of whole windows, checked on every row
-    a, b = int(cu[100]), int(cu[140])
-    sub = dict(q=w["q"][a:b], k=w["k"][a:b], v=w["v"][a:b])
-    ref = oracle.window(sub["q"], sub["k"], sub["v"], cu[100:141] - a)
-    assert_close(f64(out)[a:b], ref, "AuT window workload (40 windows, all rows)")
+    q, k, v = to_dev(w["q"]), to_dev(w["k"]), to_dev(w["v"])
+    out = torch.full_like(q, float("nan"))  # a row left unwritten fails
+    qa.qa_window_attn(q, k, v, to_dev(cu), out, debug_checks=True)
+    torch.cuda.synchronize()
+    ref = oracle.window(w["q"], w["k"], w["v"], cu)
+    got = f64(out)
+    assert_close(got, ref, f"AuT window workload ({got.shape[0]} tokens x {got.shape[1]} heads, all rows)")
+    # the worst window as a diagnostic on failure of a later change
+    err = np.abs(got - ref).max(axis=(1, 2))
+    worst = int(np.argmax(err))
+    assert err[worst] <= 1e-2, f"token {worst}"

@@ -160,6 +160,25 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def nvtx_push(name):
+    """Opens an NVTX range (a no-op without a profiler, or without NVTX)."""
+    try:
+        import torch
+
+        torch.cuda.nvtx.range_push(name)
+    except Exception:
+        pass
+
+
+def nvtx_pop():
+    try:
+        import torch
+
+        torch.cuda.nvtx.range_pop()
+    except Exception:
+        pass
+
+
 # ------------------------------------------------------------ device setup
 def dev_tensor(a, device):
     import torch
@@ -208,18 +227,20 @@ def graph_time(fns, steps, warmup, stream, sampler=None, max_per_graph=64):
 
 def lone_call_time(call, copies, stream, device, n=50):
     """Median device time of one call with no neighbour to overlap: before
-    each call the stream writes 512 MiB (evicting L2 and giving the host
-    time to queue the call), then CUDA events bracket the call alone."""
+    each call the stream reads 512 MiB (evicting L2 with clean lines, so the
+    call does not pay for write-backs, and giving the host time to queue the
+    call), then CUDA events bracket the call alone."""
     import torch
 
-    flush = torch.empty(512 << 20, dtype=torch.uint8, device=device)
+    flush = torch.ones(128 << 20, dtype=torch.float32, device=device)
+    acc = torch.zeros((), dtype=torch.float32, device=device)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
         for i in range(3):  # warm-up
             call(copies[i % len(copies)])
         for i, (a, b) in enumerate(ev):
-            flush.fill_(i & 0xFF)
+            torch.sum(flush, out=acc)
             a.record(stream)
             call(copies[i % len(copies)])
             b.record(stream)
@@ -450,6 +471,7 @@ def run_ours(args, world, rank, local_rank):
                                          workspace=ws, stream=stream, stable_metadata=stable)
 
     fns = [mk(c, 2) for c in copies]
+    nvtx_push("headline")
     sampler = ClockSampler(local_rank) if rank == 0 else None
     if dist:
         dist.barrier()
@@ -473,10 +495,13 @@ def run_ours(args, world, rank, local_rank):
                                 "ms_per_step": round(el / args.steps * 1e3, 5)}
     by_level["note"] = ("the same calls at stable_metadata 0 (everything read after the wait) and 1 (lengths and "
                         "page table read before it); the headline uses 2 (first pool pages streamed before it too)")
+    nvtx_pop()
+    nvtx_push("lone_call")
     lone = lone_call_time(lambda c: mk(c, 0)(), copies, stream, device)
+    nvtx_pop()
     lone_call = {"value": round(nbytes / lone / 1e9, 2), "unit": "GB/s", "us_per_call": round(lone * 1e6, 3),
                  "frac": round(nbytes / lone / 1e9 / peaks["hbm"], 4),
-                 "mode": "one call at a time (stable_metadata 0): 512 MiB written before each call to evict L2, "
+                 "mode": "one call at a time (stable_metadata 0): 512 MiB read before each call to evict L2, "
                          "then CUDA events around the call alone; median of 50 calls"}
 
     # ---------------- end to end: host buffers, copies inside the timed region
@@ -626,22 +651,21 @@ def measure_rows(qa, device, stream, peaks, args, which=ROW_NAMES, cpu=None):
 
     rows = {}
     steps = max(20, min(args.steps, 400))
-    if "prefill" in which:
-        _row_prefill(qa, device, stream, peaks, steps, rows, cpu)
-    if "chunk_prefill" in which:
-        _row_chunk_prefill(qa, device, stream, peaks, steps, rows)
-    if "window" in which:
-        _row_window(qa, device, stream, peaks, steps, rows, cpu)
-    if "decode_long" in which:
-        _row_decode_long(qa, device, stream, peaks, steps, rows, cpu)
-    if "decode_step" in which:
-        _row_decode_step(qa, device, stream, peaks, steps, rows)
-    if "cross_decode" in which:
-        _row_cross_decode(qa, device, stream, peaks, steps, rows)
-    if "decode_graph" in which:
-        _row_decode_graph(qa, device, stream, peaks, steps, rows)
-    if "tiny" in which:
-        _row_tiny(qa, device, stream, steps, rows, cpu)
+    table = (("prefill", lambda: _row_prefill(qa, device, stream, peaks, steps, rows, cpu)),
+             ("chunk_prefill", lambda: _row_chunk_prefill(qa, device, stream, peaks, steps, rows)),
+             ("window", lambda: _row_window(qa, device, stream, peaks, steps, rows, cpu)),
+             ("decode_long", lambda: _row_decode_long(qa, device, stream, peaks, steps, rows, cpu)),
+             ("decode_step", lambda: _row_decode_step(qa, device, stream, peaks, steps, rows)),
+             ("cross_decode", lambda: _row_cross_decode(qa, device, stream, peaks, steps, rows)),
+             ("decode_graph", lambda: _row_decode_graph(qa, device, stream, peaks, steps, rows)),
+             ("tiny", lambda: _row_tiny(qa, device, stream, steps, rows, cpu)))
+    for name, run in table:
+        if name in which:
+            # an NVTX range per row, so a profiler can select one row's kernels
+            # (e.g. ncu --nvtx --nvtx-include "row:window/")
+            nvtx_push(f"row:{name}")
+            run()
+            nvtx_pop()
     status = qa.qa_device_status(stream)
     if status:
         raise RuntimeError(f"device status {status:#x} after the row measurements")

@@ -240,7 +240,7 @@ def lone_call_time(call, copies, stream, device, n=50):
         for i in range(3):  # warm-up
             call(copies[i % len(copies)])
         for i, (a, b) in enumerate(ev):
-            torch.sum(flush, out=acc)
+            torch.sum(flush, dim=0, out=acc)
             a.record(stream)
             call(copies[i % len(copies)])
             b.record(stream)

@@ -18,12 +18,19 @@ arithmetic:
   (13 * 8 = 104 by default), the last one partial (same page, "Windowed audio
   tower"; GGUF keys n_window 50 and n_window_infer 800 in "GGUF layout").
 
+The encoder layer around the window attention (``layer_norm``, ``linear``,
+``encoder_layer``: the pre-norm AuT layer of "Windowed audio tower", bf16 at
+every operator boundary) is in the same C file.
+
 Parity status: every function here is pinned: the attention functions by
 ``tests/test_oracle_pins.py`` (brute force, torch float64 SDPA, mpmath,
 closed forms, invariants, printed values under ``tests/golden/``), QK-norm,
 RoPE and the decode append by ``tests/test_oracle_rope_pins.py`` (torch
 float64 ``rms_norm``, closed-form rotations, rotation invariants, a numpy
-scatter of the append).
+scatter of the append), the encoder layer by
+``tests/test_oracle_encoder_pins.py`` (torch float64 ``layer_norm`` and
+``gelu``, numpy products, closed forms, a numpy statement of the layer with an
+explicit block-diagonal mask, window locality, planted mistakes).
 """
 from __future__ import annotations
 
@@ -80,6 +87,12 @@ def bind_library(path: str):
     lib.oracle_qk_norm_rope.restype = I
     lib.oracle_decode_append.argtypes = [P, P, P, P, P, Dbl, Dbl, P, P, I, I, I, I, I, I, I, P, P, P, P, P]
     lib.oracle_decode_append.restype = I
+    lib.oracle_layer_norm.argtypes = [P, I, I, P, P, Dbl, P, I]
+    lib.oracle_layer_norm.restype = I
+    lib.oracle_linear.argtypes = [P, I, I, P, I, P, I, P, P, I]
+    lib.oracle_linear.restype = I
+    lib.oracle_encoder_layer.argtypes = [P, P, I, I, I, I, I] + [P] * 12 + [Dbl, I, P, I]
+    lib.oracle_encoder_layer.restype = I
     return lib
 
 
@@ -303,3 +316,61 @@ def window_plan(token_counts, window: int | None = None) -> np.ndarray:
             cu.append(cu[-1] + take)
             start += take
     return np.asarray(cu, dtype=np.int32)
+
+
+def layer_norm(x, gamma, beta, *, eps, n_threads=0):
+    """LayerNorm over the last axis of x [T, d] with gain and bias [d] (all
+    bf16 bits).  Returns float64 [T, d]."""
+    x, gamma, beta = _u16(x), _u16(gamma), _u16(beta)
+    T, d = x.shape
+    assert gamma.shape == (d,) and beta.shape == (d,)
+    y = np.zeros((T, d), np.float64)
+    rc = _load().oracle_layer_norm(_ptr(x), T, d, _ptr(gamma), _ptr(beta), float(eps), _ptr(y), _threads(n_threads))
+    if rc != 0:
+        raise ValueError("oracle_layer_norm rejected its arguments")
+    return y
+
+
+def linear(x, w, bias=None, *, gelu=False, residual=None, n_threads=0):
+    """act(x W^T + bias) + residual: x [T, K], w [N, K] (PyTorch Linear
+    layout), bias [N], residual [T, N], all bf16 bits; act = exact gelu when
+    gelu.  Returns float64 [T, N]."""
+    x, w = _u16(x), _u16(w)
+    T, K = x.shape
+    N, K2 = w.shape
+    assert K2 == K
+    bias = None if bias is None else _u16(bias)
+    residual = None if residual is None else _u16(residual)
+    assert bias is None or bias.shape == (N,)
+    assert residual is None or residual.shape == (T, N)
+    y = np.zeros((T, N), np.float64)
+    rc = _load().oracle_linear(_ptr(x), T, K, _ptr(w), N, _ptr(bias), 1 if gelu else 0, _ptr(residual), _ptr(y),
+                               _threads(n_threads))
+    if rc != 0:
+        raise ValueError("oracle_linear rejected its arguments")
+    return y
+
+
+ENCODER_WEIGHTS = ("ln1_g", "ln1_b", "w_qkv", "b_qkv", "w_o", "b_o", "ln2_g", "ln2_b", "w_fc1", "b_fc1", "w_fc2",
+                   "b_fc2")
+
+
+def encoder_layer(x, cu_windows, weights, *, n_heads, eps, blocks=2, n_threads=0):
+    """One AuT encoder layer (pre-norm; bf16 at every operator boundary) over
+    packed tokens x [T, d] (bf16 bits) cut into windows cu_windows.
+    weights: dict of bf16 arrays named as in ENCODER_WEIGHTS (w_qkv [3d, d],
+    w_o [d, d], w_fc1 [ffn, d], w_fc2 [d, ffn]).  blocks=1 stops after the
+    attention block.  Returns float64 [T, d] (the last operator unrounded)."""
+    x = _u16(x)
+    T, d = x.shape
+    cu = _i32(cu_windows)
+    ws = [_u16(weights[k]) for k in ENCODER_WEIGHTS]
+    d_ffn = ws[ENCODER_WEIGHTS.index("w_fc1")].shape[0]
+    assert ws[2].shape == (3 * d, d) and ws[4].shape == (d, d) and ws[8].shape == (d_ffn, d)
+    assert ws[10].shape == (d, d_ffn)
+    y = np.zeros((T, d), np.float64)
+    rc = _load().oracle_encoder_layer(_ptr(x), _ptr(cu), len(cu) - 1, T, d, int(n_heads), d_ffn,
+                                      *[_ptr(a) for a in ws], float(eps), int(blocks), _ptr(y), _threads(n_threads))
+    if rc != 0:
+        raise ValueError("oracle_encoder_layer rejected its arguments")
+    return y

@@ -8,7 +8,9 @@
  *
  * Precision: every bf16 input is widened exactly to double, and everything
  * after that (scores, softmax, weighted sum) is double with no intermediate
- * rounding.  Outputs are double.
+ * rounding.  Outputs are double.  (The encoder layer at the end of the file
+ * chains several operators and rounds each one's result to bf16 before the
+ * next reads it; see its section.)
  *
  * What is computed (the definition, not a fast algorithm):
  *
@@ -71,6 +73,12 @@
  *   [0, cur_len + 1)"); q and k are normalised and rotated at that position,
  *   rounded to bf16 at the operator boundary, and k with the untouched v go
  *   to slot cur_len % page_size of page page_table[b][cur_len / page_size].
+ *
+ *   Encoder layer (qwenasr.cpp ARCHITECTURE.md, "Windowed audio tower"): the
+ *   pre-norm Whisper-style layer around the window attention -- LayerNorm,
+ *   q/k/v projections with bias, window attention, output projection with
+ *   bias and residual, LayerNorm, gelu MLP with biases and residual.  Written
+ *   out at its section below.
  *
  * Threads: rows are independent; n_threads worker threads take contiguous
  * slices of the row list.  This is the only concession to speed.
@@ -617,5 +625,198 @@ ORACLE_EXPORT int oracle_decode_append(const uint16_t *q, const uint16_t *k, con
             }
         }
     }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------- */
+/* AuT encoder layer around the window attention.                             */
+/*
+ * qwenasr.cpp ARCHITECTURE.md, "Windowed audio tower": the encoder is a
+ * pre-norm Whisper-style transformer (d_model 896, 14 heads of head_dim 64,
+ * FFN 3584 with gelu on the 0.6B), LayerNorm with bias, bias on q / k / v /
+ * output, plain bidirectional attention under the block-diagonal window mask;
+ * "GGUF layout": per layer attn_norm (weight, bias), attn_q / attn_k /
+ * attn_v / attn_output (weight, bias), ffn_norm (weight, bias), ffn_up /
+ * ffn_down (weight, bias); "Tensor shape and layout": a Linear weight is
+ * PyTorch (out, in), y = x W^T + b.  One layer, for token row t:
+ *
+ *   a   = LN1(x)                       LN(v) = (v - mean) / sqrt(var + eps) * g + b,
+ *                                      mean and biased variance over the row
+ *   q|k|v = a Wqkv^T + bqkv            Wqkv = [Wq; Wk; Wv] stacked (3 d x d)
+ *   o   = window attention of q, k, v  heads: columns [h Dh, (h + 1) Dh)
+ *   h   = x + (o Wo^T + bo)
+ *   f   = gelu(LN2(h) W1^T + b1)       gelu(u) = u / 2 (1 + erf(u / sqrt 2)),
+ *                                      the exact form ("GGML conventions",
+ *                                      "Conv2d stem": ggml_gelu_erf)
+ *   y   = h + (f W2^T + b2)
+ *
+ * Precision: each of those lines is one operator; its result is rounded to
+ * bf16 (through binary32, bf16_round) before the next line reads it -- the
+ * bf16-at-operator-boundaries policy of the OneSpeech page ("Front end and
+ * graph numerics") applied to this layer.  Inside a line everything is
+ * double.  The layer's last line is returned unrounded (double).
+ */
+
+typedef struct {
+    const uint16_t *x, *g, *b;
+    int d;
+    double eps;
+} ln_ctx;
+
+static void ln_row(const void *vctx, int t, double *out)
+{
+    const ln_ctx *c = (const ln_ctx *)vctx;
+    const uint16_t *xr = c->x + (size_t)t * c->d;
+    double mean = 0.0;
+    for (int i = 0; i < c->d; ++i)
+        mean += bf16_to_double(xr[i]);
+    mean /= c->d;
+    double var = 0.0;
+    for (int i = 0; i < c->d; ++i) {
+        double u = bf16_to_double(xr[i]) - mean;
+        var += u * u;
+    }
+    var /= c->d;
+    double inv = 1.0 / sqrt(var + c->eps);
+    for (int i = 0; i < c->d; ++i)
+        out[i] = (bf16_to_double(xr[i]) - mean) * inv * bf16_to_double(c->g[i]) + bf16_to_double(c->b[i]);
+}
+
+/* y [T][d] = LayerNorm over each row of x [T][d] with gain g and bias b
+ * (bf16 [d]). */
+ORACLE_EXPORT int oracle_layer_norm(const uint16_t *x, int T, int d, const uint16_t *g, const uint16_t *b,
+                                    double eps, double *y, int n_threads)
+{
+    if (T < 0 || d <= 0 || !(eps >= 0.0))
+        return -1;
+    ln_ctx c = {x, g, b, d, eps};
+    if (T > 0)
+        run_rows(&c, ln_row, NULL, T, d, y, n_threads);
+    return 0;
+}
+
+static double gelu_erf(double u)
+{
+    return 0.5 * u * (1.0 + erf(u / sqrt(2.0)));
+}
+
+typedef struct {
+    const uint16_t *x, *w, *bias, *res;
+    int K, N, act;
+} linear_ctx;
+
+static void linear_row(const void *vctx, int t, double *out)
+{
+    const linear_ctx *c = (const linear_ctx *)vctx;
+    double *xr = (double *)malloc(sizeof(double) * (size_t)c->K);
+    for (int k = 0; k < c->K; ++k)
+        xr[k] = bf16_to_double(c->x[(size_t)t * c->K + k]);
+    for (int n = 0; n < c->N; ++n) {
+        const uint16_t *wr = c->w + (size_t)n * c->K;
+        double acc = 0.0;
+        for (int k = 0; k < c->K; ++k)
+            acc += xr[k] * bf16_to_double(wr[k]);
+        if (c->bias)
+            acc += bf16_to_double(c->bias[n]);
+        if (c->act == 1)
+            acc = gelu_erf(acc);
+        if (c->res)
+            acc += bf16_to_double(c->res[(size_t)t * c->N + n]);
+        out[n] = acc;
+    }
+    free(xr);
+}
+
+/* y [T][N] = act(x W^T + bias) + res: x [T][K], w [N][K] (PyTorch Linear
+ * layout), bias [N] or NULL, act 0 (none) or 1 (exact gelu), res [T][N] or
+ * NULL; all bf16. */
+ORACLE_EXPORT int oracle_linear(const uint16_t *x, int T, int K, const uint16_t *w, int N, const uint16_t *bias,
+                                int act, const uint16_t *res, double *y, int n_threads)
+{
+    if (T < 0 || K <= 0 || N <= 0 || (act != 0 && act != 1))
+        return -1;
+    linear_ctx c = {x, w, bias, res, K, N, act};
+    if (T > 0)
+        run_rows(&c, linear_row, NULL, T, N, y, n_threads);
+    return 0;
+}
+
+/* double [n] -> bf16 [n] at an operator boundary */
+static void round_all(const double *v, size_t n, uint16_t *out)
+{
+    for (size_t i = 0; i < n; ++i)
+        out[i] = bf16_round(v[i]);
+}
+
+/* One AuT encoder layer (see above) over T packed tokens x [T][d] cut into
+ * windows cu_windows [n_windows + 1]; H heads of d / H dims, FFN width
+ * d_ffn.  Weights bf16 in PyTorch Linear layout: w_qkv [3 d][d] (q, k, v
+ * stacked), w_o [d][d], w_fc1 [d_ffn][d], w_fc2 [d][d_ffn]; biases and
+ * LayerNorm gains / biases bf16 vectors.  blocks = 1 stops after the
+ * attention block (y = the unrounded h), 2 runs the whole layer.  y [T][d]. */
+ORACLE_EXPORT int oracle_encoder_layer(const uint16_t *x, const int32_t *cu_windows, int n_windows, int T, int d,
+                                       int H, int d_ffn, const uint16_t *ln1_g, const uint16_t *ln1_b,
+                                       const uint16_t *w_qkv, const uint16_t *b_qkv, const uint16_t *w_o,
+                                       const uint16_t *b_o, const uint16_t *ln2_g, const uint16_t *ln2_b,
+                                       const uint16_t *w_fc1, const uint16_t *b_fc1, const uint16_t *w_fc2,
+                                       const uint16_t *b_fc2, double eps, int blocks, double *y, int n_threads)
+{
+    if (T <= 0 || d <= 0 || H <= 0 || d % H || d_ffn <= 0 || (blocks != 1 && blocks != 2))
+        return -1;
+    if (n_windows <= 0 || cu_windows[0] != 0 || cu_windows[n_windows] != T)
+        return -1;
+    for (int w = 0; w < n_windows; ++w)
+        if (cu_windows[w + 1] < cu_windows[w])
+            return -1;
+    const int Dh = d / H;
+    const size_t Td = (size_t)T * d;
+    double *tmp = (double *)malloc(sizeof(double) * (size_t)T * (size_t)(d_ffn > 3 * d ? d_ffn : 3 * d));
+    uint16_t *a = (uint16_t *)malloc(sizeof(uint16_t) * Td);
+    uint16_t *qkv = (uint16_t *)malloc(sizeof(uint16_t) * Td * 3);
+    uint16_t *q = (uint16_t *)malloc(sizeof(uint16_t) * Td);
+    uint16_t *k = (uint16_t *)malloc(sizeof(uint16_t) * Td);
+    uint16_t *v = (uint16_t *)malloc(sizeof(uint16_t) * Td);
+    uint16_t *o = (uint16_t *)malloc(sizeof(uint16_t) * Td);
+    uint16_t *h = (uint16_t *)malloc(sizeof(uint16_t) * Td);
+    uint16_t *f = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)T * d_ffn);
+
+    /* a = LN1(x) */
+    oracle_layer_norm(x, T, d, ln1_g, ln1_b, eps, tmp, n_threads);
+    round_all(tmp, Td, a);
+    /* q | k | v = a Wqkv^T + bqkv, split into q, k, v [T][H][Dh] */
+    oracle_linear(a, T, d, w_qkv, 3 * d, b_qkv, 0, NULL, tmp, n_threads);
+    round_all(tmp, Td * 3, qkv);
+    for (int t = 0; t < T; ++t)
+        for (int i = 0; i < d; ++i) {
+            q[(size_t)t * d + i] = qkv[(size_t)t * 3 * d + i];
+            k[(size_t)t * d + i] = qkv[(size_t)t * 3 * d + d + i];
+            v[(size_t)t * d + i] = qkv[(size_t)t * 3 * d + 2 * d + i];
+        }
+    /* o = window attention, scale 1 / sqrt(Dh) */
+    oracle_window(q, k, v, cu_windows, n_windows, T, H, Dh, 1.0 / sqrt((double)Dh), NULL, 0, tmp, n_threads);
+    round_all(tmp, Td, o);
+    /* h = x + (o Wo^T + bo) */
+    oracle_linear(o, T, d, w_o, d, b_o, 0, x, tmp, n_threads);
+    if (blocks == 1) {
+        memcpy(y, tmp, sizeof(double) * Td);
+    } else {
+        round_all(tmp, Td, h);
+        /* f = gelu(LN2(h) W1^T + b1) */
+        oracle_layer_norm(h, T, d, ln2_g, ln2_b, eps, tmp, n_threads);
+        round_all(tmp, Td, a);
+        oracle_linear(a, T, d, w_fc1, d_ffn, b_fc1, 1, NULL, tmp, n_threads);
+        round_all(tmp, (size_t)T * d_ffn, f);
+        /* y = h + (f W2^T + b2) */
+        oracle_linear(f, T, d_ffn, w_fc2, d, b_fc2, 0, h, y, n_threads);
+    }
+    free(f);
+    free(h);
+    free(o);
+    free(v);
+    free(k);
+    free(q);
+    free(qkv);
+    free(a);
+    free(tmp);
     return 0;
 }

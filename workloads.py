@@ -280,3 +280,64 @@ def chunk_reprefill(seed: int = 7) -> dict:
 
 
 WORKLOADS = {1: tiny, 2: decode_0p6b, 3: prefill_bucket, 4: window_aut, 5: decode_1p7b}
+
+
+# --------------------------------------------------------------------------
+# AuT encoder layer around the window attention (qwenasr.cpp ARCHITECTURE.md,
+# "Windowed audio tower" and "GGUF layout": d_model 896, 14 heads of 64, FFN
+# 3584 on the 0.6B; LayerNorm with bias, biases on every projection).  The
+# checkpoint's weights are not available: they are drawn at random, with the
+# scales of a freshly initialised layer.
+
+ENC_D, ENC_FFN = 896, 3584
+ENC_LN_EPS = 1.0e-5
+
+
+def encoder_weights(rng: np.random.Generator, d: int = ENC_D, d_ffn: int = ENC_FFN) -> dict:
+    """Synthetic bf16 weights of one encoder layer, PyTorch Linear layout
+    (out, in).  Draw order: ln1 gain, ln1 bias, Wqkv, bqkv, Wo, bo, ln2 gain,
+    ln2 bias, W1, b1, W2, b2.  Matrices ~ N(0, 1 / fan_in), biases and
+    LayerNorm biases ~ N(0, 0.1^2), LayerNorm gains ~ U[0.5, 1.5]."""
+    def mat(n_out, n_in):
+        return bf16_bits(rng.standard_normal(size=(n_out, n_in), dtype=np.float32) * np.float32(n_in ** -0.5))
+
+    def vec(n):
+        return bf16_bits(rng.standard_normal(size=n, dtype=np.float32) * np.float32(0.1))
+
+    def gain(n):
+        return bf16_bits(rng.uniform(0.5, 1.5, size=n).astype(np.float32))
+
+    w = {}
+    w["ln1_g"], w["ln1_b"] = gain(d), vec(d)
+    w["w_qkv"], w["b_qkv"] = mat(3 * d, d), vec(3 * d)
+    w["w_o"], w["b_o"] = mat(d, d), vec(d)
+    w["ln2_g"], w["ln2_b"] = gain(d), vec(d)
+    w["w_fc1"], w["b_fc1"] = mat(d_ffn, d), vec(d_ffn)
+    w["w_fc2"], w["b_fc2"] = mat(d, d_ffn), vec(d)
+    return w
+
+
+def encoder_layer_workload(seed: int, token_counts, d: int = ENC_D, h: int = HE, d_ffn: int = ENC_FFN,
+                           rng=None) -> dict:
+    """Packed encoder states x [T, d] ~ N(0, 1) (bf16) of requests with the
+    given token counts, then the layer's weights.  The window plan is the
+    method's (not made here)."""
+    rng = rng_for(seed) if rng is None else rng
+    token_counts = np.asarray(token_counts, np.int32)
+    T = int(token_counts.sum())
+    x = normal_bf16(rng, (T, d))
+    w = dict(kind="encoder_layer", x=x, token_counts=token_counts, n_heads=h, d_ffn=d_ffn, eps=ENC_LN_EPS)
+    w["weights"] = encoder_weights(rng, d, d_ffn)
+    return w
+
+
+def encoder_layer_aut(seed: int = 4) -> dict:
+    """The AuT window workload's requests (8 requests, d ~ U[10, 1200] s,
+    13 tokens per 100 mel frames) through one 0.6B encoder layer: x [T, 896]
+    and the layer's weights drawn after the token counts."""
+    rng = rng_for(seed)
+    dur = rng.uniform(10.0, 1200.0, size=8)
+    counts = np.array([encoder_tokens_for_frames(int(math.floor(100.0 * x))) for x in dur], np.int32)
+    w = encoder_layer_workload(seed, counts, rng=rng)
+    w["name"] = "AuT encoder layer (8 requests, d~U[10,1200] s, d_model 896, 14x64 heads, FFN 3584)"
+    return w

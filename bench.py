@@ -24,8 +24,9 @@ pinned host memory and the output copied back and read every step),
 `rows` (the other hot-path operations measured the same way: ragged causal
 prefill with page write, chunked prefill after cached positions, AuT windowed attention, long-context decode, the
 decode step with the QK-norm + RoPE KV append, paged cross-attention decode,
-a captured 28-layer decode step, the tiny case).  With --impl reference the oracle itself is timed as the
-reference arm.
+a captured 28-layer decode step, the tiny case, the AuT encoder layer around
+the window attention).  With --impl reference the oracle itself is timed as
+the reference arm.
 """
 from __future__ import annotations
 
@@ -640,7 +641,7 @@ def run_ours(args, world, rank, local_rank):
 
 
 ROW_NAMES = ("prefill", "chunk_prefill", "window", "decode_long", "decode_step", "cross_decode", "decode_graph",
-             "tiny")
+             "tiny", "encoder_layer")
 
 
 def measure_rows(qa, device, stream, peaks, args, which=ROW_NAMES, cpu=None):
@@ -658,7 +659,8 @@ def measure_rows(qa, device, stream, peaks, args, which=ROW_NAMES, cpu=None):
              ("decode_step", lambda: _row_decode_step(qa, device, stream, peaks, steps, rows)),
              ("cross_decode", lambda: _row_cross_decode(qa, device, stream, peaks, steps, rows)),
              ("decode_graph", lambda: _row_decode_graph(qa, device, stream, peaks, steps, rows)),
-             ("tiny", lambda: _row_tiny(qa, device, stream, steps, rows, cpu)))
+             ("tiny", lambda: _row_tiny(qa, device, stream, steps, rows, cpu)),
+             ("encoder_layer", lambda: _row_encoder_layer(qa, device, stream, peaks, steps, rows)))
     for name, run in table:
         if name in which:
             # an NVTX range per row, so a profiler can select one row's kernels
@@ -955,6 +957,73 @@ def _row_tiny(qa, device, stream, steps, rows, cpu=None):
         cpu["tiny"] = cpu_leg_tiny(w, "tiny: prefill of 64 tokens, its page write, then 1 decode token")
 
 
+def encoder_flops(T, cu, d=896, h=14, d_ffn=3584):
+    """Algorithmic flops of one encoder layer: the four projections
+    (2 T d (3 d + d + 2 d_ffn)) and the window attention."""
+    return int(2 * T * d * (3 * d + d + 2 * d_ffn)) + window_flops(cu, h=h, d=d // h)
+
+
+def _row_encoder_layer(qa, device, stream, peaks, steps, rows):
+    """One AuT encoder layer (0.6B: d_model 896, 14 x 64 heads, FFN 3584)
+    over the AuT window workload's 70 220 tokens: the whole layer (seven
+    launches) and each projection alone, graphs of back-to-back calls."""
+    import torch
+
+    w = wl.encoder_layer_aut()
+    cu = qa.qa_window_plan(w["token_counts"])
+    T, d = w["x"].shape
+    d_ffn = w["d_ffn"]
+    x = dev_tensor(w["x"], device)
+    dcu = dev_tensor(cu, device)
+    W = {k: dev_tensor(v, device) for k, v in w["weights"].items()}
+    ws = torch.empty(qa.qa_encoder_workspace_size(T, d, d_ffn), dtype=torch.uint8, device=device)
+    out = torch.empty_like(x)
+
+    def layer():
+        qa.qa_encoder_layer(x, dcu, W, out, n_heads=w["n_heads"], ln_eps=w["eps"], workspace=ws, stream=stream)
+
+    n = max(5, min(40, steps // 10))
+    el, clocks = graph_time([layer], n, 3, stream, ClockSampler(0))
+    t = el / n
+    fl = encoder_flops(T, cu, d, w["n_heads"], d_ffn)
+    # each projection alone (inputs and outputs > L2)
+    a = torch.randn(T, d, device=device).to(torch.bfloat16)
+    big = torch.randn(T, d_ffn, device=device).to(torch.bfloat16)
+    qkv = torch.empty(T, 3 * d, dtype=torch.bfloat16, device=device)
+    proj = {
+        "qkv": (lambda: qa.qa_linear(a, W["w_qkv"], W["b_qkv"], qkv, stream=stream), 2 * T * d * 3 * d),
+        "out_proj_residual": (lambda: qa.qa_linear(a, W["w_o"], W["b_o"], out, residual=x, stream=stream),
+                              2 * T * d * d),
+        "fc1_gelu": (lambda: qa.qa_linear(a, W["w_fc1"], W["b_fc1"], big, gelu=True, stream=stream),
+                     2 * T * d * d_ffn),
+        "fc2_residual": (lambda: qa.qa_linear(big, W["w_fc2"], W["b_fc2"], out, residual=x, stream=stream),
+                         2 * T * d_ffn * d),
+        "layer_norm": (lambda: qa.qa_layer_norm(x, W["ln1_g"], W["ln1_b"], a, eps=w["eps"], stream=stream), 0),
+    }
+    parts = {}
+    m = max(5, min(40, steps // 10))
+    for name, (fn, pfl) in proj.items():
+        e, _ = graph_time([fn], m, 3, stream)
+        tt = e / m
+        parts[name] = {"us_per_call": round(tt * 1e6, 2)}
+        if pfl:
+            parts[name].update({"tflops": round(pfl / tt / 1e12, 1),
+                                "frac_bf16_peak": round(pfl / tt / 1e12 / peaks["bf16"], 4),
+                                "frac_bf16_sustained": round(pfl / tt / 1e12 / peaks["bf16_sustained"], 4)})
+        else:
+            by = 2 * T * d * 2
+            parts[name].update({"gbs": round(by / tt / 1e9, 1), "frac_hbm": round(by / tt / 1e9 / peaks["hbm"], 4)})
+    rows["encoder_layer"] = {
+        "workload": "AuT encoder layer 0.6B (d_model 896, 14 x 64 heads, FFN 3584, LayerNorm eps 1e-5) over the "
+                    "AuT window workload: 70 220 tokens, 680 windows of <= 104; synthetic weights",
+        "total_tokens": T, "us_per_layer": round(t * 1e6, 2), "tflops": round(fl / t / 1e12, 1),
+        "frac_bf16_peak": round(fl / t / 1e12 / peaks["bf16"], 4),
+        "frac_bf16_sustained": round(fl / t / 1e12 / peaks["bf16_sustained"], 4), "flops": fl,
+        "gpu_launches_per_layer": 7, "parts": parts, "clocks": clocks}
+    del ws, big, qkv, a
+    torch.cuda.empty_cache()
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -962,7 +1031,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--rows", default="all",
-                    help="other hot-path rows to measure: all, none, or a comma list of prefill,chunk_prefill,window,decode_long,decode_step,cross_decode,decode_graph,tiny")
+                    help="other hot-path rows to measure: all, none, or a comma list of " + ",".join(ROW_NAMES))
     ap.add_argument("--no-cpu", action="store_true", help="skip the cpu_baseline leg")
     args = ap.parse_args()
     if args.warmup < 3:

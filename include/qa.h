@@ -383,6 +383,73 @@ qa_status qa_window_attn(const void *q, const void *k, const void *v,
 int qa_window_plan(const int32_t *token_counts, int n_requests, int window_tokens,
                    int32_t *cu_windows, int capacity);
 
+/* ------------------------------------------------------------------------
+ * The AuT encoder layer around the window attention (qwenasr.cpp
+ * ARCHITECTURE.md, "Windowed audio tower": pre-norm Whisper-style layer,
+ * LayerNorm with bias, bias on q / k / v / output, gelu MLP; "GGUF layout":
+ * attn_norm, attn_q / attn_k / attn_v / attn_output, ffn_norm, ffn_up /
+ * ffn_down, each with weight and bias).  All tensors are caller-owned bf16
+ * device buffers; every row stride is the row's own width.  Linear weights
+ * keep the PyTorch (out, in) layout ("Tensor shape and layout"): y = x W^T.
+ * ------------------------------------------------------------------------ */
+
+/* Weights of one layer (device pointers, bf16). */
+typedef struct qa_encoder_weights {
+    const void *ln1_g, *ln1_b;  /* [d_model] attention LayerNorm gain, bias   */
+    const void *w_qkv, *b_qkv;  /* [3 d_model][d_model], [3 d_model]: the q,  */
+                                /* k and v projections stacked in that order */
+    const void *w_o, *b_o;      /* [d_model][d_model], [d_model]              */
+    const void *ln2_g, *ln2_b;  /* [d_model] MLP LayerNorm gain, bias         */
+    const void *w_fc1, *b_fc1;  /* [d_ffn][d_model], [d_ffn]                  */
+    const void *w_fc2, *b_fc2;  /* [d_model][d_ffn], [d_model]                */
+} qa_encoder_weights;
+
+/* Workspace bytes (256-byte aligned start) that qa_encoder_layer needs for
+ * total_tokens tokens: the layer's bf16 intermediates (LayerNorm output,
+ * q|k|v, attention output, residual stream h, MLP hidden).  0 on bad sizes. */
+size_t qa_encoder_workspace_size(int total_tokens, int d_model, int d_ffn);
+
+/* One encoder layer over total_tokens packed tokens cut into windows:
+ *
+ *   a = LN1(x);  q|k|v = a Wqkv^T + bqkv;  o = window attention(q, k, v)
+ *   h = x + (o Wo^T + bo);  f = gelu(LN2(h) W1^T + b1)
+ *   out = h + (f W2^T + b2)
+ *
+ * LN(v) = (v - mean) / sqrt(var + ln_eps) * g + b over each row (biased
+ * variance); gelu the exact u / 2 (1 + erf(u / sqrt 2)); the attention is
+ * qa_window_attn's (n_heads heads of d_model / n_heads dims, scale
+ * 1 / sqrt(head_dim)).  Each line's result is rounded to bf16; inside a line
+ * accumulation is fp32.
+ *
+ *   x, out     bf16 [total_tokens][d_model] (may not alias)
+ *   cu_windows int32 [n_windows + 1], as for qa_window_attn
+ *   params     stream, debug_checks, and workspace / workspace_bytes of at
+ *              least qa_encoder_workspace_size(); the head fields are unused
+ *
+ * Supported: d_model a multiple of 128 up to 2048 with d_model / n_heads 64
+ * or 128, d_ffn a multiple of 8.  Seven kernel launches, asynchronous on the
+ * stream. */
+qa_status qa_encoder_layer(const void *x, const int32_t *cu_windows, int n_windows, int total_tokens,
+                           int d_model, int n_heads, int d_ffn, const qa_encoder_weights *weights,
+                           float ln_eps, void *out, const qa_attn_params *params);
+
+/* One projection of the layer on the tensor cores:
+ *
+ *   out[i][j] = act(sum_k x[i][k] w[j][k] + bias[j]) + residual[i][j]
+ *
+ *   x [m][k], w [n][k], bias [n] or NULL, residual [m][n] or NULL, out
+ *   [m][n]: bf16, row-major, rows packed; act 0 (none) or 1 (exact gelu).
+ * fp32 accumulation, bf16 result.  Supported: k and n multiples of 8.  Only
+ * params->stream and debug_checks are used. */
+qa_status qa_linear(const void *x, int m, int k, const void *w, int n, const void *bias, int act,
+                    const void *residual, void *out, const qa_attn_params *params);
+
+/* LayerNorm over each row of x [t][d] with gain and bias [d] (bf16), result
+ * bf16 [t][d] (may alias x).  Supported: d a multiple of 128 up to 2048.
+ * Only params->stream and debug_checks are used. */
+qa_status qa_layer_norm(const void *x, int t, int d, const void *gain, const void *bias, float eps, void *y,
+                        const qa_attn_params *params);
+
 /* Synchronises `stream` (cudaStream_t, NULL = legacy default), then reads and
  * clears the device status word of the current device.  Returns its bits
  * (QA_DEVICE_*), 0 when nothing went wrong, or -1 on a CUDA error. */

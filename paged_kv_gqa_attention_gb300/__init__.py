@@ -23,6 +23,7 @@ __all__ = [
     "QA_ABI_VERSION", "QAError", "lib_path", "qa_version", "qa_last_error", "qa_attn_default_params",
     "qa_decode_workspace_size", "qa_decode_attn", "qa_prefill_attn", "qa_window_attn", "qa_window_plan",
     "qa_device_status", "DEVICE_STATUS_BITS", "qa_decode_attn_noalloc", "qa_check_bounded_wait",
+    "qa_encoder_workspace_size", "qa_encoder_layer", "qa_linear", "qa_layer_norm", "ENCODER_WEIGHT_NAMES",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -55,6 +56,14 @@ class qa_attn_params(ctypes.Structure):
         ("debug_checks", ctypes.c_int),
         ("stable_metadata", ctypes.c_int),
     ]
+
+
+ENCODER_WEIGHT_NAMES = ("ln1_g", "ln1_b", "w_qkv", "b_qkv", "w_o", "b_o", "ln2_g", "ln2_b", "w_fc1", "b_fc1",
+                        "w_fc2", "b_fc2")
+
+
+class qa_encoder_weights(ctypes.Structure):
+    _fields_ = [(name, ctypes.c_void_p) for name in ENCODER_WEIGHT_NAMES]
 
 
 def _load():
@@ -92,6 +101,14 @@ def _load():
     lib.qa_window_attn.argtypes = [P, P, P, P, I, I, P, PP]
     lib.qa_window_plan.restype = I
     lib.qa_window_plan.argtypes = [P, I, I, P, I]
+    lib.qa_encoder_workspace_size.restype = ctypes.c_size_t
+    lib.qa_encoder_workspace_size.argtypes = [I, I, I]
+    lib.qa_encoder_layer.restype = I
+    lib.qa_encoder_layer.argtypes = [P, P, I, I, I, I, I, ctypes.POINTER(qa_encoder_weights), ctypes.c_float, P, PP]
+    lib.qa_linear.restype = I
+    lib.qa_linear.argtypes = [P, I, I, P, I, P, I, P, P, PP]
+    lib.qa_layer_norm.restype = I
+    lib.qa_layer_norm.argtypes = [P, I, I, P, P, ctypes.c_float, P, PP]
     lib.qa_device_status.restype = I
     lib.qa_device_status.argtypes = [P]
     lib.qa_check_bounded_wait.restype = I
@@ -456,6 +473,71 @@ def qa_window_attn(q, k, v, cu_windows, out=None, *, scale=0.0, stream=None, deb
                              _dev(v, "v", torch.bfloat16, 3), _dev(cu_windows, "cu_windows", torch.int32, 1), W, T,
                              _dev(out, "out", torch.bfloat16, 3), ctypes.byref(p))
     _check("qa_window_attn", st)
+    return out
+
+
+def qa_encoder_workspace_size(total_tokens: int, d_model: int, d_ffn: int) -> int:
+    """Bytes of workspace qa_encoder_layer needs for total_tokens tokens."""
+    n = _lib.qa_encoder_workspace_size(int(total_tokens), int(d_model), int(d_ffn))
+    if n == 0 and total_tokens > 0:
+        raise QAError("qa_encoder_workspace_size", -1, qa_last_error())
+    return int(n)
+
+
+def qa_encoder_layer(x, cu_windows, weights, out=None, *, n_heads, ln_eps=1e-5, workspace=None, stream=None,
+                     debug_checks=False):
+    """One AuT encoder layer.  x bf16 [T, d]; cu_windows int32 [W+1];
+    weights: dict of bf16 device tensors named as ENCODER_WEIGHT_NAMES
+    (w_qkv [3d, d], w_o [d, d], w_fc1 [ffn, d], w_fc2 [d, ffn], vectors for
+    the rest).  Returns out bf16 [T, d]."""
+    torch = _torch()
+    T, d = x.shape
+    d_ffn = weights["w_fc1"].shape[0]
+    if out is None:
+        out = torch.empty_like(x)
+    if workspace is None:
+        workspace = torch.empty(max(1, qa_encoder_workspace_size(T, d, d_ffn)), dtype=torch.uint8, device=x.device)
+    wt = qa_encoder_weights()
+    for name in ENCODER_WEIGHT_NAMES:
+        t = weights[name]
+        setattr(wt, name, _dev(t, name, torch.bfloat16, t.dim()).value)
+    p = _params(n_q_heads=n_heads, n_kv_heads=n_heads, head_dim=d // n_heads, stream=stream, workspace=workspace,
+                debug_checks=debug_checks)
+    st = _lib.qa_encoder_layer(_dev(x, "x", torch.bfloat16, 2), _dev(cu_windows, "cu_windows", torch.int32, 1),
+                               cu_windows.shape[0] - 1, T, d, int(n_heads), d_ffn, ctypes.byref(wt), float(ln_eps),
+                               _dev(out, "out", torch.bfloat16, 2), ctypes.byref(p))
+    _check("qa_encoder_layer", st)
+    return out
+
+
+def qa_linear(x, w, bias=None, out=None, *, gelu=False, residual=None, stream=None, debug_checks=False):
+    """out = act(x W^T + bias) + residual on the tensor cores.  x bf16 [m, k],
+    w bf16 [n, k], bias [n], residual [m, n]; act = exact gelu when gelu."""
+    torch = _torch()
+    m, k = x.shape
+    n = w.shape[0]
+    if out is None:
+        out = torch.empty(m, n, dtype=torch.bfloat16, device=x.device)
+    p = _params(n_q_heads=1, n_kv_heads=1, head_dim=128, stream=stream, debug_checks=debug_checks)
+    st = _lib.qa_linear(_dev(x, "x", torch.bfloat16, 2), m, k, _dev(w, "w", torch.bfloat16, 2), n,
+                        None if bias is None else _dev(bias, "bias", torch.bfloat16, 1), 1 if gelu else 0,
+                        None if residual is None else _dev(residual, "residual", torch.bfloat16, 2),
+                        _dev(out, "out", torch.bfloat16, 2), ctypes.byref(p))
+    _check("qa_linear", st)
+    return out
+
+
+def qa_layer_norm(x, gain, bias, out=None, *, eps=1e-5, stream=None, debug_checks=False):
+    """LayerNorm over the rows of x bf16 [t, d] with gain and bias bf16 [d]."""
+    torch = _torch()
+    t, d = x.shape
+    if out is None:
+        out = torch.empty_like(x)
+    p = _params(n_q_heads=1, n_kv_heads=1, head_dim=128, stream=stream, debug_checks=debug_checks)
+    st = _lib.qa_layer_norm(_dev(x, "x", torch.bfloat16, 2), t, d, _dev(gain, "gain", torch.bfloat16, 1),
+                            _dev(bias, "bias", torch.bfloat16, 1), float(eps), _dev(out, "out", torch.bfloat16, 2),
+                            ctypes.byref(p))
+    _check("qa_layer_norm", st)
     return out
 
 

@@ -1,0 +1,144 @@
+// The AuT encoder layer around the window attention (qwenasr.cpp
+// ARCHITECTURE.md, "Windowed audio tower": a pre-norm Whisper-style
+// transformer layer, LayerNorm with bias, bias on q / k / v / output, gelu
+// MLP; "GGUF layout": attn_norm, attn_q / attn_k / attn_v / attn_output,
+// ffn_norm, ffn_up / ffn_down, each with weight and bias):
+//
+//   a = LN1(x);  q|k|v = a Wqkv^T + bqkv;  o = window attention(q, k, v)
+//   h = x + (o Wo^T + bo)
+//   f = gelu(LN2(h) W1^T + b1);  y = h + (f W2^T + b2)
+//
+// Seven launches on one stream, each a programmatic dependent of the one
+// before: LayerNorm, the fused q|k|v projection (one [T][3 d] buffer), the
+// window attention reading q, k and v straight out of that buffer (row
+// stride 3 d), the output projection with bias and residual fused in its
+// epilogue, LayerNorm, fc1 with bias and gelu fused, fc2 with bias and
+// residual fused.  Every intermediate is bf16 (the operator boundaries).
+//
+// layer_norm_kernel: one warp per token row; lane l holds 4-element chunks
+// l, l + 32, ... of the row (coalesced 8-byte loads), mean and biased
+// variance by warp sums in fp32, y = (x - mean) / sqrt(var + eps) * g + b
+// rounded to bf16.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+#include "qa_internal.h"
+
+namespace qa {
+namespace {
+
+constexpr int kLnMaxChunks = 16;  // d_model up to 16 * 128 = 2048
+
+__global__ void __launch_bounds__(256) layer_norm_kernel(const uint16_t *x, int T, int d, const uint16_t *g,
+                                                         const uint16_t *b, float eps, uint16_t *y) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int lane = threadIdx.x & 31;
+    const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (t >= T) return;
+    const int n_chunks = d / 128;  // 4-element chunks per lane
+    const uint2 *xr = reinterpret_cast<const uint2 *>(x + (size_t)t * d);
+    float v[kLnMaxChunks][4];
+    float s = 0.f;
+#pragma unroll
+    for (int c = 0; c < kLnMaxChunks; ++c) {
+        if (c < n_chunks) {
+            const uint2 w = xr[c * 32 + lane];
+            v[c][0] = bf16lo(w.x), v[c][1] = bf16hi(w.x), v[c][2] = bf16lo(w.y), v[c][3] = bf16hi(w.y);
+            s += (v[c][0] + v[c][1]) + (v[c][2] + v[c][3]);
+        }
+    }
+    const float mean = warp_sum(s) / (float)d;
+    float ss = 0.f;
+#pragma unroll
+    for (int c = 0; c < kLnMaxChunks; ++c) {
+        if (c < n_chunks) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float u = v[c][j] - mean;
+                ss = fmaf(u, u, ss);
+            }
+        }
+    }
+    const float inv = rsqrtf(warp_sum(ss) / (float)d + eps);
+    const uint2 *gr = reinterpret_cast<const uint2 *>(g);
+    const uint2 *br = reinterpret_cast<const uint2 *>(b);
+    uint2 *yr = reinterpret_cast<uint2 *>(y + (size_t)t * d);
+#pragma unroll
+    for (int c = 0; c < kLnMaxChunks; ++c) {
+        if (c < n_chunks) {
+            const uint2 gw = gr[c * 32 + lane], bw = br[c * 32 + lane];
+            const float o0 = fmaf((v[c][0] - mean) * inv, bf16lo(gw.x), bf16lo(bw.x));
+            const float o1 = fmaf((v[c][1] - mean) * inv, bf16hi(gw.x), bf16hi(bw.x));
+            const float o2 = fmaf((v[c][2] - mean) * inv, bf16lo(gw.y), bf16lo(bw.y));
+            const float o3 = fmaf((v[c][3] - mean) * inv, bf16hi(gw.y), bf16hi(bw.y));
+            yr[c * 32 + lane] = make_uint2(pack_bf16x2(o0, o1), pack_bf16x2(o2, o3));
+        }
+    }
+}
+
+size_t align256(size_t n) { return (n + 255) & ~(size_t)255; }
+
+}  // namespace
+
+bool layer_norm_supported(int d) { return d >= 128 && d % 128 == 0 && d / 128 <= kLnMaxChunks; }
+
+cudaError_t launch_layer_norm(const void *x, int T, int d, const void *g, const void *b, float eps, void *y,
+                              cudaStream_t stream) {
+    if (T == 0) return cudaSuccess;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((T + 7) / 8));
+    cfg.blockDim = dim3(256);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, layer_norm_kernel, static_cast<const uint16_t *>(x), T, d,
+                                       static_cast<const uint16_t *>(g), static_cast<const uint16_t *>(b), eps,
+                                       static_cast<uint16_t *>(y));
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+EncoderWorkspace encoder_workspace_layout(long long T, int d, int d_ffn) {
+    EncoderWorkspace w;
+    w.a = 0;
+    w.qkv = w.a + align256((size_t)T * d * 2);
+    w.o = w.qkv + align256((size_t)T * 3 * d * 2);
+    w.h = w.o + align256((size_t)T * d * 2);
+    w.f = w.h + align256((size_t)T * d * 2);
+    w.total = w.f + align256((size_t)T * d_ffn * 2);
+    return w;
+}
+
+cudaError_t launch_encoder_layer(const void *x, const int32_t *cu_windows, int n_windows, int T, int d, int H,
+                                 int d_ffn, const qa_encoder_weights &w, float eps, void *workspace, void *out,
+                                 const qa_attn_params &p, cudaStream_t stream) {
+    if (T == 0) return cudaSuccess;
+    const EncoderWorkspace L = encoder_workspace_layout(T, d, d_ffn);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    void *a = ws + L.a, *qkv = ws + L.qkv, *o = ws + L.o, *h = ws + L.h, *f = ws + L.f;
+    const uint16_t *qkv16 = static_cast<const uint16_t *>(qkv);
+    cudaError_t e;
+    // attention block
+    if ((e = launch_layer_norm(x, T, d, w.ln1_g, w.ln1_b, eps, a, stream)) != cudaSuccess) return e;
+    if ((e = launch_gemm(a, d, T, d, w.w_qkv, 3 * d, w.b_qkv, 0, nullptr, 0, qkv, 3 * d, stream)) != cudaSuccess)
+        return e;
+    qa_attn_params pw = p;
+    pw.n_q_heads = pw.n_kv_heads = H;
+    pw.head_dim = d / H;
+    if ((e = launch_window(qkv16, qkv16 + d, qkv16 + 2 * d, cu_windows, n_windows, T, o, pw,
+                           1.0f / sqrtf((float)(d / H)), stream, 3LL * d)) != cudaSuccess)
+        return e;
+    if ((e = launch_gemm(o, d, T, d, w.w_o, d, w.b_o, 0, x, d, h, d, stream)) != cudaSuccess) return e;
+    // MLP block
+    if ((e = launch_layer_norm(h, T, d, w.ln2_g, w.ln2_b, eps, a, stream)) != cudaSuccess) return e;
+    if ((e = launch_gemm(a, d, T, d, w.w_fc1, d_ffn, w.b_fc1, 1, nullptr, 0, f, d_ffn, stream)) != cudaSuccess)
+        return e;
+    return launch_gemm(f, d_ffn, T, d_ffn, w.w_fc2, d, w.b_fc2, 0, h, d, out, d, stream);
+}
+
+}  // namespace qa

@@ -1,0 +1,334 @@
+// Dense projections of the AuT encoder layer on the tensor cores:
+//
+//   out[m][n] = act(sum_k A[m][k] W[n][k] + bias[n]) + res[m][n]
+//
+// A [M][K] bf16 row-major (activations), W [N][K] bf16 (a PyTorch Linear
+// weight, qwenasr.cpp ARCHITECTURE.md "Tensor shape and layout": (out, in),
+// y = x W^T), bias [N] bf16 or none, act none or the exact gelu
+// u / 2 (1 + erf(u / sqrt 2)) ("Windowed audio tower": gelu MLP; "GGML
+// conventions": ggml_gelu_erf), res [M][N] bf16 (the residual stream) or
+// none.  fp32 accumulation, bf16 result (round to nearest even) with any row
+// stride, so the fused q|k|v projection writes one [M][3 d] buffer.
+//
+// Persistent, warp-specialised, one CTA per SM:
+//   warp 0     producer: TMA loads of 128 x 64 A tiles and BN x 64 W tiles
+//              (128-byte swizzled, K-major) into a ring of shared-memory
+//              stages, each completing on its "full" mbarrier;
+//   warp 1     allocates TMEM; one lane issues tcgen05.mma (M = 128,
+//              N = BN, K = 16 per instruction, four per 64-wide stage) into
+//              one of two fp32 accumulators in TMEM; each stage is released
+//              ("empty") by a tcgen05.commit when its MMAs are done, and an
+//              accumulator is handed to the epilogue ("acc_full") the same way;
+//   warps 2-5  epilogue: each thread owns one row of the 128-row tile (the
+//              TMEM lane quadrant of its warp), reads the accumulator 32
+//              columns at a time, adds bias, applies gelu, adds the residual,
+//              rounds to bf16 and stores; then releases the accumulator
+//              ("acc_empty") so the next-but-one tile can use it.
+// With two accumulators the epilogue of tile i overlaps the MMAs of tile
+// i + 1.  Tiles are walked m-block-major (tile = m_blk * tiles_n + n_blk), so
+// the CTAs running at any moment share a few m-blocks of A and every W tile:
+// A is fetched from HBM about once, W stays in L2.
+//
+// Rows past M and columns past N (ragged last tiles) are zero-filled by TMA
+// and never stored; K need not be a multiple of 64 (the zero fill makes the
+// tail products 0).  Every wait is bounded (common.cuh): one that expires
+// sets QA_DEVICE_TIMEOUT and the kernel runs to its end.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <algorithm>
+
+#include "common.cuh"
+#include "qa_internal.h"
+#include "tc.cuh"
+#include "tmap.h"
+
+namespace qa {
+namespace {
+
+__device__ unsigned int g_status;
+
+constexpr int kBM = 128, kBK = 64;
+constexpr int kThreads = 192;  // producer, MMA, four epilogue warps
+
+struct GemmArgs {
+    int M, N, K;
+    const uint16_t *bias;  // [N] or null
+    const uint16_t *res;   // [M][ldr] or null
+    uint16_t *out;         // [M][ldc]
+    long long ldr, ldc;
+    int act;  // 0 none, 1 gelu (erf)
+    int tiles_m, tiles_n;
+};
+
+template <int BN>
+struct GemmLayout {
+    static constexpr uint32_t kA = kBM * kBK * 2;  // 16 KiB
+    static constexpr uint32_t kB = BN * kBK * 2;
+    static constexpr uint32_t kStage = kA + kB;
+    static constexpr int kStages = (220 * 1024) / kStage < 8 ? (220 * 1024) / kStage : 8;
+    static constexpr uint32_t kBar = kStages * kStage;  // full[S], empty[S], acc_full[2], acc_empty[2]
+    static constexpr uint32_t kTmemSlot = kBar + (2 * kStages + 4) * 8;
+    static constexpr uint32_t kAbort = kTmemSlot + 8;  // set when a wait expired: every role stops
+    static constexpr uint32_t kBytes = kTmemSlot + 16;
+    static constexpr uint32_t kSmem = kBytes + 1024;  // slack for 1024-byte alignment
+    static constexpr uint32_t kAccCols = 256;         // column stride of the two accumulators
+    static_assert(kA % 1024 == 0 && kB % 1024 == 0, "stages must keep 1024-byte swizzle alignment");
+    static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "N tile: a multiple of 32, at most 256");
+    static_assert(kStages >= 2, "at least two stages");
+};
+
+__device__ __forceinline__ float gelu_erf(float u) { return 0.5f * u * (1.0f + erff(u * 0.70710678118654752f)); }
+
+// bf16x8 (one 16-byte word) -> 8 floats
+__device__ __forceinline__ void unpack8(uint4 w, float *f) {
+    f[0] = bf16lo(w.x), f[1] = bf16hi(w.x), f[2] = bf16lo(w.y), f[3] = bf16hi(w.y);
+    f[4] = bf16lo(w.z), f[5] = bf16hi(w.z), f[6] = bf16lo(w.w), f[7] = bf16hi(w.w);
+}
+
+template <int BN>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_bf16_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_w,
+                     const GemmArgs a) {
+    using L = GemmLayout<BN>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t sb = (raw + 1023u) & ~1023u;
+    uint8_t *smem = smem_raw + (sb - raw);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t bar_full = sb + L::kBar, bar_empty = bar_full + L::kStages * 8;
+    const uint32_t bar_acc_full = bar_empty + L::kStages * 8, bar_acc_empty = bar_acc_full + 16;
+    const int n_tiles = a.tiles_m * a.tiles_n;
+    const int n_kb = (a.K + kBK - 1) / kBK;
+
+    // a programmatic dependent of the kernel before it: wait for its writes
+    // before reading anything, then let the next kernel be scheduled
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+    if (threadIdx.x == 0) {
+        *reinterpret_cast<volatile int *>(smem + L::kAbort) = 0;
+        for (int s = 0; s < L::kStages; ++s) {
+            mbar_init(bar_full + 8 * s, 1);
+            mbar_init(bar_empty + 8 * s, 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar_acc_full + 8 * i, 1);
+            mbar_init(bar_acc_empty + 8 * i, 4);  // one arrival per epilogue warp
+        }
+        fence_mbar_init();
+        tc::prefetch_tmap(&tm_a);
+        tc::prefetch_tmap(&tm_w);
+    }
+    if (warp == 1) tc::tmem_alloc(sb + L::kTmemSlot, 512);
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + L::kTmemSlot);
+    // A wait that expires (a fault elsewhere) stops every role at its next
+    // wait instead of letting each later wait expire in turn.
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kAbort);
+    auto wait = [&](uint32_t bar, uint32_t parity) -> bool {
+        if (*abort_flag) return false;
+        if (mbar_wait(bar, parity, &g_status)) return true;
+        *abort_flag = 1;
+        return false;
+    };
+
+    if (warp == 0) {
+        // ---------------- producer
+        if (lane == 0) {
+            int it = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
+                const int m0 = (tile / a.tiles_n) * kBM, n0 = (tile % a.tiles_n) * BN;
+                for (int kb = 0; kb < n_kb; ++kb, ++it) {
+                    const int s = it % L::kStages;
+                    if (it >= L::kStages && !(ok = wait(bar_empty + 8 * s, ((it / L::kStages) & 1) ^ 1))) break;
+                    const uint32_t st = sb + s * L::kStage;
+                    mbar_arrive_expect_tx(bar_full + 8 * s, L::kStage);
+                    tc::tma_load_2d(st, &tm_a, kb * kBK, m0, bar_full + 8 * s);
+                    tc::tma_load_2d(st + L::kA, &tm_w, kb * kBK, n0, bar_full + 8 * s);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issue
+        if (lane == 0) {
+            constexpr uint32_t idesc = tc::idesc_bf16(kBM, BN, false);
+            int it = 0, tcount = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x, ++tcount) {
+                const int acc = tcount & 1;
+                if (tcount >= 2 && !(ok = wait(bar_acc_empty + 8 * acc, ((tcount >> 1) & 1) ^ 1))) break;
+                tc::fence_after();
+                const uint32_t d_tmem = tmem + acc * L::kAccCols;
+                for (int kb = 0; kb < n_kb; ++kb, ++it) {
+                    const int s = it % L::kStages;
+                    if (!(ok = wait(bar_full + 8 * s, (it / L::kStages) & 1))) break;
+                    tc::fence_after();
+                    const uint32_t st = sb + s * L::kStage;
+#pragma unroll
+                    for (int kk = 0; kk < kBK / 16; ++kk)
+                        tc::mma_bf16(d_tmem, tc::sw128_desc(st + kk * 32), tc::sw128_desc(st + L::kA + kk * 32), idesc,
+                                     (kb > 0 || kk > 0) ? 1u : 0u);
+                    tc::mma_commit(bar_empty + 8 * s);  // the stage is free once these MMAs are done
+                }
+                if (ok) tc::mma_commit(bar_acc_full + 8 * acc);
+            }
+        }
+    } else {
+        // ---------------- epilogue: warps 2..5, TMEM lane quadrant warp % 4
+        const int quad = warp & 3;
+        const int r_in_tile = quad * 32 + lane;
+        int tcount = 0;
+        for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++tcount) {
+            const int acc = tcount & 1;
+            const int m0 = (tile / a.tiles_n) * kBM, n0 = (tile % a.tiles_n) * BN;
+            // warp-uniform: every lane waits on the same phase
+            const bool ok = wait(bar_acc_full + 8 * acc, (tcount >> 1) & 1);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            tc::fence_after();
+            const int row = m0 + r_in_tile;
+            const bool row_ok = row < a.M;
+            const uint32_t t_base = tmem + acc * L::kAccCols + ((uint32_t)(quad * 32) << 16);
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+                float v[32];
+                tc::tmem_ld32(t_base + c * 32, v);  // warp-collective: every lane, every chunk
+                const int col0 = n0 + c * 32;
+                // 8-column groups inside N (N is a multiple of 8)
+                const int n_groups = max(0, min(4, (a.N - col0) / 8));
+                if (a.bias) {
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) {
+                        if (g < n_groups) {
+                            float bf[8];
+                            unpack8(*reinterpret_cast<const uint4 *>(a.bias + col0 + 8 * g), bf);
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) v[8 * g + j] += bf[j];
+                        }
+                    }
+                }
+                if (a.act == 1) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] = gelu_erf(v[j]);
+                }
+                if (row_ok) {
+                    if (a.res) {
+                        const uint16_t *rrow = a.res + (size_t)row * a.ldr + col0;
+#pragma unroll
+                        for (int g = 0; g < 4; ++g) {
+                            if (g < n_groups) {
+                                float rf[8];
+                                unpack8(*reinterpret_cast<const uint4 *>(rrow + 8 * g), rf);
+#pragma unroll
+                                for (int j = 0; j < 8; ++j) v[8 * g + j] += rf[j];
+                            }
+                        }
+                    }
+                    uint16_t *orow = a.out + (size_t)row * a.ldc + col0;
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) {
+                        if (g < n_groups)
+                            *reinterpret_cast<uint4 *>(orow + 8 * g) = make_uint4(
+                                pack_bf16x2(v[8 * g + 0], v[8 * g + 1]), pack_bf16x2(v[8 * g + 2], v[8 * g + 3]),
+                                pack_bf16x2(v[8 * g + 4], v[8 * g + 5]), pack_bf16x2(v[8 * g + 6], v[8 * g + 7]));
+                    }
+                }
+                __syncwarp();
+            }
+            // every TMEM read of this accumulator is done: hand it back
+            tc::fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_acc_empty + 8 * acc);
+        }
+    }
+
+    __syncwarp();  // lanes 1..31 of the producer and MMA warps wait for their lane 0
+    tc::fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc::fence_after();
+        tc::tmem_dealloc(tmem, 512);
+    }
+}
+
+// 2-D tensor map of a row-major bf16 matrix [rows][cols] with row stride ld
+// (elements): box {64 cols, box_rows rows}, 128-byte swizzle.
+bool make_matrix_tmap(CUtensorMap *map, const void *base, long long rows, long long cols, long long ld,
+                      int box_rows) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc || rows < 1 || cols < 1 || rows > 0x7fffffffLL || cols > 0x7fffffffLL) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+    cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <int BN>
+cudaError_t launch_gemm_bn(const void *x, long long ldx, int M, int K, const void *w, int N, const void *bias,
+                           int act, const void *res, long long ldr, void *out, long long ldc, cudaStream_t stream) {
+    using L = GemmLayout<BN>;
+    CUtensorMap ta, tw;
+    if (!make_matrix_tmap(&ta, x, M, K, ldx, kBM) || !make_matrix_tmap(&tw, w, N, K, K, BN))
+        return cudaErrorInvalidValue;
+    GemmArgs a{};
+    a.M = M, a.N = N, a.K = K;
+    a.bias = static_cast<const uint16_t *>(bias);
+    a.res = static_cast<const uint16_t *>(res);
+    a.out = static_cast<uint16_t *>(out);
+    a.ldr = ldr, a.ldc = ldc, a.act = act;
+    a.tiles_m = (M + kBM - 1) / kBM;
+    a.tiles_n = (N + BN - 1) / BN;
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(gemm_bf16_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
+    if (e != cudaSuccess) return e;
+    const long long tiles = (long long)a.tiles_m * a.tiles_n;
+    if (tiles > 0x7fffffffLL) return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)std::min<long long>(tiles, sms));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = L::kSmem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, gemm_bf16_kernel<BN>, ta, tw, a);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+// N tile: 224 divides the encoder's widths (896, 3 x 896, 3584) exactly;
+// other widths take 256 with a ragged last tile.
+cudaError_t launch_gemm(const void *x, long long ldx, int M, int K, const void *w, int N, const void *bias, int act,
+                        const void *res, long long ldr, void *out, long long ldc, cudaStream_t stream) {
+    if (M == 0) return cudaSuccess;
+    if (N % 224 == 0) return launch_gemm_bn<224>(x, ldx, M, K, w, N, bias, act, res, ldr, out, ldc, stream);
+    return launch_gemm_bn<256>(x, ldx, M, K, w, N, bias, act, res, ldr, out, ldc, stream);
+}
+
+unsigned int status_read_clear_gemm(cudaStream_t stream, cudaError_t *err) {
+    unsigned int v = 0, zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbolAsync(&v, g_status, sizeof v, 0, cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e == cudaSuccess && v)
+        e = cudaMemcpyToSymbolAsync(g_status, &zero, sizeof zero, 0, cudaMemcpyHostToDevice, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (err) *err = e;
+    return v;
+}
+
+}  // namespace qa

@@ -350,12 +350,104 @@ QA_API int qa_window_plan(const int32_t *token_counts, int n_requests, int windo
     return n;
 }
 
+QA_API size_t qa_encoder_workspace_size(int total_tokens, int d_model, int d_ffn) {
+    clear_error();
+    if (total_tokens < 0 || d_model < 1 || d_ffn < 1) {
+        fail(QA_STATUS_INVALID_PARAMS, "qa_encoder_workspace_size: bad sizes");
+        return 0;
+    }
+    return qa::encoder_workspace_layout(total_tokens, d_model, d_ffn).total;
+}
+
+QA_API qa_status qa_encoder_layer(const void *x, const int32_t *cu_windows, int n_windows, int total_tokens,
+                                  int d_model, int n_heads, int d_ffn, const qa_encoder_weights *w, float ln_eps,
+                                  void *out, const qa_attn_params *p) {
+    const char *fn = "qa_encoder_layer";
+    clear_error();
+    qa_status st = check_common(p, fn);
+    if (st != QA_STATUS_OK) return st;
+    if (!qa::layer_norm_supported(d_model))
+        return fail(QA_STATUS_INVALID_PARAMS, "%s: d_model %d unsupported (a multiple of 128 up to 2048)", fn,
+                    d_model);
+    if (n_heads < 1 || d_model % n_heads || (d_model / n_heads != 64 && d_model / n_heads != 128))
+        return fail(QA_STATUS_INVALID_PARAMS, "%s: d_model / n_heads must be 64 or 128 (d_model %d, n_heads %d)", fn,
+                    d_model, n_heads);
+    if (d_ffn < 8 || d_ffn % 8) return fail(QA_STATUS_INVALID_PARAMS, "%s: d_ffn %d must be a multiple of 8", fn, d_ffn);
+    if (n_windows < 1) return fail(QA_STATUS_INVALID_PARAMS, "%s: n_windows %d < 1", fn, n_windows);
+    if (total_tokens < 0) return fail(QA_STATUS_INVALID_PARAMS, "%s: total_tokens %d < 0", fn, total_tokens);
+    if (!(ln_eps >= 0.f) || !isfinite(ln_eps))
+        return fail(QA_STATUS_INVALID_PARAMS, "%s: ln_eps must be finite and >= 0", fn);
+    if (!x || !cu_windows || !out || !w) return fail(QA_STATUS_INVALID_PARAMS, "%s: NULL pointer", fn);
+    const void *wp[12] = {w->ln1_g, w->ln1_b, w->w_qkv, w->b_qkv, w->w_o, w->b_o,
+                          w->ln2_g, w->ln2_b, w->w_fc1, w->b_fc1, w->w_fc2, w->b_fc2};
+    for (const void *q : wp) {
+        if (!q) return fail(QA_STATUS_INVALID_PARAMS, "%s: NULL weight pointer", fn);
+        if (!aligned(q, 16)) return fail(QA_STATUS_INVALID_PARAMS, "%s: weights must be 16-byte aligned", fn);
+    }
+    if (!aligned(x, 16) || !aligned(out, 16) || !aligned(cu_windows, 4))
+        return fail(QA_STATUS_INVALID_PARAMS, "%s: x and out must be 16-byte aligned (cu_windows 4-byte)", fn);
+    if (x == out) return fail(QA_STATUS_INVALID_PARAMS, "%s: out may not alias x", fn);
+    const size_t need = qa::encoder_workspace_layout(total_tokens, d_model, d_ffn).total;
+    if (!p->workspace || p->workspace_bytes < need || !aligned(p->workspace, 256))
+        return fail(QA_STATUS_INVALID_PARAMS, "%s: workspace must be >= %zu bytes and 256-byte aligned (got %zu)", fn,
+                    need, p->workspace_bytes);
+    cudaStream_t stream = static_cast<cudaStream_t>(p->stream);
+    st = launch_result(qa::launch_encoder_layer(x, cu_windows, n_windows, total_tokens, d_model, n_heads, d_ffn, *w,
+                                                ln_eps, p->workspace, out, *p, stream),
+                       fn);
+    if (st != QA_STATUS_OK || !p->debug_checks) return st;
+    cudaError_t e[2];
+    const unsigned int bits = qa::status_read_clear_window(stream, &e[0]) | qa::status_read_clear_gemm(stream, &e[1]);
+    return debug_status(bits, e[0] != cudaSuccess ? e[0] : e[1], fn);
+}
+
+QA_API qa_status qa_linear(const void *x, int m, int k, const void *w, int n, const void *bias, int act,
+                           const void *residual, void *out, const qa_attn_params *p) {
+    const char *fn = "qa_linear";
+    clear_error();
+    qa_status st = check_common(p, fn);
+    if (st != QA_STATUS_OK) return st;
+    if (m < 0 || k < 8 || k % 8 || n < 8 || n % 8)
+        return fail(QA_STATUS_INVALID_PARAMS, "%s: m %d >= 0, k %d and n %d multiples of 8 required", fn, m, k, n);
+    if (act != 0 && act != 1) return fail(QA_STATUS_INVALID_PARAMS, "%s: act %d must be 0 or 1", fn, act);
+    if (!x || !w || !out) return fail(QA_STATUS_INVALID_PARAMS, "%s: NULL pointer", fn);
+    if (!aligned(x, 16) || !aligned(w, 16) || !aligned(out, 16) || !aligned(bias, 16) || !aligned(residual, 16))
+        return fail(QA_STATUS_INVALID_PARAMS, "%s: tensors must be 16-byte aligned", fn);
+    cudaStream_t stream = static_cast<cudaStream_t>(p->stream);
+    st = launch_result(qa::launch_gemm(x, k, m, k, w, n, bias, act, residual, n, out, n, stream), fn);
+    if (st != QA_STATUS_OK || !p->debug_checks) return st;
+    cudaError_t e;
+    const unsigned int bits = qa::status_read_clear_gemm(stream, &e);
+    return debug_status(bits, e, fn);
+}
+
+QA_API qa_status qa_layer_norm(const void *x, int t, int d, const void *gain, const void *bias, float eps, void *y,
+                               const qa_attn_params *p) {
+    const char *fn = "qa_layer_norm";
+    clear_error();
+    qa_status st = check_common(p, fn);
+    if (st != QA_STATUS_OK) return st;
+    if (t < 0 || !qa::layer_norm_supported(d))
+        return fail(QA_STATUS_INVALID_PARAMS, "%s: t %d >= 0 and d %d a multiple of 128 up to 2048 required", fn, t,
+                    d);
+    if (!(eps >= 0.f) || !isfinite(eps)) return fail(QA_STATUS_INVALID_PARAMS, "%s: eps must be finite and >= 0", fn);
+    if (!x || !gain || !bias || !y) return fail(QA_STATUS_INVALID_PARAMS, "%s: NULL pointer", fn);
+    if (!aligned(x, 16) || !aligned(gain, 16) || !aligned(bias, 16) || !aligned(y, 16))
+        return fail(QA_STATUS_INVALID_PARAMS, "%s: tensors must be 16-byte aligned", fn);
+    cudaStream_t stream = static_cast<cudaStream_t>(p->stream);
+    st = launch_result(qa::launch_layer_norm(x, t, d, gain, bias, eps, y, stream), fn);
+    if (st != QA_STATUS_OK || !p->debug_checks) return st;
+    cudaError_t e = cudaStreamSynchronize(stream);
+    return launch_result(e, fn);
+}
+
 QA_API int qa_device_status(void *stream) {
     clear_error();
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e[4];
+    cudaError_t e[5];
     const unsigned int bits = qa::status_read_clear_decode(s, &e[0]) | qa::status_read_clear_prefill(s, &e[1]) |
-                              qa::status_read_clear_window(s, &e[2]) | qa::status_read_clear_append(s, &e[3]);
+                              qa::status_read_clear_window(s, &e[2]) | qa::status_read_clear_append(s, &e[3]) |
+                              qa::status_read_clear_gemm(s, &e[4]);
     for (cudaError_t ei : e)
         if (ei != cudaSuccess) {
             fail(QA_STATUS_LAUNCH_FAILED, "qa_device_status: CUDA error %s", cudaGetErrorString(ei));

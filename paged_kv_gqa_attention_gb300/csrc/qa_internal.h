@@ -50,10 +50,30 @@ cudaError_t launch_append(const void *q, const void *k, const void *v, const flo
 unsigned int status_read_clear_append(cudaStream_t stream, cudaError_t *err);
 
 // ---- window (window.cu)
+// ld_qkv: row stride (elements) of q, k and v; 0 = packed (n_q_heads * head_dim)
 cudaError_t launch_window(const void *q, const void *k, const void *v, const int32_t *cu_windows,
                           int n_windows, int total_tokens, void *out, const qa_attn_params &p,
-                          float scale, cudaStream_t stream);
+                          float scale, cudaStream_t stream, long long ld_qkv = 0);
 unsigned int status_read_clear_window(cudaStream_t stream, cudaError_t *err);
+
+// ---- dense projections (gemm.cu): out = act(x W^T + bias) + res, bf16,
+// row strides in elements (multiples of 8); act 0 none, 1 exact gelu
+cudaError_t launch_gemm(const void *x, long long ldx, int M, int K, const void *w, int N, const void *bias, int act,
+                        const void *res, long long ldr, void *out, long long ldc, cudaStream_t stream);
+unsigned int status_read_clear_gemm(cudaStream_t stream, cudaError_t *err);
+
+// ---- encoder layer (encoder.cu)
+bool layer_norm_supported(int d);
+cudaError_t launch_layer_norm(const void *x, int T, int d, const void *g, const void *b, float eps, void *y,
+                              cudaStream_t stream);
+// byte offsets of the layer's intermediates in the caller's workspace
+struct EncoderWorkspace {
+    size_t a, qkv, o, h, f, total;
+};
+EncoderWorkspace encoder_workspace_layout(long long T, int d, int d_ffn);
+cudaError_t launch_encoder_layer(const void *x, const int32_t *cu_windows, int n_windows, int T, int d, int H,
+                                 int d_ffn, const qa_encoder_weights &w, float eps, void *workspace, void *out,
+                                 const qa_attn_params &p, cudaStream_t stream);
 
 // ---- qa_api.cu
 // Writes the thread-local qa_last_error() message.

@@ -26,11 +26,14 @@ inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 // dims {D, H, T} (innermost first), box {64, 1, box_rows} (128: a tile;
 // 16: one page of a [pages * 16][H][D] pool).  Returns false when the driver
 // rejects the descriptor (bad alignment or sizes).
-inline bool make_rows_tmap(CUtensorMap *map, const void *base, int D, int H, long long T, int box_rows = 128) {
+// row_elems: elements between consecutive rows (0: packed, H * D).
+inline bool make_rows_tmap(CUtensorMap *map, const void *base, int D, int H, long long T, int box_rows = 128,
+                           long long row_elems = 0) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (!enc || T < 1 || T > 0x7fffffffLL) return false;
+    if (row_elems == 0) row_elems = (long long)H * D;
     cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)T};
-    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2};
+    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)row_elems * 2};
     cuuint32_t box[3] = {64, 1, (cuuint32_t)box_rows};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,

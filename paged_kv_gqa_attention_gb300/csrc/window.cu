@@ -26,13 +26,14 @@ __device__ unsigned int g_status;
 
 cudaError_t launch_window(const void *q, const void *k, const void *v, const int32_t *cu_windows,
                           int n_windows, int total_tokens, void *out, const qa_attn_params &p,
-                          float scale, cudaStream_t stream) {
+                          float scale, cudaStream_t stream, long long ld_qkv) {
     if (total_tokens == 0) return cudaSuccess;
     if (p.n_q_heads > 65535) return cudaErrorInvalidValue;
     CUtensorMap tq, tk, tv, tout;
-    if (!make_rows_tmap(&tq, q, p.head_dim, p.n_q_heads, total_tokens) ||
-        !make_rows_tmap(&tk, k, p.head_dim, p.n_kv_heads, total_tokens) ||
-        !make_rows_tmap(&tv, v, p.head_dim, p.n_kv_heads, total_tokens))
+    // q, k and v may be column blocks of one wider row (ld_qkv elements apart)
+    if (!make_rows_tmap(&tq, q, p.head_dim, p.n_q_heads, total_tokens, 128, ld_qkv) ||
+        !make_rows_tmap(&tk, k, p.head_dim, p.n_kv_heads, total_tokens, 128, ld_qkv) ||
+        !make_rows_tmap(&tv, v, p.head_dim, p.n_kv_heads, total_tokens, 128, ld_qkv))
         return cudaErrorInvalidValue;
     // the output is written in kOutBoxRows-row (32-row) TMA boxes (store_rows_tma)
     if (!make_rows_tmap(&tout, out, p.head_dim, p.n_q_heads, total_tokens, kOutBoxRows)) return cudaErrorInvalidValue;

@@ -84,3 +84,50 @@ def assert_rounded_match(got_bits, ref, scale, what):
     # almost all elements are bit-exact
     assert (~exact).sum() <= max(4, exact.size // 200), f"{what}: {int((~exact).sum())} inexact elements"
     return int((~exact).sum())
+
+
+def assert_close_bf16(got, ref, what="", rtol=2.0 ** -8, atol=1e-3, rel_l2=REL_L2):
+    """bf16 results of operators whose outputs are not bounded by 1 (the
+    encoder layer: LayerNorm outputs, residual streams): every element within
+    rtol |ref| + atol of the oracle -- rtol = 2^-8 is one bf16 ulp relative,
+    twice the final rounding's half ulp, the rest of the budget covering
+    fp32-vs-fp64 evaluation inside the operators and the rare intermediate
+    rounding that lands on the other side of a bf16 boundary -- and the
+    relative L2 error over the whole tensor within rel_l2 (5e-3)."""
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    assert np.isfinite(got).all(), f"{what}: non-finite values in the output"
+    d = np.abs(got - ref)
+    bound = rtol * np.abs(ref) + atol
+    bad = d > bound
+    _, rel = errors(got, ref)
+    worst = int(np.argmax(d / bound))
+    assert not bad.any() and rel <= rel_l2, (
+        f"{what}: {int(bad.sum())} of {d.size} elements outside {rtol:.3g} |ref| + {atol:g} (worst at flat index "
+        f"{worst}: got {got.flat[worst]:.6g}, ref {ref.flat[worst]:.6g}); rel-L2 {rel:.3e} (<= {rel_l2})")
+    return float(d.max()), rel
+
+
+def assert_close_rows(got, ref, what="", rtol_row=2.0 ** -7, atol=1e-3, rel_l2=REL_L2):
+    """The encoder layer's output against the oracle.  The layer rounds its
+    residual stream h to bf16 between operators (the oracle at the same
+    boundaries); where the fp32 and fp64 evaluations of h fall on opposite
+    sides of a bf16 rounding boundary the two sides carry h values one ulp
+    apart, and that ulp (2^-8 of |h|) reaches the output y = h + mlp(h)
+    whatever the size of y itself.  So each row is bounded by the scale of
+    the row: max |got - ref| <= 2^-7 (two ulps) * max |ref| of the row +
+    atol; and the relative L2 error over the whole tensor stays within 5e-3."""
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    assert np.isfinite(got).all(), f"{what}: non-finite values in the output"
+    g2 = got.reshape(got.shape[0], -1)
+    r2 = ref.reshape(ref.shape[0], -1)
+    d = np.abs(g2 - r2).max(axis=1)
+    bound = rtol_row * np.abs(r2).max(axis=1) + atol
+    _, rel = errors(got, ref)
+    worst = int(np.argmax(d / bound))
+    assert (d <= bound).all() and rel <= rel_l2, (
+        f"{what}: {int((d > bound).sum())} of {len(d)} rows over {rtol_row:.3g} max|ref row| + {atol:g} (worst row "
+        f"{worst}: max err {d[worst]:.4g}, bound {bound[worst]:.4g}); rel-L2 {rel:.3e} (<= {rel_l2}); elements "
+        f"outside 2^-8|ref|+1e-3: {int((np.abs(got - ref) > 2.0 ** -8 * np.abs(ref) + 1e-3).sum())} of {got.size}")
+    return float(d.max()), rel

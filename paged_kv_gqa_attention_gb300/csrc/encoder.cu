@@ -30,52 +30,67 @@ namespace {
 
 constexpr int kLnMaxChunks = 16;  // d_model up to 16 * 128 = 2048
 
-__global__ void __launch_bounds__(256) layer_norm_kernel(const uint16_t *x, int T, int d, const uint16_t *g,
+// CH: 4-element chunks per lane (d = 128 CH), a compile-time count so the
+// row stays in 4 CH registers per lane (a short kernel that many warps of an
+// SM run at once: that is what keeps enough loads in flight).
+template <int CH>
+__global__ void __launch_bounds__(256) layer_norm_kernel(const uint16_t *x, int T, const uint16_t *g,
                                                          const uint16_t *b, float eps, uint16_t *y) {
+    constexpr int d = 128 * CH;
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (t >= T) return;
-    const int n_chunks = d / 128;  // 4-element chunks per lane
     const uint2 *xr = reinterpret_cast<const uint2 *>(x + (size_t)t * d);
-    float v[kLnMaxChunks][4];
+    uint2 w[CH];
+#pragma unroll
+    for (int c = 0; c < CH; ++c) w[c] = xr[c * 32 + lane];
+    float v[CH][4];
     float s = 0.f;
 #pragma unroll
-    for (int c = 0; c < kLnMaxChunks; ++c) {
-        if (c < n_chunks) {
-            const uint2 w = xr[c * 32 + lane];
-            v[c][0] = bf16lo(w.x), v[c][1] = bf16hi(w.x), v[c][2] = bf16lo(w.y), v[c][3] = bf16hi(w.y);
-            s += (v[c][0] + v[c][1]) + (v[c][2] + v[c][3]);
-        }
+    for (int c = 0; c < CH; ++c) {
+        v[c][0] = bf16lo(w[c].x), v[c][1] = bf16hi(w[c].x), v[c][2] = bf16lo(w[c].y), v[c][3] = bf16hi(w[c].y);
+        s += (v[c][0] + v[c][1]) + (v[c][2] + v[c][3]);
     }
-    const float mean = warp_sum(s) / (float)d;
+    const float mean = warp_sum(s) * (1.0f / d);
     float ss = 0.f;
 #pragma unroll
-    for (int c = 0; c < kLnMaxChunks; ++c) {
-        if (c < n_chunks) {
+    for (int c = 0; c < CH; ++c)
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float u = v[c][j] - mean;
-                ss = fmaf(u, u, ss);
-            }
+        for (int j = 0; j < 4; ++j) {
+            const float u = v[c][j] - mean;
+            ss = fmaf(u, u, ss);
         }
-    }
-    const float inv = rsqrtf(warp_sum(ss) / (float)d + eps);
+    const float inv = rsqrtf(warp_sum(ss) * (1.0f / d) + eps);
     const uint2 *gr = reinterpret_cast<const uint2 *>(g);
     const uint2 *br = reinterpret_cast<const uint2 *>(b);
     uint2 *yr = reinterpret_cast<uint2 *>(y + (size_t)t * d);
 #pragma unroll
-    for (int c = 0; c < kLnMaxChunks; ++c) {
-        if (c < n_chunks) {
-            const uint2 gw = gr[c * 32 + lane], bw = br[c * 32 + lane];
-            const float o0 = fmaf((v[c][0] - mean) * inv, bf16lo(gw.x), bf16lo(bw.x));
-            const float o1 = fmaf((v[c][1] - mean) * inv, bf16hi(gw.x), bf16hi(bw.x));
-            const float o2 = fmaf((v[c][2] - mean) * inv, bf16lo(gw.y), bf16lo(bw.y));
-            const float o3 = fmaf((v[c][3] - mean) * inv, bf16hi(gw.y), bf16hi(bw.y));
-            yr[c * 32 + lane] = make_uint2(pack_bf16x2(o0, o1), pack_bf16x2(o2, o3));
-        }
+    for (int c = 0; c < CH; ++c) {
+        const uint2 gw = gr[c * 32 + lane], bw = br[c * 32 + lane];
+        const float o0 = fmaf((v[c][0] - mean) * inv, bf16lo(gw.x), bf16lo(bw.x));
+        const float o1 = fmaf((v[c][1] - mean) * inv, bf16hi(gw.x), bf16hi(bw.x));
+        const float o2 = fmaf((v[c][2] - mean) * inv, bf16lo(gw.y), bf16lo(bw.y));
+        const float o3 = fmaf((v[c][3] - mean) * inv, bf16hi(gw.y), bf16hi(bw.y));
+        yr[c * 32 + lane] = make_uint2(pack_bf16x2(o0, o1), pack_bf16x2(o2, o3));
     }
+}
+
+template <int CH>
+cudaError_t launch_ln(const void *x, int T, const void *g, const void *b, float eps, void *y, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((T + 7) / 8));
+    cfg.blockDim = dim3(256);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, layer_norm_kernel<CH>, static_cast<const uint16_t *>(x), T,
+                              static_cast<const uint16_t *>(g), static_cast<const uint16_t *>(b), eps,
+                              static_cast<uint16_t *>(y));
 }
 
 size_t align256(size_t n) { return (n + 255) & ~(size_t)255; }
@@ -87,18 +102,26 @@ bool layer_norm_supported(int d) { return d >= 128 && d % 128 == 0 && d / 128 <=
 cudaError_t launch_layer_norm(const void *x, int T, int d, const void *g, const void *b, float eps, void *y,
                               cudaStream_t stream) {
     if (T == 0) return cudaSuccess;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((T + 7) / 8));
-    cfg.blockDim = dim3(256);
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, layer_norm_kernel, static_cast<const uint16_t *>(x), T, d,
-                                       static_cast<const uint16_t *>(g), static_cast<const uint16_t *>(b), eps,
-                                       static_cast<uint16_t *>(y));
+    cudaError_t e;
+    switch (d / 128) {
+        case 1: e = launch_ln<1>(x, T, g, b, eps, y, stream); break;
+        case 2: e = launch_ln<2>(x, T, g, b, eps, y, stream); break;
+        case 3: e = launch_ln<3>(x, T, g, b, eps, y, stream); break;
+        case 4: e = launch_ln<4>(x, T, g, b, eps, y, stream); break;
+        case 5: e = launch_ln<5>(x, T, g, b, eps, y, stream); break;
+        case 6: e = launch_ln<6>(x, T, g, b, eps, y, stream); break;
+        case 7: e = launch_ln<7>(x, T, g, b, eps, y, stream); break;
+        case 8: e = launch_ln<8>(x, T, g, b, eps, y, stream); break;
+        case 9: e = launch_ln<9>(x, T, g, b, eps, y, stream); break;
+        case 10: e = launch_ln<10>(x, T, g, b, eps, y, stream); break;
+        case 11: e = launch_ln<11>(x, T, g, b, eps, y, stream); break;
+        case 12: e = launch_ln<12>(x, T, g, b, eps, y, stream); break;
+        case 13: e = launch_ln<13>(x, T, g, b, eps, y, stream); break;
+        case 14: e = launch_ln<14>(x, T, g, b, eps, y, stream); break;
+        case 15: e = launch_ln<15>(x, T, g, b, eps, y, stream); break;
+        case 16: e = launch_ln<16>(x, T, g, b, eps, y, stream); break;
+        default: return cudaErrorInvalidValue;
+    }
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }

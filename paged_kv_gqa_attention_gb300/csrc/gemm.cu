@@ -19,11 +19,12 @@
 //              one of two fp32 accumulators in TMEM; each stage is released
 //              ("empty") by a tcgen05.commit when its MMAs are done, and an
 //              accumulator is handed to the epilogue ("acc_full") the same way;
-//   warps 2-5  epilogue: each thread owns one row of the 128-row tile (the
-//              TMEM lane quadrant of its warp), reads the accumulator 32
-//              columns at a time, adds bias, applies gelu, adds the residual,
-//              rounds to bf16 and stores; then releases the accumulator
-//              ("acc_empty") so the next-but-one tile can use it.
+//   warps 2-9  epilogue, two warpgroups splitting the tile's columns: each
+//              thread owns one row of the 128-row tile (the TMEM lane
+//              quadrant of its warp), reads the accumulator 32 columns at a
+//              time, adds bias, applies gelu, adds the residual, rounds to
+//              bf16 and stores; then releases the accumulator ("acc_empty")
+//              so the next-but-one tile can use it.
 // With two accumulators the epilogue of tile i overlaps the MMAs of tile
 // i + 1.  Tiles are walked m-block-major (tile = m_blk * tiles_n + n_blk), so
 // the CTAs running at any moment share a few m-blocks of A and every W tile:
@@ -50,7 +51,8 @@ namespace {
 __device__ unsigned int g_status;
 
 constexpr int kBM = 128, kBK = 64;
-constexpr int kThreads = 192;  // producer, MMA, four epilogue warps
+constexpr int kEpiWarps = 8;  // two epilogue warpgroups, each covering all 128 TMEM lanes
+constexpr int kThreads = 32 * (2 + kEpiWarps);  // producer, MMA, epilogue
 
 struct GemmArgs {
     int M, N, K;
@@ -115,7 +117,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar_acc_full + 8 * i, 1);
-            mbar_init(bar_acc_empty + 8 * i, 4);  // one arrival per epilogue warp
+            mbar_init(bar_acc_empty + 8 * i, kEpiWarps);  // one arrival per epilogue warp
         }
         fence_mbar_init();
         tc::prefetch_tmap(&tm_a);
@@ -179,55 +181,64 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     } else {
-        // ---------------- epilogue: warps 2..5, TMEM lane quadrant warp % 4
+        // ---------------- epilogue: warps 2..9, TMEM lane quadrant warp % 4;
+        // warpgroup eg = 0 takes the first half of the tile's 32-column
+        // chunks, eg = 1 the rest
         const int quad = warp & 3;
+        const int eg = (warp - 2) >> 2;
+        constexpr int kChunks = BN / 32;
+        const int c_begin = eg == 0 ? 0 : (kChunks + 1) / 2, c_end = eg == 0 ? (kChunks + 1) / 2 : kChunks;
         const int r_in_tile = quad * 32 + lane;
+        // bias and residual words of chunk c (8 bf16 per word), loaded one
+        // chunk ahead of their use -- the first chunk's before the wait for
+        // the accumulator -- so their latency hides behind the MMAs and the
+        // previous chunk's work instead of stalling every chunk
+        auto side_loads = [&](int n0, int row, int c, uint4 (&bw)[4], uint4 (&rw)[4]) {
+            const int col0 = n0 + c * 32;
+            const int n_groups = max(0, min(4, (a.N - col0) / 8));  // 8-column groups inside N
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+                bw[g] = (a.bias && g < n_groups) ? *reinterpret_cast<const uint4 *>(a.bias + col0 + 8 * g)
+                                                 : make_uint4(0u, 0u, 0u, 0u);
+                rw[g] = (a.res && row < a.M && g < n_groups)
+                            ? *reinterpret_cast<const uint4 *>(a.res + (size_t)row * a.ldr + col0 + 8 * g)
+                            : make_uint4(0u, 0u, 0u, 0u);
+            }
+        };
         int tcount = 0;
         for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++tcount) {
             const int acc = tcount & 1;
             const int m0 = (tile / a.tiles_n) * kBM, n0 = (tile % a.tiles_n) * BN;
+            const int row = m0 + r_in_tile;
+            const bool row_ok = row < a.M;
+            uint4 bw[4], rw[4];
+            side_loads(n0, row, c_begin, bw, rw);
             // warp-uniform: every lane waits on the same phase
             const bool ok = wait(bar_acc_full + 8 * acc, (tcount >> 1) & 1);
             if (!__all_sync(0xffffffffu, ok)) break;
             tc::fence_after();
-            const int row = m0 + r_in_tile;
-            const bool row_ok = row < a.M;
             const uint32_t t_base = tmem + acc * L::kAccCols + ((uint32_t)(quad * 32) << 16);
 #pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
+            for (int c = c_begin; c < c_end; ++c) {
+                uint4 nbw[4] = {}, nrw[4] = {};
+                if (c + 1 < c_end) side_loads(n0, row, c + 1, nbw, nrw);
                 float v[32];
                 tc::tmem_ld32(t_base + c * 32, v);  // warp-collective: every lane, every chunk
                 const int col0 = n0 + c * 32;
-                // 8-column groups inside N (N is a multiple of 8)
                 const int n_groups = max(0, min(4, (a.N - col0) / 8));
-                if (a.bias) {
 #pragma unroll
-                    for (int g = 0; g < 4; ++g) {
-                        if (g < n_groups) {
-                            float bf[8];
-                            unpack8(*reinterpret_cast<const uint4 *>(a.bias + col0 + 8 * g), bf);
+                for (int g = 0; g < 4; ++g) {
+                    float bf[8], rf[8];
+                    unpack8(bw[g], bf);
+                    unpack8(rw[g], rf);
 #pragma unroll
-                            for (int j = 0; j < 8; ++j) v[8 * g + j] += bf[j];
-                        }
+                    for (int j = 0; j < 8; ++j) {
+                        float u = v[8 * g + j] + bf[j];
+                        if (a.act == 1) u = gelu_erf(u);
+                        v[8 * g + j] = u + rf[j];
                     }
-                }
-                if (a.act == 1) {
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) v[j] = gelu_erf(v[j]);
                 }
                 if (row_ok) {
-                    if (a.res) {
-                        const uint16_t *rrow = a.res + (size_t)row * a.ldr + col0;
-#pragma unroll
-                        for (int g = 0; g < 4; ++g) {
-                            if (g < n_groups) {
-                                float rf[8];
-                                unpack8(*reinterpret_cast<const uint4 *>(rrow + 8 * g), rf);
-#pragma unroll
-                                for (int j = 0; j < 8; ++j) v[8 * g + j] += rf[j];
-                            }
-                        }
-                    }
                     uint16_t *orow = a.out + (size_t)row * a.ldc + col0;
 #pragma unroll
                     for (int g = 0; g < 4; ++g) {
@@ -238,6 +249,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 __syncwarp();
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                    bw[g] = nbw[g];
+                    rw[g] = nrw[g];
+                }
             }
             // every TMEM read of this accumulator is done: hand it back
             tc::fence_before();

@@ -103,3 +103,53 @@ def test_capture_reports_an_invalid_call():
     with pytest.raises(qa.QAError) as e:
         qa.qa_decode_graph_create([q], [kp], [vp], pt, sl, [torch.empty_like(q)], workspace=tiny_ws)
     assert "workspace" in str(e.value)
+
+
+def test_a_set_of_buckets_captured_side_by_side():
+    # a serving loop keeps one captured step per decode batch size and per
+    # packed prefill bucket (M* page, "Serving notes": graphs captured per
+    # decode batch and per prefill bucket) and replays whichever the step
+    # needs: two decode batches and two prefill buckets, captured up front,
+    # replayed interleaved with refills in between, each against the oracle
+    decode_sets = {}
+    for B, lengths in ((2, (33, 700)), (5, (1, 16, 17, 250, 1999))):
+        base = wl.decode_workload(540 + B, lengths, num_pages=220, max_pages=125)
+        d = {k: to_dev(base[k]) for k in ("q", "k_pages", "v_pages", "page_table", "seq_lens")}
+        ws = torch.zeros(qa.qa_decode_workspace_size(B, 2000, num_pages=220, max_pages_per_seq=125),
+                         dtype=torch.uint8, device="cuda")
+        out = torch.empty_like(d["q"])
+        g = qa.qa_decode_graph_create([d["q"]], [d["k_pages"]], [d["v_pages"]], d["page_table"], d["seq_lens"],
+                                      [out], workspace=ws)
+        decode_sets[B] = (base, d, out, g)
+    prefill_sets = {}
+    for name, lengths in (("small", (64, 9)), ("large", (300, 129, 77))):
+        base = wl.prefill_workload(550 + len(lengths), lengths, num_pages=64, max_pages=20)
+        d = {k: to_dev(base[k]) for k in ("q", "k", "v", "cu_seqlens", "page_table", "k_pages", "v_pages")}
+        out = torch.empty_like(d["q"])
+        g = qa.qa_prefill_graph_create([d["q"]], [d["k"]], [d["v"]], d["cu_seqlens"], d["page_table"],
+                                       [d["k_pages"]], [d["v_pages"]], [out])
+        prefill_sets[name] = (base, d, out, g)
+    rng = wl.rng_for(560)
+    for rnd in range(2):
+        for B, (base, d, out, g) in decode_sets.items():
+            q = wl.normal_bf16(rng, base["q"].shape)
+            d["q"].copy_(to_dev(q))
+            g.launch()
+            torch.cuda.synchronize()
+            ref = oracle.decode(q, base["k_pages"], base["v_pages"], base["page_table"], base["seq_lens"])
+            assert_close(f64(out), ref, f"decode batch {B}, round {rnd}")
+        for name, (base, d, out, g) in prefill_sets.items():
+            T = int(base["cu_seqlens"][-1])
+            q = wl.normal_bf16(rng, (T, 16, 128))
+            d["q"].copy_(to_dev(q))
+            g.launch()
+            torch.cuda.synchronize()
+            ref = oracle.prefill(q, base["k"], base["v"], base["cu_seqlens"])
+            assert_close(f64(out), ref, f"prefill bucket {name}, round {rnd}")
+            ekp, evp = oracle.page_write(base["k"], base["v"], base["cu_seqlens"], base["page_table"],
+                                         base["k_pages"], base["v_pages"])
+            np.testing.assert_array_equal(bits(d["k_pages"]), ekp)
+            np.testing.assert_array_equal(bits(d["v_pages"]), evp)
+    for _, _, _, g in list(decode_sets.values()) + list(prefill_sets.values()):
+        g.close()
+    assert qa.qa_device_status() == 0

@@ -172,7 +172,12 @@ size_t qa_decode_workspace_size(int batch, int max_seq_len, const qa_attn_params
  * n_q_heads / n_kv_heads in {1, 2}.  Needs params->workspace of at least
  * qa_decode_workspace_size(batch, ...) bytes, 256-byte aligned, zero-filled
  * before its first use (see qa_decode_workspace_size).  Calls sharing one
- * workspace must be ordered (one stream), since they share its counters. */
+ * workspace must be ordered (one stream), since they share its counters.
+ * q, page_table, seq_lens and out are read and written with plain loads and
+ * stores (only the pools go through the bulk-copy engine), so they may also
+ * be page-locked host memory that the device addresses directly (cudaHostAlloc
+ * under unified addressing): a serving step then needs no copies of its own,
+ * the kernel moves those bytes over the host link itself. */
 qa_status qa_decode_attn(const void *q, const void *k_pages, const void *v_pages,
                          const int32_t *page_table, const int32_t *seq_lens, int batch,
                          void *out, const qa_attn_params *params);

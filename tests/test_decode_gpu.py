@@ -135,3 +135,34 @@ def test_uneven_page_distributions(lengths):
         out = run_decode(w, debug_checks=True)
         ref = oracle.decode(w["q"], w["k_pages"], w["v_pages"], w["page_table"], w["seq_lens"])
         assert_close(f64(out), ref, f"lengths {lengths[:3]}... call {call}")
+
+
+def test_host_mapped_query_table_lengths_and_output():
+    # q, page table, lengths and out in page-locked host memory, passed to the
+    # C ABI as they are (the device reaches them directly); the pools stay in
+    # HBM.  Two calls in a row, each against the oracle.
+    import ctypes
+
+    w = wl.decode_workload(81, (1, 17, 300, 0, 129, 2000), num_pages=200, max_pages=125)
+    kp, vp = to_dev(w["k_pages"]), to_dev(w["v_pages"])
+    hq = torch.from_numpy(w["q"].view(np.int16).copy()).view(torch.bfloat16).pin_memory()
+    hpt = torch.from_numpy(w["page_table"].copy()).pin_memory()
+    hsl = torch.from_numpy(w["seq_lens"].copy()).pin_memory()
+    hout = torch.full(w["q"].shape, float("nan"), dtype=torch.bfloat16).pin_memory()
+    B = len(w["seq_lens"])
+    ws = torch.zeros(qa.qa_decode_workspace_size(B, 2000, num_pages=200, max_pages_per_seq=125), dtype=torch.uint8,
+                     device="cuda")
+    p = qa._params(n_q_heads=16, n_kv_heads=8, head_dim=128, num_pages=200, max_pages_per_seq=125, workspace=ws,
+                   debug_checks=True)
+    ref = oracle.decode(w["q"], w["k_pages"], w["v_pages"], w["page_table"], w["seq_lens"])
+    for call in range(2):
+        hout.fill_(float("nan"))
+        st = qa._lib.qa_decode_attn(ctypes.c_void_p(hq.data_ptr()), ctypes.c_void_p(kp.data_ptr()),
+                                    ctypes.c_void_p(vp.data_ptr()), ctypes.c_void_p(hpt.data_ptr()),
+                                    ctypes.c_void_p(hsl.data_ptr()), B, ctypes.c_void_p(hout.data_ptr()),
+                                    ctypes.byref(p))
+        assert st == 0, qa.qa_last_error()
+        torch.cuda.synchronize()
+        got = wl.bf16_to_f64(hout.view(torch.int16).numpy().view(np.uint16))
+        assert_close(got, ref, f"host-mapped decode, call {call + 1}")
+        assert (wl.bf16_to_f64(hout[3].view(torch.int16).numpy().view(np.uint16)) == 0).all()  # seq_len 0

@@ -152,12 +152,15 @@ def _stream_ptr(stream):
     return ctypes.c_void_p(s.cuda_stream)
 
 
-def _dev(t, name, dtype=None, ndim=None):
+def _dev(t, name, dtype=None, ndim=None, allow_host=False):
+    """Device address of a tensor.  allow_host: a page-locked CPU tensor is
+    accepted too (the decode's q, page table, lengths and output may live in
+    host memory the device addresses directly; see qa.h)."""
     torch = _torch()
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
-    if not t.is_cuda:
-        raise ValueError(f"{name} must be a CUDA tensor")
+    if not (t.is_cuda or (allow_host and t.is_pinned())):
+        raise ValueError(f"{name} must be a CUDA tensor" + (" or page-locked host memory" if allow_host else ""))
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     if dtype is not None and t.dtype != dtype:
@@ -202,7 +205,9 @@ def qa_decode_attn(q, k_pages, v_pages, page_table, seq_lens, out=None, *, works
                    stream=None, debug_checks=False, stable_metadata=False):
     """Paged GQA decode.  q bf16 [B,Hq,D]; pools bf16 [P,16,Hkv,D];
     page_table int32 [B,max_pages]; seq_lens int32 [B].  Returns out bf16
-    [B,Hq,D].  `workspace` is a zero-filled device byte tensor of at least
+    [B,Hq,D].  q, page_table, seq_lens and out may be page-locked CPU
+    tensors (the kernel reads and writes them over the host link; pass
+    `out` then).  `workspace` is a zero-filled device byte tensor of at least
     qa_decode_workspace_size(B, ...) bytes (allocated here if omitted); the
     call leaves its arrival counters at zero, so it can be reused across
     calls without clearing.
@@ -224,10 +229,11 @@ def qa_decode_attn(q, k_pages, v_pages, page_table, seq_lens, out=None, *, works
     p = _params(n_q_heads=Hq, n_kv_heads=Hkv, head_dim=D, page_size=PS, num_pages=P,
                 max_pages_per_seq=page_table.shape[1], scale=scale, stream=stream, workspace=workspace,
                 debug_checks=debug_checks, stable_metadata=stable_metadata)
-    st = _lib.qa_decode_attn(_dev(q, "q", torch.bfloat16, 3), _dev(k_pages, "k_pages", torch.bfloat16, 4),
+    st = _lib.qa_decode_attn(_dev(q, "q", torch.bfloat16, 3, True), _dev(k_pages, "k_pages", torch.bfloat16, 4),
                              _dev(v_pages, "v_pages", torch.bfloat16, 4),
-                             _dev(page_table, "page_table", torch.int32, 2), _dev(seq_lens, "seq_lens", torch.int32, 1),
-                             B, _dev(out, "out", torch.bfloat16, 3), ctypes.byref(p))
+                             _dev(page_table, "page_table", torch.int32, 2, True),
+                             _dev(seq_lens, "seq_lens", torch.int32, 1, True), B,
+                             _dev(out, "out", torch.bfloat16, 3, True), ctypes.byref(p))
     _check("qa_decode_attn", st)
     return out
 
@@ -399,10 +405,10 @@ class QAGraph:
             pass
 
 
-def _ptr_array(ts, name, dtype, ndim):
+def _ptr_array(ts, name, dtype, ndim, allow_host=False):
     arr = (ctypes.c_void_p * len(ts))()
     for i, t in enumerate(ts):
-        arr[i] = _dev(t, f"{name}[{i}]", dtype, ndim).value
+        arr[i] = _dev(t, f"{name}[{i}]", dtype, ndim, allow_host).value
     return arr
 
 
@@ -422,12 +428,13 @@ def qa_decode_graph_create(qs, k_pages, v_pages, page_table, seq_lens, outs, *, 
                 max_pages_per_seq=page_table.shape[1], scale=scale, workspace=workspace,
                 stable_metadata=stable_metadata)
     h = ctypes.c_void_p()
-    st = _lib.qa_decode_graph_create(n, _ptr_array(qs, "q", torch.bfloat16, 3),
+    st = _lib.qa_decode_graph_create(n, _ptr_array(qs, "q", torch.bfloat16, 3, True),
                                      _ptr_array(k_pages, "k_pages", torch.bfloat16, 4),
                                      _ptr_array(v_pages, "v_pages", torch.bfloat16, 4),
-                                     _dev(page_table, "page_table", torch.int32, 2),
-                                     _dev(seq_lens, "seq_lens", torch.int32, 1), B,
-                                     _ptr_array(outs, "out", torch.bfloat16, 3), ctypes.byref(p), ctypes.byref(h))
+                                     _dev(page_table, "page_table", torch.int32, 2, True),
+                                     _dev(seq_lens, "seq_lens", torch.int32, 1, True), B,
+                                     _ptr_array(outs, "out", torch.bfloat16, 3, True), ctypes.byref(p),
+                                     ctypes.byref(h))
     _check("qa_decode_graph_create", st)
     return QAGraph(h, (qs, k_pages, v_pages, page_table, seq_lens, outs, workspace))
 

@@ -115,3 +115,11 @@ def test_bad_cached_page_id_is_reported_not_faulted(cached_page):
     ref = oracle.prefill_chunk(w["q"][r0:r1], w["k"][r0:r1], w["v"][r0:r1], np.array([0, r1 - r0], np.int32),
                                w["n_past"][1:2], w["page_table"][1:2], w["k_pages"], w["v_pages"])
     assert_close(f64(out)[r0:r1], ref, "the request without the bad page")
+
+
+@pytest.mark.parametrize("hq,hkv", [(8, 8), (4, 2)])
+def test_other_head_counts(hq, hkv):
+    past, new = (130, 0, 16), (40, 129, 1)
+    need = [-(-(p + n) // 16) for p, n in zip(past, new)]
+    w = wl.chunk_workload(640 + hq, past, new, num_pages=sum(need) + 5, max_pages=max(need), hq=hq, hkv=hkv)
+    check(w, f"chunked prefill {hq}/{hkv} heads")

@@ -166,3 +166,19 @@ def test_host_mapped_query_table_lengths_and_output():
         got = wl.bf16_to_f64(hout.view(torch.int16).numpy().view(np.uint16))
         assert_close(got, ref, f"host-mapped decode, call {call + 1}")
         assert (wl.bf16_to_f64(hout[3].view(torch.int16).numpy().view(np.uint16)) == 0).all()  # seq_len 0
+
+
+def test_largest_batch():
+    # 4096 requests, the most one call takes (the page prefix sums live in
+    # shared memory), lengths 1..40; one more is rejected before any launch
+    rng = np.random.default_rng(90)
+    lengths = rng.integers(1, 41, size=4096).astype(np.int32)
+    n_pages = int(sum(-(-int(L) // 16) for L in lengths))
+    w = wl.decode_workload(91, lengths, num_pages=n_pages + 3, max_pages=3)
+    out = run_decode(w, debug_checks=True)
+    ref = oracle.decode(w["q"], w["k_pages"], w["v_pages"], w["page_table"], w["seq_lens"])
+    assert_close(f64(out), ref, "4096 requests")
+    big = wl.decode_workload(92, np.ones(4097, np.int32), num_pages=4097, max_pages=1)
+    with pytest.raises(qa.QAError) as e:
+        run_decode(big)
+    assert e.value.status == -1 and "batch 4097" in str(e.value)

@@ -128,3 +128,14 @@ def test_encoder_layer_rejects_bad_arguments():
     with pytest.raises(qa.QAError) as e:
         qa.qa_encoder_layer(x, cu, dw, n_heads=14, ln_eps=1e-5, workspace=small)
     assert e.value.status == -1 and "workspace" in str(e.value)
+
+
+def test_encoder_layer_1p7b_shape_matches_oracle():
+    # the 1.7B tower's layer ("GGUF layout": d_model 1024, 16 heads of 64,
+    # FFN 4096): its widths (3072, 1024, 4096) take the 256-wide N tiles
+    counts = (200, 104, 31)
+    w = wl.encoder_layer_workload(65, counts, d=1024, h=16, d_ffn=4096)
+    cu = oracle.window_plan(counts)
+    got = f64(_run_layer(w, cu))
+    ref = oracle.encoder_layer(w["x"], cu, w["weights"], n_heads=w["n_heads"], eps=w["eps"])
+    assert_close_rows(got, ref, "encoder layer 1.7B shape, 335 tokens")

@@ -93,3 +93,12 @@ def test_overlong_request_is_reported_and_clipped():
                                  w["k_pages"], w["v_pages"])
     np.testing.assert_array_equal(bits(d["k_pages"]), ekp)
     np.testing.assert_array_equal(bits(d["v_pages"]), evp)
+
+
+@pytest.mark.parametrize("hq,hkv", [(8, 8), (4, 2), (2, 1)])
+def test_other_head_counts(hq, hkv):
+    # plain MHA (one query head per KV head: that job writes both the K and
+    # the V rows) and GQA 2:1 with fewer heads than the Thinker's
+    lengths = (130, 7, 256)
+    w = wl.prefill_workload(230 + hq, lengths, num_pages=30, max_pages=16, hq=hq, hkv=hkv)
+    check(w, f"prefill {hq}/{hkv} heads")

@@ -523,25 +523,24 @@ __device__ __forceinline__ void write_kv_pages(const uint8_t *k_tile, const uint
 
 // O += P_hi V + P_lo V with both P terms in TMEM in the chunk layout of
 // softmax_tile_regs: keys [16kk, 16kk + 16) are P_hi columns
-// 32 (kk / 2) + 8 (kk % 2) + [0, 8) and P_lo columns 16 further.  N = 64
-// dims per MMA, V read MN-major.  half = 0 / 1: keys [0, 64) / [64, 128)
-// only (-1: all).  One thread.
+// 32 (kk / 2) + 8 (kk % 2) + [0, 8) and P_lo columns 16 further.  N = D:
+// one MMA covers every dim, V read MN-major across its 64-wide sub-tiles
+// (kSubTileBytes apart) -- half the instructions of one MMA per sub-tile,
+// so the issuing thread, which also owns a softmax row, spends less time
+// waiting for room in the tensor core's queue.  half = 0 / 1: keys [0, 64)
+// / [64, 128) only (-1: all).  One thread.
 template <int D>
 __device__ __forceinline__ void issue_pv_tp(uint32_t tmem, uint32_t o_col, uint32_t v_base, bool accumulate,
                                             int half = -1) {
-    constexpr uint32_t idesc_o = tc::idesc_bf16(128, 64, true);
+    constexpr uint32_t idesc_o = tc::idesc_bf16(128, D, true);
     const int kk0 = half < 0 ? 0 : 4 * half, kk1 = half < 0 ? 8 : kk0 + 4;
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) {
         if (kk < kk0 || kk >= kk1) continue;
         const uint32_t a_hi = tmem + (uint32_t)(kk >> 1) * 32 + (uint32_t)(kk & 1) * 8;
-#pragma unroll
-        for (int sd = 0; sd < D / 64; ++sd) {
-            const uint64_t vdesc = tc::sw128_desc(v_base + sd * tc::kSubTileBytes + kk * 2048);
-            const uint32_t o = o_col + sd * 64;
-            tc::mma_bf16_ts(o, a_hi, vdesc, idesc_o, (accumulate || kk > 0) ? 1u : 0u);
-            tc::mma_bf16_ts(o, a_hi + 16, vdesc, idesc_o, 1u);
-        }
+        const uint64_t vdesc = tc::sw128_desc_mn(v_base + kk * 2048, tc::kSubTileBytes);
+        tc::mma_bf16_ts(o_col, a_hi, vdesc, idesc_o, (accumulate || kk > 0) ? 1u : 0u);
+        tc::mma_bf16_ts(o_col, a_hi + 16, vdesc, idesc_o, 1u);
     }
 }
 

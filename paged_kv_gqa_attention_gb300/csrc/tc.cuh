@@ -31,6 +31,16 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
            ((uint64_t)1u << 46) | ((uint64_t)2u << 61);
 }
 
+// The same for an MN-major operand wider than one 128-byte swizzle atom in
+// its MN dimension (N = 128 of a V tile held as two 64-wide sub-tiles): the
+// leading-dimension byte offset is the distance between consecutive atoms
+// along MN (mn_stride bytes), the stride-dimension offset stays the 1024 B
+// between groups of 8 rows along K.
+__device__ __forceinline__ uint64_t sw128_desc_mn(uint32_t saddr, uint32_t mn_stride) {
+    return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((mn_stride >> 4) & 0x3FFFu) << 16) |
+           ((uint64_t)(1024u >> 4) << 32) | ((uint64_t)1u << 46) | ((uint64_t)2u << 61);
+}
+
 // Instruction descriptor of kind::f16 with bf16 A/B and fp32 accumulation.
 //   bits 4-5 D format (1 = f32), 7-9 A format (1 = bf16), 10-12 B format
 //   (1 = bf16), 15 A major (0 = K), 16 B major (1 = MN), 17-22 N >> 3,

@@ -801,14 +801,21 @@ def _row_window(qa, device, stream, peaks, steps, rows, cpu=None):
     dcu = dev_tensor(cu, device)
     outw = torch.empty(T, 14, 64, dtype=torch.bfloat16, device=device)
 
-    def mkw(c):
-        return lambda: qa.qa_window_attn(c["q"], c["k"], c["v"], dcu, outw, stream=stream)
+    # jobs claimed from a counter in a workspace (the CTAs finish together);
+    # the fixed job order (no workspace) is timed beside it
+    ws = torch.zeros(qa.qa_window_workspace_size(), dtype=torch.uint8, device=device)
 
-    el, _ = graph_time([mkw(c) for c in cps], max(10, steps // 4), 3, stream)
-    t = el / max(10, steps // 4)
+    def mkw(c, workspace):
+        return lambda: qa.qa_window_attn(c["q"], c["k"], c["v"], dcu, outw, workspace=workspace, stream=stream)
+
+    n = max(10, steps // 4)
+    el, _ = graph_time([mkw(c, ws) for c in cps], n, 3, stream)
+    t = el / n
+    el_fixed, _ = graph_time([mkw(c, None) for c in cps], n, 3, stream)
     fl, by = window_flops(cu), window_bytes(T)
     rows["window"] = {"workload": "AuT windowed attention: 8 requests d~U[10,1200] s, 104-token windows, 14 x 64",
                       "total_tokens": T, "windows": int(len(cu) - 1), "us_per_call": round(t * 1e6, 2),
+                      "us_per_call_fixed_job_order": round(el_fixed / n * 1e6, 2),
                       "tflops": round(fl / t / 1e12, 3), "gbs": round(by / t / 1e9, 1),
                       "frac_bf16_peak": round(fl / t / 1e12 / peaks["bf16"], 4),
                       "frac_hbm": round(by / t / 1e9 / peaks["hbm"], 4), "flops": fl, "bytes": by,

@@ -368,10 +368,21 @@ void qa_graph_destroy(qa_graph *graph);
  *   out        bf16 [total_tokens][n_q_heads][head_dim]
  *
  * Every row attends over all rows of its own window and nothing else.
- * Supported: head_dim 64 or 128, windows of any length. */
+ * Supported: head_dim 64 or 128, windows of any length.
+ *
+ * params->workspace is optional.  Without one, the (window, head) jobs go to
+ * the persistent grid's CTAs in a fixed order.  With one (at least
+ * qa_window_workspace_size() bytes, 4-byte aligned, zero-filled before its
+ * first use), CTAs claim the jobs one at a time from a counter in it, so
+ * CTAs that start later or run slower take fewer jobs; each call leaves the
+ * counter zero again.  Calls sharing one workspace must be ordered (one
+ * stream).  The result is the same bit for bit either way. */
 qa_status qa_window_attn(const void *q, const void *k, const void *v,
                          const int32_t *cu_windows, int n_windows, int total_tokens, void *out,
                          const qa_attn_params *params);
+
+/* Bytes of the optional qa_window_attn workspace (its job counter). */
+size_t qa_window_workspace_size(void);
 
 /* Window plan (HOST helper, host pointers).  Cuts each request's encoder
  * tokens into consecutive windows of window_tokens tokens counted from the

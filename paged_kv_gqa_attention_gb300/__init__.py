@@ -22,6 +22,7 @@ import numpy as np
 __all__ = [
     "QA_ABI_VERSION", "QAError", "lib_path", "qa_version", "qa_last_error", "qa_attn_default_params",
     "qa_decode_workspace_size", "qa_decode_attn", "qa_prefill_attn", "qa_window_attn", "qa_window_plan",
+    "qa_window_workspace_size",
     "qa_device_status", "DEVICE_STATUS_BITS", "qa_decode_attn_noalloc", "qa_check_bounded_wait",
     "qa_encoder_workspace_size", "qa_encoder_layer", "qa_linear", "qa_layer_norm", "ENCODER_WEIGHT_NAMES",
 ]
@@ -76,6 +77,8 @@ def _load():
     lib.qa_attn_default_params.argtypes = []
     lib.qa_decode_workspace_size.restype = ctypes.c_size_t
     lib.qa_decode_workspace_size.argtypes = [I, I, PP]
+    lib.qa_window_workspace_size.restype = ctypes.c_size_t
+    lib.qa_window_workspace_size.argtypes = []
     lib.qa_decode_attn.restype = I
     lib.qa_decode_attn.argtypes = [P, P, P, P, P, I, P, PP]
     lib.qa_decode_attn_noalloc.restype = I
@@ -466,15 +469,22 @@ def qa_prefill_graph_create(qs, ks, vs, cu_seqlens, page_table, k_pages, v_pages
     return QAGraph(h, (qs, ks, vs, cu_seqlens, page_table, k_pages, v_pages, outs))
 
 
-def qa_window_attn(q, k, v, cu_windows, out=None, *, scale=0.0, stream=None, debug_checks=False):
+def qa_window_workspace_size() -> int:
+    """Bytes of the optional qa_window_attn workspace (its job counter)."""
+    return int(_lib.qa_window_workspace_size())
+
+
+def qa_window_attn(q, k, v, cu_windows, out=None, *, scale=0.0, workspace=None, stream=None, debug_checks=False):
     """Windowed bidirectional attention.  q/k/v bf16 [T,H,D]; cu_windows
-    int32 [W+1].  Returns out bf16 [T,H,D]."""
+    int32 [W+1].  workspace: optional zero-filled device tensor of at least
+    qa_window_workspace_size() bytes (jobs then claimed from a counter in
+    it).  Returns out bf16 [T,H,D]."""
     torch = _torch()
     T, H, D = q.shape
     W = cu_windows.shape[0] - 1
     if out is None:
         out = torch.empty_like(q)
-    p = _params(n_q_heads=H, n_kv_heads=k.shape[1], head_dim=D, scale=scale, stream=stream,
+    p = _params(n_q_heads=H, n_kv_heads=k.shape[1], head_dim=D, scale=scale, stream=stream, workspace=workspace,
                 debug_checks=debug_checks)
     st = _lib.qa_window_attn(_dev(q, "q", torch.bfloat16, 3), _dev(k, "k", torch.bfloat16, 3),
                              _dev(v, "v", torch.bfloat16, 3), _dev(cu_windows, "cu_windows", torch.int32, 1), W, T,

@@ -68,6 +68,9 @@ struct AttnTcArgs {
     // prefill: segments, cached lengths and page table may be read before the
     // kernel before this one has finished (qa_attn_params::stable_metadata)
     int early;
+    // window: job counter in caller memory (two words, zero), or nullptr for
+    // the static job order
+    int *job_ctr;
 };
 
 template <int D>
@@ -147,51 +150,51 @@ __device__ __forceinline__ void softmax_tile(uint32_t s_row, int n_ok, float sca
     tc::tmem_ld32_wait(ra);
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-        uint32_t pk[16], pl[16];
         uint32_t(&cur)[32] = (c & 1) ? rb : ra;
         uint32_t(&nxt)[32] = (c & 1) ? ra : rb;
-        if (c >= n_chunks) {  // warp-uniform: a dead chunk gets zero probabilities
+        const bool live = c < n_chunks;  // warp-uniform: a dead chunk gets zero probabilities
+        if (live && c + 1 < n_chunks) tc::tmem_ld32_issue(s_row + (c + 1) * 32, nxt);
+        const bool full = c * 32 + 32 <= warp_min;
+        // the chunk's 32 keys in two halves of 16, each written out before
+        // the next is computed (fewer registers live at once):
+        // x = s * scale * log2(e) - m for a pair, on packed fp32; then
+        // P_hi = p truncated to bf16 (exact), P_lo = bf16(p - P_hi)
 #pragma unroll
-            for (int i = 0; i < 16; ++i) pk[i] = pl[i] = 0u;
-        } else {
-            if (c + 1 < n_chunks) tc::tmem_ld32_issue(s_row + (c + 1) * 32, nxt);
-            const bool full = c * 32 + 32 <= warp_min;
-            // x = s * scale * log2(e) - m for a pair, on packed fp32; then
-            // P_hi = p truncated to bf16 (exact), P_lo = bf16(p - P_hi)
-            auto pair = [&](int j) {
-                float2 x = ffma2(make_float2(__uint_as_float(cur[j]), __uint_as_float(cur[j + 1])), scale2, neg_m2);
-                if (!full) {
-                    x.x = c * 32 + j < n_ok ? x.x : -INFINITY;
-                    x.y = c * 32 + j + 1 < n_ok ? x.y : -INFINITY;
-                }
-                const float2 pp = make_float2(exp2_approx(x.x), exp2_approx(x.y));
-                psum4[(j >> 1) & 3] = fadd2(psum4[(j >> 1) & 3], pp);
-                const uint32_t b0 = __float_as_uint(pp.x), b1 = __float_as_uint(pp.y);
-                pk[j >> 1] = __byte_perm(b0, b1, 0x7632);
-                const float2 lo =
-                    fsub2(pp, make_float2(__uint_as_float(b0 & 0xffff0000u), __uint_as_float(b1 & 0xffff0000u)));
-                pl[j >> 1] = pack_bf16x2(lo.x, lo.y);
-            };
+        for (int hf = 0; hf < 2; ++hf) {
+            uint32_t pk[8], pl[8];
+            if (!live || (hf == 1 && half_tail && c == n_chunks - 1)) {
 #pragma unroll
-            for (int j = 0; j < 16; j += 2) pair(j);
-            if (half_tail && c == n_chunks - 1) {
-#pragma unroll
-                for (int i = 8; i < 16; ++i) pk[i] = pl[i] = 0u;
+                for (int i = 0; i < 8; ++i) pk[i] = pl[i] = 0u;
             } else {
 #pragma unroll
-                for (int j = 16; j < 32; j += 2) pair(j);
+                for (int jj = 0; jj < 16; jj += 2) {
+                    const int j = hf * 16 + jj;
+                    float2 x =
+                        ffma2(make_float2(__uint_as_float(cur[j]), __uint_as_float(cur[j + 1])), scale2, neg_m2);
+                    if (!full) {
+                        x.x = c * 32 + j < n_ok ? x.x : -INFINITY;
+                        x.y = c * 32 + j + 1 < n_ok ? x.y : -INFINITY;
+                    }
+                    const float2 pp = make_float2(exp2_approx(x.x), exp2_approx(x.y));
+                    psum4[(j >> 1) & 3] = fadd2(psum4[(j >> 1) & 3], pp);
+                    const uint32_t b0 = __float_as_uint(pp.x), b1 = __float_as_uint(pp.y);
+                    pk[jj >> 1] = __byte_perm(b0, b1, 0x7632);
+                    const float2 lo =
+                        fsub2(pp, make_float2(__uint_as_float(b0 & 0xffff0000u), __uint_as_float(b1 & 0xffff0000u)));
+                    pl[jj >> 1] = pack_bf16x2(lo.x, lo.y);
+                }
             }
-            if (c + 1 < n_chunks) tc::tmem_ld32_wait(nxt);
-        }
-        // P_hi: 32 keys = 16 TMEM columns [16c, 16c + 16) (scores there are consumed)
-        tc::tmem_st16(s_row + c * 16, pk);
-        // P_lo: 4 chunks of 16 bytes, sub-tile c / 2, chunks (c % 2) * 4 + u
+            // P_hi: 16 keys = 8 TMEM columns [16c + 8hf, +8) (scores there are consumed)
+            tc::tmem_st8(s_row + c * 16 + hf * 8, pk);
+            // P_lo: 2 chunks of 16 bytes, sub-tile c / 2, chunks (c % 2) * 4 + 2 hf + u
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const uint32_t chunk = (uint32_t)((c & 1) * 4 + u);
-            const uint32_t off = (uint32_t)(c >> 1) * tc::kSubTileBytes + ((chunk ^ sw) << 4);
-            tc::st_shared_v4(plo_row + off, pl[4 * u], pl[4 * u + 1], pl[4 * u + 2], pl[4 * u + 3]);
+            for (int u = 0; u < 2; ++u) {
+                const uint32_t chunk = (uint32_t)((c & 1) * 4 + hf * 2 + u);
+                const uint32_t off = (uint32_t)(c >> 1) * tc::kSubTileBytes + ((chunk ^ sw) << 4);
+                tc::st_shared_v4(plo_row + off, pl[4 * u], pl[4 * u + 1], pl[4 * u + 2], pl[4 * u + 3]);
+            }
         }
+        if (live && c + 1 < n_chunks) tc::tmem_ld32_wait(nxt);
     }
     tc::tmem_wait_st();
     const float2 psum2 = fadd2(fadd2(psum4[0], psum4[1]), fadd2(psum4[2], psum4[3]));
@@ -366,16 +369,16 @@ constexpr int kOutBoxRows = 32;
 // bf16) sub-tile by sub-tile -- dims [64 sd, 64 sd + 64) of row r at stage +
 // sd * 16 KiB + r * 128 with its 16-byte chunks XOR-swizzled by r, which is
 // the layout of a 128B-swizzled TMA box of 64 dims (8-row swizzle atoms
-// stacked) -- then thread 0 writes the rows of whole kOutBoxRows-row boxes
-// with TMA stores (tensor map tm_out, box {64, 1, kOutBoxRows}; tracked by
-// its bulk group: wait for their reads of shared memory before the stage is
-// reused) and the threads of the remaining rows (< kOutBoxRows) store
-// theirs.  Rows at or past row_end are not written.  CTA-collective (128
-// threads).
+// stacked) -- then thread store_tid writes the rows of whole kOutBoxRows-row
+// boxes with TMA stores (tensor map tm_out, box {64, 1, kOutBoxRows}; tracked
+// by that thread's bulk group: it waits for their reads of shared memory
+// before the stage is reused) and the threads of the remaining rows
+// (< kOutBoxRows) store theirs.  Rows at or past row_end are not written.  r
+// is the thread's row (= threadIdx.x); CTA-collective (128 threads).
 template <int D>
 __device__ __forceinline__ void store_rows_tma(uint32_t o_row, float l, uint32_t stage, const CUtensorMap *tm_out,
-                                               uint16_t *out, int hq, int h, int q0, int row_end) {
-    const int r = threadIdx.x;
+                                               uint16_t *out, int hq, int h, int q0, int row_end, int r,
+                                               int store_tid) {
     const float inv = l > 0.f ? 1.f / l : 0.f;
     const uint32_t my_row = stage + (uint32_t)r * 128u;
     const float2 inv2 = make_float2(inv, inv);
@@ -399,7 +402,7 @@ __device__ __forceinline__ void store_rows_tma(uint32_t o_row, float l, uint32_t
     __syncthreads();
     const int n_rows = min(128, row_end);
     const int full = n_rows / kOutBoxRows * kOutBoxRows;
-    if (r == 0 && full > 0) {
+    if (r == store_tid && full > 0) {
         for (int i = 0; i < full; i += kOutBoxRows)
 #pragma unroll
             for (int sd = 0; sd < D / 64; ++sd)
@@ -568,21 +571,28 @@ __device__ __forceinline__ void issue_v_loads(uint32_t sb, const CUtensorMap *tm
 }
 
 // Window attention, persistent: a grid of a few CTAs per SM walks the jobs
-// (window, head) in the order job = blockIdx.x + i * gridDim.x, job = window *
-// n_heads + head, so the CTAs running at any time hold every head of a run of
-// neighbouring windows: the heads' 128-byte slices of a token's row (all
-// heads side by side) are fetched at about the same time, which keeps DRAM
-// pages open for the whole row rather than reopening them once per head.
-// Barriers and TMEM are set up once per CTA.  Q + K and
-// V land on separate barriers, so S starts before V is in.  The next job's
-// Q and K are requested as soon as the current job's last P V has finished
-// reading shared memory, so they load during the epilogue; the epilogue
-// stages the output rows in the V buffer and writes whole rows per store
-// (store_rows_tma: 32-row TMA stores), after which the next job's V is
-// requested.  Each job
-// is computed as described at the top of this file.  TMEM: 128 columns when
-// every job of the CTA is a single 128-row tile and D = 64 (four CTAs share
-// the 512 columns of an SM), else 256.
+// (window, head), job = window * n_heads + head.  CTA c takes job c first;
+// after that either job c + i * gridDim.x (static order), or, with a job
+// counter (a.job_ctr), the next unclaimed job in index order, so CTAs that
+// run slower (later to start, or on a busier SM) take fewer jobs and every
+// CTA finishes at about the same time.  Either way the CTAs running at any
+// time hold every head of a run of neighbouring windows: the heads' 128-byte
+// slices of a token's row (all heads side by side) are fetched at about the
+// same time, which keeps DRAM pages open for the whole row rather than
+// reopening them once per head.  Barriers and TMEM are set up once per CTA.
+// Q + K and V land on separate barriers, so S starts before V is in.  The
+// next job's Q and K are requested as soon as the current job's last P V
+// has finished reading shared memory, so they load during the epilogue; the
+// epilogue stages the output rows in the V buffer and writes whole rows per
+// store (store_rows_tma: 32-row TMA stores), after which the next job's V is
+// requested.  Each job is computed as described at the top of this file.
+// TMEM: 128 columns when every job is a single 128-row tile and D = 64 (four
+// CTAs share the 512 columns of an SM), else 256.
+//
+// The job counter is two words of caller memory, zero before the launch:
+// [0] counts the claims past the first gridDim.x jobs, [1] the CTAs that
+// have finished claiming; the last of those puts both back to zero, so the
+// next launch on the stream finds them zero again.
 template <int D>
 __global__ void __launch_bounds__(128, D == 64 ? 4 : 2)
     window_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -606,16 +616,51 @@ __global__ void __launch_bounds__(128, D == 64 ? 4 : 2)
         if (blockIdx.x == 0 && tid == 0) atomicOr(status, QA_DEVICE_BAD_SEGMENTS);
         return;
     }
-    // does any job of this CTA span more than one 128-row tile?
+    // does any job span more than one 128-row tile?  (With a job counter a
+    // CTA's jobs are not known ahead: then every window is looked at.)
     int multi = 0;
-    for (int j = blockIdx.x + tid * G; j < n_jobs; j += 128 * G) {
-        const int seg = j / a.hq;
-        multi |= a.cu[seg + 1] - a.cu[seg] > 128;
+    if (a.job_ctr) {
+        for (int sg = tid; sg < a.n_seg; sg += 128) multi |= a.cu[sg + 1] - a.cu[sg] > 128;
+    } else {
+        for (long long j = blockIdx.x + (long long)tid * G; j < n_jobs; j += 128LL * G) {
+            const int seg = (int)(j / a.hq);
+            multi |= a.cu[seg + 1] - a.cu[seg] > 128;
+        }
     }
     multi = __syncthreads_or(multi);
     const uint32_t tmem_cols = (D == 64 && !multi) ? 128u : 256u;
 
     const uint32_t bar_qk = sb + L::kBar, bar_s = bar_qk + 8, bar_o = bar_qk + 16, bar_v = bar_qk + 24;
+    // Job records (job, head, s0, s1) in two shared slots.  Thread 32 fills
+    // slot (i + 1) & 1 at the top of job i -- it knows that job's index one
+    // job ahead (a claim made at the top of job i - 1, whose result has
+    // arrived by then) -- and every thread reads slot i & 1 at the top of
+    // job i (at least one CTA barrier lies between), so no job waits on a
+    // claim or on a global read of the segment array.  Slot i & 1 is
+    // rewritten only in job i + 2, after the barriers of job i + 1 that
+    // follow every read of it.  job >= n_jobs ends the walk.  Job indices
+    // stay below n_jobs + 2 G < 2^32.
+    int *rec = reinterpret_cast<int *>(smem + L::kNext);
+    auto fill = [&](int *slot, uint32_t j) {
+        int v0 = n_jobs, v1 = 0, v2 = 0, v3 = 0;
+        if (j < (uint32_t)n_jobs) {
+            const uint32_t seg = j / (uint32_t)a.hq;
+            v0 = (int)j;
+            v1 = (int)(j - seg * (uint32_t)a.hq);
+            v2 = a.cu[seg];
+            v3 = a.cu[seg + 1];
+        }
+        slot[0] = v0;
+        slot[1] = v1;
+        slot[2] = v2;
+        slot[3] = v3;
+    };
+    // the index of the job after job j (thread 32)
+    auto next_index = [&](uint32_t j) -> uint32_t {
+        if (j >= (uint32_t)n_jobs) return (uint32_t)n_jobs;  // no claims past the end
+        return a.job_ctr ? (uint32_t)G + (uint32_t)atomicAdd(a.job_ctr, 1) : j + (uint32_t)G;
+    };
+    uint32_t ahead = 0;  // thread 32: index of the job after the one in the newest record
     if (tid == 0) {
         mbar_init(bar_qk, 1);
         mbar_init(bar_s, 1);
@@ -625,6 +670,10 @@ __global__ void __launch_bounds__(128, D == 64 ? 4 : 2)
         tc::prefetch_tmap(&tm_q);
         tc::prefetch_tmap(&tm_k);
         tc::prefetch_tmap(&tm_v);
+    }
+    if (tid == 32) {
+        fill(rec, blockIdx.x);
+        ahead = next_index(blockIdx.x);
     }
     if (warp == 0) tc::tmem_alloc(sb + L::kTmemSlot, tmem_cols);
     tc::fence_before();
@@ -638,35 +687,31 @@ __global__ void __launch_bounds__(128, D == 64 ? 4 : 2)
     const uint32_t plo_row = sb + L::kPlo + r * 128;
     const uint32_t sw = (uint32_t)(r & 7);
     bool prefetched = false;  // thread 0: the job's first Q/K tiles are already requested
-    int pf_h = 0, pf_s0 = 0;  // thread 0: head and first row of that job (its V comes later)
 
-    for (int job = blockIdx.x; job < n_jobs; job += G) {
-        const int seg = job / a.hq, h = job % a.hq;
-        const int s0 = a.cu[seg], s1 = a.cu[seg + 1];
-        // one thread off the MMA-issue path reads the next job's bounds into
-        // shared memory for thread 0's early loads (seen after the softmax barrier)
-        int *nx = reinterpret_cast<int *>(smem + L::kNext);
-        if (tid == 32) {
-            const int nj = job + G;
-            int v0 = 0, v1 = 0, v2 = 0;  // (head, s0, s1); s0 == s1: nothing to request
-            if (nj < n_jobs) {
-                const int nseg = nj / a.hq;
-                v0 = nj % a.hq;
-                v1 = a.cu[nseg];
-                v2 = a.cu[nseg + 1];
-            }
-            nx[0] = v0;
-            nx[1] = v1;
-            nx[2] = v2;
+    for (int it = 0;; ++it) {
+        const int *cur = rec + (it & 1) * 4;
+        const int job = cur[0], h = cur[1], s0 = cur[2], s1 = cur[3];
+        if (job >= n_jobs) break;  // uniform: every thread read the same record
+        int *nx = rec + ((it + 1) & 1) * 4;
+        if (tid == 32) {  // off the MMA-issue path
+            fill(nx, ahead);
+            ahead = next_index(ahead);  // used at the top of the next job
         }
-        if (!(0 <= s0 && s0 <= s1 && s1 <= a.total)) {
-            if (tid == 0) atomicOr(status, QA_DEVICE_BAD_SEGMENTS);
-            continue;  // nothing was requested for an invalid job
+        const bool valid = 0 <= s0 && s0 <= s1 && s1 <= a.total;
+        if (!valid && tid == 0) atomicOr(status, QA_DEVICE_BAD_SEGMENTS);
+        const int n_tiles = valid ? (s1 - s0 + 127) / 128 : 0;
+        if (n_tiles == 0) {
+            __syncthreads();  // publishes the next record (uniform: every thread has the same bounds)
+            continue;         // nothing was requested for an empty or invalid job
         }
-        const int n_tiles = (s1 - s0 + 127) / 128;
-        if (n_tiles == 0) continue;
         const bool o_in_s = D == 64 && n_tiles == 1;
         const uint32_t col_o = o_in_s ? 64u : 128u;
+        // the thread that issues a job's output TMA stores and, once they
+        // have read the stage (the V buffer), the next job's V: thread 96 for
+        // a single-tile job, so thread 0 goes straight on to the next job's S;
+        // thread 0 when the job has more query tiles, whose loads it issues
+        // itself into the same buffer
+        const int store_tid = n_tiles == 1 ? 96 : 0;
 
         for (int qt = 0; qt < n_tiles; ++qt) {
             const int q0 = s0 + qt * 128;
@@ -708,31 +753,42 @@ __global__ void __launch_bounds__(128, D == 64 ? 4 : 2)
                 ph_o ^= 1;
                 tc::fence_after();
                 // Q/K/P buffers are free: request the next job's Q and K
+                // (the record was published by the softmax barrier above)
                 if (tid == 0 && last) {
-                    const int nx_h = nx[0], nx_s0 = nx[1], nx_s1 = nx[2];
-                    if (0 <= nx_s0 && nx_s0 < nx_s1 && nx_s1 <= a.total) {
+                    const int nx_job = nx[0], nx_h = nx[1], nx_s0 = nx[2], nx_s1 = nx[3];
+                    if (nx_job < n_jobs && 0 <= nx_s0 && nx_s0 < nx_s1 && nx_s1 <= a.total) {
                         issue_qk_loads<D>(sb, &tm_q, &tm_k, nx_h, nx_h, nx_s0, nx_s0, true, bar_qk);
                         prefetched = true;
-                        // kept in registers: thread 32 rewrites nx for the job
-                        // after next as soon as it passes the epilogue's barrier
-                        pf_h = nx_h;
-                        pf_s0 = nx_s0;
                     }
                 }
             }
             // epilogue staged in the V buffer (free since the last P V)
-            store_rows_tma<D>(t_row + col_o, l, sb + L::kV, &tm_out, a.out, a.hq, h, q0, s1 - q0);
+            store_rows_tma<D>(t_row + col_o, l, sb + L::kV, &tm_out, a.out, a.hq, h, q0, s1 - q0, tid, store_tid);
             tc::fence_before();
             __syncthreads();  // every TMEM read and staging read is done
             // the V buffer is free again once the TMA stores have read it:
-            // request the next job's V
-            if (tid == 0) {
+            // after the last query tile, request the next job's V (its Q and
+            // K went out under the same condition)
+            if (tid == store_tid) {
                 tc::bulk_wait_group_read_all();
-                if (prefetched) issue_v_loads<D>(sb, &tm_v, pf_h, pf_s0, bar_v);
+                if (qt == n_tiles - 1) {
+                    const int nx_job = nx[0], nx_h = nx[1], nx_s0 = nx[2], nx_s1 = nx[3];
+                    if (nx_job < n_jobs && 0 <= nx_s0 && nx_s0 < nx_s1 && nx_s1 <= a.total)
+                        issue_v_loads<D>(sb, &tm_v, nx_h, nx_s0, bar_v);
+                }
             }
         }
     }
 
+    // the CTA has made its last claim (its result was used above); the last
+    // CTA to get here resets the counter for the next launch
+    if (a.job_ctr && tid == 32) {
+        __threadfence();
+        if (atomicAdd(a.job_ctr + 1, 1) == G - 1) {
+            atomicExch(a.job_ctr, 0);
+            atomicExch(a.job_ctr + 1, 0);
+        }
+    }
     if (warp == 0) {
         tc::fence_after();
         tc::tmem_dealloc(tmem, tmem_cols);

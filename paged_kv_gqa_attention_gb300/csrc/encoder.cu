@@ -14,6 +14,8 @@
 // stride 3 d), the output projection with bias and residual fused in its
 // epilogue, LayerNorm, fc1 with bias and gelu fused, fc2 with bias and
 // residual fused.  Every intermediate is bf16 (the operator boundaries).
+// The window attention claims its jobs from a counter in the workspace,
+// which the first LayerNorm zeroes.
 //
 // layer_norm_kernel: one warp per token row; lane l holds 4-element chunks
 // l, l + 32, ... of the row (coalesced 8-byte loads), mean and biased
@@ -35,10 +37,11 @@ constexpr int kLnMaxChunks = 16;  // d_model up to 16 * 128 = 2048
 // SM run at once: that is what keeps enough loads in flight).
 template <int CH>
 __global__ void __launch_bounds__(256) layer_norm_kernel(const uint16_t *x, int T, const uint16_t *g,
-                                                         const uint16_t *b, float eps, uint16_t *y) {
+                                                         const uint16_t *b, float eps, uint16_t *y, int *zero2) {
     constexpr int d = 128 * CH;
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (zero2 && blockIdx.x == 0 && threadIdx.x < 2) zero2[threadIdx.x] = 0;
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (t >= T) return;
@@ -78,7 +81,8 @@ __global__ void __launch_bounds__(256) layer_norm_kernel(const uint16_t *x, int 
 }
 
 template <int CH>
-cudaError_t launch_ln(const void *x, int T, const void *g, const void *b, float eps, void *y, cudaStream_t stream) {
+cudaError_t launch_ln(const void *x, int T, const void *g, const void *b, float eps, void *y, cudaStream_t stream,
+                      int *zero2) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)((T + 7) / 8));
     cfg.blockDim = dim3(256);
@@ -90,7 +94,7 @@ cudaError_t launch_ln(const void *x, int T, const void *g, const void *b, float 
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, layer_norm_kernel<CH>, static_cast<const uint16_t *>(x), T,
                               static_cast<const uint16_t *>(g), static_cast<const uint16_t *>(b), eps,
-                              static_cast<uint16_t *>(y));
+                              static_cast<uint16_t *>(y), zero2);
 }
 
 size_t align256(size_t n) { return (n + 255) & ~(size_t)255; }
@@ -100,26 +104,26 @@ size_t align256(size_t n) { return (n + 255) & ~(size_t)255; }
 bool layer_norm_supported(int d) { return d >= 128 && d % 128 == 0 && d / 128 <= kLnMaxChunks; }
 
 cudaError_t launch_layer_norm(const void *x, int T, int d, const void *g, const void *b, float eps, void *y,
-                              cudaStream_t stream) {
+                              cudaStream_t stream, int *zero2) {
     if (T == 0) return cudaSuccess;
     cudaError_t e;
     switch (d / 128) {
-        case 1: e = launch_ln<1>(x, T, g, b, eps, y, stream); break;
-        case 2: e = launch_ln<2>(x, T, g, b, eps, y, stream); break;
-        case 3: e = launch_ln<3>(x, T, g, b, eps, y, stream); break;
-        case 4: e = launch_ln<4>(x, T, g, b, eps, y, stream); break;
-        case 5: e = launch_ln<5>(x, T, g, b, eps, y, stream); break;
-        case 6: e = launch_ln<6>(x, T, g, b, eps, y, stream); break;
-        case 7: e = launch_ln<7>(x, T, g, b, eps, y, stream); break;
-        case 8: e = launch_ln<8>(x, T, g, b, eps, y, stream); break;
-        case 9: e = launch_ln<9>(x, T, g, b, eps, y, stream); break;
-        case 10: e = launch_ln<10>(x, T, g, b, eps, y, stream); break;
-        case 11: e = launch_ln<11>(x, T, g, b, eps, y, stream); break;
-        case 12: e = launch_ln<12>(x, T, g, b, eps, y, stream); break;
-        case 13: e = launch_ln<13>(x, T, g, b, eps, y, stream); break;
-        case 14: e = launch_ln<14>(x, T, g, b, eps, y, stream); break;
-        case 15: e = launch_ln<15>(x, T, g, b, eps, y, stream); break;
-        case 16: e = launch_ln<16>(x, T, g, b, eps, y, stream); break;
+        case 1: e = launch_ln<1>(x, T, g, b, eps, y, stream, zero2); break;
+        case 2: e = launch_ln<2>(x, T, g, b, eps, y, stream, zero2); break;
+        case 3: e = launch_ln<3>(x, T, g, b, eps, y, stream, zero2); break;
+        case 4: e = launch_ln<4>(x, T, g, b, eps, y, stream, zero2); break;
+        case 5: e = launch_ln<5>(x, T, g, b, eps, y, stream, zero2); break;
+        case 6: e = launch_ln<6>(x, T, g, b, eps, y, stream, zero2); break;
+        case 7: e = launch_ln<7>(x, T, g, b, eps, y, stream, zero2); break;
+        case 8: e = launch_ln<8>(x, T, g, b, eps, y, stream, zero2); break;
+        case 9: e = launch_ln<9>(x, T, g, b, eps, y, stream, zero2); break;
+        case 10: e = launch_ln<10>(x, T, g, b, eps, y, stream, zero2); break;
+        case 11: e = launch_ln<11>(x, T, g, b, eps, y, stream, zero2); break;
+        case 12: e = launch_ln<12>(x, T, g, b, eps, y, stream, zero2); break;
+        case 13: e = launch_ln<13>(x, T, g, b, eps, y, stream, zero2); break;
+        case 14: e = launch_ln<14>(x, T, g, b, eps, y, stream, zero2); break;
+        case 15: e = launch_ln<15>(x, T, g, b, eps, y, stream, zero2); break;
+        case 16: e = launch_ln<16>(x, T, g, b, eps, y, stream, zero2); break;
         default: return cudaErrorInvalidValue;
     }
     if (e != cudaSuccess) return e;
@@ -128,7 +132,8 @@ cudaError_t launch_layer_norm(const void *x, int T, int d, const void *g, const 
 
 EncoderWorkspace encoder_workspace_layout(long long T, int d, int d_ffn) {
     EncoderWorkspace w;
-    w.a = 0;
+    w.ctr = 0;
+    w.a = 256;
     w.qkv = w.a + align256((size_t)T * d * 2);
     w.o = w.qkv + align256((size_t)T * 3 * d * 2);
     w.h = w.o + align256((size_t)T * d * 2);
@@ -144,17 +149,20 @@ cudaError_t launch_encoder_layer(const void *x, const int32_t *cu_windows, int n
     const EncoderWorkspace L = encoder_workspace_layout(T, d, d_ffn);
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     void *a = ws + L.a, *qkv = ws + L.qkv, *o = ws + L.o, *h = ws + L.h, *f = ws + L.f;
+    int *job_ctr = reinterpret_cast<int *>(ws + L.ctr);
     const uint16_t *qkv16 = static_cast<const uint16_t *>(qkv);
     cudaError_t e;
     // attention block
-    if ((e = launch_layer_norm(x, T, d, w.ln1_g, w.ln1_b, eps, a, stream)) != cudaSuccess) return e;
+    // the first LayerNorm also zeroes the window attention's job counter
+    // (the workspace holds anything on entry)
+    if ((e = launch_layer_norm(x, T, d, w.ln1_g, w.ln1_b, eps, a, stream, job_ctr)) != cudaSuccess) return e;
     if ((e = launch_gemm(a, d, T, d, w.w_qkv, 3 * d, w.b_qkv, 0, nullptr, 0, qkv, 3 * d, stream)) != cudaSuccess)
         return e;
     qa_attn_params pw = p;
     pw.n_q_heads = pw.n_kv_heads = H;
     pw.head_dim = d / H;
     if ((e = launch_window(qkv16, qkv16 + d, qkv16 + 2 * d, cu_windows, n_windows, T, o, pw,
-                           1.0f / sqrtf((float)(d / H)), stream, 3LL * d)) != cudaSuccess)
+                           1.0f / sqrtf((float)(d / H)), stream, 3LL * d, job_ctr)) != cudaSuccess)
         return e;
     if ((e = launch_gemm(o, d, T, d, w.w_o, d, w.b_o, 0, x, d, h, d, stream)) != cudaSuccess) return e;
     // MLP block

@@ -306,14 +306,24 @@ QA_API qa_status qa_window_attn(const void *q, const void *k, const void *v, con
     if (!q || !k || !v || !cu_windows || !out) return fail(QA_STATUS_INVALID_PARAMS, "%s: NULL tensor pointer", fn);
     if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) || !aligned(cu_windows, 4))
         return fail(QA_STATUS_INVALID_PARAMS, "%s: tensors must be 16-byte aligned (int32 arrays 4-byte)", fn);
+    int *job_ctr = nullptr;
+    if (p->workspace) {
+        if (p->workspace_bytes < qa_window_workspace_size() || !aligned(p->workspace, 4))
+            return fail(QA_STATUS_INVALID_PARAMS, "%s: workspace of %zu bytes (needs %zu, 4-byte aligned)", fn,
+                        p->workspace_bytes, qa_window_workspace_size());
+        job_ctr = static_cast<int *>(p->workspace);
+    }
     cudaStream_t stream = static_cast<cudaStream_t>(p->stream);
-    st = launch_result(
-        qa::launch_window(q, k, v, cu_windows, n_windows, total_tokens, out, *p, effective_scale(p), stream), fn);
+    st = launch_result(qa::launch_window(q, k, v, cu_windows, n_windows, total_tokens, out, *p, effective_scale(p),
+                                         stream, 0, job_ctr),
+                       fn);
     if (st != QA_STATUS_OK || !p->debug_checks) return st;
     cudaError_t e;
     const unsigned int bits = qa::status_read_clear_window(stream, &e);
     return debug_status(bits, e, fn);
 }
+
+QA_API size_t qa_window_workspace_size(void) { return 256; }
 
 QA_API int qa_window_plan(const int32_t *token_counts, int n_requests, int window_tokens, int32_t *cu_windows,
                           int capacity) {

@@ -51,9 +51,11 @@ unsigned int status_read_clear_append(cudaStream_t stream, cudaError_t *err);
 
 // ---- window (window.cu)
 // ld_qkv: row stride (elements) of q, k and v; 0 = packed (n_q_heads * head_dim)
+// job_ctr: two zero words of device memory (jobs claimed dynamically, the
+// kernel leaves them zero), or nullptr (fixed job order)
 cudaError_t launch_window(const void *q, const void *k, const void *v, const int32_t *cu_windows,
                           int n_windows, int total_tokens, void *out, const qa_attn_params &p,
-                          float scale, cudaStream_t stream, long long ld_qkv = 0);
+                          float scale, cudaStream_t stream, long long ld_qkv = 0, int *job_ctr = nullptr);
 unsigned int status_read_clear_window(cudaStream_t stream, cudaError_t *err);
 
 // ---- dense projections (gemm.cu): out = act(x W^T + bias) + res, bf16,
@@ -64,11 +66,13 @@ unsigned int status_read_clear_gemm(cudaStream_t stream, cudaError_t *err);
 
 // ---- encoder layer (encoder.cu)
 bool layer_norm_supported(int d);
+// zero2: two int32 words the kernel sets to zero as well (nullptr: none)
 cudaError_t launch_layer_norm(const void *x, int T, int d, const void *g, const void *b, float eps, void *y,
-                              cudaStream_t stream);
-// byte offsets of the layer's intermediates in the caller's workspace
+                              cudaStream_t stream, int *zero2 = nullptr);
+// byte offsets of the layer's intermediates in the caller's workspace (ctr:
+// the window attention's job counter)
 struct EncoderWorkspace {
-    size_t a, qkv, o, h, f, total;
+    size_t ctr, a, qkv, o, h, f, total;
 };
 EncoderWorkspace encoder_workspace_layout(long long T, int d, int d_ffn);
 cudaError_t launch_encoder_layer(const void *x, const int32_t *cu_windows, int n_windows, int T, int d, int H,

@@ -7,8 +7,9 @@
 // segment per window of every request.  Row t of window w attends over every
 // row of w and nothing else.  Runs on the tensor cores (attn_tc.cuh,
 // window_tc_kernel): a persistent grid of four CTAs per SM (two for head_dim
-// 128) walks the (window, head) jobs; a 104-token window is one 128-row tile,
-// longer windows loop over query and key tiles.
+// 128) walks the (window, head) jobs -- in a fixed order, or claimed one at a
+// time from a job counter when the caller gives one; a 104-token window is
+// one 128-row tile, longer windows loop over query and key tiles.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -26,7 +27,7 @@ __device__ unsigned int g_status;
 
 cudaError_t launch_window(const void *q, const void *k, const void *v, const int32_t *cu_windows,
                           int n_windows, int total_tokens, void *out, const qa_attn_params &p,
-                          float scale, cudaStream_t stream, long long ld_qkv) {
+                          float scale, cudaStream_t stream, long long ld_qkv, int *job_ctr) {
     if (total_tokens == 0) return cudaSuccess;
     if (p.n_q_heads > 65535) return cudaErrorInvalidValue;
     CUtensorMap tq, tk, tv, tout;
@@ -44,6 +45,7 @@ cudaError_t launch_window(const void *q, const void *k, const void *v, const int
     a.total = total_tokens;
     a.hq = p.n_q_heads;
     a.scale_log2 = scale * kLog2e;
+    a.job_ctr = job_ctr;
     unsigned int *status = nullptr;
     cudaError_t e = cudaGetSymbolAddress(reinterpret_cast<void **>(&status), g_status);
     if (e != cudaSuccess) return e;

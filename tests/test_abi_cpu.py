@@ -136,6 +136,15 @@ def test_invalid_arguments_return_status_without_device(libqa):
     w.n_kv_heads, w.scale = 14, float("nan")
     assert lib.qa_window_attn(fake, fake, fake, fake, 1, 1, fake, ctypes.byref(w)) == -1
     assert "scale" in qa.qa_last_error()
+    # window: an optional workspace must hold the job counter and be 4-byte aligned
+    assert qa.qa_window_workspace_size() >= 8
+    w.scale = 0.0
+    w.workspace, w.workspace_bytes = fake, qa.qa_window_workspace_size() - 1
+    assert lib.qa_window_attn(fake, fake, fake, fake, 1, 1, fake, ctypes.byref(w)) == -1
+    assert "workspace" in qa.qa_last_error()
+    w.workspace, w.workspace_bytes = odd, qa.qa_window_workspace_size()
+    assert lib.qa_window_attn(fake, fake, fake, fake, 1, 1, fake, ctypes.byref(w)) == -1
+    assert "workspace" in qa.qa_last_error()
     # decode append: eps and theta must be positive, pointers non-NULL, gains 8-byte aligned
     app = lib.qa_decode_append
     assert app(fake, fake, fake, fake, fake, 0.0, 1e6, fake, fake, 1, fake, fake, fake, ctypes.byref(p)) == -1

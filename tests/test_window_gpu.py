@@ -85,3 +85,55 @@ def test_workload_aut_window_full():
     err = np.abs(got - ref).max(axis=(1, 2))
     worst = int(np.argmax(err))
     assert err[worst] <= 1e-2, f"token {worst}"
+
+
+def test_many_jobs_with_empty_windows():
+    # more (window, head) jobs than the grid's sub-CTAs, so each one claims
+    # several; empty windows (repeated offsets) scattered among them are
+    # skipped and leave the jobs around them intact
+    rng = np.random.default_rng(7)
+    sizes = [int(s) if rng.random() > 0.2 else 0 for s in rng.integers(1, 129, size=180)]
+    sizes[0] = 0
+    sizes[-1] = 0
+    cu = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    w = wl.window_workload(77, (int(cu[-1]),), h=6)
+    q, k, v = to_dev(w["q"]), to_dev(w["k"]), to_dev(w["v"])
+    out = torch.full_like(q, float("nan"))
+    qa.qa_window_attn(q, k, v, to_dev(cu), out, debug_checks=True)
+    torch.cuda.synchronize()
+    ref = oracle.window(w["q"], w["k"], w["v"], cu)
+    assert_close(f64(out), ref, f"{len(sizes)} windows, {sizes.count(0)} empty")
+
+
+def test_repeated_calls_bit_identical():
+    # which sub-CTA computes a job changes from call to call (jobs are
+    # claimed dynamically); the result of a job does not
+    w = wl.window_aut()
+    cu = to_dev(qa.qa_window_plan(w["token_counts"]))
+    q, k, v = to_dev(w["q"]), to_dev(w["k"]), to_dev(w["v"])
+    first = bits(qa.qa_window_attn(q, k, v, cu))
+    for _ in range(3):
+        np.testing.assert_array_equal(bits(qa.qa_window_attn(q, k, v, cu)), first)
+
+
+def test_job_counter_workspace_same_bits_and_left_zero():
+    # with a workspace the jobs are claimed from a counter in it; the result
+    # is the same bit for bit, and every call leaves the counter zero for the
+    # next one (several calls in a row, two workloads, head_dim 64 and 128,
+    # windows longer than one tile)
+    ws = torch.zeros(qa.qa_window_workspace_size(), dtype=torch.uint8, device="cuda")
+    aut = wl.window_aut()
+    cases = [(aut, qa.qa_window_plan(aut["token_counts"]))]
+    w = wl.window_workload(43, (300, 129, 5), h=4, d=128)
+    cases.append((w, oracle.window_plan((300, 129, 5), 200)))
+    w = wl.window_workload(44, (700, 40), h=14, d=64)
+    cases.append((w, oracle.window_plan((700, 40), 150)))
+    for w, cu in cases:
+        q, k, v, dcu = to_dev(w["q"]), to_dev(w["k"]), to_dev(w["v"]), to_dev(cu)
+        fixed = bits(qa.qa_window_attn(q, k, v, dcu))
+        for _ in range(3):
+            got = qa.qa_window_attn(q, k, v, dcu, workspace=ws, debug_checks=True)
+            np.testing.assert_array_equal(bits(got), fixed)
+            assert int(ws.sum()) == 0, "job counter not reset"
+        if w is not aut:
+            assert_close(f64(got), oracle.window(w["q"], w["k"], w["v"], cu), "workspace")

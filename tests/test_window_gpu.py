@@ -137,3 +137,26 @@ def test_job_counter_workspace_same_bits_and_left_zero():
             assert int(ws.sum()) == 0, "job counter not reset"
         if w is not aut:
             assert_close(f64(got), oracle.window(w["q"], w["k"], w["v"], cu), "workspace")
+
+
+def test_job_counter_survives_malformed_windows():
+    # windows whose bounds are out of range are skipped and reported; the
+    # claims run on past them, so the counter still ends at zero and the
+    # next call on the same workspace is whole
+    ws = torch.zeros(qa.qa_window_workspace_size(), dtype=torch.uint8, device="cuda")
+    w = wl.window_workload(45, (600,), h=14)
+    q, k, v = to_dev(w["q"]), to_dev(w["k"]), to_dev(w["v"])
+    assert qa.qa_device_status() == 0
+    bad = to_dev(np.array([0, 104, 9999, 600], np.int32))  # [104, 9999) and [9999, 600) are invalid
+    out = torch.full_like(q, float("nan"))
+    qa.qa_window_attn(q, k, v, bad, out, workspace=ws)
+    bits_ = qa.qa_device_status()
+    assert bits_ & 0x4, f"status {bits_:#x}"  # bad segments
+    assert int(ws.sum()) == 0, "job counter not reset after skipped windows"
+    ref0 = oracle.window(w["q"][:104], w["k"][:104], w["v"][:104], np.array([0, 104], np.int32))
+    assert_close(f64(out[:104]), ref0, "the valid window beside the malformed ones")
+    assert torch.isnan(out[104:]).all(), "rows of skipped windows were written"
+    cu = oracle.window_plan((600,))
+    fixed = bits(qa.qa_window_attn(q, k, v, to_dev(cu)))
+    np.testing.assert_array_equal(bits(qa.qa_window_attn(q, k, v, to_dev(cu), workspace=ws)), fixed)
+    assert int(ws.sum()) == 0

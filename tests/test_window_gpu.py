@@ -160,3 +160,25 @@ def test_job_counter_survives_malformed_windows():
     fixed = bits(qa.qa_window_attn(q, k, v, to_dev(cu)))
     np.testing.assert_array_equal(bits(qa.qa_window_attn(q, k, v, to_dev(cu), workspace=ws)), fixed)
     assert int(ws.sum()) == 0
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_late_keys_far_above_the_first_block(d):
+    # A few keys of every window score tens of log2 units above the rest
+    # for many rows (keys 30 and 100 are planted as multiples of rows 7 and
+    # 5's queries, x2 and x4: exact in bf16): the row maximum sits late in
+    # the window, far from the first keys, and most probabilities of those
+    # rows underflow against it.
+    counts = (104 * 6 + 40,)
+    w = wl.window_workload(46 + d, counts, h=4, d=d)
+    cu = oracle.window_plan(counts)
+    k = w["k"].copy()
+    qf = (w["q"].astype(np.uint32) << 16).view(np.float32)
+    for s0, s1 in zip(cu[:-1], cu[1:]):
+        for key, row, mult in ((30, 7, 2.0), (100, 5, 4.0)):
+            if s0 + key < s1:
+                k[s0 + key] = ((qf[s0 + row] * mult).view(np.uint32) >> 16).astype(np.uint16)
+    w["k"] = k
+    out = run_window(w, cu, debug_checks=True)
+    ref = oracle.window(w["q"], w["k"], w["v"], cu)
+    assert_close(f64(out), ref, f"D={d}, planted late keys")

@@ -81,7 +81,31 @@ struct GemmLayout {
     static_assert(kStages >= 2, "at least two stages");
 };
 
-__device__ __forceinline__ float gelu_erf(float u) { return 0.5f * u * (1.0f + erff(u * 0.70710678118654752f)); }
+// gelu(u) = u / 2 (1 + erf(u / sqrt 2)), with erf from Abramowitz and Stegun,
+// Handbook of Mathematical Functions, formula 7.1.26: for z >= 0,
+// erf(z) = 1 - (a1 t + a2 t^2 + a3 t^3 + a4 t^4 + a5 t^5) exp(-z^2) with
+// t = 1 / (1 + p z), absolute error at most 1.5e-7 (odd in z) -- far below
+// the bf16 rounding of the result (the approximate reciprocal and exp2 add a
+// few ulps of fp32).  Two MUFU operations and a handful of FMAs per element.
+__device__ __forceinline__ float rcp_approx(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float gelu_erf(float u) {
+    const float z = fabsf(u) * 0.70710678118654752f;
+    const float t = rcp_approx(fmaf(0.3275911f, z, 1.0f));  // 1 + p z >= 1
+    float poly = fmaf(1.061405429f, t, -1.453152027f);
+    poly = fmaf(poly, t, 1.421413741f);
+    poly = fmaf(poly, t, -0.284496736f);
+    poly = fmaf(poly, t, 0.254829592f);
+    poly *= t;
+    const float e = exp2_approx(-z * z * kLog2e);  // exp(-z^2)
+    const float erf_abs = fmaf(-poly, e, 1.0f);
+    const float erf_z = copysignf(erf_abs, u);
+    const float h = 0.5f * u;
+    return fmaf(h, erf_z, h);
+}
 
 // bf16x8 (one 16-byte word) -> 8 floats
 __device__ __forceinline__ void unpack8(uint4 w, float *f) {

@@ -139,3 +139,29 @@ def test_encoder_layer_1p7b_shape_matches_oracle():
     got = f64(_run_layer(w, cu))
     ref = oracle.encoder_layer(w["x"], cu, w["weights"], n_heads=w["n_heads"], eps=w["eps"])
     assert_close_rows(got, ref, "encoder layer 1.7B shape, 335 tokens")
+
+
+def test_gelu_is_exact_to_the_rounding():
+    # every bf16 value in [-8, 8] through qa_linear with an identity weight
+    # (x W^T = x exactly): each output must be a correct bf16 rounding of a
+    # number within 4e-7 (1 + |x|) of the exact u / 2 (1 + erf(u / sqrt 2)),
+    # computed here in fp64 -- the erf approximation's own bound is 1.5e-7
+    import math
+    mag = np.arange(0x3A80, 0x4101, dtype=np.uint16)  # 2^-10 .. 8 (bf16 bit patterns)
+    vals = np.concatenate([[0], mag, mag | 0x8000]).astype(np.uint16)
+    n = 128
+    rows = -(-len(vals) // n)
+    xb = np.zeros(rows * n, np.uint16)
+    xb[:len(vals)] = vals
+    x = xb.reshape(rows, n)
+    w = np.zeros((n, n), np.uint16)
+    w[np.arange(n), np.arange(n)] = 0x3F80  # 1.0
+    out = qa.qa_linear(to_dev(x), to_dev(w), gelu=True, debug_checks=True)
+    torch.cuda.synchronize()
+    got = f64(out).reshape(-1)
+    xf = (x.reshape(-1).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    exact = np.array([u * 0.5 * (1.0 + math.erf(u / math.sqrt(2.0))) for u in xf])
+    ulp = np.where(exact != 0, 2.0 ** (np.floor(np.log2(np.abs(exact) + 1e-300)) - 7), 0.0)
+    bound = 0.5 * ulp + 4e-7 * (1.0 + np.abs(xf))
+    bad = np.abs(got - exact) > bound
+    assert not bad.any(), f"{bad.sum()} outputs, first at x={xf[bad][0]}: got {got[bad][0]} exact {exact[bad][0]}"

@@ -182,3 +182,28 @@ def test_late_keys_far_above_the_first_block(d):
     out = run_window(w, cu, debug_checks=True)
     ref = oracle.window(w["q"], w["k"], w["v"], cu)
     assert_close(f64(out), ref, f"D={d}, planted late keys")
+
+
+def test_job_counter_under_graph_replay():
+    # the counter is reset by the kernel itself, so a captured call replays
+    # with the same result every time (a CUDA graph of three calls, replayed
+    # three times on its own stream)
+    w = wl.window_aut()
+    cu = to_dev(qa.qa_window_plan(w["token_counts"]))
+    q, k, v = to_dev(w["q"]), to_dev(w["k"]), to_dev(w["v"])
+    ws = torch.zeros(qa.qa_window_workspace_size(), dtype=torch.uint8, device="cuda")
+    fixed = bits(qa.qa_window_attn(q, k, v, cu))
+    out = torch.empty_like(q)
+    s = torch.cuda.Stream()
+    qa.qa_window_attn(q, k, v, cu, out, workspace=ws, stream=s)  # loads the kernel before the capture
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for _ in range(3):
+            qa.qa_window_attn(q, k, v, cu, out, workspace=ws, stream=s)
+    for _ in range(3):
+        out.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(bits(out), fixed)
+        assert int(ws.sum()) == 0

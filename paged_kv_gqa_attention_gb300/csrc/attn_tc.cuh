@@ -112,6 +112,7 @@ __device__ __forceinline__ void softmax_tile(uint32_t s_row, int n_ok, float sca
     // the last live chunk holds at most 16 live keys: its upper half is
     // neither reduced nor exponentiated (its probabilities are written as 0)
     const bool half_tail = warp_max - (n_chunks - 1) * 32 <= 16;
+    const uint32_t plo_sw = plo_row | (sw << 4);
     uint32_t ra[32], rb[32];
     // four independent running maxima and sums: no reduction is one long
     // dependency chain
@@ -124,14 +125,26 @@ __device__ __forceinline__ void softmax_tile(uint32_t s_row, int n_ok, float sca
         uint32_t(&cur)[32] = (c & 1) ? rb : ra;
         uint32_t(&nxt)[32] = (c & 1) ? ra : rb;
         if (c + 1 < n_chunks) tc::tmem_ld32_issue(s_row + (c + 1) * 32, nxt);
+        // masked keys become -inf in place (only the 16 keys the max reads
+        // when the chunk is a half tail)
+        // and go back to TMEM, so the exponential pass reads them masked
+        const bool tail_chunk = half_tail && c == n_chunks - 1;
         if (c * 32 + 32 > warp_min) {
+            if (tail_chunk) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) cur[j] = c * 32 + j < n_ok ? cur[j] : __float_as_uint(-INFINITY);
+                for (int j = 0; j < 16; ++j) cur[j] = c * 32 + j < n_ok ? cur[j] : __float_as_uint(-INFINITY);
+                tc::tmem_st16(s_row + c * 32, *reinterpret_cast<const uint32_t(*)[16]>(&cur[0]));
+            } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) cur[j] = c * 32 + j < n_ok ? cur[j] : __float_as_uint(-INFINITY);
+                tc::tmem_st16(s_row + c * 32, *reinterpret_cast<const uint32_t(*)[16]>(&cur[0]));
+                tc::tmem_st16(s_row + c * 32 + 16, *reinterpret_cast<const uint32_t(*)[16]>(&cur[16]));
+            }
         }
 #pragma unroll
         for (int j = 0; j < 16; j += 2)
             mx4[(j >> 1) & 3] = fmax3(mx4[(j >> 1) & 3], __uint_as_float(cur[j]), __uint_as_float(cur[j + 1]));
-        if (!(half_tail && c == n_chunks - 1)) {
+        if (!tail_chunk) {
 #pragma unroll
             for (int j = 16; j < 32; j += 2)
                 mx4[(j >> 1) & 3] = fmax3(mx4[(j >> 1) & 3], __uint_as_float(cur[j]), __uint_as_float(cur[j + 1]));
@@ -146,6 +159,7 @@ __device__ __forceinline__ void softmax_tile(uint32_t s_row, int n_ok, float sca
     float2 psum4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
     const float2 scale2 = make_float2(scale_log2, scale_log2);
     const float2 neg_m2 = make_float2(-m_new, -m_new);
+    tc::tmem_wait_st();  // the masked chunk's write-back lands before it is read again
     tc::tmem_ld32_issue(s_row, ra);
     tc::tmem_ld32_wait(ra);
 #pragma unroll
@@ -154,7 +168,6 @@ __device__ __forceinline__ void softmax_tile(uint32_t s_row, int n_ok, float sca
         uint32_t(&nxt)[32] = (c & 1) ? ra : rb;
         const bool live = c < n_chunks;  // warp-uniform: a dead chunk gets zero probabilities
         if (live && c + 1 < n_chunks) tc::tmem_ld32_issue(s_row + (c + 1) * 32, nxt);
-        const bool full = c * 32 + 32 <= warp_min;
         // the chunk's 32 keys in two halves of 16, each written out before
         // the next is computed (fewer registers live at once):
         // x = s * scale * log2(e) - m for a pair, on packed fp32; then
@@ -169,29 +182,30 @@ __device__ __forceinline__ void softmax_tile(uint32_t s_row, int n_ok, float sca
 #pragma unroll
                 for (int jj = 0; jj < 16; jj += 2) {
                     const int j = hf * 16 + jj;
-                    float2 x =
+                    // masked keys read back as -inf (the max pass wrote them)
+                    const float2 x =
                         ffma2(make_float2(__uint_as_float(cur[j]), __uint_as_float(cur[j + 1])), scale2, neg_m2);
-                    if (!full) {
-                        x.x = c * 32 + j < n_ok ? x.x : -INFINITY;
-                        x.y = c * 32 + j + 1 < n_ok ? x.y : -INFINITY;
-                    }
                     const float2 pp = make_float2(exp2_approx(x.x), exp2_approx(x.y));
                     psum4[(j >> 1) & 3] = fadd2(psum4[(j >> 1) & 3], pp);
-                    const uint32_t b0 = __float_as_uint(pp.x), b1 = __float_as_uint(pp.y);
-                    pk[jj >> 1] = __byte_perm(b0, b1, 0x7632);
-                    const float2 lo =
-                        fsub2(pp, make_float2(__uint_as_float(b0 & 0xffff0000u), __uint_as_float(b1 & 0xffff0000u)));
+                    // P_hi of both keys in one word; the two truncated values
+                    // back as floats from that word (a multiply by 2^16 for
+                    // the low half, which the multiply-add pipe can take)
+                    const uint32_t w = __byte_perm(__float_as_uint(pp.x), __float_as_uint(pp.y), 0x7632);
+                    pk[jj >> 1] = w;
+                    const float2 lo = fsub2(pp, make_float2(__uint_as_float(w * 65536u), __uint_as_float(w & 0xffff0000u)));
                     pl[jj >> 1] = pack_bf16x2(lo.x, lo.y);
                 }
             }
             // P_hi: 16 keys = 8 TMEM columns [16c + 8hf, +8) (scores there are consumed)
             tc::tmem_st8(s_row + c * 16 + hf * 8, pk);
             // P_lo: 2 chunks of 16 bytes, sub-tile c / 2, chunks (c % 2) * 4 + 2 hf + u
+            // (plo_row's bits 4-6 are zero: the swizzle is one XOR of a base
+            // that already holds sw)
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
                 const uint32_t chunk = (uint32_t)((c & 1) * 4 + hf * 2 + u);
-                const uint32_t off = (uint32_t)(c >> 1) * tc::kSubTileBytes + ((chunk ^ sw) << 4);
-                tc::st_shared_v4(plo_row + off, pl[4 * u], pl[4 * u + 1], pl[4 * u + 2], pl[4 * u + 3]);
+                tc::st_shared_v4((plo_sw ^ (chunk << 4)) + (uint32_t)(c >> 1) * tc::kSubTileBytes, pl[4 * u],
+                                 pl[4 * u + 1], pl[4 * u + 2], pl[4 * u + 3]);
             }
         }
         if (live && c + 1 < n_chunks) tc::tmem_ld32_wait(nxt);
@@ -381,6 +395,9 @@ __device__ __forceinline__ void store_rows_tma(uint32_t o_row, float l, uint32_t
                                                int store_tid) {
     const float inv = l > 0.f ? 1.f / l : 0.f;
     const uint32_t my_row = stage + (uint32_t)r * 128u;
+    // my_row's bits 4-6 are zero: the chunk swizzle is one XOR of a base
+    // that already holds r & 7
+    const uint32_t my_row_sw = my_row | ((uint32_t)(r & 7) << 4);
     const float2 inv2 = make_float2(inv, inv);
 #pragma unroll
     for (int c = 0; c < D / 32; ++c) {
@@ -393,8 +410,8 @@ __device__ __forceinline__ void store_rows_tma(uint32_t o_row, float l, uint32_t
             const float2 o1 = fmul2(make_float2(ov[8 * u + 2], ov[8 * u + 3]), inv2);
             const float2 o2 = fmul2(make_float2(ov[8 * u + 4], ov[8 * u + 5]), inv2);
             const float2 o3 = fmul2(make_float2(ov[8 * u + 6], ov[8 * u + 7]), inv2);
-            const uint32_t pos = (uint32_t)((c & 1) * 4 + u) ^ (uint32_t)(r & 7);
-            tc::st_shared_v4(my_row + sub + pos * 16, pack_bf16x2(o0.x, o0.y), pack_bf16x2(o1.x, o1.y),
+            const uint32_t chunk = (uint32_t)((c & 1) * 4 + u);
+            tc::st_shared_v4((my_row_sw ^ (chunk << 4)) + sub, pack_bf16x2(o0.x, o0.y), pack_bf16x2(o1.x, o1.y),
                              pack_bf16x2(o2.x, o2.y), pack_bf16x2(o3.x, o3.y));
         }
     }

@@ -748,8 +748,11 @@ __global__ void __launch_bounds__(128, D == 64 ? 4 : 2)
                     tc::mma_commit(bar_s);
                 }
                 ph_qk ^= 1;
-                mbar_wait(bar_s, ph_s, status);
+                // warp 0 waits for S; the other warps sleep in the CTA
+                // barrier instead of re-testing the mbarrier
+                if (warp == 0) mbar_wait(bar_s, ph_s, status);
                 ph_s ^= 1;
+                __syncthreads();
                 tc::fence_after();
 
                 int n_ok = min(128, s1 - k0);
@@ -766,8 +769,9 @@ __global__ void __launch_bounds__(128, D == 64 ? 4 : 2)
                     tc::mma_commit(bar_o);
                 }
                 ph_v ^= 1;
-                mbar_wait(bar_o, ph_o, status);
+                if (warp == 0) mbar_wait(bar_o, ph_o, status);  // the other warps sleep in the barrier
                 ph_o ^= 1;
+                __syncthreads();
                 tc::fence_after();
                 // Q/K/P buffers are free: request the next job's Q and K
                 // (the record was published by the softmax barrier above)

@@ -10,24 +10,33 @@
 // none.  fp32 accumulation, bf16 result (round to nearest even) with any row
 // stride, so the fused q|k|v projection writes one [M][3 d] buffer.
 //
-// Persistent, warp-specialised, one CTA per SM:
-//   warp 0     producer: TMA loads of 128 x 64 A tiles and BN x 64 W tiles
-//              (128-byte swizzled, K-major) into a ring of shared-memory
-//              stages, each completing on its "full" mbarrier;
-//   warp 1     allocates TMEM; one lane issues tcgen05.mma (M = 128,
-//              N = BN, K = 16 per instruction, four per 64-wide stage) into
-//              one of two fp32 accumulators in TMEM; each stage is released
-//              ("empty") by a tcgen05.commit when its MMAs are done, and an
-//              accumulator is handed to the epilogue ("acc_full") the same way;
-//   warps 2-9  epilogue, two warpgroups splitting the tile's columns: each
-//              thread owns one row of the 128-row tile (the TMEM lane
-//              quadrant of its warp), reads the accumulator 32 columns at a
-//              time, adds bias, applies gelu, adds the residual, rounds to
-//              bf16 and stores; then releases the accumulator ("acc_empty")
-//              so the next-but-one tile can use it.
+// Persistent, warp-specialised, one CTA per SM, the CTAs in pairs (clusters
+// of two on two SMs) that share one 256 x BN output tile: rank r of the pair
+// holds rows [128 r, 128 r + 128) of the tile's A block and W rows
+// [BN / 2 r, BN / 2 (r + 1)) of its W block, and one tcgen05.mma.cta_group::2
+// (M = 256) reads both CTAs' halves and writes each CTA's 128 rows of the
+// accumulator into that CTA's TMEM -- so an SM takes in 16 KiB of A and
+// BN / 2 x 128 bytes of W per 64-wide K step instead of the whole W tile:
+//   warp 0     producer (both CTAs): TMA loads of its 128 x 64 A tile and its
+//              BN / 2 x 64 W half (128-byte swizzled, K-major) into a ring of
+//              shared-memory stages; both CTAs' loads of a stage complete on
+//              rank 0's "full" mbarrier, whose producer expects the bytes of
+//              both;
+//   warp 1     allocates the pair's TMEM; on rank 0 one lane issues the MMAs
+//              (K = 16 per instruction, four per 64-wide stage) into one of two
+//              fp32 accumulators; a stage is released ("empty") in both CTAs
+//              by a multicast tcgen05.commit when its MMAs are done, and an
+//              accumulator is handed to both epilogues ("acc_full") the same
+//              way;
+//   warps 2-9  epilogue (both CTAs), two warpgroups splitting the tile's
+//              columns: each thread owns one row of its CTA's 128 rows (the
+//              TMEM lane quadrant of its warp), reads the accumulator 32
+//              columns at a time, adds bias, applies gelu, adds the residual,
+//              rounds to bf16 and stores; then releases the accumulator on
+//              rank 0's "acc_empty" barrier so the next-but-one tile can use it.
 // With two accumulators the epilogue of tile i overlaps the MMAs of tile
 // i + 1.  Tiles are walked m-block-major (tile = m_blk * tiles_n + n_blk), so
-// the CTAs running at any moment share a few m-blocks of A and every W tile:
+// the pairs running at any moment share a few m-blocks of A and every W tile:
 // A is fetched from HBM about once, W stays in L2.
 //
 // Rows past M and columns past N (ragged last tiles) are zero-filled by TMA
@@ -50,7 +59,7 @@ namespace {
 
 __device__ unsigned int g_status;
 
-constexpr int kBM = 128, kBK = 64;
+constexpr int kBM = 128, kBK = 64;  // rows of A per CTA (256 per pair), K step
 constexpr int kEpiWarps = 8;  // two epilogue warpgroups, each covering all 128 TMEM lanes
 constexpr int kThreads = 32 * (2 + kEpiWarps);  // producer, MMA, epilogue
 
@@ -66,8 +75,8 @@ struct GemmArgs {
 
 template <int BN>
 struct GemmLayout {
-    static constexpr uint32_t kA = kBM * kBK * 2;  // 16 KiB
-    static constexpr uint32_t kB = BN * kBK * 2;
+    static constexpr uint32_t kA = kBM * kBK * 2;        // 16 KiB
+    static constexpr uint32_t kB = (BN / 2) * kBK * 2;   // this CTA's half of the W tile
     static constexpr uint32_t kStage = kA + kB;
     static constexpr int kStages = (220 * 1024) / kStage < 8 ? (220 * 1024) / kStage : 8;
     static constexpr uint32_t kBar = kStages * kStage;  // full[S], empty[S], acc_full[2], acc_empty[2]
@@ -123,10 +132,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sb = (raw + 1023u) & ~1023u;
     uint8_t *smem = smem_raw + (sb - raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = tc::cluster_rank();  // 0: issues the pair's MMAs
     const uint32_t bar_full = sb + L::kBar, bar_empty = bar_full + L::kStages * 8;
     const uint32_t bar_acc_full = bar_empty + L::kStages * 8, bar_acc_empty = bar_acc_full + 16;
-    const int n_tiles = a.tiles_m * a.tiles_n;
+    const int n_tiles = a.tiles_m * a.tiles_n;  // 256-row tiles
     const int n_kb = (a.K + kBK - 1) / kBK;
+    const int pair = (int)blockIdx.x >> 1, n_pairs = (int)gridDim.x >> 1;
 
     // a programmatic dependent of the kernel before it: wait for its writes
     // before reading anything, then let the next kernel be scheduled
@@ -136,24 +147,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         *reinterpret_cast<volatile int *>(smem + L::kAbort) = 0;
         for (int s = 0; s < L::kStages; ++s) {
-            mbar_init(bar_full + 8 * s, 1);
-            mbar_init(bar_empty + 8 * s, 1);
+            mbar_init(bar_full + 8 * s, 1);   // rank 0's: its producer's arrival (both CTAs' bytes)
+            mbar_init(bar_empty + 8 * s, 1);  // the MMA thread's multicast commit
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar_acc_full + 8 * i, 1);
-            mbar_init(bar_acc_empty + 8 * i, kEpiWarps);  // one arrival per epilogue warp
+            mbar_init(bar_acc_empty + 8 * i, 2 * kEpiWarps);  // rank 0's: every epilogue warp of the pair
         }
         fence_mbar_init();
         tc::prefetch_tmap(&tm_a);
         tc::prefetch_tmap(&tm_w);
     }
-    if (warp == 1) tc::tmem_alloc(sb + L::kTmemSlot, 512);
+    if (warp == 1) tc::tmem_alloc_pair(sb + L::kTmemSlot, 512);
     tc::fence_before();
-    __syncthreads();
+    tc::cluster_sync();  // both CTAs' barriers are set up before either signals the other's
     tc::fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + L::kTmemSlot);
-    // A wait that expires (a fault elsewhere) stops every role at its next
-    // wait instead of letting each later wait expire in turn.
+    // A wait that expires (a fault elsewhere) stops every role of this CTA
+    // at its next wait instead of letting each later wait expire in turn.
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kAbort);
     auto wait = [&](uint32_t bar, uint32_t parity) -> bool {
         if (*abort_flag) return false;
@@ -161,31 +172,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         *abort_flag = 1;
         return false;
     };
+    const uint32_t full0 = tc::map_to_rank(bar_full, 0);            // rank 0's full barriers
+    const uint32_t acc_empty0 = tc::map_to_rank(bar_acc_empty, 0);  // rank 0's acc_empty barriers
 
     if (warp == 0) {
-        // ---------------- producer
+        // ---------------- producer (both CTAs): this CTA's A rows and W half
         if (lane == 0) {
             int it = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
-                const int m0 = (tile / a.tiles_n) * kBM, n0 = (tile % a.tiles_n) * BN;
+            for (int tile = pair; tile < n_tiles && ok; tile += n_pairs) {
+                const int m0 = (tile / a.tiles_n) * (2 * kBM) + (int)rank * kBM;
+                const int n0 = (tile % a.tiles_n) * BN + (int)rank * (BN / 2);
                 for (int kb = 0; kb < n_kb; ++kb, ++it) {
                     const int s = it % L::kStages;
                     if (it >= L::kStages && !(ok = wait(bar_empty + 8 * s, ((it / L::kStages) & 1) ^ 1))) break;
                     const uint32_t st = sb + s * L::kStage;
-                    mbar_arrive_expect_tx(bar_full + 8 * s, L::kStage);
-                    tc::tma_load_2d(st, &tm_a, kb * kBK, m0, bar_full + 8 * s);
-                    tc::tma_load_2d(st + L::kA, &tm_w, kb * kBK, n0, bar_full + 8 * s);
+                    // rank 0 expects the bytes of both CTAs' loads; rank 1's
+                    // loads only count theirs on rank 0's barrier (a stage is
+                    // refilled only after the MMAs that read it, so no count
+                    // from the next round can meet the current one)
+                    if (rank == 0) mbar_arrive_expect_tx(bar_full + 8 * s, 2 * L::kStage);
+                    tc::tma_load_2d_pair(st, &tm_a, kb * kBK, m0, full0 + 8 * s);
+                    tc::tma_load_2d_pair(st + L::kA, &tm_w, kb * kBK, n0, full0 + 8 * s);
                 }
             }
         }
     } else if (warp == 1) {
-        // ---------------- MMA issue
-        if (lane == 0) {
-            constexpr uint32_t idesc = tc::idesc_bf16(kBM, BN, false);
+        // ---------------- MMA issue (rank 0 only)
+        if (lane == 0 && rank == 0) {
+            constexpr uint32_t idesc = tc::idesc_bf16(2 * kBM, BN, false);
             int it = 0, tcount = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x, ++tcount) {
+            for (int tile = pair; tile < n_tiles && ok; tile += n_pairs, ++tcount) {
                 const int acc = tcount & 1;
                 if (tcount >= 2 && !(ok = wait(bar_acc_empty + 8 * acc, ((tcount >> 1) & 1) ^ 1))) break;
                 tc::fence_after();
@@ -197,22 +215,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t st = sb + s * L::kStage;
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; ++kk)
-                        tc::mma_bf16(d_tmem, tc::sw128_desc(st + kk * 32), tc::sw128_desc(st + L::kA + kk * 32), idesc,
-                                     (kb > 0 || kk > 0) ? 1u : 0u);
-                    tc::mma_commit(bar_empty + 8 * s);  // the stage is free once these MMAs are done
+                        tc::mma_bf16_pair(d_tmem, tc::sw128_desc(st + kk * 32), tc::sw128_desc(st + L::kA + kk * 32),
+                                          idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+                    tc::mma_commit_pair(bar_empty + 8 * s);  // the stage is free (both CTAs) once these are done
                 }
-                if (ok) tc::mma_commit(bar_acc_full + 8 * acc);
+                if (ok) tc::mma_commit_pair(bar_acc_full + 8 * acc);
             }
         }
     } else {
-        // ---------------- epilogue: warps 2..9, TMEM lane quadrant warp % 4;
-        // warpgroup eg = 0 takes the first half of the tile's 32-column
-        // chunks, eg = 1 the rest
+        // ---------------- epilogue (both CTAs): warps 2..9, TMEM lane
+        // quadrant warp % 4; warpgroup eg = 0 takes the first half of the
+        // tile's 32-column chunks, eg = 1 the rest
         const int quad = warp & 3;
         const int eg = (warp - 2) >> 2;
         constexpr int kChunks = BN / 32;
         const int c_begin = eg == 0 ? 0 : (kChunks + 1) / 2, c_end = eg == 0 ? (kChunks + 1) / 2 : kChunks;
-        const int r_in_tile = quad * 32 + lane;
+        const int r_in_tile = (int)rank * kBM + quad * 32 + lane;
         // bias and residual words of chunk c (8 bf16 per word), loaded one
         // chunk ahead of their use -- the first chunk's before the wait for
         // the accumulator -- so their latency hides behind the MMAs and the
@@ -230,9 +248,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         };
         int tcount = 0;
-        for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++tcount) {
+        for (int tile = pair; tile < n_tiles; tile += n_pairs, ++tcount) {
             const int acc = tcount & 1;
-            const int m0 = (tile / a.tiles_n) * kBM, n0 = (tile % a.tiles_n) * BN;
+            const int m0 = (tile / a.tiles_n) * (2 * kBM), n0 = (tile % a.tiles_n) * BN;
             const int row = m0 + r_in_tile;
             const bool row_ok = row < a.M;
             uint4 bw[4], rw[4];
@@ -279,19 +297,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                     rw[g] = nrw[g];
                 }
             }
-            // every TMEM read of this accumulator is done: hand it back
+            // every TMEM read of this accumulator is done: hand it back to
+            // the MMA thread (on rank 0)
             tc::fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar_acc_empty + 8 * acc);
+            if (lane == 0) tc::mbar_arrive_cluster(acc_empty0 + 8 * acc);
         }
     }
 
     __syncwarp();  // lanes 1..31 of the producer and MMA warps wait for their lane 0
+    if (*abort_flag && warp == 0 && lane == 0) {
+        // a wait expired: give the loads this CTA issued (whose completion is
+        // counted on rank 0's barriers) 100 us to land before its shared
+        // memory is given up
+        const unsigned long long t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < 100000ull) {
+        }
+    }
     tc::fence_before();
-    __syncthreads();
+    // both CTAs are done: rank 0's MMAs no longer read rank 1's shared memory,
+    // and no arrival on rank 0's barriers is still on its way
+    tc::cluster_sync();
     if (warp == 1) {
         tc::fence_after();
-        tc::tmem_dealloc(tmem, 512);
+        tc::tmem_dealloc_pair(tmem, 512);
     }
 }
 
@@ -316,7 +345,8 @@ cudaError_t launch_gemm_bn(const void *x, long long ldx, int M, int K, const voi
                            int act, const void *res, long long ldr, void *out, long long ldc, cudaStream_t stream) {
     using L = GemmLayout<BN>;
     CUtensorMap ta, tw;
-    if (!make_matrix_tmap(&ta, x, M, K, ldx, kBM) || !make_matrix_tmap(&tw, w, N, K, K, BN))
+    // each CTA of a pair loads 128 rows of A and BN / 2 rows of W
+    if (!make_matrix_tmap(&ta, x, M, K, ldx, kBM) || !make_matrix_tmap(&tw, w, N, K, K, BN / 2))
         return cudaErrorInvalidValue;
     GemmArgs a{};
     a.M = M, a.N = N, a.K = K;
@@ -324,7 +354,7 @@ cudaError_t launch_gemm_bn(const void *x, long long ldx, int M, int K, const voi
     a.res = static_cast<const uint16_t *>(res);
     a.out = static_cast<uint16_t *>(out);
     a.ldr = ldr, a.ldc = ldc, a.act = act;
-    a.tiles_m = (M + kBM - 1) / kBM;
+    a.tiles_m = (M + 2 * kBM - 1) / (2 * kBM);
     a.tiles_n = (N + BN - 1) / BN;
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -335,15 +365,32 @@ cudaError_t launch_gemm_bn(const void *x, long long ldx, int M, int K, const voi
     const long long tiles = (long long)a.tiles_m * a.tiles_n;
     if (tiles > 0x7fffffffLL) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)std::min<long long>(tiles, sms));
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = L::kSmem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 2;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
+    // Persistent: as many pairs as can be resident at once (an SM whose
+    // partner SM is disabled hosts no pair, so this is below sms / 2; more
+    // pairs than fit would run as a second wave), cached per device.
+    static int max_pairs[64] = {};
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (max_pairs[dev] == 0) {
+        int n = 0;
+        cfg.gridDim = dim3((unsigned)(2 * std::max(1, sms / 2)));
+        e = cudaOccupancyMaxActiveClusters(&n, gemm_bf16_kernel<BN>, &cfg);
+        if (e != cudaSuccess) return e;
+        max_pairs[dev] = std::max(1, n);
+    }
+    const long long pairs = std::min<long long>(tiles, max_pairs[dev]);
+    cfg.gridDim = dim3((unsigned)(2 * pairs));
     e = cudaLaunchKernelEx(&cfg, gemm_bf16_kernel<BN>, ta, tw, a);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();

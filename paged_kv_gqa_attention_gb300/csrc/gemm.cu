@@ -78,9 +78,17 @@ struct GemmLayout {
     static constexpr uint32_t kA = kBM * kBK * 2;        // 16 KiB
     static constexpr uint32_t kB = (BN / 2) * kBK * 2;   // this CTA's half of the W tile
     static constexpr uint32_t kStage = kA + kB;
-    static constexpr int kStages = (220 * 1024) / kStage < 8 ? (220 * 1024) / kStage : 8;
-    static constexpr uint32_t kBar = kStages * kStage;  // full[S], empty[S], acc_full[2], acc_empty[2]
-    static constexpr uint32_t kTmemSlot = kBar + (2 * kStages + 4) * 8;
+    // epilogue staging, per epilogue warp: two 32 x 32 output blocks and two
+    // 32 x 32 residual blocks of bf16 (2 KiB each, 64-byte swizzled)
+    static constexpr uint32_t kEpiWarpBytes = 4 * 2048;
+    static constexpr uint32_t kEpiBytes = kEpiWarps * kEpiWarpBytes;
+    static constexpr int kStages = (220 * 1024 - kEpiBytes) / kStage < 8 ? (220 * 1024 - kEpiBytes) / kStage : 8;
+    static constexpr uint32_t kEpi = kStages * kStage;
+    // full[S], empty[S], acc_full[2], acc_empty[2], then two residual
+    // barriers per epilogue warp
+    static constexpr uint32_t kBar = kEpi + kEpiBytes;
+    static constexpr uint32_t kResBar = kBar + (2 * kStages + 4) * 8;
+    static constexpr uint32_t kTmemSlot = kResBar + kEpiWarps * 2 * 8;
     static constexpr uint32_t kAbort = kTmemSlot + 8;  // set when a wait expired: every role stops
     static constexpr uint32_t kBytes = kTmemSlot + 16;
     static constexpr uint32_t kSmem = kBytes + 1024;  // slack for 1024-byte alignment
@@ -88,6 +96,7 @@ struct GemmLayout {
     static_assert(kA % 1024 == 0 && kB % 1024 == 0, "stages must keep 1024-byte swizzle alignment");
     static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "N tile: a multiple of 32, at most 256");
     static_assert(kStages >= 2, "at least two stages");
+    static_assert(kSmem <= 227 * 1024, "shared memory");
 };
 
 // gelu(u) = u / 2 (1 + erf(u / sqrt 2)), with erf from Abramowitz and Stegun,
@@ -125,6 +134,7 @@ __device__ __forceinline__ void unpack8(uint4 w, float *f) {
 template <int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_bf16_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_w,
+                     const __grid_constant__ CUtensorMap tm_out, const __grid_constant__ CUtensorMap tm_res,
                      const GemmArgs a) {
     using L = GemmLayout<BN>;
     extern __shared__ uint8_t smem_raw[];
@@ -154,9 +164,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar_acc_full + 8 * i, 1);
             mbar_init(bar_acc_empty + 8 * i, 2 * kEpiWarps);  // rank 0's: every epilogue warp of the pair
         }
+        for (int i = 0; i < 2 * kEpiWarps; ++i) mbar_init(sb + L::kResBar + 8 * i, 1);
         fence_mbar_init();
         tc::prefetch_tmap(&tm_a);
         tc::prefetch_tmap(&tm_w);
+        tc::prefetch_tmap(&tm_out);
+        if (a.res) tc::prefetch_tmap(&tm_res);
     }
     if (warp == 1) tc::tmem_alloc_pair(sb + L::kTmemSlot, 512);
     tc::fence_before();
@@ -225,77 +238,110 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // ---------------- epilogue (both CTAs): warps 2..9, TMEM lane
         // quadrant warp % 4; warpgroup eg = 0 takes the first half of the
-        // tile's 32-column chunks, eg = 1 the rest
+        // tile's 32-column chunks, eg = 1 the rest.  A warp's 32 rows of a
+        // chunk form one 32 x 32 block: the residual block comes in by TMA
+        // (one chunk ahead, the first before the wait for the accumulator)
+        // and the output block leaves by a TMA store from a staging block,
+        // so no thread waits on a global load or issues a scattered store.
+        // The blocks are 64-byte swizzled: 16-byte chunk k of row r sits at
+        // chunk position k ^ ((r / 2) % 4), which spreads a warp's row
+        // accesses over every bank.
         const int quad = warp & 3;
-        const int eg = (warp - 2) >> 2;
+        const int ew = warp - 2;
+        const int eg = ew >> 2;
         constexpr int kChunks = BN / 32;
         const int c_begin = eg == 0 ? 0 : (kChunks + 1) / 2, c_end = eg == 0 ? (kChunks + 1) / 2 : kChunks;
-        const int r_in_tile = (int)rank * kBM + quad * 32 + lane;
-        // bias and residual words of chunk c (8 bf16 per word), loaded one
-        // chunk ahead of their use -- the first chunk's before the wait for
-        // the accumulator -- so their latency hides behind the MMAs and the
-        // previous chunk's work instead of stalling every chunk
-        auto side_loads = [&](int n0, int row, int c, uint4 (&bw)[4], uint4 (&rw)[4]) {
+        const uint32_t ostage = sb + L::kEpi + (uint32_t)ew * L::kEpiWarpBytes;  // two output blocks
+        const uint32_t rstage = ostage + 2 * 2048;                               // two residual blocks
+        const uint32_t bar_res = sb + L::kResBar + (uint32_t)ew * 16;
+        const uint32_t sw = (uint32_t)((lane >> 1) & 3);
+        const uint32_t orow = (uint32_t)lane * 64u;
+        uint32_t res_phase = 0;  // bit b: parity of residual block b's next completion
+        int kc = 0;              // chunks this warp has handled (block index kc & 1)
+        // bias words of chunk c (8 bf16 per word), loaded one chunk ahead
+        auto bias_loads = [&](int n0, int c, uint4 (&bw)[4]) {
             const int col0 = n0 + c * 32;
             const int n_groups = max(0, min(4, (a.N - col0) / 8));  // 8-column groups inside N
 #pragma unroll
-            for (int g = 0; g < 4; ++g) {
+            for (int g = 0; g < 4; ++g)
                 bw[g] = (a.bias && g < n_groups) ? *reinterpret_cast<const uint4 *>(a.bias + col0 + 8 * g)
                                                  : make_uint4(0u, 0u, 0u, 0u);
-                rw[g] = (a.res && row < a.M && g < n_groups)
-                            ? *reinterpret_cast<const uint4 *>(a.res + (size_t)row * a.ldr + col0 + 8 * g)
-                            : make_uint4(0u, 0u, 0u, 0u);
+        };
+        auto res_load = [&](int n0, int row0, int c, int blk) {
+            if (a.res && lane == 0) {
+                mbar_arrive_expect_tx(bar_res + 8 * blk, 2048);
+                tc::tma_load_2d(rstage + (uint32_t)blk * 2048, &tm_res, n0 + 32 * c, row0, bar_res + 8 * blk);
             }
         };
         int tcount = 0;
         for (int tile = pair; tile < n_tiles; tile += n_pairs, ++tcount) {
             const int acc = tcount & 1;
             const int m0 = (tile / a.tiles_n) * (2 * kBM), n0 = (tile % a.tiles_n) * BN;
-            const int row = m0 + r_in_tile;
-            const bool row_ok = row < a.M;
-            uint4 bw[4], rw[4];
-            side_loads(n0, row, c_begin, bw, rw);
+            const int row0 = m0 + (int)rank * kBM + quad * 32;  // the warp's first row
+            uint4 bw[4];
+            bias_loads(n0, c_begin, bw);
+            res_load(n0, row0, c_begin, kc & 1);
             // warp-uniform: every lane waits on the same phase
             const bool ok = wait(bar_acc_full + 8 * acc, (tcount >> 1) & 1);
             if (!__all_sync(0xffffffffu, ok)) break;
             tc::fence_after();
             const uint32_t t_base = tmem + acc * L::kAccCols + ((uint32_t)(quad * 32) << 16);
 #pragma unroll 1
-            for (int c = c_begin; c < c_end; ++c) {
-                uint4 nbw[4] = {}, nrw[4] = {};
-                if (c + 1 < c_end) side_loads(n0, row, c + 1, nbw, nrw);
+            for (int c = c_begin; c < c_end; ++c, ++kc) {
+                const int blk = kc & 1;
+                uint4 nbw[4] = {};
+                if (c + 1 < c_end) {
+                    bias_loads(n0, c + 1, nbw);
+                    res_load(n0, row0, c + 1, blk ^ 1);  // that block was read in the previous chunk
+                }
                 float v[32];
                 tc::tmem_ld32(t_base + c * 32, v);  // warp-collective: every lane, every chunk
-                const int col0 = n0 + c * 32;
-                const int n_groups = max(0, min(4, (a.N - col0) / 8));
+                float rf[32];
+                if (a.res) {
+                    wait(bar_res + 8 * blk, (res_phase >> blk) & 1);
+                    res_phase ^= 1u << blk;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        uint32_t x0, x1, x2, x3;
+                        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                                     : "=r"(x0), "=r"(x1), "=r"(x2), "=r"(x3)
+                                     : "r"(rstage + (uint32_t)blk * 2048 + orow + (((uint32_t)k ^ sw) << 4)));
+                        unpack8(make_uint4(x0, x1, x2, x3), rf + 8 * k);
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) rf[j] = 0.f;
+                }
 #pragma unroll
                 for (int g = 0; g < 4; ++g) {
-                    float bf[8], rf[8];
+                    float bf[8];
                     unpack8(bw[g], bf);
-                    unpack8(rw[g], rf);
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
                         float u = v[8 * g + j] + bf[j];
                         if (a.act == 1) u = gelu_erf(u);
-                        v[8 * g + j] = u + rf[j];
+                        v[8 * g + j] = u + rf[8 * g + j];
                     }
                 }
-                if (row_ok) {
-                    uint16_t *orow = a.out + (size_t)row * a.ldc + col0;
-#pragma unroll
-                    for (int g = 0; g < 4; ++g) {
-                        if (g < n_groups)
-                            *reinterpret_cast<uint4 *>(orow + 8 * g) = make_uint4(
-                                pack_bf16x2(v[8 * g + 0], v[8 * g + 1]), pack_bf16x2(v[8 * g + 2], v[8 * g + 3]),
-                                pack_bf16x2(v[8 * g + 4], v[8 * g + 5]), pack_bf16x2(v[8 * g + 6], v[8 * g + 7]));
-                    }
-                }
+                // the output block written two chunks ago has been read by
+                // its TMA store before this one overwrites it
+                if (lane == 0) tc::bulk_wait_group_read_1();
                 __syncwarp();
+                const uint32_t ob = ostage + (uint32_t)blk * 2048 + orow;
 #pragma unroll
-                for (int g = 0; g < 4; ++g) {
-                    bw[g] = nbw[g];
-                    rw[g] = nrw[g];
+                for (int g = 0; g < 4; ++g)
+                    tc::st_shared_v4(ob + (((uint32_t)g ^ sw) << 4), pack_bf16x2(v[8 * g + 0], v[8 * g + 1]),
+                                     pack_bf16x2(v[8 * g + 2], v[8 * g + 3]), pack_bf16x2(v[8 * g + 4], v[8 * g + 5]),
+                                     pack_bf16x2(v[8 * g + 6], v[8 * g + 7]));
+                tc::fence_proxy_async_smem();  // the block is read by the TMA unit
+                __syncwarp();
+                // rows past M and columns past N are clipped by the store
+                if (lane == 0) {
+                    tc::tma_store_2d(&tm_out, ostage + (uint32_t)blk * 2048, n0 + 32 * c, row0);
+                    tc::bulk_commit_group();
                 }
+#pragma unroll
+                for (int g = 0; g < 4; ++g) bw[g] = nbw[g];
             }
             // every TMEM read of this accumulator is done: hand it back to
             // the MMA thread (on rank 0)
@@ -303,6 +349,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) tc::mbar_arrive_cluster(acc_empty0 + 8 * acc);
         }
+        if (lane == 0) tc::bulk_wait_group_read_all();  // the stores have read their blocks
     }
 
     __syncwarp();  // lanes 1..31 of the producer and MMA warps wait for their lane 0
@@ -340,14 +387,33 @@ bool make_matrix_tmap(CUtensorMap *map, const void *base, long long rows, long l
     return r == CUDA_SUCCESS;
 }
 
+// 2-D tensor map of a row-major bf16 matrix [rows][cols] with row stride ld
+// (elements, a multiple of 8): box {32 cols, 32 rows}, 64-byte swizzle (the
+// epilogue's blocks).
+bool make_block_tmap(CUtensorMap *map, const void *base, long long rows, long long cols, long long ld) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc || rows < 1 || cols < 1 || rows > 0x7fffffffLL || cols > 0x7fffffffLL) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+    cuuint32_t box[2] = {32, 32};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 template <int BN>
 cudaError_t launch_gemm_bn(const void *x, long long ldx, int M, int K, const void *w, int N, const void *bias,
                            int act, const void *res, long long ldr, void *out, long long ldc, cudaStream_t stream) {
     using L = GemmLayout<BN>;
-    CUtensorMap ta, tw;
-    // each CTA of a pair loads 128 rows of A and BN / 2 rows of W
-    if (!make_matrix_tmap(&ta, x, M, K, ldx, kBM) || !make_matrix_tmap(&tw, w, N, K, K, BN / 2))
+    CUtensorMap ta, tw, tout, tres;
+    // each CTA of a pair loads 128 rows of A and BN / 2 rows of W; the
+    // epilogue moves 32 x 32 blocks of the output and the residual
+    if (!make_matrix_tmap(&ta, x, M, K, ldx, kBM) || !make_matrix_tmap(&tw, w, N, K, K, BN / 2) ||
+        !make_block_tmap(&tout, out, M, N, ldc) || (res && !make_block_tmap(&tres, res, M, N, ldr)))
         return cudaErrorInvalidValue;
+    if (!res) tres = tout;  // not read
     GemmArgs a{};
     a.M = M, a.N = N, a.K = K;
     a.bias = static_cast<const uint16_t *>(bias);
@@ -391,7 +457,7 @@ cudaError_t launch_gemm_bn(const void *x, long long ldx, int M, int K, const voi
     }
     const long long pairs = std::min<long long>(tiles, max_pairs[dev]);
     cfg.gridDim = dim3((unsigned)(2 * pairs));
-    e = cudaLaunchKernelEx(&cfg, gemm_bf16_kernel<BN>, ta, tw, a);
+    e = cudaLaunchKernelEx(&cfg, gemm_bf16_kernel<BN>, ta, tw, tout, tres, a);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }

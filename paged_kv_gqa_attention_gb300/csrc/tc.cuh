@@ -279,11 +279,6 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank) {
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
 }
-__device__ __forceinline__ void mbar_arrive_expect_tx_cluster(uint32_t cluster_bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.release.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(cluster_bar),
-                 "r"(bytes)
-                 : "memory");
-}
 
 // Whole-warp TMEM allocation for a CTA pair: one warp of each CTA executes
 // it; both CTAs get the same columns, the base written to smem[dst] of each.
@@ -341,12 +336,27 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, uint32_t sr
                  : "memory");
 }
 
+// Tiled 2-D TMA store shared -> global of one box (same rules as
+// tma_store_3d).
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, uint32_t src, int c0, int c1) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c0), "r"(c1), "r"(src)
+                 : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 
 // Waits until every bulk group this thread committed has finished reading
 // shared memory.
 __device__ __forceinline__ void bulk_wait_group_read_all() {
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// Waits until at most the most recent bulk group this thread committed is
+// still reading shared memory.
+__device__ __forceinline__ void bulk_wait_group_read_1() {
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
 }
 
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map) {

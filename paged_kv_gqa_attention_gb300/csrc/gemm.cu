@@ -73,14 +73,15 @@ struct GemmArgs {
     int tiles_m, tiles_n;
 };
 
-template <int BN>
+template <int BN, bool RES>
 struct GemmLayout {
     static constexpr uint32_t kA = kBM * kBK * 2;        // 16 KiB
     static constexpr uint32_t kB = (BN / 2) * kBK * 2;   // this CTA's half of the W tile
     static constexpr uint32_t kStage = kA + kB;
-    // epilogue staging, per epilogue warp: two 32 x 32 output blocks and two
-    // 32 x 32 residual blocks of bf16 (2 KiB each, 64-byte swizzled)
-    static constexpr uint32_t kEpiWarpBytes = 4 * 2048;
+    // epilogue staging, per epilogue warp: two 32 x 32 output blocks and, with
+    // a residual, two 32 x 32 residual blocks of bf16 (2 KiB each, 64-byte
+    // swizzled)
+    static constexpr uint32_t kEpiWarpBytes = (RES ? 4 : 2) * 2048;
     static constexpr uint32_t kEpiBytes = kEpiWarps * kEpiWarpBytes;
     static constexpr int kStages = (220 * 1024 - kEpiBytes) / kStage < 8 ? (220 * 1024 - kEpiBytes) / kStage : 8;
     static constexpr uint32_t kEpi = kStages * kStage;
@@ -131,12 +132,12 @@ __device__ __forceinline__ void unpack8(uint4 w, float *f) {
     f[4] = bf16lo(w.z), f[5] = bf16hi(w.z), f[6] = bf16lo(w.w), f[7] = bf16hi(w.w);
 }
 
-template <int BN>
+template <int BN, bool RES>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_bf16_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_w,
                      const __grid_constant__ CUtensorMap tm_out, const __grid_constant__ CUtensorMap tm_res,
                      const GemmArgs a) {
-    using L = GemmLayout<BN>;
+    using L = GemmLayout<BN, RES>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t sb = (raw + 1023u) & ~1023u;
@@ -169,7 +170,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::prefetch_tmap(&tm_a);
         tc::prefetch_tmap(&tm_w);
         tc::prefetch_tmap(&tm_out);
-        if (a.res) tc::prefetch_tmap(&tm_res);
+        if (RES) tc::prefetch_tmap(&tm_res);
     }
     if (warp == 1) tc::tmem_alloc_pair(sb + L::kTmemSlot, 512);
     tc::fence_before();
@@ -268,7 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                  : make_uint4(0u, 0u, 0u, 0u);
         };
         auto res_load = [&](int n0, int row0, int c, int blk) {
-            if (a.res && lane == 0) {
+            if (RES && lane == 0) {
                 mbar_arrive_expect_tx(bar_res + 8 * blk, 2048);
                 tc::tma_load_2d(rstage + (uint32_t)blk * 2048, &tm_res, n0 + 32 * c, row0, bar_res + 8 * blk);
             }
@@ -297,7 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float v[32];
                 tc::tmem_ld32(t_base + c * 32, v);  // warp-collective: every lane, every chunk
                 float rf[32];
-                if (a.res) {
+                if (RES) {
                     wait(bar_res + 8 * blk, (res_phase >> blk) & 1);
                     res_phase ^= 1u << blk;
 #pragma unroll
@@ -403,10 +404,10 @@ bool make_block_tmap(CUtensorMap *map, const void *base, long long rows, long lo
     return r == CUDA_SUCCESS;
 }
 
-template <int BN>
+template <int BN, bool RES>
 cudaError_t launch_gemm_bn(const void *x, long long ldx, int M, int K, const void *w, int N, const void *bias,
                            int act, const void *res, long long ldr, void *out, long long ldc, cudaStream_t stream) {
-    using L = GemmLayout<BN>;
+    using L = GemmLayout<BN, RES>;
     CUtensorMap ta, tw, tout, tres;
     // each CTA of a pair loads 128 rows of A and BN / 2 rows of W; the
     // epilogue moves 32 x 32 blocks of the output and the residual
@@ -426,7 +427,7 @@ cudaError_t launch_gemm_bn(const void *x, long long ldx, int M, int K, const voi
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(gemm_bf16_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
+    e = cudaFuncSetAttribute(gemm_bf16_kernel<BN, RES>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
     if (e != cudaSuccess) return e;
     const long long tiles = (long long)a.tiles_m * a.tiles_n;
     if (tiles > 0x7fffffffLL) return cudaErrorInvalidValue;
@@ -451,13 +452,13 @@ cudaError_t launch_gemm_bn(const void *x, long long ldx, int M, int K, const voi
     if (max_pairs[dev] == 0) {
         int n = 0;
         cfg.gridDim = dim3((unsigned)(2 * std::max(1, sms / 2)));
-        e = cudaOccupancyMaxActiveClusters(&n, gemm_bf16_kernel<BN>, &cfg);
+        e = cudaOccupancyMaxActiveClusters(&n, gemm_bf16_kernel<BN, RES>, &cfg);
         if (e != cudaSuccess) return e;
         max_pairs[dev] = std::max(1, n);
     }
     const long long pairs = std::min<long long>(tiles, max_pairs[dev]);
     cfg.gridDim = dim3((unsigned)(2 * pairs));
-    e = cudaLaunchKernelEx(&cfg, gemm_bf16_kernel<BN>, ta, tw, tout, tres, a);
+    e = cudaLaunchKernelEx(&cfg, gemm_bf16_kernel<BN, RES>, ta, tw, tout, tres, a);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
@@ -469,8 +470,11 @@ cudaError_t launch_gemm_bn(const void *x, long long ldx, int M, int K, const voi
 cudaError_t launch_gemm(const void *x, long long ldx, int M, int K, const void *w, int N, const void *bias, int act,
                         const void *res, long long ldr, void *out, long long ldc, cudaStream_t stream) {
     if (M == 0) return cudaSuccess;
-    if (N % 224 == 0) return launch_gemm_bn<224>(x, ldx, M, K, w, N, bias, act, res, ldr, out, ldc, stream);
-    return launch_gemm_bn<256>(x, ldx, M, K, w, N, bias, act, res, ldr, out, ldc, stream);
+    if (N % 224 == 0)
+        return res ? launch_gemm_bn<224, true>(x, ldx, M, K, w, N, bias, act, res, ldr, out, ldc, stream)
+                   : launch_gemm_bn<224, false>(x, ldx, M, K, w, N, bias, act, res, ldr, out, ldc, stream);
+    return res ? launch_gemm_bn<256, true>(x, ldx, M, K, w, N, bias, act, res, ldr, out, ldc, stream)
+               : launch_gemm_bn<256, false>(x, ldx, M, K, w, N, bias, act, res, ldr, out, ldc, stream);
 }
 
 unsigned int status_read_clear_gemm(cudaStream_t stream, cudaError_t *err) {

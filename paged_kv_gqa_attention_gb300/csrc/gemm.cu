@@ -111,19 +111,23 @@ __device__ __forceinline__ float rcp_approx(float x) {
     asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
-__device__ __forceinline__ float gelu_erf(float u) {
-    const float z = fabsf(u) * 0.70710678118654752f;
-    const float t = rcp_approx(fmaf(0.3275911f, z, 1.0f));  // 1 + p z >= 1
-    float poly = fmaf(1.061405429f, t, -1.453152027f);
-    poly = fmaf(poly, t, 1.421413741f);
-    poly = fmaf(poly, t, -0.284496736f);
-    poly = fmaf(poly, t, 0.254829592f);
-    poly *= t;
-    const float e = exp2_approx(-z * z * kLog2e);  // exp(-z^2)
-    const float erf_abs = fmaf(-poly, e, 1.0f);
-    const float erf_z = copysignf(erf_abs, u);
-    const float h = 0.5f * u;
-    return fmaf(h, erf_z, h);
+// Two elements at once on packed fp32 pairs, written as
+// gelu(u) = max(u, 0) - |u| / 2 * Q(|u| / sqrt 2), Q(z) = 1 - erf(z) =
+// (a1 t + ... + a5 t^5) exp(-z^2) from the same formula (no cancellation in
+// 1 - Q for negative u).
+__device__ __forceinline__ float2 gelu_erf2(float2 u) {
+    const float2 a = make_float2(fabsf(u.x), fabsf(u.y));
+    const float2 z = fmul2(a, make_float2(0.70710678118654752f, 0.70710678118654752f));
+    const float2 d = ffma2(z, make_float2(0.3275911f, 0.3275911f), make_float2(1.0f, 1.0f));  // 1 + p z >= 1
+    const float2 t = make_float2(rcp_approx(d.x), rcp_approx(d.y));
+    float2 poly = ffma2(make_float2(1.061405429f, 1.061405429f), t, make_float2(-1.453152027f, -1.453152027f));
+    poly = ffma2(poly, t, make_float2(1.421413741f, 1.421413741f));
+    poly = ffma2(poly, t, make_float2(-0.284496736f, -0.284496736f));
+    poly = ffma2(poly, t, make_float2(0.254829592f, 0.254829592f));
+    poly = fmul2(poly, t);
+    const float2 x = fmul2(z, fmul2(z, make_float2(-kLog2e, -kLog2e)));  // -z^2 log2(e)
+    const float2 q = fmul2(poly, make_float2(exp2_approx(x.x), exp2_approx(x.y)));
+    return ffma2(fmul2(a, make_float2(-0.5f, -0.5f)), q, make_float2(fmaxf(u.x, 0.f), fmaxf(u.y, 0.f)));
 }
 
 // bf16x8 (one 16-byte word) -> 8 floats
@@ -297,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 float v[32];
                 tc::tmem_ld32(t_base + c * 32, v);  // warp-collective: every lane, every chunk
-                float rf[32];
+                float rf[32] = {};
                 if (RES) {
                     wait(bar_res + 8 * blk, (res_phase >> blk) & 1);
                     res_phase ^= 1u << blk;
@@ -309,19 +313,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                                      : "r"(rstage + (uint32_t)blk * 2048 + orow + (((uint32_t)k ^ sw) << 4)));
                         unpack8(make_uint4(x0, x1, x2, x3), rf + 8 * k);
                     }
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) rf[j] = 0.f;
                 }
 #pragma unroll
                 for (int g = 0; g < 4; ++g) {
                     float bf[8];
                     unpack8(bw[g], bf);
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        float u = v[8 * g + j] + bf[j];
-                        if (a.act == 1) u = gelu_erf(u);
-                        v[8 * g + j] = u + rf[8 * g + j];
+                    for (int j = 0; j < 8; j += 2) {
+                        float2 u = fadd2(make_float2(v[8 * g + j], v[8 * g + j + 1]), make_float2(bf[j], bf[j + 1]));
+                        if (a.act == 1) u = gelu_erf2(u);
+                        if (RES) u = fadd2(u, make_float2(rf[8 * g + j], rf[8 * g + j + 1]));
+                        v[8 * g + j] = u.x;
+                        v[8 * g + j + 1] = u.y;
                     }
                 }
                 // the output block written two chunks ago has been read by

@@ -36,6 +36,8 @@ def test_layer_norm_matches_oracle(T, d):
     (128, 896, 896, False, False, False),   # one exact M tile, no epilogue extras
     (1, 136, 200, True, True, True),        # a single row, K not a multiple of 64, N not of 224
     (700, 64, 520, True, False, True),      # several M tiles, a ragged N tile, one K block
+    (4096, 896, 2688, True, False, True),   # 192 tiles: several per pair of SMs (both accumulators reused)
+    (5000, 512, 1040, True, True, False),   # 100 tiles of the 256-wide N tile, the last one ragged
 ])
 def test_linear_matches_oracle(M, K, N, bias, gelu, res):
     rng = np.random.default_rng(M * 7 + K + N)

@@ -31,16 +31,18 @@
 //   warps 2-9  epilogue (both CTAs), two warpgroups splitting the tile's
 //              columns: each thread owns one row of its CTA's 128 rows (the
 //              TMEM lane quadrant of its warp), reads the accumulator 32
-//              columns at a time, adds bias, applies gelu, adds the residual,
-//              rounds to bf16 and stores; then releases the accumulator on
-//              rank 0's "acc_empty" barrier so the next-but-one tile can use it.
+//              columns at a time, adds bias, applies gelu, adds the residual
+//              (its 32 x 32 block brought in by TMA one chunk ahead), rounds
+//              to bf16 into a staging block that one lane writes out with a
+//              TMA store; then releases the accumulator on rank 0's
+//              "acc_empty" barrier so the next-but-one tile can use it.
 // With two accumulators the epilogue of tile i overlaps the MMAs of tile
 // i + 1.  Tiles are walked m-block-major (tile = m_blk * tiles_n + n_blk), so
 // the pairs running at any moment share a few m-blocks of A and every W tile:
 // A is fetched from HBM about once, W stays in L2.
 //
-// Rows past M and columns past N (ragged last tiles) are zero-filled by TMA
-// and never stored; K need not be a multiple of 64 (the zero fill makes the
+// Rows past M and columns past N (ragged last tiles) are zero-filled by the
+// TMA loads and clipped by the TMA stores; K need not be a multiple of 64 (the zero fill makes the
 // tail products 0).  Every wait is bounded (common.cuh): one that expires
 // sets QA_DEVICE_TIMEOUT and the kernel runs to its end.
 #include <cuda.h>

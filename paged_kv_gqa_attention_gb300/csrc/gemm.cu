@@ -470,12 +470,14 @@ cudaError_t launch_gemm_bn(const void *x, long long ldx, int M, int K, const voi
 
 }  // namespace
 
-// N tile: 224 divides the encoder's widths (896, 3 x 896, 3584) exactly;
-// other widths take 256 with a ragged last tile.
+// N tile: 256 where it divides N (per flop, fewer A bytes through L2 than
+// 224, and both epilogue warpgroups take four 32-column chunks of a tile;
+// fc1's 3584: 305 us instead of 324); else 224 where that divides N exactly
+// (the encoder's 896 and 3 x 896); else 256 with a ragged last tile.
 cudaError_t launch_gemm(const void *x, long long ldx, int M, int K, const void *w, int N, const void *bias, int act,
                         const void *res, long long ldr, void *out, long long ldc, cudaStream_t stream) {
     if (M == 0) return cudaSuccess;
-    if (N % 224 == 0)
+    if (N % 256 != 0 && N % 224 == 0)
         return res ? launch_gemm_bn<224, true>(x, ldx, M, K, w, N, bias, act, res, ldr, out, ldc, stream)
                    : launch_gemm_bn<224, false>(x, ldx, M, K, w, N, bias, act, res, ldr, out, ldc, stream);
     return res ? launch_gemm_bn<256, true>(x, ldx, M, K, w, N, bias, act, res, ldr, out, ldc, stream)

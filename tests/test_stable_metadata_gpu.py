@@ -174,6 +174,47 @@ def test_chunked_prefill_twice_at_level_1():
     assert qa.qa_device_status() == 0
 
 
+@pytest.mark.parametrize("level", [1, 2])
+def test_chunked_prefill_layers_chained_through_q(level):
+    # three layers of the re-prefill bucket queued on one stream, each with
+    # its own k, v and pool buffers (one cu_seqlens, n_past and page table); layer
+    # i's q is layer i - 1's output, written by the kernel right before it,
+    # so q must be read only after the wait even where (level 2) the first
+    # cached tile's K and V rows are requested before it
+    base = wl.chunk_reprefill()
+    layers = []
+    for i in range(3):
+        c = dict(base)
+        rng = wl.rng_for(900 + i)
+        for key in ("k", "v"):
+            c[key] = wl.normal_bf16(rng, base[key].shape)
+        layers.append(c)  # its pools: a device copy of its own (same cached rows)
+    cu, npast, pt = to_dev(base["cu_seqlens"]), to_dev(base["n_past"]), to_dev(base["page_table"])
+    dev = [{key: to_dev(c[key]) for key in ("k", "v", "k_pages", "v_pages")} for c in layers]
+    q0 = to_dev(base["q"])
+    s = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    outs = []
+    with torch.cuda.stream(s):
+        q = q0
+        for d in dev:
+            q = qa.qa_prefill_chunk_attn(q, d["k"], d["v"], cu, npast, pt, d["k_pages"], d["v_pages"], stream=s,
+                                         stable_metadata=level)
+            outs.append(q)
+    torch.cuda.synchronize()
+    q_in = base["q"]
+    for i, (c, d, o) in enumerate(zip(layers, dev, outs)):
+        ref = oracle.prefill_chunk(q_in, c["k"], c["v"], c["cu_seqlens"], c["n_past"], c["page_table"],
+                                   c["k_pages"], c["v_pages"])
+        assert_close(f64(o), ref, f"chunked prefill layer {i}, level {level}")
+        ekp, evp = oracle.page_write_at(c["k"], c["v"], c["cu_seqlens"], c["n_past"], c["page_table"],
+                                        c["k_pages"], c["v_pages"])
+        np.testing.assert_array_equal(bits(d["k_pages"]), ekp)
+        np.testing.assert_array_equal(bits(d["v_pages"]), evp)
+        q_in = bits(o)
+    assert qa.qa_device_status() == 0
+
+
 def test_graph_of_layers_follows_refills():
     base = wl.decode_0p6b()
     layers = [_layer(base, i) for i in range(3)]

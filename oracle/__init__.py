@@ -1,7 +1,7 @@
 """Reference oracle for paged GQA attention -- TEST INFRASTRUCTURE ONLY.
 
 Plain fp64 CPU statement of what the attention hot path computes, used to
-judge the CUDA library.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+check the CUDA library.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
 ``cpu_baseline`` leg of ``bench.py`` may import it; the library itself never
 does, and shares no code with it.
 

@@ -20,9 +20,13 @@
 // of (request, KV head); the warp that arrives last merges every partial of
 // its two query heads, writes the output and resets the counter to zero, so
 // nothing ever waits on another CTA and the workspace is left as it was
-// found.  A CTA takes its last segment first and its first segment second:
-// those are the only ones it can share with a neighbour, so partial results
-// (and the merges) happen early, not at the end of the run.
+// found.  Only a CTA's first and last segment can be shared with a
+// neighbour; their partials stay in registers until the CTA's last page and
+// are written, counted in and merged then: a release and an atomic in the
+// middle of the stream had stalled the consumer warps while the memory
+// system was saturated (the ring filled and the producer stopped), and
+// CTAs with two segments ended ~3 us after the others.  The q rows of the
+// next segment are loaded one segment ahead for the same reason.
 //
 // Inside a CTA.  One producer warp streams whole pages (K page and V page,
 // 16 tokens x Hkv heads x 128 dims of bf16 each, contiguous in the pool) into
@@ -177,11 +181,13 @@ __device__ __forceinline__ int first_request_past(const int *prefix, int batch, 
     return l;
 }
 
-__device__ __forceinline__ int atom_add_acq_rel_gpu(int *p, int v) {
+__device__ __forceinline__ int atom_add_relaxed_gpu(int *p, int v) {
     int old;
-    asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    asm volatile("atom.add.relaxed.gpu.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
     return old;
 }
+
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 
 __device__ __forceinline__ void bf16x4(uint2 w, float2 &lo, float2 &hi) {
     lo = make_float2(bf16lo(w.x), bf16hi(w.x));
@@ -371,8 +377,27 @@ __global__ void __launch_bounds__((kMaxHkv + 1) * 32, 1) decode_splitk_kernel(co
     const int my_h = GROUP == 2 ? lane & 1 : 0;
     const bool p_writer = GROUP == 2 ? true : (lane & 1) == 0;
     int it = 0;
+    // The q rows of the next segment are loaded one segment ahead, so a
+    // segment does not start with a round trip to memory.
+    auto load_q = [&](int b, uint2 (&w)[GROUP]) {
+#pragma unroll
+        for (int i = 0; i < GROUP; ++i)
+            w[i] = *reinterpret_cast<const uint2 *>(a.q + ((size_t)b * hq + g * GROUP + i) * kD + 4 * lane);
+    };
+    uint2 q_next[GROUP];
+    load_q(b_last, q_next);
+    // Partials of split segments (at most two per CTA: the first and the
+    // last request of its range; the ones between are whole) are kept in
+    // registers and written, counted in and merged after the last page, so
+    // no segment switch waits on a release or an atomic while pages stream.
+    int n_def = 0, def_b[2] = {0, 0};
+    float def_acc[2][GROUP][4], def_m[2][GROUP], def_l[2][GROUP];
     for (int k = 0; k < n_visit; ++k) {
         const int b = k == 0 ? b_last : b0 + k - 1;
+        uint2 qw[GROUP];
+#pragma unroll
+        for (int i = 0; i < GROUP; ++i) qw[i] = q_next[i];
+        if (k + 1 < n_visit) load_q(b0 + k, q_next);  // segment k + 1 is request b0 + k
         const int p0 = prefix[b], p1 = prefix[b + 1];
         if (p1 == p0) continue;
         const int j0 = max(lo, p0) - p0, j1 = min(hi, p1) - p0;
@@ -382,11 +407,6 @@ __global__ void __launch_bounds__((kMaxHkv + 1) * 32, 1) decode_splitk_kernel(co
         // fused step: the new token's K/V rows for KV head g (rotated k,
         // bf16) when this segment holds the request's last page
         const bool has_new = APPEND && j1 == p1 - p0;
-        // every load of the segment's prologue is issued before any is used
-        uint2 qw[GROUP];
-#pragma unroll
-        for (int i = 0; i < GROUP; ++i)
-            qw[i] = *reinterpret_cast<const uint2 *>(a.q + ((size_t)b * hq + g * GROUP + i) * kD + 4 * lane);
         uint2 k_new_w = make_uint2(0u, 0u), v_new_w = make_uint2(0u, 0u);
         float4 gain_q = make_float4(0.f, 0.f, 0.f, 0.f), gain_k = gain_q;
         if (APPEND) {
@@ -571,102 +591,134 @@ __global__ void __launch_bounds__((kMaxHkv + 1) * 32, 1) decode_splitk_kernel(co
         }
 
         const bool whole = (j0 == 0 && j1 == p1 - p0);
-        const int slot = blockIdx.x + b;
+        if (whole) {
 #pragma unroll
-        for (int i = 0; i < GROUP; ++i) {
-            const int h = g * GROUP + i;
-            if (whole) {
+            for (int i = 0; i < GROUP; ++i) {
+                const int h = g * GROUP + i;
                 const float inv = l[i] > 0.f ? 1.f / l[i] : 0.f;
                 uint2 w;
                 w.x = pack_bf16x2(acc[i][0] * inv, acc[i][1] * inv);
                 w.y = pack_bf16x2(acc[i][2] * inv, acc[i][3] * inv);
                 *reinterpret_cast<uint2 *>(a.out + ((size_t)b * hq + h) * kD + 4 * lane) = w;
-            } else {
-                *reinterpret_cast<float4 *>(a.part_acc + ((size_t)slot * hq + h) * kD + 4 * lane) =
-                    make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
-                if (lane == 0) {
-                    a.part_ml[((size_t)slot * hq + h) * 2 + 0] = m[i];
-                    a.part_ml[((size_t)slot * hq + h) * 2 + 1] = l[i];
-                }
             }
-        }
-        if (!whole) {
-            // Count this partial in; the last arriving warp of (b, g) merges.
-            const int c_lo = p0 / per, c_hi = (p1 - 1) / per;
-            // the warp barrier orders every lane's partial before lane 0's
-            // release; lane 0's acquire orders the reads below after it
-            __syncwarp();
-            int prev = 0;
-            if (lane == 0) prev = atom_add_acq_rel_gpu(a.arrivals + (size_t)b * kMaxHkv + g, 1);
-            prev = __shfl_sync(0xffffffffu, prev, 0);
-            if (prev == c_hi - c_lo) {
-                // online merge over batches of up to 8 partials per query
-                // head, the loads of both heads of the group all in flight
-                // together (one L2 round trip per batch; requests of this
-                // workload span a few CTAs)
-                constexpr int kBatch = 8;
-                float mm[GROUP], ls[GROUP], o[GROUP][4];
+        } else {
+            // warp-uniform; a third split segment cannot occur (see above)
+#pragma unroll
+            for (int d = 0; d < 2; ++d) {
+                if (d != n_def) continue;
+                def_b[d] = b;
 #pragma unroll
                 for (int i = 0; i < GROUP; ++i) {
-                    mm[i] = -INFINITY;
-                    ls[i] = 0.f;
-                    o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+                    def_m[d][i] = m[i];
+                    def_l[d][i] = l[i];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) def_acc[d][i][e] = acc[i][e];
                 }
-                for (int c0 = c_lo; c0 <= c_hi; c0 += kBatch) {
-                    float mc[GROUP][kBatch], lc[GROUP][kBatch];
-                    float4 pv[GROUP][kBatch];
+            }
+            n_def = min(n_def + 1, 2);
+        }
+    }
+
+    // The split segments' partials: written to slot c + b, counted in the
+    // arrival counter of (request, KV head); the last arriving warp merges.
 #pragma unroll
-                    for (int i = 0; i < GROUP; ++i) {
+    for (int d = 0; d < 2; ++d) {
+        if (d >= n_def) continue;
+        const int slot = blockIdx.x + def_b[d];
 #pragma unroll
-                        for (int u = 0; u < kBatch; ++u) {
-                            if (c0 + u <= c_hi) {
-                                const size_t r = (size_t)(c0 + u + b) * hq + g * GROUP + i;
-                                mc[i][u] = __ldcg(a.part_ml + r * 2);
-                                lc[i][u] = __ldcg(a.part_ml + r * 2 + 1);
-                                pv[i][u] = __ldcg(reinterpret_cast<const float4 *>(a.part_acc + r * kD + 4 * lane));
-                            } else {
-                                mc[i][u] = -INFINITY;
-                                lc[i][u] = 0.f;
-                                pv[i][u] = make_float4(0.f, 0.f, 0.f, 0.f);
-                            }
-                        }
-                    }
-#pragma unroll
-                    for (int i = 0; i < GROUP; ++i) {
-                        float mb = mm[i];
-#pragma unroll
-                        for (int u = 0; u < kBatch; ++u) mb = fmaxf(mb, mc[i][u]);
-                        if (mb == -INFINITY) continue;  // nothing attended so far
-                        const float alpha = exp2_approx(mm[i] - mb);  // 0 while mm = -inf
-                        ls[i] *= alpha;
-                        o[i][0] *= alpha;
-                        o[i][1] *= alpha;
-                        o[i][2] *= alpha;
-                        o[i][3] *= alpha;
-#pragma unroll
-                        for (int u = 0; u < kBatch; ++u) {
-                            const float w = exp2_approx(mc[i][u] - mb);  // 0 for an empty partial (mc = -inf)
-                            ls[i] += w * lc[i][u];
-                            o[i][0] += w * pv[i][u].x;
-                            o[i][1] += w * pv[i][u].y;
-                            o[i][2] += w * pv[i][u].z;
-                            o[i][3] += w * pv[i][u].w;
-                        }
-                        mm[i] = mb;
-                    }
-                }
-#pragma unroll
-                for (int i = 0; i < GROUP; ++i) {
-                    const int h = g * GROUP + i;
-                    const float inv = ls[i] > 0.f ? 1.f / ls[i] : 0.f;
-                    uint2 w;
-                    w.x = pack_bf16x2(o[i][0] * inv, o[i][1] * inv);
-                    w.y = pack_bf16x2(o[i][2] * inv, o[i][3] * inv);
-                    *reinterpret_cast<uint2 *>(a.out + ((size_t)b * hq + h) * kD + 4 * lane) = w;
-                }
-                if (lane == 0) a.arrivals[(size_t)b * kMaxHkv + g] = 0;  // ready for the next call
+        for (int i = 0; i < GROUP; ++i) {
+            const int h = g * GROUP + i;
+            *reinterpret_cast<float4 *>(a.part_acc + ((size_t)slot * hq + h) * kD + 4 * lane) =
+                make_float4(def_acc[d][i][0], def_acc[d][i][1], def_acc[d][i][2], def_acc[d][i][3]);
+            if (lane == 0) {
+                a.part_ml[((size_t)slot * hq + h) * 2 + 0] = def_m[d][i];
+                a.part_ml[((size_t)slot * hq + h) * 2 + 1] = def_l[d][i];
             }
         }
+    }
+    // the warp barrier orders every lane's partials before lane 0's
+    // release fence; both arrivals then leave together, and lane 0's
+    // acquire fence orders the reads of the merges after them
+    __syncwarp();
+    int prev[2] = {0, 0};
+    if (lane == 0 && n_def > 0) {
+        fence_acq_rel_gpu();
+#pragma unroll
+        for (int d = 0; d < 2; ++d)
+            if (d < n_def) prev[d] = atom_add_relaxed_gpu(a.arrivals + (size_t)def_b[d] * kMaxHkv + g, 1);
+        fence_acq_rel_gpu();
+    }
+#pragma unroll
+    for (int d = 0; d < 2; ++d) {
+        if (d >= n_def) continue;
+        const int b = def_b[d];
+        const int p0 = prefix[b], p1 = prefix[b + 1];
+        const int c_lo = p0 / per, c_hi = (p1 - 1) / per;
+        if (__shfl_sync(0xffffffffu, prev[d], 0) != c_hi - c_lo) continue;
+        // online merge over batches of up to 8 partials per query head, the
+        // loads of both heads of the group all in flight together (one L2
+        // round trip per batch; requests of this workload span a few CTAs)
+        constexpr int kBatch = 8;
+        float mm[GROUP], ls[GROUP], o[GROUP][4];
+#pragma unroll
+        for (int i = 0; i < GROUP; ++i) {
+            mm[i] = -INFINITY;
+            ls[i] = 0.f;
+            o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+        }
+        for (int c0 = c_lo; c0 <= c_hi; c0 += kBatch) {
+            float mc[GROUP][kBatch], lc[GROUP][kBatch];
+            float4 pv[GROUP][kBatch];
+#pragma unroll
+            for (int i = 0; i < GROUP; ++i) {
+#pragma unroll
+                for (int u = 0; u < kBatch; ++u) {
+                    if (c0 + u <= c_hi) {
+                        const size_t r = (size_t)(c0 + u + b) * hq + g * GROUP + i;
+                        mc[i][u] = __ldcg(a.part_ml + r * 2);
+                        lc[i][u] = __ldcg(a.part_ml + r * 2 + 1);
+                        pv[i][u] = __ldcg(reinterpret_cast<const float4 *>(a.part_acc + r * kD + 4 * lane));
+                    } else {
+                        mc[i][u] = -INFINITY;
+                        lc[i][u] = 0.f;
+                        pv[i][u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < GROUP; ++i) {
+                float mb = mm[i];
+#pragma unroll
+                for (int u = 0; u < kBatch; ++u) mb = fmaxf(mb, mc[i][u]);
+                if (mb == -INFINITY) continue;  // nothing attended so far
+                const float alpha = exp2_approx(mm[i] - mb);  // 0 while mm = -inf
+                ls[i] *= alpha;
+                o[i][0] *= alpha;
+                o[i][1] *= alpha;
+                o[i][2] *= alpha;
+                o[i][3] *= alpha;
+#pragma unroll
+                for (int u = 0; u < kBatch; ++u) {
+                    const float w = exp2_approx(mc[i][u] - mb);  // 0 for an empty partial (mc = -inf)
+                    ls[i] += w * lc[i][u];
+                    o[i][0] += w * pv[i][u].x;
+                    o[i][1] += w * pv[i][u].y;
+                    o[i][2] += w * pv[i][u].z;
+                    o[i][3] += w * pv[i][u].w;
+                }
+                mm[i] = mb;
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < GROUP; ++i) {
+            const int h = g * GROUP + i;
+            const float inv = ls[i] > 0.f ? 1.f / ls[i] : 0.f;
+            uint2 w;
+            w.x = pack_bf16x2(o[i][0] * inv, o[i][1] * inv);
+            w.y = pack_bf16x2(o[i][2] * inv, o[i][3] * inv);
+            *reinterpret_cast<uint2 *>(a.out + ((size_t)b * hq + h) * kD + 4 * lane) = w;
+        }
+        if (lane == 0) a.arrivals[(size_t)b * kMaxHkv + g] = 0;  // ready for the next call
     }
 }
 
